@@ -1,0 +1,277 @@
+/*
+ * oscar.h -- C ABI of the GB300 (sm_103a) OSCAR INT2 rotated KV-cache library.
+ *
+ * OSCAR keeps a mixed-precision paged KV cache: the first 64 tokens (attention
+ * sinks) and the last 256 tokens before the current position stay BF16, and
+ * everything in between is stored as 2-bit codes after a fixed per-layer
+ * rotation R = U * H_Had * P_br and per-layer clipping.
+ *   - ainsights.it "OSCAR: Come Together AI Comprime la KV Cache a 2-bit per
+ *     LLM", sections "I tre fattori della rotazione" and "Architettura del
+ *     Sistema di Serving e Layout di Memoria";
+ *   - edge.aivizor.me "Together AI выпустила исходники OSCAR — INT2-квантование
+ *     KV-кэша для долгих контекстов LLM", composition and deployment paragraphs;
+ *   - gist.science "Resumen Técnico: OSCAR - Rotación Consciente de la
+ *     Covarianza Espectral Offline para Cuantización de Cache KV de 2 bits",
+ *     §2.2 A (rotations, clip thresholds) and §2.2 B (paged cache, fused kernel).
+ *
+ * Conventions for every call
+ *   - All pointers named "device" point to memory on the context's CUDA
+ *     device; the caller allocates and frees them.  "host" pointers are read
+ *     before the call returns.  The library allocates device memory only in
+ *     oscar_create (a 4-byte error word) and oscar_load_rotation (rotation
+ *     constants); append and decode never allocate.
+ *   - Work is queued asynchronously on the given stream (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream).
+ *   - Host-side argument checks return a status and launch nothing.
+ *   - Index checks that need device data (page ids, slots, lengths) are made
+ *     by the kernels: a bad index sets a bit in the context's device error
+ *     word and the offending work item is skipped (never a trap).  Read and
+ *     clear the word with oscar_check_device_error.
+ *   - Nothing throws across the ABI.  The library is not thread-safe per
+ *     context; distinct contexts are independent.
+ *
+ * Fixed shape: head_dim 128, page 64 tokens, sink 64, recent window 256,
+ * quantisation group 64 channels (one fp16 scale per token per group).
+ */
+#ifndef OSCAR_H
+#define OSCAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSCAR_HEAD_DIM 128
+#define OSCAR_PAGE_TOKENS 64
+#define OSCAR_SINK_TOKENS 64
+#define OSCAR_RECENT_TOKENS 256
+#define OSCAR_GROUP 64
+#define OSCAR_MAX_GQA 8
+
+/*
+ * Packed INT2 block: one page (64 positions) of one KV head, 4608 bytes.
+ *   [   0, 2048)  K codes      [2048, 2304)  K scales fp16 [64 tokens][2 groups]
+ *   [2304, 4352)  V codes      [4352, 4608)  V scales fp16 [64 tokens][2 groups]
+ * Codes come in 16-token tiles of 512 bytes (tile T = t / 16 at byte 512*T of
+ * the code area).  With u = t % 16, the 2-bit code of rotated channel j is at
+ *   K: lane = 4*(u%8) + (j%64)/16, word = 2*(u/8) + j/64,
+ *      bit  = 16*((j%16)/8) + 2*(j%8)
+ *   V: lane = 4*(j%8) + (u%8)/2,   word = 2*(u/8) + (j%16)/8,
+ *      bit  = 16*(u%2) + 2*(j/16)
+ *   byte = 512*T + 16*lane + 4*word + bit/8, bit-in-byte = bit%8
+ * (little-endian 32-bit words).  A code c stands for the level (c - 1.5) * s.
+ * The layout lets one warp load a 16-token tile with one 16-byte load per
+ * lane and hand the unpacked codes straight to the tensor cores.
+ */
+#define OSCAR_BLOCK_BYTES 4608
+#define OSCAR_BLOCK_K_CODES 0
+#define OSCAR_BLOCK_K_SCALES 2048
+#define OSCAR_BLOCK_V_CODES 2304
+#define OSCAR_BLOCK_V_SCALES 4352
+
+typedef enum {
+  OSCAR_OK = 0,
+  OSCAR_ERR_INVALID_ARG = 1,   /* null pointer, bad size or index, unsupported shape */
+  OSCAR_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+  OSCAR_ERR_NOT_LOADED = 3,    /* the layer's rotation was never loaded */
+  OSCAR_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  OSCAR_ERR_DEVICE_CHECK = 5,  /* a kernel found a bad index (see oscar_check_device_error) */
+  OSCAR_ERR_WORKSPACE = 6      /* workspace missing or too small */
+} oscar_status;
+
+/* Device error word bits (oscar_check_device_error). */
+#define OSCAR_DEVERR_PAGE 1u       /* page-table entry outside [0, num_pages) */
+#define OSCAR_DEVERR_SINK 2u       /* sink page index outside [0, num_sink_pages) */
+#define OSCAR_DEVERR_RING 4u       /* ring slot outside [0, num_ring_slots) */
+#define OSCAR_DEVERR_LENGTH 8u     /* a length or position beyond the table's capacity */
+#define OSCAR_DEVERR_TOKENS 16u    /* cu_seqlens inconsistent with n_tokens */
+
+typedef struct oscar_ctx oscar_ctx;
+
+typedef struct {
+  int32_t num_layers;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;   /* num_q_heads % num_kv_heads == 0, ratio <= 8 */
+  int32_t head_dim;       /* must be 128 */
+  int32_t page_size;      /* must be 64 */
+  int32_t sink;           /* must be 64 */
+  int32_t recent;         /* must be 256 */
+  int32_t group;          /* must be 64 */
+  int32_t device;         /* CUDA device ordinal */
+} oscar_config;
+
+/*
+ * One layer's cache, all device memory owned by the caller.
+ *   int2_pages  [num_pages][num_kv_heads][OSCAR_BLOCK_BYTES] bytes.
+ *   k_sink, v_sink  bf16 [num_sink_pages][num_kv_heads][64][128]: positions 0..63.
+ *   k_ring, v_ring  bf16 [num_ring_slots][num_kv_heads][256][128]: position p >= 64
+ *               of a request lives in row (p - 64) % 256 of its ring slot.
+ *   page_table  int32 [batch][max_pages_per_req]: entry i (i >= 1) is the
+ *               physical INT2 page of positions [64 i, 64 i + 64); entry 0 is
+ *               unused.  Entries may alias (shared prefixes); the caller
+ *               allocates pages, including the page an upcoming eviction
+ *               writes, and never lets an append write a shared page.
+ *   sink_page   int32 [batch]: physical sink page of each request (may alias).
+ *   ring_slot   int32 [batch]: ring slot of each request (must not alias).
+ * The same view describes every layer when the caller keeps per-layer pools;
+ * only the pool pointers differ between layers.
+ */
+typedef struct {
+  void* int2_pages;
+  int64_t num_pages;
+  void* k_sink;
+  void* v_sink;
+  int64_t num_sink_pages;
+  void* k_ring;
+  void* v_ring;
+  int64_t num_ring_slots;
+  const int32_t* page_table;
+  int32_t max_pages_per_req;
+  const int32_t* sink_page;
+  const int32_t* ring_slot;
+  int32_t batch;
+} oscar_cache_view;
+
+/* Append flags. */
+#define OSCAR_APPEND_FRESH_RING 1u  /* positions before pos[] are already sink/history
+                                       (e.g. an aliased prefix): evict nothing.  The
+                                       ring then holds only new tokens, so each request
+                                       must append >= 256 tokens unless pos <= 64
+                                       (else OSCAR_DEVERR_LENGTH, nothing written). */
+
+/*
+ * New tokens.  k, v: device bf16 [n_tokens][num_kv_heads][128].
+ *   pos         device int32 [batch]: position of each request's first new token
+ *               (its context length before this append).
+ *   cu_seqlens  device int32 [batch + 1]: request b owns tokens
+ *               [cu_seqlens[b], cu_seqlens[b+1]); NULL means exactly one token
+ *               per request (decode) and n_tokens == batch.
+ *   max_tokens_per_req  host upper bound of cu_seqlens[b+1] - cu_seqlens[b].
+ */
+typedef struct {
+  const void* k;
+  const void* v;
+  const int32_t* pos;
+  const int32_t* cu_seqlens;
+  int32_t n_tokens;
+  int32_t max_tokens_per_req;
+  uint32_t flags;
+} oscar_append_args;
+
+/*
+ * Decode queries: one new query per request, attending over its whole context
+ * (the just-appended token included; no mask is needed for the last query).
+ *   q        device bf16 [batch][num_q_heads][128], original (unrotated) basis.
+ *   out      device fp32 [batch][num_q_heads][128].  Query head h reads KV
+ *            head h / (num_q_heads / num_kv_heads).  A request with
+ *            ctx_len 0 gets zeros.
+ *   ctx_len  device int32 [batch]: context length after the append.
+ *   max_ctx_len  host upper bound of ctx_len (sizes the launch grid).
+ *   sm_scale softmax scale; <= 0 selects 1/sqrt(128).
+ */
+typedef struct {
+  const void* q;
+  float* out;
+  const int32_t* ctx_len;
+  int32_t max_ctx_len;
+  float sm_scale;
+} oscar_decode_args;
+
+/* BF16-cache comparator: every position BF16 in 64-token pages.
+ *   k_pages, v_pages  bf16 [num_pages][num_kv_heads][64][128]
+ *   page_table        int32 [batch][max_pages_per_req]: entry i holds positions
+ *                     [64 i, 64 i + 64) (entry 0 included). */
+typedef struct {
+  const void* k_pages;
+  const void* v_pages;
+  int64_t num_pages;
+  const int32_t* page_table;
+  int32_t max_pages_per_req;
+  int32_t batch;
+} oscar_bf16_cache_view;
+
+/* Rotation flags for oscar_load_rotation: which factors of R = U H P to use.
+ * OSCAR_ROT_ALL is the method; dropping factors gives the pages' baselines
+ * (naive INT2: none; Hadamard-only: H|P). */
+#define OSCAR_ROT_U 1u
+#define OSCAR_ROT_H 2u
+#define OSCAR_ROT_P 4u
+#define OSCAR_ROT_ALL 7u
+
+/* Create a context for one model shape on config->device.  Fails with
+ * OSCAR_ERR_INVALID_ARG for any shape other than the fixed one above. */
+oscar_status oscar_create(const oscar_config* config, oscar_ctx** out);
+
+/* Free the context and its device constants.  NULL is a no-op. */
+void oscar_destroy(oscar_ctx* ctx);
+
+/*
+ * Upload one layer's rotation: R_K = U_K H P and R_V = U_V H P ([ES] §2.2 A.3;
+ * [RU] composition paragraph) and the clip thresholds tau_k, tau_v
+ * ([ES] §2.2 A.4).  U_K, U_V: host fp32 [128][128] row-major, columns are
+ * the eigenvectors (a token row x is rotated as x' = x R).  They must be
+ * orthogonal; the library does not check.  tau > 0, finite or +inf, and
+ * tau / 1.5 must fit fp16 (tau <= 98256).  Synchronous (copies before return).
+ */
+oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K, const float* U_V,
+                                 float tau_k, float tau_v, uint32_t flags);
+
+/*
+ * Append new K/V tokens to one layer's cache ([IT] "Architettura ...": each
+ * token is rotated, clipped and quantised when it enters the INT2 history).
+ * Phase 1 (unless OSCAR_APPEND_FRESH_RING) moves ring tokens that fall out of
+ * the 256-token window into their INT2 rows; phase 2 writes each new token:
+ * positions < 64 to the sink page, positions >= L - 256 (L = final length) to
+ * the ring, the rest straight into INT2 rows.  Rotation: x' = x R in fp32
+ * (x U, then an in-register Walsh-Hadamard butterfly, then the bit-reversal
+ * permutation), clip a = min(max|x'|, tau) per group of 64, s = fp16(a / 1.5),
+ * code = [x' >= -s] + [x' >= 0] + [x' >= s].
+ */
+oscar_status oscar_kv_append(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                             const oscar_append_args* args, void* stream);
+
+/* Workspace bytes oscar_decode_attention needs for up to max_batch requests
+ * of up to max_ctx_len tokens. */
+size_t oscar_decode_workspace_bytes(const oscar_ctx* ctx, int32_t max_batch, int32_t max_ctx_len);
+
+/*
+ * Fused decode attention over one layer's mixed cache ([ES] §2.2 B: one
+ * kernel unpacks, de-quantises, undoes the rotation and computes attention;
+ * [IT] "Architettura ...": no extra memory traffic).  q is rotated into the
+ * K basis (q' = q R_K), the INT2 history is unpacked in registers and
+ * consumed by split-K flash-decoding on the tensor cores, the BF16 sink and
+ * recent tokens are attended in the original basis, and the rotated-basis
+ * part of the output is rotated back (acc R_V^T) when the splits are merged.
+ * No dequantised cache is materialised.  workspace: device, at least
+ * oscar_decode_workspace_bytes(ctx, batch, max_ctx_len) bytes, 256-byte
+ * aligned, owned by the caller; its contents need no initialisation and are
+ * scratch between calls.  Calls that share a workspace must not overlap on
+ * the GPU.
+ */
+oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                                    const oscar_decode_args* args, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/* Comparator: the same decode over a plain BF16 paged cache (the baseline
+ * the pages' decode speed-ups are quoted against).  Same workspace rules. */
+oscar_status oscar_decode_attention_bf16(oscar_ctx* ctx, const oscar_bf16_cache_view* view,
+                                         const oscar_decode_args* args, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/* Synchronise the stream, return and clear the device error word in *bits
+ * (may be NULL).  Returns OSCAR_ERR_DEVICE_CHECK when any bit was set. */
+oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bits);
+
+/* Number of SMs of the context's device (used to size launch grids). */
+int32_t oscar_device_sm_count(const oscar_ctx* ctx);
+
+/* Static description of a status code. */
+const char* oscar_status_string(oscar_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H */

@@ -1,0 +1,308 @@
+// C ABI of the OSCAR library: argument checks, rotation constants, launches.
+// See include/oscar.h for the contract of every entry point.
+
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/oscar.h"
+#include "oscar_device.cuh"
+#include "oscar_internal.h"
+
+using namespace oscar;
+
+struct oscar_ctx {
+  oscar_config cfg;
+  int num_sms = 0;
+  unsigned* d_err = nullptr;
+  std::vector<float*> d_rot;       // per layer: U_K | U_V | U_V^T, 3 * 128 * 128 floats
+  std::vector<float> tau_k, tau_v;
+  std::vector<unsigned> flags;
+  std::vector<bool> loaded;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+bool valid_view(const oscar_ctx* ctx, const oscar_cache_view* v) {
+  if (v == nullptr || v->batch < 0) return false;
+  if (v->batch == 0) return true;
+  return v->int2_pages && v->k_sink && v->v_sink && v->k_ring && v->v_ring && v->page_table && v->sink_page &&
+         v->ring_slot && v->num_pages > 0 && v->num_sink_pages > 0 && v->num_ring_slots > 0 &&
+         v->max_pages_per_req > 0 && v->num_pages <= INT32_MAX && v->num_sink_pages <= INT32_MAX &&
+         v->num_ring_slots <= INT32_MAX && ctx != nullptr;
+}
+
+CacheRefs refs_of(const oscar_ctx* ctx, const oscar_cache_view* v) {
+  CacheRefs c;
+  c.pages = static_cast<uint8_t*>(v->int2_pages);
+  c.num_pages = v->num_pages;
+  c.k_sink = static_cast<uint16_t*>(v->k_sink);
+  c.v_sink = static_cast<uint16_t*>(v->v_sink);
+  c.num_sink = v->num_sink_pages;
+  c.k_ring = static_cast<uint16_t*>(v->k_ring);
+  c.v_ring = static_cast<uint16_t*>(v->v_ring);
+  c.num_ring = v->num_ring_slots;
+  c.page_table = v->page_table;
+  c.max_pages = v->max_pages_per_req;
+  c.sink_page = v->sink_page;
+  c.ring_slot = v->ring_slot;
+  c.batch = v->batch;
+  c.num_kv_heads = ctx->cfg.num_kv_heads;
+  return c;
+}
+
+LayerRotation rotation_of(const oscar_ctx* ctx, int layer) {
+  LayerRotation r;
+  const float* base = ctx->d_rot[layer];
+  r.U_K = base;
+  r.U_V = base + 128 * 128;
+  r.U_VT = base + 2 * 128 * 128;
+  r.tau_k = ctx->tau_k[layer];
+  r.tau_v = ctx->tau_v[layer];
+  r.flags = ctx->flags[layer];
+  return r;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* oscar_status_string(oscar_status s) {
+  switch (s) {
+    case OSCAR_OK: return "ok";
+    case OSCAR_ERR_INVALID_ARG: return "invalid argument";
+    case OSCAR_ERR_UNSUPPORTED: return "unsupported";
+    case OSCAR_ERR_NOT_LOADED: return "rotation not loaded for this layer";
+    case OSCAR_ERR_CUDA: return "CUDA error";
+    case OSCAR_ERR_DEVICE_CHECK: return "device-side index check failed";
+    case OSCAR_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
+  if (cfg == nullptr || out == nullptr) return OSCAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg->head_dim != OSCAR_HEAD_DIM || cfg->page_size != OSCAR_PAGE_TOKENS || cfg->sink != OSCAR_SINK_TOKENS ||
+      cfg->recent != OSCAR_RECENT_TOKENS || cfg->group != OSCAR_GROUP)
+    return OSCAR_ERR_INVALID_ARG;
+  if (cfg->num_layers <= 0 || cfg->num_kv_heads <= 0 || cfg->num_q_heads <= 0 ||
+      cfg->num_q_heads % cfg->num_kv_heads != 0 || cfg->num_q_heads / cfg->num_kv_heads > OSCAR_MAX_GQA ||
+      cfg->num_layers > 4096 || cfg->num_kv_heads > 1024)
+    return OSCAR_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cfg->device < 0 || cfg->device >= ndev) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(cfg->device);
+  oscar_ctx* ctx = new (std::nothrow) oscar_ctx();
+  if (ctx == nullptr) return OSCAR_ERR_CUDA;
+  ctx->cfg = *cfg;
+  if (cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, cfg->device) != cudaSuccess ||
+      cudaMalloc(&ctx->d_err, sizeof(unsigned)) != cudaSuccess || cudaMemset(ctx->d_err, 0, sizeof(unsigned)) != cudaSuccess) {
+    if (ctx->d_err) cudaFree(ctx->d_err);
+    delete ctx;
+    return OSCAR_ERR_CUDA;
+  }
+  ctx->d_rot.assign(cfg->num_layers, nullptr);
+  ctx->tau_k.assign(cfg->num_layers, 0.f);
+  ctx->tau_v.assign(cfg->num_layers, 0.f);
+  ctx->flags.assign(cfg->num_layers, 0u);
+  ctx->loaded.assign(cfg->num_layers, false);
+  *out = ctx;
+  return OSCAR_OK;
+}
+
+void oscar_destroy(oscar_ctx* ctx) {
+  if (ctx == nullptr) return;
+  DeviceGuard guard(ctx->cfg.device);
+  for (float* p : ctx->d_rot)
+    if (p) cudaFree(p);
+  if (ctx->d_err) cudaFree(ctx->d_err);
+  delete ctx;
+}
+
+int32_t oscar_device_sm_count(const oscar_ctx* ctx) { return ctx ? ctx->num_sms : 0; }
+
+oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K, const float* U_V, float tau_k,
+                                 float tau_v, uint32_t flags) {
+  if (ctx == nullptr || U_K == nullptr || U_V == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if ((flags & ~OSCAR_ROT_ALL) != 0) return OSCAR_ERR_INVALID_ARG;
+  const float tmax = 65504.0f * 1.5f;
+  if (!(tau_k > 0.f) || !(tau_v > 0.f) || std::isnan(tau_k) || std::isnan(tau_v)) return OSCAR_ERR_INVALID_ARG;
+  if ((std::isfinite(tau_k) && tau_k > tmax) || (std::isfinite(tau_v) && tau_v > tmax)) return OSCAR_ERR_INVALID_ARG;
+  const int n = 128 * 128;
+  std::vector<float> host(3 * n);
+  for (int i = 0; i < 128; ++i)
+    for (int j = 0; j < 128; ++j) {
+      const float ident = (i == j) ? 1.f : 0.f;
+      const float uk = (flags & OSCAR_ROT_U) ? U_K[i * 128 + j] : ident;
+      const float uv = (flags & OSCAR_ROT_U) ? U_V[i * 128 + j] : ident;
+      if (!std::isfinite(uk) || !std::isfinite(uv)) return OSCAR_ERR_INVALID_ARG;
+      host[i * 128 + j] = uk;
+      host[n + i * 128 + j] = uv;
+      host[2 * n + j * 128 + i] = uv;
+    }
+  DeviceGuard guard(ctx->cfg.device);
+  if (ctx->d_rot[layer] == nullptr) {
+    if (cudaMalloc(&ctx->d_rot[layer], sizeof(float) * 3 * n) != cudaSuccess) {
+      ctx->d_rot[layer] = nullptr;
+      return OSCAR_ERR_CUDA;
+    }
+  }
+  if (cudaMemcpy(ctx->d_rot[layer], host.data(), sizeof(float) * 3 * n, cudaMemcpyHostToDevice) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  ctx->tau_k[layer] = tau_k;
+  ctx->tau_v[layer] = tau_v;
+  ctx->flags[layer] = flags & (OSCAR_ROT_H | OSCAR_ROT_P);
+  ctx->loaded[layer] = true;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_kv_append(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                             const oscar_append_args* args, void* stream) {
+  if (ctx == nullptr || view == nullptr || args == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded[layer]) return OSCAR_ERR_NOT_LOADED;
+  if (!valid_view(ctx, view)) return OSCAR_ERR_INVALID_ARG;
+  if (view->batch == 0) return OSCAR_OK;
+  if (args->k == nullptr || args->v == nullptr || args->pos == nullptr || args->n_tokens < 0) return OSCAR_ERR_INVALID_ARG;
+  if ((args->flags & ~OSCAR_APPEND_FRESH_RING) != 0) return OSCAR_ERR_INVALID_ARG;
+  if (args->cu_seqlens == nullptr) {
+    if (args->n_tokens != view->batch) return OSCAR_ERR_INVALID_ARG;
+  } else if (args->max_tokens_per_req <= 0 || args->max_tokens_per_req > (1 << 28)) {
+    return OSCAR_ERR_INVALID_ARG;
+  }
+  if (!aligned16(view->int2_pages)) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->cfg.device);
+  AppendLaunch a;
+  a.c = refs_of(ctx, view);
+  a.rot = rotation_of(ctx, layer);
+  a.k = static_cast<const uint16_t*>(args->k);
+  a.v = static_cast<const uint16_t*>(args->v);
+  a.pos = args->pos;
+  a.cu_seqlens = args->cu_seqlens;
+  a.n_tokens = args->n_tokens;
+  a.max_tokens_per_req = args->max_tokens_per_req;
+  a.flags = args->flags;
+  a.err = ctx->d_err;
+  return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+size_t oscar_decode_workspace_bytes(const oscar_ctx* ctx, int32_t max_batch, int32_t max_ctx_len) {
+  if (ctx == nullptr || max_batch < 0 || max_ctx_len < 0) return 0;
+  size_t best = 0;
+  // the plan depends on the batch actually passed; take the largest over 1..max_batch
+  for (int b = 1; b <= max_batch; ++b) {
+    for (int mode = 0; mode < 2; ++mode) {
+      const DecodePlan p = plan_decode(mode, b, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, max_ctx_len, ctx->num_sms);
+      if (p.total > best) best = p.total;
+    }
+  }
+  return best;
+}
+
+static oscar_status check_decode_args(const oscar_ctx* ctx, const oscar_decode_args* args, int batch, void* ws,
+                                      size_t ws_bytes, int mode, DecodePlan* plan) {
+  if (args == nullptr || args->q == nullptr || args->out == nullptr || args->ctx_len == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (args->max_ctx_len < 0 || std::isnan(args->sm_scale)) return OSCAR_ERR_INVALID_ARG;
+  *plan = plan_decode(mode, batch, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, args->max_ctx_len, ctx->num_sms);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < plan->total) return OSCAR_ERR_WORKSPACE;
+  if (plan->n_items > 65535 * 16) return OSCAR_ERR_UNSUPPORTED;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                                    const oscar_decode_args* args, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (ctx == nullptr || view == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded[layer]) return OSCAR_ERR_NOT_LOADED;
+  if (!valid_view(ctx, view)) return OSCAR_ERR_INVALID_ARG;
+  if (view->batch == 0) return OSCAR_OK;
+  if (view->batch > 65535) return OSCAR_ERR_UNSUPPORTED;
+  DecodePlan plan;
+  const oscar_status st = check_decode_args(ctx, args, view->batch, workspace, workspace_bytes, 0, &plan);
+  if (st != OSCAR_OK) return st;
+  if (!aligned16(view->int2_pages)) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->cfg.device);
+  DecodeLaunch d;
+  d.mode = 0;
+  d.c = refs_of(ctx, view);
+  d.rot = rotation_of(ctx, layer);
+  d.q = static_cast<const uint16_t*>(args->q);
+  d.out = args->out;
+  d.ctx_len = args->ctx_len;
+  d.sm_scale = args->sm_scale > 0.f ? args->sm_scale : 1.0f / std::sqrt(128.0f);
+  d.plan = plan;
+  d.workspace = static_cast<uint8_t*>(workspace);
+  d.err = ctx->d_err;
+  return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+oscar_status oscar_decode_attention_bf16(oscar_ctx* ctx, const oscar_bf16_cache_view* view,
+                                         const oscar_decode_args* args, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  if (ctx == nullptr || view == nullptr || view->batch < 0) return OSCAR_ERR_INVALID_ARG;
+  if (view->batch == 0) return OSCAR_OK;
+  if (view->batch > 65535) return OSCAR_ERR_UNSUPPORTED;
+  if (view->k_pages == nullptr || view->v_pages == nullptr || view->page_table == nullptr || view->num_pages <= 0 ||
+      view->num_pages > INT32_MAX || view->max_pages_per_req <= 0)
+    return OSCAR_ERR_INVALID_ARG;
+  DecodePlan plan;
+  const oscar_status st = check_decode_args(ctx, args, view->batch, workspace, workspace_bytes, 1, &plan);
+  if (st != OSCAR_OK) return st;
+  DeviceGuard guard(ctx->cfg.device);
+  DecodeLaunch d;
+  d.mode = 1;
+  d.c.page_table = view->page_table;
+  d.c.max_pages = view->max_pages_per_req;
+  d.c.num_pages = view->num_pages;
+  d.c.batch = view->batch;
+  d.c.num_kv_heads = ctx->cfg.num_kv_heads;
+  d.kb_pages = static_cast<const uint16_t*>(view->k_pages);
+  d.vb_pages = static_cast<const uint16_t*>(view->v_pages);
+  d.q = static_cast<const uint16_t*>(args->q);
+  d.out = args->out;
+  d.ctx_len = args->ctx_len;
+  d.sm_scale = args->sm_scale > 0.f ? args->sm_scale : 1.0f / std::sqrt(128.0f);
+  d.plan = plan;
+  d.workspace = static_cast<uint8_t*>(workspace);
+  d.err = ctx->d_err;
+  // the prep kernel needs a rotation matrix; the plain path only uses the unrotated q
+  d.rot.flags = 0;
+  for (size_t l = 0; l < ctx->d_rot.size(); ++l)
+    if (ctx->loaded[l]) {
+      d.rot = rotation_of(ctx, (int)l);
+      break;
+    }
+  if (d.rot.U_K == nullptr) return OSCAR_ERR_NOT_LOADED;
+  return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bits) {
+  if (ctx == nullptr) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->cfg.device);
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return OSCAR_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, ctx->d_err, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (v != 0 && cudaMemset(ctx->d_err, 0, sizeof(unsigned)) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (bits) *bits = v;
+  return v ? OSCAR_ERR_DEVICE_CHECK : OSCAR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,418 @@
+// OSCAR KV-cache write path: rotate, clip, quantise, pack; BF16 sink/ring
+// writes; recent-window eviction.
+//
+// ainsights.it "OSCAR: Come Together AI Comprime la KV Cache a 2-bit per LLM",
+// section "Architettura del Sistema di Serving e Layout di Memoria": during
+// the write every token is rotated, clipped and quantised; the first 64 tokens
+// and the last 256 stay BF16.  gist.science "Resumen Técnico: OSCAR ...",
+// §2.2 A.3-4 (R = U H_Had P_br, per-layer clip thresholds) and §2.2 B (paged
+// cache, sink/recent in BF16, INT2 history after rotation and clipping).
+//
+// Rotation x' = x R is computed as (x U) in fp32, then the Walsh-Hadamard
+// factor as a butterfly (shuffles within a warp, shared memory across warps),
+// then the bit-reversal permutation as an index map.  Quantiser per group of
+// 64 rotated channels: a = min(max|x'|, tau), s = fp16(a / 1.5),
+// code = [x' >= -s] + [x' >= 0] + [x' >= s].
+
+#include "oscar_device.cuh"
+#include "oscar_internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)
+
+// Byte offset inside a block's K code area of the 32-bit word holding the
+// codes of (row t, quarter tig, group grp).
+__device__ __forceinline__ int k_word_offset(int t, int tig, int grp) {
+  const int T = t >> 4, u = t & 15;
+  return 512 * T + 16 * (4 * (u & 7) + tig) + 4 * (2 * (u >> 3) + grp);
+}
+
+// Byte offset inside a block's V code area of the 16-bit half holding the
+// codes of row t for the channels {jj + 16 r : r = 0..7}.
+__device__ __forceinline__ int v_half_offset(int t, int jj) {
+  const int T = t >> 4, u = t & 15;
+  return 512 * T + 16 * (4 * (jj & 7) + ((u & 7) >> 1)) + 4 * (2 * (u >> 3) + (jj >> 3)) + 2 * (u & 1);
+}
+
+struct QuantSmem {
+  float x[kD];
+  float scratch[kD];
+  float red[4];
+  uint8_t code[kD];
+};
+
+// Rotate + clip + quantise one token held one channel per thread (128
+// threads) and store its codes and scales in row `row` of the K or V half of
+// `block`.  All 128 threads must call it.
+__device__ void quantize_token(float x, const float* __restrict__ U, unsigned flags, float tau, uint8_t* block,
+                               int row, bool is_v, QuantSmem& sm) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  sm.x[t] = x;
+  __syncthreads();
+  float z = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < kD; ++i) z = fmaf(sm.x[i], __ldg(U + i * kD + t), z);
+  if (flags & kRotH) z = fwht128_block(z, sm.scratch) * kInvSqrtD;
+  if (flags & kRotP) {
+    __syncthreads();
+    sm.scratch[t] = z;
+    __syncthreads();
+    z = sm.scratch[brev7(t)];
+  }
+  const float amax = warp_max(fabsf(z));
+  if (lane == 0) sm.red[warp] = amax;
+  __syncthreads();
+  const int grp = t >> 6;
+  const float a = fminf(fmaxf(sm.red[2 * grp], sm.red[2 * grp + 1]), tau);
+  const __half sh = __float2half_rn(a / 1.5f);
+  const float s = __half2float(sh);
+  sm.code[t] = (uint8_t)((z >= -s) + (z >= 0.f) + (z >= s));
+  __syncthreads();
+  if (!is_v) {
+    if (t < 8) {
+      const int tig = t & 3, g = t >> 2, base = 64 * g + 16 * tig;
+      uint32_t w = 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        w |= (uint32_t)sm.code[base + r] << (2 * r);
+        w |= (uint32_t)sm.code[base + 8 + r] << (16 + 2 * r);
+      }
+      *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, tig, g)) = w;
+    }
+  } else {
+    if (t < 16) {
+      uint32_t hv = 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[t + 16 * r] << (2 * r);
+      *reinterpret_cast<uint16_t*>(block + kVCodes + v_half_offset(row, t)) = (uint16_t)hv;
+    }
+  }
+  if ((t & 63) == 0)
+    *reinterpret_cast<__half*>(block + (is_v ? kVScales : kKScales) + 4 * row + 2 * grp) = sh;
+  __syncthreads();
+}
+
+// Locate (and check) the INT2 block of position e of request b, head h.
+__device__ __forceinline__ uint8_t* history_block(const CacheRefs& c, int b, int h, int e, unsigned* err) {
+  const int lp = e >> 6;
+  if (lp >= c.max_pages) {
+    if (threadIdx.x == 0) set_error(err, kErrLength);
+    return nullptr;
+  }
+  const int phys = c.page_table[(size_t)b * c.max_pages + lp];
+  if (phys < 0 || phys >= c.num_pages) {
+    if (threadIdx.x == 0) set_error(err, kErrPage);
+    return nullptr;
+  }
+  return c.pages + ((size_t)phys * c.num_kv_heads + h) * kBlockBytes;
+}
+
+// ------------------------------------------------------------------ decode append
+// One new token per request.  grid (Hkv, B), 128 threads.
+__global__ void __launch_bounds__(128) append_one_kernel(AppendLaunch a) {
+  __shared__ QuantSmem sm;
+  const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  const CacheRefs& c = a.c;
+  const int Hkv = c.num_kv_heads;
+  const int p = a.pos[b];
+  const size_t src = ((size_t)b * Hkv + h) * kD + t;
+  const uint16_t kn = a.k[src], vn = a.v[src];
+  if (p < 0 || ((a.flags & 1u) && p > kSink)) {
+    if (t == 0) set_error(a.err, kErrLength);
+    return;
+  }
+  if (p < kSink) {
+    const int sp = c.sink_page[b];
+    if (sp < 0 || sp >= c.num_sink) {
+      if (t == 0) set_error(a.err, kErrSink);
+      return;
+    }
+    const size_t dst = (((size_t)sp * Hkv + h) * kSink + p) * kD + t;
+    c.k_sink[dst] = kn;
+    c.v_sink[dst] = vn;
+    return;
+  }
+  const int slot = c.ring_slot[b];
+  if (slot < 0 || slot >= c.num_ring) {
+    if (t == 0) set_error(a.err, kErrRing);
+    return;
+  }
+  const size_t rdst = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
+  if (p >= kSink + kRecent) {
+    // the token at e = p - 256 leaves the window: same ring row, read before overwrite
+    const int e = p - kRecent;
+    uint8_t* blk = history_block(c, b, h, e, a.err);
+    if (blk != nullptr) {
+      const float xk = bf16_bits_to_float(c.k_ring[rdst]);
+      const float xv = bf16_bits_to_float(c.v_ring[rdst]);
+      quantize_token(xk, a.rot.U_K, a.rot.flags, a.rot.tau_k, blk, e & 63, false, sm);
+      quantize_token(xv, a.rot.U_V, a.rot.flags, a.rot.tau_v, blk, e & 63, true, sm);
+    }
+  }
+  c.k_ring[rdst] = kn;
+  c.v_ring[rdst] = vn;
+}
+
+// ------------------------------------------------------------------ multi-token append
+__device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& p0, int& n, int& tok0) {
+  if (a.cu_seqlens == nullptr) {
+    tok0 = b;
+    n = 1;
+  } else {
+    tok0 = a.cu_seqlens[b];
+    n = a.cu_seqlens[b + 1] - tok0;
+    if (n < 0 || tok0 < 0 || tok0 + n > a.n_tokens || n > a.max_tokens_per_req) {
+      if (threadIdx.x == 0) set_error(a.err, kErrTokens);
+      return false;
+    }
+  }
+  p0 = a.pos[b];
+  if (p0 < 0) {
+    if (threadIdx.x == 0) set_error(a.err, kErrLength);
+    return false;
+  }
+  // a fresh ring holds only the new tokens: the recent window must lie inside them
+  if ((a.flags & 1u) && p0 > kSink && n < kRecent) {
+    if (threadIdx.x == 0) set_error(a.err, kErrLength);
+    return false;
+  }
+  return n > 0;
+}
+
+// Phase 1: ring tokens that fall out of the recent window go to the history.
+// grid (256, Hkv, B), 128 threads: one token-head per block.
+__global__ void __launch_bounds__(128) append_evict_kernel(AppendLaunch a) {
+  __shared__ QuantSmem sm;
+  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
+  int p0, n, tok0;
+  if (!request_span(a, b, p0, n, tok0)) return;
+  const int L = p0 + n;
+  const int e0 = max(kSink, p0 - kRecent), e1 = min(p0, L - kRecent);
+  const int e = e0 + x;
+  if (e >= e1) return;
+  const CacheRefs& c = a.c;
+  const int slot = c.ring_slot[b];
+  if (slot < 0 || slot >= c.num_ring) {
+    if (t == 0) set_error(a.err, kErrRing);
+    return;
+  }
+  uint8_t* blk = history_block(c, b, h, e, a.err);
+  if (blk == nullptr) return;
+  const size_t r = (((size_t)slot * c.num_kv_heads + h) * kRecent + ((e - kSink) % kRecent)) * kD + t;
+  const float xk = bf16_bits_to_float(c.k_ring[r]);
+  const float xv = bf16_bits_to_float(c.v_ring[r]);
+  quantize_token(xk, a.rot.U_K, a.rot.flags, a.rot.tau_k, blk, e & 63, false, sm);
+  quantize_token(xv, a.rot.U_V, a.rot.flags, a.rot.tau_v, blk, e & 63, true, sm);
+}
+
+// Phase 2a: new tokens that stay BF16 (sink rows, ring rows).
+// grid (320, B), 128 threads; all KV heads of one position per block.
+__global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
+  const int x = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  int p0, n, tok0;
+  if (!request_span(a, b, p0, n, tok0)) return;
+  const int L = p0 + n;
+  const CacheRefs& c = a.c;
+  const int Hkv = c.num_kv_heads;
+  int p;
+  uint16_t *kd, *vd;
+  size_t row0;
+  if (x < kSink) {
+    p = p0 + x;
+    if (p >= min(L, kSink)) return;
+    const int sp = c.sink_page[b];
+    if (sp < 0 || sp >= c.num_sink) {
+      if (t == 0) set_error(a.err, kErrSink);
+      return;
+    }
+    kd = c.k_sink;
+    vd = c.v_sink;
+    row0 = (size_t)sp * Hkv * kSink;  // + h * 64 + p
+    for (int h = 0; h < Hkv; ++h) {
+      const size_t s = ((size_t)(tok0 + p - p0) * Hkv + h) * kD + t;
+      const size_t d = (row0 + (size_t)h * kSink + p) * kD + t;
+      kd[d] = a.k[s];
+      vd[d] = a.v[s];
+    }
+    return;
+  }
+  p = max(max(p0, L - kRecent), kSink) + (x - kSink);
+  if (p >= L) return;
+  const int slot = c.ring_slot[b];
+  if (slot < 0 || slot >= c.num_ring) {
+    if (t == 0) set_error(a.err, kErrRing);
+    return;
+  }
+  kd = c.k_ring;
+  vd = c.v_ring;
+  for (int h = 0; h < Hkv; ++h) {
+    const size_t s = ((size_t)(tok0 + p - p0) * Hkv + h) * kD + t;
+    const size_t d = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
+    kd[d] = a.k[s];
+    vd[d] = a.v[s];
+  }
+}
+
+// Phase 2b: new tokens that go straight into the INT2 history, one page of
+// one KV head per block.  grid (pages, Hkv, B), 256 threads.
+struct TileSmem {
+  float z[64][kD + 4];
+  uint8_t code[64][kD];
+  __half scale[64][2];
+};
+
+__device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int p0, int r_lo, int r_hi, int lp,
+                              uint8_t* blk, bool is_v, TileSmem& sm) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int Hkv = a.c.num_kv_heads;
+  const uint16_t* src = is_v ? a.v : a.k;
+  const float* U = is_v ? a.rot.U_V : a.rot.U_K;
+  const float tau = is_v ? a.rot.tau_v : a.rot.tau_k;
+  // load the tile (rows outside [r_lo, r_hi) are zero)
+  for (int i = t; i < 64 * kD; i += blockDim.x) {
+    const int r = i >> 7, ch = i & 127;
+    float v = 0.f;
+    if (r >= r_lo && r < r_hi) {
+      const int p = lp * kPage + r;
+      v = bf16_bits_to_float(src[((size_t)(tok0 + p - p0) * Hkv + h) * kD + ch]);
+    }
+    sm.z[r][ch] = v;
+  }
+  __syncthreads();
+  // x U: warp w owns rows 8w..8w+7, lane owns channels 4 lane..4 lane+3
+  float acc[8][4];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[r][k] = 0.f;
+  for (int i = 0; i < kD; ++i) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(U + i * kD) + lane);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float xv = sm.z[8 * warp + r][i];
+      acc[r][0] = fmaf(xv, u.x, acc[r][0]);
+      acc[r][1] = fmaf(xv, u.y, acc[r][1]);
+      acc[r][2] = fmaf(xv, u.z, acc[r][2]);
+      acc[r][3] = fmaf(xv, u.w, acc[r][3]);
+    }
+  }
+  __syncthreads();
+  const unsigned flags = a.rot.flags;
+#pragma unroll 1
+  for (int r = 0; r < 8; ++r) {
+    const int row = 8 * warp + r;
+    float v[4] = {acc[r][0], acc[r][1], acc[r][2], acc[r][3]};
+    if (flags & kRotH) {
+      // index bits 0,1 live inside the lane, bits 2..6 across lanes
+      float t0 = v[0] + v[1], t1 = v[0] - v[1], t2 = v[2] + v[3], t3 = v[2] - v[3];
+      v[0] = t0 + t2;
+      v[1] = t1 + t3;
+      v[2] = t0 - t2;
+      v[3] = t1 - t3;
+#pragma unroll
+      for (int bb = 0; bb < 5; ++bb) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, v[k], 1 << bb);
+          v[k] = ((lane >> bb) & 1) ? (o - v[k]) : (v[k] + o);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD;
+    }
+    if (flags & kRotP) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sm.z[row][4 * lane + k] = v[k];
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = sm.z[row][brev7(4 * lane + k)];
+      __syncwarp();
+    }
+    // group absmax: channels 0..63 on lanes 0..15, 64..127 on lanes 16..31
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float aa = fminf(m, tau);
+    const __half sh = __float2half_rn(aa / 1.5f);
+    const float s = __half2float(sh);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sm.code[row][4 * lane + k] = (uint8_t)((v[k] >= -s) + (v[k] >= 0.f) + (v[k] >= s));
+    if ((lane & 15) == 0) sm.scale[row][lane >> 4] = sh;
+  }
+  __syncthreads();
+  // pack the rows in [r_lo, r_hi) only: other rows of this page may hold
+  // history tokens written by earlier appends
+  for (int i = t; i < 64 * 8; i += blockDim.x) {
+    const int row = i >> 3, w = i & 7;
+    if (row < r_lo || row >= r_hi) continue;
+    if (!is_v) {
+      const int tig = w & 3, g = w >> 2, base = 64 * g + 16 * tig;
+      uint32_t word = 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        word |= (uint32_t)sm.code[row][base + r] << (2 * r);
+        word |= (uint32_t)sm.code[row][base + 8 + r] << (16 + 2 * r);
+      }
+      *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, tig, g)) = word;
+    } else {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int jj = 2 * w + hh;
+        uint32_t hv = 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[row][jj + 16 * r] << (2 * r);
+        *reinterpret_cast<uint16_t*>(blk + kVCodes + v_half_offset(row, jj)) = (uint16_t)hv;
+      }
+    }
+  }
+  for (int i = t; i < 64 * 2; i += blockDim.x) {
+    const int row = i >> 1, g = i & 1;
+    if (row < r_lo || row >= r_hi) continue;
+    *reinterpret_cast<__half*>(blk + (is_v ? kVScales : kKScales) + 4 * row + 2 * g) = sm.scale[row][g];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(256) append_tile_kernel(AppendLaunch a) {
+  extern __shared__ __align__(16) uint8_t tile_smem_raw[];
+  TileSmem& sm = *reinterpret_cast<TileSmem*>(tile_smem_raw);
+  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  int p0, n, tok0;
+  if (!request_span(a, b, p0, n, tok0)) return;
+  const int L = p0 + n;
+  const int lo = max(p0, kSink), hi = L - kRecent;
+  if (hi <= lo) return;
+  const int lp = lo / kPage + x;
+  if (lp * kPage >= hi) return;
+  const int r_lo = max(lo - lp * kPage, 0), r_hi = min(hi - lp * kPage, kPage);
+  uint8_t* blk = history_block(a.c, b, h, lp * kPage, a.err);
+  if (blk == nullptr) return;
+  quantize_tile(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, false, sm);
+  quantize_tile(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, true, sm);
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
+  const int B = a.c.batch, Hkv = a.c.num_kv_heads;
+  if (a.cu_seqlens == nullptr) {
+    append_one_kernel<<<dim3(Hkv, B), 128, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+  if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 128, 0, stream>>>(a);
+  append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
+  const int tiles = (a.max_tokens_per_req + kPage - 1) / kPage + 1;
+  const size_t smem = sizeof(TileSmem);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(append_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  append_tile_kernel<<<dim3(tiles, Hkv, B), 256, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace oscar

@@ -1,0 +1,159 @@
+// Device helpers shared by the OSCAR kernels (sm_103a).
+//
+// Everything here is plain inline PTX or CUDA intrinsics: warp-level
+// tensor-core MMA (fp16 in, fp32 accumulate), 8x8 b16 transposes, mbarriers
+// and bulk asynchronous copies (the TMA engine's untiled mode) for staging
+// cache pages into shared memory, and the Walsh-Hadamard butterfly.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+namespace oscar {
+
+constexpr int kD = 128;           // head dim
+constexpr int kPage = 64;         // tokens per page
+constexpr int kSink = 64;         // BF16 attention-sink tokens
+constexpr int kRecent = 256;      // BF16 recent window
+constexpr int kGroup = 64;        // channels per quantisation group
+constexpr int kMaxG = 8;          // query heads per KV head (GQA) handled per warp
+
+// Packed block (one page, one KV head): see include/oscar.h for the layout.
+constexpr int kBlockBytes = 4608;
+constexpr int kKCodes = 0;
+constexpr int kKScales = 2048;
+constexpr int kVCodes = 2304;
+constexpr int kVScales = 4352;
+
+// device error word bits (mirror of the public OSCAR_DEVERR_* values)
+constexpr unsigned kErrPage = 1u, kErrSink = 2u, kErrRing = 4u, kErrLength = 8u, kErrTokens = 16u,
+                   kErrTimeout = 32u;
+
+constexpr unsigned kRotU = 1u, kRotH = 2u, kRotP = 4u;
+
+__device__ __forceinline__ void set_error(unsigned* err, unsigned bits) { atomicOr(err, bits); }
+
+// reverse the 7 index bits of a channel (P_br for d = 128)
+__device__ __forceinline__ int brev7(int j) { return (int)(__brev((unsigned)j) >> 25); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  return h2_as_u32(__floats2half2_rn(lo, hi));
+}
+
+// bf16 pair (low element in the low half) -> fp16 pair, round to nearest
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+  const float lo = __uint_as_float(u << 16);
+  const float hi = __uint_as_float(u & 0xffff0000u);
+  return pack_f16x2(lo, hi);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// D += A * B, m16n8k16, A row-major fp16, B col-major fp16, fp32 accumulate
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// transpose an 8x8 b16 matrix held one row-pair per lane
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- mbarrier / bulk copy
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after `limit` polls (each poll may suspend briefly).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned limit) {
+  for (unsigned i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Untiled bulk copy global -> shared (TMA), completion counted on `bar` in bytes.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- warp reductions
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Walsh-Hadamard butterfly (Sylvester order, unnormalised) over 128 values
+// held one per thread of a 128-thread block: index bits 0..4 are exchanged
+// in registers through warp shuffles, bits 5..6 through shared memory.
+// `scratch` holds 128 floats.  All 128 threads must call it.
+__device__ __forceinline__ float fwht128_block(float v, float* scratch) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int b = 0; b < 5; ++b) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, 1 << b);
+    v = ((t >> b) & 1) ? (o - v) : (v + o);
+  }
+#pragma unroll
+  for (int b = 5; b < 7; ++b) {
+    scratch[t] = v;
+    __syncthreads();
+    const float o = scratch[t ^ (1 << b)];
+    __syncthreads();
+    v = ((t >> b) & 1) ? (o - v) : (v + o);
+  }
+  return v;
+}
+
+}  // namespace oscar

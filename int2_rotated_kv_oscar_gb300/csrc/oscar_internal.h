@@ -1,0 +1,83 @@
+// Internal launch interface between the C-ABI layer (oscar_api.cu) and the
+// kernels (oscar_append.cu, oscar_decode.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace oscar {
+
+// Rotation constants of one layer on the device.
+struct LayerRotation {
+  const float* U_K = nullptr;   // [128][128] row-major (identity when the U factor is off)
+  const float* U_V = nullptr;   // [128][128] row-major
+  const float* U_VT = nullptr;  // [128][128] = U_V transposed (inverse rotation of outputs)
+  float tau_k = 0.f, tau_v = 0.f;
+  unsigned flags = 0;           // kRotH | kRotP (the U factor is folded into the matrices)
+};
+
+struct CacheRefs {
+  uint8_t* pages = nullptr;
+  int64_t num_pages = 0;
+  uint16_t* k_sink = nullptr;
+  uint16_t* v_sink = nullptr;
+  int64_t num_sink = 0;
+  uint16_t* k_ring = nullptr;
+  uint16_t* v_ring = nullptr;
+  int64_t num_ring = 0;
+  const int32_t* page_table = nullptr;
+  int32_t max_pages = 0;
+  const int32_t* sink_page = nullptr;
+  const int32_t* ring_slot = nullptr;
+  int32_t batch = 0;
+  int32_t num_kv_heads = 0;
+};
+
+struct AppendLaunch {
+  CacheRefs c;
+  LayerRotation rot;
+  const uint16_t* k = nullptr;  // bf16 [n_tokens][Hkv][128]
+  const uint16_t* v = nullptr;
+  const int32_t* pos = nullptr;
+  const int32_t* cu_seqlens = nullptr;  // nullptr: one token per request
+  int32_t n_tokens = 0;
+  int32_t max_tokens_per_req = 0;
+  unsigned flags = 0;
+  unsigned* err = nullptr;
+};
+
+cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
+
+// decode workspace layout (bytes, all offsets 256-aligned)
+struct DecodePlan {
+  int32_t batch = 0, Hq = 0, Hkv = 0, g = 0;
+  int32_t chunk_pages = 0;   // pages per work item
+  int32_t n_chunks = 0;      // paged work items per (request, KV head)
+  int32_t n_items = 0;       // all work items per (request, KV head)
+  size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
+};
+
+constexpr int kPartialFloats = 16 + 8 * 128;   // m[8], l[8], acc[8][128]
+constexpr int kQConstFloats = 32;
+
+DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, int num_sms);
+
+struct DecodeLaunch {
+  int mode = 0;   // 0: mixed INT2 + BF16 cache, 1: plain BF16 paged cache
+  CacheRefs c;
+  const uint16_t* kb_pages = nullptr;   // mode 1
+  const uint16_t* vb_pages = nullptr;
+  LayerRotation rot;                    // mode 0
+  const uint16_t* q = nullptr;
+  float* out = nullptr;
+  const int32_t* ctx_len = nullptr;
+  float sm_scale = 0.f;
+  DecodePlan plan;
+  uint8_t* workspace = nullptr;
+  unsigned* err = nullptr;
+};
+
+cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream);
+
+}  // namespace oscar

@@ -141,3 +141,33 @@ def expected_history(tokens_k, tokens_v, L, R_K, R_V, tau_k, tau_v):
             out[p] = (kc[i], ks[i], vc[i], vs[i])
             rot[p] = (Kr[i], Vr[i])
     return out, rot
+
+
+def reconstruct_from_storage(sink_k, sink_v, ring_k, ring_v, blocks, L, R_K, R_V):
+    """K_hat, V_hat [L, 128] (fp64) of one request and KV head from stored bytes.
+
+    sink_k/v: [64, 128] BF16 values; ring_k/v: [256, 128] BF16 values (slot
+    order); blocks: uint8 [n, 4608], the INT2 blocks of logical pages 1..n in
+    order.  History rows are unpacked with the oracle's own layout map,
+    dequantised and rotated back: x_hat = ((c - 1.5) s) R^T.
+    """
+    from . import layout
+    K = np.zeros((L, HEAD_DIM))
+    V = np.zeros((L, HEAD_DIM))
+    (s0, s1), (h0, h1), (r0, r1) = segments(L)
+    K[s0:s1] = np.asarray(sink_k, dtype=np.float64)[s0:s1]
+    V[s0:s1] = np.asarray(sink_v, dtype=np.float64)[s0:s1]
+    if r1 > r0:
+        slots = [ring_slot(p) for p in range(r0, r1)]
+        K[r0:r1] = np.asarray(ring_k, dtype=np.float64)[slots]
+        V[r0:r1] = np.asarray(ring_v, dtype=np.float64)[slots]
+    if h1 > h0:
+        kc, ks, vc, vs = layout.unpack_blocks(blocks)
+        n = h1 - h0          # history starts at row 0 of logical page 1
+        kc = kc.reshape(-1, HEAD_DIM)[:n]
+        vc = vc.reshape(-1, HEAD_DIM)[:n]
+        ks = ks.reshape(-1, 2)[:n]
+        vs = vs.reshape(-1, 2)[:n]
+        K[h0:h1] = rotation.unrotate(quant.dequantize_rows(kc, ks), R_K)
+        V[h0:h1] = rotation.unrotate(quant.dequantize_rows(vc, vs), R_V)
+    return K, V

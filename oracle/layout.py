@@ -130,3 +130,14 @@ def unpack_block(block, n_tokens=PAGE_TOKENS):
     ks = block[K_SCALES:K_SCALES + SCALE_BYTES].copy().view('<f2').reshape(PAGE_TOKENS, 2)
     vs = block[V_SCALES:V_SCALES + SCALE_BYTES].copy().view('<f2').reshape(PAGE_TOKENS, 2)
     return kc, ks[:n_tokens].astype(np.float64), vc, vs[:n_tokens].astype(np.float64)
+
+
+def unpack_blocks(blocks):
+    """Vectorised unpack_block over blocks [N, 4608] -> (kc [N,64,128], ks [N,64,2], vc, vs)."""
+    kb, ki, vb, vi = _tables()
+    blocks = np.asarray(blocks, dtype=np.uint8).reshape(-1, BLOCK_BYTES)
+    kc = (blocks[:, K_CODES + kb] >> ki.astype(np.uint8)) & 3
+    vc = (blocks[:, V_CODES + vb] >> vi.astype(np.uint8)) & 3
+    ks = blocks[:, K_SCALES:K_SCALES + SCALE_BYTES].copy().view('<f2').reshape(-1, PAGE_TOKENS, 2)
+    vs = blocks[:, V_SCALES:V_SCALES + SCALE_BYTES].copy().view('<f2').reshape(-1, PAGE_TOKENS, 2)
+    return kc.astype(np.uint8), ks.astype(np.float64), vc.astype(np.uint8), vs.astype(np.float64)

@@ -46,23 +46,21 @@ def group_codes(xg, s):
 
 
 def quantize_rows(Xr, tau, group=GROUP):
-    """Quantise rotated rows Xr [n, d] group by group.
+    """Quantise rotated rows Xr [n, d] group by group (vectorised over rows).
 
     Returns (codes uint8 [n, d], scales fp64 [n, d // group]); every scale is
-    an fp16 value held in fp64.
+    an fp16 value held in fp64.  Same arithmetic as group_scale/group_codes
+    applied to each (row, group).
     """
     Xr = np.asarray(Xr, dtype=np.float64)
     n, d = Xr.shape
     ng = d // group
-    codes = np.zeros((n, d), dtype=np.uint8)
-    scales = np.zeros((n, ng))
-    for t in range(n):
-        for g in range(ng):
-            xg = Xr[t, g * group:(g + 1) * group]
-            s = group_scale(xg, tau)
-            scales[t, g] = s
-            codes[t, g * group:(g + 1) * group] = group_codes(xg, s)
-    return codes, scales
+    Xg = Xr.reshape(n, ng, group)
+    a = np.minimum(np.abs(Xg).max(axis=2), float(tau))
+    scales = fp16_round(a / LEVEL_OFFSET)
+    s = scales[:, :, None]
+    codes = ((Xg >= -s).astype(np.uint8) + (Xg >= 0).astype(np.uint8) + (Xg >= s).astype(np.uint8))
+    return codes.reshape(n, d), scales
 
 
 def dequantize_rows(codes, scales, group=GROUP):

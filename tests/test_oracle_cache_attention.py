@@ -190,3 +190,32 @@ def test_score_weighted_covariance_matches_output_second_moment():
         o = attention.softmax_attention(Q[n], K, V, 0.5)[0]
         acc += np.outer(o, o)
     assert np.allclose(C, acc / 7)
+
+
+def test_reconstruct_from_storage_matches_cache_model():
+    # storing the model's state with the oracle's packer and reading it back
+    # gives the same K_hat, V_hat as the model itself
+    from oracle import layout
+    r = np.random.default_rng(19)
+    R_K = rotation.composite_rotation(_rand_orth(7))
+    R_V = rotation.composite_rotation(_rand_orth(8))
+    L = 777
+    Kt = _bf16_like(r.standard_normal((L, 128)) * 2)
+    Vt = _bf16_like(r.standard_normal((L, 128)) * 2)
+    c = cache.RequestCache(R_K, R_V, 5.0, 6.0)
+    c.append(Kt[:500], Vt[:500])
+    c.append(Kt[500:], Vt[500:])
+    (_, _), (h0, h1), _ = cache.segments(L)
+    n_pages = (h1 + 63) // 64 - 1
+    blocks = np.zeros((n_pages, 4608), dtype=np.uint8)
+    for i in range(n_pages):
+        lp = i + 1
+        rows = [p for p in range(64 * lp, 64 * lp + 64) if h0 <= p < h1]
+        kc = np.array([c.hist[p][0] for p in rows])
+        ks = np.array([c.hist[p][1] for p in rows])
+        vc = np.array([c.hist[p][2] for p in rows])
+        vs = np.array([c.hist[p][3] for p in rows])
+        blocks[i] = layout.pack_block(kc, ks, vc, vs)
+    K, V = cache.reconstruct_from_storage(c.sink_k, c.sink_v, c.ring_k, c.ring_v, blocks, L, R_K, R_V)
+    Km, Vm = c.dequantized()
+    assert np.abs(K - Km).max() < 1e-12 and np.abs(V - Vm).max() < 1e-12

@@ -180,3 +180,30 @@ def test_partial_block_leaves_rest_zero():
     blk = layout.pack_block(kc, np.ones((10, 2)), kc, np.ones((10, 2)))
     a, _, c, _ = layout.unpack_block(blk)
     assert np.all(a[:10] == 3) and np.all(a[10:] == 0) and np.all(c[10:] == 0)
+
+
+def test_vectorised_rows_equal_per_group_definition():
+    r = np.random.default_rng(21)
+    X = r.standard_normal((50, 128)) * r.uniform(0.1, 5, (50, 1))
+    X[3, :64] = 0.0
+    codes, scales = quant.quantize_rows(X, 2.5)
+    for t in range(50):
+        for g in range(2):
+            xg = X[t, 64 * g:64 * (g + 1)]
+            s = quant.group_scale(xg, 2.5)
+            assert scales[t, g] == s
+            assert np.array_equal(codes[t, 64 * g:64 * (g + 1)], quant.group_codes(xg, s))
+
+
+def test_vectorised_unpack_equals_unpack_block():
+    r = np.random.default_rng(22)
+    blocks = r.integers(0, 256, (3, 4608)).astype(np.uint8)
+    # keep the scale bytes finite fp16 values
+    for i in range(3):
+        blocks[i, 2048:2304] = np.float16(r.uniform(0, 4, 128)).view(np.uint8)
+        blocks[i, 4352:4608] = np.float16(r.uniform(0, 4, 128)).view(np.uint8)
+    kc, ks, vc, vs = layout.unpack_blocks(blocks)
+    for i in range(3):
+        a, b, c, d = layout.unpack_block(blocks[i])
+        assert np.array_equal(kc[i], a) and np.array_equal(vc[i], c)
+        assert np.array_equal(ks[i], b) and np.array_equal(vs[i], d)
