@@ -8,25 +8,29 @@
 //
 // Design (GB300):
 //  * prep kernel, one block per (request, KV head): q' = q R_K (fp32 x U,
-//    Walsh-Hadamard butterfly, bit reversal), folded with sm_scale * log2(e)
-//    and a power-of-two normalisation into fp16 tensor-core B fragments whose
-//    per-channel power-of-two factors match the code unpacking below; the
-//    plain q for the BF16 segment likewise; zeroes the split counters.
+//    Walsh-Hadamard butterfly, bit reversal), times sm_scale * log2(e) and a
+//    power-of-two normalisation, split into fp16 value + fp16 residual and
+//    laid out as tensor-core B fragments; the plain q for the BF16 segment
+//    likewise; zeroes the split counters.
 //  * decode kernel, one block per (work item, KV head, request), 4 warps.
 //    Work items are chunks of INT2 history pages (rotated basis) or 64-token
 //    BF16 blocks (sink, ring quarters; original basis).  Each warp streams
 //    its pages through a private ring of shared-memory stages filled by bulk
-//    asynchronous copies (one 4608-byte copy per page), unpacks the 2-bit
-//    codes in registers with one AND per fp16 pair (a code c masked in place
-//    at bit 2r of an fp16 is the subnormal value c * 2^(2r-24); the 2^(24-2r)
-//    factor lives in the other operand or is applied to the accumulator),
-//    runs QK^T and PV on mma.sync m16n8k16 (tokens x channels, channels x
-//    heads) with an online softmax in the log2 domain, and folds the -1.5
-//    code offset in exactly (accumulator initialisation for K, a ones-row
-//    MMA for V).  Warps merge in shared memory; each block writes one partial
-//    (m, l, acc); the last block of a (request, KV head) merges all partials
-//    (log-sum-exp), rotates the INT2 part back (acc P H U_V^T) and writes the
-//    fp32 output.  No block ever waits on another.
+//    asynchronous copies (one 4608-byte copy per page), turns each pair of
+//    2-bit codes into the exact fp16 levels (c - 1.5) with one LOP3 and one
+//    HFMA2, runs QK^T and PV on mma.sync m16n8k16 (tokens x channels and
+//    channels x tokens against the query heads) with an online softmax in
+//    the log2 domain.  Warps merge in shared memory; each block writes one
+//    partial (m, l, acc); the last block of a (request, KV head) merges all
+//    partials (log-sum-exp), rotates the INT2 part back (acc P H U_V^T) and
+//    writes the fp32 output.  No block ever waits on another.
+//
+// Precision: q and the softmax weights times the V scales enter the MMAs as
+// fp16 value + fp16 residual (~22 significant bits).  With at most 4 query
+// heads per KV head the residual rides in the MMA's otherwise unused N
+// columns 4..7 (no extra MMAs); with 5..8 heads it takes a second MMA.
+
+#include <cmath>
 
 #include "oscar_device.cuh"
 #include "oscar_internal.h"
@@ -39,23 +43,59 @@ constexpr float kInvSqrtD = 0.08838834764831845f;
 constexpr int kWarps = 4;
 constexpr int kStages = 3;
 constexpr unsigned kWaitLimit = 1u << 22;
-constexpr uint32_t kOnesF16x2 = 0x3C003C00u;
-constexpr float kPScale = 1.0f / 256.0f;  // B operand = p * s * 2^-8 keeps lazily-rescaled p in fp16 range
-constexpr float kLazy = 8.0f;             // rescale only when the max grows by more than 2^8
+// The PV B operand is p * s * 2^k (INT2 history, s = V scale) or p * 2^k (BF16
+// tiles), with p <= 2^kLazy.  k is the largest power of two that keeps it
+// below 60000 for the layer's largest possible scale, so small weights stay
+// clear of the fp16 subnormal range.
+constexpr float kLazy = 4.0f;           // rescale only when the max grows by more than 2^4
+constexpr float kPScaleBF16 = 2048.0f;  // 2^4 * 2048 < 60000
 
-// exponent of the fp16 value of a code masked in place at index r of a 16-bit half
-__host__ __device__ constexpr int code_exp(int r) { return r < 5 ? 2 * r - 24 : 2 * r - 30; }
+// Exact fp16 pair of the levels (c - 1.5) of the codes at index r (0..7) of
+// both 16-bit halves of a code word.  One LOP3 puts the code into the low
+// mantissa of the fp16 1024 ((w & mask) | 0x6400: the value 1024 + c 4^r'),
+// one HFMA2 maps it to (1024 + c 4^r') 4^-r' - (1024 4^-r' + 1.5) = c - 1.5.
+// r' is the code's 2-bit position in the source word: index 0 is taken from
+// w << 2 (r' = 1; at r' = 0 the offset 1025.5 would not be an fp16), indices
+// 1..4 from w (r' = r), indices 5..7 from w >> 6 (r' = r - 3).  The levels
+// are normal fp16 numbers: tensor-core products of subnormal operands lose
+// precision.
+struct CodeWord {
+  uint32_t lo2, w, hi6;  // w << 2, w, w >> 6
+  __device__ __forceinline__ explicit CodeWord(uint32_t x) : lo2(x << 2), w(x), hi6(x >> 6) {}
+};
 
-// fp16 pair of the codes at index r (0..7) of both halves of w, masked in place
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t mask) {
+  uint32_t y;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(y) : "r"(x), "r"(mask), "r"(0x64006400u));  // (a & b) | c
+  return y;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 template <int R>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t ws) {
-  return R < 5 ? (w & (0x00030003u << (2 * R))) : (ws & (0x00030003u << (2 * (R - 3))));
+__device__ __forceinline__ uint32_t code_level(const CodeWord& cw) {
+  constexpr int rp = R == 0 ? 1 : (R < 5 ? R : R - 3);
+  // fp16 constants 4^-r' and -(1024 4^-r' + 1.5) for r' = 1..4, in both halves
+  constexpr uint32_t kScale = rp == 1 ? 0x34003400u : rp == 2 ? 0x2C002C00u : rp == 3 ? 0x24002400u : 0x1C001C00u;
+  constexpr uint32_t kBias = rp == 1 ? 0xDC06DC06u : rp == 2 ? 0xD418D418u : rp == 3 ? 0xCC60CC60u : 0xC580C580u;
+  const uint32_t src = R == 0 ? cw.lo2 : (R < 5 ? cw.w : cw.hi6);
+  return hfma2_u32(lop_and_or(src, 0x00030003u << (2 * rp)), kScale, kBias);
 }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// fp16 value of v (part 0) or the fp32 residual v - fp16(v) (part 1, rounded later)
+__device__ __forceinline__ float split_part(float v, int part) {
+  const float hi = __half2float(__float2half_rn(v));
+  return part == 0 ? hi : v - hi;
 }
 
 struct PrepArgs {
@@ -72,6 +112,12 @@ struct PrepArgs {
 
 // ------------------------------------------------------------------ prep
 // grid (Hkv, B), 128 threads.
+//
+// Fragment words per (request, KV head): [32 lanes][32].  The MMA B column of
+// lane L is n = L / 4.  With g <= 4 ("packed"), column n carries head n % 4
+// and part n / 4 (0: fp16 value, 1: fp16 residual) in words 0..15; with
+// g > 4 column n is head n, words 0..15 hold the values and 16..31 the
+// residuals.
 __global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
   __shared__ float xs[kMaxG][kD];
   __shared__ float qr[kMaxG][kD];
@@ -80,6 +126,7 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
   __shared__ float red[8];
   const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int g = a.g, bh = b * a.Hkv + h;
+  const bool packed = g <= 4;
   if (t == 0) a.counters[bh] = 0;
   const float c = a.sm_scale * kLog2e;
   for (int n = 0; n < g; ++n) xs[n][t] = bf16_bits_to_float(a.q[((size_t)b * a.Hq + h * g + n) * kD + t]);
@@ -94,20 +141,26 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
     for (int n = 0; n < kMaxG; ++n)
       if (n < g) z[n] = fmaf(xs[n][i], u, z[n]);
   }
-  for (int n = 0; n < g; ++n) {
+#pragma unroll
+  for (int n = 0; n < kMaxG; ++n) {
+    if (n >= g) break;
     float v = z[n];
     if (a.flags & kRotH) v = fwht128_block(v, scratch) * kInvSqrtD;
     qr[n][t] = v;
   }
   __syncthreads();
-  for (int n = 0; n < g; ++n) {
+#pragma unroll
+  for (int n = 0; n < kMaxG; ++n) {
+    if (n >= g) break;
     const float v = (a.flags & kRotP) ? qr[n][brev7(t)] : qr[n][t];
     z[n] = v * c;
     qp[n][t] = xs[n][t] * c;
   }
   __syncthreads();
-  for (int n = 0; n < g; ++n) qr[n][t] = z[n];
-  // power-of-two normalisations: max |q'| * 2^-E <= 2^-9, max |q| * 2^-Ep <= 2^10
+#pragma unroll
+  for (int n = 0; n < kMaxG; ++n)
+    if (n < g) qr[n][t] = z[n];
+  // power-of-two normalisations: max |q'| 2^-E <= 2^10, max |q| 2^-Ep <= 2^10
   float mr = 0.f, mp = 0.f;
   for (int n = 0; n < g; ++n) {
     mr = fmaxf(mr, fabsf(qr[n][t]));
@@ -125,53 +178,36 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
   int er = 0, ep = 0;
   if (mr > 0.f) {
     frexpf(mr, &er);
-    er += 9;
+    er -= 10;
   }
   if (mp > 0.f) {
     frexpf(mp, &ep);
     ep -= 10;
   }
   const float sr = ldexpf(1.f, -er), sp = ldexpf(1.f, -ep);
-  // B fragments for QK over the INT2 history: lane L = 4 n + tig holds, for
-  // MMA i (group i / 4, r0 = 2 (i % 4)), b0 = q'[n][64 grp + 16 tig + {0, 8} + r0]
-  // and b1 = the same at r0 + 1, each times 2^(-code_exp(r)).
-  uint32_t* qf = a.qfrag + (size_t)bh * 512;
-  uint32_t* qpl = a.qplain + (size_t)bh * 512;
-  for (int e = t; e < 512; e += 128) {
-    const int L = e >> 4, w = e & 15, i = w >> 1, bs = w & 1;
+  // QK B fragments over the INT2 history: MMA i (group i / 4, r0 = 2 (i % 4))
+  // takes b0 = q'[64 grp + 16 tig + {0, 8} + r0] and b1 = the same at r0 + 1.
+  // BF16 segment: MMA ks = i takes channels 32 tig + 4 ks + {0,1} (b0) and {2,3} (b1).
+  uint32_t* qf = a.qfrag + (size_t)bh * kQFragWords;
+  uint32_t* qpl = a.qplain + (size_t)bh * kQFragWords;
+  for (int e = t; e < kQFragWords; e += 128) {
+    const int L = e >> 5, w = e & 31, set = w >> 4, ww = w & 15, i = ww >> 1, bs = ww & 1;
     const int n = L >> 2, tig = L & 3;
+    const int head = packed ? (n & 3) : n;
+    const int part = packed ? (n >> 2) : set;
     uint32_t vr = 0, vp = 0;
-    if (n < g) {
+    if (head < g && !(packed && set == 1)) {
       const int grp = i >> 2, r = 2 * (i & 3) + bs;
       const int ch = 64 * grp + 16 * tig + r;
-      const float f = sr * ldexpf(1.f, -code_exp(r));
-      vr = pack_f16x2(qr[n][ch] * f, qr[n][ch + 8] * f);
-      // BF16 segment: MMA ks = i covers channels 32 tig + 4 ks + {0,1} (b0), {2,3} (b1)
+      vr = pack_f16x2(split_part(qr[head][ch] * sr, part), split_part(qr[head][ch + 8] * sr, part));
       const int cp = 32 * tig + 4 * i + 2 * bs;
-      vp = pack_f16x2(qp[n][cp] * sp, qp[n][cp + 1] * sp);
+      vp = pack_f16x2(split_part(qp[head][cp] * sp, part), split_part(qp[head][cp + 1] * sp, part));
     }
-    qf[L * 16 + w] = vr;
-    qpl[L * 16 + w] = vp;
-  }
-  // -1.5 * sum over each group of the exact fp16 values the MMA multiplies
-  float* qc = a.qconst + (size_t)bh * kQConstFloats;
-  for (int n = 0; n < kMaxG; ++n) {
-    float v = 0.f;
-    if (n < g) {
-      const int r = t & 7;
-      const float f = ldexpf(1.f, -code_exp(r));
-      v = __half2float(__float2half_rn(qr[n][t] * sr * f)) * ldexpf(1.f, code_exp(r));
-    }
-    v = warp_sum(v);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    if (t == 0) {
-      qc[2 * n + 0] = -1.5f * (red[0] + red[1]);
-      qc[2 * n + 1] = -1.5f * (red[2] + red[3]);
-    }
+    qf[e] = vr;
+    qpl[e] = vp;
   }
   if (t == 0) {
+    float* qc = a.qconst + (size_t)bh * kQConstFloats;
     qc[16] = ldexpf(1.f, er);
     qc[17] = ldexpf(1.f, ep);
   }
@@ -193,6 +229,7 @@ struct DecodeArgs {
   int* counters;
   const float* U_VT;
   unsigned flags;
+  float pscale, inv_pscale;
   float* out;
   unsigned* err;
 };
@@ -200,7 +237,6 @@ struct DecodeArgs {
 struct WarpState {
   float m[2], l[2];
   float acc[8][4];
-  float corr[2][4];
 };
 
 __device__ __forceinline__ void state_init(WarpState& st) {
@@ -210,13 +246,9 @@ __device__ __forceinline__ void state_init(WarpState& st) {
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int k = 0; k < 4; ++k) st.acc[i][k] = 0.f;
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) st.corr[i][k] = 0.f;
 }
 
-// Update the running maxima with this page's maxima (per lane: heads 2 tig, 2 tig + 1).
+// Update the running maxima with this tile's maxima (per lane: columns 2 tig, 2 tig + 1).
 __device__ __forceinline__ void online_max(WarpState& st, float mx0, float mx1) {
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -235,13 +267,6 @@ __device__ __forceinline__ void online_max(WarpState& st, float mx0, float mx1) 
       st.acc[i][1] *= a1;
       st.acc[i][3] *= a1;
     }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      st.corr[i][0] *= a0;
-      st.corr[i][2] *= a0;
-      st.corr[i][1] *= a1;
-      st.corr[i][3] *= a1;
-    }
     st.l[0] *= a0;
     st.l[1] *= a1;
     st.m[0] = n0;
@@ -253,10 +278,27 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t u) {
   return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 
+// fp16 pair of (x0, x1) and of their rounding residuals
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_f16x2(x0, x1);
+  const float2 h = half2_bits_to_float2(hi);
+  lo = pack_f16x2(x0 - h.x, x1 - h.y);
+}
+
+// packed mode: lanes holding value columns take the fp16 value, lanes holding
+// residual columns (tig >= 2) take the residual
+__device__ __forceinline__ uint32_t pick_pair(float x0, float x1, bool residual) {
+  uint32_t hi, lo;
+  split_pair(x0, x1, hi, lo);
+  return residual ? lo : hi;
+}
+
 // One 64-token INT2 page (K and V codes + scales) staged in shared memory.
-__device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n_valid, const uint32_t (&qf)[16],
-                                          const float (&qi)[4], float scaleE, WarpState& st, int lane) {
+template <bool PACK4>
+__device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n_valid, const uint32_t* qf,
+                                          float scaleE, float pscale, WarpState& st, int lane) {
   const int q = lane >> 2;
+  const bool resid = (lane & 3) >= 2;
   float lg[4][4];
 #pragma unroll
   for (int T = 0; T < 4; ++T) {
@@ -269,30 +311,47 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
     const float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q)));
     const float2 sb =
         half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q + 8)));
-    float d0[4] = {qi[0], qi[1], qi[0], qi[1]};
-    float d1[4] = {qi[2], qi[3], qi[2], qi[3]};
+    // Tensor-core f32 accumulation truncates, so each group's four MMAs run as
+    // two zero-started chains that are added in fp32.
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, e0[4] = {0.f, 0.f, 0.f, 0.f};
+    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#define OSCAR_QK(D, X, Y, R, I)                                                              \
+  do {                                                                                      \
+    const uint32_t a0 = code_level<R>(X), a1 = code_level<R>(Y), a2 = code_level<R + 1>(X), \
+                   a3 = code_level<R + 1>(Y);                                             \
+    mma_f16(D, a0, a1, a2, a3, qf[2 * (I)], qf[2 * (I) + 1]);                              \
+    if (!PACK4) mma_f16(D, a0, a1, a2, a3, qf[16 + 2 * (I)], qf[16 + 2 * (I) + 1]);        \
+  } while (0)
     {
-      const uint32_t x = kw.x, y = kw.z, xs = x >> 6, ys = y >> 6;  // group 0: token q, token q+8
-      mma_f16(d0, code_pair<0>(x, xs), code_pair<0>(y, ys), code_pair<1>(x, xs), code_pair<1>(y, ys), qf[0], qf[1]);
-      mma_f16(d0, code_pair<2>(x, xs), code_pair<2>(y, ys), code_pair<3>(x, xs), code_pair<3>(y, ys), qf[2], qf[3]);
-      mma_f16(d0, code_pair<4>(x, xs), code_pair<4>(y, ys), code_pair<5>(x, xs), code_pair<5>(y, ys), qf[4], qf[5]);
-      mma_f16(d0, code_pair<6>(x, xs), code_pair<6>(y, ys), code_pair<7>(x, xs), code_pair<7>(y, ys), qf[6], qf[7]);
+      const CodeWord x(kw.x), y(kw.z);  // group 0: token q, token q+8
+      OSCAR_QK(d0, x, y, 0, 0);
+      OSCAR_QK(e0, x, y, 2, 1);
+      OSCAR_QK(d0, x, y, 4, 2);
+      OSCAR_QK(e0, x, y, 6, 3);
     }
     {
-      const uint32_t x = kw.y, y = kw.w, xs = x >> 6, ys = y >> 6;  // group 1
-      mma_f16(d1, code_pair<0>(x, xs), code_pair<0>(y, ys), code_pair<1>(x, xs), code_pair<1>(y, ys), qf[8], qf[9]);
-      mma_f16(d1, code_pair<2>(x, xs), code_pair<2>(y, ys), code_pair<3>(x, xs), code_pair<3>(y, ys), qf[10],
-              qf[11]);
-      mma_f16(d1, code_pair<4>(x, xs), code_pair<4>(y, ys), code_pair<5>(x, xs), code_pair<5>(y, ys), qf[12],
-              qf[13]);
-      mma_f16(d1, code_pair<6>(x, xs), code_pair<6>(y, ys), code_pair<7>(x, xs), code_pair<7>(y, ys), qf[14],
-              qf[15]);
+      const CodeWord x(kw.y), y(kw.w);  // group 1
+      OSCAR_QK(d1, x, y, 0, 4);
+      OSCAR_QK(e1, x, y, 2, 5);
+      OSCAR_QK(d1, x, y, 4, 6);
+      OSCAR_QK(e1, x, y, 6, 7);
+    }
+#undef OSCAR_QK
+    float l0 = fmaf(d0[0] + e0[0], sa.x, (d1[0] + e1[0]) * sa.y) * scaleE;
+    float l1 = fmaf(d0[1] + e0[1], sa.x, (d1[1] + e1[1]) * sa.y) * scaleE;
+    float l2 = fmaf(d0[2] + e0[2], sb.x, (d1[2] + e1[2]) * sb.y) * scaleE;
+    float l3 = fmaf(d0[3] + e0[3], sb.x, (d1[3] + e1[3]) * sb.y) * scaleE;
+    if (PACK4) {  // value column + residual column
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      l2 += __shfl_xor_sync(0xffffffffu, l2, 2);
+      l3 += __shfl_xor_sync(0xffffffffu, l3, 2);
     }
     const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
-    lg[T][0] = va ? fmaf(d0[0], sa.x, d1[0] * sa.y) * scaleE : -INFINITY;
-    lg[T][1] = va ? fmaf(d0[1], sa.x, d1[1] * sa.y) * scaleE : -INFINITY;
-    lg[T][2] = vb ? fmaf(d0[2], sb.x, d1[2] * sb.y) * scaleE : -INFINITY;
-    lg[T][3] = vb ? fmaf(d0[3], sb.x, d1[3] * sb.y) * scaleE : -INFINITY;
+    lg[T][0] = va ? l0 : -INFINITY;
+    lg[T][1] = va ? l1 : -INFINITY;
+    lg[T][2] = vb ? l2 : -INFINITY;
+    lg[T][3] = vb ? l3 : -INFINITY;
   }
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -309,40 +368,71 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
     st.l[0] += p0 + p2;
     st.l[1] += p1 + p3;
     const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
-    float2 va_s = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
-    float2 vb_s = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q + 8)));
-    va_s.x = va ? va_s.x * kPScale : 0.f;
-    va_s.y = va ? va_s.y * kPScale : 0.f;
-    vb_s.x = vb ? vb_s.x * kPScale : 0.f;
-    vb_s.y = vb ? vb_s.y * kPScale : 0.f;
-    const uint32_t b00 = movmatrix_trans(pack_f16x2(p0 * va_s.x, p1 * va_s.x));
-    const uint32_t b01 = movmatrix_trans(pack_f16x2(p2 * vb_s.x, p3 * vb_s.x));
-    const uint32_t b10 = movmatrix_trans(pack_f16x2(p0 * va_s.y, p1 * va_s.y));
-    const uint32_t b11 = movmatrix_trans(pack_f16x2(p2 * vb_s.y, p3 * vb_s.y));
+    float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
+    float2 sb = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q + 8)));
+    sa.x = va ? sa.x * pscale : 0.f;
+    sa.y = va ? sa.y * pscale : 0.f;
+    sb.x = vb ? sb.x * pscale : 0.f;
+    sb.y = vb ? sb.y * pscale : 0.f;
     const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVCodes + 512 * T + 16 * lane);
-    const uint32_t w0 = vw.x, w1 = vw.y, w2 = vw.z, w3 = vw.w;
-    const uint32_t s0 = w0 >> 6, s1 = w1 >> 6, s2 = w2 >> 6, s3 = w3 >> 6;
-#define OSCAR_PV(M, B0, B1)                                                                                  \
-  mma_f16(st.acc[M], code_pair<M>(w0, s0), code_pair<M>(w1, s1), code_pair<M>(w2, s2), code_pair<M>(w3, s3), \
-          B0, B1)
-    OSCAR_PV(0, b00, b01);
-    OSCAR_PV(1, b00, b01);
-    OSCAR_PV(2, b00, b01);
-    OSCAR_PV(3, b00, b01);
-    OSCAR_PV(4, b10, b11);
-    OSCAR_PV(5, b10, b11);
-    OSCAR_PV(6, b10, b11);
-    OSCAR_PV(7, b10, b11);
+    const CodeWord w0(vw.x), w1(vw.y), w2(vw.z), w3(vw.w);
+    if (PACK4) {
+      const uint32_t b00 = movmatrix_trans(pick_pair(p0 * sa.x, p1 * sa.x, resid));
+      const uint32_t b01 = movmatrix_trans(pick_pair(p2 * sb.x, p3 * sb.x, resid));
+      const uint32_t b10 = movmatrix_trans(pick_pair(p0 * sa.y, p1 * sa.y, resid));
+      const uint32_t b11 = movmatrix_trans(pick_pair(p2 * sb.y, p3 * sb.y, resid));
+#define OSCAR_PV(M, B0, B1) \
+  mma_f16(st.acc[M], code_level<M>(w0), code_level<M>(w1), code_level<M>(w2), code_level<M>(w3), B0, B1)
+      OSCAR_PV(0, b00, b01);
+      OSCAR_PV(1, b00, b01);
+      OSCAR_PV(2, b00, b01);
+      OSCAR_PV(3, b00, b01);
+      OSCAR_PV(4, b10, b11);
+      OSCAR_PV(5, b10, b11);
+      OSCAR_PV(6, b10, b11);
+      OSCAR_PV(7, b10, b11);
 #undef OSCAR_PV
-    mma_f16(st.corr[0], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, b00, b01);
-    mma_f16(st.corr[1], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, b10, b11);
+    } else {
+      uint32_t h00, l00, h01, l01, h10, l10, h11, l11;
+      split_pair(p0 * sa.x, p1 * sa.x, h00, l00);
+      split_pair(p2 * sb.x, p3 * sb.x, h01, l01);
+      split_pair(p0 * sa.y, p1 * sa.y, h10, l10);
+      split_pair(p2 * sb.y, p3 * sb.y, h11, l11);
+      h00 = movmatrix_trans(h00);
+      l00 = movmatrix_trans(l00);
+      h01 = movmatrix_trans(h01);
+      l01 = movmatrix_trans(l01);
+      h10 = movmatrix_trans(h10);
+      l10 = movmatrix_trans(l10);
+      h11 = movmatrix_trans(h11);
+      l11 = movmatrix_trans(l11);
+#define OSCAR_PV2(M, H0, H1, L0, L1)                                                       \
+  do {                                                                                     \
+    const uint32_t a0 = code_level<M>(w0), a1 = code_level<M>(w1), a2 = code_level<M>(w2), \
+                   a3 = code_level<M>(w3);                                               \
+    mma_f16(st.acc[M], a0, a1, a2, a3, H0, H1);                                            \
+    mma_f16(st.acc[M], a0, a1, a2, a3, L0, L1);                                            \
+  } while (0)
+      OSCAR_PV2(0, h00, h01, l00, l01);
+      OSCAR_PV2(1, h00, h01, l00, l01);
+      OSCAR_PV2(2, h00, h01, l00, l01);
+      OSCAR_PV2(3, h00, h01, l00, l01);
+      OSCAR_PV2(4, h10, h11, l10, l11);
+      OSCAR_PV2(5, h10, h11, l10, l11);
+      OSCAR_PV2(6, h10, h11, l10, l11);
+      OSCAR_PV2(7, h10, h11, l10, l11);
+#undef OSCAR_PV2
+    }
   }
 }
 
 // One 16-token BF16 tile (rows of K and V in global memory, original basis).
-__device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt, int n_valid,
-                                          const uint32_t (&qpf)[16], float scaleEp, WarpState& st, int lane) {
+template <bool PACK4>
+__device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
+                                          int n_valid, const uint32_t* qpf, float scaleEp, WarpState& st,
+                                          int lane) {
   const int q = lane >> 2, tig = lane & 3;
+  const bool resid = tig >= 2;
   const bool va = q < n_valid, vb = q + 8 < n_valid;
   uint32_t ka[16], kb[16];
 #pragma unroll
@@ -358,17 +448,43 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
     kb[4 * k + 2] = bf16x2_to_f16x2(u.z);
     kb[4 * k + 3] = bf16x2_to_f16x2(u.w);
   }
-  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) mma_f16(d, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[2 * ks], qpf[2 * ks + 1]);
-  const float l0 = va ? d[0] * scaleEp : -INFINITY, l1 = va ? d[1] * scaleEp : -INFINITY;
-  const float l2 = vb ? d[2] * scaleEp : -INFINITY, l3 = vb ? d[3] * scaleEp : -INFINITY;
+  for (int ks = 0; ks < 8; ++ks) {
+    float(&acc)[4] = (ks & 1) ? e : d;  // two chains, added in fp32 (the MMA accumulation truncates)
+    mma_f16(acc, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[2 * ks], qpf[2 * ks + 1]);
+    if (!PACK4)
+      mma_f16(acc, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[16 + 2 * ks], qpf[17 + 2 * ks]);
+  }
+  float l0 = (d[0] + e[0]) * scaleEp, l1 = (d[1] + e[1]) * scaleEp;
+  float l2 = (d[2] + e[2]) * scaleEp, l3 = (d[3] + e[3]) * scaleEp;
+  if (PACK4) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    l2 += __shfl_xor_sync(0xffffffffu, l2, 2);
+    l3 += __shfl_xor_sync(0xffffffffu, l3, 2);
+  }
+  l0 = va ? l0 : -INFINITY;
+  l1 = va ? l1 : -INFINITY;
+  l2 = vb ? l2 : -INFINITY;
+  l3 = vb ? l3 : -INFINITY;
   online_max(st, fmaxf(l0, l2), fmaxf(l1, l3));
   const float p0 = ex2(l0 - st.m[0]), p1 = ex2(l1 - st.m[1]), p2 = ex2(l2 - st.m[0]), p3 = ex2(l3 - st.m[1]);
   st.l[0] += p0 + p2;
   st.l[1] += p1 + p3;
-  const uint32_t b0 = movmatrix_trans(pack_f16x2(p0 * kPScale, p1 * kPScale));
-  const uint32_t b1 = movmatrix_trans(pack_f16x2(p2 * kPScale, p3 * kPScale));
+  uint32_t b0h, b0l, b1h, b1l;
+  if (PACK4) {
+    b0h = movmatrix_trans(pick_pair(p0 * kPScaleBF16, p1 * kPScaleBF16, resid));
+    b1h = movmatrix_trans(pick_pair(p2 * kPScaleBF16, p3 * kPScaleBF16, resid));
+    b0l = b1l = 0u;
+  } else {
+    split_pair(p0 * kPScaleBF16, p1 * kPScaleBF16, b0h, b0l);
+    split_pair(p2 * kPScaleBF16, p3 * kPScaleBF16, b1h, b1l);
+    b0h = movmatrix_trans(b0h);
+    b0l = movmatrix_trans(b0l);
+    b1h = movmatrix_trans(b1h);
+    b1l = movmatrix_trans(b1l);
+  }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     uint32_t a[4];
@@ -376,12 +492,13 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
     for (int blkid = 0; blkid < 4; ++blkid) {
       const int tr = blkid >> 1, cc = blkid & 1;  // token half, channel half
       const bool ok = tr ? vb : va;
-      const uint32_t u = ok ? __ldg(reinterpret_cast<const uint32_t*>(Vt + (8 * tr + q) * kD + 16 * mt + 8 * cc + 2 * tig))
-                            : 0u;
+      const uint32_t u =
+          ok ? __ldg(reinterpret_cast<const uint32_t*>(Vt + (8 * tr + q) * kD + 16 * mt + 8 * cc + 2 * tig)) : 0u;
       a[blkid] = movmatrix_trans(bf16x2_to_f16x2(u));
     }
     // a[0]: channels 16mt+q, tokens 2tig..; a[1]: channels +8; a[2]: tokens +8; a[3]: both
-    mma_f16(st.acc[mt], a[0], a[1], a[2], a[3], b0, b1);
+    mma_f16(st.acc[mt], a[0], a[1], a[2], a[3], b0h, b1h);
+    if (!PACK4) mma_f16(st.acc[mt], a[0], a[1], a[2], a[3], b0l, b1l);
   }
 }
 
@@ -391,7 +508,7 @@ struct MergeSmem {
   float acc[kWarps][8][kD];
 };
 
-template <int MODE>
+template <int MODE, bool PACK4>
 __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -406,6 +523,7 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
   WarpState st;
   state_init(st);
   const bool rotated = (MODE == 0) && item < a.n_chunks;
+  constexpr int kQW = PACK4 ? 16 : 32;
 
   if (rotated) {
     // ---------------- INT2 history pages
@@ -420,11 +538,11 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
     const int first = lp0 + warp;
     const int n_my = first < lp1 ? (lp1 - first + kWarps - 1) / kWarps : 0;
     if (n_my > 0) {
-      uint32_t qf[16];
+      uint32_t qf[kQW];
       {
-        const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bh * 512 + lane * 16);
+        const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bh * kQFragWords + lane * 32);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kQW / 4; ++k) {
           const uint4 u = __ldg(src + k);
           qf[4 * k] = u.x;
           qf[4 * k + 1] = u.y;
@@ -432,10 +550,7 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
           qf[4 * k + 3] = u.w;
         }
       }
-      const float* qc = a.qconst + (size_t)bh * kQConstFloats;
-      const float qi[4] = {__ldg(qc + 2 * (2 * tig) + 0), __ldg(qc + 2 * (2 * tig + 1) + 0), __ldg(qc + 2 * (2 * tig) + 1),
-                           __ldg(qc + 2 * (2 * tig + 1) + 1)};
-      const float scaleE = __ldg(qc + 16);
+      const float scaleE = __ldg(a.qconst + (size_t)bh * kQConstFloats + 16);
       uint8_t* stages = smem + (size_t)warp * kStages * kBlockBytes;
       uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + warp * kStages;
       const uint8_t* pool = c.pages;
@@ -475,7 +590,7 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
         const int lp = first + kWarps * k;
         if (phys_of(k) >= 0) {
           const int n_valid = min(kPage, hist_end - kPage * lp);
-          int2_page(stages + (size_t)s * kBlockBytes, n_valid, qf, qi, scaleE, st, lane);
+          int2_page<PACK4>(stages + (size_t)s * kBlockBytes, n_valid, qf, scaleE, a.pscale, st, lane);
         }
         __syncwarp();
         if (lane == 0 && k + kStages < n_my) {
@@ -484,16 +599,17 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
         }
       }
       // after a timeout, wait (bounded) for the copies still in flight
-      for (int kk = k + 1; kk < min(k + kStages, n_my); ++kk) mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, kWaitLimit);
+      for (int kk = k + 1; kk < min(k + kStages, n_my); ++kk)
+        mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, kWaitLimit);
       if (k < n_my) mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1, kWaitLimit);
     }
   } else {
     // ---------------- BF16 tiles (original basis)
-    uint32_t qpf[16];
+    uint32_t qpf[kQW];
     {
-      const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * 512 + lane * 16);
+      const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kQW / 4; ++k) {
         const uint4 u = __ldg(src + k);
         qpf[4 * k] = u.x;
         qpf[4 * k + 1] = u.y;
@@ -535,26 +651,25 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
         }
       }
       const int nv = min(16, valid - 16 * warp);
-      if (nv > 0) bf16_tile(Kb + 16 * warp * kD, Vb + 16 * warp * kD, nv, qpf, scaleEp, st, lane);
+      if (nv > 0) bf16_tile<PACK4>(Kb + 16 * warp * kD, Vb + 16 * warp * kD, nv, qpf, scaleEp, st, lane);
     } else {
-      // plain BF16 paged cache: item covers pages [item*C, item*C + C)
+      // plain BF16 paged cache: item covers pages [item*C, item*C + C); warp w takes tile w of each
       const int n_pages = (L + kPage - 1) / kPage;
       if (n_pages > c.max_pages) {
         if (t == 0 && item == 0) set_error(a.err, kErrLength);
       }
       const int pg0 = item * a.chunk_pages;
       const int pg1 = min(min(pg0 + a.chunk_pages, n_pages), c.max_pages);
-      for (int tt = warp; (pg0 + tt / 4) < pg1; tt += kWarps) {
-        const int pg = pg0 + tt / 4, tile = tt & 3;
+      for (int pg = pg0; pg < pg1; ++pg) {
         const int ph = c.page_table[(size_t)b * c.max_pages + pg];
         if (ph < 0 || ph >= c.num_pages) {
           if (lane == 0) set_error(a.err, kErrPage);
           continue;
         }
-        const int nv = min(16, L - kPage * pg - 16 * tile);
+        const int nv = min(16, L - kPage * pg - 16 * warp);
         if (nv <= 0) continue;
-        const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
-        bf16_tile(a.kb_pages + off, a.vb_pages + off, nv, qpf, scaleEp, st, lane);
+        const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * warp) * kD;
+        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, nv, qpf, scaleEp, st, lane);
       }
     }
   }
@@ -567,22 +682,23 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
     st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
     st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
   }
-  if (q == 0) {
+  // packed mode: columns 4..7 hold the residual parts of heads 0..3
+  const bool writer = PACK4 ? (tig < 2) : true;
+  if (q == 0 && writer) {
     ms.m[warp][2 * tig] = st.m[0];
     ms.m[warp][2 * tig + 1] = st.m[1];
     ms.l[warp][2 * tig] = st.l[0];
     ms.l[warp][2 * tig + 1] = st.l[1];
   }
+  const float inv = rotated ? a.inv_pscale : 1.0f / kPScaleBF16;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    const float f = rotated ? ldexpf(256.f, -code_exp(mt)) : 256.f;
-    const int grp = mt >> 2;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ch = 16 * mt + q + 8 * (i >> 1), n = 2 * tig + (i & 1);
-      float v = st.acc[mt][i] * f;
-      if (rotated) v = fmaf(-1.5f * 256.f, st.corr[grp][i & 1], v);
-      ms.acc[warp][n][ch] = v;
+      float v = st.acc[mt][i] * inv;
+      if (PACK4) v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (writer) ms.acc[warp][n][ch] = v;
     }
   }
   __syncthreads();
@@ -655,7 +771,9 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
     // rotate the INT2 part back: y = acc P, y = y H / sqrt(d), out = y U_V^T
     float* ys = reinterpret_cast<float*>(smem);  // [8][128]
     float* scratch = ys + kMaxG * kD;
-    for (int n = 0; n < a.g; ++n) ys[n * kD + t] = Ar[n];
+#pragma unroll
+    for (int n = 0; n < kMaxG; ++n)
+      if (n < a.g) ys[n * kD + t] = Ar[n];
     __syncthreads();
     for (int n = 0; n < a.g; ++n) {
       float v = (a.flags & kRotP) ? ys[n * kD + brev7(t)] : ys[n * kD + t];
@@ -723,9 +841,9 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   p.off_counters = off;
   off = align256(off + bh * sizeof(int));
   p.off_qfrag = off;
-  off = align256(off + bh * 512 * sizeof(uint32_t));
+  off = align256(off + bh * kQFragWords * sizeof(uint32_t));
   p.off_qplain = off;
-  off = align256(off + bh * 512 * sizeof(uint32_t));
+  off = align256(off + bh * kQFragWords * sizeof(uint32_t));
   p.off_qconst = off;
   off = align256(off + bh * kQConstFloats * sizeof(float));
   p.off_partials = off;
@@ -773,26 +891,29 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
   a.counters = pa.counters;
   a.U_VT = d.rot.U_VT;
   a.flags = d.rot.flags;
+  {
+    // largest V scale the layer can store: fp16(min(absmax, tau_v) / 1.5) <= 65504
+    const float smax = std::isfinite(d.rot.tau_v) ? fminf(65504.f, d.rot.tau_v / 1.5f * 1.001f) : 65504.f;
+    int k = (int)floorf(log2f(60000.f / (16.f * smax)));
+    k = k < -20 ? -20 : (k > 20 ? 20 : k);
+    a.pscale = ldexpf(1.f, k);
+    a.inv_pscale = ldexpf(1.f, -k);
+  }
   a.out = d.out;
   a.err = d.err;
   const size_t smem = decode_smem_bytes();
-  static bool attr0 = false, attr1 = false;
   const dim3 grid(p.n_items, p.Hkv, p.batch);
-  if (d.mode == 0) {
-    if (!attr0) {
-      e = cudaFuncSetAttribute(decode_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr0 = true;
-    }
-    decode_kernel<0><<<grid, 128, smem, stream>>>(a);
-  } else {
-    if (!attr1) {
-      e = cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr1 = true;
-    }
-    decode_kernel<1><<<grid, 128, smem, stream>>>(a);
+  const bool pack4 = p.g <= 4;
+  void (*kern)(DecodeArgs) = d.mode == 0 ? (pack4 ? decode_kernel<0, true> : decode_kernel<0, false>)
+                                         : (pack4 ? decode_kernel<1, true> : decode_kernel<1, false>);
+  static bool attr_done[4] = {false, false, false, false};
+  const int which = 2 * d.mode + (pack4 ? 1 : 0);
+  if (!attr_done[which]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done[which] = true;
   }
+  kern<<<grid, 128, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

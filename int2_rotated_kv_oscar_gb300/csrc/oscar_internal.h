@@ -60,6 +60,7 @@ struct DecodePlan {
 
 constexpr int kPartialFloats = 16 + 8 * 128;   // m[8], l[8], acc[8][128]
 constexpr int kQConstFloats = 32;
+constexpr int kQFragWords = 32 * 32;   // q fragments per (request, KV head): [lane][32]
 
 DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, int num_sms);
 
