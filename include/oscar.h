@@ -254,6 +254,30 @@ oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
                                     const oscar_decode_args* args, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/*
+ * Allocation-free variant of oscar_decode_attention (the pages have no
+ * counterpart: this is a service of this library).  Some callers cannot
+ * allocate device memory: a plugin inside an inference engine whose memory
+ * planner owns every device allocation and hands out no workspace, or a
+ * latency-critical serving loop that must not call cudaMalloc (it can
+ * synchronise the device) once it is running.  This entry point takes the
+ * decode scratch from a static device array of OSCAR_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) built into the library; every GPU that loads the library holds it
+ * until the process exits.  Same arguments and results as
+ * oscar_decode_attention minus the workspace; the caller still owns q, out,
+ * the cache and the lengths.  A call whose scratch need
+ * (oscar_decode_workspace_bytes for its batch and max_ctx_len) exceeds the
+ * array returns OSCAR_ERR_WORKSPACE and launches nothing.  The first call on
+ * a device looks up the array's device address with that device current, so
+ * make that first call before any stream capture.  All calls share the one
+ * array, which keeps the last call's contents (the kernels re-initialise what
+ * they need): calls that overlap on the GPU, from any stream or thread, race
+ * and must be serialised by the caller.  Allocates nothing.
+ */
+#define OSCAR_NOALLOC_SCRATCH_BYTES (16u << 20)
+oscar_status oscar_decode_attention_noalloc(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                                            const oscar_decode_args* args, void* stream);
+
 /* Comparator: the same decode over a plain BF16 paged cache (the baseline
  * the pages' decode speed-ups are quoted against).  Same workspace rules. */
 oscar_status oscar_decode_attention_bf16(oscar_ctx* ctx, const oscar_bf16_cache_view* view,

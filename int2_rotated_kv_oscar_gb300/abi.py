@@ -17,6 +17,7 @@ RECENT_TOKENS = 256
 GROUP = 64
 MAX_GQA = 8
 BLOCK_BYTES = 4608
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 OSCAR_OK = 0
 STATUS_NAMES = {0: "OSCAR_OK", 1: "OSCAR_ERR_INVALID_ARG", 2: "OSCAR_ERR_UNSUPPORTED", 3: "OSCAR_ERR_NOT_LOADED",
@@ -85,6 +86,8 @@ SIGNATURES = {
     "oscar_decode_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
                                               ctypes.POINTER(oscar_decode_args), ctypes.c_void_p, ctypes.c_size_t,
                                               ctypes.c_void_p]),
+    "oscar_decode_attention_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
+                                                      ctypes.POINTER(oscar_decode_args), ctypes.c_void_p]),
     "oscar_decode_attention_bf16": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(oscar_bf16_cache_view),
                                                    ctypes.POINTER(oscar_decode_args), ctypes.c_void_p,
                                                    ctypes.c_size_t, ctypes.c_void_p]),
@@ -182,6 +185,12 @@ def oscar_decode_workspace_bytes(ctx, max_batch, max_ctx_len):
 def oscar_decode_attention(ctx, layer, view, args, workspace, workspace_bytes, stream=None):
     _check(load().oscar_decode_attention(ctx, layer, ctypes.byref(view), ctypes.byref(args), _ptr(workspace),
                                          workspace_bytes, _stream(stream)), "oscar_decode_attention")
+
+
+def oscar_decode_attention_noalloc(ctx, layer, view, args, stream=None):
+    """Decode with the library's built-in scratch array instead of a caller workspace."""
+    _check(load().oscar_decode_attention_noalloc(ctx, layer, ctypes.byref(view), ctypes.byref(args),
+                                                 _stream(stream)), "oscar_decode_attention_noalloc")
 
 
 def oscar_decode_attention_bf16(ctx, view, args, workspace, workspace_bytes, stream=None):

@@ -3,6 +3,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -306,3 +307,62 @@ oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bi
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode: the same launch as oscar_decode_attention, with its
+// workspace in a file-scope device array instead of caller memory.  Every GPU
+// that loads this library holds the array until the process exits.  Its
+// device address is looked up once per device, on the first call made with
+// that device current, and cached.
+
+static __device__ __align__(256) uint8_t g_decode_scratch[OSCAR_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of g_decode_scratch on `device` (which must be current).
+cudaError_t scratch_address(int device, void** out) {
+  if (device < 0 || device >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[device] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[device] = p;
+  }
+  *out = g_scratch_addr[device];
+  return cudaSuccess;
+}
+}  // namespace
+
+extern "C" oscar_status oscar_decode_attention_noalloc(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                                                       const oscar_decode_args* args, void* stream) {
+  if (ctx == nullptr || view == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded[layer]) return OSCAR_ERR_NOT_LOADED;
+  if (!valid_view(ctx, view)) return OSCAR_ERR_INVALID_ARG;
+  if (view->batch == 0) return OSCAR_OK;
+  if (view->batch > 65535) return OSCAR_ERR_UNSUPPORTED;
+  if (!aligned16(view->int2_pages)) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->cfg.device);
+  void* scratch = nullptr;
+  if (scratch_address(ctx->cfg.device, &scratch) != cudaSuccess) return OSCAR_ERR_CUDA;
+  DecodePlan plan;
+  const oscar_status st =
+      check_decode_args(ctx, args, view->batch, scratch, OSCAR_NOALLOC_SCRATCH_BYTES, 0, &plan);
+  if (st != OSCAR_OK) return st;  // OSCAR_ERR_WORKSPACE when the call needs more than the array holds
+  DecodeLaunch d;
+  d.mode = 0;
+  d.c = refs_of(ctx, view);
+  d.rot = rotation_of(ctx, layer);
+  d.q = static_cast<const uint16_t*>(args->q);
+  d.out = args->out;
+  d.ctx_len = args->ctx_len;
+  d.sm_scale = args->sm_scale > 0.f ? args->sm_scale : 1.0f / std::sqrt(128.0f);
+  d.plan = plan;
+  d.workspace = static_cast<uint8_t*>(scratch);
+  d.err = ctx->d_err;
+  return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
