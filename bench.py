@@ -267,10 +267,14 @@ def run_cuda(args):
 
     def step(j, stream, events=None):
         for layer in range(N_LAYERS):
-            abi.oscar_kv_append(ctx, layer, views[layer], app_args[layer][j], stream)
             if events is not None:
                 events[layer][0].record(stream)
-            abi.oscar_decode_attention(ctx, layer, views[layer], dec_args[layer][j], ws, ws_bytes, stream)
+            if args.split:
+                abi.oscar_kv_append(ctx, layer, views[layer], app_args[layer][j], stream)
+                abi.oscar_decode_attention(ctx, layer, views[layer], dec_args[layer][j], ws, ws_bytes, stream)
+            else:
+                abi.oscar_decode_step(ctx, layer, views[layer], app_args[layer][j], dec_args[layer][j], ws, ws_bytes,
+                                      stream)
             if events is not None:
                 events[layer][1].record(stream)
 
@@ -313,9 +317,9 @@ def run_cuda(args):
     bytes_step = N_LAYERS * bytes_layer
     kv_gbs = bytes_step / (ms_step / 1e3) / 1e9
 
-    # ---- per-call timing of the decode call (prep + split-K decode): eager
-    # launches queued behind a GPU-side sleep, so the host runs ahead and each
-    # event pair brackets only GPU work
+    # ---- per-layer timing of one decode step (append + q rotation, split-K
+    # decode): eager launches queued behind a GPU-side sleep, so the host runs
+    # ahead and each event pair brackets only GPU work
     ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(N_LAYERS)]
     durs = []
     for j in range(16):
@@ -404,7 +408,8 @@ def run_cuda(args):
                 "kv_read_gbs": b_bytes_layer / (b_ms_layer / 1e3) / 1e9, "layers_timed": layers_b,
                 "int2_decode_speedup": b_ms_layer / dec_ms,
                 "note": "BF16 paged cache of the same shape (all 100,001 positions BF16), decode calls only, "
-                        "CUDA graph over the layers; speedup = BF16 decode call time / INT2 decode call time"}
+                        "CUDA graph over the layers; speedup = BF16 decode call time / INT2 layer step time "
+                        "(the INT2 step includes its append)"}
         assert abi.oscar_check_device_error(ctx) == 0
         del bcaches, gb
 
@@ -455,12 +460,15 @@ def run_cuda(args):
         "hbm_frac": kv_gbs / peak,
         "algorithmic_bytes_per_step": bytes_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "decode call: prep + split-K decode with in-kernel combine",
+                     "traffic": None,
+                     "kernel": ("one layer's decode step: " + ("append kernel, then q-rotation + split-K decode"
+                                if args.split else "fused append + q-rotation kernel, then split-K decode") +
+                                " with in-kernel combine (bytes: the decode's reads and writes only)"),
                      "peak_kind": peak_kind, "bytes_per_launch": bytes_layer, "avg_launch_ms": dec_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": world * 1000.0 / e2e_ms, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": N_LAYERS * 3 * args.steps,
+        "gpu_launches": N_LAYERS * (3 if args.split else 2) * args.steps,
         "clocks": clocks.summary(),
         "bf16_comparator": bf16,
         "setup_s": {"calibration": t_cal, "prefill": t_prefill},
@@ -482,6 +490,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--split", action="store_true", help="append and decode as separate calls (3 launches a layer)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

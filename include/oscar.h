@@ -255,6 +255,28 @@ oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
                                     void* stream);
 
 /*
+ * One decode step of one layer: oscar_kv_append of one new token per
+ * request, then oscar_decode_attention, in two kernel launches instead of
+ * three ([IT] "Architettura ...": the decode path is append, evict/quantise,
+ * attend).  The first kernel writes the new K/V token of every
+ * (request, KV head) (evicting and quantising the ring row it replaces) and
+ * rotates that request's queries into the K basis in the same block; the
+ * second is the split-K decode kernel.  Both are launched with programmatic
+ * dependent launch, so each may start its prologue while the kernel before it
+ * on the stream drains; neither reads a buffer the kernel before it writes
+ * until that kernel has completed.  append: cu_seqlens NULL, n_tokens ==
+ * batch, flags 0 or OSCAR_APPEND_FRESH_RING (same meaning as for
+ * oscar_kv_append); decode: as oscar_decode_attention, with ctx_len[b]
+ * normally pos[b] + 1 so that the token just written is attended.  Results
+ * equal oscar_kv_append followed by oscar_decode_attention on the same
+ * arguments.  Errors: as the two calls; nothing is launched when either
+ * argument set is rejected.
+ */
+oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                               const oscar_append_args* append, const oscar_decode_args* decode,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Allocation-free variant of oscar_decode_attention (the pages have no
  * counterpart: this is a service of this library).  Some callers cannot
  * allocate device memory: a plugin inside an inference engine whose memory

@@ -255,6 +255,48 @@ oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
   return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                               const oscar_append_args* append, const oscar_decode_args* decode, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (ctx == nullptr || view == nullptr || append == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded[layer]) return OSCAR_ERR_NOT_LOADED;
+  if (!valid_view(ctx, view)) return OSCAR_ERR_INVALID_ARG;
+  if (view->batch == 0) return OSCAR_OK;
+  if (view->batch > 65535) return OSCAR_ERR_UNSUPPORTED;
+  if (append->k == nullptr || append->v == nullptr || append->pos == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (append->cu_seqlens != nullptr || append->n_tokens != view->batch) return OSCAR_ERR_INVALID_ARG;
+  if ((append->flags & ~OSCAR_APPEND_FRESH_RING) != 0) return OSCAR_ERR_INVALID_ARG;
+  DecodePlan plan;
+  const oscar_status st = check_decode_args(ctx, decode, view->batch, workspace, workspace_bytes, 0, &plan);
+  if (st != OSCAR_OK) return st;
+  if (!aligned16(view->int2_pages)) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->cfg.device);
+  AppendLaunch a;
+  a.c = refs_of(ctx, view);
+  a.rot = rotation_of(ctx, layer);
+  a.k = static_cast<const uint16_t*>(append->k);
+  a.v = static_cast<const uint16_t*>(append->v);
+  a.pos = append->pos;
+  a.cu_seqlens = nullptr;
+  a.n_tokens = append->n_tokens;
+  a.max_tokens_per_req = 1;
+  a.flags = append->flags;
+  a.err = ctx->d_err;
+  DecodeLaunch d;
+  d.mode = 0;
+  d.c = a.c;
+  d.rot = a.rot;
+  d.q = static_cast<const uint16_t*>(decode->q);
+  d.out = decode->out;
+  d.ctx_len = decode->ctx_len;
+  d.sm_scale = decode->sm_scale > 0.f ? decode->sm_scale : 1.0f / std::sqrt(128.0f);
+  d.plan = plan;
+  d.workspace = static_cast<uint8_t*>(workspace);
+  d.err = ctx->d_err;
+  return launch_decode_step(a, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
 oscar_status oscar_decode_attention_bf16(oscar_ctx* ctx, const oscar_bf16_cache_view* view,
                                          const oscar_decode_args* args, void* workspace, size_t workspace_bytes,
                                          void* stream) {

@@ -16,143 +16,19 @@
 
 #include "oscar_device.cuh"
 #include "oscar_internal.h"
+#include "oscar_quant.cuh"
 
 namespace oscar {
 namespace {
 
-constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)
-
-// Byte offset inside a block's K code area of the 32-bit word holding the
-// codes of (row t, quarter tig, group grp).
-__device__ __forceinline__ int k_word_offset(int t, int tig, int grp) {
-  const int T = t >> 4, u = t & 15;
-  return 512 * T + 16 * (4 * (u & 7) + tig) + 4 * (2 * (u >> 3) + grp);
-}
-
-// Byte offset inside a block's V code area of the 16-bit half holding the
-// codes of row t for the channels {jj + 16 r : r = 0..7}.
-__device__ __forceinline__ int v_half_offset(int t, int jj) {
-  const int T = t >> 4, u = t & 15;
-  return 512 * T + 16 * (4 * (jj & 7) + ((u & 7) >> 1)) + 4 * (2 * (u >> 3) + (jj >> 3)) + 2 * (u & 1);
-}
-
-struct QuantSmem {
-  float x[kD];
-  float scratch[kD];
-  float red[4];
-  uint8_t code[kD];
-};
-
-// Rotate + clip + quantise one token held one channel per thread (128
-// threads) and store its codes and scales in row `row` of the K or V half of
-// `block`.  All 128 threads must call it.
-__device__ void quantize_token(float x, const float* __restrict__ U, unsigned flags, float tau, uint8_t* block,
-                               int row, bool is_v, QuantSmem& sm) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  sm.x[t] = x;
-  __syncthreads();
-  float z = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < kD; ++i) z = fmaf(sm.x[i], __ldg(U + i * kD + t), z);
-  if (flags & kRotH) z = fwht128_block(z, sm.scratch) * kInvSqrtD;
-  if (flags & kRotP) {
-    __syncthreads();
-    sm.scratch[t] = z;
-    __syncthreads();
-    z = sm.scratch[brev7(t)];
-  }
-  const float amax = warp_max(fabsf(z));
-  if (lane == 0) sm.red[warp] = amax;
-  __syncthreads();
-  const int grp = t >> 6;
-  const float a = fminf(fmaxf(sm.red[2 * grp], sm.red[2 * grp + 1]), tau);
-  const __half sh = __float2half_rn(a / 1.5f);
-  const float s = __half2float(sh);
-  sm.code[t] = (uint8_t)((z >= -s) + (z >= 0.f) + (z >= s));
-  __syncthreads();
-  if (!is_v) {
-    if (t < 8) {
-      const int tig = t & 3, g = t >> 2, base = 64 * g + 16 * tig;
-      uint32_t w = 0;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        w |= (uint32_t)sm.code[base + r] << (2 * r);
-        w |= (uint32_t)sm.code[base + 8 + r] << (16 + 2 * r);
-      }
-      *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, tig, g)) = w;
-    }
-  } else {
-    if (t < 16) {
-      uint32_t hv = 0;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[t + 16 * r] << (2 * r);
-      *reinterpret_cast<uint16_t*>(block + kVCodes + v_half_offset(row, t)) = (uint16_t)hv;
-    }
-  }
-  if ((t & 63) == 0)
-    *reinterpret_cast<__half*>(block + (is_v ? kVScales : kKScales) + 4 * row + 2 * grp) = sh;
-  __syncthreads();
-}
-
-// Locate (and check) the INT2 block of position e of request b, head h.
-__device__ __forceinline__ uint8_t* history_block(const CacheRefs& c, int b, int h, int e, unsigned* err) {
-  const int lp = e >> 6;
-  if (lp >= c.max_pages) {
-    if (threadIdx.x == 0) set_error(err, kErrLength);
-    return nullptr;
-  }
-  const int phys = c.page_table[(size_t)b * c.max_pages + lp];
-  if (phys < 0 || phys >= c.num_pages) {
-    if (threadIdx.x == 0) set_error(err, kErrPage);
-    return nullptr;
-  }
-  return c.pages + ((size_t)phys * c.num_kv_heads + h) * kBlockBytes;
-}
-
 // ------------------------------------------------------------------ decode append
-// One new token per request.  grid (Hkv, B), 128 threads.
-__global__ void __launch_bounds__(128) append_one_kernel(AppendLaunch a) {
-  __shared__ QuantSmem sm;
-  const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const CacheRefs& c = a.c;
-  const int Hkv = c.num_kv_heads;
-  const int p = a.pos[b];
-  const size_t src = ((size_t)b * Hkv + h) * kD + t;
-  const uint16_t kn = a.k[src], vn = a.v[src];
-  if (p < 0 || ((a.flags & 1u) && p > kSink)) {
-    if (t == 0) set_error(a.err, kErrLength);
-    return;
-  }
-  if (p < kSink) {
-    const int sp = c.sink_page[b];
-    if (sp < 0 || sp >= c.num_sink) {
-      if (t == 0) set_error(a.err, kErrSink);
-      return;
-    }
-    const size_t dst = (((size_t)sp * Hkv + h) * kSink + p) * kD + t;
-    c.k_sink[dst] = kn;
-    c.v_sink[dst] = vn;
-    return;
-  }
-  const int slot = c.ring_slot[b];
-  if (slot < 0 || slot >= c.num_ring) {
-    if (t == 0) set_error(a.err, kErrRing);
-    return;
-  }
-  const size_t rdst = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
-  if (p >= kSink + kRecent) {
-    // the token at e = p - 256 leaves the window: same ring row, read before overwrite
-    const int e = p - kRecent;
-    uint8_t* blk = history_block(c, b, h, e, a.err);
-    if (blk != nullptr) {
-      const float xk = bf16_bits_to_float(c.k_ring[rdst]);
-      const float xv = bf16_bits_to_float(c.v_ring[rdst]);
-      quantize_token(xk, a.rot.U_K, a.rot.flags, a.rot.tau_k, blk, e & 63, false, sm);
-      quantize_token(xv, a.rot.U_V, a.rot.flags, a.rot.tau_v, blk, e & 63, true, sm);
-    }
-  }
-  c.k_ring[rdst] = kn;
-  c.v_ring[rdst] = vn;
+// One new token per request.  grid (Hkv, B), 256 threads: threads 0..127
+// handle K, threads 128..255 handle V, each a channel per thread.
+__global__ void __launch_bounds__(256) append_one_kernel(AppendLaunch a) {
+  __shared__ QuantSmem sm[2];
+  griddep_wait();
+  const int half = threadIdx.x >> 7;
+  append_one_body(a, blockIdx.y, blockIdx.x, half, threadIdx.x & 127, a.rot.U_K, a.rot.U_V, sm[half]);
 }
 
 // ------------------------------------------------------------------ multi-token append
@@ -183,9 +59,10 @@ __device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& 
 
 // Phase 1: ring tokens that fall out of the recent window go to the history.
 // grid (256, Hkv, B), 128 threads: one token-head per block.
-__global__ void __launch_bounds__(128) append_evict_kernel(AppendLaunch a) {
-  __shared__ QuantSmem sm;
-  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
+__global__ void __launch_bounds__(256) append_evict_kernel(AppendLaunch a) {
+  __shared__ QuantSmem sm[2];
+  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, half = threadIdx.x >> 7, t = threadIdx.x & 127;
+  const bool is_v = half == 1;
   int p0, n, tok0;
   if (!request_span(a, b, p0, n, tok0)) return;
   const int L = p0 + n;
@@ -195,16 +72,15 @@ __global__ void __launch_bounds__(128) append_evict_kernel(AppendLaunch a) {
   const CacheRefs& c = a.c;
   const int slot = c.ring_slot[b];
   if (slot < 0 || slot >= c.num_ring) {
-    if (t == 0) set_error(a.err, kErrRing);
+    if (threadIdx.x == 0) set_error(a.err, kErrRing);
     return;
   }
   uint8_t* blk = history_block(c, b, h, e, a.err);
   if (blk == nullptr) return;
   const size_t r = (((size_t)slot * c.num_kv_heads + h) * kRecent + ((e - kSink) % kRecent)) * kD + t;
-  const float xk = bf16_bits_to_float(c.k_ring[r]);
-  const float xv = bf16_bits_to_float(c.v_ring[r]);
-  quantize_token(xk, a.rot.U_K, a.rot.flags, a.rot.tau_k, blk, e & 63, false, sm);
-  quantize_token(xv, a.rot.U_V, a.rot.flags, a.rot.tau_v, blk, e & 63, true, sm);
+  const float xv = bf16_bits_to_float((is_v ? c.v_ring : c.k_ring)[r]);
+  quantize_token(xv, is_v ? a.rot.U_V : a.rot.U_K, a.rot.flags, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v,
+                 sm[half]);
 }
 
 // Phase 2a: new tokens that stay BF16 (sink rows, ring rows).
@@ -398,10 +274,10 @@ __global__ void __launch_bounds__(256) append_tile_kernel(AppendLaunch a) {
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   const int B = a.c.batch, Hkv = a.c.num_kv_heads;
   if (a.cu_seqlens == nullptr) {
-    append_one_kernel<<<dim3(Hkv, B), 128, 0, stream>>>(a);
+    append_one_kernel<<<dim3(Hkv, B), 256, 0, stream>>>(a);
     return cudaGetLastError();
   }
-  if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 128, 0, stream>>>(a);
+  if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 256, 0, stream>>>(a);
   append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
   const int tiles = (a.max_tokens_per_req + kPage - 1) / kPage + 1;
   const size_t smem = sizeof(TileSmem);

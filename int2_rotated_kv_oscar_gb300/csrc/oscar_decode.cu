@@ -34,13 +34,13 @@
 
 #include "oscar_device.cuh"
 #include "oscar_internal.h"
+#include "oscar_quant.cuh"
 
 namespace oscar {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kInvSqrtD = 0.08838834764831845f;
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kStages = 3;
 constexpr unsigned kWaitLimit = 1u << 22;
 // The PV B operand is p * s * 2^k (INT2 history, s = V scale) or p * 2^k (BF16
@@ -48,20 +48,27 @@ constexpr unsigned kWaitLimit = 1u << 22;
 // below 60000 for the layer's largest possible scale, so small weights stay
 // clear of the fp16 subnormal range.
 constexpr float kLazy = 4.0f;           // rescale only when the max grows by more than 2^4
-constexpr float kPScaleBF16 = 2048.0f;  // 2^4 * 2048 < 60000
+constexpr float kPScaleBF16 = 2048.0f;  // 2^4 * 2048 < 60000 (log2 = 11)
+constexpr int kMaxChunks = 256;        // work items per (request, KV head)
 
 // Exact fp16 pair of the levels (c - 1.5) of the codes at index r (0..7) of
 // both 16-bit halves of a code word.  One LOP3 puts the code into the low
 // mantissa of the fp16 1024 ((w & mask) | 0x6400: the value 1024 + c 4^r'),
 // one HFMA2 maps it to (1024 + c 4^r') 4^-r' - (1024 4^-r' + 1.5) = c - 1.5.
-// r' is the code's 2-bit position in the source word: index 0 is taken from
-// w << 2 (r' = 1; at r' = 0 the offset 1025.5 would not be an fp16), indices
-// 1..4 from w (r' = r), indices 5..7 from w >> 6 (r' = r - 3).  The levels
-// are normal fp16 numbers: tensor-core products of subnormal operands lose
-// precision.
+// r' is the code's 2-bit position in the source word: indices 1..4 come
+// from w (r' = r); indices 0 and 5..7 from w with the two bytes of each half
+// swapped (r' = 4 and 1..3; at r' = 0 the offset 1025.5 would not be an
+// fp16).  The levels are normal fp16 numbers: tensor-core products of
+// subnormal operands lose precision.
+__device__ __forceinline__ uint32_t swap_half_bytes(uint32_t x) {
+  uint32_t y;
+  asm("prmt.b32 %0, %1, 0, 0x2301;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 struct CodeWord {
-  uint32_t lo2, w, hi6;  // w << 2, w, w >> 6
-  __device__ __forceinline__ explicit CodeWord(uint32_t x) : lo2(x << 2), w(x), hi6(x >> 6) {}
+  uint32_t w, sw;  // w, and w with the bytes of each 16-bit half swapped
+  __device__ __forceinline__ explicit CodeWord(uint32_t x) : w(x), sw(swap_half_bytes(x)) {}
 };
 
 __device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t mask) {
@@ -78,11 +85,11 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
 
 template <int R>
 __device__ __forceinline__ uint32_t code_level(const CodeWord& cw) {
-  constexpr int rp = R == 0 ? 1 : (R < 5 ? R : R - 3);
+  constexpr int rp = R == 0 ? 4 : (R < 5 ? R : R - 4);
   // fp16 constants 4^-r' and -(1024 4^-r' + 1.5) for r' = 1..4, in both halves
   constexpr uint32_t kScale = rp == 1 ? 0x34003400u : rp == 2 ? 0x2C002C00u : rp == 3 ? 0x24002400u : 0x1C001C00u;
   constexpr uint32_t kBias = rp == 1 ? 0xDC06DC06u : rp == 2 ? 0xD418D418u : rp == 3 ? 0xCC60CC60u : 0xC580C580u;
-  const uint32_t src = R == 0 ? cw.lo2 : (R < 5 ? cw.w : cw.hi6);
+  const uint32_t src = (R == 0 || R >= 5) ? cw.sw : cw.w;
   return hfma2_u32(lop_and_or(src, 0x00030003u << (2 * rp)), kScale, kBias);
 }
 
@@ -111,70 +118,75 @@ struct PrepArgs {
 };
 
 // ------------------------------------------------------------------ prep
-// grid (Hkv, B), 128 threads.
+// q' = q R_K for the g query heads of (request b, KV head h), by the 128
+// threads t = 0..127 of a named-barrier group `bar`; U_K may be in shared or
+// global memory.
 //
 // Fragment words per (request, KV head): [32 lanes][32].  The MMA B column of
 // lane L is n = L / 4.  With g <= 4 ("packed"), column n carries head n % 4
 // and part n / 4 (0: fp16 value, 1: fp16 residual) in words 0..15; with
 // g > 4 column n is head n, words 0..15 hold the values and 16..31 the
 // residuals.
-__global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
-  __shared__ float xs[kMaxG][kD];
-  __shared__ float qr[kMaxG][kD];
-  __shared__ float qp[kMaxG][kD];
-  __shared__ float scratch[kD];
-  __shared__ float red[8];
-  const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+struct PrepSmem {
+  float xs[kMaxG][kD];
+  float qr[kMaxG][kD];
+  float qp[kMaxG][kD];
+  float scratch[kD];
+  float red[8];
+};
+
+__device__ void prep_body(const PrepArgs& a, int b, int h, int t, const float* UK, PrepSmem& sm, int bar) {
+  const int lane = t & 31, warp = t >> 5;
   const int g = a.g, bh = b * a.Hkv + h;
   const bool packed = g <= 4;
   if (t == 0) a.counters[bh] = 0;
   const float c = a.sm_scale * kLog2e;
-  for (int n = 0; n < g; ++n) xs[n][t] = bf16_bits_to_float(a.q[((size_t)b * a.Hq + h * g + n) * kD + t]);
-  __syncthreads();
+  for (int n = 0; n < g; ++n) sm.xs[n][t] = bf16_bits_to_float(a.q[((size_t)b * a.Hq + h * g + n) * kD + t]);
+  half_sync(bar);
   float z[kMaxG];
 #pragma unroll
   for (int n = 0; n < kMaxG; ++n) z[n] = 0.f;
-#pragma unroll 4
+#pragma unroll 32
   for (int i = 0; i < kD; ++i) {
-    const float u = __ldg(a.U_K + i * kD + t);
+    const float u = UK[i * kD + t];
 #pragma unroll
     for (int n = 0; n < kMaxG; ++n)
-      if (n < g) z[n] = fmaf(xs[n][i], u, z[n]);
+      if (n < g) z[n] = fmaf(sm.xs[n][i], u, z[n]);
   }
 #pragma unroll
   for (int n = 0; n < kMaxG; ++n) {
     if (n >= g) break;
     float v = z[n];
-    if (a.flags & kRotH) v = fwht128_block(v, scratch) * kInvSqrtD;
-    qr[n][t] = v;
+    if (a.flags & kRotH) v = fwht128_half(v, sm.scratch, t, bar) * kInvSqrtD;
+    sm.qr[n][t] = v;
   }
-  __syncthreads();
+  half_sync(bar);
 #pragma unroll
   for (int n = 0; n < kMaxG; ++n) {
     if (n >= g) break;
-    const float v = (a.flags & kRotP) ? qr[n][brev7(t)] : qr[n][t];
+    const float v = (a.flags & kRotP) ? sm.qr[n][brev7(t)] : sm.qr[n][t];
     z[n] = v * c;
-    qp[n][t] = xs[n][t] * c;
+    sm.qp[n][t] = sm.xs[n][t] * c;
   }
-  __syncthreads();
+  half_sync(bar);
 #pragma unroll
   for (int n = 0; n < kMaxG; ++n)
-    if (n < g) qr[n][t] = z[n];
+    if (n < g) sm.qr[n][t] = z[n];
   // power-of-two normalisations: max |q'| 2^-E <= 2^10, max |q| 2^-Ep <= 2^10
   float mr = 0.f, mp = 0.f;
   for (int n = 0; n < g; ++n) {
-    mr = fmaxf(mr, fabsf(qr[n][t]));
-    mp = fmaxf(mp, fabsf(qp[n][t]));
+    mr = fmaxf(mr, fabsf(sm.qr[n][t]));
+    mp = fmaxf(mp, fabsf(sm.qp[n][t]));
   }
   mr = warp_max(mr);
   mp = warp_max(mp);
   if (lane == 0) {
-    red[warp] = mr;
-    red[4 + warp] = mp;
+    sm.red[warp] = mr;
+    sm.red[4 + warp] = mp;
   }
-  __syncthreads();
-  mr = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  mp = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
+  half_sync(bar);
+  mr = fmaxf(fmaxf(sm.red[0], sm.red[1]), fmaxf(sm.red[2], sm.red[3]));
+  mp = fmaxf(fmaxf(sm.red[4], sm.red[5]), fmaxf(sm.red[6], sm.red[7]));
   int er = 0, ep = 0;
   if (mr > 0.f) {
     frexpf(mr, &er);
@@ -199,9 +211,9 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
     if (head < g && !(packed && set == 1)) {
       const int grp = i >> 2, r = 2 * (i & 3) + bs;
       const int ch = 64 * grp + 16 * tig + r;
-      vr = pack_f16x2(split_part(qr[head][ch] * sr, part), split_part(qr[head][ch + 8] * sr, part));
+      vr = pack_f16x2(split_part(sm.qr[head][ch] * sr, part), split_part(sm.qr[head][ch + 8] * sr, part));
       const int cp = 32 * tig + 4 * i + 2 * bs;
-      vp = pack_f16x2(split_part(qp[head][cp] * sp, part), split_part(qp[head][cp + 1] * sp, part));
+      vp = pack_f16x2(split_part(sm.qp[head][cp] * sp, part), split_part(sm.qp[head][cp + 1] * sp, part));
     }
     qf[e] = vr;
     qpl[e] = vp;
@@ -211,6 +223,51 @@ __global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
     qc[16] = ldexpf(1.f, er);
     qc[17] = ldexpf(1.f, ep);
   }
+}
+
+// grid (Hkv, B), 128 threads
+__global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
+  __shared__ PrepSmem sm;
+  griddep_wait();
+  griddep_launch_dependents();
+  prep_body(a, blockIdx.y, blockIdx.x, threadIdx.x, a.U_K, sm, 1);
+}
+
+// Fused decode step, part 1: the decode append (K and V) and the q rotation
+// of one (KV head, request).  grid (Hkv, B), 384 threads in three roles:
+// 0..127 append K, 128..255 append V, 256..383 rotate q.  U_K and U_V are
+// brought into shared memory by bulk copies while the previous kernel
+// finishes (programmatic dependent launch).
+constexpr size_t kStepSmemBytes = 2 * kD * kD * sizeof(float) + 16;
+
+__global__ void __launch_bounds__(384) step_kernel(AppendLaunch ap, PrepArgs pr) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ QuantSmem qsm[2];
+  __shared__ PrepSmem psm;
+  float* uk = reinterpret_cast<float*>(dsm);
+  float* uv = uk + kD * kD;
+  uint64_t* ubar = reinterpret_cast<uint64_t*>(uv + kD * kD);
+  const int h = blockIdx.x, b = blockIdx.y, role = threadIdx.x >> 7, t = threadIdx.x & 127;
+  if (threadIdx.x == 0) {
+    mbar_init(ubar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(ubar, 2 * kD * kD * 4);
+    bulk_copy_g2s(uk, ap.rot.U_K, kD * kD * 4, ubar);
+    bulk_copy_g2s(uv, ap.rot.U_V, kD * kD * 4, ubar);
+  }
+  griddep_launch_dependents();
+  __syncthreads();
+  griddep_wait();
+  if (!mbar_wait_bounded(ubar, 0, kWaitLimit)) {
+    if (threadIdx.x == 0) set_error(ap.err, kErrTimeout);
+    mbar_wait_bounded(ubar, 0, kWaitLimit);
+    return;
+  }
+  if (role == 2)
+    prep_body(pr, b, h, t, uk, psm, 3);
+  else
+    append_one_body(ap, b, h, role, t, uk, uv, qsm[role]);
 }
 
 // ------------------------------------------------------------------ decode
@@ -294,15 +351,17 @@ __device__ __forceinline__ uint32_t pick_pair(float x0, float x1, bool residual)
 }
 
 // One 64-token INT2 page (K and V codes + scales) staged in shared memory.
-template <bool PACK4>
+// FULL: all 64 rows valid (no masking).  The softmax weights come out scaled
+// by 2^kp (kp = log2 of the B-operand scale), which the caller undoes.
+template <bool PACK4, bool FULL>
 __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n_valid, const uint32_t* qf,
-                                          float scaleE, float pscale, WarpState& st, int lane) {
+                                          float scaleE, float kp, WarpState& st, int lane) {
   const int q = lane >> 2;
   const bool resid = (lane & 3) >= 2;
   float lg[4][4];
 #pragma unroll
   for (int T = 0; T < 4; ++T) {
-    if (16 * T >= n_valid) {
+    if (!FULL && 16 * T >= n_valid) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) lg[T][k] = -INFINITY;
       continue;
@@ -311,10 +370,7 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
     const float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q)));
     const float2 sb =
         half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q + 8)));
-    // Tensor-core f32 accumulation truncates, so each group's four MMAs run as
-    // two zero-started chains that are added in fp32.
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, e0[4] = {0.f, 0.f, 0.f, 0.f};
-    float d1[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #define OSCAR_QK(D, X, Y, R, I)                                                              \
   do {                                                                                      \
     const uint32_t a0 = code_level<R>(X), a1 = code_level<R>(Y), a2 = code_level<R + 1>(X), \
@@ -325,33 +381,40 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
     {
       const CodeWord x(kw.x), y(kw.z);  // group 0: token q, token q+8
       OSCAR_QK(d0, x, y, 0, 0);
-      OSCAR_QK(e0, x, y, 2, 1);
+      OSCAR_QK(d0, x, y, 2, 1);
       OSCAR_QK(d0, x, y, 4, 2);
-      OSCAR_QK(e0, x, y, 6, 3);
+      OSCAR_QK(d0, x, y, 6, 3);
     }
     {
       const CodeWord x(kw.y), y(kw.w);  // group 1
       OSCAR_QK(d1, x, y, 0, 4);
-      OSCAR_QK(e1, x, y, 2, 5);
+      OSCAR_QK(d1, x, y, 2, 5);
       OSCAR_QK(d1, x, y, 4, 6);
-      OSCAR_QK(e1, x, y, 6, 7);
+      OSCAR_QK(d1, x, y, 6, 7);
     }
 #undef OSCAR_QK
-    float l0 = fmaf(d0[0] + e0[0], sa.x, (d1[0] + e1[0]) * sa.y) * scaleE;
-    float l1 = fmaf(d0[1] + e0[1], sa.x, (d1[1] + e1[1]) * sa.y) * scaleE;
-    float l2 = fmaf(d0[2] + e0[2], sb.x, (d1[2] + e1[2]) * sb.y) * scaleE;
-    float l3 = fmaf(d0[3] + e0[3], sb.x, (d1[3] + e1[3]) * sb.y) * scaleE;
+    float l0 = fmaf(d0[0], sa.x, d1[0] * sa.y) * scaleE;
+    float l1 = fmaf(d0[1], sa.x, d1[1] * sa.y) * scaleE;
+    float l2 = fmaf(d0[2], sb.x, d1[2] * sb.y) * scaleE;
+    float l3 = fmaf(d0[3], sb.x, d1[3] * sb.y) * scaleE;
     if (PACK4) {  // value column + residual column
       l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
       l2 += __shfl_xor_sync(0xffffffffu, l2, 2);
       l3 += __shfl_xor_sync(0xffffffffu, l3, 2);
     }
-    const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
-    lg[T][0] = va ? l0 : -INFINITY;
-    lg[T][1] = va ? l1 : -INFINITY;
-    lg[T][2] = vb ? l2 : -INFINITY;
-    lg[T][3] = vb ? l3 : -INFINITY;
+    if (FULL) {
+      lg[T][0] = l0;
+      lg[T][1] = l1;
+      lg[T][2] = l2;
+      lg[T][3] = l3;
+    } else {
+      const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
+      lg[T][0] = va ? l0 : -INFINITY;
+      lg[T][1] = va ? l1 : -INFINITY;
+      lg[T][2] = vb ? l2 : -INFINITY;
+      lg[T][3] = vb ? l3 : -INFINITY;
+    }
   }
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -360,20 +423,23 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
     mx1 = fmaxf(mx1, fmaxf(lg[T][1], lg[T][3]));
   }
   online_max(st, mx0, mx1);
+  const float ms0 = st.m[0] - kp, ms1 = st.m[1] - kp;  // weights p 2^kp
 #pragma unroll
   for (int T = 0; T < 4; ++T) {
-    if (16 * T >= n_valid) continue;
-    const float p0 = ex2(lg[T][0] - st.m[0]), p1 = ex2(lg[T][1] - st.m[1]);
-    const float p2 = ex2(lg[T][2] - st.m[0]), p3 = ex2(lg[T][3] - st.m[1]);
+    if (!FULL && 16 * T >= n_valid) continue;
+    const float p0 = ex2(lg[T][0] - ms0), p1 = ex2(lg[T][1] - ms1);
+    const float p2 = ex2(lg[T][2] - ms0), p3 = ex2(lg[T][3] - ms1);
     st.l[0] += p0 + p2;
     st.l[1] += p1 + p3;
-    const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
     float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
     float2 sb = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q + 8)));
-    sa.x = va ? sa.x * pscale : 0.f;
-    sa.y = va ? sa.y * pscale : 0.f;
-    sb.x = vb ? sb.x * pscale : 0.f;
-    sb.y = vb ? sb.y * pscale : 0.f;
+    if (!FULL) {  // rows past the history end may hold anything
+      const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
+      sa.x = va ? sa.x : 0.f;
+      sa.y = va ? sa.y : 0.f;
+      sb.x = vb ? sb.x : 0.f;
+      sb.y = vb ? sb.y : 0.f;
+    }
     const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVCodes + 512 * T + 16 * lane);
     const CodeWord w0(vw.x), w1(vw.y), w2(vw.z), w3(vw.w);
     if (PACK4) {
@@ -448,16 +514,13 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
     kb[4 * k + 2] = bf16x2_to_f16x2(u.z);
     kb[4 * k + 3] = bf16x2_to_f16x2(u.w);
   }
-  float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    float(&acc)[4] = (ks & 1) ? e : d;  // two chains, added in fp32 (the MMA accumulation truncates)
-    mma_f16(acc, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[2 * ks], qpf[2 * ks + 1]);
-    if (!PACK4)
-      mma_f16(acc, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[16 + 2 * ks], qpf[17 + 2 * ks]);
+    mma_f16(d, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[2 * ks], qpf[2 * ks + 1]);
+    if (!PACK4) mma_f16(d, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[16 + 2 * ks], qpf[17 + 2 * ks]);
   }
-  float l0 = (d[0] + e[0]) * scaleEp, l1 = (d[1] + e[1]) * scaleEp;
-  float l2 = (d[2] + e[2]) * scaleEp, l3 = (d[3] + e[3]) * scaleEp;
+  float l0 = d[0] * scaleEp, l1 = d[1] * scaleEp, l2 = d[2] * scaleEp, l3 = d[3] * scaleEp;
   if (PACK4) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
@@ -469,17 +532,19 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
   l2 = vb ? l2 : -INFINITY;
   l3 = vb ? l3 : -INFINITY;
   online_max(st, fmaxf(l0, l2), fmaxf(l1, l3));
-  const float p0 = ex2(l0 - st.m[0]), p1 = ex2(l1 - st.m[1]), p2 = ex2(l2 - st.m[0]), p3 = ex2(l3 - st.m[1]);
+  // weights scaled by 2^11 (kPScaleBF16) through the exponent
+  const float ms0 = st.m[0] - 11.f, ms1 = st.m[1] - 11.f;
+  const float p0 = ex2(l0 - ms0), p1 = ex2(l1 - ms1), p2 = ex2(l2 - ms0), p3 = ex2(l3 - ms1);
   st.l[0] += p0 + p2;
   st.l[1] += p1 + p3;
   uint32_t b0h, b0l, b1h, b1l;
   if (PACK4) {
-    b0h = movmatrix_trans(pick_pair(p0 * kPScaleBF16, p1 * kPScaleBF16, resid));
-    b1h = movmatrix_trans(pick_pair(p2 * kPScaleBF16, p3 * kPScaleBF16, resid));
+    b0h = movmatrix_trans(pick_pair(p0, p1, resid));
+    b1h = movmatrix_trans(pick_pair(p2, p3, resid));
     b0l = b1l = 0u;
   } else {
-    split_pair(p0 * kPScaleBF16, p1 * kPScaleBF16, b0h, b0l);
-    split_pair(p2 * kPScaleBF16, p3 * kPScaleBF16, b1h, b1l);
+    split_pair(p0, p1, b0h, b0l);
+    split_pair(p2, p3, b1h, b1l);
     b0h = movmatrix_trans(b0h);
     b0l = movmatrix_trans(b0l);
     b1h = movmatrix_trans(b1h);
@@ -502,31 +567,75 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
   }
 }
 
-struct MergeSmem {
-  float m[kWarps][8];
-  float l[kWarps][8];
-  float acc[kWarps][8][kD];
-};
+// A warp's state as written to its own stage memory: m[8], l[8], acc[8][128].
+// inv undoes the B-operand scaling; packed mode adds the residual columns.
+template <bool PACK4>
+__device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv, int lane) {
+  const int q = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
+    st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
+  }
+  const bool writer = PACK4 ? (tig < 2) : true;  // packed: columns 4..7 hold residuals of heads 0..3
+  if (q == 0 && writer) {
+    dst[2 * tig] = st.m[0];
+    dst[2 * tig + 1] = st.m[1];
+    dst[8 + 2 * tig] = st.l[0] * inv;
+    dst[8 + 2 * tig + 1] = st.l[1] * inv;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ch = 16 * mt + q + 8 * (i >> 1), n = 2 * tig + (i & 1);
+      float v = st.acc[mt][i] * inv;
+      if (PACK4) v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (writer) dst[16 + n * kD + ch] = v;
+    }
+  }
+}
+
+// BF16 tile j (0..19) of a (request, KV head): tiles 0..3 are the sink page's
+// rows 16 j .. 16 j + 15, tiles 4..19 rows 16 (j - 4) .. of the 256-row ring.
+__device__ __forceinline__ int bf16_tile_rows(int j, int L, size_t& row_off, bool& ring) {
+  if (j < 4) {
+    ring = false;
+    row_off = 16 * j;
+    return max(0, min(16, min(L, kSink) - 16 * j));
+  }
+  ring = true;
+  const int rr = 16 * (j - 4);
+  row_off = rr;
+  const int live = L >= kSink + kRecent ? kRecent : max(0, L - kSink);
+  return max(0, min(16, live - rr));
+}
 
 template <int MODE, bool PACK4>
-__global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, q = lane >> 2, tig = lane & 3;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int bh = b * a.Hkv + h;
   const CacheRefs& c = a.c;
+  griddep_wait();
+  if (MODE == 0 && item == 0)  // the last block of this (request, KV head) reads U_V^T
+    for (int i = t; i < kD * kD / 32; i += 256) prefetch_l2(a.U_VT + 32 * i);
   int L = a.ctx_len[b];
   if (L < 0) {
     if (t == 0 && item == 0) set_error(a.err, kErrLength);
     L = 0;
   }
-  WarpState st;
-  state_init(st);
-  const bool rotated = (MODE == 0) && item < a.n_chunks;
   constexpr int kQW = PACK4 ? 16 : 32;
+  // warp-private stage memory; after the warp's pages are done it holds the
+  // warp's two finished states (rotated basis, original basis)
+  uint8_t* stages = smem + (size_t)warp * kStages * kBlockBytes;
+  float* wstate = reinterpret_cast<float*>(stages);
+  WarpState st;
 
-  if (rotated) {
-    // ---------------- INT2 history pages
+  if (MODE == 0) {
+    // ---------------- INT2 history pages of this chunk (rotated basis)
+    state_init(st);
     const int hist_end = max(kSink, L - kRecent);
     const int n_hist = (hist_end + kPage - 1) / kPage - 1;  // logical pages 1..n_hist
     if (n_hist + 1 > c.max_pages) {
@@ -551,7 +660,7 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
         }
       }
       const float scaleE = __ldg(a.qconst + (size_t)bh * kQConstFloats + 16);
-      uint8_t* stages = smem + (size_t)warp * kStages * kBlockBytes;
+      const float kp = log2f(a.pscale);
       uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + warp * kStages;
       const uint8_t* pool = c.pages;
       auto phys_of = [&](int k) -> int {
@@ -590,7 +699,10 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
         const int lp = first + kWarps * k;
         if (phys_of(k) >= 0) {
           const int n_valid = min(kPage, hist_end - kPage * lp);
-          int2_page<PACK4>(stages + (size_t)s * kBlockBytes, n_valid, qf, scaleE, a.pscale, st, lane);
+          if (n_valid == kPage)
+            int2_page<PACK4, true>(stages + (size_t)s * kBlockBytes, n_valid, qf, scaleE, kp, st, lane);
+          else
+            int2_page<PACK4, false>(stages + (size_t)s * kBlockBytes, n_valid, qf, scaleE, kp, st, lane);
         }
         __syncwarp();
         if (lane == 0 && k + kStages < n_my) {
@@ -602,9 +714,17 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
       for (int kk = k + 1; kk < min(k + kStages, n_my); ++kk)
         mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, kWaitLimit);
       if (k < n_my) mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1, kWaitLimit);
+      __syncwarp();
     }
+    store_state<PACK4>(st, wstate, a.inv_pscale, lane);
   } else {
-    // ---------------- BF16 tiles (original basis)
+    state_init(st);
+    store_state<PACK4>(st, wstate, 1.f, lane);
+  }
+
+  // ---------------- BF16 tiles (original basis)
+  state_init(st);
+  {
     uint32_t qpf[kQW];
     {
       const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
@@ -619,110 +739,80 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
     }
     const float scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
     if (MODE == 0) {
-      const int kb = item - a.n_chunks;  // 0: sink, 1..4: ring quarters
-      const uint16_t *Kb = nullptr, *Vb = nullptr;
-      int valid = 0;
-      if (kb == 0) {
-        valid = min(L, kSink);
-        if (valid > 0) {
-          const int sp = c.sink_page[b];
-          if (sp < 0 || sp >= c.num_sink) {
-            if (t == 0) set_error(a.err, kErrSink);
-            valid = 0;
-          } else {
-            const size_t off = ((size_t)sp * a.Hkv + h) * kSink * kD;
-            Kb = c.k_sink + off;
-            Vb = c.v_sink + off;
-          }
+      // this item's tiles: j = item, item + n_items, ...; warp w takes the w-th, (w+8)-th, ...
+      const int sp = c.sink_page[b], slot = c.ring_slot[b];
+      const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
+      for (int i = warp;; i += kWarps) {
+        const int j = item + a.n_items * i;
+        if (j >= 20) break;
+        size_t row_off;
+        bool ring;
+        const int nv = bf16_tile_rows(j, L, row_off, ring);
+        if (nv <= 0) continue;
+        if (ring ? !ring_ok : !sink_ok) {
+          if (lane == 0) set_error(a.err, ring ? kErrRing : kErrSink);
+          continue;
         }
-      } else {
-        const int q4 = kb - 1;
-        valid = L >= kSink + kRecent ? kPage : max(0, min(kPage, L - kSink - kPage * q4));
-        if (valid > 0) {
-          const int slot = c.ring_slot[b];
-          if (slot < 0 || slot >= c.num_ring) {
-            if (t == 0) set_error(a.err, kErrRing);
-            valid = 0;
-          } else {
-            const size_t off = (((size_t)slot * a.Hkv + h) * kRecent + kPage * q4) * kD;
-            Kb = c.k_ring + off;
-            Vb = c.v_ring + off;
-          }
-        }
+        const size_t off = ring ? ((((size_t)slot * a.Hkv + h) * kRecent + row_off) * kD)
+                                : ((((size_t)sp * a.Hkv + h) * kSink + row_off) * kD);
+        bf16_tile<PACK4>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, nv, qpf, scaleEp, st,
+                         lane);
       }
-      const int nv = min(16, valid - 16 * warp);
-      if (nv > 0) bf16_tile<PACK4>(Kb + 16 * warp * kD, Vb + 16 * warp * kD, nv, qpf, scaleEp, st, lane);
     } else {
-      // plain BF16 paged cache: item covers pages [item*C, item*C + C); warp w takes tile w of each
+      // plain BF16 paged cache: item covers pages [item*C, item*C + C), 4 tiles each
       const int n_pages = (L + kPage - 1) / kPage;
       if (n_pages > c.max_pages) {
         if (t == 0 && item == 0) set_error(a.err, kErrLength);
       }
       const int pg0 = item * a.chunk_pages;
       const int pg1 = min(min(pg0 + a.chunk_pages, n_pages), c.max_pages);
-      for (int pg = pg0; pg < pg1; ++pg) {
+      for (int i = warp; pg0 + i / 4 < pg1; i += kWarps) {
+        const int pg = pg0 + i / 4, tile = i & 3;
         const int ph = c.page_table[(size_t)b * c.max_pages + pg];
         if (ph < 0 || ph >= c.num_pages) {
           if (lane == 0) set_error(a.err, kErrPage);
           continue;
         }
-        const int nv = min(16, L - kPage * pg - 16 * warp);
+        const int nv = min(16, L - kPage * pg - 16 * tile);
         if (nv <= 0) continue;
-        const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * warp) * kD;
+        const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
         bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, nv, qpf, scaleEp, st, lane);
       }
     }
   }
-
-  // ---------------- finalise each warp's state and merge the warps
-  __syncthreads();  // stage memory is reused below
-  MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
-    st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
-  }
-  // packed mode: columns 4..7 hold the residual parts of heads 0..3
-  const bool writer = PACK4 ? (tig < 2) : true;
-  if (q == 0 && writer) {
-    ms.m[warp][2 * tig] = st.m[0];
-    ms.m[warp][2 * tig + 1] = st.m[1];
-    ms.l[warp][2 * tig] = st.l[0];
-    ms.l[warp][2 * tig + 1] = st.l[1];
-  }
-  const float inv = rotated ? a.inv_pscale : 1.0f / kPScaleBF16;
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int ch = 16 * mt + q + 8 * (i >> 1), n = 2 * tig + (i & 1);
-      float v = st.acc[mt][i] * inv;
-      if (PACK4) v += __shfl_xor_sync(0xffffffffu, v, 2);
-      if (writer) ms.acc[warp][n][ch] = v;
-    }
-  }
+  store_state<PACK4>(st, wstate + kPartialFloats, 1.0f / kPScaleBF16, lane);
+  griddep_launch_dependents();  // a dependent step kernel may start loading its constants
   __syncthreads();
-  float* part = a.partials + ((size_t)bh * a.n_items + item) * kPartialFloats;
-  for (int n = 0; n < a.g; ++n) {
-    float M = -INFINITY;
+
+  // ---------------- merge the 8 warps' states into this item's two partial records
+  {
+    const int kind = t >> 7, ch = t & 127;
+    float* part = a.partials + (((size_t)bh * a.n_items + item) * 2 + kind) * kPartialFloats;
+    const size_t wstride = (size_t)kStages * kBlockBytes / sizeof(float);
+    const float* base = reinterpret_cast<const float*>(smem) + kind * kPartialFloats;
+    for (int n = 0; n < a.g; ++n) {
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ms.m[w][n]);
-    float acc = 0.f, l = 0.f;
-    if (M != -INFINITY) {
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, base[w * wstride + n]);
+      float acc = 0.f, l = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = ms.m[w][n];
-        const float al = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        acc = fmaf(al, ms.acc[w][n][t], acc);
-        l = fmaf(al, ms.l[w][n], l);
+        for (int w = 0; w < kWarps; ++w) {
+          const float* ws = base + w * wstride;
+          const float mw = ws[n];
+          const float al = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          acc = fmaf(al, ws[16 + n * kD + ch], acc);
+          l = fmaf(al, ws[8 + n], l);
+        }
+      }
+      part[16 + n * kD + ch] = acc;
+      if (ch == 0) {
+        part[n] = M;
+        part[8 + n] = l;
       }
     }
-    part[16 + n * kD + t] = acc;
-    if (t == 0) {
-      part[n] = M;
-      part[8 + n] = l;
-    }
   }
+
   // ---------------- last block of this (request, KV head) merges all partials
   __shared__ int s_last;
   __syncthreads();
@@ -734,80 +824,141 @@ __global__ void __launch_bounds__(128, 4) decode_kernel(DecodeArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  float Mr[kMaxG], Lr[kMaxG], Ar[kMaxG], Mp[kMaxG], Lp[kMaxG], Ap[kMaxG];
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n) {
-    Mr[n] = Mp[n] = -INFINITY;
-    Lr[n] = Lp[n] = Ar[n] = Ap[n] = 0.f;
+  const int X = a.n_items, g = a.g;
+  const float* recs = a.partials + (size_t)bh * X * 2 * kPartialFloats;
+  float* uvt = reinterpret_cast<float*>(smem);  // [128][128] U_V^T (rotated-basis part only)
+  float* ml = uvt + kD * kD;                     // [X][2][16] m, l of every partial; m becomes its weight
+  float* stat = ml + X * 32;                     // [2][8][2] per basis and head: M, sum of weighted l
+  float* ys = stat + 32;                         // [8][128]
+  uint64_t* ubar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + kWarps * kStages;
+  if (MODE == 0 && t == 0) {
+    mbar_init(ubar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(ubar, kD * kD * 4);
+    bulk_copy_g2s(uvt, a.U_VT, kD * kD * 4, ubar);
   }
-  for (int x = 0; x < a.n_items; ++x) {
-    const float* rec = a.partials + ((size_t)bh * a.n_items + x) * kPartialFloats;
-    const bool rot = (MODE == 0) && x < a.n_chunks;
+  for (int i = t; i < X * 32; i += 256) ml[i] = __ldcg(recs + (size_t)(i >> 4) * kPartialFloats + (i & 15));
+  __syncthreads();
+  for (int pair = warp; pair < 2 * kMaxG; pair += kWarps) {  // one warp per (basis, head)
+    const int kind = pair >> 3, n = pair & 7;
+    if (n >= g) continue;
+    float M = -INFINITY;
+    for (int x = lane; x < X; x += 32) M = fmaxf(M, ml[x * 32 + kind * 16 + n]);
+    M = warp_max(M);
+    float Ls = 0.f;
+    for (int x = lane; x < X; x += 32) {
+      const float m = ml[x * 32 + kind * 16 + n];
+      const float wx = (m == -INFINITY) ? 0.f : ex2(m - M);
+      ml[x * 32 + kind * 16 + n] = wx;
+      Ls = fmaf(wx, ml[x * 32 + kind * 16 + 8 + n], Ls);
+    }
+    Ls = warp_sum(Ls);
+    if (lane == 0) {
+      stat[(kind * 8 + n) * 2] = M;
+      stat[(kind * 8 + n) * 2 + 1] = Ls;
+    }
+  }
+  __syncthreads();
+  if (warp < g) {
+    // warp n: head n; lane: channels 4 lane .. 4 lane + 3
+    const int n = warp;
+    float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
+#pragma unroll 8
+    for (int x = 0; x < X; ++x) {
+      const float* rec = recs + (size_t)x * 2 * kPartialFloats + 16 + n * kD + 4 * lane;
+      const float wr = ml[x * 32 + n], wp = ml[x * 32 + 16 + n];
+      if (MODE == 0) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(rec));
+        ar.x = fmaf(wr, v.x, ar.x);
+        ar.y = fmaf(wr, v.y, ar.y);
+        ar.z = fmaf(wr, v.z, ar.z);
+        ar.w = fmaf(wr, v.w, ar.w);
+      }
+      const float4 u = __ldcg(reinterpret_cast<const float4*>(rec + kPartialFloats));
+      ap.x = fmaf(wp, u.x, ap.x);
+      ap.y = fmaf(wp, u.y, ap.y);
+      ap.z = fmaf(wp, u.z, ap.z);
+      ap.w = fmaf(wp, u.w, ap.w);
+    }
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    if (MODE == 0) {
+      // rotate back: y = acc P, y = y H / sqrt(d), out = y U_V^T
+      float* y = ys + n * kD;
+      float v[4] = {ar.x, ar.y, ar.z, ar.w};
+      if (a.flags & kRotP) {
 #pragma unroll
-    for (int n = 0; n < kMaxG; ++n) {
-      if (n >= a.g) break;
-      const float m = __ldcg(rec + n);
-      if (m == -INFINITY) continue;
-      const float l = __ldcg(rec + 8 + n), v = __ldcg(rec + 16 + n * kD + t);
-      if (rot) {
-        const float Mn = fmaxf(Mr[n], m);
-        const float a0 = (Mr[n] == -INFINITY) ? 0.f : ex2(Mr[n] - Mn), a1 = ex2(m - Mn);
-        Ar[n] = Ar[n] * a0 + v * a1;
-        Lr[n] = Lr[n] * a0 + l * a1;
-        Mr[n] = Mn;
-      } else {
-        const float Mn = fmaxf(Mp[n], m);
-        const float a0 = (Mp[n] == -INFINITY) ? 0.f : ex2(Mp[n] - Mn), a1 = ex2(m - Mn);
-        Ap[n] = Ap[n] * a0 + v * a1;
-        Lp[n] = Lp[n] * a0 + l * a1;
-        Mp[n] = Mn;
+        for (int k = 0; k < 4; ++k) y[4 * lane + k] = v[k];
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = y[brev7(4 * lane + k)];
+        __syncwarp();
+      }
+      if (a.flags & kRotH) {
+        const float t0 = v[0] + v[1], t1 = v[0] - v[1], t2 = v[2] + v[3], t3 = v[2] - v[3];
+        v[0] = t0 + t2;
+        v[1] = t1 + t3;
+        v[2] = t0 - t2;
+        v[3] = t1 - t3;
+#pragma unroll
+        for (int bb = 0; bb < 5; ++bb) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float oth = __shfl_xor_sync(0xffffffffu, v[k], 1 << bb);
+            v[k] = ((lane >> bb) & 1) ? (oth - v[k]) : (v[k] + oth);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[4 * lane + k] = v[k];
+      __syncwarp();
+      const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(ubar, 0, kWaitLimit));
+      if (!got) {
+        if (lane == 0) set_error(a.err, kErrTimeout);
+        mbar_wait_bounded(ubar, 0, kWaitLimit);
+      }
+#pragma unroll 8
+      for (int j = 0; j < kD; ++j) {
+        const float yj = y[j];
+        const float4 u = *reinterpret_cast<const float4*>(uvt + j * kD + 4 * lane);
+        o[0] = fmaf(yj, u.x, o[0]);
+        o[1] = fmaf(yj, u.y, o[1]);
+        o[2] = fmaf(yj, u.z, o[2]);
+        o[3] = fmaf(yj, u.w, o[3]);
       }
     }
-  }
-  float Or[kMaxG];
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n) Or[n] = 0.f;
-  if (MODE == 0) {
-    // rotate the INT2 part back: y = acc P, y = y H / sqrt(d), out = y U_V^T
-    float* ys = reinterpret_cast<float*>(smem);  // [8][128]
-    float* scratch = ys + kMaxG * kD;
-#pragma unroll
-    for (int n = 0; n < kMaxG; ++n)
-      if (n < a.g) ys[n * kD + t] = Ar[n];
-    __syncthreads();
-    for (int n = 0; n < a.g; ++n) {
-      float v = (a.flags & kRotP) ? ys[n * kD + brev7(t)] : ys[n * kD + t];
-      if (a.flags & kRotH) v = fwht128_block(v, scratch) * kInvSqrtD;
-      __syncthreads();
-      ys[n * kD + t] = v;
-      __syncthreads();
-    }
-#pragma unroll 4
-    for (int j = 0; j < kD; ++j) {
-      const float u = __ldg(a.U_VT + j * kD + t);
-#pragma unroll
-      for (int n = 0; n < kMaxG; ++n)
-        if (n < a.g) Or[n] = fmaf(ys[n * kD + j], u, Or[n]);
-    }
-  }
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n) {
-    if (n >= a.g) break;
-    const float M = fmaxf(Mr[n], Mp[n]);
-    float o = 0.f;
+    const float Mr = stat[n * 2], Lr = stat[n * 2 + 1];
+    const float Mp = stat[(8 + n) * 2], Lp = stat[(8 + n) * 2 + 1];
+    const float M = fmaxf(Mr, Mp);
+    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      const float ar = (Mr[n] == -INFINITY) ? 0.f : ex2(Mr[n] - M);
-      const float ap = (Mp[n] == -INFINITY) ? 0.f : ex2(Mp[n] - M);
-      const float l = ar * Lr[n] + ap * Lp[n];
-      o = (ar * Or[n] + ap * Ap[n]) / l;
+      const float fr = (Mr == -INFINITY) ? 0.f : ex2(Mr - M);
+      const float fp = (Mp == -INFINITY) ? 0.f : ex2(Mp - M);
+      const float inv_l = 1.0f / (fr * Lr + fp * Lp);
+      res.x = (fr * o[0] + fp * ap.x) * inv_l;
+      res.y = (fr * o[1] + fp * ap.y) * inv_l;
+      res.z = (fr * o[2] + fp * ap.z) * inv_l;
+      res.w = (fr * o[3] + fp * ap.w) * inv_l;
     }
-    a.out[((size_t)b * a.Hq + h * a.g + n) * kD + t] = o;
+    *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + h * a.g + n) * kD + 4 * lane) = res;
+  } else if (MODE == 0 && warp == kWarps - 1 && g < kWarps) {
+    // make sure the U_V^T copy has landed before the block exits even if no warp waited
+  }
+  if (MODE == 0) {
+    __syncthreads();
+    if (t == 0) mbar_wait_bounded(ubar, 0, kWaitLimit);
   }
 }
 
 constexpr size_t decode_smem_bytes() {
-  return (size_t)kWarps * kStages * kBlockBytes + (size_t)kWarps * kStages * sizeof(uint64_t);
+  return (size_t)kWarps * kStages * kBlockBytes + (size_t)(kWarps * kStages + 1) * sizeof(uint64_t);
 }
+// two finished warp states fit in a warp's stage memory; the last block's
+// merge (U_V^T, staged m/l, stats, rotation scratch) fits in all of it
+static_assert(2 * kPartialFloats * 4 <= kStages * kBlockBytes, "warp states");
+static_assert((kD * kD + kMaxChunks * 32 + 32 + kMaxG * kD) * 4 <= kWarps * kStages * kBlockBytes, "merge staging");
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -827,15 +978,16 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
     pages = (max_ctx_len + kPage - 1) / kPage;
   }
   if (pages < 0) pages = 0;
+  // one balanced wave of blocks (2 per SM) when the work is small, <= 64 pages per block otherwise
   const long long total = (long long)batch * Hkv * pages;
-  const long long target = 6LL * (num_sms > 0 ? num_sms : 148);
-  long long C = (total + target - 1) / target;
-  const int cmin = mode == 0 ? 4 : 1;
-  if (C < cmin) C = cmin;
+  const long long slots = 2LL * (num_sms > 0 ? num_sms : 148);
+  long long C = (total + slots - 1) / slots;
+  if (C < 2) C = 2;
   if (C > 64) C = 64;
+  if (pages > C * kMaxChunks) C = (pages + kMaxChunks - 1) / kMaxChunks;
   p.chunk_pages = (int)C;
   p.n_chunks = pages > 0 ? (int)((pages + C - 1) / C) : 0;
-  p.n_items = mode == 0 ? p.n_chunks + 5 : (p.n_chunks > 0 ? p.n_chunks : 1);
+  p.n_items = p.n_chunks > 0 ? p.n_chunks : 1;
   const size_t bh = (size_t)batch * Hkv;
   size_t off = 0;
   p.off_counters = off;
@@ -847,14 +999,29 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   p.off_qconst = off;
   off = align256(off + bh * kQConstFloats * sizeof(float));
   p.off_partials = off;
-  off = align256(off + bh * (size_t)p.n_items * kPartialFloats * sizeof(float));
+  off = align256(off + bh * (size_t)p.n_items * 2 * kPartialFloats * sizeof(float));
   p.total = off;
   return p;
 }
 
-cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+PrepArgs prep_args_of(const DecodeLaunch& d) {
   const DecodePlan& p = d.plan;
-  if (p.batch == 0) return cudaSuccess;
   uint8_t* ws = d.workspace;
   PrepArgs pa;
   pa.q = d.q;
@@ -868,10 +1035,13 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
   pa.qplain = reinterpret_cast<uint32_t*>(ws + p.off_qplain);
   pa.qconst = reinterpret_cast<float*>(ws + p.off_qconst);
   pa.counters = reinterpret_cast<int*>(ws + p.off_counters);
-  prep_kernel<<<dim3(p.Hkv, p.batch), 128, 0, stream>>>(pa);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return pa;
+}
 
+// the split-K decode kernel (after its prep has been queued)
+cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cudaStream_t stream) {
+  const DecodePlan& p = d.plan;
+  uint8_t* ws = d.workspace;
   DecodeArgs a;
   a.mode = d.mode;
   a.c = d.c;
@@ -909,12 +1079,44 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
   static bool attr_done[4] = {false, false, false, false};
   const int which = 2 * d.mode + (pack4 ? 1 : 0);
   if (!attr_done[which]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done[which] = true;
   }
-  kern<<<grid, 128, smem, stream>>>(a);
-  return cudaGetLastError();
+  void* args[] = {&a};
+  return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(256), smem, stream, args);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
+  const DecodePlan& p = d.plan;
+  if (p.batch == 0) return cudaSuccess;
+  PrepArgs pa = prep_args_of(d);
+  void* args[] = {&pa};
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(prep_kernel), dim3(p.Hkv, p.batch), dim3(128), 0, stream,
+                             args);
+  if (e != cudaSuccess) return e;
+  return launch_decode_kernel(d, pa, stream);
+}
+
+cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cudaStream_t stream) {
+  const DecodePlan& p = d.plan;
+  if (p.batch == 0) return cudaSuccess;
+  PrepArgs pa = prep_args_of(d);
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStepSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  AppendLaunch apc = ap;
+  void* args[] = {&apc, &pa};
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(step_kernel), dim3(p.Hkv, p.batch), dim3(384),
+                             kStepSmemBytes, stream, args);
+  if (e != cudaSuccess) return e;
+  return launch_decode_kernel(d, pa, stream);
 }
 
 }  // namespace oscar

@@ -156,4 +156,37 @@ __device__ __forceinline__ float fwht128_block(float v, float* scratch) {
   return v;
 }
 
+// Programmatic dependent launch: wait for the grids this one depends on (no-op
+// when launched without the attribute) / let dependent grids start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
+// Barrier over the 128 threads [128 * (id - 1), 128 * id) of the block (id >= 1).
+__device__ __forceinline__ void half_sync(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
+
+// fwht128_block for one 128-thread half of a larger block, synchronised by
+// named barrier `bar_id`; thread index within the half is t.
+__device__ __forceinline__ float fwht128_half(float v, float* scratch, int t, int bar_id) {
+#pragma unroll
+  for (int b = 0; b < 5; ++b) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, 1 << b);
+    v = ((t >> b) & 1) ? (o - v) : (v + o);
+  }
+#pragma unroll
+  for (int b = 5; b < 7; ++b) {
+    scratch[t] = v;
+    half_sync(bar_id);
+    const float o = scratch[t ^ (1 << b)];
+    half_sync(bar_id);
+    v = ((t >> b) & 1) ? (o - v) : (v + o);
+  }
+  return v;
+}
+
 }  // namespace oscar

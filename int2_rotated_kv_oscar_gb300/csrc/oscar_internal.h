@@ -81,4 +81,7 @@ struct DecodeLaunch {
 
 cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream);
 
+// fused: decode append (one token per request) + q rotation, then the decode kernel
+cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cudaStream_t stream);
+
 }  // namespace oscar

@@ -1,0 +1,151 @@
+// Rotate + clip + quantise one token into a packed INT2 block (device code
+// shared by the append kernels and the fused decode-step kernel).
+//
+// ainsights.it "OSCAR: Come Together AI Comprime la KV Cache a 2-bit per LLM",
+// "Architettura del Sistema di Serving e Layout di Memoria": each token is
+// rotated, clipped and quantised on its way into the INT2 history.
+// gist.science "Resumen Técnico: OSCAR ...", §2.2 A.3-4: R = U H_Had P_br and
+// per-layer clip thresholds.
+#pragma once
+
+#include "oscar_device.cuh"
+#include "oscar_internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)
+
+// Byte offset inside a block's K code area of the 32-bit word holding the
+// codes of (row t, quarter tig, group grp).
+__device__ __forceinline__ int k_word_offset(int t, int tig, int grp) {
+  const int T = t >> 4, u = t & 15;
+  return 512 * T + 16 * (4 * (u & 7) + tig) + 4 * (2 * (u >> 3) + grp);
+}
+
+// Byte offset inside a block's V code area of the 16-bit half holding the
+// codes of row t for the channels {jj + 16 r : r = 0..7}.
+__device__ __forceinline__ int v_half_offset(int t, int jj) {
+  const int T = t >> 4, u = t & 15;
+  return 512 * T + 16 * (4 * (jj & 7) + ((u & 7) >> 1)) + 4 * (2 * (u >> 3) + (jj >> 3)) + 2 * (u & 1);
+}
+
+struct QuantSmem {
+  float x[kD];
+  float scratch[kD];
+  float red[4];
+  uint8_t code[kD];
+};
+
+// Rotate + clip + quantise one token held one channel per thread by one
+// 128-thread half of the block (half 0: K, half 1: V, synchronised by named
+// barrier 1 + half) and store its codes and scale in row `row` of the K or V
+// part of `block`.  All 128 threads of the half must call it.
+__device__ void quantize_token(float x, const float* __restrict__ U, unsigned flags, float tau, uint8_t* block,
+                               int row, bool is_v, QuantSmem& sm) {
+  const int t = threadIdx.x & 127, lane = t & 31, warp = t >> 5, bar = 1 + (threadIdx.x >> 7);
+  sm.x[t] = x;
+  half_sync(bar);
+  float z = 0.f;
+#pragma unroll 32
+  for (int i = 0; i < kD; ++i) z = fmaf(sm.x[i], U[i * kD + t], z);
+  if (flags & kRotH) z = fwht128_half(z, sm.scratch, t, bar) * kInvSqrtD;
+  if (flags & kRotP) {
+    half_sync(bar);
+    sm.scratch[t] = z;
+    half_sync(bar);
+    z = sm.scratch[brev7(t)];
+  }
+  const float amax = warp_max(fabsf(z));
+  if (lane == 0) sm.red[warp] = amax;
+  half_sync(bar);
+  const int grp = t >> 6;
+  const float a = fminf(fmaxf(sm.red[2 * grp], sm.red[2 * grp + 1]), tau);
+  const __half sh = __float2half_rn(a / 1.5f);
+  const float s = __half2float(sh);
+  sm.code[t] = (uint8_t)((z >= -s) + (z >= 0.f) + (z >= s));
+  half_sync(bar);
+  if (!is_v) {
+    if (t < 8) {
+      const int tig = t & 3, g = t >> 2, base = 64 * g + 16 * tig;
+      uint32_t w = 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        w |= (uint32_t)sm.code[base + r] << (2 * r);
+        w |= (uint32_t)sm.code[base + 8 + r] << (16 + 2 * r);
+      }
+      *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, tig, g)) = w;
+    }
+  } else {
+    if (t < 16) {
+      uint32_t hv = 0;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[t + 16 * r] << (2 * r);
+      *reinterpret_cast<uint16_t*>(block + kVCodes + v_half_offset(row, t)) = (uint16_t)hv;
+    }
+  }
+  if ((t & 63) == 0)
+    *reinterpret_cast<__half*>(block + (is_v ? kVScales : kKScales) + 4 * row + 2 * grp) = sh;
+  half_sync(bar);
+}
+
+// Locate (and check) the INT2 block of position e of request b, head h.
+__device__ __forceinline__ uint8_t* history_block(const CacheRefs& c, int b, int h, int e, unsigned* err) {
+  const int lp = e >> 6;
+  if (lp >= c.max_pages) {
+    if (threadIdx.x == 0) set_error(err, kErrLength);
+    return nullptr;
+  }
+  const int phys = c.page_table[(size_t)b * c.max_pages + lp];
+  if (phys < 0 || phys >= c.num_pages) {
+    if (threadIdx.x == 0) set_error(err, kErrPage);
+    return nullptr;
+  }
+  return c.pages + ((size_t)phys * c.num_kv_heads + h) * kBlockBytes;
+}
+
+// Decode append of request b, KV head h: K (half 0) or V (half 1), one
+// channel per thread t of the 128-thread half.  Writes the token into the
+// sink page (position < 64) or its ring row; a position >= 320 first moves
+// the ring row's old token (position - 256) into its INT2 history row.
+__device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, int h, int half, int t,
+                                                const float* Uk, const float* Uv, QuantSmem& sm) {
+  const bool is_v = half == 1;
+  const CacheRefs& c = a.c;
+  const int Hkv = c.num_kv_heads;
+  const int p = a.pos[b];
+  const uint16_t xn = (is_v ? a.v : a.k)[((size_t)b * Hkv + h) * kD + t];
+  if (p < 0 || ((a.flags & 1u) && p > kSink)) {
+    if (threadIdx.x == 0) set_error(a.err, kErrLength);
+    return;
+  }
+  if (p < kSink) {
+    const int sp = c.sink_page[b];
+    if (sp < 0 || sp >= c.num_sink) {
+      if (threadIdx.x == 0) set_error(a.err, kErrSink);
+      return;
+    }
+    (is_v ? c.v_sink : c.k_sink)[(((size_t)sp * Hkv + h) * kSink + p) * kD + t] = xn;
+    return;
+  }
+  const int slot = c.ring_slot[b];
+  if (slot < 0 || slot >= c.num_ring) {
+    if (threadIdx.x == 0) set_error(a.err, kErrRing);
+    return;
+  }
+  uint16_t* ring = is_v ? c.v_ring : c.k_ring;
+  const size_t rdst = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
+  if (p >= kSink + kRecent) {
+    // the token at e = p - 256 leaves the window: same ring row, read before overwrite
+    const int e = p - kRecent;
+    uint8_t* blk = history_block(c, b, h, e, a.err);
+    if (blk != nullptr) {
+      const float x = bf16_bits_to_float(ring[rdst]);
+      quantize_token(x, is_v ? Uv : Uk, a.rot.flags, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm);
+    }
+  }
+  ring[rdst] = xn;
+}
+
+}  // namespace
+}  // namespace oscar
