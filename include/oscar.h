@@ -213,7 +213,10 @@ void oscar_destroy(oscar_ctx* ctx);
  * ([ES] §2.2 A.4).  U_K, U_V: host fp32 [128][128] row-major, columns are
  * the eigenvectors (a token row x is rotated as x' = x R).  They must be
  * orthogonal; the library does not check.  tau > 0, finite or +inf, and
- * tau / 1.5 must fit fp16 (tau <= 98256).  Synchronous (copies before return).
+ * tau / 1.5 must fit fp16 (tau <= 98256).  The library forms the composite
+ * R = U H P of the enabled factors (flags) in double precision and keeps R_K,
+ * R_V and R_V^T in fp32 on the device; every kernel applies the rotation as
+ * one dense product with R.  Synchronous (copies before return).
  */
 oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K, const float* U_V,
                                  float tau_k, float tau_v, uint32_t flags);
@@ -225,9 +228,8 @@ oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K
  * the 256-token window into their INT2 rows; phase 2 writes each new token:
  * positions < 64 to the sink page, positions >= L - 256 (L = final length) to
  * the ring, the rest straight into INT2 rows.  Rotation: x' = x R in fp32
- * (x U, then an in-register Walsh-Hadamard butterfly, then the bit-reversal
- * permutation), clip a = min(max|x'|, tau) per group of 64, s = fp16(a / 1.5),
- * code = [x' >= -s] + [x' >= 0] + [x' >= s].
+ * with the layer's composite R, clip a = min(max|x'|, tau) per group of 64,
+ * s = fp16(a / 1.5), code = [x' >= -s] + [x' >= 0] + [x' >= s].
  */
 oscar_status oscar_kv_append(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
                              const oscar_append_args* args, void* stream);

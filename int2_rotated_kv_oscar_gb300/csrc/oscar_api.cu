@@ -17,9 +17,8 @@ struct oscar_ctx {
   oscar_config cfg;
   int num_sms = 0;
   unsigned* d_err = nullptr;
-  std::vector<float*> d_rot;       // per layer: U_K | U_V | U_V^T, 3 * 128 * 128 floats
+  std::vector<float*> d_rot;       // per layer: R_K | R_V | R_V^T, 3 * 128 * 128 floats
   std::vector<float> tau_k, tau_v;
-  std::vector<unsigned> flags;
   std::vector<bool> loaded;
 };
 
@@ -67,13 +66,39 @@ CacheRefs refs_of(const oscar_ctx* ctx, const oscar_cache_view* v) {
 LayerRotation rotation_of(const oscar_ctx* ctx, int layer) {
   LayerRotation r;
   const float* base = ctx->d_rot[layer];
-  r.U_K = base;
-  r.U_V = base + 128 * 128;
-  r.U_VT = base + 2 * 128 * 128;
+  r.R_K = base;
+  r.R_V = base + 128 * 128;
+  r.R_VT = base + 2 * 128 * 128;
   r.tau_k = ctx->tau_k[layer];
   r.tau_v = ctx->tau_v[layer];
-  r.flags = ctx->flags[layer];
   return r;
+}
+
+// R = U H P in double precision (gist.science "Resumen Técnico: OSCAR ...",
+// §2.2 A.3): U the calibrated basis (identity without OSCAR_ROT_U), H the
+// 128-point Sylvester Hadamard matrix scaled by 1/sqrt(128), P the 7-bit
+// bit-reversal permutation, so that (y P)_j = y_{rev(j)}.
+void composite_rotation(const float* U, uint32_t flags, double* R) {
+  const int n = 128;
+  std::vector<double> M(n * n), T(n * n);
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j) M[i * n + j] = (flags & OSCAR_ROT_U) ? (double)U[i * n + j] : (i == j ? 1.0 : 0.0);
+  if (flags & OSCAR_ROT_H) {
+    const double c = 1.0 / std::sqrt((double)n);
+    for (int i = 0; i < n; ++i)
+      for (int j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int k = 0; k < n; ++k) acc += (__builtin_popcount(k & j) & 1) ? -M[i * n + k] : M[i * n + k];
+        T[i * n + j] = acc * c;
+      }
+    M.swap(T);
+  }
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j) {
+      int r = 0;
+      for (int b = 0; b < 7; ++b) r |= ((j >> b) & 1) << (6 - b);
+      R[i * n + j] = (flags & OSCAR_ROT_P) ? M[i * n + r] : M[i * n + j];
+    }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -121,7 +146,6 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   ctx->d_rot.assign(cfg->num_layers, nullptr);
   ctx->tau_k.assign(cfg->num_layers, 0.f);
   ctx->tau_v.assign(cfg->num_layers, 0.f);
-  ctx->flags.assign(cfg->num_layers, 0u);
   ctx->loaded.assign(cfg->num_layers, false);
   *out = ctx;
   return OSCAR_OK;
@@ -147,16 +171,17 @@ oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K
   if (!(tau_k > 0.f) || !(tau_v > 0.f) || std::isnan(tau_k) || std::isnan(tau_v)) return OSCAR_ERR_INVALID_ARG;
   if ((std::isfinite(tau_k) && tau_k > tmax) || (std::isfinite(tau_v) && tau_v > tmax)) return OSCAR_ERR_INVALID_ARG;
   const int n = 128 * 128;
+  for (int i = 0; i < n; ++i)
+    if ((flags & OSCAR_ROT_U) && (!std::isfinite(U_K[i]) || !std::isfinite(U_V[i]))) return OSCAR_ERR_INVALID_ARG;
+  std::vector<double> rk(n), rv(n);
+  composite_rotation(U_K, flags, rk.data());
+  composite_rotation(U_V, flags, rv.data());
   std::vector<float> host(3 * n);
   for (int i = 0; i < 128; ++i)
     for (int j = 0; j < 128; ++j) {
-      const float ident = (i == j) ? 1.f : 0.f;
-      const float uk = (flags & OSCAR_ROT_U) ? U_K[i * 128 + j] : ident;
-      const float uv = (flags & OSCAR_ROT_U) ? U_V[i * 128 + j] : ident;
-      if (!std::isfinite(uk) || !std::isfinite(uv)) return OSCAR_ERR_INVALID_ARG;
-      host[i * 128 + j] = uk;
-      host[n + i * 128 + j] = uv;
-      host[2 * n + j * 128 + i] = uv;
+      host[i * 128 + j] = (float)rk[i * 128 + j];
+      host[n + i * 128 + j] = (float)rv[i * 128 + j];
+      host[2 * n + j * 128 + i] = (float)rv[i * 128 + j];
     }
   DeviceGuard guard(ctx->cfg.device);
   if (ctx->d_rot[layer] == nullptr) {
@@ -169,7 +194,6 @@ oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K
     return OSCAR_ERR_CUDA;
   ctx->tau_k[layer] = tau_k;
   ctx->tau_v[layer] = tau_v;
-  ctx->flags[layer] = flags & (OSCAR_ROT_H | OSCAR_ROT_P);
   ctx->loaded[layer] = true;
   return OSCAR_OK;
 }
@@ -327,13 +351,12 @@ oscar_status oscar_decode_attention_bf16(oscar_ctx* ctx, const oscar_bf16_cache_
   d.workspace = static_cast<uint8_t*>(workspace);
   d.err = ctx->d_err;
   // the prep kernel needs a rotation matrix; the plain path only uses the unrotated q
-  d.rot.flags = 0;
   for (size_t l = 0; l < ctx->d_rot.size(); ++l)
     if (ctx->loaded[l]) {
       d.rot = rotation_of(ctx, (int)l);
       break;
     }
-  if (d.rot.U_K == nullptr) return OSCAR_ERR_NOT_LOADED;
+  if (d.rot.R_K == nullptr) return OSCAR_ERR_NOT_LOADED;
   return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 

@@ -24,11 +24,11 @@ namespace {
 // ------------------------------------------------------------------ decode append
 // One new token per request.  grid (Hkv, B), 256 threads: threads 0..127
 // handle K, threads 128..255 handle V, each a channel per thread.
-__global__ void __launch_bounds__(256) append_one_kernel(AppendLaunch a) {
+__global__ void __launch_bounds__(256, 1) append_one_kernel(AppendLaunch a) {
   __shared__ QuantSmem sm[2];
   griddep_wait();
   const int half = threadIdx.x >> 7;
-  append_one_body(a, blockIdx.y, blockIdx.x, half, threadIdx.x & 127, a.rot.U_K, a.rot.U_V, sm[half]);
+  append_one_body(a, blockIdx.y, blockIdx.x, half, threadIdx.x & 127, a.rot.R_K, a.rot.R_V, sm[half]);
 }
 
 // ------------------------------------------------------------------ multi-token append
@@ -59,7 +59,7 @@ __device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& 
 
 // Phase 1: ring tokens that fall out of the recent window go to the history.
 // grid (256, Hkv, B), 128 threads: one token-head per block.
-__global__ void __launch_bounds__(256) append_evict_kernel(AppendLaunch a) {
+__global__ void __launch_bounds__(256, 1) append_evict_kernel(AppendLaunch a) {
   __shared__ QuantSmem sm[2];
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, half = threadIdx.x >> 7, t = threadIdx.x & 127;
   const bool is_v = half == 1;
@@ -79,8 +79,7 @@ __global__ void __launch_bounds__(256) append_evict_kernel(AppendLaunch a) {
   if (blk == nullptr) return;
   const size_t r = (((size_t)slot * c.num_kv_heads + h) * kRecent + ((e - kSink) % kRecent)) * kD + t;
   const float xv = bf16_bits_to_float((is_v ? c.v_ring : c.k_ring)[r]);
-  quantize_token(xv, is_v ? a.rot.U_V : a.rot.U_K, a.rot.flags, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v,
-                 sm[half]);
+  quantize_token(xv, is_v ? a.rot.R_V : a.rot.R_K, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm[half]);
 }
 
 // Phase 2a: new tokens that stay BF16 (sink rows, ring rows).
@@ -144,7 +143,7 @@ __device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int Hkv = a.c.num_kv_heads;
   const uint16_t* src = is_v ? a.v : a.k;
-  const float* U = is_v ? a.rot.U_V : a.rot.U_K;
+  const float* R = is_v ? a.rot.R_V : a.rot.R_K;
   const float tau = is_v ? a.rot.tau_v : a.rot.tau_k;
   // load the tile (rows outside [r_lo, r_hi) are zero)
   for (int i = t; i < 64 * kD; i += blockDim.x) {
@@ -157,14 +156,14 @@ __device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int
     sm.z[r][ch] = v;
   }
   __syncthreads();
-  // x U: warp w owns rows 8w..8w+7, lane owns channels 4 lane..4 lane+3
+  // x R: warp w owns rows 8w..8w+7, lane owns channels 4 lane..4 lane+3
   float acc[8][4];
 #pragma unroll
   for (int r = 0; r < 8; ++r)
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[r][k] = 0.f;
   for (int i = 0; i < kD; ++i) {
-    const float4 u = __ldg(reinterpret_cast<const float4*>(U + i * kD) + lane);
+    const float4 u = __ldg(reinterpret_cast<const float4*>(R + i * kD) + lane);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const float xv = sm.z[8 * warp + r][i];
@@ -175,37 +174,10 @@ __device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int
     }
   }
   __syncthreads();
-  const unsigned flags = a.rot.flags;
 #pragma unroll 1
   for (int r = 0; r < 8; ++r) {
     const int row = 8 * warp + r;
-    float v[4] = {acc[r][0], acc[r][1], acc[r][2], acc[r][3]};
-    if (flags & kRotH) {
-      // index bits 0,1 live inside the lane, bits 2..6 across lanes
-      float t0 = v[0] + v[1], t1 = v[0] - v[1], t2 = v[2] + v[3], t3 = v[2] - v[3];
-      v[0] = t0 + t2;
-      v[1] = t1 + t3;
-      v[2] = t0 - t2;
-      v[3] = t1 - t3;
-#pragma unroll
-      for (int bb = 0; bb < 5; ++bb) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float o = __shfl_xor_sync(0xffffffffu, v[k], 1 << bb);
-          v[k] = ((lane >> bb) & 1) ? (o - v[k]) : (v[k] + o);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD;
-    }
-    if (flags & kRotP) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sm.z[row][4 * lane + k] = v[k];
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = sm.z[row][brev7(4 * lane + k)];
-      __syncwarp();
-    }
+    const float v[4] = {acc[r][0], acc[r][1], acc[r][2], acc[r][3]};
     // group absmax: channels 0..63 on lanes 0..15, 64..127 on lanes 16..31
     float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll

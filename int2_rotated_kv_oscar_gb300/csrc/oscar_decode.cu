@@ -50,6 +50,9 @@ constexpr unsigned kWaitLimit = 1u << 22;
 constexpr float kLazy = 4.0f;           // rescale only when the max grows by more than 2^4
 constexpr float kPScaleBF16 = 2048.0f;  // 2^4 * 2048 < 60000 (log2 = 11)
 constexpr int kMaxChunks = 256;        // work items per (request, KV head)
+constexpr int kBf16Tiles = (kSink + kRecent) / 16;  // 16-token BF16 tiles per request
+constexpr int kMergeBatch = 12;        // partial records in flight per warp in the final merge
+constexpr int kStash = kD + 4;          // merged state of one warp: acc[128], m, l (16-byte rows)
 
 // Exact fp16 pair of the levels (c - 1.5) of the codes at index r (0..7) of
 // both 16-bit halves of a code word.  One LOP3 puts the code into the low
@@ -107,8 +110,7 @@ __device__ __forceinline__ float split_part(float v, int part) {
 
 struct PrepArgs {
   const uint16_t* q;
-  const float* U_K;
-  unsigned flags;
+  const float* R_K;
   float sm_scale;
   int Hq, Hkv, g;
   uint32_t* qfrag;
@@ -119,7 +121,7 @@ struct PrepArgs {
 
 // ------------------------------------------------------------------ prep
 // q' = q R_K for the g query heads of (request b, KV head h), by the 128
-// threads t = 0..127 of a named-barrier group `bar`; U_K may be in shared or
+// threads t = 0..127 of a named-barrier group `bar`; R_K may be in shared or
 // global memory.
 //
 // Fragment words per (request, KV head): [32 lanes][32].  The MMA B column of
@@ -128,14 +130,14 @@ struct PrepArgs {
 // g > 4 column n is head n, words 0..15 hold the values and 16..31 the
 // residuals.
 struct PrepSmem {
-  float xs[kMaxG][kD];
+  __align__(16) float xs[kMaxG][kD];
   float qr[kMaxG][kD];
   float qp[kMaxG][kD];
-  float scratch[kD];
   float red[8];
 };
 
-__device__ void prep_body(const PrepArgs& a, int b, int h, int t, const float* UK, PrepSmem& sm, int bar) {
+__device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t, const float* __restrict__ RK,
+                                          PrepSmem& sm, int bar) {
   const int lane = t & 31, warp = t >> 5;
   const int g = a.g, bh = b * a.Hkv + h;
   const bool packed = g <= 4;
@@ -146,38 +148,27 @@ __device__ void prep_body(const PrepArgs& a, int b, int h, int t, const float* U
   float z[kMaxG];
 #pragma unroll
   for (int n = 0; n < kMaxG; ++n) z[n] = 0.f;
-#pragma unroll 32
-  for (int i = 0; i < kD; ++i) {
-    const float u = UK[i * kD + t];
+#pragma unroll 4
+  for (int i = 0; i < kD; i += 4) {
+    const float r0 = RK[i * kD + t], r1 = RK[(i + 1) * kD + t], r2 = RK[(i + 2) * kD + t], r3 = RK[(i + 3) * kD + t];
 #pragma unroll
     for (int n = 0; n < kMaxG; ++n)
-      if (n < g) z[n] = fmaf(sm.xs[n][i], u, z[n]);
+      if (n < g) {
+        const float4 x = *reinterpret_cast<const float4*>(&sm.xs[n][i]);
+        z[n] = fmaf(x.x, r0, fmaf(x.y, r1, fmaf(x.z, r2, fmaf(x.w, r3, z[n]))));
+      }
   }
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n) {
-    if (n >= g) break;
-    float v = z[n];
-    if (a.flags & kRotH) v = fwht128_half(v, sm.scratch, t, bar) * kInvSqrtD;
-    sm.qr[n][t] = v;
-  }
-  half_sync(bar);
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n) {
-    if (n >= g) break;
-    const float v = (a.flags & kRotP) ? sm.qr[n][brev7(t)] : sm.qr[n][t];
-    z[n] = v * c;
-    sm.qp[n][t] = sm.xs[n][t] * c;
-  }
-  half_sync(bar);
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n)
-    if (n < g) sm.qr[n][t] = z[n];
   // power-of-two normalisations: max |q'| 2^-E <= 2^10, max |q| 2^-Ep <= 2^10
   float mr = 0.f, mp = 0.f;
-  for (int n = 0; n < g; ++n) {
-    mr = fmaxf(mr, fabsf(sm.qr[n][t]));
-    mp = fmaxf(mp, fabsf(sm.qp[n][t]));
-  }
+#pragma unroll
+  for (int n = 0; n < kMaxG; ++n)
+    if (n < g) {
+      const float vr = z[n] * c, vp = sm.xs[n][t] * c;
+      sm.qr[n][t] = vr;
+      sm.qp[n][t] = vp;
+      mr = fmaxf(mr, fabsf(vr));
+      mp = fmaxf(mp, fabsf(vp));
+    }
   mr = warp_max(mr);
   mp = warp_max(mp);
   if (lane == 0) {
@@ -226,21 +217,21 @@ __device__ void prep_body(const PrepArgs& a, int b, int h, int t, const float* U
 }
 
 // grid (Hkv, B), 128 threads
-__global__ void __launch_bounds__(128) prep_kernel(PrepArgs a) {
+__global__ void __launch_bounds__(128, 1) prep_kernel(PrepArgs a) {
   __shared__ PrepSmem sm;
   griddep_wait();
   griddep_launch_dependents();
-  prep_body(a, blockIdx.y, blockIdx.x, threadIdx.x, a.U_K, sm, 1);
+  prep_body(a, blockIdx.y, blockIdx.x, threadIdx.x, a.R_K, sm, 1);
 }
 
 // Fused decode step, part 1: the decode append (K and V) and the q rotation
 // of one (KV head, request).  grid (Hkv, B), 384 threads in three roles:
-// 0..127 append K, 128..255 append V, 256..383 rotate q.  U_K and U_V are
+// 0..127 append K, 128..255 append V, 256..383 rotate q.  R_K and R_V are
 // brought into shared memory by bulk copies while the previous kernel
 // finishes (programmatic dependent launch).
 constexpr size_t kStepSmemBytes = 2 * kD * kD * sizeof(float) + 16;
 
-__global__ void __launch_bounds__(384) step_kernel(AppendLaunch ap, PrepArgs pr) {
+__global__ void __launch_bounds__(384, 1) step_kernel(AppendLaunch ap, PrepArgs pr) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ QuantSmem qsm[2];
   __shared__ PrepSmem psm;
@@ -253,8 +244,8 @@ __global__ void __launch_bounds__(384) step_kernel(AppendLaunch ap, PrepArgs pr)
     fence_mbar_init();
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(ubar, 2 * kD * kD * 4);
-    bulk_copy_g2s(uk, ap.rot.U_K, kD * kD * 4, ubar);
-    bulk_copy_g2s(uv, ap.rot.U_V, kD * kD * 4, ubar);
+    bulk_copy_g2s(uk, ap.rot.R_K, kD * kD * 4, ubar);
+    bulk_copy_g2s(uv, ap.rot.R_V, kD * kD * 4, ubar);
   }
   griddep_launch_dependents();
   __syncthreads();
@@ -278,14 +269,13 @@ struct DecodeArgs {
   const uint16_t* vb_pages;
   const int32_t* ctx_len;
   int Hq, Hkv, g;
-  int n_items, n_chunks, chunk_pages;
+  int n_items, n_chunks, chunk_pages, tiles_per_item, plain_items;
   const uint32_t* qfrag;
   const uint32_t* qplain;
   const float* qconst;
   float* partials;
   int* counters;
-  const float* U_VT;
-  unsigned flags;
+  const float* R_VT;
   float pscale, inv_pscale;
   float* out;
   unsigned* err;
@@ -329,6 +319,19 @@ __device__ __forceinline__ void online_max(WarpState& st, float mx0, float mx1) 
     st.m[0] = n0;
     st.m[1] = n1;
   }
+}
+
+// Fold one partial softmax state (m, l, acc slice) into a running one.
+__device__ __forceinline__ void merge_record(float& m, float& l, float4& acc, float mx, float lx, float4 v) {
+  const float M = fmaxf(m, mx);
+  if (M == -INFINITY) return;
+  const float so = ex2(m - M), sn = ex2(mx - M);  // an empty state (-inf) gets weight 0
+  acc.x = fmaf(acc.x, so, v.x * sn);
+  acc.y = fmaf(acc.y, so, v.y * sn);
+  acc.z = fmaf(acc.z, so, v.z * sn);
+  acc.w = fmaf(acc.w, so, v.w * sn);
+  l = fmaf(l, so, lx * sn);
+  m = M;
 }
 
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t u) {
@@ -619,8 +622,8 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   const int bh = b * a.Hkv + h;
   const CacheRefs& c = a.c;
   griddep_wait();
-  if (MODE == 0 && item == 0)  // the last block of this (request, KV head) reads U_V^T
-    for (int i = t; i < kD * kD / 32; i += 256) prefetch_l2(a.U_VT + 32 * i);
+  if (MODE == 0 && item == 0)  // the last block of this (request, KV head) reads R_V^T
+    for (int i = t; i < kD * kD / 32; i += 256) prefetch_l2(a.R_VT + 32 * i);
   int L = a.ctx_len[b];
   if (L < 0) {
     if (t == 0 && item == 0) set_error(a.err, kErrLength);
@@ -739,12 +742,13 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
     }
     const float scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
     if (MODE == 0) {
-      // this item's tiles: j = item, item + n_items, ...; warp w takes the w-th, (w+8)-th, ...
+      // this item's tiles j = item * tiles_per_item + k; local tile k goes to
+      // warp 7 - k % 8 (the warps with the fewest pages come last)
       const int sp = c.sink_page[b], slot = c.ring_slot[b];
       const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
-      for (int i = warp;; i += kWarps) {
-        const int j = item + a.n_items * i;
-        if (j >= 20) break;
+      for (int k = kWarps - 1 - warp; k < a.tiles_per_item; k += kWarps) {
+        const int j = item * a.tiles_per_item + k;
+        if (j >= kBf16Tiles) break;
         size_t row_off;
         bool ring;
         const int nv = bf16_tile_rows(j, L, row_off, ring);
@@ -785,12 +789,15 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   __syncthreads();
 
   // ---------------- merge the 8 warps' states into this item's two partial records
+  // (items from plain_items on attend no BF16 tile: they leave their
+  // original-basis record unwritten and the final merge skips it)
   {
     const int kind = t >> 7, ch = t & 127;
+    const bool live = !(kind == 1 && item >= a.plain_items);
     float* part = a.partials + (((size_t)bh * a.n_items + item) * 2 + kind) * kPartialFloats;
     const size_t wstride = (size_t)kStages * kBlockBytes / sizeof(float);
     const float* base = reinterpret_cast<const float*>(smem) + kind * kPartialFloats;
-    for (int n = 0; n < a.g; ++n) {
+    for (int n = 0; live && n < a.g; ++n) {
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) M = fmaxf(M, base[w * wstride + n]);
@@ -799,8 +806,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float* ws = base + w * wstride;
-          const float mw = ws[n];
-          const float al = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          const float al = ex2(ws[n] - M);  // 0 for an empty warp state (m = -inf)
           acc = fmaf(al, ws[16 + n * kD + ch], acc);
           l = fmaf(al, ws[8 + n], l);
         }
@@ -817,136 +823,176 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   __shared__ int s_last;
   __syncthreads();
   if (t == 0) {
-    __threadfence();
-    const int ticket = atomicAdd(&a.counters[bh], 1);
+    // release this block's partial records, acquire the other blocks' ones
+    int ticket;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(ticket) : "l"(&a.counters[bh]) : "memory");
     s_last = (ticket == a.n_items - 1);
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const int X = a.n_items, g = a.g;
   const float* recs = a.partials + (size_t)bh * X * 2 * kPartialFloats;
-  float* uvt = reinterpret_cast<float*>(smem);  // [128][128] U_V^T (rotated-basis part only)
-  float* ml = uvt + kD * kD;                     // [X][2][16] m, l of every partial; m becomes its weight
-  float* stat = ml + X * 32;                     // [2][8][2] per basis and head: M, sum of weighted l
-  float* ys = stat + 32;                         // [8][128]
+  float* rvt = reinterpret_cast<float*>(smem);   // [128][128] R_V^T
+  float* stash = rvt + kD * kD;                  // [kWarps][2][kStash]: acc[128], m, l per warp and basis
+  float* ystage = stash + kWarps * 2 * kStash;   // [g][128] merged rotated-basis accumulators
+  float* opart = rvt;                            // [kWarps][g][128] partial products with R_V^T (after the product)
   uint64_t* ubar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + kWarps * kStages;
   if (MODE == 0 && t == 0) {
     mbar_init(ubar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(ubar, kD * kD * 4);
-    bulk_copy_g2s(uvt, a.U_VT, kD * kD * 4, ubar);
+    bulk_copy_g2s(rvt, a.R_VT, kD * kD * 4, ubar);
   }
-  for (int i = t; i < X * 32; i += 256) ml[i] = __ldcg(recs + (size_t)(i >> 4) * kPartialFloats + (i & 15));
-  __syncthreads();
-  for (int pair = warp; pair < 2 * kMaxG; pair += kWarps) {  // one warp per (basis, head)
-    const int kind = pair >> 3, n = pair & 7;
-    if (n >= g) continue;
-    float M = -INFINITY;
-    for (int x = lane; x < X; x += 32) M = fmaxf(M, ml[x * 32 + kind * 16 + n]);
-    M = warp_max(M);
-    float Ls = 0.f;
-    for (int x = lane; x < X; x += 32) {
-      const float m = ml[x * 32 + kind * 16 + n];
-      const float wx = (m == -INFINITY) ? 0.f : ex2(m - M);
-      ml[x * 32 + kind * 16 + n] = wx;
-      Ls = fmaf(wx, ml[x * 32 + kind * 16 + 8 + n], Ls);
+  // warp (n, part): head n = warp % g merges records part, part + n_parts, ...
+  const int n_parts = kWarps / g, n = warp % g, part = warp / g;
+  const bool active = part < n_parts;
+  if (active) {
+    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    // this warp's records, rotated-basis ones first: r < n_rot is rotated
+    // record x = part + n_parts r, the rest original-basis record
+    // x = part + n_parts (r - n_rot); loaded kMergeBatch at a time so that the
+    // L2 round trips overlap
+    const int n_rot = MODE == 0 ? (X - part + n_parts - 1) / n_parts : 0;
+    const int x_plain = a.plain_items;
+    const int n_pl = x_plain > part ? (x_plain - part + n_parts - 1) / n_parts : 0;
+    const int n_all = n_rot + n_pl;
+    for (int r0 = 0; r0 < n_all; r0 += kMergeBatch) {
+      float mm[kMergeBatch], ll[kMergeBatch];
+      float4 vv[kMergeBatch];
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k) {
+        const int r = r0 + k;
+        mm[k] = -INFINITY;
+        ll[k] = 0.f;
+        vv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < n_all) {
+          const int kind = r < n_rot ? 0 : 1;
+          const int x = part + n_parts * (kind == 0 ? r : r - n_rot);
+          const float* rec = recs + ((size_t)x * 2 + kind) * kPartialFloats;
+          mm[k] = __ldcg(rec + n);
+          ll[k] = __ldcg(rec + 8 + n);
+          vv[k] = __ldcg(reinterpret_cast<const float4*>(rec + 16 + n * kD) + lane);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k) {
+        if (r0 + k < n_rot)
+          merge_record(m0, l0, a0, mm[k], ll[k], vv[k]);
+        else
+          merge_record(m1, l1, a1, mm[k], ll[k], vv[k]);
+      }
     }
-    Ls = warp_sum(Ls);
+    float* s0 = stash + (size_t)warp * 2 * kStash;
+    float* s1 = s0 + kStash;
+    reinterpret_cast<float4*>(s0)[lane] = a0;
+    reinterpret_cast<float4*>(s1)[lane] = a1;
     if (lane == 0) {
-      stat[(kind * 8 + n) * 2] = M;
-      stat[(kind * 8 + n) * 2 + 1] = Ls;
+      s0[kD] = m0;
+      s0[kD + 1] = l0;
+      s1[kD] = m1;
+      s1[kD + 1] = l1;
     }
+  }
+  __syncthreads();
+  if (MODE == 0) {
+    // merged rotated-basis accumulator y[n][j] (unnormalised, scaled to the head's max)
+    for (int e = t; e < g * kD; e += 256) {
+      const int hn = e >> 7, j = e & (kD - 1);
+      float M = -INFINITY;
+      for (int p = 0; p < n_parts; ++p) M = fmaxf(M, stash[(size_t)(p * g + hn) * 2 * kStash + kD]);
+      float v = 0.f;
+      if (M != -INFINITY)
+        for (int p = 0; p < n_parts; ++p) {
+          const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
+          v = fmaf(ex2(sp[kD] - M), sp[j], v);
+        }
+      ystage[e] = v;
+    }
+    __syncthreads();
+    // out_rot = y R_V^T: warp w takes rows j in [16 w, 16 w + 16) of R_V^T for
+    // every head; lane: output channels 4 lane .. 4 lane + 3
+    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(ubar, 0, kWaitLimit));
+    if (!got) {
+      if (lane == 0) set_error(a.err, kErrTimeout);
+      mbar_wait_bounded(ubar, 0, kWaitLimit);
+    }
+    float o[kMaxG][4];
+#pragma unroll
+    for (int hn = 0; hn < kMaxG; ++hn) o[hn][0] = o[hn][1] = o[hn][2] = o[hn][3] = 0.f;
+#pragma unroll 4
+    for (int j = kD / kWarps * warp; j < kD / kWarps * (warp + 1); ++j) {
+      const float4 u = *reinterpret_cast<const float4*>(rvt + j * kD + 4 * lane);
+#pragma unroll
+      for (int hn = 0; hn < kMaxG; ++hn)
+        if (hn < g) {
+          const float yj = ystage[hn * kD + j];
+          o[hn][0] = fmaf(yj, u.x, o[hn][0]);
+          o[hn][1] = fmaf(yj, u.y, o[hn][1]);
+          o[hn][2] = fmaf(yj, u.z, o[hn][2]);
+          o[hn][3] = fmaf(yj, u.w, o[hn][3]);
+        }
+    }
+    __syncthreads();  // every warp is done with R_V^T: its space takes the partial products
+#pragma unroll
+    for (int hn = 0; hn < kMaxG; ++hn)
+      if (hn < g)
+        reinterpret_cast<float4*>(opart + (warp * g + hn) * kD)[lane] =
+            make_float4(o[hn][0], o[hn][1], o[hn][2], o[hn][3]);
   }
   __syncthreads();
   if (warp < g) {
-    // warp n: head n; lane: channels 4 lane .. 4 lane + 3
-    const int n = warp;
-    float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ap = ar;
-#pragma unroll 8
-    for (int x = 0; x < X; ++x) {
-      const float* rec = recs + (size_t)x * 2 * kPartialFloats + 16 + n * kD + 4 * lane;
-      const float wr = ml[x * 32 + n], wp = ml[x * 32 + 16 + n];
-      if (MODE == 0) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(rec));
-        ar.x = fmaf(wr, v.x, ar.x);
-        ar.y = fmaf(wr, v.y, ar.y);
-        ar.z = fmaf(wr, v.z, ar.z);
-        ar.w = fmaf(wr, v.w, ar.w);
-      }
-      const float4 u = __ldcg(reinterpret_cast<const float4*>(rec + kPartialFloats));
-      ap.x = fmaf(wp, u.x, ap.x);
-      ap.y = fmaf(wp, u.y, ap.y);
-      ap.z = fmaf(wp, u.z, ap.z);
-      ap.w = fmaf(wp, u.w, ap.w);
+    // final: rotated-basis and original-basis parts of head n = warp, normalised together
+    const int hn = warp;
+    float Mr = -INFINITY, Mp = -INFINITY;
+    for (int p = 0; p < n_parts; ++p) {
+      const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
+      Mr = fmaxf(Mr, sp[kD]);
+      Mp = fmaxf(Mp, sp[kStash + kD]);
     }
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
-    if (MODE == 0) {
-      // rotate back: y = acc P, y = y H / sqrt(d), out = y U_V^T
-      float* y = ys + n * kD;
-      float v[4] = {ar.x, ar.y, ar.z, ar.w};
-      if (a.flags & kRotP) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) y[4 * lane + k] = v[k];
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = y[brev7(4 * lane + k)];
-        __syncwarp();
-      }
-      if (a.flags & kRotH) {
-        const float t0 = v[0] + v[1], t1 = v[0] - v[1], t2 = v[2] + v[3], t3 = v[2] - v[3];
-        v[0] = t0 + t2;
-        v[1] = t1 + t3;
-        v[2] = t0 - t2;
-        v[3] = t1 - t3;
-#pragma unroll
-        for (int bb = 0; bb < 5; ++bb) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float oth = __shfl_xor_sync(0xffffffffu, v[k], 1 << bb);
-            v[k] = ((lane >> bb) & 1) ? (oth - v[k]) : (v[k] + oth);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD;
+    float Lr = 0.f, Lp = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f), ap = o;
+    if (MODE == 0 && Mr != -INFINITY) {
+      for (int p = 0; p < n_parts; ++p) {
+        const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
+        Lr = fmaf(ex2(sp[kD] - Mr), sp[kD + 1], Lr);
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) y[4 * lane + k] = v[k];
-      __syncwarp();
-      const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(ubar, 0, kWaitLimit));
-      if (!got) {
-        if (lane == 0) set_error(a.err, kErrTimeout);
-        mbar_wait_bounded(ubar, 0, kWaitLimit);
-      }
-#pragma unroll 8
-      for (int j = 0; j < kD; ++j) {
-        const float yj = y[j];
-        const float4 u = *reinterpret_cast<const float4*>(uvt + j * kD + 4 * lane);
-        o[0] = fmaf(yj, u.x, o[0]);
-        o[1] = fmaf(yj, u.y, o[1]);
-        o[2] = fmaf(yj, u.z, o[2]);
-        o[3] = fmaf(yj, u.w, o[3]);
+      for (int w = 0; w < kWarps; ++w) {
+        const float4 op = reinterpret_cast<const float4*>(opart + (w * g + hn) * kD)[lane];
+        o.x += op.x;
+        o.y += op.y;
+        o.z += op.z;
+        o.w += op.w;
       }
     }
-    const float Mr = stat[n * 2], Lr = stat[n * 2 + 1];
-    const float Mp = stat[(8 + n) * 2], Lp = stat[(8 + n) * 2 + 1];
+    if (Mp != -INFINITY) {
+      for (int p = 0; p < n_parts; ++p) {
+        const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
+        const float wp = ex2(sp[kStash + kD] - Mp);
+        Lp = fmaf(wp, sp[kStash + kD + 1], Lp);
+        const float4 v = reinterpret_cast<const float4*>(sp + kStash)[lane];
+        ap.x = fmaf(wp, v.x, ap.x);
+        ap.y = fmaf(wp, v.y, ap.y);
+        ap.z = fmaf(wp, v.z, ap.z);
+        ap.w = fmaf(wp, v.w, ap.w);
+      }
+    }
     const float M = fmaxf(Mr, Mp);
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      const float fr = (Mr == -INFINITY) ? 0.f : ex2(Mr - M);
-      const float fp = (Mp == -INFINITY) ? 0.f : ex2(Mp - M);
+      const float fr = ex2(Mr - M), fp = ex2(Mp - M);
       const float inv_l = 1.0f / (fr * Lr + fp * Lp);
-      res.x = (fr * o[0] + fp * ap.x) * inv_l;
-      res.y = (fr * o[1] + fp * ap.y) * inv_l;
-      res.z = (fr * o[2] + fp * ap.z) * inv_l;
-      res.w = (fr * o[3] + fp * ap.w) * inv_l;
+      res.x = (fr * o.x + fp * ap.x) * inv_l;
+      res.y = (fr * o.y + fp * ap.y) * inv_l;
+      res.z = (fr * o.z + fp * ap.z) * inv_l;
+      res.w = (fr * o.w + fp * ap.w) * inv_l;
     }
-    *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + h * a.g + n) * kD + 4 * lane) = res;
-  } else if (MODE == 0 && warp == kWarps - 1 && g < kWarps) {
-    // make sure the U_V^T copy has landed before the block exits even if no warp waited
+    *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + h * g + hn) * kD + 4 * lane) = res;
   }
   if (MODE == 0) {
+    // no block exits with its bulk copy in flight
     __syncthreads();
     if (t == 0) mbar_wait_bounded(ubar, 0, kWaitLimit);
   }
@@ -958,7 +1004,8 @@ constexpr size_t decode_smem_bytes() {
 // two finished warp states fit in a warp's stage memory; the last block's
 // merge (U_V^T, staged m/l, stats, rotation scratch) fits in all of it
 static_assert(2 * kPartialFloats * 4 <= kStages * kBlockBytes, "warp states");
-static_assert((kD * kD + kMaxChunks * 32 + 32 + kMaxG * kD) * 4 <= kWarps * kStages * kBlockBytes, "merge staging");
+static_assert((kD * kD + kWarps * 2 * kStash + kMaxG * kD) * 4 <= kWarps * kStages * kBlockBytes, "merge staging");
+static_assert(kWarps * kMaxG * kD <= kD * kD, "partial products fit where R_V^T was");
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -988,6 +1035,12 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   p.chunk_pages = (int)C;
   p.n_chunks = pages > 0 ? (int)((pages + C - 1) / C) : 0;
   p.n_items = p.n_chunks > 0 ? p.n_chunks : 1;
+  // BF16 tiles go to the first items, onto the warps that have one page fewer
+  // than warp 0 (pages are dealt round-robin over the 8 warps), so that they
+  // cost no extra time and only a few items produce original-basis partials
+  const int spare = (p.chunk_pages % kWarps) == 0 ? kWarps : kWarps - p.chunk_pages % kWarps;
+  p.tiles_per_item = max(spare, (kBf16Tiles + p.n_items - 1) / p.n_items);
+  p.plain_items = mode == 0 ? min(p.n_items, (kBf16Tiles + p.tiles_per_item - 1) / p.tiles_per_item) : p.n_items;
   const size_t bh = (size_t)batch * Hkv;
   size_t off = 0;
   p.off_counters = off;
@@ -1025,8 +1078,7 @@ PrepArgs prep_args_of(const DecodeLaunch& d) {
   uint8_t* ws = d.workspace;
   PrepArgs pa;
   pa.q = d.q;
-  pa.U_K = d.rot.U_K;
-  pa.flags = d.rot.flags;
+  pa.R_K = d.rot.R_K;
   pa.sm_scale = d.sm_scale;
   pa.Hq = p.Hq;
   pa.Hkv = p.Hkv;
@@ -1054,13 +1106,14 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
   a.n_items = p.n_items;
   a.n_chunks = p.n_chunks;
   a.chunk_pages = p.chunk_pages;
+  a.tiles_per_item = p.tiles_per_item;
+  a.plain_items = p.plain_items;
   a.qfrag = pa.qfrag;
   a.qplain = pa.qplain;
   a.qconst = pa.qconst;
   a.partials = reinterpret_cast<float*>(ws + p.off_partials);
   a.counters = pa.counters;
-  a.U_VT = d.rot.U_VT;
-  a.flags = d.rot.flags;
+  a.R_VT = d.rot.R_VT;
   {
     // largest V scale the layer can store: fp16(min(absmax, tau_v) / 1.5) <= 65504
     const float smax = std::isfinite(d.rot.tau_v) ? fminf(65504.f, d.rot.tau_v / 1.5f * 1.001f) : 65504.f;

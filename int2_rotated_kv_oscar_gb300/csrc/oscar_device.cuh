@@ -31,7 +31,6 @@ constexpr int kVScales = 4352;
 constexpr unsigned kErrPage = 1u, kErrSink = 2u, kErrRing = 4u, kErrLength = 8u, kErrTokens = 16u,
                    kErrTimeout = 32u;
 
-constexpr unsigned kRotU = 1u, kRotH = 2u, kRotP = 4u;
 
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) { atomicOr(err, bits); }
 
@@ -134,28 +133,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Walsh-Hadamard butterfly (Sylvester order, unnormalised) over 128 values
-// held one per thread of a 128-thread block: index bits 0..4 are exchanged
-// in registers through warp shuffles, bits 5..6 through shared memory.
-// `scratch` holds 128 floats.  All 128 threads must call it.
-__device__ __forceinline__ float fwht128_block(float v, float* scratch) {
-  const int t = threadIdx.x;
-#pragma unroll
-  for (int b = 0; b < 5; ++b) {
-    const float o = __shfl_xor_sync(0xffffffffu, v, 1 << b);
-    v = ((t >> b) & 1) ? (o - v) : (v + o);
-  }
-#pragma unroll
-  for (int b = 5; b < 7; ++b) {
-    scratch[t] = v;
-    __syncthreads();
-    const float o = scratch[t ^ (1 << b)];
-    __syncthreads();
-    v = ((t >> b) & 1) ? (o - v) : (v + o);
-  }
-  return v;
-}
-
 // Programmatic dependent launch: wait for the grids this one depends on (no-op
 // when launched without the attribute) / let dependent grids start launching.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
@@ -169,24 +146,5 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 
 // Barrier over the 128 threads [128 * (id - 1), 128 * id) of the block (id >= 1).
 __device__ __forceinline__ void half_sync(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
-
-// fwht128_block for one 128-thread half of a larger block, synchronised by
-// named barrier `bar_id`; thread index within the half is t.
-__device__ __forceinline__ float fwht128_half(float v, float* scratch, int t, int bar_id) {
-#pragma unroll
-  for (int b = 0; b < 5; ++b) {
-    const float o = __shfl_xor_sync(0xffffffffu, v, 1 << b);
-    v = ((t >> b) & 1) ? (o - v) : (v + o);
-  }
-#pragma unroll
-  for (int b = 5; b < 7; ++b) {
-    scratch[t] = v;
-    half_sync(bar_id);
-    const float o = scratch[t ^ (1 << b)];
-    half_sync(bar_id);
-    v = ((t >> b) & 1) ? (o - v) : (v + o);
-  }
-  return v;
-}
 
 }  // namespace oscar

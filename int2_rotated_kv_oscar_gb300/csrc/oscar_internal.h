@@ -9,12 +9,13 @@
 namespace oscar {
 
 // Rotation constants of one layer on the device.
+// One layer's rotation as dense matrices: R = U H P (the factors a layer
+// enables), formed in double precision on the host and rounded to fp32.
 struct LayerRotation {
-  const float* U_K = nullptr;   // [128][128] row-major (identity when the U factor is off)
-  const float* U_V = nullptr;   // [128][128] row-major
-  const float* U_VT = nullptr;  // [128][128] = U_V transposed (inverse rotation of outputs)
+  const float* R_K = nullptr;   // [128][128] row-major: a K row x is rotated as x R_K
+  const float* R_V = nullptr;   // [128][128] row-major
+  const float* R_VT = nullptr;  // [128][128] = R_V transposed (inverse rotation of outputs)
   float tau_k = 0.f, tau_v = 0.f;
-  unsigned flags = 0;           // kRotH | kRotP (the U factor is folded into the matrices)
 };
 
 struct CacheRefs {
@@ -55,6 +56,8 @@ struct DecodePlan {
   int32_t chunk_pages = 0;   // pages per work item
   int32_t n_chunks = 0;      // paged work items per (request, KV head)
   int32_t n_items = 0;       // all work items per (request, KV head)
+  int32_t tiles_per_item = 0;  // mixed cache: BF16 sink/recent tiles per item (items 0, 1, ... take them)
+  int32_t plain_items = 0;     // mixed cache: items that attend BF16 tiles (original-basis partials)
   size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
 };
 

@@ -5,7 +5,8 @@
 // "Architettura del Sistema di Serving e Layout di Memoria": each token is
 // rotated, clipped and quantised on its way into the INT2 history.
 // gist.science "Resumen Técnico: OSCAR ...", §2.2 A.3-4: R = U H_Had P_br and
-// per-layer clip thresholds.
+// per-layer clip thresholds.  The rotation is applied as one dense product
+// with the composite R formed on the host.
 #pragma once
 
 #include "oscar_device.cuh"
@@ -13,8 +14,6 @@
 
 namespace oscar {
 namespace {
-
-constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)
 
 // Byte offset inside a block's K code area of the 32-bit word holding the
 // codes of (row t, quarter tig, group grp).
@@ -31,8 +30,7 @@ __device__ __forceinline__ int v_half_offset(int t, int jj) {
 }
 
 struct QuantSmem {
-  float x[kD];
-  float scratch[kD];
+  __align__(16) float x[kD];
   float red[4];
   uint8_t code[kD];
 };
@@ -40,22 +38,24 @@ struct QuantSmem {
 // Rotate + clip + quantise one token held one channel per thread by one
 // 128-thread half of the block (half 0: K, half 1: V, synchronised by named
 // barrier 1 + half) and store its codes and scale in row `row` of the K or V
-// part of `block`.  All 128 threads of the half must call it.
-__device__ void quantize_token(float x, const float* __restrict__ U, unsigned flags, float tau, uint8_t* block,
-                               int row, bool is_v, QuantSmem& sm) {
+// part of `block`.  R: the layer's composite rotation (global or shared
+// memory).  All 128 threads of the half must call it.
+__device__ __forceinline__ void quantize_token(float x, const float* __restrict__ R, float tau, uint8_t* block,
+                                               int row, bool is_v, QuantSmem& sm) {
   const int t = threadIdx.x & 127, lane = t & 31, warp = t >> 5, bar = 1 + (threadIdx.x >> 7);
   sm.x[t] = x;
   half_sync(bar);
-  float z = 0.f;
-#pragma unroll 32
-  for (int i = 0; i < kD; ++i) z = fmaf(sm.x[i], U[i * kD + t], z);
-  if (flags & kRotH) z = fwht128_half(z, sm.scratch, t, bar) * kInvSqrtD;
-  if (flags & kRotP) {
-    half_sync(bar);
-    sm.scratch[t] = z;
-    half_sync(bar);
-    z = sm.scratch[brev7(t)];
+  // z_t = sum_i x_i R[i][t]
+  float z0 = 0.f, z1 = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < kD; i += 4) {
+    const float4 xv = *reinterpret_cast<const float4*>(&sm.x[i]);
+    z0 = fmaf(xv.x, R[i * kD + t], z0);
+    z1 = fmaf(xv.y, R[(i + 1) * kD + t], z1);
+    z0 = fmaf(xv.z, R[(i + 2) * kD + t], z0);
+    z1 = fmaf(xv.w, R[(i + 3) * kD + t], z1);
   }
+  const float z = z0 + z1;
   const float amax = warp_max(fabsf(z));
   if (lane == 0) sm.red[warp] = amax;
   half_sync(bar);
@@ -109,7 +109,7 @@ __device__ __forceinline__ uint8_t* history_block(const CacheRefs& c, int b, int
 // sink page (position < 64) or its ring row; a position >= 320 first moves
 // the ring row's old token (position - 256) into its INT2 history row.
 __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, int h, int half, int t,
-                                                const float* Uk, const float* Uv, QuantSmem& sm) {
+                                                const float* Rk, const float* Rv, QuantSmem& sm) {
   const bool is_v = half == 1;
   const CacheRefs& c = a.c;
   const int Hkv = c.num_kv_heads;
@@ -141,7 +141,7 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
     uint8_t* blk = history_block(c, b, h, e, a.err);
     if (blk != nullptr) {
       const float x = bf16_bits_to_float(ring[rdst]);
-      quantize_token(x, is_v ? Uv : Uk, a.rot.flags, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm);
+      quantize_token(x, is_v ? Rv : Rk, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm);
     }
   }
   ring[rdst] = xn;
