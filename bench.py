@@ -47,6 +47,29 @@ def algorithmic_bytes_per_layer(L, batch=1):
     return batch * (HKV * (hist * 72 + bf16 * 512) + HQ * D * 2 + HQ * D * 4)
 
 
+def profiled_traffic():
+    """DRAM bytes per layer step (fused step kernel + decode kernel) from the
+    committed ncu summary of this workload, or None when the decode source has
+    changed since those counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_step_qwen3_8b_100k.md")
+    src = os.path.join(ROOT, "int2_rotated_kv_oscar_gb300", "csrc", "oscar_decode.cu")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if line.startswith("- ") and ":" in line:
+                    k, v = line[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        if fields.get("oscar_decode.cu sha256") != digest:
+            return None
+        return int(fields["dram bytes per layer step"])
+    except Exception:
+        return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -206,6 +229,7 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- CUDA arm
 def run_cuda(args):
+    N_LAYERS = args.layers
     import torch
     from int2_rotated_kv_oscar_gb300 import abi, calibrate, inputs
     from int2_rotated_kv_oscar_gb300 import build as _build
@@ -299,11 +323,13 @@ def run_cuda(args):
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed")
         e0.record()
         for i in range(args.steps):
             graphs[(args.warmup + i) % LOOP].replay()
         e1.record()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     ms_total = e0.elapsed_time(e1)
     if world > 1:
         t = torch.tensor([ms_total], device=dev)
@@ -358,6 +384,36 @@ def run_cuda(args):
     h2d = (h_q.numel() + h_kn.numel() + h_vn.numel()) * 2
     d2h = h_out.numel() * 4
     del egraphs
+
+    # ---- bulk write path: prefill-append of 131,072 tokens x 8 KV heads into a
+    # fresh one-layer cache (rotation, clip, quantise, pack), device inputs
+    bulk = None
+    if not args.no_append:
+        n_b = 131_072
+        maxp_a = (n_b + 63) // 64 + 1
+        acache = kvcache.MixedCache(1, HKV, maxp_a, 1, 1, 1, maxp_a, device=dev)
+        acache.page_table.copy_(torch.from_numpy(inputs.shuffled_pages(CFG, maxp_a, layer=1).reshape(1, maxp_a)))
+        ka, va = inputs.kv_tokens_device(4, 0, HKV, inputs.STREAM_KV, n_b, dev)
+        cu_a = torch.tensor([0, n_b], dtype=torch.int32, device=dev)
+        aargs = kvcache.append_args(ka, va, pos0, cu_a, n_b)
+        aview = acache.view(0)
+        for _ in range(3):
+            abi.oscar_kv_append(ctx, 0, aview, aargs, cur)
+        torch.cuda.synchronize()
+        reps = 10
+        e0.record()
+        for _ in range(reps):
+            abi.oscar_kv_append(ctx, 0, aview, aargs, cur)
+        e1.record()
+        torch.cuda.synchronize()
+        a_ms = e0.elapsed_time(e1) / reps
+        assert abi.oscar_check_device_error(ctx) == 0
+        a_bytes = 2 * n_b * HKV * D * 2 + (n_b - 320) * HKV * 72 + 320 * HKV * 2 * D * 2
+        bulk = {"tokens": n_b, "kv_heads": HKV, "ms": a_ms, "gbs": a_bytes / (a_ms / 1e3) / 1e9,
+                "algorithmic_bytes": a_bytes, "hbm_frac": a_bytes / (a_ms / 1e3) / 1e9 / measured_peaks()[0],
+                "note": "oscar_kv_append of one 131,072-token prompt (BF16 K and V in, INT2 history + BF16 "
+                        "sink/recent out), mean of 10 eager calls"}
+        del acache, ka, va
 
     # ---- BF16-cache comparator of the same shape (decode attention, all 36 layers)
     bf16 = None
@@ -453,14 +509,16 @@ def run_cuda(args):
         "vs_baseline": None,
         "dtype": "int2 codes; f16 tensor-core MMA (value + residual), f32 accumulate",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD,
-                   "l2": "inputs larger than L2: 2.1 GB of cache read per step (129 MB L2), no flush",
+        "config": {"workload": WORKLOAD if N_LAYERS == 36 else
+                   WORKLOAD.replace("36 layers", "%d layers (reduced profiling case)" % N_LAYERS),
+                   "l2": ("inputs larger than L2: %.2f GB of cache read per step (129 MB L2), no flush" % (bytes_step / 1e9)
+                          if bytes_step > 129e6 else "cache smaller than L2: a profiling case, not a bench number"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "kv_read_gbs": kv_gbs,
         "hbm_frac": kv_gbs / peak,
         "algorithmic_bytes_per_step": bytes_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None,
+                     "traffic": profiled_traffic(),
                      "kernel": ("one layer's decode step: " + ("append kernel, then q-rotation + split-K decode"
                                 if args.split else "fused append + q-rotation kernel, then split-K decode") +
                                 " with in-kernel combine (bytes: the decode's reads and writes only)"),
@@ -471,6 +529,7 @@ def run_cuda(args):
         "gpu_launches": N_LAYERS * (3 if args.split else 2) * args.steps,
         "clocks": clocks.summary(),
         "bf16_comparator": bf16,
+        "bulk_append": bulk,
         "setup_s": {"calibration": t_cal, "prefill": t_prefill},
     }
     if rank == 0:
@@ -490,6 +549,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-append", action="store_true")
+    ap.add_argument("--layers", type=int, default=N_LAYERS, help="attention layers (36; fewer only for profiling)")
     ap.add_argument("--split", action="store_true", help="append and decode as separate calls (3 launches a layer)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

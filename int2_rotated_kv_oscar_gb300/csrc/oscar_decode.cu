@@ -269,7 +269,7 @@ struct DecodeArgs {
   const uint16_t* vb_pages;
   const int32_t* ctx_len;
   int Hq, Hkv, g;
-  int n_items, n_chunks, chunk_pages, tiles_per_item, plain_items;
+  int n_items, n_chunks, chunk_pages, tiles_per_item, plain_items, rec_floats;
   const uint32_t* qfrag;
   const uint32_t* qplain;
   const float* qconst;
@@ -794,7 +794,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   {
     const int kind = t >> 7, ch = t & 127;
     const bool live = !(kind == 1 && item >= a.plain_items);
-    float* part = a.partials + (((size_t)bh * a.n_items + item) * 2 + kind) * kPartialFloats;
+    float* part = a.partials + (((size_t)bh * a.n_items + item) * 2 + kind) * a.rec_floats;
     const size_t wstride = (size_t)kStages * kBlockBytes / sizeof(float);
     const float* base = reinterpret_cast<const float*>(smem) + kind * kPartialFloats;
     for (int n = 0; live && n < a.g; ++n) {
@@ -831,7 +831,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   __syncthreads();
   if (!s_last) return;
   const int X = a.n_items, g = a.g;
-  const float* recs = a.partials + (size_t)bh * X * 2 * kPartialFloats;
+  const float* recs = a.partials + (size_t)bh * X * 2 * a.rec_floats;
   float* rvt = reinterpret_cast<float*>(smem);   // [128][128] R_V^T
   float* stash = rvt + kD * kD;                  // [kWarps][2][kStash]: acc[128], m, l per warp and basis
   float* ystage = stash + kWarps * 2 * kStash;   // [g][128] merged rotated-basis accumulators
@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
         if (r < n_all) {
           const int kind = r < n_rot ? 0 : 1;
           const int x = part + n_parts * (kind == 0 ? r : r - n_rot);
-          const float* rec = recs + ((size_t)x * 2 + kind) * kPartialFloats;
+          const float* rec = recs + ((size_t)x * 2 + kind) * a.rec_floats;
           mm[k] = __ldcg(rec + n);
           ll[k] = __ldcg(rec + 8 + n);
           vv[k] = __ldcg(reinterpret_cast<const float4*>(rec + 16 + n * kD) + lane);
@@ -1052,7 +1052,8 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   p.off_qconst = off;
   off = align256(off + bh * kQConstFloats * sizeof(float));
   p.off_partials = off;
-  off = align256(off + bh * (size_t)p.n_items * 2 * kPartialFloats * sizeof(float));
+  p.rec_floats = partial_record_floats(p.g);
+  off = align256(off + bh * (size_t)p.n_items * 2 * p.rec_floats * sizeof(float));
   p.total = off;
   return p;
 }
@@ -1108,6 +1109,7 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
   a.chunk_pages = p.chunk_pages;
   a.tiles_per_item = p.tiles_per_item;
   a.plain_items = p.plain_items;
+  a.rec_floats = p.rec_floats;
   a.qfrag = pa.qfrag;
   a.qplain = pa.qplain;
   a.qconst = pa.qconst;

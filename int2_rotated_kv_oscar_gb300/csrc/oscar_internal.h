@@ -58,10 +58,13 @@ struct DecodePlan {
   int32_t n_items = 0;       // all work items per (request, KV head)
   int32_t tiles_per_item = 0;  // mixed cache: BF16 sink/recent tiles per item (items 0, 1, ... take them)
   int32_t plain_items = 0;     // mixed cache: items that attend BF16 tiles (original-basis partials)
+  int32_t rec_floats = 0;      // floats per partial record
   size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
 };
 
-constexpr int kPartialFloats = 16 + 8 * 128;   // m[8], l[8], acc[8][128]
+constexpr int kPartialFloats = 16 + 8 * 128;   // m[8], l[8], acc[8][128]: a warp state in shared memory
+// a partial record in the workspace: m[8], l[8], acc[g][128]
+constexpr int partial_record_floats(int g) { return 16 + 128 * g; }
 constexpr int kQConstFloats = 32;
 constexpr int kQFragWords = 32 * 32;   // q fragments per (request, KV head): [lane][32]
 

@@ -154,3 +154,47 @@ def compare_history_codes(setup, layer, b, L, tok_k, tok_v, h):
         n_edge += int((edge & ~gmask).sum())
         n_mid += int(mid.sum())
     return n_cmp, n_bad, n_edge, n_mid
+
+
+def compare_sampled_pages(setup, layer, b, lpages, tok_k, tok_v):
+    """Bit-exact code comparison of whole history pages against the oracle's
+    direct definition, for large contexts where comparing every position would
+    be slow.  lpages: logical page indices (>= 1, all 64 rows in the history);
+    tok_k, tok_v: fp64 [len(lpages) * 64, H_kv, 128] token values of those pages
+    in order.  Returns (n_compared, n_mismatch, n_edge_excluded, n_midpoint_groups)."""
+    R_K, R_V, tk, tv = setup.rot[layer]
+    c = setup.cache
+    phys = c.page_table[b, torch.tensor(lpages, dtype=torch.int64, device="cuda")].long()
+    pages = c.int2_pages[layer][phys].cpu().numpy()          # [n, H_kv, 4608]
+    n_cmp = n_bad = n_edge = n_mid = 0
+    for h in range(setup.Hkv):
+        kc, ks, vc, vs = layout.unpack_blocks(pages[:, h, :])
+        got = ((kc.reshape(-1, 128), ks.reshape(-1, 2)), (vc.reshape(-1, 128), vs.reshape(-1, 2)))
+        for which, (tok, R, tau) in enumerate(((tok_k, R_K, tk), (tok_v, R_V, tv))):
+            X = rotation.rotate(np.asarray(tok)[:, h], R)
+            codes, scales = quant.quantize_rows(X, tau)
+            mid = quant.fp16_midpoint_mask(X, tau)
+            edge = quant.near_edge_mask(X, scales)
+            gmask = np.repeat(mid, 64, axis=1)
+            gc, gs = got[which]
+            assert ((gs == scales) | mid).all(), "scale mismatch outside fp16 midpoint groups"
+            cmp = ~(edge | gmask)
+            n_cmp += int(cmp.sum())
+            n_bad += int(((gc != codes) & cmp).sum())
+            n_edge += int((edge & ~gmask).sum())
+            n_mid += int(mid.sum())
+    return n_cmp, n_bad, n_edge, n_mid
+
+
+def request_view(setup, b0, b1):
+    """Swap the cache's per-request tables for rows [b0, b1) (for appending a
+    subset of the batch); returns a function that restores them."""
+    c = setup.cache
+    saved = (c.page_table, c.sink_page, c.ring_slot)
+    c.page_table = saved[0][b0:b1].contiguous()
+    c.sink_page = saved[1][b0:b1].contiguous()
+    c.ring_slot = saved[2][b0:b1].contiguous()
+
+    def restore():
+        c.page_table, c.sink_page, c.ring_slot = saved
+    return restore
