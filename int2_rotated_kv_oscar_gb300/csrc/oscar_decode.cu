@@ -40,7 +40,8 @@ namespace oscar {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 3;
 constexpr unsigned kWaitLimit = 1u << 22;
 // The PV B operand is p * s * 2^k (INT2 history, s = V scale) or p * 2^k (BF16
@@ -51,8 +52,11 @@ constexpr float kLazy = 4.0f;           // rescale only when the max grows by mo
 constexpr float kPScaleBF16 = 2048.0f;  // 2^4 * 2048 < 60000 (log2 = 11)
 constexpr int kMaxChunks = 256;        // work items per (request, KV head)
 constexpr int kBf16Tiles = (kSink + kRecent) / 16;  // 16-token BF16 tiles per request
-constexpr int kMergeBatch = 12;        // partial records in flight per warp in the final merge
-constexpr int kStash = kD + 4;          // merged state of one warp: acc[128], m, l (16-byte rows)
+constexpr int kStash = kD + 4;
+constexpr int kBf16Slots = 2;            // warps per work item that attend BF16 tiles (mixed cache)
+// dynamic shared memory: kStages bulk-copy stages per warp, their mbarriers (+1
+// for the final merge), then the BF16 warps' finished states
+constexpr size_t kSlotsOffset = ((size_t)kWarps * kStages * kBlockBytes + (size_t)(kWarps * kStages + 1) * 8 + 15) / 16 * 16;          // merged state of one warp: acc[128], m, l (16-byte rows)
 
 // Exact fp16 pair of the levels (c - 1.5) of the codes at index r (0..7) of
 // both 16-bit halves of a code word.  One LOP3 puts the code into the low
@@ -353,20 +357,22 @@ __device__ __forceinline__ uint32_t pick_pair(float x0, float x1, bool residual)
   return residual ? lo : hi;
 }
 
-// One 64-token INT2 page (K and V codes + scales) staged in shared memory.
+// One 64-token INT2 page (NT = 4) or its 16-token tile T0 (NT = 1), K and V
+// codes + scales staged in shared memory at their block offsets.
 // FULL: all 64 rows valid (no masking).  The softmax weights come out scaled
 // by 2^kp (kp = log2 of the B-operand scale), which the caller undoes.
-template <bool PACK4, bool FULL>
-__device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n_valid, const uint32_t* qf,
+template <bool PACK4, bool FULL, int NT>
+__device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n_valid, int T0, const uint32_t* qf,
                                           float scaleE, float kp, WarpState& st, int lane) {
   const int q = lane >> 2;
   const bool resid = (lane & 3) >= 2;
-  float lg[4][4];
+  float lg[NT][4];
 #pragma unroll
-  for (int T = 0; T < 4; ++T) {
+  for (int i = 0; i < NT; ++i) {
+    const int T = NT == 4 ? i : T0;
     if (!FULL && 16 * T >= n_valid) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) lg[T][k] = -INFINITY;
+      for (int k = 0; k < 4; ++k) lg[i][k] = -INFINITY;
       continue;
     }
     const uint4 kw = *reinterpret_cast<const uint4*>(blk + kKCodes + 512 * T + 16 * lane);
@@ -407,31 +413,32 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
       l3 += __shfl_xor_sync(0xffffffffu, l3, 2);
     }
     if (FULL) {
-      lg[T][0] = l0;
-      lg[T][1] = l1;
-      lg[T][2] = l2;
-      lg[T][3] = l3;
+      lg[i][0] = l0;
+      lg[i][1] = l1;
+      lg[i][2] = l2;
+      lg[i][3] = l3;
     } else {
       const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
-      lg[T][0] = va ? l0 : -INFINITY;
-      lg[T][1] = va ? l1 : -INFINITY;
-      lg[T][2] = vb ? l2 : -INFINITY;
-      lg[T][3] = vb ? l3 : -INFINITY;
+      lg[i][0] = va ? l0 : -INFINITY;
+      lg[i][1] = va ? l1 : -INFINITY;
+      lg[i][2] = vb ? l2 : -INFINITY;
+      lg[i][3] = vb ? l3 : -INFINITY;
     }
   }
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-  for (int T = 0; T < 4; ++T) {
-    mx0 = fmaxf(mx0, fmaxf(lg[T][0], lg[T][2]));
-    mx1 = fmaxf(mx1, fmaxf(lg[T][1], lg[T][3]));
+  for (int i = 0; i < NT; ++i) {
+    mx0 = fmaxf(mx0, fmaxf(lg[i][0], lg[i][2]));
+    mx1 = fmaxf(mx1, fmaxf(lg[i][1], lg[i][3]));
   }
   online_max(st, mx0, mx1);
   const float ms0 = st.m[0] - kp, ms1 = st.m[1] - kp;  // weights p 2^kp
 #pragma unroll
-  for (int T = 0; T < 4; ++T) {
+  for (int i = 0; i < NT; ++i) {
+    const int T = NT == 4 ? i : T0;
     if (!FULL && 16 * T >= n_valid) continue;
-    const float p0 = ex2(lg[T][0] - ms0), p1 = ex2(lg[T][1] - ms1);
-    const float p2 = ex2(lg[T][2] - ms0), p3 = ex2(lg[T][3] - ms1);
+    const float p0 = ex2(lg[i][0] - ms0), p1 = ex2(lg[i][1] - ms1);
+    const float p2 = ex2(lg[i][2] - ms0), p3 = ex2(lg[i][3] - ms1);
     st.l[0] += p0 + p2;
     st.l[1] += p1 + p3;
     float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
@@ -614,276 +621,74 @@ __device__ __forceinline__ int bf16_tile_rows(int j, int L, size_t& row_off, boo
   return max(0, min(16, live - rr));
 }
 
+// Final merge of one (request, KV head): every partial record of its work
+// items, the R_V^T rotation of the rotated-basis part, one normalisation.
+// Run by the block that took the last ticket; kept out of line so that its
+// registers are allocated apart from the page loop's.
 template <int MODE, bool PACK4>
-__global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+__device__ __noinline__ void final_merge(const DecodeArgs& a, uint8_t* smem, int b, int h, int bh) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int bh = b * a.Hkv + h;
-  const CacheRefs& c = a.c;
-  griddep_wait();
-  if (MODE == 0 && item == 0)  // the last block of this (request, KV head) reads R_V^T
-    for (int i = t; i < kD * kD / 32; i += 256) prefetch_l2(a.R_VT + 32 * i);
-  int L = a.ctx_len[b];
-  if (L < 0) {
-    if (t == 0 && item == 0) set_error(a.err, kErrLength);
-    L = 0;
-  }
-  constexpr int kQW = PACK4 ? 16 : 32;
-  // warp-private stage memory; after the warp's pages are done it holds the
-  // warp's two finished states (rotated basis, original basis)
-  uint8_t* stages = smem + (size_t)warp * kStages * kBlockBytes;
-  float* wstate = reinterpret_cast<float*>(stages);
-  WarpState st;
-
-  if (MODE == 0) {
-    // ---------------- INT2 history pages of this chunk (rotated basis)
-    state_init(st);
-    const int hist_end = max(kSink, L - kRecent);
-    const int n_hist = (hist_end + kPage - 1) / kPage - 1;  // logical pages 1..n_hist
-    if (n_hist + 1 > c.max_pages) {
-      if (t == 0 && item == 0) set_error(a.err, kErrLength);
-    }
-    const int n_hist_ok = min(n_hist, c.max_pages - 1);
-    const int lp0 = 1 + item * a.chunk_pages;
-    const int lp1 = min(lp0 + a.chunk_pages, 1 + n_hist_ok);
-    const int first = lp0 + warp;
-    const int n_my = first < lp1 ? (lp1 - first + kWarps - 1) / kWarps : 0;
-    if (n_my > 0) {
-      uint32_t qf[kQW];
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bh * kQFragWords + lane * 32);
-#pragma unroll
-        for (int k = 0; k < kQW / 4; ++k) {
-          const uint4 u = __ldg(src + k);
-          qf[4 * k] = u.x;
-          qf[4 * k + 1] = u.y;
-          qf[4 * k + 2] = u.z;
-          qf[4 * k + 3] = u.w;
-        }
-      }
-      const float scaleE = __ldg(a.qconst + (size_t)bh * kQConstFloats + 16);
-      const float kp = log2f(a.pscale);
-      uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + warp * kStages;
-      const uint8_t* pool = c.pages;
-      auto phys_of = [&](int k) -> int {
-        const int lp = first + kWarps * k;
-        const int ph = c.page_table[(size_t)b * c.max_pages + lp];
-        return (ph >= 0 && ph < c.num_pages) ? ph : -1;
-      };
-      auto issue = [&](int k) {  // lane 0 only
-        const int s = k % kStages;
-        const int ph = phys_of(k);
-        if (ph >= 0) {
-          mbar_arrive_expect_tx(&bars[s], kBlockBytes);
-          bulk_copy_g2s(stages + (size_t)s * kBlockBytes, pool + ((size_t)ph * a.Hkv + h) * kBlockBytes, kBlockBytes,
-                        &bars[s]);
-        } else {
-          set_error(a.err, kErrPage);
-          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&bars[s])) : "memory");
-        }
-      };
-      if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (lane == 0)
-        for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
-      int k = 0;
-      for (; k < n_my; ++k) {
-        const int s = k % kStages;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (k / kStages) & 1, kWaitLimit));
-        if (!ok) {
-          if (lane == 0) set_error(a.err, kErrTimeout);
-          break;
-        }
-        const int lp = first + kWarps * k;
-        if (phys_of(k) >= 0) {
-          const int n_valid = min(kPage, hist_end - kPage * lp);
-          if (n_valid == kPage)
-            int2_page<PACK4, true>(stages + (size_t)s * kBlockBytes, n_valid, qf, scaleE, kp, st, lane);
-          else
-            int2_page<PACK4, false>(stages + (size_t)s * kBlockBytes, n_valid, qf, scaleE, kp, st, lane);
-        }
-        __syncwarp();
-        if (lane == 0 && k + kStages < n_my) {
-          fence_proxy_async_smem();
-          issue(k + kStages);
-        }
-      }
-      // after a timeout, wait (bounded) for the copies still in flight
-      for (int kk = k + 1; kk < min(k + kStages, n_my); ++kk)
-        mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, kWaitLimit);
-      if (k < n_my) mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1, kWaitLimit);
-      __syncwarp();
-    }
-    store_state<PACK4>(st, wstate, a.inv_pscale, lane);
-  } else {
-    state_init(st);
-    store_state<PACK4>(st, wstate, 1.f, lane);
-  }
-
-  // ---------------- BF16 tiles (original basis)
-  state_init(st);
-  {
-    uint32_t qpf[kQW];
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
-#pragma unroll
-      for (int k = 0; k < kQW / 4; ++k) {
-        const uint4 u = __ldg(src + k);
-        qpf[4 * k] = u.x;
-        qpf[4 * k + 1] = u.y;
-        qpf[4 * k + 2] = u.z;
-        qpf[4 * k + 3] = u.w;
-      }
-    }
-    const float scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
-    if (MODE == 0) {
-      // this item's tiles j = item * tiles_per_item + k; local tile k goes to
-      // warp 7 - k % 8 (the warps with the fewest pages come last)
-      const int sp = c.sink_page[b], slot = c.ring_slot[b];
-      const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
-      for (int k = kWarps - 1 - warp; k < a.tiles_per_item; k += kWarps) {
-        const int j = item * a.tiles_per_item + k;
-        if (j >= kBf16Tiles) break;
-        size_t row_off;
-        bool ring;
-        const int nv = bf16_tile_rows(j, L, row_off, ring);
-        if (nv <= 0) continue;
-        if (ring ? !ring_ok : !sink_ok) {
-          if (lane == 0) set_error(a.err, ring ? kErrRing : kErrSink);
-          continue;
-        }
-        const size_t off = ring ? ((((size_t)slot * a.Hkv + h) * kRecent + row_off) * kD)
-                                : ((((size_t)sp * a.Hkv + h) * kSink + row_off) * kD);
-        bf16_tile<PACK4>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, nv, qpf, scaleEp, st,
-                         lane);
-      }
-    } else {
-      // plain BF16 paged cache: item covers pages [item*C, item*C + C), 4 tiles each
-      const int n_pages = (L + kPage - 1) / kPage;
-      if (n_pages > c.max_pages) {
-        if (t == 0 && item == 0) set_error(a.err, kErrLength);
-      }
-      const int pg0 = item * a.chunk_pages;
-      const int pg1 = min(min(pg0 + a.chunk_pages, n_pages), c.max_pages);
-      for (int i = warp; pg0 + i / 4 < pg1; i += kWarps) {
-        const int pg = pg0 + i / 4, tile = i & 3;
-        const int ph = c.page_table[(size_t)b * c.max_pages + pg];
-        if (ph < 0 || ph >= c.num_pages) {
-          if (lane == 0) set_error(a.err, kErrPage);
-          continue;
-        }
-        const int nv = min(16, L - kPage * pg - 16 * tile);
-        if (nv <= 0) continue;
-        const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
-        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, nv, qpf, scaleEp, st, lane);
-      }
-    }
-  }
-  store_state<PACK4>(st, wstate + kPartialFloats, 1.0f / kPScaleBF16, lane);
-  griddep_launch_dependents();  // a dependent step kernel may start loading its constants
-  __syncthreads();
-
-  // ---------------- merge the 8 warps' states into this item's two partial records
-  // (items from plain_items on attend no BF16 tile: they leave their
-  // original-basis record unwritten and the final merge skips it)
-  {
-    const int kind = t >> 7, ch = t & 127;
-    const bool live = !(kind == 1 && item >= a.plain_items);
-    float* part = a.partials + (((size_t)bh * a.n_items + item) * 2 + kind) * a.rec_floats;
-    const size_t wstride = (size_t)kStages * kBlockBytes / sizeof(float);
-    const float* base = reinterpret_cast<const float*>(smem) + kind * kPartialFloats;
-    for (int n = 0; live && n < a.g; ++n) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, base[w * wstride + n]);
-      float acc = 0.f, l = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float* ws = base + w * wstride;
-          const float al = ex2(ws[n] - M);  // 0 for an empty warp state (m = -inf)
-          acc = fmaf(al, ws[16 + n * kD + ch], acc);
-          l = fmaf(al, ws[8 + n], l);
-        }
-      }
-      part[16 + n * kD + ch] = acc;
-      if (ch == 0) {
-        part[n] = M;
-        part[8 + n] = l;
-      }
-    }
-  }
-
-  // ---------------- last block of this (request, KV head) merges all partials
-  __shared__ int s_last;
-  __syncthreads();
-  if (t == 0) {
-    // release this block's partial records, acquire the other blocks' ones
-    int ticket;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(ticket) : "l"(&a.counters[bh]) : "memory");
-    s_last = (ticket == a.n_items - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  const int X = a.n_items, g = a.g;
-  const float* recs = a.partials + (size_t)bh * X * 2 * a.rec_floats;
-  float* rvt = reinterpret_cast<float*>(smem);   // [128][128] R_V^T
-  float* stash = rvt + kD * kD;                  // [kWarps][2][kStash]: acc[128], m, l per warp and basis
-  float* ystage = stash + kWarps * 2 * kStash;   // [g][128] merged rotated-basis accumulators
-  float* opart = rvt;                            // [kWarps][g][128] partial products with R_V^T (after the product)
+  const int X = a.n_items, g = a.g, RF = a.rec_floats;
+  // rotated-basis records first (MODE 0), then the original-basis ones
+  const int n_rot = MODE == 0 ? X : 0, n_rec = n_rot + a.plain_items;
+  const float* recs = a.partials + (size_t)bh * X * 2 * RF;
+  float* buf = reinterpret_cast<float*>(smem);  // record batch buffer
+  const int cap = (int)((size_t)kWarps * kStages * kBlockBytes / 4 / RF);
   uint64_t* ubar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + kWarps * kStages;
-  if (MODE == 0 && t == 0) {
+  // warp w's rows [kD / kWarps w, kD / kWarps (w + 1)) of R_V^T (lane: output
+  // channels 4 lane .. 4 lane + 3), loaded while the records arrive
+  constexpr int kRows = kD / kWarps;
+  float4 rv[kRows];
+  if (MODE == 0) {
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+      rv[i] = __ldg(reinterpret_cast<const float4*>(a.R_VT + (size_t)(kRows * warp + i) * kD) + lane);
+  }
+  if (t == 0) {
     mbar_init(ubar, 1);
     fence_mbar_init();
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(ubar, kD * kD * 4);
-    bulk_copy_g2s(rvt, a.R_VT, kD * kD * 4, ubar);
   }
-  // warp (n, part): head n = warp % g merges records part, part + n_parts, ...
+  __syncthreads();
+  // warp (n, part): head n = warp % g merges records part, part + n_parts, ... of each batch
   const int n_parts = kWarps / g, n = warp % g, part = warp / g;
   const bool active = part < n_parts;
-  if (active) {
-    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-    // this warp's records, rotated-basis ones first: r < n_rot is rotated
-    // record x = part + n_parts r, the rest original-basis record
-    // x = part + n_parts (r - n_rot); loaded kMergeBatch at a time so that the
-    // L2 round trips overlap
-    const int n_rot = MODE == 0 ? (X - part + n_parts - 1) / n_parts : 0;
-    const int x_plain = a.plain_items;
-    const int n_pl = x_plain > part ? (x_plain - part + n_parts - 1) / n_parts : 0;
-    const int n_all = n_rot + n_pl;
-    for (int r0 = 0; r0 < n_all; r0 += kMergeBatch) {
-      float mm[kMergeBatch], ll[kMergeBatch];
-      float4 vv[kMergeBatch];
-#pragma unroll
-      for (int k = 0; k < kMergeBatch; ++k) {
-        const int r = r0 + k;
-        mm[k] = -INFINITY;
-        ll[k] = 0.f;
-        vv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < n_all) {
-          const int kind = r < n_rot ? 0 : 1;
-          const int x = part + n_parts * (kind == 0 ? r : r - n_rot);
-          const float* rec = recs + ((size_t)x * 2 + kind) * a.rec_floats;
-          mm[k] = __ldcg(rec + n);
-          ll[k] = __ldcg(rec + 8 + n);
-          vv[k] = __ldcg(reinterpret_cast<const float4*>(rec + 16 + n * kD) + lane);
-        }
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  for (int r0 = 0, batch = 0; r0 < n_rec; r0 += cap, ++batch) {
+    const int nb = min(cap, n_rec - r0);
+    if (warp == 0) {
+      if (lane == 0) {
+        fence_proxy_async_smem();  // the buffer was last used through generic loads and stores
+        mbar_arrive_expect_tx(ubar, (unsigned)(nb * RF * 4));
       }
-#pragma unroll
-      for (int k = 0; k < kMergeBatch; ++k) {
-        if (r0 + k < n_rot)
-          merge_record(m0, l0, a0, mm[k], ll[k], vv[k]);
-        else
-          merge_record(m1, l1, a1, mm[k], ll[k], vv[k]);
+      __syncwarp();
+      for (int i = lane; i < nb; i += 32) {
+        const int r = r0 + i;
+        const int kind = r < n_rot ? 0 : 1;
+        const int x = r < n_rot ? r : r - n_rot;
+        bulk_copy_g2s(buf + (size_t)i * RF, recs + ((size_t)x * 2 + kind) * RF, (unsigned)(RF * 4), ubar);
       }
     }
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(ubar, batch & 1, kWaitLimit))) {
+      if (lane == 0) set_error(a.err, kErrTimeout);
+      mbar_wait_bounded(ubar, batch & 1, kWaitLimit);
+    }
+    if (active) {
+      for (int i = part; i < nb; i += n_parts) {
+        const float* rec = buf + (size_t)i * RF;
+        const float4 v = reinterpret_cast<const float4*>(rec + 16 + n * kD)[lane];
+        if (r0 + i < n_rot)
+          merge_record(m0, l0, a0, rec[n], rec[8 + n], v);
+        else
+          merge_record(m1, l1, a1, rec[n], rec[8 + n], v);
+      }
+    }
+    __syncthreads();  // the buffer is refilled by the next batch, or becomes the stash
+  }
+  float* stash = buf;                            // [kWarps][2][kStash]: acc[128], m, l per warp and basis
+  float* ystage = stash + kWarps * 2 * kStash;   // [g][128] merged rotated-basis accumulators
+  float* opart = ystage + kMaxG * kD;            // [kWarps][g][128] partial products with R_V^T
+  if (active) {
     float* s0 = stash + (size_t)warp * 2 * kStash;
     float* s1 = s0 + kStash;
     reinterpret_cast<float4*>(s0)[lane] = a0;
@@ -898,7 +703,7 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
   __syncthreads();
   if (MODE == 0) {
     // merged rotated-basis accumulator y[n][j] (unnormalised, scaled to the head's max)
-    for (int e = t; e < g * kD; e += 256) {
+    for (int e = t; e < g * kD; e += kThreads) {
       const int hn = e >> 7, j = e & (kD - 1);
       float M = -INFINITY;
       for (int p = 0; p < n_parts; ++p) M = fmaxf(M, stash[(size_t)(p * g + hn) * 2 * kStash + kD]);
@@ -911,21 +716,17 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
       ystage[e] = v;
     }
     __syncthreads();
-    // out_rot = y R_V^T: warp w takes rows j in [16 w, 16 w + 16) of R_V^T for
-    // every head; lane: output channels 4 lane .. 4 lane + 3
-    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(ubar, 0, kWaitLimit));
-    if (!got) {
-      if (lane == 0) set_error(a.err, kErrTimeout);
-      mbar_wait_bounded(ubar, 0, kWaitLimit);
-    }
-    float o[kMaxG][4];
+    // out_rot = y R_V^T: warp w takes rows j in [kRows w, kRows (w + 1)) for every head
+    constexpr int kG = PACK4 ? 4 : kMaxG;  // heads per KV head this variant serves
+    float o[kG][4];
 #pragma unroll
-    for (int hn = 0; hn < kMaxG; ++hn) o[hn][0] = o[hn][1] = o[hn][2] = o[hn][3] = 0.f;
-#pragma unroll 4
-    for (int j = kD / kWarps * warp; j < kD / kWarps * (warp + 1); ++j) {
-      const float4 u = *reinterpret_cast<const float4*>(rvt + j * kD + 4 * lane);
+    for (int hn = 0; hn < kG; ++hn) o[hn][0] = o[hn][1] = o[hn][2] = o[hn][3] = 0.f;
 #pragma unroll
-      for (int hn = 0; hn < kMaxG; ++hn)
+    for (int i = 0; i < kRows; ++i) {
+      const int j = kRows * warp + i;
+      const float4 u = rv[i];
+#pragma unroll
+      for (int hn = 0; hn < kG; ++hn)
         if (hn < g) {
           const float yj = ystage[hn * kD + j];
           o[hn][0] = fmaf(yj, u.x, o[hn][0]);
@@ -934,9 +735,8 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
           o[hn][3] = fmaf(yj, u.w, o[hn][3]);
         }
     }
-    __syncthreads();  // every warp is done with R_V^T: its space takes the partial products
 #pragma unroll
-    for (int hn = 0; hn < kMaxG; ++hn)
+    for (int hn = 0; hn < kG; ++hn)
       if (hn < g)
         reinterpret_cast<float4*>(opart + (warp * g + hn) * kD)[lane] =
             make_float4(o[hn][0], o[hn][1], o[hn][2], o[hn][3]);
@@ -991,21 +791,299 @@ __global__ void __launch_bounds__(256, 2) decode_kernel(DecodeArgs a) {
     }
     *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + h * g + hn) * kD + 4 * lane) = res;
   }
-  if (MODE == 0) {
-    // no block exits with its bulk copy in flight
-    __syncthreads();
-    if (t == 0) mbar_wait_bounded(ubar, 0, kWaitLimit);
-  }
 }
 
-constexpr size_t decode_smem_bytes() {
-  return (size_t)kWarps * kStages * kBlockBytes + (size_t)(kWarps * kStages + 1) * sizeof(uint64_t);
+template <int MODE, bool PACK4>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int bh = b * a.Hkv + h;
+  const CacheRefs& c = a.c;
+  griddep_wait();
+  if (MODE == 0 && item == 0)  // the last block of this (request, KV head) reads R_V^T
+    for (int i = t; i < kD * kD / 32; i += kThreads) prefetch_l2(a.R_VT + 32 * i);
+  int L = a.ctx_len[b];
+  if (L < 0) {
+    if (t == 0 && item == 0) set_error(a.err, kErrLength);
+    L = 0;
+  }
+  constexpr int kQW = PACK4 ? 16 : 32;
+  // warp-private stage memory; after the warp's pages are done it holds the
+  // warp's two finished states (rotated basis, original basis)
+  uint8_t* stages = smem + (size_t)warp * kStages * kBlockBytes;
+  float* wstate = reinterpret_cast<float*>(stages);
+  float* bf16_slots = reinterpret_cast<float*>(smem + kSlotsOffset);  // [kBf16Slots][kPartialFloats]
+  WarpState st;
+
+  if (MODE == 0) {
+    // ---------------- INT2 history pages of this chunk (rotated basis)
+    const int hist_end = max(kSink, L - kRecent);
+    const int n_hist = (hist_end + kPage - 1) / kPage - 1;  // logical pages 1..n_hist
+    if (n_hist + 1 > c.max_pages) {
+      if (t == 0 && item == 0) set_error(a.err, kErrLength);
+    }
+    const int n_hist_ok = min(n_hist, c.max_pages - 1);
+    // this item's pages [lp0, lp1): R whole rounds dealt round-robin over the
+    // warps (warp w: pages lp0 + w + kWarps k, k < R), then the E left-over
+    // pages as 4 E 16-token tiles (warp w: tiles w, w + kWarps, ...; tile tau
+    // is tile tau % 4 of page lp0 + R kWarps + tau / 4)
+    const int lp0 = 1 + item * a.chunk_pages;
+    const int lp1 = max(lp0, min(lp0 + a.chunk_pages, 1 + n_hist_ok));
+    const int R = (lp1 - lp0) / kWarps, E = (lp1 - lp0) - R * kWarps;
+    const int n_tiles = 4 * E > warp ? (4 * E - warp + kWarps - 1) / kWarps : 0;
+    const int n_my = R + n_tiles;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + warp * kStages;
+    const uint8_t* pool = c.pages;
+      // unit k: logical page and tile (-1: the whole page)
+      auto unit_of = [&](int k, int& lp, int& T) {
+        if (k < R) {
+          lp = lp0 + warp + kWarps * k;
+          T = -1;
+        } else {
+          const int tau = warp + kWarps * (k - R);
+          lp = lp0 + R * kWarps + (tau >> 2);
+          T = tau & 3;
+        }
+      };
+      auto phys_of = [&](int lp) -> int {
+        const int ph = c.page_table[(size_t)b * c.max_pages + lp];
+        return (ph >= 0 && ph < c.num_pages) ? ph : -1;
+      };
+      auto issue = [&](int k) {  // lane 0 only
+        const int s = k % kStages;
+        int lp, T;
+        unit_of(k, lp, T);
+        const int ph = phys_of(lp);
+        uint8_t* dst = stages + (size_t)s * kBlockBytes;
+        if (ph < 0) {
+          set_error(a.err, kErrPage);
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&bars[s])) : "memory");
+          return;
+        }
+        const uint8_t* src = pool + ((size_t)ph * a.Hkv + h) * kBlockBytes;
+        if (T < 0) {
+          mbar_arrive_expect_tx(&bars[s], kBlockBytes);
+          bulk_copy_g2s(dst, src, kBlockBytes, &bars[s]);
+        } else {  // the tile's K codes, K scales, V codes, V scales at their block offsets
+          mbar_arrive_expect_tx(&bars[s], 2 * (512 + 64));
+          bulk_copy_g2s(dst + kKCodes + 512 * T, src + kKCodes + 512 * T, 512, &bars[s]);
+          bulk_copy_g2s(dst + kKScales + 64 * T, src + kKScales + 64 * T, 64, &bars[s]);
+          bulk_copy_g2s(dst + kVCodes + 512 * T, src + kVCodes + 512 * T, 512, &bars[s]);
+          bulk_copy_g2s(dst + kVScales + 64 * T, src + kVScales + 64 * T, 64, &bars[s]);
+        }
+      };
+    if (n_my > 0) {
+      if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0)
+        for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
+    }
+    // BF16 sink/recent tiles (original basis) while the first pages arrive:
+    // local tile k of this item goes to warp kWarps - 1 - k % kBf16Slots,
+    // whose state waits in its slot until the block merge
+    if (kWarps - 1 - warp < kBf16Slots) {
+      const int bk = kWarps - 1 - warp;
+      state_init(st);
+      if (bk < a.tiles_per_item && item * a.tiles_per_item + bk < kBf16Tiles) {
+        uint32_t qpf[kQW];
+        {
+          const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
+#pragma unroll
+          for (int k = 0; k < kQW / 4; ++k) {
+            const uint4 u = __ldg(src + k);
+            qpf[4 * k] = u.x;
+            qpf[4 * k + 1] = u.y;
+            qpf[4 * k + 2] = u.z;
+            qpf[4 * k + 3] = u.w;
+          }
+        }
+        const float scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
+        const int sp = c.sink_page[b], slot = c.ring_slot[b];
+        const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
+        for (int k = bk; k < a.tiles_per_item; k += kBf16Slots) {
+          const int j = item * a.tiles_per_item + k;
+          if (j >= kBf16Tiles) break;
+          size_t row_off;
+          bool ring;
+          const int nv = bf16_tile_rows(j, L, row_off, ring);
+          if (nv <= 0) continue;
+          if (ring ? !ring_ok : !sink_ok) {
+            if (lane == 0) set_error(a.err, ring ? kErrRing : kErrSink);
+            continue;
+          }
+          const size_t off = ring ? ((((size_t)slot * a.Hkv + h) * kRecent + row_off) * kD)
+                                  : ((((size_t)sp * a.Hkv + h) * kSink + row_off) * kD);
+          bf16_tile<PACK4>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, nv, qpf, scaleEp,
+                           st, lane);
+        }
+      }
+      store_state<PACK4>(st, bf16_slots + (size_t)bk * kPartialFloats, 1.0f / kPScaleBF16, lane);
+    }
+    state_init(st);
+    if (n_my > 0) {
+      uint32_t qf[kQW];
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bh * kQFragWords + lane * 32);
+#pragma unroll
+        for (int k = 0; k < kQW / 4; ++k) {
+          const uint4 u = __ldg(src + k);
+          qf[4 * k] = u.x;
+          qf[4 * k + 1] = u.y;
+          qf[4 * k + 2] = u.z;
+          qf[4 * k + 3] = u.w;
+        }
+      }
+      const float scaleE = __ldg(a.qconst + (size_t)bh * kQConstFloats + 16);
+      const float kp = log2f(a.pscale);
+      int k = 0;
+      for (; k < n_my; ++k) {
+        const int s = k % kStages;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (k / kStages) & 1, kWaitLimit));
+        if (!ok) {
+          if (lane == 0) set_error(a.err, kErrTimeout);
+          break;
+        }
+        int lp, T;
+        unit_of(k, lp, T);
+        if (phys_of(lp) >= 0) {
+          const uint8_t* blk = stages + (size_t)s * kBlockBytes;
+          const int n_valid = min(kPage, hist_end - kPage * lp);
+          if (T < 0) {
+            if (n_valid == kPage)
+              int2_page<PACK4, true, 4>(blk, n_valid, 0, qf, scaleE, kp, st, lane);
+            else
+              int2_page<PACK4, false, 4>(blk, n_valid, 0, qf, scaleE, kp, st, lane);
+          } else if (16 * T < n_valid) {
+            if (n_valid >= 16 * T + 16)
+              int2_page<PACK4, true, 1>(blk, n_valid, T, qf, scaleE, kp, st, lane);
+            else
+              int2_page<PACK4, false, 1>(blk, n_valid, T, qf, scaleE, kp, st, lane);
+          }
+        }
+        __syncwarp();
+        if (lane == 0 && k + kStages < n_my) {
+          fence_proxy_async_smem();
+          issue(k + kStages);
+        }
+      }
+      // after a timeout, wait (bounded) for the copies still in flight
+      for (int kk = k + 1; kk < min(k + kStages, n_my); ++kk)
+        mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, kWaitLimit);
+      if (k < n_my) mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1, kWaitLimit);
+      __syncwarp();
+    }
+    store_state<PACK4>(st, wstate, a.inv_pscale, lane);
+  } else {
+    state_init(st);
+    store_state<PACK4>(st, wstate, 1.f, lane);
+  }
+
+  // ---------------- BF16 paged cache (comparator): every warp, original basis
+  if (MODE == 1) {
+    state_init(st);
+    uint32_t qpf[kQW];
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
+#pragma unroll
+      for (int k = 0; k < kQW / 4; ++k) {
+        const uint4 u = __ldg(src + k);
+        qpf[4 * k] = u.x;
+        qpf[4 * k + 1] = u.y;
+        qpf[4 * k + 2] = u.z;
+        qpf[4 * k + 3] = u.w;
+      }
+    }
+    const float scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
+    {
+      // plain BF16 paged cache: item covers pages [item*C, item*C + C), 4 tiles each
+      const int n_pages = (L + kPage - 1) / kPage;
+      if (n_pages > c.max_pages) {
+        if (t == 0 && item == 0) set_error(a.err, kErrLength);
+      }
+      const int pg0 = item * a.chunk_pages;
+      const int pg1 = min(min(pg0 + a.chunk_pages, n_pages), c.max_pages);
+      for (int i = warp; pg0 + i / 4 < pg1; i += kWarps) {
+        const int pg = pg0 + i / 4, tile = i & 3;
+        const int ph = c.page_table[(size_t)b * c.max_pages + pg];
+        if (ph < 0 || ph >= c.num_pages) {
+          if (lane == 0) set_error(a.err, kErrPage);
+          continue;
+        }
+        const int nv = min(16, L - kPage * pg - 16 * tile);
+        if (nv <= 0) continue;
+        const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
+        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, nv, qpf, scaleEp, st, lane);
+      }
+    }
+    store_state<PACK4>(st, wstate + kPartialFloats, 1.0f / kPScaleBF16, lane);
+  }
+  griddep_launch_dependents();  // a dependent step kernel may start loading its constants
+  __syncthreads();
+
+  // ---------------- merge the warps' states into this item's two partial records
+  // (items from plain_items on attend no BF16 tile: they leave their
+  // original-basis record unwritten and the final merge skips it)
+  {
+    // thread: basis kind, channel ch, heads n = t / 256, t / 256 + kThreads / 256, ...
+    const int kind = (t >> 7) & 1, ch = t & 127;
+    const bool live = !(kind == 1 && item >= a.plain_items);
+    float* part = a.partials + (((size_t)bh * a.n_items + item) * 2 + kind) * a.rec_floats;
+    // warp states: the stage memory of every warp, or (original basis of the
+    // mixed cache) the BF16 slots
+    const bool slots = MODE == 0 && kind == 1;
+    const size_t wstride = slots ? kPartialFloats : (size_t)kStages * kBlockBytes / sizeof(float);
+    const int n_states = slots ? kBf16Slots : kWarps;
+    const float* base = slots ? bf16_slots : reinterpret_cast<const float*>(smem) + kind * kPartialFloats;
+    for (int n = t >> 8; live && n < a.g; n += kThreads / 256) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w)
+        if (w < n_states) M = fmaxf(M, base[w * wstride + n]);
+      float acc = 0.f, l = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          if (w >= n_states) break;
+          const float* ws = base + w * wstride;
+          const float al = ex2(ws[n] - M);  // 0 for an empty warp state (m = -inf)
+          acc = fmaf(al, ws[16 + n * kD + ch], acc);
+          l = fmaf(al, ws[8 + n], l);
+        }
+      }
+      part[16 + n * kD + ch] = acc;
+      if (ch == 0) {
+        part[n] = M;
+        part[8 + n] = l;
+      }
+    }
+  }
+
+  // ---------------- last block of this (request, KV head) merges all partials
+  __shared__ int s_last;
+  __syncthreads();
+  if (t == 0) {
+    // release this block's partial records, acquire the other blocks' ones
+    int ticket;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(ticket) : "l"(&a.counters[bh]) : "memory");
+    s_last = (ticket == a.n_items - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  final_merge<MODE, PACK4>(a, smem, b, h, bh);
 }
+
+constexpr size_t decode_smem_bytes() { return kSlotsOffset + (size_t)kBf16Slots * kPartialFloats * sizeof(float); }
 // two finished warp states fit in a warp's stage memory; the last block's
 // merge (U_V^T, staged m/l, stats, rotation scratch) fits in all of it
 static_assert(2 * kPartialFloats * 4 <= kStages * kBlockBytes, "warp states");
-static_assert((kD * kD + kWarps * 2 * kStash + kMaxG * kD) * 4 <= kWarps * kStages * kBlockBytes, "merge staging");
-static_assert(kWarps * kMaxG * kD <= kD * kD, "partial products fit where R_V^T was");
+static_assert((kWarps * 2 * kStash + kMaxG * kD + kWarps * kMaxG * kD) * 4 <= kWarps * kStages * kBlockBytes,
+              "merge staging");
+static_assert(kWarps * kStages * kBlockBytes / 4 / (16 + 128 * kMaxG) >= 1, "a record batch holds a record");
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -1025,21 +1103,20 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
     pages = (max_ctx_len + kPage - 1) / kPage;
   }
   if (pages < 0) pages = 0;
-  // one balanced wave of blocks (2 per SM) when the work is small, <= 64 pages per block otherwise
+  // one balanced wave of blocks (one per SM) when the work is small, <= 8 pages per warp otherwise
   const long long total = (long long)batch * Hkv * pages;
-  const long long slots = 2LL * (num_sms > 0 ? num_sms : 148);
+  const long long slots = num_sms > 0 ? num_sms : 148;
   long long C = (total + slots - 1) / slots;
   if (C < 2) C = 2;
-  if (C > 64) C = 64;
+  if (C > 8 * kWarps) C = 8 * kWarps;
   if (pages > C * kMaxChunks) C = (pages + kMaxChunks - 1) / kMaxChunks;
   p.chunk_pages = (int)C;
   p.n_chunks = pages > 0 ? (int)((pages + C - 1) / C) : 0;
   p.n_items = p.n_chunks > 0 ? p.n_chunks : 1;
-  // BF16 tiles go to the first items, onto the warps that have one page fewer
-  // than warp 0 (pages are dealt round-robin over the 8 warps), so that they
-  // cost no extra time and only a few items produce original-basis partials
-  const int spare = (p.chunk_pages % kWarps) == 0 ? kWarps : kWarps - p.chunk_pages % kWarps;
-  p.tiles_per_item = max(spare, (kBf16Tiles + p.n_items - 1) / p.n_items);
+  // BF16 tiles go to the first items, two warps each (the last two, which
+  // hold the fewest left-over INT2 tiles); they run while those warps' first
+  // pages arrive, and only a few items produce original-basis partials
+  p.tiles_per_item = max(kBf16Slots, (kBf16Tiles + p.n_items - 1) / p.n_items);
   p.plain_items = mode == 0 ? min(p.n_items, (kBf16Tiles + p.tiles_per_item - 1) / p.tiles_per_item) : p.n_items;
   const size_t bh = (size_t)batch * Hkv;
   size_t off = 0;
@@ -1139,7 +1216,7 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
     attr_done[which] = true;
   }
   void* args[] = {&a};
-  return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(256), smem, stream, args);
+  return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), smem, stream, args);
 }
 
 }  // namespace
