@@ -131,52 +131,65 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 }
 
 // Phase 2b: new tokens that go straight into the INT2 history, one page of
-// one KV head per block.  grid (pages, Hkv, B), 256 threads.
+// one KV head per block.  grid (pages, Hkv, B), 256 threads: threads 0..127
+// quantise the K rows, 128..255 the V rows, concurrently (named barriers
+// 1 and 2).  x R runs on the CUDA cores in fp32 (summed in channel order):
+// warp q of a half owns rows 16 q .. 16 q + 15, lane owns channels
+// 4 lane .. 4 lane + 3.
 struct TileSmem {
-  float z[64][kD + 4];
-  uint8_t code[64][kD];
-  __half scale[64][2];
+  __align__(16) float z[2][64][kD + 4];  // K and V rows (fp32)
+  uint8_t code[2][64][kD];
+  __half scale[2][64][2];
 };
 
-__device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int p0, int r_lo, int r_hi, int lp,
-                              uint8_t* blk, bool is_v, TileSmem& sm) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+__device__ __forceinline__ void quantize_tile_half(const AppendLaunch& a, int b, int h, int tok0, int p0, int r_lo,
+                                                   int r_hi, int lp, uint8_t* blk, int half, TileSmem& sm) {
+  const bool is_v = half == 1;
+  const int t = threadIdx.x & 127, lane = t & 31, wq = t >> 5, bar = 1 + half;
   const int Hkv = a.c.num_kv_heads;
   const uint16_t* src = is_v ? a.v : a.k;
-  const float* R = is_v ? a.rot.R_V : a.rot.R_K;
+  const float* __restrict__ R = is_v ? a.rot.R_V : a.rot.R_K;
   const float tau = is_v ? a.rot.tau_v : a.rot.tau_k;
-  // load the tile (rows outside [r_lo, r_hi) are zero)
-  for (int i = t; i < 64 * kD; i += blockDim.x) {
-    const int r = i >> 7, ch = i & 127;
-    float v = 0.f;
+  float(*z)[kD + 4] = sm.z[half];
+  // load the tile, 8 channels per load (rows outside [r_lo, r_hi) are zero)
+  for (int i = t; i < 64 * (kD / 8); i += 128) {
+    const int r = i >> 4, c8 = (i & 15) * 8;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
     if (r >= r_lo && r < r_hi) {
       const int p = lp * kPage + r;
-      v = bf16_bits_to_float(src[((size_t)(tok0 + p - p0) * Hkv + h) * kD + ch]);
+      u = *reinterpret_cast<const uint4*>(src + ((size_t)(tok0 + p - p0) * Hkv + h) * kD + c8);
     }
-    sm.z[r][ch] = v;
-  }
-  __syncthreads();
-  // x R: warp w owns rows 8w..8w+7, lane owns channels 4 lane..4 lane+3
-  float acc[8][4];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int r = 0; r < 8; ++r)
+    for (int k = 0; k < 4; ++k) {
+      z[r][c8 + 2 * k] = __uint_as_float(w[k] << 16);
+      z[r][c8 + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+  half_sync(bar);
+  float acc[16][4];
+#pragma unroll
+  for (int r = 0; r < 16; ++r)
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[r][k] = 0.f;
-  for (int i = 0; i < kD; ++i) {
-    const float4 u = __ldg(reinterpret_cast<const float4*>(R + i * kD) + lane);
+#pragma unroll 2
+  for (int i = 0; i < kD; i += 4) {
+    const float4 r0 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 0) * kD) + lane);
+    const float4 r1 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 1) * kD) + lane);
+    const float4 r2 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 2) * kD) + lane);
+    const float4 r3 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 3) * kD) + lane);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float xv = sm.z[8 * warp + r][i];
-      acc[r][0] = fmaf(xv, u.x, acc[r][0]);
-      acc[r][1] = fmaf(xv, u.y, acc[r][1]);
-      acc[r][2] = fmaf(xv, u.z, acc[r][2]);
-      acc[r][3] = fmaf(xv, u.w, acc[r][3]);
+    for (int r = 0; r < 16; ++r) {
+      const float4 x = *reinterpret_cast<const float4*>(&z[16 * wq + r][i]);
+      acc[r][0] = fmaf(x.w, r3.x, fmaf(x.z, r2.x, fmaf(x.y, r1.x, fmaf(x.x, r0.x, acc[r][0]))));
+      acc[r][1] = fmaf(x.w, r3.y, fmaf(x.z, r2.y, fmaf(x.y, r1.y, fmaf(x.x, r0.y, acc[r][1]))));
+      acc[r][2] = fmaf(x.w, r3.z, fmaf(x.z, r2.z, fmaf(x.y, r1.z, fmaf(x.x, r0.z, acc[r][2]))));
+      acc[r][3] = fmaf(x.w, r3.w, fmaf(x.z, r2.w, fmaf(x.y, r1.w, fmaf(x.x, r0.w, acc[r][3]))));
     }
   }
-  __syncthreads();
-#pragma unroll 1
-  for (int r = 0; r < 8; ++r) {
-    const int row = 8 * warp + r;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int row = 16 * wq + r;
     const float v[4] = {acc[r][0], acc[r][1], acc[r][2], acc[r][3]};
     // group absmax: channels 0..63 on lanes 0..15, 64..127 on lanes 16..31
     float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -184,15 +197,18 @@ __device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int
     for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     const float aa = fminf(m, tau);
     const __half sh = __float2half_rn(aa / 1.5f);
-    const float s = __half2float(sh);
+    const float sc = __half2float(sh);
+    uint32_t packed = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sm.code[row][4 * lane + k] = (uint8_t)((v[k] >= -s) + (v[k] >= 0.f) + (v[k] >= s));
-    if ((lane & 15) == 0) sm.scale[row][lane >> 4] = sh;
+    for (int k = 0; k < 4; ++k)
+      packed |= (uint32_t)((v[k] >= -sc) + (v[k] >= 0.f) + (v[k] >= sc)) << (8 * k);
+    *reinterpret_cast<uint32_t*>(&sm.code[half][row][4 * lane]) = packed;
+    if ((lane & 15) == 0) sm.scale[half][row][lane >> 4] = sh;
   }
-  __syncthreads();
+  half_sync(bar);
   // pack the rows in [r_lo, r_hi) only: other rows of this page may hold
   // history tokens written by earlier appends
-  for (int i = t; i < 64 * 8; i += blockDim.x) {
+  for (int i = t; i < 64 * 8; i += 128) {
     const int row = i >> 3, w = i & 7;
     if (row < r_lo || row >= r_hi) continue;
     if (!is_v) {
@@ -200,8 +216,8 @@ __device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int
       uint32_t word = 0;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        word |= (uint32_t)sm.code[row][base + r] << (2 * r);
-        word |= (uint32_t)sm.code[row][base + 8 + r] << (16 + 2 * r);
+        word |= (uint32_t)sm.code[0][row][base + r] << (2 * r);
+        word |= (uint32_t)sm.code[0][row][base + 8 + r] << (16 + 2 * r);
       }
       *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, tig, g)) = word;
     } else {
@@ -210,20 +226,19 @@ __device__ void quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int
         const int jj = 2 * w + hh;
         uint32_t hv = 0;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[row][jj + 16 * r] << (2 * r);
+        for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[1][row][jj + 16 * r] << (2 * r);
         *reinterpret_cast<uint16_t*>(blk + kVCodes + v_half_offset(row, jj)) = (uint16_t)hv;
       }
     }
   }
-  for (int i = t; i < 64 * 2; i += blockDim.x) {
+  for (int i = t; i < 64 * 2; i += 128) {
     const int row = i >> 1, g = i & 1;
     if (row < r_lo || row >= r_hi) continue;
-    *reinterpret_cast<__half*>(blk + (is_v ? kVScales : kKScales) + 4 * row + 2 * g) = sm.scale[row][g];
+    *reinterpret_cast<__half*>(blk + (is_v ? kVScales : kKScales) + 4 * row + 2 * g) = sm.scale[half][row][g];
   }
-  __syncthreads();
 }
 
-__global__ void __launch_bounds__(256) append_tile_kernel(AppendLaunch a) {
+__global__ void __launch_bounds__(256, 2) append_tile_kernel(AppendLaunch a) {
   extern __shared__ __align__(16) uint8_t tile_smem_raw[];
   TileSmem& sm = *reinterpret_cast<TileSmem*>(tile_smem_raw);
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -237,8 +252,7 @@ __global__ void __launch_bounds__(256) append_tile_kernel(AppendLaunch a) {
   const int r_lo = max(lo - lp * kPage, 0), r_hi = min(hi - lp * kPage, kPage);
   uint8_t* blk = history_block(a.c, b, h, lp * kPage, a.err);
   if (blk == nullptr) return;
-  quantize_tile(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, false, sm);
-  quantize_tile(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, true, sm);
+  quantize_tile_half(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, threadIdx.x >> 7, sm);
 }
 
 }  // namespace

@@ -43,7 +43,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 3;
-constexpr unsigned kWaitLimit = 1u << 22;
 // The PV B operand is p * s * 2^k (INT2 history, s = V scale) or p * 2^k (BF16
 // tiles), with p <= 2^kLazy.  k is the largest power of two that keeps it
 // below 60000 for the layer's largest possible scale, so small weights stay
