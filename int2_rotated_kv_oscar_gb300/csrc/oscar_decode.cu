@@ -52,6 +52,7 @@ constexpr float kPScaleBF16 = 2048.0f;  // 2^4 * 2048 < 60000 (log2 = 11)
 constexpr int kMaxChunks = 256;        // work items per (request, KV head)
 constexpr int kBf16Tiles = (kSink + kRecent) / 16;  // 16-token BF16 tiles per request
 constexpr int kStash = kD + 4;
+constexpr int kPrefetchPages = 1;        // pages per warp pulled into L2 before the dependency wait
 constexpr int kBf16Slots = 2;            // warps per work item that attend BF16 tiles (mixed cache)
 // dynamic shared memory: kStages bulk-copy stages per warp, their mbarriers (+1
 // for the final merge), then the BF16 warps' finished states
@@ -251,6 +252,20 @@ __global__ void __launch_bounds__(384, 1) step_kernel(AppendLaunch ap, PrepArgs 
     bulk_copy_g2s(uv, ap.rot.R_V, kD * kD * 4, ubar);
   }
   griddep_launch_dependents();
+  // while the kernel before this one finishes: pull this block's rows into L2
+  // (a hint only; everything is read again after the wait)
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x, Hkv = ap.c.num_kv_heads;
+    const size_t row = ((size_t)b * Hkv + h) * kD;  // new K / V token rows, 256 bytes each
+    if (lane < 2) prefetch_l2(ap.k + row + 64 * lane);
+    else if (lane < 4) prefetch_l2(ap.v + row + 64 * (lane - 2));
+    else if (lane < 4 + 2 * pr.g) prefetch_l2(pr.q + ((size_t)b * pr.Hq + h * pr.g) * kD + 64 * (lane - 4));
+    const int p = ap.pos[b], slot = ap.c.ring_slot[b];
+    if (lane >= 28 && p >= kSink + kRecent && slot >= 0 && slot < ap.c.num_ring) {  // the ring row to evict
+      const size_t r = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + 64 * (lane & 1);
+      prefetch_l2(((lane & 2) ? ap.c.v_ring : ap.c.k_ring) + r);
+    }
+  }
   __syncthreads();
   griddep_wait();
   if (!mbar_wait_bounded(ubar, 0, kWaitLimit)) {
@@ -799,9 +814,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int bh = b * a.Hkv + h;
   const CacheRefs& c = a.c;
+  if (MODE == 0) {
+    // While the kernel before this one finishes: pull this warp's first
+    // pages into L2 (a hint only -- the tables read here may still change, and
+    // the pages are read again, coherently, after the wait).  More than one
+    // page per warp competes with the previous layer's final merge.
+    if (item == 0)  // the last block of this (request, KV head) reads R_V^T
+      for (int i = t; i < kD * kD / 32; i += kThreads) prefetch_l2(a.R_VT + 32 * i);
+    if (lane == 0) {
+      const int Lh = a.ctx_len[b];
+      const int he = max(kSink, Lh - kRecent);
+      const int nh = min((he + kPage - 1) / kPage - 1, c.max_pages - 1);
+      const int q0 = 1 + item * a.chunk_pages, q1 = max(q0, min(q0 + a.chunk_pages, 1 + nh));
+      const int rr = (q1 - q0) / kWarps, ee = (q1 - q0) - rr * kWarps;
+      for (int k = 0; k <= rr && k < kPrefetchPages; ++k) {
+        const int lp = k < rr ? q0 + warp + kWarps * k : (warp < ee ? q0 + kWarps * rr + warp : -1);
+        if (lp < 0) break;
+        const int ph = c.page_table[(size_t)b * c.max_pages + lp];
+        if (ph >= 0 && ph < c.num_pages) bulk_prefetch_l2(c.pages + ((size_t)ph * a.Hkv + h) * kBlockBytes, kBlockBytes);
+      }
+    }
+  }
   griddep_wait();
-  if (MODE == 0 && item == 0)  // the last block of this (request, KV head) reads R_V^T
-    for (int i = t; i < kD * kD / 32; i += kThreads) prefetch_l2(a.R_VT + 32 * i);
   int L = a.ctx_len[b];
   if (L < 0) {
     if (t == 0 && item == 0) set_error(a.err, kErrLength);
