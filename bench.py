@@ -401,11 +401,13 @@ def run_cuda(args):
             abi.oscar_kv_append(ctx, 0, aview, aargs, cur)
         torch.cuda.synchronize()
         reps = 10
+        torch.cuda.nvtx.range_push("bulk_append")
         e0.record()
         for _ in range(reps):
             abi.oscar_kv_append(ctx, 0, aview, aargs, cur)
         e1.record()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         a_ms = e0.elapsed_time(e1) / reps
         assert abi.oscar_check_device_error(ctx) == 0
         a_bytes = 2 * n_b * HKV * D * 2 + (n_b - 320) * HKV * 72 + 320 * HKV * 2 * D * 2
