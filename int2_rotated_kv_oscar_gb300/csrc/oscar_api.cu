@@ -17,7 +17,9 @@ struct oscar_ctx {
   oscar_config cfg;
   int num_sms = 0;
   unsigned* d_err = nullptr;
-  std::vector<float*> d_rot;       // per layer: R_K | R_V | R_V^T, 3 * 128 * 128 floats
+  // per layer: R_K | R_V | R_V^T (3 * 128 * 128 floats), then the bf16
+  // three-term splits of R_K^T and R_V^T (6 * 128 * 128 bf16)
+  std::vector<float*> d_rot;
   std::vector<float> tau_k, tau_v;
   std::vector<bool> loaded;
 };
@@ -69,9 +71,26 @@ LayerRotation rotation_of(const oscar_ctx* ctx, int layer) {
   r.R_K = base;
   r.R_V = base + 128 * 128;
   r.R_VT = base + 2 * 128 * 128;
+  r.RT_split = reinterpret_cast<const uint16_t*>(base + 3 * 128 * 128);
   r.tau_k = ctx->tau_k[layer];
   r.tau_v = ctx->tau_v[layer];
   return r;
+}
+
+// Round to bf16 (nearest even) through fp32; returns the bit pattern.
+uint16_t bf16_bits(double x) {
+  const float f = (float)x;
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+double bf16_value(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return (double)f;
 }
 
 // R = U H P in double precision (gist.science "Resumen Técnico: OSCAR ...",
@@ -183,14 +202,31 @@ oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K
       host[n + i * 128 + j] = (float)rv[i * 128 + j];
       host[2 * n + j * 128 + i] = (float)rv[i * 128 + j];
     }
+  // three bf16 terms of R^T per matrix: t0 = bf16(R), t1 = bf16(R - t0), t2 = bf16(R - t0 - t1)
+  std::vector<uint16_t> split(6 * n);
+  for (int m = 0; m < 2; ++m) {
+    const std::vector<double>& R = m == 0 ? rk : rv;
+    for (int kk = 0; kk < 128; ++kk)
+      for (int nn = 0; nn < 128; ++nn) {
+        double r = R[kk * 128 + nn];
+        for (int t = 0; t < 3; ++t) {
+          const uint16_t b = bf16_bits(r);
+          split[((size_t)(m * 3 + t) * 128 + nn) * 128 + kk] = b;
+          r -= bf16_value(b);
+        }
+      }
+  }
+  const size_t bytes = sizeof(float) * 3 * n + sizeof(uint16_t) * 6 * n;
   DeviceGuard guard(ctx->cfg.device);
   if (ctx->d_rot[layer] == nullptr) {
-    if (cudaMalloc(&ctx->d_rot[layer], sizeof(float) * 3 * n) != cudaSuccess) {
+    if (cudaMalloc(&ctx->d_rot[layer], bytes) != cudaSuccess) {
       ctx->d_rot[layer] = nullptr;
       return OSCAR_ERR_CUDA;
     }
   }
-  if (cudaMemcpy(ctx->d_rot[layer], host.data(), sizeof(float) * 3 * n, cudaMemcpyHostToDevice) != cudaSuccess)
+  if (cudaMemcpy(ctx->d_rot[layer], host.data(), sizeof(float) * 3 * n, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(ctx->d_rot[layer] + 3 * n, split.data(), sizeof(uint16_t) * 6 * n, cudaMemcpyHostToDevice) !=
+          cudaSuccess)
     return OSCAR_ERR_CUDA;
   ctx->tau_k[layer] = tau_k;
   ctx->tau_v[layer] = tau_v;

@@ -14,6 +14,8 @@
 // 64 rotated channels: a = min(max|x'|, tau), s = fp16(a / 1.5),
 // code = [x' >= -s] + [x' >= 0] + [x' >= s].
 
+#include <algorithm>
+
 #include "oscar_device.cuh"
 #include "oscar_internal.h"
 #include "oscar_quant.cuh"
@@ -130,80 +132,118 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
   }
 }
 
-// Phase 2b: new tokens that go straight into the INT2 history, one page of
-// one KV head per block.  grid (pages, Hkv, B), 256 threads: threads 0..127
-// quantise the K rows, 128..255 the V rows, concurrently (named barriers
-// 1 and 2).  x R runs on the CUDA cores in fp32 (summed in channel order):
-// warp q of a half owns rows 16 q .. 16 q + 15, lane owns channels
-// 4 lane .. 4 lane + 3.
-struct TileSmem {
-  __align__(16) float z[2][64][kD + 4];  // K and V rows (fp32)
-  uint8_t code[2][64][kD];
-  __half scale[2][64][2];
+// Phase 2b: new tokens that go straight into the INT2 history.
+//
+// x R on the tensor cores: x is a bf16 row, R^T is held as three bf16 terms
+// (R = t0 + t1 + t2 to ~2^-24 relative), and each m16n8k16 product is exact
+// in the MMA.  The t0 products of each 16-channel step land in a fresh
+// accumulator and are summed in fp32 with round-to-nearest, so the tensor
+// core's truncation of its fp32 result does not pile up; the much smaller t1,
+// t2 products share one chained accumulator.  Persistent blocks of 512
+// threads, one per SM, keep the six R^T terms (192 KB) in shared memory and
+// run two tile slots: warps 0..7 and 8..15 each take one (request, KV head,
+// page) tile at a time, K rows on their first four warps and V rows on the
+// last four; each warp owns 16 rows of the tile.
+constexpr int kTcSlots = 2;
+constexpr int kTcThreads = 32 * 8 * kTcSlots;
+
+struct TcSmem {
+  uint16_t rt[2][3][kD][kD];          // [K, V][term][n][k], 16-byte chunks swizzled by n % 8
+  uint8_t code[kTcSlots][2][64][kD];  // codes of the tile being packed
+  __half scale[kTcSlots][2][64][2];
 };
 
-__device__ __forceinline__ void quantize_tile_half(const AppendLaunch& a, int b, int h, int tok0, int p0, int r_lo,
-                                                   int r_hi, int lp, uint8_t* blk, int half, TileSmem& sm) {
-  const bool is_v = half == 1;
-  const int t = threadIdx.x & 127, lane = t & 31, wq = t >> 5, bar = 1 + half;
+__device__ __forceinline__ int rt_index(int n, int k) { return n * kD + ((((k >> 3) ^ (n & 7)) << 3) | (k & 7)); }
+
+// One (request, KV head, page) tile, rows [r_lo, r_hi) of page lp, for the
+// 128 threads of (slot, matrix m) -- m = 0: K, 1: V -- synchronised by named
+// barrier `bar`.
+__device__ __forceinline__ void tc_quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int p0, int r_lo,
+                                                 int r_hi, int lp, uint8_t* blk, int slot, int m, int bar,
+                                                 TcSmem& sm) {
+  const int t = threadIdx.x & 127, lane = t & 31, wq = t >> 5, g = lane >> 2, tq = lane & 3;
   const int Hkv = a.c.num_kv_heads;
-  const uint16_t* src = is_v ? a.v : a.k;
-  const float* __restrict__ R = is_v ? a.rot.R_V : a.rot.R_K;
-  const float tau = is_v ? a.rot.tau_v : a.rot.tau_k;
-  float(*z)[kD + 4] = sm.z[half];
-  // load the tile, 8 channels per load (rows outside [r_lo, r_hi) are zero)
-  for (int i = t; i < 64 * (kD / 8); i += 128) {
-    const int r = i >> 4, c8 = (i & 15) * 8;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (r >= r_lo && r < r_hi) {
-      const int p = lp * kPage + r;
-      u = *reinterpret_cast<const uint4*>(src + ((size_t)(tok0 + p - p0) * Hkv + h) * kD + c8);
-    }
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  const uint16_t* src = m ? a.v : a.k;
+  const float tau = m ? a.rot.tau_v : a.rot.tau_k;
+  // A fragments of this warp's rows 16 wq + {g, g + 8}, all 8 channel steps
+  uint32_t af[8][4];
+  {
+    const int r0 = 16 * wq + g, r1 = r0 + 8;
+    const bool v0 = r0 >= r_lo && r0 < r_hi, v1 = r1 >= r_lo && r1 < r_hi;
+    const uint16_t* x0 = src + ((size_t)(tok0 + lp * kPage + r0 - p0) * Hkv + h) * kD + 2 * tq;
+    const uint16_t* x1 = src + ((size_t)(tok0 + lp * kPage + r1 - p0) * Hkv + h) * kD + 2 * tq;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      z[r][c8 + 2 * k] = __uint_as_float(w[k] << 16);
-      z[r][c8 + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    for (int i = 0; i < 8; ++i) {
+      af[i][0] = v0 ? *reinterpret_cast<const uint32_t*>(x0 + 16 * i) : 0u;
+      af[i][1] = v1 ? *reinterpret_cast<const uint32_t*>(x1 + 16 * i) : 0u;
+      af[i][2] = v0 ? *reinterpret_cast<const uint32_t*>(x0 + 16 * i + 8) : 0u;
+      af[i][3] = v1 ? *reinterpret_cast<const uint32_t*>(x1 + 16 * i + 8) : 0u;
     }
   }
-  half_sync(bar);
-  float acc[16][4];
+  const uint16_t* rtm = &sm.rt[m][0][0][0];
+  // ldmatrix row of this lane: matrix q = lane / 8 covers n-block (pair base + q / 2), k half q % 2
+  const int lq = lane >> 3, lr = lane & 7;
+#pragma unroll 1
+  for (int G = 0; G < 2; ++G) {  // quantisation group: output channels 64 G .. 64 G + 63
+    float run[8][4], chn[8][4];
 #pragma unroll
-  for (int r = 0; r < 16; ++r)
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[r][k] = 0.f;
-#pragma unroll 2
-  for (int i = 0; i < kD; i += 4) {
-    const float4 r0 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 0) * kD) + lane);
-    const float4 r1 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 1) * kD) + lane);
-    const float4 r2 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 2) * kD) + lane);
-    const float4 r3 = __ldg(reinterpret_cast<const float4*>(R + (size_t)(i + 3) * kD) + lane);
+      for (int e = 0; e < 4; ++e) run[j][e] = chn[j][e] = 0.f;
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(&z[16 * wq + r][i]);
-      acc[r][0] = fmaf(x.w, r3.x, fmaf(x.z, r2.x, fmaf(x.y, r1.x, fmaf(x.x, r0.x, acc[r][0]))));
-      acc[r][1] = fmaf(x.w, r3.y, fmaf(x.z, r2.y, fmaf(x.y, r1.y, fmaf(x.x, r0.y, acc[r][1]))));
-      acc[r][2] = fmaf(x.w, r3.z, fmaf(x.z, r2.z, fmaf(x.y, r1.z, fmaf(x.x, r0.z, acc[r][2]))));
-      acc[r][3] = fmaf(x.w, r3.w, fmaf(x.z, r2.w, fmaf(x.y, r1.w, fmaf(x.x, r0.w, acc[r][3]))));
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {
+        const int n = 64 * G + 16 * jp + 8 * (lq >> 1) + lr, k = 16 * i + 8 * (lq & 1);
+        const int off = rt_index(n, k);
+        uint32_t b[4];
+        ldmatrix_x4(b[0], b[1], b[2], b[3], rtm + off);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float f[4];
+          mma_bf16(f, af[i], b[2 * q], b[2 * q + 1], zero);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) run[2 * jp + q][e] += f[e];
+        }
+#pragma unroll
+        for (int term = 1; term < 3; ++term) {
+          ldmatrix_x4(b[0], b[1], b[2], b[3], rtm + term * kD * kD + off);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) mma_bf16(chn[2 * jp + q], af[i], b[2 * q], b[2 * q + 1], chn[2 * jp + q]);
+        }
+      }
     }
-  }
+    // x' of rows 16 wq + g (elements 0, 1) and + 8 (2, 3), channels 64 G + 8 j + 2 tq + {0, 1}
+    float mx0 = 0.f, mx1 = 0.f;
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const int row = 16 * wq + r;
-    const float v[4] = {acc[r][0], acc[r][1], acc[r][2], acc[r][3]};
-    // group absmax: channels 0..63 on lanes 0..15, 64..127 on lanes 16..31
-    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    for (int j = 0; j < 8; ++j) {
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float aa = fminf(m, tau);
-    const __half sh = __float2half_rn(aa / 1.5f);
-    const float sc = __half2float(sh);
-    uint32_t packed = 0;
+      for (int e = 0; e < 4; ++e) run[j][e] += chn[j][e];
+      mx0 = fmaxf(mx0, fmaxf(fabsf(run[j][0]), fabsf(run[j][1])));
+      mx1 = fmaxf(mx1, fmaxf(fabsf(run[j][2]), fabsf(run[j][3])));
+    }
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      packed |= (uint32_t)((v[k] >= -sc) + (v[k] >= 0.f) + (v[k] >= sc)) << (8 * k);
-    *reinterpret_cast<uint32_t*>(&sm.code[half][row][4 * lane]) = packed;
-    if ((lane & 15) == 0) sm.scale[half][row][lane >> 4] = sh;
+    for (int o = 1; o < 4; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const __half h0 = __float2half_rn(fminf(mx0, tau) / 1.5f), h1 = __float2half_rn(fminf(mx1, tau) / 1.5f);
+    const float s0 = __half2float(h0), s1 = __half2float(h1);
+    const int row0 = 16 * wq + g, row1 = row0 + 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int ch = 64 * G + 8 * j + 2 * tq;
+      const float* v = run[j];
+      sm.code[slot][m][row0][ch] = (uint8_t)((v[0] >= -s0) + (v[0] >= 0.f) + (v[0] >= s0));
+      sm.code[slot][m][row0][ch + 1] = (uint8_t)((v[1] >= -s0) + (v[1] >= 0.f) + (v[1] >= s0));
+      sm.code[slot][m][row1][ch] = (uint8_t)((v[2] >= -s1) + (v[2] >= 0.f) + (v[2] >= s1));
+      sm.code[slot][m][row1][ch + 1] = (uint8_t)((v[3] >= -s1) + (v[3] >= 0.f) + (v[3] >= s1));
+    }
+    if (tq == 0) {
+      sm.scale[slot][m][row0][G] = h0;
+      sm.scale[slot][m][row1][G] = h1;
+    }
   }
   half_sync(bar);
   // pack the rows in [r_lo, r_hi) only: other rows of this page may hold
@@ -211,48 +251,67 @@ __device__ __forceinline__ void quantize_tile_half(const AppendLaunch& a, int b,
   for (int i = t; i < 64 * 8; i += 128) {
     const int row = i >> 3, w = i & 7;
     if (row < r_lo || row >= r_hi) continue;
-    if (!is_v) {
-      const int tig = w & 3, g = w >> 2, base = 64 * g + 16 * tig;
+    const uint8_t* cr = sm.code[slot][m][row];
+    if (m == 0) {
+      const int tig = w & 3, gg = w >> 2, base = 64 * gg + 16 * tig;
       uint32_t word = 0;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        word |= (uint32_t)sm.code[0][row][base + r] << (2 * r);
-        word |= (uint32_t)sm.code[0][row][base + 8 + r] << (16 + 2 * r);
+        word |= (uint32_t)cr[base + r] << (2 * r);
+        word |= (uint32_t)cr[base + 8 + r] << (16 + 2 * r);
       }
-      *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, tig, g)) = word;
+      *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, tig, gg)) = word;
     } else {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int jj = 2 * w + hh;
         uint32_t hv = 0;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[1][row][jj + 16 * r] << (2 * r);
+        for (int r = 0; r < 8; ++r) hv |= (uint32_t)cr[jj + 16 * r] << (2 * r);
         *reinterpret_cast<uint16_t*>(blk + kVCodes + v_half_offset(row, jj)) = (uint16_t)hv;
       }
     }
   }
-  for (int i = t; i < 64 * 2; i += 128) {
-    const int row = i >> 1, g = i & 1;
-    if (row < r_lo || row >= r_hi) continue;
-    *reinterpret_cast<__half*>(blk + (is_v ? kVScales : kKScales) + 4 * row + 2 * g) = sm.scale[half][row][g];
+  {
+    const int row = t >> 1, gg = t & 1;
+    if (row >= r_lo && row < r_hi)
+      *reinterpret_cast<__half*>(blk + (m ? kVScales : kKScales) + 4 * row + 2 * gg) = sm.scale[slot][m][row][gg];
   }
+  half_sync(bar);  // the staging is reused by this slot's next tile
 }
 
-__global__ void __launch_bounds__(256, 2) append_tile_kernel(AppendLaunch a) {
+__global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch a, int tiles_per_req) {
   extern __shared__ __align__(16) uint8_t tile_smem_raw[];
-  TileSmem& sm = *reinterpret_cast<TileSmem*>(tile_smem_raw);
-  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  int p0, n, tok0;
-  if (!request_span(a, b, p0, n, tok0)) return;
-  const int L = p0 + n;
-  const int lo = max(p0, kSink), hi = L - kRecent;
-  if (hi <= lo) return;
-  const int lp = lo / kPage + x;
-  if (lp * kPage >= hi) return;
-  const int r_lo = max(lo - lp * kPage, 0), r_hi = min(hi - lp * kPage, kPage);
-  uint8_t* blk = history_block(a.c, b, h, lp * kPage, a.err);
-  if (blk == nullptr) return;
-  quantize_tile_half(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, threadIdx.x >> 7, sm);
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(tile_smem_raw);
+  // the six R^T terms into shared memory, 16-byte chunks swizzled
+  {
+    const uint4* srcv = reinterpret_cast<const uint4*>(a.rot.RT_split);
+    constexpr int kChunks = 2 * 3 * kD * kD / 8;
+    for (int c = threadIdx.x; c < kChunks; c += kTcThreads) {
+      const int row = c >> 4, chunk = c & 15, n = row & (kD - 1);
+      reinterpret_cast<uint4*>(&sm.rt[0][0][0][0])[(row << 4) | (chunk ^ (n & 7))] = __ldg(srcv + c);
+    }
+  }
+  __syncthreads();
+  const int slot = threadIdx.x / 256, m = (threadIdx.x >> 7) & 1, bar = 1 + 2 * slot + m;
+  const int Hkv = a.c.num_kv_heads;
+  const long long n_tiles = (long long)tiles_per_req * Hkv * a.c.batch;
+  for (long long tile = (long long)blockIdx.x * kTcSlots + slot; tile < n_tiles; tile += (long long)gridDim.x * kTcSlots) {
+    const int x = (int)(tile % tiles_per_req);
+    const int h = (int)((tile / tiles_per_req) % Hkv);
+    const int b = (int)(tile / ((long long)tiles_per_req * Hkv));
+    int p0, n, tok0;
+    if (!request_span(a, b, p0, n, tok0)) continue;
+    const int L = p0 + n;
+    const int lo = max(p0, kSink), hi = L - kRecent;
+    if (hi <= lo) continue;
+    const int lp = lo / kPage + x;
+    if (lp * kPage >= hi) continue;
+    const int r_lo = max(lo - lp * kPage, 0), r_hi = min(hi - lp * kPage, kPage);
+    uint8_t* blk = history_block(a.c, b, h, lp * kPage, a.err);
+    if (blk == nullptr) continue;
+    tc_quantize_tile(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, slot, m, bar, sm);
+  }
 }
 
 }  // namespace
@@ -265,15 +324,21 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   }
   if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 256, 0, stream>>>(a);
   append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
-  const int tiles = (a.max_tokens_per_req + kPage - 1) / kPage + 1;
-  const size_t smem = sizeof(TileSmem);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(append_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int tiles = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
+  const size_t smem = sizeof(TcSmem);
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, n_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(append_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    sms = n_sm;
   }
-  append_tile_kernel<<<dim3(tiles, Hkv, B), 256, smem, stream>>>(a);
+  const long long work = (long long)tiles * Hkv * B;
+  const int blocks = (int)std::min<long long>((work + kTcSlots - 1) / kTcSlots, (long long)sms);
+  append_tile_kernel<<<blocks, kTcThreads, smem, stream>>>(a, tiles);
   return cudaGetLastError();
 }
 

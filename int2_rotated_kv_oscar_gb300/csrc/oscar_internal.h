@@ -15,6 +15,9 @@ struct LayerRotation {
   const float* R_K = nullptr;   // [128][128] row-major: a K row x is rotated as x R_K
   const float* R_V = nullptr;   // [128][128] row-major
   const float* R_VT = nullptr;  // [128][128] = R_V transposed (inverse rotation of outputs)
+  // bf16 bit patterns [2 (K, V)][3][128 n][128 k]: R[k][n] = sum of the three
+  // terms up to ~2^-24 relative (the bulk append's tensor-core operand)
+  const uint16_t* RT_split = nullptr;
   float tau_k = 0.f, tau_v = 0.f;
 };
 
