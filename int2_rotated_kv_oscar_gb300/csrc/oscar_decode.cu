@@ -129,9 +129,10 @@ struct PrepArgs {
 // global memory.
 //
 // Fragment words per (request, KV head): [32 lanes][32].  The MMA B column of
-// lane L is n = L / 4.  With g <= 4 ("packed"), column n carries head n % 4
-// and part n / 4 (0: fp16 value, 1: fp16 residual) in words 0..15; with
-// g > 4 column n is head n, words 0..15 hold the values and 16..31 the
+// lane L is n = L / 4.  With g <= 4 ("packed"), column n carries head n / 2
+// and part n % 2 (0: fp16 value, 1: fp16 residual) in words 0..15, so that
+// the accumulator lane holding columns 2 h and 2 h + 1 holds all of head h;
+// with g > 4 column n is head n, words 0..15 hold the values and 16..31 the
 // residuals.
 struct PrepSmem {
   __align__(16) float xs[kMaxG][kD];
@@ -200,8 +201,8 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t
   for (int e = t; e < kQFragWords; e += 128) {
     const int L = e >> 5, w = e & 31, set = w >> 4, ww = w & 15, i = ww >> 1, bs = ww & 1;
     const int n = L >> 2, tig = L & 3;
-    const int head = packed ? (n & 3) : n;
-    const int part = packed ? (n >> 2) : set;
+    const int head = packed ? (n >> 1) : n;
+    const int part = packed ? (n & 1) : set;
     uint32_t vr = 0, vp = 0;
     if (head < g && !(packed && set == 1)) {
       const int grp = i >> 2, r = 2 * (i & 3) + bs;
@@ -339,6 +340,29 @@ __device__ __forceinline__ void online_max(WarpState& st, float mx0, float mx1) 
   }
 }
 
+// Packed mode: the lane's two accumulator columns are one head's value and
+// residual parts, so a single running maximum covers all its accumulators.
+__device__ __forceinline__ void online_max1(WarpState& st, float mx) {
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (__any_sync(0xffffffffu, mx > st.m[0] + kLazy)) {
+    const float nm = fmaxf(st.m[0], mx);
+    const float al = (nm == -INFINITY) ? 1.f : ex2(st.m[0] - nm);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) st.acc[i][k] *= al;
+    st.l[0] *= al;
+    st.m[0] = nm;
+  }
+}
+
+// x as an fp16 pair (value, residual): the value in the low half
+__device__ __forceinline__ uint32_t value_residual(float x) {
+  const float hi = __half2float(__float2half_rn(x));
+  return pack_f16x2(x, x - hi);
+}
+
 // Fold one partial softmax state (m, l, acc slice) into a running one.
 __device__ __forceinline__ void merge_record(float& m, float& l, float4& acc, float mx, float lx, float4 v) {
   const float M = fmaxf(m, mx);
@@ -363,14 +387,6 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = pack_f16x2(x0 - h.x, x1 - h.y);
 }
 
-// packed mode: lanes holding value columns take the fp16 value, lanes holding
-// residual columns (tig >= 2) take the residual
-__device__ __forceinline__ uint32_t pick_pair(float x0, float x1, bool residual) {
-  uint32_t hi, lo;
-  split_pair(x0, x1, hi, lo);
-  return residual ? lo : hi;
-}
-
 // One 64-token INT2 page (NT = 4) or its 16-token tile T0 (NT = 1), K and V
 // codes + scales staged in shared memory at their block offsets.
 // FULL: all 64 rows valid (no masking).  The softmax weights come out scaled
@@ -379,8 +395,7 @@ template <bool PACK4, bool FULL, int NT>
 __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n_valid, int T0, const uint32_t* qf,
                                           float scaleE, float kp, WarpState& st, int lane) {
   const int q = lane >> 2;
-  const bool resid = (lane & 3) >= 2;
-  float lg[NT][4];
+  float lg[NT][4];  // packed: [0] token q, [1] token q + 8 of head lane % 4
 #pragma unroll
   for (int i = 0; i < NT; ++i) {
     const int T = NT == 4 ? i : T0;
@@ -416,16 +431,17 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
       OSCAR_QK(d1, x, y, 6, 7);
     }
 #undef OSCAR_QK
-    float l0 = fmaf(d0[0], sa.x, d1[0] * sa.y) * scaleE;
-    float l1 = fmaf(d0[1], sa.x, d1[1] * sa.y) * scaleE;
-    float l2 = fmaf(d0[2], sb.x, d1[2] * sb.y) * scaleE;
-    float l3 = fmaf(d0[3], sb.x, d1[3] * sb.y) * scaleE;
-    if (PACK4) {  // value column + residual column
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      l2 += __shfl_xor_sync(0xffffffffu, l2, 2);
-      l3 += __shfl_xor_sync(0xffffffffu, l3, 2);
+    if constexpr (PACK4) {  // columns 2 h, 2 h + 1: value and residual parts of head h = lane % 4
+      const float lq = fmaf(d0[0] + d0[1], sa.x, (d1[0] + d1[1]) * sa.y) * scaleE;
+      const float lq8 = fmaf(d0[2] + d0[3], sb.x, (d1[2] + d1[3]) * sb.y) * scaleE;
+      lg[i][0] = (FULL || 16 * T + q < n_valid) ? lq : -INFINITY;
+      lg[i][1] = (FULL || 16 * T + q + 8 < n_valid) ? lq8 : -INFINITY;
+      continue;
     }
+    const float l0 = fmaf(d0[0], sa.x, d1[0] * sa.y) * scaleE;
+    const float l1 = fmaf(d0[1], sa.x, d1[1] * sa.y) * scaleE;
+    const float l2 = fmaf(d0[2], sb.x, d1[2] * sb.y) * scaleE;
+    const float l3 = fmaf(d0[3], sb.x, d1[3] * sb.y) * scaleE;
     if (FULL) {
       lg[i][0] = l0;
       lg[i][1] = l1;
@@ -438,6 +454,47 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
       lg[i][2] = vb ? l2 : -INFINITY;
       lg[i][3] = vb ? l3 : -INFINITY;
     }
+  }
+  if constexpr (PACK4) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) mx = fmaxf(mx, fmaxf(lg[i][0], lg[i][1]));
+    online_max1(st, mx);
+    const float ms = st.m[0] - kp;  // weights p 2^kp
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const int T = NT == 4 ? i : T0;
+      if (!FULL && 16 * T >= n_valid) continue;
+      const float pq = ex2(lg[i][0] - ms), pq8 = ex2(lg[i][1] - ms);
+      st.l[0] += pq + pq8;
+      float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
+      float2 sb = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q + 8)));
+      if (!FULL) {  // rows past the history end may hold anything
+        const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
+        sa.x = va ? sa.x : 0.f;
+        sa.y = va ? sa.y : 0.f;
+        sb.x = vb ? sb.x : 0.f;
+        sb.y = vb ? sb.y : 0.f;
+      }
+      const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVCodes + 512 * T + 16 * lane);
+      const CodeWord w0(vw.x), w1(vw.y), w2(vw.z), w3(vw.w);
+      const uint32_t b00 = movmatrix_trans(value_residual(pq * sa.x));
+      const uint32_t b01 = movmatrix_trans(value_residual(pq8 * sb.x));
+      const uint32_t b10 = movmatrix_trans(value_residual(pq * sa.y));
+      const uint32_t b11 = movmatrix_trans(value_residual(pq8 * sb.y));
+#define OSCAR_PV(M, B0, B1) \
+  mma_f16(st.acc[M], code_level<M>(w0), code_level<M>(w1), code_level<M>(w2), code_level<M>(w3), B0, B1)
+      OSCAR_PV(0, b00, b01);
+      OSCAR_PV(1, b00, b01);
+      OSCAR_PV(2, b00, b01);
+      OSCAR_PV(3, b00, b01);
+      OSCAR_PV(4, b10, b11);
+      OSCAR_PV(5, b10, b11);
+      OSCAR_PV(6, b10, b11);
+      OSCAR_PV(7, b10, b11);
+#undef OSCAR_PV
+    }
+    return;
   }
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -466,23 +523,7 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
     }
     const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVCodes + 512 * T + 16 * lane);
     const CodeWord w0(vw.x), w1(vw.y), w2(vw.z), w3(vw.w);
-    if (PACK4) {
-      const uint32_t b00 = movmatrix_trans(pick_pair(p0 * sa.x, p1 * sa.x, resid));
-      const uint32_t b01 = movmatrix_trans(pick_pair(p2 * sb.x, p3 * sb.x, resid));
-      const uint32_t b10 = movmatrix_trans(pick_pair(p0 * sa.y, p1 * sa.y, resid));
-      const uint32_t b11 = movmatrix_trans(pick_pair(p2 * sb.y, p3 * sb.y, resid));
-#define OSCAR_PV(M, B0, B1) \
-  mma_f16(st.acc[M], code_level<M>(w0), code_level<M>(w1), code_level<M>(w2), code_level<M>(w3), B0, B1)
-      OSCAR_PV(0, b00, b01);
-      OSCAR_PV(1, b00, b01);
-      OSCAR_PV(2, b00, b01);
-      OSCAR_PV(3, b00, b01);
-      OSCAR_PV(4, b10, b11);
-      OSCAR_PV(5, b10, b11);
-      OSCAR_PV(6, b10, b11);
-      OSCAR_PV(7, b10, b11);
-#undef OSCAR_PV
-    } else {
+    {
       uint32_t h00, l00, h01, l01, h10, l10, h11, l11;
       split_pair(p0 * sa.x, p1 * sa.x, h00, l00);
       split_pair(p2 * sb.x, p3 * sb.x, h01, l01);
@@ -522,7 +563,6 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
                                           int n_valid, const uint32_t* qpf, float scaleEp, WarpState& st,
                                           int lane) {
   const int q = lane >> 2, tig = lane & 3;
-  const bool resid = tig >= 2;
   const bool va = q < n_valid, vb = q + 8 < n_valid;
   uint32_t ka[16], kb[16];
 #pragma unroll
@@ -544,13 +584,20 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
     mma_f16(d, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[2 * ks], qpf[2 * ks + 1]);
     if (!PACK4) mma_f16(d, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qpf[16 + 2 * ks], qpf[17 + 2 * ks]);
   }
+  uint32_t b0h, b0l, b1h, b1l;
+  if constexpr (PACK4) {  // columns 2 h, 2 h + 1: value and residual parts of head h = lane % 4
+    const float lq = va ? (d[0] + d[1]) * scaleEp : -INFINITY;
+    const float lq8 = vb ? (d[2] + d[3]) * scaleEp : -INFINITY;
+    online_max1(st, fmaxf(lq, lq8));
+    // weights scaled by 2^11 (kPScaleBF16) through the exponent
+    const float ms = st.m[0] - 11.f;
+    const float pq = ex2(lq - ms), pq8 = ex2(lq8 - ms);
+    st.l[0] += pq + pq8;
+    b0h = movmatrix_trans(value_residual(pq));
+    b1h = movmatrix_trans(value_residual(pq8));
+    b0l = b1l = 0u;
+  } else {
   float l0 = d[0] * scaleEp, l1 = d[1] * scaleEp, l2 = d[2] * scaleEp, l3 = d[3] * scaleEp;
-  if (PACK4) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    l2 += __shfl_xor_sync(0xffffffffu, l2, 2);
-    l3 += __shfl_xor_sync(0xffffffffu, l3, 2);
-  }
   l0 = va ? l0 : -INFINITY;
   l1 = va ? l1 : -INFINITY;
   l2 = vb ? l2 : -INFINITY;
@@ -561,18 +608,12 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
   const float p0 = ex2(l0 - ms0), p1 = ex2(l1 - ms1), p2 = ex2(l2 - ms0), p3 = ex2(l3 - ms1);
   st.l[0] += p0 + p2;
   st.l[1] += p1 + p3;
-  uint32_t b0h, b0l, b1h, b1l;
-  if (PACK4) {
-    b0h = movmatrix_trans(pick_pair(p0, p1, resid));
-    b1h = movmatrix_trans(pick_pair(p2, p3, resid));
-    b0l = b1l = 0u;
-  } else {
-    split_pair(p0, p1, b0h, b0l);
-    split_pair(p2, p3, b1h, b1l);
-    b0h = movmatrix_trans(b0h);
-    b0l = movmatrix_trans(b0l);
-    b1h = movmatrix_trans(b1h);
-    b1l = movmatrix_trans(b1l);
+  split_pair(p0, p1, b0h, b0l);
+  split_pair(p2, p3, b1h, b1l);
+  b0h = movmatrix_trans(b0h);
+  b0l = movmatrix_trans(b0l);
+  b1h = movmatrix_trans(b1h);
+  b1l = movmatrix_trans(b1l);
   }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
@@ -592,7 +633,8 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
 }
 
 // A warp's state as written to its own stage memory: m[8], l[8], acc[8][128].
-// inv undoes the B-operand scaling; packed mode adds the residual columns.
+// inv undoes the B-operand scaling; packed mode adds each head's residual
+// column to its value column.
 template <bool PACK4>
 __device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv, int lane) {
   const int q = lane >> 2, tig = lane & 3;
@@ -601,8 +643,19 @@ __device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv
     st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
     st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
   }
-  const bool writer = PACK4 ? (tig < 2) : true;  // packed: columns 4..7 hold residuals of heads 0..3
-  if (q == 0 && writer) {
+  if constexpr (PACK4) {  // lane: head tig; columns 2 tig, 2 tig + 1 are its value and residual parts
+    if (q == 0) {
+      dst[tig] = st.m[0];
+      dst[8 + tig] = st.l[0] * inv;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      dst[16 + tig * kD + 16 * mt + q] = (st.acc[mt][0] + st.acc[mt][1]) * inv;
+      dst[16 + tig * kD + 16 * mt + q + 8] = (st.acc[mt][2] + st.acc[mt][3]) * inv;
+    }
+    return;
+  }
+  if (q == 0) {
     dst[2 * tig] = st.m[0];
     dst[2 * tig + 1] = st.m[1];
     dst[8 + 2 * tig] = st.l[0] * inv;
@@ -613,9 +666,7 @@ __device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ch = 16 * mt + q + 8 * (i >> 1), n = 2 * tig + (i & 1);
-      float v = st.acc[mt][i] * inv;
-      if (PACK4) v += __shfl_xor_sync(0xffffffffu, v, 2);
-      if (writer) dst[16 + n * kD + ch] = v;
+      dst[16 + n * kD + ch] = st.acc[mt][i] * inv;
     }
   }
 }
