@@ -141,6 +141,27 @@ struct PrepSmem {
   float red[8];
 };
 
+// z[n] = (q_n R_K)[t] for the first G heads of sm.xs (two partial sums per
+// head so that the shared-memory loads and the multiply-adds overlap).
+template <int G>
+__device__ __forceinline__ void rotate_heads(const PrepSmem& sm, const float* __restrict__ RK, int t, float (&z)[kMaxG]) {
+  float za[G], zb[G];
+#pragma unroll
+  for (int n = 0; n < G; ++n) za[n] = zb[n] = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < kD; i += 4) {
+    const float r0 = RK[i * kD + t], r1 = RK[(i + 1) * kD + t], r2 = RK[(i + 2) * kD + t], r3 = RK[(i + 3) * kD + t];
+#pragma unroll
+    for (int n = 0; n < G; ++n) {
+      const float4 x = *reinterpret_cast<const float4*>(&sm.xs[n][i]);
+      za[n] = fmaf(x.y, r1, fmaf(x.x, r0, za[n]));
+      zb[n] = fmaf(x.w, r3, fmaf(x.z, r2, zb[n]));
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < kMaxG; ++n) z[n] = n < G ? za[n] + zb[n] : 0.f;
+}
+
 __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t, const float* __restrict__ RK,
                                           PrepSmem& sm, int bar) {
   const int lane = t & 31, warp = t >> 5;
@@ -148,21 +169,16 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t
   const bool packed = g <= 4;
   if (t == 0) a.counters[bh] = 0;
   const float c = a.sm_scale * kLog2e;
-  for (int n = 0; n < g; ++n) sm.xs[n][t] = bf16_bits_to_float(a.q[((size_t)b * a.Hq + h * g + n) * kD + t]);
+  // heads g .. G - 1 of the padded set are zero (G = 4 when g <= 4, else 8)
+  const int G = packed ? 4 : kMaxG;
+  for (int n = 0; n < G; ++n)
+    sm.xs[n][t] = n < g ? bf16_bits_to_float(a.q[((size_t)b * a.Hq + h * g + n) * kD + t]) : 0.f;
   half_sync(bar);
   float z[kMaxG];
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n) z[n] = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < kD; i += 4) {
-    const float r0 = RK[i * kD + t], r1 = RK[(i + 1) * kD + t], r2 = RK[(i + 2) * kD + t], r3 = RK[(i + 3) * kD + t];
-#pragma unroll
-    for (int n = 0; n < kMaxG; ++n)
-      if (n < g) {
-        const float4 x = *reinterpret_cast<const float4*>(&sm.xs[n][i]);
-        z[n] = fmaf(x.x, r0, fmaf(x.y, r1, fmaf(x.z, r2, fmaf(x.w, r3, z[n]))));
-      }
-  }
+  if (packed)
+    rotate_heads<4>(sm, RK, t, z);
+  else
+    rotate_heads<kMaxG>(sm, RK, t, z);
   // power-of-two normalisations: max |q'| 2^-E <= 2^10, max |q| 2^-Ep <= 2^10
   float mr = 0.f, mp = 0.f;
 #pragma unroll
