@@ -282,6 +282,8 @@ __global__ void __launch_bounds__(384, 1) step_kernel(AppendLaunch ap, PrepArgs 
       const size_t r = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + 64 * (lane & 1);
       prefetch_l2(((lane & 2) ? ap.c.v_ring : ap.c.k_ring) + r);
     }
+    if (lane == 27 && p >= kSink + kRecent && ((p - kRecent) >> 6) < ap.c.max_pages)  // its page-table entry
+      prefetch_l2(ap.c.page_table + (size_t)b * ap.c.max_pages + ((p - kRecent) >> 6));
   }
   __syncthreads();
   griddep_wait();

@@ -113,7 +113,9 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
   const bool is_v = half == 1;
   const CacheRefs& c = a.c;
   const int Hkv = c.num_kv_heads;
+  // independent loads first, so that their round trips overlap
   const int p = a.pos[b];
+  const int slot = c.ring_slot[b];
   const uint16_t xn = (is_v ? a.v : a.k)[((size_t)b * Hkv + h) * kD + t];
   if (p < 0 || ((a.flags & 1u) && p > kSink)) {
     if (threadIdx.x == 0) set_error(a.err, kErrLength);
@@ -128,7 +130,6 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
     (is_v ? c.v_sink : c.k_sink)[(((size_t)sp * Hkv + h) * kSink + p) * kD + t] = xn;
     return;
   }
-  const int slot = c.ring_slot[b];
   if (slot < 0 || slot >= c.num_ring) {
     if (threadIdx.x == 0) set_error(a.err, kErrRing);
     return;
@@ -138,11 +139,11 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
   if (p >= kSink + kRecent) {
     // the token at e = p - 256 leaves the window: same ring row, read before overwrite
     const int e = p - kRecent;
+    const uint16_t xo = ring[rdst];  // in flight while the page table is read
     uint8_t* blk = history_block(c, b, h, e, a.err);
-    if (blk != nullptr) {
-      const float x = bf16_bits_to_float(ring[rdst]);
-      quantize_token(x, is_v ? Rv : Rk, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm);
-    }
+    if (blk != nullptr)
+      quantize_token(bf16_bits_to_float(xo), is_v ? Rv : Rk, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v,
+                     sm);
   }
   ring[rdst] = xn;
 }
