@@ -56,8 +56,8 @@ extern "C" {
  *   [2304, 4352)  V codes      [4352, 4608)  V scales fp16 [64 tokens][2 groups]
  * Codes come in 16-token tiles of 512 bytes (tile T = t / 16 at byte 512*T of
  * the code area).  With u = t % 16, the 2-bit code of rotated channel j is at
- *   K: lane = 4*(u%8) + (j%64)/16, word = 2*(u/8) + j/64,
- *      bit  = 16*((j%16)/8) + 2*(j%8)
+ *   K: lane = 4*(u%8) + (j/4)%4,   word = 2*(u/8) + j/64,
+ *      bit  = 8*(j%4) + 2*(2*((j/32)%2) + (j/16)%2)
  *   V: lane = 4*(j%8) + (u%8)/2,   word = 2*(u/8) + (j%16)/8,
  *      bit  = 16*(u%2) + 2*(j/16)
  *   byte = 512*T + 16*lane + 4*word + bit/8, bit-in-byte = bit%8

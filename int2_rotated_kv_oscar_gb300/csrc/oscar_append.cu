@@ -253,14 +253,7 @@ __device__ __forceinline__ void tc_quantize_tile(const AppendLaunch& a, int b, i
     if (row < r_lo || row >= r_hi) continue;
     const uint8_t* cr = sm.code[slot][m][row];
     if (m == 0) {
-      const int tig = w & 3, gg = w >> 2, base = 64 * gg + 16 * tig;
-      uint32_t word = 0;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        word |= (uint32_t)cr[base + r] << (2 * r);
-        word |= (uint32_t)cr[base + 8 + r] << (16 + 2 * r);
-      }
-      *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, tig, gg)) = word;
+      *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, w & 3, w >> 2)) = k_word(cr, w & 3, w >> 2);
     } else {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {

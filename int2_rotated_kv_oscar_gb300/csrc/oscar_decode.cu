@@ -209,8 +209,10 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t
     ep -= 10;
   }
   const float sr = ldexpf(1.f, -er), sp = ldexpf(1.f, -ep);
-  // QK B fragments over the INT2 history: MMA i (group i / 4, r0 = 2 (i % 4))
-  // takes b0 = q'[64 grp + 16 tig + {0, 8} + r0] and b1 = the same at r0 + 1.
+  // QK B fragments over the INT2 history: MMA i reads the code pairs at
+  // in-half position 2 R, R = 2 (i % 4) (b0) and R + 1 (b1), of word i / 4
+  // (ks = 2 (i / 4) + (i % 4) % 2, byte parity pb = (i % 4) / 2), i.e.
+  // channels 32 ks + 16 bs + 4 tig + pb and + 2 for b_bs.
   // BF16 segment: MMA ks = i takes channels 32 tig + 4 ks + {0,1} (b0) and {2,3} (b1).
   uint32_t* qf = a.qfrag + (size_t)bh * kQFragWords;
   uint32_t* qpl = a.qplain + (size_t)bh * kQFragWords;
@@ -221,9 +223,10 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t
     const int part = packed ? (n & 1) : set;
     uint32_t vr = 0, vp = 0;
     if (head < g && !(packed && set == 1)) {
-      const int grp = i >> 2, r = 2 * (i & 3) + bs;
-      const int ch = 64 * grp + 16 * tig + r;
-      vr = pack_f16x2(split_part(sm.qr[head][ch] * sr, part), split_part(sm.qr[head][ch + 8] * sr, part));
+      // MMA i of the history: group i / 4, channel step ks, byte parity pb (see the K layout)
+      const int ii = i & 3, ks = 2 * (i >> 2) + (ii & 1), pb = ii >> 1;
+      const int ch = 32 * ks + 16 * bs + 4 * tig + pb;
+      vr = pack_f16x2(split_part(sm.qr[head][ch] * sr, part), split_part(sm.qr[head][ch + 2] * sr, part));
       const int cp = 32 * tig + 4 * i + 2 * bs;
       vp = pack_f16x2(split_part(sm.qp[head][cp] * sp, part), split_part(sm.qp[head][cp + 1] * sp, part));
     }

@@ -15,11 +15,26 @@
 namespace oscar {
 namespace {
 
-// Byte offset inside a block's K code area of the 32-bit word holding the
-// codes of (row t, quarter tig, group grp).
-__device__ __forceinline__ int k_word_offset(int t, int tig, int grp) {
+// K codes of a 16-token tile: the 32-bit word (lane 4 (u % 8) + tq, word
+// 2 (u / 8) + kp) of row u holds channels j = 32 ks + 16 kh + 4 tq + b for
+// ks in {2 kp, 2 kp + 1}, kh, b in 0..3 at bit 8 b + 2 (2 (ks % 2) + kh).
+// Byte offset inside a block's K code area of that word for row t.
+__device__ __forceinline__ int k_word_offset(int t, int tq, int kp) {
   const int T = t >> 4, u = t & 15;
-  return 512 * T + 16 * (4 * (u & 7) + tig) + 4 * (2 * (u >> 3) + grp);
+  return 512 * T + 16 * (4 * (u & 7) + tq) + 4 * (2 * (u >> 3) + kp);
+}
+
+// The K word (tq, kp) of one row from its 128 codes (one byte each).
+__device__ __forceinline__ uint32_t k_word(const uint8_t* codes, int tq, int kp) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int ks2 = 0; ks2 < 2; ++ks2)
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        w |= (uint32_t)codes[32 * (2 * kp + ks2) + 16 * kh + 4 * tq + b] << (8 * b + 2 * (2 * ks2 + kh));
+  return w;
 }
 
 // Byte offset inside a block's V code area of the 16-bit half holding the
@@ -66,16 +81,8 @@ __device__ __forceinline__ void quantize_token(float x, const float* __restrict_
   sm.code[t] = (uint8_t)((z >= -s) + (z >= 0.f) + (z >= s));
   half_sync(bar);
   if (!is_v) {
-    if (t < 8) {
-      const int tig = t & 3, g = t >> 2, base = 64 * g + 16 * tig;
-      uint32_t w = 0;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        w |= (uint32_t)sm.code[base + r] << (2 * r);
-        w |= (uint32_t)sm.code[base + 8 + r] << (16 + 2 * r);
-      }
-      *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, tig, g)) = w;
-    }
+    if (t < 8)
+      *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, t & 3, t >> 2)) = k_word(sm.code, t & 3, t >> 2);
   } else {
     if (t < 16) {
       uint32_t hv = 0;

@@ -19,9 +19,9 @@ Codes are grouped in 16-token tiles of 512 bytes (tile T = t // 16 starts at
 byte 512 T of the code area).  Inside a tile, with u = t % 16, the 2-bit code
 of rotated channel j sits at
 
-    K:  lane  = 4 (u % 8) + (j % 64) // 16
+    K:  lane  = 4 (u % 8) + (j // 4) % 4
         word  = 2 (u // 8) + j // 64
-        bit   = 16 ((j % 16) // 8) + 2 (j % 8)
+        bit   = 8 (j % 4) + 2 (2 ((j // 32) % 2) + (j // 16) % 2)
     V:  lane  = 4 (j % 8) + (u % 8) // 2
         word  = 2 (u // 8) + (j % 16) // 8
         bit   = 16 (u % 2) + 2 (j // 16)
@@ -50,9 +50,9 @@ BLOCK_BYTES = 4608
 def k_code_position(t, j):
     """(byte, bit-in-byte) of the K code of token t (0..63), channel j (0..127)."""
     T, u = divmod(t, 16)
-    lane = 4 * (u % 8) + (j % 64) // 16
+    lane = 4 * (u % 8) + (j // 4) % 4
     word = 2 * (u // 8) + j // 64
-    bit = 16 * ((j % 16) // 8) + 2 * (j % 8)
+    bit = 8 * (j % 4) + 2 * (2 * ((j // 32) % 2) + (j // 16) % 2)
     return 512 * T + 16 * lane + 4 * word + bit // 8, bit % 8
 
 
