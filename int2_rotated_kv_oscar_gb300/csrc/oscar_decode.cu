@@ -56,7 +56,10 @@ constexpr int kPrefetchPages = 1;        // pages per warp pulled into L2 before
 constexpr int kBf16Slots = 2;            // warps per work item that attend BF16 tiles (mixed cache)
 // dynamic shared memory: kStages bulk-copy stages per warp, their mbarriers (+1
 // for the final merge), then the BF16 warps' finished states
-constexpr size_t kSlotsOffset = ((size_t)kWarps * kStages * kBlockBytes + (size_t)(kWarps * kStages + 1) * 8 + 15) / 16 * 16;          // merged state of one warp: acc[128], m, l (16-byte rows)
+constexpr size_t kSlotsOffset = ((size_t)kWarps * kStages * kBlockBytes + (size_t)(kWarps * (kStages + 1) + 1) * 8 + 15) / 16 * 16;
+// each warp's rows of R_V^T, copied into its last stage once that is free
+constexpr int kRvRows = kD / kWarps;
+constexpr unsigned kRvBytes = kRvRows * kD * 4;
 
 // Exact fp16 pair of the levels (c - 1.5) of the codes at index r (0..7) of
 // both 16-bit halves of a code word.  One LOP3 puts the code into the low
@@ -309,7 +312,7 @@ struct DecodeArgs {
   const uint16_t* vb_pages;
   const int32_t* ctx_len;
   int Hq, Hkv, g;
-  int n_items, n_chunks, chunk_pages, tiles_per_item, plain_items, rec_floats;
+  int n_items, n_chunks, chunk_pages, tiles_per_item, rec_floats;
   const uint32_t* qfrag;
   const uint32_t* qplain;
   const float* qconst;
@@ -711,25 +714,14 @@ __device__ __forceinline__ int bf16_tile_rows(int j, int L, size_t& row_off, boo
 // items, the R_V^T rotation of the rotated-basis part, one normalisation.
 // Run by the block that took the last ticket; kept out of line so that its
 // registers are allocated apart from the page loop's.
-template <int MODE, bool PACK4>
+template <bool PACK4>
 __device__ __noinline__ void final_merge(const DecodeArgs& a, uint8_t* smem, int b, int h, int bh) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int X = a.n_items, g = a.g, RF = a.rec_floats;
-  // rotated-basis records first (MODE 0), then the original-basis ones
-  const int n_rot = MODE == 0 ? X : 0, n_rec = n_rot + a.plain_items;
-  const float* recs = a.partials + (size_t)bh * X * 2 * RF;
-  float* buf = reinterpret_cast<float*>(smem);  // record batch buffer
+  const float* recs = a.partials + (size_t)bh * X * RF;  // one original-basis record per item
+  float* buf = reinterpret_cast<float*>(smem);            // record batch buffer
   const int cap = (int)((size_t)kWarps * kStages * kBlockBytes / 4 / RF);
   uint64_t* ubar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + kWarps * kStages;
-  // warp w's rows [kD / kWarps w, kD / kWarps (w + 1)) of R_V^T (lane: output
-  // channels 4 lane .. 4 lane + 3), loaded while the records arrive
-  constexpr int kRows = kD / kWarps;
-  float4 rv[kRows];
-  if (MODE == 0) {
-#pragma unroll
-    for (int i = 0; i < kRows; ++i)
-      rv[i] = __ldg(reinterpret_cast<const float4*>(a.R_VT + (size_t)(kRows * warp + i) * kD) + lane);
-  }
   if (t == 0) {
     mbar_init(ubar, 1);
     fence_mbar_init();
@@ -738,145 +730,185 @@ __device__ __noinline__ void final_merge(const DecodeArgs& a, uint8_t* smem, int
   // warp (n, part): head n = warp % g merges records part, part + n_parts, ... of each batch
   const int n_parts = kWarps / g, n = warp % g, part = warp / g;
   const bool active = part < n_parts;
-  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-  for (int r0 = 0, batch = 0; r0 < n_rec; r0 += cap, ++batch) {
-    const int nb = min(cap, n_rec - r0);
+  float m = -INFINITY, l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r0 = 0, batch = 0; r0 < X; r0 += cap, ++batch) {
+    const int nb = min(cap, X - r0);
     if (warp == 0) {
       if (lane == 0) {
         fence_proxy_async_smem();  // the buffer was last used through generic loads and stores
         mbar_arrive_expect_tx(ubar, (unsigned)(nb * RF * 4));
       }
       __syncwarp();
-      for (int i = lane; i < nb; i += 32) {
-        const int r = r0 + i;
-        const int kind = r < n_rot ? 0 : 1;
-        const int x = r < n_rot ? r : r - n_rot;
-        bulk_copy_g2s(buf + (size_t)i * RF, recs + ((size_t)x * 2 + kind) * RF, (unsigned)(RF * 4), ubar);
-      }
+      for (int i = lane; i < nb; i += 32)
+        bulk_copy_g2s(buf + (size_t)i * RF, recs + (size_t)(r0 + i) * RF, (unsigned)(RF * 4), ubar);
     }
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(ubar, batch & 1, kWaitLimit))) {
       if (lane == 0) set_error(a.err, kErrTimeout);
       mbar_wait_bounded(ubar, batch & 1, kWaitLimit);
     }
-    if (active) {
+    if (active)
       for (int i = part; i < nb; i += n_parts) {
         const float* rec = buf + (size_t)i * RF;
-        const float4 v = reinterpret_cast<const float4*>(rec + 16 + n * kD)[lane];
-        if (r0 + i < n_rot)
-          merge_record(m0, l0, a0, rec[n], rec[8 + n], v);
-        else
-          merge_record(m1, l1, a1, rec[n], rec[8 + n], v);
+        merge_record(m, l, acc, rec[n], rec[8 + n], reinterpret_cast<const float4*>(rec + 16 + n * kD)[lane]);
       }
-    }
     __syncthreads();  // the buffer is refilled by the next batch, or becomes the stash
   }
-  float* stash = buf;                            // [kWarps][2][kStash]: acc[128], m, l per warp and basis
-  float* ystage = stash + kWarps * 2 * kStash;   // [g][128] merged rotated-basis accumulators
-  float* opart = ystage + kMaxG * kD;            // [kWarps][g][128] partial products with R_V^T
+  float* stash = buf;  // [kWarps][kStash]: acc[128], m, l per warp
   if (active) {
-    float* s0 = stash + (size_t)warp * 2 * kStash;
-    float* s1 = s0 + kStash;
-    reinterpret_cast<float4*>(s0)[lane] = a0;
-    reinterpret_cast<float4*>(s1)[lane] = a1;
+    float* s = stash + (size_t)warp * kStash;
+    reinterpret_cast<float4*>(s)[lane] = acc;
     if (lane == 0) {
-      s0[kD] = m0;
-      s0[kD + 1] = l0;
-      s1[kD] = m1;
-      s1[kD + 1] = l1;
+      s[kD] = m;
+      s[kD + 1] = l;
     }
-  }
-  __syncthreads();
-  if (MODE == 0) {
-    // merged rotated-basis accumulator y[n][j] (unnormalised, scaled to the head's max)
-    for (int e = t; e < g * kD; e += kThreads) {
-      const int hn = e >> 7, j = e & (kD - 1);
-      float M = -INFINITY;
-      for (int p = 0; p < n_parts; ++p) M = fmaxf(M, stash[(size_t)(p * g + hn) * 2 * kStash + kD]);
-      float v = 0.f;
-      if (M != -INFINITY)
-        for (int p = 0; p < n_parts; ++p) {
-          const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
-          v = fmaf(ex2(sp[kD] - M), sp[j], v);
-        }
-      ystage[e] = v;
-    }
-    __syncthreads();
-    // out_rot = y R_V^T: warp w takes rows j in [kRows w, kRows (w + 1)) for every head
-    constexpr int kG = PACK4 ? 4 : kMaxG;  // heads per KV head this variant serves
-    float o[kG][4];
-#pragma unroll
-    for (int hn = 0; hn < kG; ++hn) o[hn][0] = o[hn][1] = o[hn][2] = o[hn][3] = 0.f;
-#pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      const int j = kRows * warp + i;
-      const float4 u = rv[i];
-#pragma unroll
-      for (int hn = 0; hn < kG; ++hn)
-        if (hn < g) {
-          const float yj = ystage[hn * kD + j];
-          o[hn][0] = fmaf(yj, u.x, o[hn][0]);
-          o[hn][1] = fmaf(yj, u.y, o[hn][1]);
-          o[hn][2] = fmaf(yj, u.z, o[hn][2]);
-          o[hn][3] = fmaf(yj, u.w, o[hn][3]);
-        }
-    }
-#pragma unroll
-    for (int hn = 0; hn < kG; ++hn)
-      if (hn < g)
-        reinterpret_cast<float4*>(opart + (warp * g + hn) * kD)[lane] =
-            make_float4(o[hn][0], o[hn][1], o[hn][2], o[hn][3]);
   }
   __syncthreads();
   if (warp < g) {
-    // final: rotated-basis and original-basis parts of head n = warp, normalised together
     const int hn = warp;
-    float Mr = -INFINITY, Mp = -INFINITY;
-    for (int p = 0; p < n_parts; ++p) {
-      const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
-      Mr = fmaxf(Mr, sp[kD]);
-      Mp = fmaxf(Mp, sp[kStash + kD]);
-    }
-    float Lr = 0.f, Lp = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f), ap = o;
-    if (MODE == 0 && Mr != -INFINITY) {
-      for (int p = 0; p < n_parts; ++p) {
-        const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
-        Lr = fmaf(ex2(sp[kD] - Mr), sp[kD + 1], Lr);
-      }
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float4 op = reinterpret_cast<const float4*>(opart + (w * g + hn) * kD)[lane];
-        o.x += op.x;
-        o.y += op.y;
-        o.z += op.z;
-        o.w += op.w;
-      }
-    }
-    if (Mp != -INFINITY) {
-      for (int p = 0; p < n_parts; ++p) {
-        const float* sp = stash + (size_t)(p * g + hn) * 2 * kStash;
-        const float wp = ex2(sp[kStash + kD] - Mp);
-        Lp = fmaf(wp, sp[kStash + kD + 1], Lp);
-        const float4 v = reinterpret_cast<const float4*>(sp + kStash)[lane];
-        ap.x = fmaf(wp, v.x, ap.x);
-        ap.y = fmaf(wp, v.y, ap.y);
-        ap.z = fmaf(wp, v.z, ap.z);
-        ap.w = fmaf(wp, v.w, ap.w);
-      }
-    }
-    const float M = fmaxf(Mr, Mp);
+    float M = -INFINITY;
+    for (int p = 0; p < n_parts; ++p) M = fmaxf(M, stash[(size_t)(p * g + hn) * kStash + kD]);
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      const float fr = ex2(Mr - M), fp = ex2(Mp - M);
-      const float inv_l = 1.0f / (fr * Lr + fp * Lp);
-      res.x = (fr * o.x + fp * ap.x) * inv_l;
-      res.y = (fr * o.y + fp * ap.y) * inv_l;
-      res.z = (fr * o.z + fp * ap.z) * inv_l;
-      res.w = (fr * o.w + fp * ap.w) * inv_l;
+      float L = 0.f;
+      float4 o = res;
+      for (int p = 0; p < n_parts; ++p) {
+        const float* sp = stash + (size_t)(p * g + hn) * kStash;
+        const float w = ex2(sp[kD] - M);
+        L = fmaf(w, sp[kD + 1], L);
+        const float4 v = reinterpret_cast<const float4*>(sp)[lane];
+        o.x = fmaf(w, v.x, o.x);
+        o.y = fmaf(w, v.y, o.y);
+        o.z = fmaf(w, v.z, o.z);
+        o.w = fmaf(w, v.w, o.w);
+      }
+      const float inv_l = 1.0f / L;
+      res = make_float4(o.x * inv_l, o.y * inv_l, o.z * inv_l, o.w * inv_l);
     }
     *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + h * g + hn) * kD + 4 * lane) = res;
   }
+}
+
+// The block merge, after every warp of the block has stored its states.
+template <int MODE, bool PACK4>
+__device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, const float* bf16_slots, int bh, int item) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  // warp w's rows [kRows w, kRows (w + 1)) of R_V^T (lane: output channels
+  // 4 lane .. 4 lane + 3), copied into the warp's last stage during its last pages
+  constexpr int kRows = kRvRows;
+  float4 rv[kRows];
+  if (MODE == 0) {
+    uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + kWarps * kStages + 1 + warp;
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(rbar, 0, kWaitLimit)) && lane == 0) set_error(a.err, kErrTimeout);
+    const float4* src = reinterpret_cast<const float4*>(smem + ((size_t)warp * kStages + kStages - 1) * kBlockBytes);
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) rv[i] = src[i * (kD / 4) + lane];
+  }
+  griddep_launch_dependents();  // a dependent step kernel may start loading its constants
+  __syncthreads();
+  // merge the warps' states into this item's partial record:
+  // the rotated-basis (INT2) states merged and multiplied by R_V^T, then
+  // joined with the original-basis (BF16) states.  Thread t: head n = t / 128
+  // (+ 4, + 8, ...), channel ch = t % 128.
+  {
+    constexpr int kG = PACK4 ? 4 : kMaxG;  // heads per KV head this variant serves
+    constexpr int kHT = kG / 4;            // heads per thread
+    const int ch = t & (kD - 1), n0 = t >> 7;
+    float* ystage = reinterpret_cast<float*>(smem + (size_t)(kStages - 1) * kBlockBytes);  // [kG][kD], warp 0's last stage
+    float* opart = reinterpret_cast<float*>(smem + (size_t)kStages * kBlockBytes);       // [kWarps][kG][kD]
+    const float* rot = reinterpret_cast<const float*>(smem);  // warp states, stride: a warp's stage memory
+    const size_t rstride = (size_t)kStages * kBlockBytes / sizeof(float);
+    // original-basis states: the BF16 slots (mixed cache) or every warp's second state
+    const float* pln = MODE == 0 ? bf16_slots : rot + kPartialFloats;
+    const size_t pstride = MODE == 0 ? (size_t)kPartialFloats : rstride;
+    const int n_pln = MODE == 0 ? kBf16Slots : kWarps;
+    float Mr[kHT], Lr[kHT], Mp[kHT], Lp[kHT], yp[kHT];
+#pragma unroll
+    for (int k = 0; k < kHT; ++k) {
+      const int n = n0 + 4 * k;
+      Mr[k] = Mp[k] = -INFINITY;
+      Lr[k] = Lp[k] = yp[k] = 0.f;
+      if (n >= a.g) continue;
+      float yr = 0.f;
+      if (MODE == 0) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) Mr[k] = fmaxf(Mr[k], rot[w * rstride + n]);
+        if (Mr[k] != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            const float* ws = rot + w * rstride;
+            const float al = ex2(ws[n] - Mr[k]);  // 0 for an empty warp state (m = -inf)
+            yr = fmaf(al, ws[16 + n * kD + ch], yr);
+            Lr[k] = fmaf(al, ws[8 + n], Lr[k]);
+          }
+        }
+        ystage[n * kD + ch] = yr;
+      }
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w)
+        if (w < n_pln) Mp[k] = fmaxf(Mp[k], pln[w * pstride + n]);
+      if (Mp[k] != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          if (w >= n_pln) break;
+          const float* ws = pln + w * pstride;
+          const float al = ex2(ws[n] - Mp[k]);
+          yp[k] = fmaf(al, ws[16 + n * kD + ch], yp[k]);
+          Lp[k] = fmaf(al, ws[8 + n], Lp[k]);
+        }
+      }
+    }
+    if (MODE == 0) {
+      __syncthreads();  // ystage complete; the warp states are dead from here on
+      // partial products y R_V^T over warp w's rows, for every head
+      float o[kG][4];
+#pragma unroll
+      for (int hn = 0; hn < kG; ++hn) o[hn][0] = o[hn][1] = o[hn][2] = o[hn][3] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const int j = kRows * warp + i;
+        const float4 u = rv[i];
+#pragma unroll
+        for (int hn = 0; hn < kG; ++hn)
+          if (hn < a.g) {
+            const float yj = ystage[hn * kD + j];
+            o[hn][0] = fmaf(yj, u.x, o[hn][0]);
+            o[hn][1] = fmaf(yj, u.y, o[hn][1]);
+            o[hn][2] = fmaf(yj, u.z, o[hn][2]);
+            o[hn][3] = fmaf(yj, u.w, o[hn][3]);
+          }
+      }
+#pragma unroll
+      for (int hn = 0; hn < kG; ++hn)
+        if (hn < a.g)
+          reinterpret_cast<float4*>(opart + (warp * kG + hn) * kD)[lane] =
+              make_float4(o[hn][0], o[hn][1], o[hn][2], o[hn][3]);
+      __syncthreads();
+    }
+    float* part = a.partials + ((size_t)bh * a.n_items + item) * a.rec_floats;
+#pragma unroll
+    for (int k = 0; k < kHT; ++k) {
+      const int n = n0 + 4 * k;
+      if (n >= a.g) continue;
+      float yr = 0.f;
+      if (MODE == 0)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) yr += opart[(w * kG + n) * kD + ch];
+      const float M = fmaxf(Mr[k], Mp[k]);
+      float acc = 0.f, l = 0.f;
+      if (M != -INFINITY) {
+        const float fr = ex2(Mr[k] - M), fp = ex2(Mp[k] - M);
+        acc = fmaf(fr, yr, fp * yp[k]);
+        l = fmaf(fr, Lr[k], fp * Lp[k]);
+      }
+      part[16 + n * kD + ch] = acc;
+      if (ch == 0) {
+        part[n] = M;
+        part[8 + n] = l;
+      }
+    }
+  }
+
 }
 
 template <int MODE, bool PACK4>
@@ -891,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     // pages into L2 (a hint only -- the tables read here may still change, and
     // the pages are read again, coherently, after the wait).  More than one
     // page per warp competes with the previous layer's final merge.
-    if (item == 0)  // the last block of this (request, KV head) reads R_V^T
+    if (item == 0)  // every block of this layer reads R_V^T in its block merge
       for (int i = t; i < kD * kD / 32; i += kThreads) prefetch_l2(a.R_VT + 32 * i);
     if (lane == 0) {
       const int Lh = a.ctx_len[b];
@@ -978,13 +1010,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           bulk_copy_g2s(dst + kVScales + 64 * T, src + kVScales + 64 * T, 64, &bars[s]);
         }
       };
+    // barrier of this warp's R_V^T rows (after the stage barriers and the final merge's)
+    uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + kWarps * kStages + 1 + warp;
+    bool rv_issued = false;  // lane 0
+    auto issue_rv = [&]() {  // lane 0, once the last stage is free for good
+      mbar_arrive_expect_tx(rbar, kRvBytes);
+      bulk_copy_g2s(stages + (size_t)(kStages - 1) * kBlockBytes, a.R_VT + (size_t)kRvRows * warp * kD, kRvBytes, rbar);
+      rv_issued = true;
+    };
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+      mbar_init(rbar, 1);
+      fence_mbar_init();
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0 && n_my < kStages) issue_rv();
     if (n_my > 0) {
-      if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
       if (lane == 0)
         for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
     }
@@ -1074,12 +1116,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         if (lane == 0 && k + kStages < n_my) {
           fence_proxy_async_smem();
           issue(k + kStages);
+        } else if (lane == 0 && s == kStages - 1) {
+          fence_proxy_async_smem();
+          issue_rv();
         }
       }
       // after a timeout, wait (bounded) for the copies still in flight
       for (int kk = k + 1; kk < min(k + kStages, n_my); ++kk)
         mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, kWaitLimit);
       if (k < n_my) mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1, kWaitLimit);
+      if (lane == 0 && !rv_issued) {
+        fence_proxy_async_smem();
+        issue_rv();
+      }
       __syncwarp();
     }
     store_state<PACK4>(st, wstate, a.inv_pscale, lane);
@@ -1127,46 +1176,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
     store_state<PACK4>(st, wstate + kPartialFloats, 1.0f / kPScaleBF16, lane);
   }
-  griddep_launch_dependents();  // a dependent step kernel may start loading its constants
-  __syncthreads();
-
-  // ---------------- merge the warps' states into this item's two partial records
-  // (items from plain_items on attend no BF16 tile: they leave their
-  // original-basis record unwritten and the final merge skips it)
-  {
-    // thread: basis kind, channel ch, heads n = t / 256, t / 256 + kThreads / 256, ...
-    const int kind = (t >> 7) & 1, ch = t & 127;
-    const bool live = !(kind == 1 && item >= a.plain_items);
-    float* part = a.partials + (((size_t)bh * a.n_items + item) * 2 + kind) * a.rec_floats;
-    // warp states: the stage memory of every warp, or (original basis of the
-    // mixed cache) the BF16 slots
-    const bool slots = MODE == 0 && kind == 1;
-    const size_t wstride = slots ? kPartialFloats : (size_t)kStages * kBlockBytes / sizeof(float);
-    const int n_states = slots ? kBf16Slots : kWarps;
-    const float* base = slots ? bf16_slots : reinterpret_cast<const float*>(smem) + kind * kPartialFloats;
-    for (int n = t >> 8; live && n < a.g; n += kThreads / 256) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w)
-        if (w < n_states) M = fmaxf(M, base[w * wstride + n]);
-      float acc = 0.f, l = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          if (w >= n_states) break;
-          const float* ws = base + w * wstride;
-          const float al = ex2(ws[n] - M);  // 0 for an empty warp state (m = -inf)
-          acc = fmaf(al, ws[16 + n * kD + ch], acc);
-          l = fmaf(al, ws[8 + n], l);
-        }
-      }
-      part[16 + n * kD + ch] = acc;
-      if (ch == 0) {
-        part[n] = M;
-        part[8 + n] = l;
-      }
-    }
-  }
+  block_merge<MODE, PACK4>(a, smem, bf16_slots, bh, item);
 
   // ---------------- last block of this (request, KV head) merges all partials
   __shared__ int s_last;
@@ -1179,15 +1189,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   }
   __syncthreads();
   if (!s_last) return;
-  final_merge<MODE, PACK4>(a, smem, b, h, bh);
+  final_merge<PACK4>(a, smem, b, h, bh);
 }
 
 constexpr size_t decode_smem_bytes() { return kSlotsOffset + (size_t)kBf16Slots * kPartialFloats * sizeof(float); }
-// two finished warp states fit in a warp's stage memory; the last block's
-// merge (U_V^T, staged m/l, stats, rotation scratch) fits in all of it
+// two finished warp states fit in a warp's stage memory; the block merge's
+// partial products with R_V^T fit in the stage memory of warps 1 .. 15; the
+// final merge's stash fits in all of it
 static_assert(2 * kPartialFloats * 4 <= kStages * kBlockBytes, "warp states");
-static_assert((kWarps * 2 * kStash + kMaxG * kD + kWarps * kMaxG * kD) * 4 <= kWarps * kStages * kBlockBytes,
-              "merge staging");
+static_assert(kPartialFloats * 4 <= (kStages - 1) * kBlockBytes && kRvBytes <= kBlockBytes &&
+                  kMaxG * kD * 4 <= kBlockBytes,
+              "mixed cache: a warp's state before its last stage, which holds its R_V^T rows, then the staged accumulators");
+static_assert(kStages * kBlockBytes + kWarps * kMaxG * kD * 4 <= kWarps * kStages * kBlockBytes, "block merge products");
+static_assert(kWarps * kStash * 4 <= kWarps * kStages * kBlockBytes, "final merge stash");
 static_assert(kWarps * kStages * kBlockBytes / 4 / (16 + 128 * kMaxG) >= 1, "a record batch holds a record");
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1220,9 +1234,8 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   p.n_items = p.n_chunks > 0 ? p.n_chunks : 1;
   // BF16 tiles go to the first items, two warps each (the last two, which
   // hold the fewest left-over INT2 tiles); they run while those warps' first
-  // pages arrive, and only a few items produce original-basis partials
+  // pages arrive
   p.tiles_per_item = max(kBf16Slots, (kBf16Tiles + p.n_items - 1) / p.n_items);
-  p.plain_items = mode == 0 ? min(p.n_items, (kBf16Tiles + p.tiles_per_item - 1) / p.tiles_per_item) : p.n_items;
   const size_t bh = (size_t)batch * Hkv;
   size_t off = 0;
   p.off_counters = off;
@@ -1235,7 +1248,7 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   off = align256(off + bh * kQConstFloats * sizeof(float));
   p.off_partials = off;
   p.rec_floats = partial_record_floats(p.g);
-  off = align256(off + bh * (size_t)p.n_items * 2 * p.rec_floats * sizeof(float));
+  off = align256(off + bh * (size_t)p.n_items * p.rec_floats * sizeof(float));
   p.total = off;
   return p;
 }
@@ -1290,7 +1303,6 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
   a.n_chunks = p.n_chunks;
   a.chunk_pages = p.chunk_pages;
   a.tiles_per_item = p.tiles_per_item;
-  a.plain_items = p.plain_items;
   a.rec_floats = p.rec_floats;
   a.qfrag = pa.qfrag;
   a.qplain = pa.qplain;

@@ -60,7 +60,6 @@ struct DecodePlan {
   int32_t n_chunks = 0;      // paged work items per (request, KV head)
   int32_t n_items = 0;       // all work items per (request, KV head)
   int32_t tiles_per_item = 0;  // mixed cache: BF16 sink/recent tiles per item (items 0, 1, ... take them)
-  int32_t plain_items = 0;     // mixed cache: items that attend BF16 tiles (original-basis partials)
   int32_t rec_floats = 0;      // floats per partial record
   size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
 };

@@ -61,13 +61,15 @@ def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
 
 
 def test_noalloc_decode_refuses_calls_larger_than_its_scratch():
-    s = harness.Setup(32, 8, 600, 2, cfg=9, calibrate=False)
+    # 4 requests x 8 KV heads at an 8M-token maximum: 256 work items each, one
+    # partial record apiece, more workspace than the library's scratch
+    s = harness.Setup(32, 8, 600, 4, cfg=9, calibrate=False)
     try:
-        need = abi.oscar_decode_workspace_bytes(s.ctx, 2, 8_000_000)
+        need = abi.oscar_decode_workspace_bytes(s.ctx, 4, 8_000_000)
         assert need > abi.NOALLOC_SCRATCH_BYTES
-        q = torch.zeros((2, 32, 128), dtype=torch.bfloat16, device="cuda")
-        out = torch.zeros((2, 32, 128), dtype=torch.float32, device="cuda")
-        lens = torch.tensor([10, 10], dtype=torch.int32, device="cuda")
+        q = torch.zeros((4, 32, 128), dtype=torch.bfloat16, device="cuda")
+        out = torch.zeros((4, 32, 128), dtype=torch.float32, device="cuda")
+        lens = torch.tensor([10, 10, 10, 10], dtype=torch.int32, device="cuda")
         args = kvcache.decode_args(q, out, lens, 8_000_000)
         with pytest.raises(abi.OscarError) as e:
             abi.oscar_decode_attention_noalloc(s.ctx, 0, s.cache.view(0), args, None)
