@@ -24,13 +24,14 @@ namespace oscar {
 namespace {
 
 // ------------------------------------------------------------------ decode append
-// One new token per request.  grid (Hkv, B), 256 threads: threads 0..127
-// handle K, threads 128..255 handle V, each a channel per thread.
-__global__ void __launch_bounds__(256, 1) append_one_kernel(AppendLaunch a) {
+// One new token per request.  grid (Hkv, B), 2 kQuantThreads threads: the
+// first kQuantThreads handle K, the others V.
+__global__ void __launch_bounds__(2 * kQuantThreads, 1) append_one_kernel(AppendLaunch a) {
   __shared__ QuantSmem sm[2];
   griddep_wait();
-  const int half = threadIdx.x >> 7;
-  append_one_body(a, blockIdx.y, blockIdx.x, half, threadIdx.x & 127, a.rot.R_K, a.rot.R_V, sm[half]);
+  const int half = threadIdx.x / kQuantThreads;
+  append_one_body(a, blockIdx.y, blockIdx.x, half, threadIdx.x % kQuantThreads, a.rot.R_K, a.rot.R_V, sm[half],
+                  1 + half);
 }
 
 // ------------------------------------------------------------------ multi-token append
@@ -60,10 +61,12 @@ __device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& 
 }
 
 // Phase 1: ring tokens that fall out of the recent window go to the history.
-// grid (256, Hkv, B), 128 threads: one token-head per block.
-__global__ void __launch_bounds__(256, 1) append_evict_kernel(AppendLaunch a) {
+// grid (256, Hkv, B), 2 kQuantThreads threads: one token-head per block, K
+// by the first kQuantThreads threads, V by the others.
+__global__ void __launch_bounds__(2 * kQuantThreads, 1) append_evict_kernel(AppendLaunch a) {
   __shared__ QuantSmem sm[2];
-  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, half = threadIdx.x >> 7, t = threadIdx.x & 127;
+  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, half = threadIdx.x / kQuantThreads;
+  const int u = threadIdx.x % kQuantThreads, t = u & 127;
   const bool is_v = half == 1;
   int p0, n, tok0;
   if (!request_span(a, b, p0, n, tok0)) return;
@@ -81,7 +84,8 @@ __global__ void __launch_bounds__(256, 1) append_evict_kernel(AppendLaunch a) {
   if (blk == nullptr) return;
   const size_t r = (((size_t)slot * c.num_kv_heads + h) * kRecent + ((e - kSink) % kRecent)) * kD + t;
   const float xv = bf16_bits_to_float((is_v ? c.v_ring : c.k_ring)[r]);
-  quantize_token(xv, is_v ? a.rot.R_V : a.rot.R_K, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm[half]);
+  quantize_token(xv, is_v ? a.rot.R_V : a.rot.R_K, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm[half], u,
+                 1 + half);
 }
 
 // Phase 2a: new tokens that stay BF16 (sink rows, ring rows).
@@ -312,10 +316,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   const int B = a.c.batch, Hkv = a.c.num_kv_heads;
   if (a.cu_seqlens == nullptr) {
-    append_one_kernel<<<dim3(Hkv, B), 256, 0, stream>>>(a);
+    append_one_kernel<<<dim3(Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
     return cudaGetLastError();
   }
-  if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 256, 0, stream>>>(a);
+  if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
   append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
   const int tiles = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
   const size_t smem = sizeof(TcSmem);

@@ -137,22 +137,26 @@ struct PrepArgs {
 // the accumulator lane holding columns 2 h and 2 h + 1 holds all of head h;
 // with g > 4 column n is head n, words 0..15 hold the values and 16..31 the
 // residuals.
+constexpr int kPrepThreads = 512;  // channel t = u % 128, row quarter u / 128 of R_K
+
 struct PrepSmem {
   __align__(16) float xs[kMaxG][kD];
+  float zq[4][kMaxG][kD];  // partial products over the four quarters of the rows of R_K
   float qr[kMaxG][kD];
   float qp[kMaxG][kD];
-  float red[8];
+  float red[2 * kPrepThreads / 32];
 };
 
-// z[n] = (q_n R_K)[t] for the first G heads of sm.xs (two partial sums per
-// head so that the shared-memory loads and the multiply-adds overlap).
+// Partial q_n R_K over rows [32 kq, 32 kq + 32), channel t, for the first G
+// heads of sm.xs, into sm.zq[kq] (two sums per head, so that the
+// shared-memory loads and the multiply-adds overlap).
 template <int G>
-__device__ __forceinline__ void rotate_heads(const PrepSmem& sm, const float* __restrict__ RK, int t, float (&z)[kMaxG]) {
+__device__ __forceinline__ void rotate_heads(PrepSmem& sm, const float* __restrict__ RK, int t, int kq) {
   float za[G], zb[G];
 #pragma unroll
   for (int n = 0; n < G; ++n) za[n] = zb[n] = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < kD; i += 4) {
+#pragma unroll
+  for (int i = 32 * kq; i < 32 * kq + 32; i += 4) {
     const float r0 = RK[i * kD + t], r1 = RK[(i + 1) * kD + t], r2 = RK[(i + 2) * kD + t], r3 = RK[(i + 3) * kD + t];
 #pragma unroll
     for (int n = 0; n < G; ++n) {
@@ -162,46 +166,51 @@ __device__ __forceinline__ void rotate_heads(const PrepSmem& sm, const float* __
     }
   }
 #pragma unroll
-  for (int n = 0; n < kMaxG; ++n) z[n] = n < G ? za[n] + zb[n] : 0.f;
+  for (int n = 0; n < G; ++n) sm.zq[kq][n][t] = za[n] + zb[n];
 }
 
-__device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t, const float* __restrict__ RK,
+__device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u, const float* __restrict__ RK,
                                           PrepSmem& sm, int bar) {
-  const int lane = t & 31, warp = t >> 5;
+  const int t = u & 127, kq = u >> 7, lane = u & 31, warp = u >> 5;
   const int g = a.g, bh = b * a.Hkv + h;
   const bool packed = g <= 4;
-  if (t == 0) a.counters[bh] = 0;
+  if (u == 0) a.counters[bh] = 0;
   const float c = a.sm_scale * kLog2e;
   // heads g .. G - 1 of the padded set are zero (G = 4 when g <= 4, else 8)
   const int G = packed ? 4 : kMaxG;
-  for (int n = 0; n < G; ++n)
+  for (int n = kq; n < G; n += 4)
     sm.xs[n][t] = n < g ? bf16_bits_to_float(a.q[((size_t)b * a.Hq + h * g + n) * kD + t]) : 0.f;
-  half_sync(bar);
-  float z[kMaxG];
+  group_sync(bar, kPrepThreads);
   if (packed)
-    rotate_heads<4>(sm, RK, t, z);
+    rotate_heads<4>(sm, RK, t, kq);
   else
-    rotate_heads<kMaxG>(sm, RK, t, z);
+    rotate_heads<kMaxG>(sm, RK, t, kq);
+  group_sync(bar, kPrepThreads);
   // power-of-two normalisations: max |q'| 2^-E <= 2^10, max |q| 2^-Ep <= 2^10
   float mr = 0.f, mp = 0.f;
-#pragma unroll
-  for (int n = 0; n < kMaxG; ++n)
-    if (n < g) {
-      const float vr = z[n] * c, vp = sm.xs[n][t] * c;
-      sm.qr[n][t] = vr;
-      sm.qp[n][t] = vp;
-      mr = fmaxf(mr, fabsf(vr));
-      mp = fmaxf(mp, fabsf(vp));
-    }
+  for (int n = kq; n < g; n += 4) {
+    const float z = ((sm.zq[0][n][t] + sm.zq[1][n][t]) + sm.zq[2][n][t]) + sm.zq[3][n][t];
+    const float vr = z * c, vp = sm.xs[n][t] * c;
+    sm.qr[n][t] = vr;
+    sm.qp[n][t] = vp;
+    mr = fmaxf(mr, fabsf(vr));
+    mp = fmaxf(mp, fabsf(vp));
+  }
   mr = warp_max(mr);
   mp = warp_max(mp);
+  constexpr int kW = kPrepThreads / 32;
   if (lane == 0) {
     sm.red[warp] = mr;
-    sm.red[4 + warp] = mp;
+    sm.red[kW + warp] = mp;
   }
-  half_sync(bar);
-  mr = fmaxf(fmaxf(sm.red[0], sm.red[1]), fmaxf(sm.red[2], sm.red[3]));
-  mp = fmaxf(fmaxf(sm.red[4], sm.red[5]), fmaxf(sm.red[6], sm.red[7]));
+  group_sync(bar, kPrepThreads);
+  mr = 0.f;
+  mp = 0.f;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) {
+    mr = fmaxf(mr, sm.red[w]);
+    mp = fmaxf(mp, sm.red[kW + w]);
+  }
   int er = 0, ep = 0;
   if (mr > 0.f) {
     frexpf(mr, &er);
@@ -219,7 +228,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t
   // BF16 segment: MMA ks = i takes channels 32 tig + 4 ks + {0,1} (b0) and {2,3} (b1).
   uint32_t* qf = a.qfrag + (size_t)bh * kQFragWords;
   uint32_t* qpl = a.qplain + (size_t)bh * kQFragWords;
-  for (int e = t; e < kQFragWords; e += 128) {
+  for (int e = u; e < kQFragWords; e += kPrepThreads) {
     const int L = e >> 5, w = e & 31, set = w >> 4, ww = w & 15, i = ww >> 1, bs = ww & 1;
     const int n = L >> 2, tig = L & 3;
     const int head = packed ? (n >> 1) : n;
@@ -236,15 +245,15 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int t
     qf[e] = vr;
     qpl[e] = vp;
   }
-  if (t == 0) {
+  if (u == 0) {
     float* qc = a.qconst + (size_t)bh * kQConstFloats;
     qc[16] = ldexpf(1.f, er);
     qc[17] = ldexpf(1.f, ep);
   }
 }
 
-// grid (Hkv, B), 128 threads
-__global__ void __launch_bounds__(128, 1) prep_kernel(PrepArgs a) {
+// grid (Hkv, B), kPrepThreads threads
+__global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(PrepArgs a) {
   __shared__ PrepSmem sm;
   griddep_wait();
   griddep_launch_dependents();
@@ -252,56 +261,58 @@ __global__ void __launch_bounds__(128, 1) prep_kernel(PrepArgs a) {
 }
 
 // Fused decode step, part 1: the decode append (K and V) and the q rotation
-// of one (KV head, request).  grid (Hkv, B), 384 threads in three roles:
-// 0..127 append K, 128..255 append V, 256..383 rotate q.  R_K and R_V are
-// brought into shared memory by bulk copies while the previous kernel
-// finishes (programmatic dependent launch).
-constexpr size_t kStepSmemBytes = 2 * kD * kD * sizeof(float) + 16;
+// of one (KV head, request).  grid (Hkv, B, 3), 512 threads; blockIdx.z is
+// the role: 0 appends K, 1 appends V, 2 rotates q.  The block's rotation
+// (R_K, or R_V for role 1) is brought into shared memory by a bulk copy
+// while the previous kernel finishes (programmatic dependent launch).
+constexpr size_t kStepSmemBytes = kD * kD * sizeof(float) + 16;
+static_assert(kQuantThreads == kPrepThreads, "one block size for the three roles");
 
-__global__ void __launch_bounds__(384, 1) step_kernel(AppendLaunch ap, PrepArgs pr) {
+__global__ void __launch_bounds__(kPrepThreads, 1) step_kernel(AppendLaunch ap, PrepArgs pr) {
   extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ QuantSmem qsm[2];
+  __shared__ QuantSmem qsm;
   __shared__ PrepSmem psm;
-  float* uk = reinterpret_cast<float*>(dsm);
-  float* uv = uk + kD * kD;
-  uint64_t* ubar = reinterpret_cast<uint64_t*>(uv + kD * kD);
-  const int h = blockIdx.x, b = blockIdx.y, role = threadIdx.x >> 7, t = threadIdx.x & 127;
-  if (threadIdx.x == 0) {
+  float* R = reinterpret_cast<float*>(dsm);
+  uint64_t* ubar = reinterpret_cast<uint64_t*>(R + kD * kD);
+  const int h = blockIdx.x, b = blockIdx.y, role = blockIdx.z, u = threadIdx.x;
+  if (u == 0) {
     mbar_init(ubar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(ubar, 2 * kD * kD * 4);
-    bulk_copy_g2s(uk, ap.rot.R_K, kD * kD * 4, ubar);
-    bulk_copy_g2s(uv, ap.rot.R_V, kD * kD * 4, ubar);
+    mbar_arrive_expect_tx(ubar, kD * kD * 4);
+    bulk_copy_g2s(R, role == 1 ? ap.rot.R_V : ap.rot.R_K, kD * kD * 4, ubar);
   }
   griddep_launch_dependents();
   // while the kernel before this one finishes: pull this block's rows into L2
   // (a hint only; everything is read again after the wait)
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x, Hkv = ap.c.num_kv_heads;
+  if (u < 32) {
+    const int lane = u, Hkv = ap.c.num_kv_heads;
     const size_t row = ((size_t)b * Hkv + h) * kD;  // new K / V token rows, 256 bytes each
-    if (lane < 2) prefetch_l2(ap.k + row + 64 * lane);
-    else if (lane < 4) prefetch_l2(ap.v + row + 64 * (lane - 2));
-    else if (lane < 4 + 2 * pr.g) prefetch_l2(pr.q + ((size_t)b * pr.Hq + h * pr.g) * kD + 64 * (lane - 4));
-    const int p = ap.pos[b], slot = ap.c.ring_slot[b];
-    if (lane >= 28 && p >= kSink + kRecent && slot >= 0 && slot < ap.c.num_ring) {  // the ring row to evict
-      const size_t r = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + 64 * (lane & 1);
-      prefetch_l2(((lane & 2) ? ap.c.v_ring : ap.c.k_ring) + r);
+    if (role == 2) {
+      if (lane < 2 * pr.g) prefetch_l2(pr.q + ((size_t)b * pr.Hq + h * pr.g) * kD + 64 * lane);
+    } else {
+      const uint16_t* src = role == 0 ? ap.k : ap.v;
+      if (lane < 2) prefetch_l2(src + row + 64 * lane);
+      const int p = ap.pos[b], slot = ap.c.ring_slot[b];
+      if (lane >= 2 && lane < 4 && p >= kSink + kRecent && slot >= 0 && slot < ap.c.num_ring) {  // the ring row to evict
+        const size_t r = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + 64 * (lane & 1);
+        prefetch_l2((role == 0 ? ap.c.k_ring : ap.c.v_ring) + r);
+      }
+      if (lane == 4 && p >= kSink + kRecent && ((p - kRecent) >> 6) < ap.c.max_pages)  // its page-table entry
+        prefetch_l2(ap.c.page_table + (size_t)b * ap.c.max_pages + ((p - kRecent) >> 6));
     }
-    if (lane == 27 && p >= kSink + kRecent && ((p - kRecent) >> 6) < ap.c.max_pages)  // its page-table entry
-      prefetch_l2(ap.c.page_table + (size_t)b * ap.c.max_pages + ((p - kRecent) >> 6));
   }
   __syncthreads();
   griddep_wait();
   if (!mbar_wait_bounded(ubar, 0, kWaitLimit)) {
-    if (threadIdx.x == 0) set_error(ap.err, kErrTimeout);
+    if (u == 0) set_error(ap.err, kErrTimeout);
     mbar_wait_bounded(ubar, 0, kWaitLimit);
     return;
   }
   if (role == 2)
-    prep_body(pr, b, h, t, uk, psm, 3);
+    prep_body(pr, b, h, u, R, psm, 1);
   else
-    append_one_body(ap, b, h, role, t, uk, uv, qsm[role]);
+    append_one_body(ap, b, h, role, u, R, R, qsm, 1);
 }
 
 // ------------------------------------------------------------------ decode
@@ -1343,7 +1354,7 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
   if (p.batch == 0) return cudaSuccess;
   PrepArgs pa = prep_args_of(d);
   void* args[] = {&pa};
-  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(prep_kernel), dim3(p.Hkv, p.batch), dim3(128), 0, stream,
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(prep_kernel), dim3(p.Hkv, p.batch), dim3(kPrepThreads), 0, stream,
                              args);
   if (e != cudaSuccess) return e;
   return launch_decode_kernel(d, pa, stream);
@@ -1362,7 +1373,7 @@ cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cu
   }
   AppendLaunch apc = ap;
   void* args[] = {&apc, &pa};
-  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(step_kernel), dim3(p.Hkv, p.batch), dim3(384),
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(step_kernel), dim3(p.Hkv, p.batch, 3), dim3(kPrepThreads),
                              kStepSmemBytes, stream, args);
   if (e != cudaSuccess) return e;
   return launch_decode_kernel(d, pa, stream);

@@ -171,4 +171,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 // Barrier over the 128 threads [128 * (id - 1), 128 * id) of the block (id >= 1).
 __device__ __forceinline__ void half_sync(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
 
+// Barrier `id` (>= 1) over a group of n threads (whole warps) of the block.
+__device__ __forceinline__ void group_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
+
 }  // namespace oscar

@@ -46,41 +46,53 @@ __device__ __forceinline__ int v_half_offset(int t, int jj) {
 
 struct QuantSmem {
   __align__(16) float x[kD];
+  float zq[4][kD];  // partial products over the four quarters of the rows of R
   float red[4];
   uint8_t code[kD];
 };
 
-// Rotate + clip + quantise one token held one channel per thread by one
-// 128-thread half of the block (half 0: K, half 1: V, synchronised by named
-// barrier 1 + half) and store its codes and scale in row `row` of the K or V
-// part of `block`.  R: the layer's composite rotation (global or shared
-// memory).  All 128 threads of the half must call it.
+constexpr int kQuantThreads = 512;  // threads per token: channel t = u % 128, row quarter u / 128
+
+// Rotate + clip + quantise one token and store its codes and scale in row
+// `row` of the K or V part of `block`.  Called by the kQuantThreads threads
+// u of a group synchronised by named barrier `bar`; x: the token's channel
+// u % 128 (read from the threads u < 128).  R: the layer's composite
+// rotation (global or shared memory).  Thread u forms the partial product of
+// rows [32 (u / 128), 32 (u / 128) + 32) of R for channel u % 128; the four
+// partials are added in quarter order.
 __device__ __forceinline__ void quantize_token(float x, const float* __restrict__ R, float tau, uint8_t* block,
-                                               int row, bool is_v, QuantSmem& sm) {
-  const int t = threadIdx.x & 127, lane = t & 31, warp = t >> 5, bar = 1 + (threadIdx.x >> 7);
-  sm.x[t] = x;
-  half_sync(bar);
-  // z_t = sum_i x_i R[i][t]
+                                               int row, bool is_v, QuantSmem& sm, int u, int bar) {
+  const int t = u & 127, kq = u >> 7, lane = u & 31, warp = (u >> 5) & 3;
+  if (kq == 0) sm.x[t] = x;
+  group_sync(bar, kQuantThreads);
   float z0 = 0.f, z1 = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < kD; i += 4) {
+#pragma unroll
+  for (int i = 32 * kq; i < 32 * kq + 32; i += 4) {
     const float4 xv = *reinterpret_cast<const float4*>(&sm.x[i]);
     z0 = fmaf(xv.x, R[i * kD + t], z0);
     z1 = fmaf(xv.y, R[(i + 1) * kD + t], z1);
     z0 = fmaf(xv.z, R[(i + 2) * kD + t], z0);
     z1 = fmaf(xv.w, R[(i + 3) * kD + t], z1);
   }
-  const float z = z0 + z1;
-  const float amax = warp_max(fabsf(z));
-  if (lane == 0) sm.red[warp] = amax;
-  half_sync(bar);
+  sm.zq[kq][t] = z0 + z1;
+  group_sync(bar, kQuantThreads);
+  float z = 0.f;
+  if (kq == 0) {
+    z = ((sm.zq[0][t] + sm.zq[1][t]) + sm.zq[2][t]) + sm.zq[3][t];
+    const float amax = warp_max(fabsf(z));
+    if (lane == 0) sm.red[warp] = amax;
+  }
+  group_sync(bar, kQuantThreads);
   const int grp = t >> 6;
   const float a = fminf(fmaxf(sm.red[2 * grp], sm.red[2 * grp + 1]), tau);
   const __half sh = __float2half_rn(a / 1.5f);
-  const float s = __half2float(sh);
-  sm.code[t] = (uint8_t)((z >= -s) + (z >= 0.f) + (z >= s));
-  half_sync(bar);
-  if (!is_v) {
+  if (kq == 0) {
+    const float s = __half2float(sh);
+    sm.code[t] = (uint8_t)((z >= -s) + (z >= 0.f) + (z >= s));
+  }
+  group_sync(bar, kQuantThreads);
+  if (kq != 0) {
+  } else if (!is_v) {
     if (t < 8)
       *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, t & 3, t >> 2)) = k_word(sm.code, t & 3, t >> 2);
   } else {
@@ -91,9 +103,9 @@ __device__ __forceinline__ void quantize_token(float x, const float* __restrict_
       *reinterpret_cast<uint16_t*>(block + kVCodes + v_half_offset(row, t)) = (uint16_t)hv;
     }
   }
-  if ((t & 63) == 0)
+  if (kq == 0 && (t & 63) == 0)
     *reinterpret_cast<__half*>(block + (is_v ? kVScales : kKScales) + 4 * row + 2 * grp) = sh;
-  half_sync(bar);
+  group_sync(bar, kQuantThreads);
 }
 
 // Locate (and check) the INT2 block of position e of request b, head h.
@@ -111,13 +123,16 @@ __device__ __forceinline__ uint8_t* history_block(const CacheRefs& c, int b, int
   return c.pages + ((size_t)phys * c.num_kv_heads + h) * kBlockBytes;
 }
 
-// Decode append of request b, KV head h: K (half 0) or V (half 1), one
-// channel per thread t of the 128-thread half.  Writes the token into the
-// sink page (position < 64) or its ring row; a position >= 320 first moves
-// the ring row's old token (position - 256) into its INT2 history row.
-__device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, int h, int half, int t,
-                                                const float* Rk, const float* Rv, QuantSmem& sm) {
+// Decode append of request b, KV head h: K (half 0) or V (half 1), by the
+// kQuantThreads threads u of a group synchronised by named barrier `bar`;
+// the threads u < 128 move channel u.  Writes the token into the sink page
+// (position < 64) or its ring row; a position >= 320 first moves the ring
+// row's old token (position - 256) into its INT2 history row.
+__device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, int h, int half, int u,
+                                                const float* Rk, const float* Rv, QuantSmem& sm, int bar) {
   const bool is_v = half == 1;
+  const int t = u & 127;
+  const bool mover = u < kD;
   const CacheRefs& c = a.c;
   const int Hkv = c.num_kv_heads;
   // independent loads first, so that their round trips overlap
@@ -134,7 +149,7 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
       if (threadIdx.x == 0) set_error(a.err, kErrSink);
       return;
     }
-    (is_v ? c.v_sink : c.k_sink)[(((size_t)sp * Hkv + h) * kSink + p) * kD + t] = xn;
+    if (mover) (is_v ? c.v_sink : c.k_sink)[(((size_t)sp * Hkv + h) * kSink + p) * kD + t] = xn;
     return;
   }
   if (slot < 0 || slot >= c.num_ring) {
@@ -150,9 +165,9 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
     uint8_t* blk = history_block(c, b, h, e, a.err);
     if (blk != nullptr)
       quantize_token(bf16_bits_to_float(xo), is_v ? Rv : Rk, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v,
-                     sm);
+                     sm, u, bar);
   }
-  ring[rdst] = xn;
+  if (mover) ring[rdst] = xn;
 }
 
 }  // namespace
