@@ -998,11 +998,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         const int ph = c.page_table[(size_t)b * c.max_pages + lp];
         return (ph >= 0 && ph < c.num_pages) ? ph : -1;
       };
-      auto issue = [&](int k) {  // lane 0 only
+      auto phys_unit = [&](int k) -> int {  // physical page of unit k (-1: invalid)
+        int lp, T;
+        unit_of(k, lp, T);
+        return phys_of(lp);
+      };
+      auto issue = [&](int k, int ph) {  // lane 0 only; ph = phys_unit(k)
         const int s = k % kStages;
         int lp, T;
         unit_of(k, lp, T);
-        const int ph = phys_of(lp);
         uint8_t* dst = stages + (size_t)s * kBlockBytes;
         if (ph < 0) {
           set_error(a.err, kErrPage);
@@ -1037,9 +1041,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
     __syncwarp();
     if (lane == 0 && n_my < kStages) issue_rv();
+    // bit s: stage s holds a valid unit.  The page-table entry of unit
+    // k + kStages is read during unit k - 1, so that issuing its copy after
+    // unit k waits on nothing.
+    uint32_t valid = 0;
+    int ph_ahead = -1;
     if (n_my > 0) {
-      if (lane == 0)
-        for (int k = 0; k < min(kStages, n_my); ++k) issue(k);
+      for (int k = 0; k < min(kStages, n_my); ++k) {
+        const int ph = phys_unit(k);
+        valid |= (ph >= 0 ? 1u : 0u) << k;
+        if (lane == 0) issue(k, ph);
+      }
+      if (kStages < n_my) ph_ahead = phys_unit(kStages);
     }
     // BF16 sink/recent tiles (original basis) while the first pages arrive:
     // local tile k of this item goes to warp kWarps - 1 - k % kBf16Slots,
@@ -1108,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
         int lp, T;
         unit_of(k, lp, T);
-        if (phys_of(lp) >= 0) {
+        if ((valid >> s) & 1u) {
           const uint8_t* blk = stages + (size_t)s * kBlockBytes;
           const int n_valid = min(kPage, hist_end - kPage * lp);
           if (T < 0) {
@@ -1124,9 +1137,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           }
         }
         __syncwarp();
-        if (lane == 0 && k + kStages < n_my) {
-          fence_proxy_async_smem();
-          issue(k + kStages);
+        if (k + kStages < n_my) {
+          const int ph = ph_ahead;
+          ph_ahead = k + kStages + 1 < n_my ? phys_unit(k + kStages + 1) : -1;
+          valid = (valid & ~(1u << s)) | ((ph >= 0 ? 1u : 0u) << s);
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            issue(k + kStages, ph);
+          }
         } else if (lane == 0 && s == kStages - 1) {
           fence_proxy_async_smem();
           issue_rv();
