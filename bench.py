@@ -66,7 +66,7 @@ def replica_tokens_per_s(ms_per_step, world):
 
 
 def profiled_traffic():
-    """DRAM bytes per layer step (fused step kernel + decode kernel) from the
+    """DRAM bytes per layer step (the fused decode-step kernel) from the
     committed ncu summary of this workload, or None when the decode source has
     changed since those counters were taken."""
     import hashlib
@@ -599,14 +599,14 @@ def run_cuda(args):
         "algorithmic_bytes_per_step": bytes_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profiled_traffic(),
-                     "kernel": ("one layer's decode step: " + ("append kernel, then q-rotation + split-K decode"
-                                if args.split else "fused append + q-rotation kernel, then split-K decode") +
+                     "kernel": ("one layer's decode step: " + ("append kernel, then q-rotation kernel, then split-K decode"
+                                if args.split else "one kernel: q rotation, append with eviction and split-K decode") +
                                 " with in-kernel combine (bytes: the decode's reads and writes only)"),
                      "peak_kind": peak_kind, "bytes_per_launch": bytes_layer, "avg_launch_ms": dec_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": replica_tokens_per_s(e2e_ms, world), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": N_LAYERS * (3 if args.split else 2) * args.steps,
+        "gpu_launches": N_LAYERS * (3 if args.split else 1) * args.steps,
         "clocks": clocks.summary(),
         "bf16_comparator": bf16,
         "bulk_append": bulk,

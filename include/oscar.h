@@ -248,9 +248,10 @@ size_t oscar_decode_workspace_bytes(const oscar_ctx* ctx, int32_t max_batch, int
  * part of the output is rotated back (acc R_V^T) when the splits are merged.
  * No dequantised cache is materialised.  workspace: device, at least
  * oscar_decode_workspace_bytes(ctx, batch, max_ctx_len) bytes, 256-byte
- * aligned, owned by the caller; its contents need no initialisation and are
- * scratch between calls.  Calls that share a workspace must not overlap on
- * the GPU.
+ * aligned, owned by the caller; its contents need no initialisation for
+ * this call and are scratch between calls (oscar_decode_step wants them
+ * zero before its first use).  Calls that share a workspace must not
+ * overlap on the GPU.
  */
 oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
                                     const oscar_decode_args* args, void* workspace, size_t workspace_bytes,
@@ -258,21 +259,25 @@ oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
 
 /*
  * One decode step of one layer: oscar_kv_append of one new token per
- * request, then oscar_decode_attention, in two kernel launches instead of
+ * request, then oscar_decode_attention, in one kernel launch instead of
  * three ([IT] "Architettura ...": the decode path is append, evict/quantise,
- * attend).  The first kernel writes the new K/V token of every
- * (request, KV head) (evicting and quantising the ring row it replaces) and
- * rotates that request's queries into the K basis in the same block; the
- * second is the split-K decode kernel.  Both are launched with programmatic
- * dependent launch, so each may start its prologue while the kernel before it
- * on the stream drains; neither reads a buffer the kernel before it writes
- * until that kernel has completed.  append: cu_seqlens NULL, n_tokens ==
- * batch, flags 0 or OSCAR_APPEND_FRESH_RING (same meaning as for
- * oscar_kv_append); decode: as oscar_decode_attention, with ctx_len[b]
- * normally pos[b] + 1 so that the token just written is attended.  Results
- * equal oscar_kv_append followed by oscar_decode_attention on the same
- * arguments.  Errors: as the two calls; nothing is launched when either
- * argument set is rejected.
+ * attend).  Every block of the split-K decode rotates its request's queries
+ * into the K basis itself; the block whose history pages hold the row the
+ * new token evicts writes the new K/V token (evicting and quantising the
+ * ring row it replaces) and attends that row from its own copy; the BF16
+ * tiles take the new token's row from the input.  The kernel is launched
+ * with programmatic dependent launch, so it may start its prologue (loads of
+ * the layer's constants and L2 prefetches) while the kernel before it on the
+ * stream drains; it reads nothing that kernel writes until it has completed.
+ * append: cu_seqlens NULL, n_tokens == batch, flags 0 or
+ * OSCAR_APPEND_FRESH_RING (same meaning as for oscar_kv_append); decode: as
+ * oscar_decode_attention, with ctx_len[b] normally pos[b] + 1 so that the
+ * token just written is attended.  Results equal oscar_kv_append followed by
+ * oscar_decode_attention on the same arguments.  workspace: as for
+ * oscar_decode_attention, except that it must hold zeros before its first
+ * use by this call (every decode call leaves the counters it uses at zero).
+ * Errors: as the two calls; nothing is launched when either argument set is
+ * rejected.
  */
 oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
                                const oscar_append_args* append, const oscar_decode_args* decode,

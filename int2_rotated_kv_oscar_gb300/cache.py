@@ -89,8 +89,9 @@ def decode_args(q, out, ctx_len, max_ctx_len, sm_scale=0.0):
 
 
 def workspace(ctx, max_batch, max_ctx_len, device="cuda"):
-    """A caller-owned decode workspace (uint8 tensor, 256-byte aligned)."""
+    """A caller-owned decode workspace (uint8 tensor, 256-byte aligned, zero-filled
+    as the fused decode step wants it before its first use)."""
     n = abi.oscar_decode_workspace_bytes(ctx, max_batch, max_ctx_len)
-    t = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    t = torch.zeros(n + 256, dtype=torch.uint8, device=device)
     off = (-t.data_ptr()) % 256
     return t, t.data_ptr() + off, n

@@ -149,15 +149,16 @@ struct PrepSmem {
 
 // Partial q_n R_K over rows [32 kq, 32 kq + 32), channel t, for the first G
 // heads of sm.xs, into sm.zq[kq] (two sums per head, so that the
-// shared-memory loads and the multiply-adds overlap).
-template <int G>
-__device__ __forceinline__ void rotate_heads(PrepSmem& sm, const float* __restrict__ RK, int t, int kq) {
+// shared-memory loads and the multiply-adds overlap).  rk(ii) = R_K[32 kq + ii][t].
+template <int G, typename RowOf>
+__device__ __forceinline__ void rotate_heads(PrepSmem& sm, RowOf rk, int t, int kq) {
   float za[G], zb[G];
 #pragma unroll
   for (int n = 0; n < G; ++n) za[n] = zb[n] = 0.f;
 #pragma unroll
-  for (int i = 32 * kq; i < 32 * kq + 32; i += 4) {
-    const float r0 = RK[i * kD + t], r1 = RK[(i + 1) * kD + t], r2 = RK[(i + 2) * kD + t], r3 = RK[(i + 3) * kD + t];
+  for (int ii = 0; ii < 32; ii += 4) {
+    const int i = 32 * kq + ii;
+    const float r0 = rk(ii), r1 = rk(ii + 1), r2 = rk(ii + 2), r3 = rk(ii + 3);
 #pragma unroll
     for (int n = 0; n < G; ++n) {
       const float4 x = *reinterpret_cast<const float4*>(&sm.xs[n][i]);
@@ -169,22 +170,27 @@ __device__ __forceinline__ void rotate_heads(PrepSmem& sm, const float* __restri
   for (int n = 0; n < G; ++n) sm.zq[kq][n][t] = za[n] + zb[n];
 }
 
-__device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u, const float* __restrict__ RK,
-                                          PrepSmem& sm, int bar) {
+// q' = q R_K and the fragments of q' and q for (request b, KV head h), by
+// the kPrepThreads threads u of a group synchronised by named barrier `bar`.
+// rk(ii) = R_K[32 (u / 128) + ii][u % 128]; qbits(n) = the bf16 bits of
+// q[b][h g + n][u % 128] for n = u / 128 and u / 128 + 4 below g.  Outputs:
+// the history and BF16 fragment words (kQFragWords each) and the constants
+// (kQConstFloats).
+template <typename RowOf, typename QOf>
+__device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u, RowOf rk, QOf qbits, PrepSmem& sm,
+                                          int bar, uint32_t* qf, uint32_t* qpl, float* qc) {
   const int t = u & 127, kq = u >> 7, lane = u & 31, warp = u >> 5;
-  const int g = a.g, bh = b * a.Hkv + h;
+  const int g = a.g;
   const bool packed = g <= 4;
-  if (u == 0) a.counters[bh] = 0;
   const float c = a.sm_scale * kLog2e;
   // heads g .. G - 1 of the padded set are zero (G = 4 when g <= 4, else 8)
   const int G = packed ? 4 : kMaxG;
-  for (int n = kq; n < G; n += 4)
-    sm.xs[n][t] = n < g ? bf16_bits_to_float(a.q[((size_t)b * a.Hq + h * g + n) * kD + t]) : 0.f;
+  for (int n = kq; n < G; n += 4) sm.xs[n][t] = n < g ? bf16_bits_to_float(qbits(n)) : 0.f;
   group_sync(bar, kPrepThreads);
   if (packed)
-    rotate_heads<4>(sm, RK, t, kq);
+    rotate_heads<4>(sm, rk, t, kq);
   else
-    rotate_heads<kMaxG>(sm, RK, t, kq);
+    rotate_heads<kMaxG>(sm, rk, t, kq);
   group_sync(bar, kPrepThreads);
   // power-of-two normalisations: max |q'| 2^-E <= 2^10, max |q| 2^-Ep <= 2^10
   float mr = 0.f, mp = 0.f;
@@ -226,8 +232,6 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
   // (ks = 2 (i / 4) + (i % 4) % 2, byte parity pb = (i % 4) / 2), i.e.
   // channels 32 ks + 16 bs + 4 tig + pb and + 2 for b_bs.
   // BF16 segment: MMA ks = i takes channels 32 tig + 4 ks + {0,1} (b0) and {2,3} (b1).
-  uint32_t* qf = a.qfrag + (size_t)bh * kQFragWords;
-  uint32_t* qpl = a.qplain + (size_t)bh * kQFragWords;
   for (int e = u; e < kQFragWords; e += kPrepThreads) {
     const int L = e >> 5, w = e & 31, set = w >> 4, ww = w & 15, i = ww >> 1, bs = ww & 1;
     const int n = L >> 2, tig = L & 3;
@@ -246,7 +250,6 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
     qpl[e] = vp;
   }
   if (u == 0) {
-    float* qc = a.qconst + (size_t)bh * kQConstFloats;
     qc[16] = ldexpf(1.f, er);
     qc[17] = ldexpf(1.f, ep);
   }
@@ -257,62 +260,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(PrepArgs a) {
   __shared__ PrepSmem sm;
   griddep_wait();
   griddep_launch_dependents();
-  prep_body(a, blockIdx.y, blockIdx.x, threadIdx.x, a.R_K, sm, 1);
-}
-
-// Fused decode step, part 1: the decode append (K and V) and the q rotation
-// of one (KV head, request).  grid (Hkv, B, 3), 512 threads; blockIdx.z is
-// the role: 0 appends K, 1 appends V, 2 rotates q.  The block's rotation
-// (R_K, or R_V for role 1) is brought into shared memory by a bulk copy
-// while the previous kernel finishes (programmatic dependent launch).
-constexpr size_t kStepSmemBytes = kD * kD * sizeof(float) + 16;
-static_assert(kQuantThreads == kPrepThreads, "one block size for the three roles");
-
-__global__ void __launch_bounds__(kPrepThreads, 1) step_kernel(AppendLaunch ap, PrepArgs pr) {
-  extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ QuantSmem qsm;
-  __shared__ PrepSmem psm;
-  float* R = reinterpret_cast<float*>(dsm);
-  uint64_t* ubar = reinterpret_cast<uint64_t*>(R + kD * kD);
-  const int h = blockIdx.x, b = blockIdx.y, role = blockIdx.z, u = threadIdx.x;
-  if (u == 0) {
-    mbar_init(ubar, 1);
-    fence_mbar_init();
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(ubar, kD * kD * 4);
-    bulk_copy_g2s(R, role == 1 ? ap.rot.R_V : ap.rot.R_K, kD * kD * 4, ubar);
-  }
-  griddep_launch_dependents();
-  // while the kernel before this one finishes: pull this block's rows into L2
-  // (a hint only; everything is read again after the wait)
-  if (u < 32) {
-    const int lane = u, Hkv = ap.c.num_kv_heads;
-    const size_t row = ((size_t)b * Hkv + h) * kD;  // new K / V token rows, 256 bytes each
-    if (role == 2) {
-      if (lane < 2 * pr.g) prefetch_l2(pr.q + ((size_t)b * pr.Hq + h * pr.g) * kD + 64 * lane);
-    } else {
-      const uint16_t* src = role == 0 ? ap.k : ap.v;
-      if (lane < 2) prefetch_l2(src + row + 64 * lane);
-      const int p = ap.pos[b], slot = ap.c.ring_slot[b];
-      if (lane >= 2 && lane < 4 && p >= kSink + kRecent && slot >= 0 && slot < ap.c.num_ring) {  // the ring row to evict
-        const size_t r = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + 64 * (lane & 1);
-        prefetch_l2((role == 0 ? ap.c.k_ring : ap.c.v_ring) + r);
-      }
-      if (lane == 4 && p >= kSink + kRecent && ((p - kRecent) >> 6) < ap.c.max_pages)  // its page-table entry
-        prefetch_l2(ap.c.page_table + (size_t)b * ap.c.max_pages + ((p - kRecent) >> 6));
-    }
-  }
-  __syncthreads();
-  griddep_wait();
-  if (!mbar_wait_bounded(ubar, 0, kWaitLimit)) {
-    if (u == 0) set_error(ap.err, kErrTimeout);
-    mbar_wait_bounded(ubar, 0, kWaitLimit);
-    return;
-  }
-  if (role == 2)
-    prep_body(pr, b, h, u, R, psm, 1);
-  else
-    append_one_body(ap, b, h, role, u, R, R, qsm, 1);
+  const int b = blockIdx.y, h = blockIdx.x, u = threadIdx.x, bh = b * a.Hkv + h;
+  if (u == 0) a.counters[bh] = 0;
+  const float* RK = a.R_K + (size_t)32 * (u >> 7) * kD + (u & 127);
+  const uint16_t* qrow = a.q + ((size_t)b * a.Hq + h * a.g) * kD + (u & 127);
+  prep_body(a, b, h, u, [&](int ii) { return RK[ii * kD]; }, [&](int n) { return qrow[(size_t)n * kD]; }, sm, 1,
+            a.qfrag + (size_t)bh * kQFragWords, a.qplain + (size_t)bh * kQFragWords,
+            a.qconst + (size_t)bh * kQConstFloats);
 }
 
 // ------------------------------------------------------------------ decode
@@ -333,6 +287,13 @@ struct DecodeArgs {
   float pscale, inv_pscale;
   float* out;
   unsigned* err;
+};
+
+// The fused decode step's other inputs: the append of this step's token and
+// the q rotation.
+struct StepArgs {
+  AppendLaunch ap;
+  PrepArgs pr;
 };
 
 struct WarpState {
@@ -593,21 +554,25 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
 }
 
 // One 16-token BF16 tile (rows of K and V in global memory, original basis).
+// Row `sub` of the tile (-1: none) is read from knew / vnew instead.
 template <bool PACK4>
 __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
                                           int n_valid, const uint32_t* qpf, float scaleEp, WarpState& st,
-                                          int lane) {
+                                          int lane, int sub = -1, const uint16_t* knew = nullptr,
+                                          const uint16_t* vnew = nullptr) {
   const int q = lane >> 2, tig = lane & 3;
   const bool va = q < n_valid, vb = q + 8 < n_valid;
+  const uint16_t* krow_a = q == sub ? knew : Kt + q * kD;
+  const uint16_t* krow_b = q + 8 == sub ? knew : Kt + (q + 8) * kD;
   uint32_t ka[16], kb[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint4 u = va ? __ldg(reinterpret_cast<const uint4*>(Kt + q * kD + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+    uint4 u = va ? __ldg(reinterpret_cast<const uint4*>(krow_a + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
     ka[4 * k + 0] = bf16x2_to_f16x2(u.x);
     ka[4 * k + 1] = bf16x2_to_f16x2(u.y);
     ka[4 * k + 2] = bf16x2_to_f16x2(u.z);
     ka[4 * k + 3] = bf16x2_to_f16x2(u.w);
-    u = vb ? __ldg(reinterpret_cast<const uint4*>(Kt + (q + 8) * kD + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+    u = vb ? __ldg(reinterpret_cast<const uint4*>(krow_b + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
     kb[4 * k + 0] = bf16x2_to_f16x2(u.x);
     kb[4 * k + 1] = bf16x2_to_f16x2(u.y);
     kb[4 * k + 2] = bf16x2_to_f16x2(u.z);
@@ -657,8 +622,9 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
     for (int blkid = 0; blkid < 4; ++blkid) {
       const int tr = blkid >> 1, cc = blkid & 1;  // token half, channel half
       const bool ok = tr ? vb : va;
-      const uint32_t u =
-          ok ? __ldg(reinterpret_cast<const uint32_t*>(Vt + (8 * tr + q) * kD + 16 * mt + 8 * cc + 2 * tig)) : 0u;
+      const int r = 8 * tr + q;
+      const uint16_t* vrow = r == sub ? vnew : Vt + r * kD;
+      const uint32_t u = ok ? __ldg(reinterpret_cast<const uint32_t*>(vrow + 16 * mt + 8 * cc + 2 * tig)) : 0u;
       a[blkid] = movmatrix_trans(bf16x2_to_f16x2(u));
     }
     // a[0]: channels 16mt+q, tokens 2tig..; a[1]: channels +8; a[2]: tokens +8; a[3]: both
@@ -798,6 +764,7 @@ __device__ __noinline__ void final_merge(const DecodeArgs& a, uint8_t* smem, int
     }
     *reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + h * g + hn) * kD + 4 * lane) = res;
   }
+  if (t == 0) a.counters[bh] = 0;  // ready for the next launch on this workspace
 }
 
 // The block merge, after every warp of the block has stored its states.
@@ -811,7 +778,7 @@ __device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, con
   if (MODE == 0) {
     uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + kWarps * kStages + 1 + warp;
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(rbar, 0, kWaitLimit)) && lane == 0) set_error(a.err, kErrTimeout);
-    const float4* src = reinterpret_cast<const float4*>(smem + ((size_t)warp * kStages + kStages - 1) * kBlockBytes);
+    const float4* src = reinterpret_cast<const float4*>(smem + ((size_t)(kStages - 1) * kWarps + warp) * kBlockBytes);
 #pragma unroll
     for (int i = 0; i < kRows; ++i) rv[i] = src[i * (kD / 4) + lane];
   }
@@ -825,12 +792,12 @@ __device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, con
     constexpr int kG = PACK4 ? 4 : kMaxG;  // heads per KV head this variant serves
     constexpr int kHT = kG / 4;            // heads per thread
     const int ch = t & (kD - 1), n0 = t >> 7;
-    float* ystage = reinterpret_cast<float*>(smem + (size_t)(kStages - 1) * kBlockBytes);  // [kG][kD], warp 0's last stage
-    float* opart = reinterpret_cast<float*>(smem + (size_t)kStages * kBlockBytes);       // [kWarps][kG][kD]
+    float* ystage = reinterpret_cast<float*>(smem + (size_t)(kStages - 1) * kWarps * kBlockBytes);  // [kG][kD], warp 0's last stage
+    float* opart = reinterpret_cast<float*>(smem);  // [kWarps][kG][kD], over the first stages once the states are merged
     const float* rot = reinterpret_cast<const float*>(smem);  // warp states, stride: a warp's stage memory
-    const size_t rstride = (size_t)kStages * kBlockBytes / sizeof(float);
-    // original-basis states: the BF16 slots (mixed cache) or every warp's second state
-    const float* pln = MODE == 0 ? bf16_slots : rot + kPartialFloats;
+    const size_t rstride = kBlockBytes / sizeof(float);  // warp w's state: its first stage
+    // original-basis states: the BF16 slots (mixed cache) or every warp's second stage
+    const float* pln = MODE == 0 ? bf16_slots : rot + (size_t)kWarps * rstride;
     const size_t pstride = MODE == 0 ? (size_t)kPartialFloats : rstride;
     const int n_pln = MODE == 0 ? kBf16Slots : kWarps;
     float Mr[kHT], Lr[kHT], Mp[kHT], Lp[kHT], yp[kHT];
@@ -922,8 +889,40 @@ __device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, con
 
 }
 
-template <int MODE, bool PACK4>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
+// Fused decode step (FUSED, mixed cache only): the kernel also appends this
+// step's token and rotates q.  Before the dependency wait each thread loads
+// its rows of R_K; after it every block rotates q itself (its warps' last
+// stages serve as scratch while their first two units arrive); the block
+// owning the history page that receives the evicted token moves that token
+// in (and the new token into the ring or sink) and patches its own staged
+// copy of the page; BF16 tiles read the new token's row from the input.
+constexpr size_t kPatchOffset = (kSlotsOffset + (size_t)kBf16Slots * kPartialFloats * sizeof(float) + 15) / 16 * 16;
+
+struct FusedScratch {  // in the warps' last stages
+  PrepSmem prep;
+  QuantSmem quant;
+  uint32_t qf[kQFragWords];
+  uint32_t qpl[kQFragWords];
+  float qc[kQConstFloats];
+};
+static_assert(sizeof(FusedScratch) <= (size_t)kWarps * kBlockBytes, "fused scratch in the last stages");
+
+// lanes 0..27 write the row's K words, V halves and scales into a staged block
+__device__ __forceinline__ void apply_patch(uint8_t* blk, const RowPatch& pt, int row, int lane) {
+  if (lane < 8) {
+    *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, lane & 3, lane >> 2)) = pt.kword[lane];
+  } else if (lane < 24) {
+    *reinterpret_cast<uint16_t*>(blk + kVCodes + v_half_offset(row, lane - 8)) = pt.vhalf[lane - 8];
+  } else if (lane < 26) {
+    *reinterpret_cast<uint16_t*>(blk + kKScales + 4 * row + 2 * (lane - 24)) = pt.kscale[lane - 24];
+  } else if (lane < 28) {
+    *reinterpret_cast<uint16_t*>(blk + kVScales + 4 * row + 2 * (lane - 26)) = pt.vscale[lane - 26];
+  }
+}
+
+template <int MODE, bool PACK4, bool FUSED>
+__device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs* f) {
+  static_assert(!FUSED || MODE == 0, "the fused step serves the mixed cache");
   extern __shared__ __align__(128) uint8_t smem[];
   const int item = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -950,6 +949,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
   }
+  float rk[FUSED ? 32 : 1];  // fused step: R_K[32 (t / 128) + ii][t % 128] (a constant of the layer)
+  if constexpr (FUSED) {
+    const float* RK = f->pr.R_K + (size_t)32 * (t >> 7) * kD + (t & 127);
+#pragma unroll
+    for (int ii = 0; ii < 32; ++ii) rk[ii] = __ldg(RK + ii * kD);
+  }
   griddep_wait();
   int L = a.ctx_len[b];
   if (L < 0) {
@@ -959,8 +964,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   constexpr int kQW = PACK4 ? 16 : 32;
   // warp-private stage memory; after the warp's pages are done it holds the
   // warp's two finished states (rotated basis, original basis)
-  uint8_t* stages = smem + (size_t)warp * kStages * kBlockBytes;
-  float* wstate = reinterpret_cast<float*>(stages);
+  // stage s of warp w: smem + (s kWarps + w) kBlockBytes (the warps' last
+  // stages form one block)
+  auto stage_ptr = [&](int s) -> uint8_t* { return smem + ((size_t)s * kWarps + warp) * kBlockBytes; };
+  float* wstate = reinterpret_cast<float*>(stage_ptr(0));
   float* bf16_slots = reinterpret_cast<float*>(smem + kSlotsOffset);  // [kBf16Slots][kPartialFloats]
   WarpState st;
 
@@ -981,6 +988,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     const int R = (lp1 - lp0) / kWarps, E = (lp1 - lp0) - R * kWarps;
     const int n_tiles = 4 * E > warp ? (4 * E - warp + kWarps - 1) / kWarps : 0;
     const int n_my = R + n_tiles;
+    // fused step: the loads the q rotation and the append wait on go first
+    int p_new = -1, owner = 0, e_lp = -1, e_T = -1, e_row = -1;  // the new token; the evicted row to patch
+    uint16_t qb0 = 0, qb1 = 0;
+    float rvr[FUSED ? 32 : 1];  // the append block: R_V[32 (t / 128) + ii][t % 128]
+    if constexpr (FUSED) {
+      const int kq = t >> 7;
+      const uint16_t* qrow = f->pr.q + ((size_t)b * f->pr.Hq + h * a.g) * kD + (t & 127);
+      if (kq < a.g) qb0 = qrow[(size_t)kq * kD];
+      if (kq + 4 < a.g) qb1 = qrow[(size_t)(kq + 4) * kD];
+      p_new = f->ap.pos[b];
+      if (p_new >= kSink + kRecent) {
+        const int e = p_new - kRecent, lpe = e >> 6;
+        if (lpe >= 1 && lpe < 1 + n_hist_ok) owner = (lpe - 1) / a.chunk_pages;
+        e_lp = lpe;
+        e_T = (e & 63) >> 4;
+        e_row = e & 63;
+      }
+      if (item == owner) {
+        const float* RV = f->ap.rot.R_V + (size_t)32 * kq * kD + (t & 127);
+#pragma unroll
+        for (int ii = 0; ii < 32; ++ii) rvr[ii] = __ldg(RV + ii * kD);
+      }
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + warp * kStages;
     const uint8_t* pool = c.pages;
       // unit k: logical page and tile (-1: the whole page)
@@ -1007,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         const int s = k % kStages;
         int lp, T;
         unit_of(k, lp, T);
-        uint8_t* dst = stages + (size_t)s * kBlockBytes;
+        uint8_t* dst = stage_ptr(s);
         if (ph < 0) {
           set_error(a.err, kErrPage);
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&bars[s])) : "memory");
@@ -1030,7 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     bool rv_issued = false;  // lane 0
     auto issue_rv = [&]() {  // lane 0, once the last stage is free for good
       mbar_arrive_expect_tx(rbar, kRvBytes);
-      bulk_copy_g2s(stages + (size_t)(kStages - 1) * kBlockBytes, a.R_VT + (size_t)kRvRows * warp * kD, kRvBytes, rbar);
+      bulk_copy_g2s(stage_ptr(kStages - 1), a.R_VT + (size_t)kRvRows * warp * kD, kRvBytes, rbar);
       rv_issued = true;
     };
     if (lane == 0) {
@@ -1040,29 +1070,85 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       fence_proxy_async_smem();
     }
     __syncwarp();
-    if (lane == 0 && n_my < kStages) issue_rv();
+    // (fused step: the last stages are scratch until the rotation and the
+    // append are done; only the first kStages - 1 units are issued before)
+    constexpr int kFirst = FUSED ? kStages - 1 : kStages;
+    if (!FUSED && lane == 0 && n_my < kStages) issue_rv();
     // bit s: stage s holds a valid unit.  The page-table entry of unit
     // k + kStages is read during unit k - 1, so that issuing its copy after
     // unit k waits on nothing.
     uint32_t valid = 0;
-    int ph_ahead = -1;
+    int ph_ahead = -1, ph_late = -1;
     if (n_my > 0) {
-      for (int k = 0; k < min(kStages, n_my); ++k) {
-        const int ph = phys_unit(k);
-        valid |= (ph >= 0 ? 1u : 0u) << k;
-        if (lane == 0) issue(k, ph);
-      }
+      // the entries first: the copies' asm keeps later loads from moving above them
+      int phs[kStages];
+#pragma unroll
+      for (int k = 0; k < kStages; ++k) phs[k] = k < n_my ? phys_unit(k) : -1;
       if (kStages < n_my) ph_ahead = phys_unit(kStages);
+#pragma unroll
+      for (int k = 0; k < kStages; ++k) {
+        if (k >= n_my) break;
+        valid |= (phs[k] >= 0 ? 1u : 0u) << k;
+        if (k < kFirst) {
+          if (lane == 0) issue(k, phs[k]);
+        } else {
+          ph_late = phs[k];
+        }
+      }
+    }
+    uint32_t qf[kQW], qpf[kQW];
+    float scaleE = 0.f, scaleEp = 0.f;
+    const bool bf16_warp = kWarps - 1 - warp < kBf16Slots;
+    if constexpr (FUSED) {
+      FusedScratch& fs = *reinterpret_cast<FusedScratch*>(smem + (size_t)(kStages - 1) * kWarps * kBlockBytes);
+      RowPatch* patch = reinterpret_cast<RowPatch*>(smem + kPatchOffset);
+      prep_body(
+          f->pr, b, h, t, [&](int ii) { return rk[ii]; }, [&](int n) { return n == (t >> 7) ? qb0 : qb1; }, fs.prep,
+          1, fs.qf, fs.qpl, fs.qc);
+      // the append, by the block whose pages hold the evicted token's row (else item 0)
+      if (item == owner) {
+        if (t == 0) patch->row = -1;
+        append_pair_body(
+            f->ap, b, h, t, [&](int ii) { return rk[ii]; }, [&](int ii) { return rvr[ii]; }, fs.quant, 1, patch);
+      }
+      __syncthreads();
+      if (item != owner || patch->row != e_row) e_lp = -1;  // no staged row to patch
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(fs.qf + lane * 32);
+        const uint4* srcp = reinterpret_cast<const uint4*>(fs.qpl + lane * 32);
+#pragma unroll
+        for (int k = 0; k < kQW / 4; ++k) {
+          const uint4 u = src[k];
+          qf[4 * k] = u.x;
+          qf[4 * k + 1] = u.y;
+          qf[4 * k + 2] = u.z;
+          qf[4 * k + 3] = u.w;
+          const uint4 v = bf16_warp ? srcp[k] : make_uint4(0, 0, 0, 0);
+          qpf[4 * k] = v.x;
+          qpf[4 * k + 1] = v.y;
+          qpf[4 * k + 2] = v.z;
+          qpf[4 * k + 3] = v.w;
+        }
+        scaleE = fs.qc[16];
+        scaleEp = fs.qc[17];
+      }
+      __syncthreads();  // the scratch is released
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        if (n_my >= kStages)
+          issue(kStages - 1, ph_late);
+        else
+          issue_rv();
+      }
     }
     // BF16 sink/recent tiles (original basis) while the first pages arrive:
     // local tile k of this item goes to warp kWarps - 1 - k % kBf16Slots,
     // whose state waits in its slot until the block merge
-    if (kWarps - 1 - warp < kBf16Slots) {
+    if (bf16_warp) {
       const int bk = kWarps - 1 - warp;
       state_init(st);
       if (bk < a.tiles_per_item && item * a.tiles_per_item + bk < kBf16Tiles) {
-        uint32_t qpf[kQW];
-        {
+        if (!FUSED) {
           const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
 #pragma unroll
           for (int k = 0; k < kQW / 4; ++k) {
@@ -1072,8 +1158,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
             qpf[4 * k + 2] = u.z;
             qpf[4 * k + 3] = u.w;
           }
+          scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
         }
-        const float scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
         const int sp = c.sink_page[b], slot = c.ring_slot[b];
         const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
         for (int k = bk; k < a.tiles_per_item; k += kBf16Slots) {
@@ -1089,16 +1175,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           }
           const size_t off = ring ? ((((size_t)slot * a.Hkv + h) * kRecent + row_off) * kD)
                                   : ((((size_t)sp * a.Hkv + h) * kSink + row_off) * kD);
+          // fused step: the new token's row comes from the input
+          int sub = -1;
+          if (FUSED && p_new >= 0) {
+            const int rr = p_new < kSink ? p_new : (p_new - kSink) % kRecent;
+            if (ring == (p_new >= kSink) && (ring ? 4 + rr / 16 : rr / 16) == j) sub = rr % 16;
+          }
+          const size_t nrow = ((size_t)b * a.Hkv + h) * kD;
           bf16_tile<PACK4>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, nv, qpf, scaleEp,
-                           st, lane);
+                           st, lane, sub, FUSED ? f->ap.k + nrow : nullptr, FUSED ? f->ap.v + nrow : nullptr);
         }
       }
       store_state<PACK4>(st, bf16_slots + (size_t)bk * kPartialFloats, 1.0f / kPScaleBF16, lane);
     }
     state_init(st);
     if (n_my > 0) {
-      uint32_t qf[kQW];
-      {
+      if (!FUSED) {
         const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bh * kQFragWords + lane * 32);
 #pragma unroll
         for (int k = 0; k < kQW / 4; ++k) {
@@ -1108,8 +1200,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           qf[4 * k + 2] = u.z;
           qf[4 * k + 3] = u.w;
         }
+        scaleE = __ldg(a.qconst + (size_t)bh * kQConstFloats + 16);
       }
-      const float scaleE = __ldg(a.qconst + (size_t)bh * kQConstFloats + 16);
       const float kp = log2f(a.pscale);
       int k = 0;
       for (; k < n_my; ++k) {
@@ -1122,7 +1214,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         int lp, T;
         unit_of(k, lp, T);
         if ((valid >> s) & 1u) {
-          const uint8_t* blk = stages + (size_t)s * kBlockBytes;
+          uint8_t* blk = stage_ptr(s);
+          if (FUSED && lp == e_lp && (T < 0 || T == e_T)) {  // the row the append just evicted
+            apply_patch(blk, *reinterpret_cast<const RowPatch*>(smem + kPatchOffset), e_row, lane);
+            __syncwarp();
+          }
           const int n_valid = min(kPage, hist_end - kPage * lp);
           if (T < 0) {
             if (n_valid == kPage)
@@ -1203,7 +1299,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, nv, qpf, scaleEp, st, lane);
       }
     }
-    store_state<PACK4>(st, wstate + kPartialFloats, 1.0f / kPScaleBF16, lane);
+    store_state<PACK4>(st, reinterpret_cast<float*>(stage_ptr(1)), 1.0f / kPScaleBF16, lane);
   }
   block_merge<MODE, PACK4>(a, smem, bf16_slots, bh, item);
 
@@ -1221,15 +1317,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   final_merge<PACK4>(a, smem, b, h, bh);
 }
 
+template <int MODE, bool PACK4>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+  decode_body<MODE, PACK4, false>(a, nullptr);
+}
+
+template <bool PACK4>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_step_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ StepArgs f) {
+  decode_body<0, PACK4, true>(a, &f);
+}
+
 constexpr size_t decode_smem_bytes() { return kSlotsOffset + (size_t)kBf16Slots * kPartialFloats * sizeof(float); }
-// two finished warp states fit in a warp's stage memory; the block merge's
-// partial products with R_V^T fit in the stage memory of warps 1 .. 15; the
+// a warp state fits in one stage (the rotated-basis one in the warp's first
+// stage, the comparator's original-basis one in its second); the block
+// merge's partial products with R_V^T fit in the first two stages of all
+// warps, below warp 0's last stage, which holds the staged accumulators; the
 // final merge's stash fits in all of it
-static_assert(2 * kPartialFloats * 4 <= kStages * kBlockBytes, "warp states");
-static_assert(kPartialFloats * 4 <= (kStages - 1) * kBlockBytes && kRvBytes <= kBlockBytes &&
-                  kMaxG * kD * 4 <= kBlockBytes,
-              "mixed cache: a warp's state before its last stage, which holds its R_V^T rows, then the staged accumulators");
-static_assert(kStages * kBlockBytes + kWarps * kMaxG * kD * 4 <= kWarps * kStages * kBlockBytes, "block merge products");
+static_assert(kPartialFloats * 4 <= kBlockBytes && kRvBytes <= kBlockBytes && kMaxG * kD * 4 <= kBlockBytes,
+              "states, R_V^T rows and staged accumulators in one stage");
+static_assert(kWarps * kMaxG * kD * 4 <= (kStages - 1) * kWarps * kBlockBytes, "block merge products");
 static_assert(kWarps * kStash * 4 <= kWarps * kStages * kBlockBytes, "final merge stash");
 static_assert(kWarps * kStages * kBlockBytes / 4 / (16 + 128 * kMaxG) >= 1, "a record batch holds a record");
 
@@ -1315,8 +1422,7 @@ PrepArgs prep_args_of(const DecodeLaunch& d) {
   return pa;
 }
 
-// the split-K decode kernel (after its prep has been queued)
-cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cudaStream_t stream) {
+DecodeArgs decode_args_of(const DecodeLaunch& d, const PrepArgs& pa) {
   const DecodePlan& p = d.plan;
   uint8_t* ws = d.workspace;
   DecodeArgs a;
@@ -1349,6 +1455,13 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
   }
   a.out = d.out;
   a.err = d.err;
+  return a;
+}
+
+// the split-K decode kernel (after its prep has been queued)
+cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cudaStream_t stream) {
+  const DecodePlan& p = d.plan;
+  DecodeArgs a = decode_args_of(d, pa);
   const size_t smem = decode_smem_bytes();
   const dim3 grid(p.n_items, p.Hkv, p.batch);
   const bool pack4 = p.g <= 4;
@@ -1381,20 +1494,23 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
 cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cudaStream_t stream) {
   const DecodePlan& p = d.plan;
   if (p.batch == 0) return cudaSuccess;
-  PrepArgs pa = prep_args_of(d);
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStepSmemBytes);
+  const PrepArgs pa = prep_args_of(d);
+  DecodeArgs a = decode_args_of(d, pa);
+  StepArgs sa;
+  sa.ap = ap;
+  sa.pr = pa;
+  const size_t smem = kPatchOffset + sizeof(RowPatch);
+  const bool pack4 = p.g <= 4;
+  void (*kern)(DecodeArgs, StepArgs) = pack4 ? decode_step_kernel<true> : decode_step_kernel<false>;
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[pack4 ? 1 : 0]) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr_done[pack4 ? 1 : 0] = true;
   }
-  AppendLaunch apc = ap;
-  void* args[] = {&apc, &pa};
-  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(step_kernel), dim3(p.Hkv, p.batch, 3), dim3(kPrepThreads),
-                             kStepSmemBytes, stream, args);
-  if (e != cudaSuccess) return e;
-  return launch_decode_kernel(d, pa, stream);
+  void* args[] = {&a, &sa};
+  return launch_pdl(reinterpret_cast<const void*>(kern), dim3(p.n_items, p.Hkv, p.batch), dim3(kThreads), smem,
+                    stream, args);
 }
 
 }  // namespace oscar

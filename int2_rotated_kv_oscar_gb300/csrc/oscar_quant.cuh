@@ -53,6 +53,15 @@ struct QuantSmem {
 
 constexpr int kQuantThreads = 512;  // threads per token: channel t = u % 128, row quarter u / 128
 
+// The packed bytes one token adds to a block, as quantize_token stores them
+// (for a reader that already holds a copy of the block from before the store).
+struct RowPatch {
+  uint32_t kword[8];   // K word (tq, kp) = (i % 4, i / 4) of the row
+  uint16_t vhalf[16];  // V half of channels {jj + 16 r : r = 0..7}, jj = i
+  uint16_t kscale[2], vscale[2];
+  int row;  // the block row these bytes belong to (-1: none)
+};
+
 // Rotate + clip + quantise one token and store its codes and scale in row
 // `row` of the K or V part of `block`.  Called by the kQuantThreads threads
 // u of a group synchronised by named barrier `bar`; x: the token's channel
@@ -60,19 +69,21 @@ constexpr int kQuantThreads = 512;  // threads per token: channel t = u % 128, r
 // rotation (global or shared memory).  Thread u forms the partial product of
 // rows [32 (u / 128), 32 (u / 128) + 32) of R for channel u % 128; the four
 // partials are added in quarter order.
-__device__ __forceinline__ void quantize_token(float x, const float* __restrict__ R, float tau, uint8_t* block,
-                                               int row, bool is_v, QuantSmem& sm, int u, int bar) {
+// rr(ii) = R[32 (u / 128) + ii][u % 128] (from memory or from registers).
+template <typename RowOf>
+__device__ __forceinline__ void quantize_token(float x, RowOf rr, float tau, uint8_t* block, int row, bool is_v,
+                                               QuantSmem& sm, int u, int bar, RowPatch* patch = nullptr) {
   const int t = u & 127, kq = u >> 7, lane = u & 31, warp = (u >> 5) & 3;
   if (kq == 0) sm.x[t] = x;
   group_sync(bar, kQuantThreads);
   float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-  for (int i = 32 * kq; i < 32 * kq + 32; i += 4) {
-    const float4 xv = *reinterpret_cast<const float4*>(&sm.x[i]);
-    z0 = fmaf(xv.x, R[i * kD + t], z0);
-    z1 = fmaf(xv.y, R[(i + 1) * kD + t], z1);
-    z0 = fmaf(xv.z, R[(i + 2) * kD + t], z0);
-    z1 = fmaf(xv.w, R[(i + 3) * kD + t], z1);
+  for (int ii = 0; ii < 32; ii += 4) {
+    const float4 xv = *reinterpret_cast<const float4*>(&sm.x[32 * kq + ii]);
+    z0 = fmaf(xv.x, rr(ii), z0);
+    z1 = fmaf(xv.y, rr(ii + 1), z1);
+    z0 = fmaf(xv.z, rr(ii + 2), z0);
+    z1 = fmaf(xv.w, rr(ii + 3), z1);
   }
   sm.zq[kq][t] = z0 + z1;
   group_sync(bar, kQuantThreads);
@@ -93,19 +104,34 @@ __device__ __forceinline__ void quantize_token(float x, const float* __restrict_
   group_sync(bar, kQuantThreads);
   if (kq != 0) {
   } else if (!is_v) {
-    if (t < 8)
-      *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, t & 3, t >> 2)) = k_word(sm.code, t & 3, t >> 2);
+    if (t < 8) {
+      const uint32_t kw = k_word(sm.code, t & 3, t >> 2);
+      *reinterpret_cast<uint32_t*>(block + kKCodes + k_word_offset(row, t & 3, t >> 2)) = kw;
+      if (patch != nullptr) patch->kword[t] = kw;
+    }
   } else {
     if (t < 16) {
       uint32_t hv = 0;
 #pragma unroll
       for (int r = 0; r < 8; ++r) hv |= (uint32_t)sm.code[t + 16 * r] << (2 * r);
       *reinterpret_cast<uint16_t*>(block + kVCodes + v_half_offset(row, t)) = (uint16_t)hv;
+      if (patch != nullptr) patch->vhalf[t] = (uint16_t)hv;
     }
   }
-  if (kq == 0 && (t & 63) == 0)
+  if (kq == 0 && (t & 63) == 0) {
     *reinterpret_cast<__half*>(block + (is_v ? kVScales : kKScales) + 4 * row + 2 * grp) = sh;
+    if (patch != nullptr) (is_v ? patch->vscale : patch->kscale)[grp] = __half_as_ushort(sh);
+  }
+  if (patch != nullptr && u == 0) patch->row = row;
   group_sync(bar, kQuantThreads);
+}
+
+// R: the layer's composite rotation, row-major in global or shared memory.
+__device__ __forceinline__ void quantize_token(float x, const float* __restrict__ R, float tau, uint8_t* block,
+                                               int row, bool is_v, QuantSmem& sm, int u, int bar,
+                                               RowPatch* patch = nullptr) {
+  const float* col = R + (size_t)32 * (u >> 7) * kD + (u & 127);
+  quantize_token(x, [&](int ii) { return col[ii * kD]; }, tau, block, row, is_v, sm, u, bar, patch);
 }
 
 // Locate (and check) the INT2 block of position e of request b, head h.
@@ -129,7 +155,8 @@ __device__ __forceinline__ uint8_t* history_block(const CacheRefs& c, int b, int
 // (position < 64) or its ring row; a position >= 320 first moves the ring
 // row's old token (position - 256) into its INT2 history row.
 __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, int h, int half, int u,
-                                                const float* Rk, const float* Rv, QuantSmem& sm, int bar) {
+                                                const float* Rk, const float* Rv, QuantSmem& sm, int bar,
+                                                RowPatch* patch = nullptr) {
   const bool is_v = half == 1;
   const int t = u & 127;
   const bool mover = u < kD;
@@ -165,9 +192,61 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
     uint8_t* blk = history_block(c, b, h, e, a.err);
     if (blk != nullptr)
       quantize_token(bf16_bits_to_float(xo), is_v ? Rv : Rk, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v,
-                     sm, u, bar);
+                     sm, u, bar, patch);
   }
   if (mover) ring[rdst] = xn;
+}
+
+// The decode append of append_one_body for K and then V of one (request b,
+// KV head h), by one kQuantThreads group, with the loads of both halves
+// issued together and R_K / R_V given by rk / rv as for quantize_token (the
+// same arithmetic, so the same bytes); the evicted row's bytes also go to
+// *patch.
+template <typename RowK, typename RowV>
+__device__ __forceinline__ void append_pair_body(const AppendLaunch& a, int b, int h, int u, RowK rk, RowV rv,
+                                                 QuantSmem& sm, int bar, RowPatch* patch) {
+  const CacheRefs& c = a.c;
+  const int Hkv = c.num_kv_heads, t = u & 127;
+  const bool mover = u < kD;
+  const int p = a.pos[b];
+  const int slot = c.ring_slot[b];
+  const size_t nrow = ((size_t)b * Hkv + h) * kD + t;
+  const uint16_t xk = a.k[nrow], xv = a.v[nrow];
+  if (p < 0 || ((a.flags & 1u) && p > kSink)) {
+    if (threadIdx.x == 0) set_error(a.err, kErrLength);
+    return;
+  }
+  if (p < kSink) {
+    const int sp = c.sink_page[b];
+    if (sp < 0 || sp >= c.num_sink) {
+      if (threadIdx.x == 0) set_error(a.err, kErrSink);
+      return;
+    }
+    const size_t d = (((size_t)sp * Hkv + h) * kSink + p) * kD + t;
+    if (mover) {
+      c.k_sink[d] = xk;
+      c.v_sink[d] = xv;
+    }
+    return;
+  }
+  if (slot < 0 || slot >= c.num_ring) {
+    if (threadIdx.x == 0) set_error(a.err, kErrRing);
+    return;
+  }
+  const size_t rdst = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
+  if (p >= kSink + kRecent) {
+    const int e = p - kRecent;
+    const uint16_t ok = c.k_ring[rdst], ov = c.v_ring[rdst];  // in flight while the page table is read
+    uint8_t* blk = history_block(c, b, h, e, a.err);
+    if (blk != nullptr) {
+      quantize_token(bf16_bits_to_float(ok), rk, a.rot.tau_k, blk, e & 63, false, sm, u, bar, patch);
+      quantize_token(bf16_bits_to_float(ov), rv, a.rot.tau_v, blk, e & 63, true, sm, u, bar, patch);
+    }
+  }
+  if (mover) {
+    c.k_ring[rdst] = xk;
+    c.v_ring[rdst] = xv;
+  }
 }
 
 }  // namespace

@@ -1,6 +1,6 @@
 """GPU: the fused decode step (oscar_decode_step) against its two parts.
 
-oscar_decode_step appends one token per request and decodes in two launches;
+oscar_decode_step appends one token per request and decodes in one launch;
 its results must be bit-identical to oscar_kv_append followed by
 oscar_decode_attention on the same inputs (the same arithmetic runs in both),
 for every cache byte and every output value, while requests cross the sink
