@@ -246,8 +246,11 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
       const int cp = 32 * tig + 4 * i + 2 * bs;
       vp = pack_f16x2(split_part(sm.qp[head][cp] * sp, part), split_part(sm.qp[head][cp + 1] * sp, part));
     }
-    qf[e] = vr;
-    qpl[e] = vp;
+    // 16-byte chunk c of lane L's row stored at chunk c ^ (L % 8): the readers'
+    // 16-byte loads of one chunk index spread over all banks
+    const int ep = (e & ~31) | ((((e >> 2) & 7) ^ (L & 7)) << 2) | (e & 3);
+    qf[ep] = vr;
+    qpl[ep] = vp;
   }
   if (u == 0) {
     qc[16] = ldexpf(1.f, er);
@@ -554,16 +557,16 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
 }
 
 // One 16-token BF16 tile (rows of K and V in global memory, original basis).
-// Row `sub` of the tile (-1: none) is read from knew / vnew instead.
-template <bool PACK4>
+// SUB: row `sub` of the tile (-1: none) is read from knew / vnew instead.
+template <bool PACK4, bool SUB = false>
 __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
                                           int n_valid, const uint32_t* qpf, float scaleEp, WarpState& st,
                                           int lane, int sub = -1, const uint16_t* knew = nullptr,
                                           const uint16_t* vnew = nullptr) {
   const int q = lane >> 2, tig = lane & 3;
   const bool va = q < n_valid, vb = q + 8 < n_valid;
-  const uint16_t* krow_a = q == sub ? knew : Kt + q * kD;
-  const uint16_t* krow_b = q + 8 == sub ? knew : Kt + (q + 8) * kD;
+  const uint16_t* krow_a = SUB && q == sub ? knew : Kt + q * kD;
+  const uint16_t* krow_b = SUB && q + 8 == sub ? knew : Kt + (q + 8) * kD;
   uint32_t ka[16], kb[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -623,7 +626,7 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
       const int tr = blkid >> 1, cc = blkid & 1;  // token half, channel half
       const bool ok = tr ? vb : va;
       const int r = 8 * tr + q;
-      const uint16_t* vrow = r == sub ? vnew : Vt + r * kD;
+      const uint16_t* vrow = SUB && r == sub ? vnew : Vt + r * kD;
       const uint32_t u = ok ? __ldg(reinterpret_cast<const uint32_t*>(vrow + 16 * mt + 8 * cc + 2 * tig)) : 0u;
       a[blkid] = movmatrix_trans(bf16x2_to_f16x2(u));
     }
@@ -651,8 +654,8 @@ __device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      dst[16 + tig * kD + 16 * mt + q] = (st.acc[mt][0] + st.acc[mt][1]) * inv;
-      dst[16 + tig * kD + 16 * mt + q + 8] = (st.acc[mt][2] + st.acc[mt][3]) * inv;
+      dst[16 + tig * kStateStride + 16 * mt + q] = (st.acc[mt][0] + st.acc[mt][1]) * inv;
+      dst[16 + tig * kStateStride + 16 * mt + q + 8] = (st.acc[mt][2] + st.acc[mt][3]) * inv;
     }
     return;
   }
@@ -667,7 +670,7 @@ __device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ch = 16 * mt + q + 8 * (i >> 1), n = 2 * tig + (i & 1);
-      dst[16 + n * kD + ch] = st.acc[mt][i] * inv;
+      dst[16 + n * kStateStride + ch] = st.acc[mt][i] * inv;
     }
   }
 }
@@ -816,7 +819,7 @@ __device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, con
           for (int w = 0; w < kWarps; ++w) {
             const float* ws = rot + w * rstride;
             const float al = ex2(ws[n] - Mr[k]);  // 0 for an empty warp state (m = -inf)
-            yr = fmaf(al, ws[16 + n * kD + ch], yr);
+            yr = fmaf(al, ws[16 + n * kStateStride + ch], yr);
             Lr[k] = fmaf(al, ws[8 + n], Lr[k]);
           }
         }
@@ -831,7 +834,7 @@ __device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, con
           if (w >= n_pln) break;
           const float* ws = pln + w * pstride;
           const float al = ex2(ws[n] - Mp[k]);
-          yp[k] = fmaf(al, ws[16 + n * kD + ch], yp[k]);
+          yp[k] = fmaf(al, ws[16 + n * kStateStride + ch], yp[k]);
           Lp[k] = fmaf(al, ws[8 + n], Lp[k]);
         }
       }
@@ -1118,12 +1121,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
         const uint4* srcp = reinterpret_cast<const uint4*>(fs.qpl + lane * 32);
 #pragma unroll
         for (int k = 0; k < kQW / 4; ++k) {
-          const uint4 u = src[k];
+          const uint4 u = src[k ^ (lane & 7)];
           qf[4 * k] = u.x;
           qf[4 * k + 1] = u.y;
           qf[4 * k + 2] = u.z;
           qf[4 * k + 3] = u.w;
-          const uint4 v = bf16_warp ? srcp[k] : make_uint4(0, 0, 0, 0);
+          const uint4 v = bf16_warp ? srcp[k ^ (lane & 7)] : make_uint4(0, 0, 0, 0);
           qpf[4 * k] = v.x;
           qpf[4 * k + 1] = v.y;
           qpf[4 * k + 2] = v.z;
@@ -1152,7 +1155,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
           const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
 #pragma unroll
           for (int k = 0; k < kQW / 4; ++k) {
-            const uint4 u = __ldg(src + k);
+            const uint4 u = __ldg(src + (k ^ (lane & 7)));
             qpf[4 * k] = u.x;
             qpf[4 * k + 1] = u.y;
             qpf[4 * k + 2] = u.z;
@@ -1182,8 +1185,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
             if (ring == (p_new >= kSink) && (ring ? 4 + rr / 16 : rr / 16) == j) sub = rr % 16;
           }
           const size_t nrow = ((size_t)b * a.Hkv + h) * kD;
-          bf16_tile<PACK4>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, nv, qpf, scaleEp,
-                           st, lane, sub, FUSED ? f->ap.k + nrow : nullptr, FUSED ? f->ap.v + nrow : nullptr);
+          bf16_tile<PACK4, FUSED>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, nv, qpf,
+                                  scaleEp, st, lane, sub, FUSED ? f->ap.k + nrow : nullptr,
+                                  FUSED ? f->ap.v + nrow : nullptr);
         }
       }
       store_state<PACK4>(st, bf16_slots + (size_t)bk * kPartialFloats, 1.0f / kPScaleBF16, lane);
@@ -1194,7 +1198,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
         const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bh * kQFragWords + lane * 32);
 #pragma unroll
         for (int k = 0; k < kQW / 4; ++k) {
-          const uint4 u = __ldg(src + k);
+          const uint4 u = __ldg(src + (k ^ (lane & 7)));
           qf[4 * k] = u.x;
           qf[4 * k + 1] = u.y;
           qf[4 * k + 2] = u.z;
@@ -1270,7 +1274,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
       const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
 #pragma unroll
       for (int k = 0; k < kQW / 4; ++k) {
-        const uint4 u = __ldg(src + k);
+        const uint4 u = __ldg(src + (k ^ (lane & 7)));
         qpf[4 * k] = u.x;
         qpf[4 * k + 1] = u.y;
         qpf[4 * k + 2] = u.z;

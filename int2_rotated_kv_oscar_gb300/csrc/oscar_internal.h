@@ -64,7 +64,10 @@ struct DecodePlan {
   size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
 };
 
-constexpr int kPartialFloats = 16 + 8 * 128;   // m[8], l[8], acc[8][128]: a warp state in shared memory
+// a warp state in shared memory: m[8], l[8], acc[8][kStateStride] (a head's
+// 128 channels, padded so that the packed state stores hit distinct banks)
+constexpr int kStateStride = 128 + 8;
+constexpr int kPartialFloats = 16 + 8 * kStateStride;
 // a partial record in the workspace: m[8], l[8], acc[g][128]
 constexpr int partial_record_floats(int g) { return 16 + 128 * g; }
 constexpr int kQConstFloats = 32;
