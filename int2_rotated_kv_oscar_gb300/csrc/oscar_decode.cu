@@ -142,9 +142,7 @@ constexpr int kPrepThreads = 512;  // channel t = u % 128, row quarter u / 128 o
 struct PrepSmem {
   __align__(16) float xs[kMaxG][kD];
   float zq[4][kMaxG][kD];  // partial products over the four quarters of the rows of R_K
-  float qr[kMaxG][kD];
-  float qp[kMaxG][kD];
-  float red[2 * kPrepThreads / 32];
+  float red[kPrepThreads / 32];
 };
 
 // Partial q_n R_K over rows [32 kq, 32 kq + 32), channel t, for the first G
@@ -183,50 +181,40 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
   const int g = a.g;
   const bool packed = g <= 4;
   const float c = a.sm_scale * kLog2e;
-  // heads g .. G - 1 of the padded set are zero (G = 4 when g <= 4, else 8)
+  // heads g .. G - 1 of the padded set are zero (G = 4 when g <= 4, else 8);
+  // the sum of squares over the heads: sqrt of it bounds every |q| and, the
+  // rotation keeping lengths, every |q'|
   const int G = packed ? 4 : kMaxG;
-  for (int n = kq; n < G; n += 4) sm.xs[n][t] = n < g ? bf16_bits_to_float(qbits(n)) : 0.f;
+  float ss = 0.f;
+  for (int n = kq; n < G; n += 4) {
+    const float x = n < g ? bf16_bits_to_float(qbits(n)) : 0.f;
+    sm.xs[n][t] = x;
+    ss = fmaf(x, x, ss);
+  }
+  ss = warp_sum(ss);
+  constexpr int kW = kPrepThreads / 32;
+  if (lane == 0) sm.red[warp] = ss;
   group_sync(bar, kPrepThreads);
   if (packed)
     rotate_heads<4>(sm, rk, t, kq);
   else
     rotate_heads<kMaxG>(sm, rk, t, kq);
   group_sync(bar, kPrepThreads);
-  // power-of-two normalisations: max |q'| 2^-E <= 2^10, max |q| 2^-Ep <= 2^10
-  float mr = 0.f, mp = 0.f;
-  for (int n = kq; n < g; n += 4) {
-    const float z = ((sm.zq[0][n][t] + sm.zq[1][n][t]) + sm.zq[2][n][t]) + sm.zq[3][n][t];
-    const float vr = z * c, vp = sm.xs[n][t] * c;
-    sm.qr[n][t] = vr;
-    sm.qp[n][t] = vp;
-    mr = fmaxf(mr, fabsf(vr));
-    mp = fmaxf(mp, fabsf(vp));
-  }
-  mr = warp_max(mr);
-  mp = warp_max(mp);
-  constexpr int kW = kPrepThreads / 32;
-  if (lane == 0) {
-    sm.red[warp] = mr;
-    sm.red[kW + warp] = mp;
-  }
-  group_sync(bar, kPrepThreads);
-  mr = 0.f;
-  mp = 0.f;
+  // one power-of-two normalisation for q' and q: their magnitudes times 2^-E stay below 2^10
+  float S = 0.f;
 #pragma unroll
-  for (int w = 0; w < kW; ++w) {
-    mr = fmaxf(mr, sm.red[w]);
-    mp = fmaxf(mp, sm.red[kW + w]);
-  }
-  int er = 0, ep = 0;
-  if (mr > 0.f) {
-    frexpf(mr, &er);
+  for (int w = 0; w < kW; ++w) S += sm.red[w];
+  int er = 0;
+  const float bound = sqrtf(S) * c;
+  if (bound > 0.f) {
+    frexpf(bound, &er);
     er -= 10;
   }
-  if (mp > 0.f) {
-    frexpf(mp, &ep);
-    ep -= 10;
-  }
-  const float sr = ldexpf(1.f, -er), sp = ldexpf(1.f, -ep);
+  const float sr = ldexpf(1.f, -er);
+  // q' (scaled by c) of head n, channel j, from the four row-quarter partial products
+  auto qrot = [&](int n, int j) {
+    return (((sm.zq[0][n][j] + sm.zq[1][n][j]) + sm.zq[2][n][j]) + sm.zq[3][n][j]) * c;
+  };
   // QK B fragments over the INT2 history: MMA i reads the code pairs at
   // in-half position 2 R, R = 2 (i % 4) (b0) and R + 1 (b1), of word i / 4
   // (ks = 2 (i / 4) + (i % 4) % 2, byte parity pb = (i % 4) / 2), i.e.
@@ -242,19 +230,19 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
       // MMA i of the history: group i / 4, channel step ks, byte parity pb (see the K layout)
       const int ii = i & 3, ks = 2 * (i >> 2) + (ii & 1), pb = ii >> 1;
       const int ch = 32 * ks + 16 * bs + 4 * tig + pb;
-      vr = pack_f16x2(split_part(sm.qr[head][ch] * sr, part), split_part(sm.qr[head][ch + 2] * sr, part));
+      vr = pack_f16x2(split_part(qrot(head, ch) * sr, part), split_part(qrot(head, ch + 2) * sr, part));
       const int cp = 32 * tig + 4 * i + 2 * bs;
-      vp = pack_f16x2(split_part(sm.qp[head][cp] * sp, part), split_part(sm.qp[head][cp + 1] * sp, part));
+      vp = pack_f16x2(split_part(sm.xs[head][cp] * c * sr, part), split_part(sm.xs[head][cp + 1] * c * sr, part));
     }
     // 16-byte chunk c of lane L's row stored at chunk c ^ (L % 8): the readers'
     // 16-byte loads of one chunk index spread over all banks
-    const int ep = (e & ~31) | ((((e >> 2) & 7) ^ (L & 7)) << 2) | (e & 3);
-    qf[ep] = vr;
-    qpl[ep] = vp;
+    const int es = (e & ~31) | ((((e >> 2) & 7) ^ (L & 7)) << 2) | (e & 3);
+    qf[es] = vr;
+    qpl[es] = vp;
   }
   if (u == 0) {
     qc[16] = ldexpf(1.f, er);
-    qc[17] = ldexpf(1.f, ep);
+    qc[17] = ldexpf(1.f, er);
   }
 }
 
