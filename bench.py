@@ -272,11 +272,38 @@ def run_cuda(args):
     rots = []
     t0 = time.time()
     for layer in range(N_LAYERS):
-        U_K, U_V, tk, tv = calibrate.synthetic_layer_rotation(CFG, layer, HKV, n_cal=2048, n_keys=args.cal_keys)
-        U_K, U_V = U_K.astype(np.float32), U_V.astype(np.float32)
+        U_K, U_V, tk, tv = calibrate.synthetic_layer_rotation(ctx, CFG, layer, HKV, n_cal=2048, n_keys=args.cal_keys,
+                                                              device=dev)
         abi.oscar_load_rotation(ctx, layer, U_K, U_V, tk, tv)
         rots.append((U_K, U_V))
     t_cal = time.time() - t0
+    # the GPU part of one layer's calibration (C_Q and C_S, then tau_K and tau_V), timed with events
+    cal_gpu = None
+    if rank == 0:
+        Qc = torch.as_tensor(inputs.queries(CFG, 0, inputs.STREAM_Q_CAL, 2048), dtype=torch.float32, device=dev)
+        Kc = torch.as_tensor(np.stack([inputs.kv_tokens(CFG, 0, h, inputs.STREAM_KV_CAL, args.cal_keys, 0)
+                                       for h in range(HKV)]), dtype=torch.float32, device=dev)
+        Vc = torch.as_tensor(np.stack([inputs.kv_tokens(CFG, 0, h, inputs.STREAM_KV_CAL, args.cal_keys, 1)
+                                       for h in range(HKV)]), dtype=torch.float32, device=dev)
+        cws = calibrate.CalibWorkspace(2048, args.cal_keys, HKV, HKV * args.cal_keys, device=dev)
+        cq = torch.empty((2, 128, 128), dtype=torch.float64, device=dev)
+        ce0, ce1, ce2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        for _ in range(2):
+            ce0.record()
+            abi.oscar_calib_covariances(ctx, Qc, 2048, Kc, Vc, args.cal_keys, HKV, 1.0 / np.sqrt(128.0), cq[0], cq[1],
+                                        cws.ptr, cws.bytes, cur)
+            ce1.record()
+            torch.cuda.synchronize()
+            t1 = time.perf_counter()
+            calibrate.clip_threshold(ctx, Kc.view(-1, 128), rots[0][0], (True, True, True), 99.9, cws)
+            calibrate.clip_threshold(ctx, Vc.view(-1, 128), rots[0][1], (True, True, True), 99.9, cws)
+            t2 = time.perf_counter()
+        cal_gpu = {"covariances_ms": ce0.elapsed_time(ce1), "clip_thresholds_ms": (t2 - t1) * 1e3,
+                   "queries": 2048, "keys_per_head": args.cal_keys, "kv_heads": HKV,
+                   "note": "one layer: C_Q and C_S on the GPU (event-timed), then tau_K and tau_V (sort of "
+                           "|x R| over 8 heads x keys x 128 values each, host-timed with the result read back); "
+                           "the eigendecomposition runs on the host"}
+        del Qc, Kc, Vc, cws, cq
 
     # ---- the cache: one request, shuffled pages, CTX0 tokens prefilled per layer
     max_ctx = CTX0 + LOOP
@@ -510,7 +537,8 @@ def run_cuda(args):
                                                  page_size=64, sink=64, recent=256, group=64, device=local))
         try:
             for i, (_, fl) in enumerate(variants):
-                Uk, Uv, tk_, tv_ = calibrate.synthetic_layer_rotation(CFG, 0, HKV, n_cal=2048, n_keys=1024, flags=fl)
+                Uk, Uv, tk_, tv_ = calibrate.synthetic_layer_rotation(actx, CFG, 0, HKV, n_cal=2048, n_keys=1024,
+                                                                      flags=fl, device=dev)
                 bits = (abi.OSCAR_ROT_U if fl[0] else 0) | (abi.OSCAR_ROT_H if fl[1] else 0) | \
                        (abi.OSCAR_ROT_P if fl[2] else 0)
                 abi.oscar_load_rotation(actx, i, Uk.astype(np.float32), Uv.astype(np.float32), tk_, tv_, bits)
@@ -611,6 +639,7 @@ def run_cuda(args):
         "bf16_comparator": bf16,
         "bulk_append": bulk,
         "ablation": ablation,
+        "calibration_gpu": cal_gpu,
         "setup_s": {"calibration": t_cal, "prefill": t_prefill},
     }
     if rank == 0:

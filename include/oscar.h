@@ -313,6 +313,55 @@ oscar_status oscar_decode_attention_bf16(oscar_ctx* ctx, const oscar_bf16_cache_
                                          const oscar_decode_args* args, void* workspace,
                                          size_t workspace_bytes, void* stream);
 
+/*
+ * Offline calibration on the GPU ([RU] "Техническая идея": the keys' basis
+ * from C_Q = (1/N) sum_n q_n^T q_n, the values' basis from the score-weighted
+ * C_S = (1/N) V^T S^T S V; [ES] §2.2 A steps 1-4: both covariances on a
+ * small calibration set, a spectral decomposition, per-layer clip
+ * thresholds from the rotated calibration activations).  The
+ * eigendecomposition (U = eigenvectors of C_Q or C_S by descending
+ * eigenvalue) is left to the caller, on the host; its U then goes to
+ * oscar_calib_clip_threshold and oscar_load_rotation.
+ *
+ * Workspace: device, 256-byte aligned, at least
+ * oscar_calib_workspace_bytes(n_queries, n_keys, n_kv_heads, n_clip_rows)
+ * bytes (0: arguments out of range), owned by the caller, scratch between
+ * calls.  Row counts are at most OSCAR_CALIB_MAX_ROWS.
+ */
+#define OSCAR_CALIB_MAX_ROWS (1 << 20)
+size_t oscar_calib_workspace_bytes(int64_t n_queries, int64_t n_keys, int32_t n_kv_heads, int64_t n_clip_rows);
+
+/*
+ * C_Q and C_S of one layer.  q: device fp32 [n_q][128] calibration queries;
+ * k, v: device fp32 [n_kv_heads][n_k][128] calibration keys and values per
+ * KV head.  S = softmax(q k_h^T sm_scale) row-wise over the n_k keys of head
+ * h (no causal mask); C_S averages (1/n_q) (S_h v_h)^T (S_h v_h) over the
+ * heads.  Outputs: device fp64 [128][128] c_q and c_s (row-major).  Products
+ * in fp32 within 32-row stages, sums across stages in fp64; the attention in
+ * fp32 with an online softmax.  Asynchronous on the stream.  Errors:
+ * OSCAR_ERR_INVALID_ARG (null pointers, counts out of range, sm_scale not
+ * positive and finite), OSCAR_ERR_WORKSPACE, OSCAR_ERR_CUDA.
+ */
+oscar_status oscar_calib_covariances(oscar_ctx* ctx, const float* q, int64_t n_q, const float* k, const float* v,
+                                     int64_t n_k, int32_t n_kv_heads, float sm_scale, double* c_q, double* c_s,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Clip threshold: the given percentile (0..100) of |x R| over all n_rows x
+ * 128 entries, with numpy's linear interpolation between the order
+ * statistics around percentile / 100 (n - 1).  x: device fp32 [n_rows][128]
+ * (e.g. every calibration K row of a layer, all heads); U: host fp32
+ * [128][128] with the flags of oscar_load_rotation, R = U H P formed in fp64
+ * as there.  |x R| is sorted on the device (an exact bitonic sort of the
+ * float bits).  Synchronises the stream and writes the threshold to the host
+ * double *tau.  Errors: OSCAR_ERR_INVALID_ARG (null pointers, counts or
+ * percentile out of range, unknown flags, non-finite U), OSCAR_ERR_WORKSPACE,
+ * OSCAR_ERR_CUDA.
+ */
+oscar_status oscar_calib_clip_threshold(oscar_ctx* ctx, const float* x, int64_t n_rows, const float* U,
+                                        uint32_t flags, double percentile, double* tau, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
 /* Synchronise the stream, return and clear the device error word in *bits
  * (may be NULL).  Returns OSCAR_ERR_DEVICE_CHECK when any bit was set. */
 oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bits);

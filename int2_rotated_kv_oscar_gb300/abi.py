@@ -94,6 +94,14 @@ SIGNATURES = {
     "oscar_decode_attention_bf16": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(oscar_bf16_cache_view),
                                                    ctypes.POINTER(oscar_decode_args), ctypes.c_void_p,
                                                    ctypes.c_size_t, ctypes.c_void_p]),
+    "oscar_calib_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64]),
+    "oscar_calib_covariances": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                               ctypes.c_void_p]),
+    "oscar_calib_clip_threshold": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                                  ctypes.c_uint32, ctypes.c_double, ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "oscar_check_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "oscar_device_sm_count": (ctypes.c_int32, [ctypes.c_void_p]),
     "oscar_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -191,7 +199,7 @@ def oscar_decode_attention(ctx, layer, view, args, workspace, workspace_bytes, s
 
 
 def oscar_decode_step(ctx, layer, view, append, decode, workspace, workspace_bytes, stream=None):
-    """Append one token per request, then decode, in two launches."""
+    """Append one token per request, then decode, in one launch."""
     _check(load().oscar_decode_step(ctx, layer, ctypes.byref(view), ctypes.byref(append), ctypes.byref(decode),
                                     _ptr(workspace), workspace_bytes, _stream(stream)), "oscar_decode_step")
 
@@ -205,6 +213,31 @@ def oscar_decode_attention_noalloc(ctx, layer, view, args, stream=None):
 def oscar_decode_attention_bf16(ctx, view, args, workspace, workspace_bytes, stream=None):
     _check(load().oscar_decode_attention_bf16(ctx, ctypes.byref(view), ctypes.byref(args), _ptr(workspace),
                                               workspace_bytes, _stream(stream)), "oscar_decode_attention_bf16")
+
+
+def oscar_calib_workspace_bytes(n_queries, n_keys, n_kv_heads, n_clip_rows):
+    return int(load().oscar_calib_workspace_bytes(n_queries, n_keys, n_kv_heads, n_clip_rows))
+
+
+def oscar_calib_covariances(ctx, q, n_q, k, v, n_k, n_kv_heads, sm_scale, c_q, c_s, workspace, workspace_bytes,
+                            stream=None):
+    """q [n_q, 128], k and v [heads, n_k, 128] device float32; c_q, c_s device float64 [128, 128]."""
+    _check(load().oscar_calib_covariances(ctx, _ptr(q), n_q, _ptr(k), _ptr(v), n_k, n_kv_heads, float(sm_scale),
+                                          _ptr(c_q), _ptr(c_s), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "oscar_calib_covariances")
+
+
+def oscar_calib_clip_threshold(ctx, x, n_rows, U, flags, percentile, workspace, workspace_bytes, stream=None):
+    """x [n_rows, 128] device float32; U host float32 [128, 128]; returns the threshold (float)."""
+    import numpy as np
+    u = np.ascontiguousarray(U, dtype=np.float32)
+    if u.shape != (HEAD_DIM, HEAD_DIM):
+        raise ValueError("U must be [128, 128]")
+    tau = ctypes.c_double(0.0)
+    _check(load().oscar_calib_clip_threshold(ctx, _ptr(x), n_rows, u.ctypes.data, flags, float(percentile),
+                                             ctypes.byref(tau), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "oscar_calib_clip_threshold")
+    return float(tau.value)
 
 
 def oscar_check_device_error(ctx, stream=None):

@@ -396,6 +396,101 @@ oscar_status oscar_decode_attention_bf16(oscar_ctx* ctx, const oscar_bf16_cache_
   return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- offline calibration
+namespace {
+
+size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t calib_cov_bytes(int64_t n_q, int64_t n_k, int32_t heads) {
+  (void)n_k;
+  const int64_t rows = n_q * heads;
+  const int parts = oscar::gram_parts(rows > n_q ? rows : n_q);
+  return align_up((size_t)parts * 128 * 128 * sizeof(double)) + align_up((size_t)rows * 128 * sizeof(float));
+}
+
+size_t calib_clip_bytes(int64_t n_rows) {
+  return align_up(128 * 128 * sizeof(float)) + align_up((size_t)oscar::sort_size(n_rows * 128) * sizeof(uint32_t));
+}
+
+}  // namespace
+
+size_t oscar_calib_workspace_bytes(int64_t n_queries, int64_t n_keys, int32_t n_kv_heads, int64_t n_clip_rows) {
+  if (n_queries < 1 || n_keys < 1 || n_kv_heads < 1 || n_clip_rows < 1 || n_clip_rows > OSCAR_CALIB_MAX_ROWS ||
+      n_queries > OSCAR_CALIB_MAX_ROWS || n_keys > OSCAR_CALIB_MAX_ROWS || n_kv_heads > 256)
+    return 0;
+  const size_t a = calib_cov_bytes(n_queries, n_keys, n_kv_heads), b = calib_clip_bytes(n_clip_rows);
+  return a > b ? a : b;
+}
+
+oscar_status oscar_calib_covariances(oscar_ctx* ctx, const float* q, int64_t n_q, const float* k, const float* v,
+                                     int64_t n_k, int32_t n_kv_heads, float sm_scale, double* c_q, double* c_s,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (ctx == nullptr || q == nullptr || k == nullptr || v == nullptr || c_q == nullptr || c_s == nullptr)
+    return OSCAR_ERR_INVALID_ARG;
+  if (n_q < 1 || n_k < 1 || n_kv_heads < 1 || n_q > OSCAR_CALIB_MAX_ROWS || n_k > OSCAR_CALIB_MAX_ROWS ||
+      n_kv_heads > 256 || !(sm_scale > 0.f) || !std::isfinite(sm_scale))
+    return OSCAR_ERR_INVALID_ARG;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < calib_cov_bytes(n_q, n_k, n_kv_heads))
+    return OSCAR_ERR_WORKSPACE;
+  DeviceGuard guard(ctx->cfg.device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t rows = n_q * n_kv_heads;
+  double* partial = reinterpret_cast<double*>(ws);
+  float* O = reinterpret_cast<float*>(
+      ws + align_up((size_t)oscar::gram_parts(rows > n_q ? rows : n_q) * 128 * 128 * sizeof(double)));
+  if (oscar::launch_gram(q, n_q, 1.0 / (double)n_q, c_q, false, partial, st) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (oscar::launch_calib_attention(q, n_q, k, v, n_k, n_kv_heads, sm_scale, O, st) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  // C_S = (1 / heads) sum_h (1 / N) O_h^T O_h = (1 / (N heads)) over the rows of every O_h
+  if (oscar::launch_gram(O, rows, 1.0 / (double)rows, c_s, false, partial, st) != cudaSuccess) return OSCAR_ERR_CUDA;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_calib_clip_threshold(oscar_ctx* ctx, const float* x, int64_t n_rows, const float* U,
+                                        uint32_t flags, double percentile, double* tau, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (ctx == nullptr || x == nullptr || U == nullptr || tau == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (n_rows < 1 || n_rows > OSCAR_CALIB_MAX_ROWS || (flags & ~OSCAR_ROT_ALL) != 0) return OSCAR_ERR_INVALID_ARG;
+  if (!(percentile >= 0.0 && percentile <= 100.0)) return OSCAR_ERR_INVALID_ARG;
+  for (int i = 0; i < 128 * 128; ++i)
+    if ((flags & OSCAR_ROT_U) && !std::isfinite(U[i])) return OSCAR_ERR_INVALID_ARG;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < calib_clip_bytes(n_rows))
+    return OSCAR_ERR_WORKSPACE;
+  DeviceGuard guard(ctx->cfg.device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the composite R = U H P, formed in fp64 exactly as for oscar_load_rotation
+  std::vector<double> r(128 * 128);
+  composite_rotation(U, flags, r.data());
+  std::vector<float> rf(128 * 128);
+  for (int i = 0; i < 128 * 128; ++i) rf[i] = (float)r[i];
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* R = reinterpret_cast<float*>(ws);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(ws + align_up(128 * 128 * sizeof(float)));
+  if (cudaMemcpyAsync(R, rf.data(), rf.size() * sizeof(float), cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  if (oscar::launch_sorted_abs_rotated(x, n_rows, R, keys, st) != cudaSuccess) return OSCAR_ERR_CUDA;
+  // numpy's linear interpolation between the order statistics around p (n - 1)
+  const int64_t n = n_rows * 128;
+  const double pos = percentile / 100.0 * (double)(n - 1);
+  int64_t lo = (int64_t)std::floor(pos);
+  if (lo > n - 1) lo = n - 1;
+  const int64_t hi = lo + 1 < n ? lo + 1 : lo;
+  uint32_t pair[2];
+  if (cudaMemcpyAsync(&pair[0], keys + lo, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(&pair[1], keys + hi, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  float a, b;
+  std::memcpy(&a, &pair[0], 4);
+  std::memcpy(&b, &pair[1], 4);
+  const double g = pos - (double)lo;
+  *tau = (double)a + g * ((double)b - (double)a);
+  return OSCAR_OK;
+}
+
 oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bits) {
   if (ctx == nullptr) return OSCAR_ERR_INVALID_ARG;
   DeviceGuard guard(ctx->cfg.device);

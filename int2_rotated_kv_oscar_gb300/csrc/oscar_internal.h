@@ -95,4 +95,17 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream);
 // fused: decode append (one token per request) + q rotation, then the decode kernel
 cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cudaStream_t stream);
 
+// offline calibration (oscar_calib.cu)
+int gram_parts(int64_t n_rows);  // fp64 partial tiles a Gram matrix of n_rows rows needs (x 128 x 128)
+// C = scale X^T X (or C += ...) for X [n_rows][128] fp32; partial: gram_parts(n_rows) x 128 x 128 doubles
+cudaError_t launch_gram(const float* X, int64_t n_rows, double scale, double* C, bool accumulate, double* partial,
+                        cudaStream_t stream);
+// O[h] = softmax(Q K[h]^T sm_scale) V[h] for every head h; Q [n_q][128], K, V [heads][n_k][128], O [heads][n_q][128]
+cudaError_t launch_calib_attention(const float* Q, int64_t n_q, const float* K, const float* V, int64_t n_k,
+                                   int n_heads, float sm_scale, float* O, cudaStream_t stream);
+int64_t sort_size(int64_t n);  // keys the sort of n values needs (a power of two >= 2048)
+// keys[0 .. n_rows 128) = |X R| ascending (as float bits), then +inf up to sort_size
+cudaError_t launch_sorted_abs_rotated(const float* X, int64_t n_rows, const float* R, uint32_t* keys,
+                                      cudaStream_t stream);
+
 }  // namespace oscar

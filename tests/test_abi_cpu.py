@@ -63,6 +63,14 @@ def test_host_checks_need_no_gpu(lib):
     assert lib.oscar_decode_workspace_bytes(None, 1, 10) == 0
     assert lib.oscar_check_device_error(None, None, None) == 1
     assert lib.oscar_device_sm_count(None) == 0
+    # calibration: sizes out of range give 0 bytes, null arguments are rejected
+    assert lib.oscar_calib_workspace_bytes(0, 1, 1, 1) == 0
+    assert lib.oscar_calib_workspace_bytes(1, 1, 1, (1 << 20) + 1) == 0
+    assert lib.oscar_calib_workspace_bytes(2048, 2048, 8, 8 * 2048) >= 8 * 2048 * 128 * 4
+    assert lib.oscar_calib_covariances(None, None, 1, None, None, 1, 1, 1.0, None, None, None, 0, None) == 1
+    tau = ctypes.c_double(0.0)
+    assert lib.oscar_calib_clip_threshold(None, None, 1, u.ctypes.data, 7, 99.9, ctypes.byref(tau), None, 0,
+                                          None) == 1
     lib.oscar_destroy(None)
 
 
