@@ -298,7 +298,16 @@ def run_cuda(args):
             calibrate.clip_threshold(ctx, Kc.view(-1, 128), rots[0][0], (True, True, True), 99.9, cws)
             calibrate.clip_threshold(ctx, Vc.view(-1, 128), rots[0][1], (True, True, True), 99.9, cws)
             t2 = time.perf_counter()
-        cal_gpu = {"covariances_ms": ce0.elapsed_time(ce1), "clip_thresholds_ms": (t2 - t1) * 1e3,
+        # fp32 FMAs of C_Q, the calibration attention (Q K^T and P V per head) and C_S
+        cal_flop = 2.0 * 128 * 128 * 2048 * (1 + HKV) + 2.0 * 2 * 2048 * args.cal_keys * 128 * HKV
+        # fp32 CUDA-core peak: 152 SMs x 128 FMA lanes x 2 flop x the SM clock seen (2.07 GHz nominal)
+        f32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        cov_ms = ce0.elapsed_time(ce1)
+        cal_gpu = {"covariances_ms": cov_ms, "clip_thresholds_ms": (t2 - t1) * 1e3,
+                   "roofline": {"bound": "alu", "achieved": cal_flop / (cov_ms / 1e3) / 1e12, "peak": f32_peak,
+                                "unit": "TFLOP/s", "frac": cal_flop / (cov_ms / 1e3) / 1e12 / f32_peak,
+                                "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz",
+                                "flop": cal_flop},
                    "queries": 2048, "keys_per_head": args.cal_keys, "kv_heads": HKV,
                    "note": "one layer: C_Q and C_S on the GPU (event-timed), then tau_K and tau_V (sort of "
                            "|x R| over 8 heads x keys x 128 values each, host-timed with the result read back); "
@@ -600,6 +609,18 @@ def run_cuda(args):
                 units.append((sk[h], sv[h], rk[h], rv[h], pages[:, h], L_s, R_K, R_V, qh[4 * h:4 * h + 4]))
         t_unit, n_units = oracle_unit_time(units, args.cpu_seconds)
         cpu_ms = t_unit * 1e3 * N_LAYERS * HKV
+        if cal_gpu is not None:  # the oracle's covariances for the same calibration layer, beside the GPU's
+            from oracle import calibration as ocal
+            Qo = inputs.queries(CFG, 0, inputs.STREAM_Q_CAL, 2048).astype(np.float64)
+            Ko = [inputs.kv_tokens(CFG, 0, h, inputs.STREAM_KV_CAL, args.cal_keys, 0).astype(np.float64)
+                  for h in range(HKV)]
+            Vo = [inputs.kv_tokens(CFG, 0, h, inputs.STREAM_KV_CAL, args.cal_keys, 1).astype(np.float64)
+                  for h in range(HKV)]
+            t0c = time.perf_counter()
+            ocal.query_covariance(Qo)
+            ocal.score_weighted_value_covariance(Qo, Ko, Vo, 1.0 / np.sqrt(128.0))
+            cal_gpu["oracle_covariances_ms"] = (time.perf_counter() - t0c) * 1e3
+            cal_gpu["oracle_cores"] = blas_threads()
         cpu = {"value": 1000.0 / cpu_ms, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                "sample": "%d (layer, KV head) decode units at %d tokens, time per unit x 288 units per token"
                          % (n_units, L_s)}
