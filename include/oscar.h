@@ -258,6 +258,26 @@ oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
                                     void* stream);
 
 /*
+ * Extend (chunk) attention over one layer's mixed cache (the second workload
+ * on the same layout: a chunk of new queries reading the cached prefix --
+ * [IT] "Architettura ...": SGLang serves prefix-cache hits and chunked
+ * prefill from the same paged INT2 cache; [ES] §2.2 B).  Query b attends,
+ * through the cache of its table row b, the positions p < min(limit[b],
+ * ctx_len[b]) of the cache as it stands: ctx_len[b] is the cache length
+ * (the chunk appended first with oscar_kv_append), and the sink / INT2
+ * history / BF16 recent split follows ctx_len[b]; limit[b] (device int32
+ * [batch], e.g. P + i + 1 for the i-th token of a chunk appended at P) is
+ * the causal bound.  The queries of one chunk are batch rows whose table
+ * entries alias the same pages, sink page and ring slot.  Each query runs
+ * the split-K decode over the shared pages (the unpack is not shared across
+ * the queries of a chunk).  Same arguments, workspace, errors and output as
+ * oscar_decode_attention.
+ */
+oscar_status oscar_extend_attention(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                                    const oscar_decode_args* args, const int32_t* limit, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
  * One decode step of one layer: oscar_kv_append of one new token per
  * request, then oscar_decode_attention, in one kernel launch instead of
  * three ([IT] "Architettura ...": the decode path is append, evict/quantise,

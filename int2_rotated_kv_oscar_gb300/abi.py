@@ -86,6 +86,9 @@ SIGNATURES = {
     "oscar_decode_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
                                               ctypes.POINTER(oscar_decode_args), ctypes.c_void_p, ctypes.c_size_t,
                                               ctypes.c_void_p]),
+    "oscar_extend_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
+                                              ctypes.POINTER(oscar_decode_args), ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_size_t, ctypes.c_void_p]),
     "oscar_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
                                          ctypes.POINTER(oscar_append_args), ctypes.POINTER(oscar_decode_args),
                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -196,6 +199,12 @@ def oscar_decode_workspace_bytes(ctx, max_batch, max_ctx_len):
 def oscar_decode_attention(ctx, layer, view, args, workspace, workspace_bytes, stream=None):
     _check(load().oscar_decode_attention(ctx, layer, ctypes.byref(view), ctypes.byref(args), _ptr(workspace),
                                          workspace_bytes, _stream(stream)), "oscar_decode_attention")
+
+
+def oscar_extend_attention(ctx, layer, view, args, limit, workspace, workspace_bytes, stream=None):
+    """Decode-style attention of batch rows (a chunk's queries) with per-row causal limits (device int32)."""
+    _check(load().oscar_extend_attention(ctx, layer, ctypes.byref(view), ctypes.byref(args), _ptr(limit),
+                                         _ptr(workspace), workspace_bytes, _stream(stream)), "oscar_extend_attention")
 
 
 def oscar_decode_step(ctx, layer, view, append, decode, workspace, workspace_bytes, stream=None):

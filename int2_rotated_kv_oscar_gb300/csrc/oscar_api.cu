@@ -315,6 +315,35 @@ oscar_status oscar_decode_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
   return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+oscar_status oscar_extend_attention(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
+                                    const oscar_decode_args* args, const int32_t* limit, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  if (ctx == nullptr || view == nullptr || limit == nullptr) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded[layer]) return OSCAR_ERR_NOT_LOADED;
+  if (!valid_view(ctx, view)) return OSCAR_ERR_INVALID_ARG;
+  if (view->batch == 0) return OSCAR_OK;
+  if (view->batch > 65535) return OSCAR_ERR_UNSUPPORTED;
+  DecodePlan plan;
+  const oscar_status st = check_decode_args(ctx, args, view->batch, workspace, workspace_bytes, 0, &plan);
+  if (st != OSCAR_OK) return st;
+  if (!aligned16(view->int2_pages)) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->cfg.device);
+  DecodeLaunch d;
+  d.mode = 0;
+  d.c = refs_of(ctx, view);
+  d.rot = rotation_of(ctx, layer);
+  d.q = static_cast<const uint16_t*>(args->q);
+  d.out = args->out;
+  d.ctx_len = args->ctx_len;
+  d.sm_scale = args->sm_scale > 0.f ? args->sm_scale : 1.0f / std::sqrt(128.0f);
+  d.plan = plan;
+  d.workspace = static_cast<uint8_t*>(workspace);
+  d.err = ctx->d_err;
+  d.limit = limit;
+  return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
 oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
                                const oscar_append_args* append, const oscar_decode_args* decode, void* workspace,
                                size_t workspace_bytes, void* stream) {

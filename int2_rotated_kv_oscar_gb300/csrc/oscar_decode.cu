@@ -278,6 +278,7 @@ struct DecodeArgs {
   float pscale, inv_pscale;
   float* out;
   unsigned* err;
+  const int32_t* limit;  // extend attention: per-request causal limit (nullptr otherwise)
 };
 
 // The fused decode step's other inputs: the append of this step's token and
@@ -545,14 +546,15 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
 }
 
 // One 16-token BF16 tile (rows of K and V in global memory, original basis).
+// rows: bit r set when row r of the tile is attended.
 // SUB: row `sub` of the tile (-1: none) is read from knew / vnew instead.
 template <bool PACK4, bool SUB = false>
 __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
-                                          int n_valid, const uint32_t* qpf, float scaleEp, WarpState& st,
+                                          uint32_t rows, const uint32_t* qpf, float scaleEp, WarpState& st,
                                           int lane, int sub = -1, const uint16_t* knew = nullptr,
                                           const uint16_t* vnew = nullptr) {
   const int q = lane >> 2, tig = lane & 3;
-  const bool va = q < n_valid, vb = q + 8 < n_valid;
+  const bool va = (rows >> q) & 1u, vb = (rows >> (q + 8)) & 1u;
   const uint16_t* krow_a = SUB && q == sub ? knew : Kt + q * kD;
   const uint16_t* krow_b = SUB && q + 8 == sub ? knew : Kt + (q + 8) * kD;
   uint32_t ka[16], kb[16];
@@ -911,7 +913,7 @@ __device__ __forceinline__ void apply_patch(uint8_t* blk, const RowPatch& pt, in
   }
 }
 
-template <int MODE, bool PACK4, bool FUSED>
+template <int MODE, bool PACK4, bool FUSED, bool LIMIT = false>
 __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs* f) {
   static_assert(!FUSED || MODE == 0, "the fused step serves the mixed cache");
   extern __shared__ __align__(128) uint8_t smem[];
@@ -952,6 +954,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
     if (t == 0 && item == 0) set_error(a.err, kErrLength);
     L = 0;
   }
+  // extend attention: the query attends positions below lim only (the cache holds L)
+  int lim = L;
+  if constexpr (LIMIT) lim = max(0, min(a.limit[b], L));
   constexpr int kQW = PACK4 ? 16 : 32;
   // warp-private stage memory; after the warp's pages are done it holds the
   // warp's two finished states (rotated basis, original basis)
@@ -1173,8 +1178,23 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
             if (ring == (p_new >= kSink) && (ring ? 4 + rr / 16 : rr / 16) == j) sub = rr % 16;
           }
           const size_t nrow = ((size_t)b * a.Hkv + h) * kD;
-          bf16_tile<PACK4, FUSED>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, nv, qpf,
-                                  scaleEp, st, lane, sub, FUSED ? f->ap.k + nrow : nullptr,
+          uint32_t rows = (1u << nv) - 1u;
+          if (LIMIT) {  // rows of positions at or past the query's limit are not attended
+            if (!ring) {
+              rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
+            } else {
+              // ring row rr holds position hist_end + ((rr - (hist_end - 64)) mod 256)
+              const int hist_end = max(kSink, L - kRecent);
+              for (int r = 0; r < nv; ++r) {
+                const int rr = (int)row_off + r;
+                const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
+                if (p >= lim) rows &= ~(1u << r);
+              }
+            }
+            if (rows == 0) continue;  // nothing to attend (and a state with no max yet must stay empty)
+          }
+          bf16_tile<PACK4, FUSED>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, rows,
+                                  qpf, scaleEp, st, lane, sub, FUSED ? f->ap.k + nrow : nullptr,
                                   FUSED ? f->ap.v + nrow : nullptr);
         }
       }
@@ -1211,8 +1231,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
             apply_patch(blk, *reinterpret_cast<const RowPatch*>(smem + kPatchOffset), e_row, lane);
             __syncwarp();
           }
-          const int n_valid = min(kPage, hist_end - kPage * lp);
-          if (T < 0) {
+          const int n_valid = min(kPage, (LIMIT ? min(hist_end, lim) : hist_end) - kPage * lp);
+          if (LIMIT && n_valid <= 0) {
+          } else if (T < 0) {
             if (n_valid == kPage)
               int2_page<PACK4, true, 4>(blk, n_valid, 0, qf, scaleE, kp, st, lane);
             else
@@ -1288,7 +1309,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
         const int nv = min(16, L - kPage * pg - 16 * tile);
         if (nv <= 0) continue;
         const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
-        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, nv, qpf, scaleEp, st, lane);
+        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, (1u << nv) - 1u, qpf, scaleEp, st, lane);
       }
     }
     store_state<PACK4>(st, reinterpret_cast<float*>(stage_ptr(1)), 1.0f / kPScaleBF16, lane);
@@ -1309,9 +1330,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
   final_merge<PACK4>(a, smem, b, h, bh);
 }
 
-template <int MODE, bool PACK4>
+template <int MODE, bool PACK4, bool LIMIT = false>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
-  decode_body<MODE, PACK4, false>(a, nullptr);
+  decode_body<MODE, PACK4, false, LIMIT>(a, nullptr);
 }
 
 template <bool PACK4>
@@ -1447,6 +1468,7 @@ DecodeArgs decode_args_of(const DecodeLaunch& d, const PrepArgs& pa) {
   }
   a.out = d.out;
   a.err = d.err;
+  a.limit = d.limit;
   return a;
 }
 
@@ -1457,10 +1479,13 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
   const size_t smem = decode_smem_bytes();
   const dim3 grid(p.n_items, p.Hkv, p.batch);
   const bool pack4 = p.g <= 4;
-  void (*kern)(DecodeArgs) = d.mode == 0 ? (pack4 ? decode_kernel<0, true> : decode_kernel<0, false>)
-                                         : (pack4 ? decode_kernel<1, true> : decode_kernel<1, false>);
-  static bool attr_done[4] = {false, false, false, false};
-  const int which = 2 * d.mode + (pack4 ? 1 : 0);
+  const bool lim = d.limit != nullptr;
+  void (*kern)(DecodeArgs) =
+      d.mode == 0 ? (lim ? (pack4 ? decode_kernel<0, true, true> : decode_kernel<0, false, true>)
+                         : (pack4 ? decode_kernel<0, true> : decode_kernel<0, false>))
+                  : (pack4 ? decode_kernel<1, true> : decode_kernel<1, false>);
+  static bool attr_done[6] = {false, false, false, false, false, false};
+  const int which = (lim ? 4 : 2 * d.mode) + (pack4 ? 1 : 0);
   if (!attr_done[which]) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

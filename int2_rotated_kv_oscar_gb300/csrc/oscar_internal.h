@@ -88,6 +88,7 @@ struct DecodeLaunch {
   DecodePlan plan;
   uint8_t* workspace = nullptr;
   unsigned* err = nullptr;
+  const int32_t* limit = nullptr;  // mode 0: per-request causal limit (extend attention), or none
 };
 
 cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream);
