@@ -479,6 +479,39 @@ def run_cuda(args):
                         "sink/recent out), mean of 10 eager calls"}
         del acache, ka, va
 
+    # ---- extend attention: the queries of a 16-token chunk at the end of the context, one layer
+    ext = None
+    if rank == 0:
+        n_e, L_e = 16, CTX0 + LOOP
+        eview, etabs = cache.chunk_view(0, 0, n_e)
+        q_e = inputs.decode_queries_bf16(CFG, 0, n_e, HQ, step=7).to(dev)
+        out_e = torch.empty((n_e, HQ, D), dtype=torch.float32, device=dev)
+        len_e = torch.full((n_e,), L_e, dtype=torch.int32, device=dev)
+        lim_e = torch.arange(L_e - n_e + 1, L_e + 1, dtype=torch.int32, device=dev)
+        wse_t, wse, wse_bytes = kvcache.workspace(ctx, n_e, L_e, device=dev)
+        eargs = kvcache.decode_args(q_e, out_e, len_e, L_e)
+        for _ in range(3):
+            abi.oscar_extend_attention(ctx, 0, eview, eargs, lim_e, wse, wse_bytes, cur)
+        torch.cuda.synchronize()
+        reps = 20
+        e0.record()
+        for _ in range(reps):
+            abi.oscar_extend_attention(ctx, 0, eview, eargs, lim_e, wse, wse_bytes, cur)
+        e1.record()
+        torch.cuda.synchronize()
+        assert abi.oscar_check_device_error(ctx) == 0
+        e_ms = e0.elapsed_time(e1) / reps
+        e_bytes = algorithmic_bytes_per_layer(L_e)
+        peak_e = measured_peaks()[0]
+        ext = {"chunk_tokens": n_e, "context": L_e, "layers": 1, "ms_per_call": e_ms,
+               "tokens_per_s": n_e / (e_ms / 1e3), "prefix_bytes": e_bytes,
+               "gbs_prefix_once": e_bytes / (e_ms / 1e3) / 1e9,
+               "hbm_frac_prefix_once": e_bytes / (e_ms / 1e3) / 1e9 / peak_e,
+               "note": "oscar_extend_attention, 32 query / 8 KV heads: each query of the chunk runs the split-K "
+                       "decode over the shared pages with its causal limit, so the pages are read once per query "
+                       "(from L2 when they stay there) and unpacked once per query; the prefix bytes are counted once"}
+        del wse_t, etabs
+
     # ---- BF16-cache comparator of the same shape (decode attention, all 36 layers)
     bf16 = None
     if not args.no_bf16:
@@ -659,6 +692,7 @@ def run_cuda(args):
         "clocks": clocks.summary(),
         "bf16_comparator": bf16,
         "bulk_append": bulk,
+        "extend_attention": ext,
         "ablation": ablation,
         "calibration_gpu": cal_gpu,
         "setup_s": {"calibration": t_cal, "prefill": t_prefill},

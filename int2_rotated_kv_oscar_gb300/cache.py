@@ -54,6 +54,23 @@ class MixedCache:
             sink_page=self.sink_page.data_ptr(), ring_slot=self.ring_slot.data_ptr(),
             batch=self.batch if batch is None else batch)
 
+    def chunk_view(self, layer, b, n):
+        """A view of n batch rows that all alias request b's page table row, sink
+        page and ring slot (the queries of one chunk, for oscar_extend_attention).
+        Returns (view, tables); keep ``tables`` alive while the view is in use."""
+        pt = self.page_table[b:b + 1].expand(n, -1).contiguous()
+        sp = self.sink_page[b:b + 1].expand(n).contiguous()
+        rs = self.ring_slot[b:b + 1].expand(n).contiguous()
+        view = abi.oscar_cache_view(
+            int2_pages=self.int2_pages[layer].data_ptr(), num_pages=self.num_pages,
+            k_sink=self.k_sink[layer].data_ptr(), v_sink=self.v_sink[layer].data_ptr(),
+            num_sink_pages=self.num_sink_pages,
+            k_ring=self.k_ring[layer].data_ptr(), v_ring=self.v_ring[layer].data_ptr(),
+            num_ring_slots=self.num_ring_slots,
+            page_table=pt.data_ptr(), max_pages_per_req=self.max_pages_per_req,
+            sink_page=sp.data_ptr(), ring_slot=rs.data_ptr(), batch=n)
+        return view, (pt, sp, rs)
+
 
 class BF16PagedCache:
     """A plain BF16 paged cache of one layer (the comparator)."""
