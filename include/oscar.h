@@ -278,6 +278,29 @@ oscar_status oscar_extend_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * Extend attention for equal-size chunks, with the work shared across each
+ * chunk's queries (the prefill / extend workload of [ES] §2.2 B and [IT]
+ * "Architettura ...").  Request b of the view (its own table row) has
+ * ctx_len[b] cached positions, the chunk at pos0[b] .. pos0[b] + chunk - 1
+ * among them (appended first); query i of request b attends positions
+ * p < min(pos0[b] + i + 1, ctx_len[b]), as oscar_extend_attention would.
+ * q: device bf16 [batch][chunk][H_q][128]; out: device fp32, same shape.
+ * One block serves 16 queries of one (request, KV head): each INT2 page is
+ * copied once and unpacked once into fp16 tiles in shared memory that the 16
+ * queries' MMAs read.  Needs H_q / H_kv <= 4 (else OSCAR_ERR_UNSUPPORTED;
+ * oscar_extend_attention serves any GQA ratio) and batch * chunk <= 65535.
+ * workspace: device, 256-byte aligned, at least
+ * oscar_extend_workspace_bytes(ctx, batch, chunk, max_ctx_len) bytes; zero
+ * before its first use (as for oscar_decode_step).  max_ctx_len: the largest
+ * ctx_len[b] of the call.  Errors: as oscar_decode_attention.
+ */
+size_t oscar_extend_workspace_bytes(const oscar_ctx* ctx, int32_t batch, int32_t chunk, int32_t max_ctx_len);
+oscar_status oscar_extend_chunk(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view, const void* q,
+                                float* out, const int32_t* ctx_len, const int32_t* pos0, int32_t chunk,
+                                int32_t max_ctx_len, float sm_scale, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
  * One decode step of one layer: oscar_kv_append of one new token per
  * request, then oscar_decode_attention, in one kernel launch instead of
  * three ([IT] "Architettura ...": the decode path is append, evict/quantise,

@@ -89,6 +89,12 @@ SIGNATURES = {
     "oscar_extend_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
                                               ctypes.POINTER(oscar_decode_args), ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_void_p]),
+    "oscar_extend_workspace_bytes": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                        ctypes.c_int32]),
+    "oscar_extend_chunk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.c_void_p]),
     "oscar_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(oscar_cache_view),
                                          ctypes.POINTER(oscar_append_args), ctypes.POINTER(oscar_decode_args),
                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -205,6 +211,18 @@ def oscar_extend_attention(ctx, layer, view, args, limit, workspace, workspace_b
     """Decode-style attention of batch rows (a chunk's queries) with per-row causal limits (device int32)."""
     _check(load().oscar_extend_attention(ctx, layer, ctypes.byref(view), ctypes.byref(args), _ptr(limit),
                                          _ptr(workspace), workspace_bytes, _stream(stream)), "oscar_extend_attention")
+
+
+def oscar_extend_workspace_bytes(ctx, batch, chunk, max_ctx_len):
+    return int(load().oscar_extend_workspace_bytes(ctx, batch, chunk, max_ctx_len))
+
+
+def oscar_extend_chunk(ctx, layer, view, q, out, ctx_len, pos0, chunk, max_ctx_len, workspace, workspace_bytes,
+                       sm_scale=0.0, stream=None):
+    """q bf16 [batch, chunk, Hq, 128], out fp32 (same), ctx_len and pos0 int32 [batch] (all device tensors)."""
+    _check(load().oscar_extend_chunk(ctx, layer, ctypes.byref(view), _ptr(q), _ptr(out), _ptr(ctx_len), _ptr(pos0),
+                                     chunk, max_ctx_len, float(sm_scale), _ptr(workspace), workspace_bytes,
+                                     _stream(stream)), "oscar_extend_chunk")
 
 
 def oscar_decode_step(ctx, layer, view, append, decode, workspace, workspace_bytes, stream=None):

@@ -344,6 +344,44 @@ oscar_status oscar_extend_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
   return launch_decode(d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+size_t oscar_extend_workspace_bytes(const oscar_ctx* ctx, int32_t batch, int32_t chunk, int32_t max_ctx_len) {
+  if (ctx == nullptr || batch < 1 || chunk < 1 || max_ctx_len < 0 || (int64_t)batch * chunk > 65535) return 0;
+  return plan_extend(batch, chunk, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, max_ctx_len, ctx->num_sms).total;
+}
+
+oscar_status oscar_extend_chunk(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view, const void* q,
+                                float* out, const int32_t* ctx_len, const int32_t* pos0, int32_t chunk,
+                                int32_t max_ctx_len, float sm_scale, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (ctx == nullptr || view == nullptr || q == nullptr || out == nullptr || ctx_len == nullptr || pos0 == nullptr)
+    return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded[layer]) return OSCAR_ERR_NOT_LOADED;
+  if (!valid_view(ctx, view)) return OSCAR_ERR_INVALID_ARG;
+  if (chunk < 1 || max_ctx_len < 0) return OSCAR_ERR_INVALID_ARG;
+  if (view->batch == 0) return OSCAR_OK;
+  if ((int64_t)view->batch * chunk > 65535) return OSCAR_ERR_UNSUPPORTED;
+  if (ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads > 4) return OSCAR_ERR_UNSUPPORTED;
+  if (!aligned16(view->int2_pages)) return OSCAR_ERR_INVALID_ARG;
+  const ExtendPlan plan = plan_extend(view->batch, chunk, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, max_ctx_len,
+                                      ctx->num_sms);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < plan.total)
+    return OSCAR_ERR_WORKSPACE;
+  DeviceGuard guard(ctx->cfg.device);
+  ExtendLaunch e;
+  e.c = refs_of(ctx, view);
+  e.rot = rotation_of(ctx, layer);
+  e.q = static_cast<const uint16_t*>(q);
+  e.out = out;
+  e.ctx_len = ctx_len;
+  e.pos0 = pos0;
+  e.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(128.0f);
+  e.plan = plan;
+  e.workspace = static_cast<uint8_t*>(workspace);
+  e.err = ctx->d_err;
+  return launch_extend(e, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
 oscar_status oscar_decode_step(oscar_ctx* ctx, int32_t layer, const oscar_cache_view* view,
                                const oscar_append_args* append, const oscar_decode_args* decode, void* workspace,
                                size_t workspace_bytes, void* stream) {

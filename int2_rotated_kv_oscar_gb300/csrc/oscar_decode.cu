@@ -1341,6 +1341,371 @@ __global__ void __launch_bounds__(kThreads, 1)
   decode_body<0, PACK4, true>(a, &f);
 }
 
+// ------------------------------------------------------------------ extend (chunk) attention
+// The queries of a chunk read the same cached pages, so one block serves one
+// (request, KV head) and 16 of its chunk's queries, one per warp: a page is
+// bulk-copied once, all 512 threads unpack it once into fp16 level tiles in
+// shared memory (K: [64 tokens][128 columns in the decode's MMA order], V:
+// [128 channels][64 tokens], 16-byte chunks XOR-swizzled by row mod 8), and
+// every warp runs its query's Q.K and P.V MMAs from those tiles through
+// ldmatrix, with the decode's q fragments, softmax and state.  Records: per
+// (query, KV head, item) a rotated-basis (INT2) and an original-basis (BF16)
+// state; the last block of each (request, KV head, query group) merges them,
+// applies R_V^T and normalises.
+constexpr int kExtQ = kWarps;  // queries per block
+constexpr size_t kExtKp = 2 * kBlockBytes;                // after the two raw pages
+constexpr size_t kExtVp = kExtKp + 64 * 128 * 2;
+constexpr size_t kExtSc = kExtVp + 128 * 64 * 2;          // K scales [64][2], V scales [64][2] (float)
+constexpr size_t kExtRv = 128 * 128 * 4;                  // the final merge stages R_V^T over the tiles
+constexpr size_t kExtBars = kExtRv;                        // the two stage barriers, past it
+constexpr size_t kExtSmem = kExtBars + 16;
+static_assert(kExtSc + 2 * 64 * 2 * 4 <= kExtRv, "extend staging");
+
+struct ExtendArgs {
+  CacheRefs c;
+  const int32_t* ctx_len;  // [B] cache lengths
+  const int32_t* pos0;     // [B] chunk start positions
+  int chunk, ngpr, Hq, Hkv, g;
+  int n_items, chunk_pages, tiles_per_item;
+  const uint32_t* qfrag;
+  const uint32_t* qplain;
+  const float* qconst;
+  float* partials;  // [B chunk][Hkv][n_items][2][kPartialFloats]
+  int* counters;    // [(b ngpr + group) Hkv + h]
+  const float* R_VT;
+  float pscale, inv_pscale;
+  float* out;  // [B chunk][Hq][128]
+  unsigned* err;
+};
+
+__device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
+
+// Unpack one staged INT2 block into the level tiles and scales (thread t of 512).
+__device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint8_t* vp, float* ksc, float* vsc,
+                                           int t) {
+  const int T = t >> 7, ln = (t >> 2) & 31, wd = t & 3;
+  {
+    // K word t: row u, channels 32 ks + 16 kh + 4 tq + b, ks = 2 kpar + (p / 2), kh = p % 2, at bit 8 b + 2 p;
+    // code_level<4 bb + p> gives channels (.. + bb, .. + bb + 2): MMA 4 (ks / 2) + 2 bb + ks % 2, columns
+    // 8 kh + 2 tq and + 1 of it
+    const int row = 16 * T + 8 * (wd >> 1) + (ln >> 2), tq = ln & 3, kpar = wd & 1;
+    const CodeWord cw(*reinterpret_cast<const uint32_t*>(raw + kKCodes + 4 * t));
+    uint8_t* base = kp + row * 256;
+#define OSCAR_EXT_K(R)                                                                                  \
+  do {                                                                                                  \
+    constexpr int bb = (R) >> 2, p = (R)&3;                                                             \
+    const int ks = 2 * kpar + (p >> 1), kh = p & 1;                                                     \
+    const int col = 16 * (4 * (ks >> 1) + 2 * bb + (ks & 1)) + 8 * kh + 2 * tq;                         \
+    st_shared_u32(base + ((((col >> 3) ^ (row & 7))) << 4) + 2 * (col & 7), code_level<R>(cw));         \
+  } while (0)
+    OSCAR_EXT_K(0);
+    OSCAR_EXT_K(1);
+    OSCAR_EXT_K(2);
+    OSCAR_EXT_K(3);
+    OSCAR_EXT_K(4);
+    OSCAR_EXT_K(5);
+    OSCAR_EXT_K(6);
+    OSCAR_EXT_K(7);
+#undef OSCAR_EXT_K
+  }
+  {
+    // V word t: tokens u0, u0 + 1 (the halves), channels 16 r + jm at in-half index r
+    const int u0 = 8 * (wd >> 1) + 2 * (ln & 3), jm = 8 * (wd & 1) + (ln >> 2);
+    const int col = 16 * T + u0;
+    const CodeWord cw(*reinterpret_cast<const uint32_t*>(raw + kVCodes + 4 * t));
+#define OSCAR_EXT_V(R)                                                                                  \
+  do {                                                                                                  \
+    const int j = 16 * (R) + jm;                                                                        \
+    st_shared_u32(vp + j * 128 + ((((col >> 3) ^ (j & 7))) << 4) + 2 * (col & 7), code_level<R>(cw));   \
+  } while (0)
+    OSCAR_EXT_V(0);
+    OSCAR_EXT_V(1);
+    OSCAR_EXT_V(2);
+    OSCAR_EXT_V(3);
+    OSCAR_EXT_V(4);
+    OSCAR_EXT_V(5);
+    OSCAR_EXT_V(6);
+    OSCAR_EXT_V(7);
+#undef OSCAR_EXT_V
+  }
+  if (t < 64) {
+    const float2 k2 = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(raw + kKScales + 4 * t));
+    const float2 v2 = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(raw + kVScales + 4 * t));
+    ksc[2 * t] = k2.x;
+    ksc[2 * t + 1] = k2.y;
+    vsc[2 * t] = v2.x;
+    vsc[2 * t + 1] = v2.y;
+  }
+}
+
+// One page for one warp's query from the unpacked tiles (g <= 4: the decode's
+// packed fragments and state); rows >= n_valid are not attended.
+template <bool FULL>
+__device__ __forceinline__ void ext_page(const uint8_t* kp, const uint8_t* vp, const float* ksc, const float* vsc,
+                                         int n_valid, const uint32_t* qf, float scaleE, float kpl, WarpState& st,
+                                         int lane) {
+  const int q = lane >> 2, l7 = lane & 7, mi = lane >> 3;
+  float lg[4][2];
+#pragma unroll
+  for (int T = 0; T < 4; ++T) {
+    if (!FULL && 16 * T >= n_valid) {
+      lg[T][0] = lg[T][1] = -INFINITY;
+      continue;
+    }
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    const int row = 16 * T + l7 + 8 * (mi & 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int chunk = 2 * i + (mi >> 1);
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(a0, a1, a2, a3, kp + row * 256 + ((chunk ^ (row & 7)) << 4));
+      if (i < 4)
+        mma_f16(d0, a0, a1, a2, a3, qf[2 * i], qf[2 * i + 1]);
+      else
+        mma_f16(d1, a0, a1, a2, a3, qf[2 * i], qf[2 * i + 1]);
+    }
+    const int ra = 16 * T + q, rb = ra + 8;
+    const float lq = fmaf(d0[0] + d0[1], ksc[2 * ra], (d1[0] + d1[1]) * ksc[2 * ra + 1]) * scaleE;
+    const float lq8 = fmaf(d0[2] + d0[3], ksc[2 * rb], (d1[2] + d1[3]) * ksc[2 * rb + 1]) * scaleE;
+    lg[T][0] = (FULL || ra < n_valid) ? lq : -INFINITY;
+    lg[T][1] = (FULL || rb < n_valid) ? lq8 : -INFINITY;
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int T = 0; T < 4; ++T) mx = fmaxf(mx, fmaxf(lg[T][0], lg[T][1]));
+  online_max1(st, mx);
+  const float ms = st.m[0] - kpl;
+#pragma unroll
+  for (int T = 0; T < 4; ++T) {
+    if (!FULL && 16 * T >= n_valid) continue;
+    const float pq = ex2(lg[T][0] - ms), pq8 = ex2(lg[T][1] - ms);
+    st.l[0] += pq + pq8;
+    const int ra = 16 * T + q, rb = ra + 8;
+    const bool va = FULL || ra < n_valid, vb = FULL || rb < n_valid;
+    const float sax = va ? vsc[2 * ra] : 0.f, say = va ? vsc[2 * ra + 1] : 0.f;
+    const float sbx = vb ? vsc[2 * rb] : 0.f, sby = vb ? vsc[2 * rb + 1] : 0.f;
+    const uint32_t b00 = movmatrix_trans(value_residual(pq * sax));
+    const uint32_t b01 = movmatrix_trans(value_residual(pq8 * sbx));
+    const uint32_t b10 = movmatrix_trans(value_residual(pq * say));
+    const uint32_t b11 = movmatrix_trans(value_residual(pq8 * sby));
+    const int chunk = 2 * T + (mi >> 1);
+#pragma unroll
+    for (int M = 0; M < 8; ++M) {
+      const int row = 16 * M + l7 + 8 * (mi & 1);
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(a0, a1, a2, a3, vp + row * 128 + ((chunk ^ (row & 7)) << 4));
+      if (M < 4)
+        mma_f16(st.acc[M], a0, a1, a2, a3, b00, b01);
+      else
+        mma_f16(st.acc[M], a0, a1, a2, a3, b10, b11);
+    }
+  }
+}
+
+// The last block of a (request, KV head, query group): warp w merges the
+// records of its query per head, applies R_V^T (staged in shared memory) to
+// the rotated-basis part, joins the original-basis part and normalises.
+__device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* smem, int b, int h, int grp, int z) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  float* rvt = reinterpret_cast<float*>(smem);
+  for (int e = t; e < 128 * 128 / 4; e += kThreads)
+    reinterpret_cast<float4*>(rvt)[e] = __ldg(reinterpret_cast<const float4*>(a.R_VT) + e);
+  __syncthreads();
+  if (t == 0) a.counters[z * a.Hkv + h] = 0;  // ready for the next launch on this workspace
+  const int qi = grp * kExtQ + warp;
+  if (qi >= a.chunk) return;
+  const int qg = b * a.chunk + qi;
+  for (int n = 0; n < a.g; ++n) {
+    float Mr = -INFINITY, Lr = 0.f, Mp = -INFINITY, Lp = 0.f;
+    float4 yr = make_float4(0.f, 0.f, 0.f, 0.f), yp = yr;
+    for (int x = 0; x < a.n_items; ++x) {
+      const float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + x) * 2 * kPartialFloats;
+      merge_record(Mr, Lr, yr, __ldcg(rec + n), __ldcg(rec + 8 + n),
+                   __ldcg(reinterpret_cast<const float4*>(rec + 16 + n * kStateStride) + lane));
+      const float* rp = rec + kPartialFloats;
+      merge_record(Mp, Lp, yp, __ldcg(rp + n), __ldcg(rp + 8 + n),
+                   __ldcg(reinterpret_cast<const float4*>(rp + 16 + n * kStateStride) + lane));
+    }
+    // y R_V^T: lane holds channels 4 lane .. + 3 of y and computes outputs 4 lane .. + 3
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < 32; ++s) {
+      const float y[4] = {__shfl_sync(0xffffffffu, yr.x, s), __shfl_sync(0xffffffffu, yr.y, s),
+                          __shfl_sync(0xffffffffu, yr.z, s), __shfl_sync(0xffffffffu, yr.w, s)};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 r = reinterpret_cast<const float4*>(rvt + (4 * s + c) * 128)[lane];
+        o.x = fmaf(y[c], r.x, o.x);
+        o.y = fmaf(y[c], r.y, o.y);
+        o.z = fmaf(y[c], r.z, o.z);
+        o.w = fmaf(y[c], r.w, o.w);
+      }
+    }
+    const float M = fmaxf(Mr, Mp);
+    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      const float fr = ex2(Mr - M), fp = ex2(Mp - M);
+      const float inv_l = 1.0f / (fr * Lr + fp * Lp);
+      res = make_float4((fr * o.x + fp * yp.x) * inv_l, (fr * o.y + fp * yp.y) * inv_l,
+                        (fr * o.z + fp * yp.z) * inv_l, (fr * o.w + fp * yp.w) * inv_l);
+    }
+    *reinterpret_cast<float4*>(a.out + ((size_t)qg * a.Hq + h * a.g + n) * kD + 4 * lane) = res;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_constant__ ExtendArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int item = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  const int b = z / a.ngpr, grp = z % a.ngpr;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int qi = grp * kExtQ + warp;
+  const bool active = qi < a.chunk;
+  const int qg = b * a.chunk + (active ? qi : 0);
+  const int bq = qg * a.Hkv + h;
+  const CacheRefs& c = a.c;
+  uint8_t* kp = smem + kExtKp;
+  uint8_t* vp = smem + kExtVp;
+  float* ksc = reinterpret_cast<float*>(smem + kExtSc);
+  float* vsc = ksc + 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kExtBars);
+  if (t == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  griddep_wait();
+  int L = a.ctx_len[b];
+  if (L < 0) {
+    if (t == 0 && item == 0) set_error(a.err, kErrLength);
+    L = 0;
+  }
+  const int lim = active ? max(0, min(a.pos0[b] + qi + 1, L)) : 0;
+  const int hist_end = max(kSink, L - kRecent);
+  const int n_hist = (hist_end + kPage - 1) / kPage - 1;
+  if (n_hist + 1 > c.max_pages && t == 0 && item == 0) set_error(a.err, kErrLength);
+  const int n_hist_ok = min(n_hist, c.max_pages - 1);
+  const int lp0 = 1 + item * a.chunk_pages;
+  const int lp1 = max(lp0, min(lp0 + a.chunk_pages, 1 + n_hist_ok));
+  const int n_units = lp1 - lp0;
+  const int hlim = min(hist_end, lim);
+
+  uint32_t qf[16], qpf[16];
+  float scaleE = 0.f, scaleEp = 0.f;
+  if (active) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bq * kQFragWords + lane * 32);
+    const uint4* srcp = reinterpret_cast<const uint4*>(a.qplain + (size_t)bq * kQFragWords + lane * 32);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 u = __ldg(src + (k ^ (lane & 7)));
+      const uint4 v = __ldg(srcp + (k ^ (lane & 7)));
+      qf[4 * k] = u.x;
+      qf[4 * k + 1] = u.y;
+      qf[4 * k + 2] = u.z;
+      qf[4 * k + 3] = u.w;
+      qpf[4 * k] = v.x;
+      qpf[4 * k + 1] = v.y;
+      qpf[4 * k + 2] = v.z;
+      qpf[4 * k + 3] = v.w;
+    }
+    scaleE = __ldg(a.qconst + (size_t)bq * kQConstFloats + 16);
+    scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
+  }
+  // copies of this item's pages, two in flight
+  auto issue = [&](int k) {  // thread 0
+    const int s = k & 1;
+    const int ph = c.page_table[(size_t)b * c.max_pages + lp0 + k];
+    if (ph < 0 || ph >= c.num_pages) {
+      set_error(a.err, kErrPage);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&bars[s])) : "memory");
+      return;
+    }
+    mbar_arrive_expect_tx(&bars[s], kBlockBytes);
+    bulk_copy_g2s(smem + (size_t)s * kBlockBytes, c.pages + ((size_t)ph * a.Hkv + h) * kBlockBytes, kBlockBytes,
+                  &bars[s]);
+  };
+  __syncthreads();  // barriers initialised
+  if (t == 0) {
+    fence_proxy_async_smem();
+    for (int k = 0; k < min(2, n_units); ++k) issue(k);
+  }
+  WarpState st;
+  float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats;
+  // BF16 sink/recent tiles of this item, each warp for its query (original basis)
+  state_init(st);
+  if (active) {
+    const int sp = c.sink_page[b], slot = c.ring_slot[b];
+    const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
+    for (int k = 0; k < a.tiles_per_item; ++k) {
+      const int j = item * a.tiles_per_item + k;
+      if (j >= kBf16Tiles) break;
+      size_t row_off;
+      bool ring;
+      const int nv = bf16_tile_rows(j, L, row_off, ring);
+      if (nv <= 0) continue;
+      if (ring ? !ring_ok : !sink_ok) {
+        if (lane == 0) set_error(a.err, ring ? kErrRing : kErrSink);
+        continue;
+      }
+      uint32_t rows = (1u << nv) - 1u;
+      if (!ring) {
+        rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
+      } else {
+        for (int r = 0; r < nv; ++r) {
+          const int rr = (int)row_off + r;
+          const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
+          if (p >= lim) rows &= ~(1u << r);
+        }
+      }
+      if (rows == 0) continue;
+      const size_t off = ring ? ((((size_t)slot * a.Hkv + h) * kRecent + row_off) * kD)
+                              : ((((size_t)sp * a.Hkv + h) * kSink + row_off) * kD);
+      bf16_tile<true>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, rows, qpf, scaleEp,
+                      st, lane);
+    }
+    store_state<true>(st, rec + kPartialFloats, 1.0f / kPScaleBF16, lane);
+  }
+  // INT2 history pages (rotated basis), unpacked once per block
+  state_init(st);
+  const float kpl = log2f(a.pscale);
+  int k = 0;
+  for (; k < n_units; ++k) {
+    const int s = k & 1;
+    const bool ok = mbar_wait_bounded(&bars[s], (k >> 1) & 1, kWaitLimit);
+    if (!__syncthreads_and(ok)) {  // also: the previous page's tiles are consumed
+      if (t == 0) set_error(a.err, kErrTimeout);
+      break;
+    }
+    ext_unpack(smem + (size_t)s * kBlockBytes, kp, vp, ksc, vsc, t);
+    __syncthreads();  // tiles ready; raw stage s free
+    if (t == 0 && k + 2 < n_units) {
+      fence_proxy_async_smem();
+      issue(k + 2);
+    }
+    const int lp = lp0 + k;
+    const int n_valid = min(kPage, hlim - kPage * lp);
+    const int ph = c.page_table[(size_t)b * c.max_pages + lp];
+    if (active && n_valid > 0 && ph >= 0 && ph < c.num_pages) {
+      if (n_valid == kPage)
+        ext_page<true>(kp, vp, ksc, vsc, n_valid, qf, scaleE, kpl, st, lane);
+      else
+        ext_page<false>(kp, vp, ksc, vsc, n_valid, qf, scaleE, kpl, st, lane);
+    }
+  }
+  // after a timeout, wait (bounded) for the copies still in flight
+  for (int kk = k; kk < min(k + 2, n_units); ++kk) mbar_wait_bounded(&bars[kk & 1], (kk >> 1) & 1, kWaitLimit);
+  if (active) store_state<true>(st, rec, a.inv_pscale, lane);
+  griddep_launch_dependents();
+  __shared__ int s_last;
+  __syncthreads();
+  if (t == 0) {
+    int ticket;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(ticket) : "l"(&a.counters[z * a.Hkv + h]) : "memory");
+    s_last = (ticket == a.n_items - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  extend_final_merge(a, smem, b, h, grp, z);
+}
+
 constexpr size_t decode_smem_bytes() { return kSlotsOffset + (size_t)kBf16Slots * kPartialFloats * sizeof(float); }
 // a warp state fits in one stage (the rotated-basis one in the warp's first
 // stage, the comparator's original-basis one in its second); the block
@@ -1496,6 +1861,99 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
 }
 
 }  // namespace
+
+ExtendPlan plan_extend(int batch, int chunk, int Hq, int Hkv, int max_ctx_len, int num_sms) {
+  ExtendPlan p;
+  p.batch = batch;
+  p.chunk = chunk;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.g = Hq / Hkv;
+  p.ngpr = (chunk + kExtQ - 1) / kExtQ;
+  const int hist_end = max_ctx_len > kSink + kRecent ? max_ctx_len - kRecent : kSink;
+  int pages = (hist_end + kPage - 1) / kPage - 1;
+  if (pages < 0) pages = 0;
+  const long long total = (long long)batch * p.ngpr * Hkv * pages;
+  const long long slots = num_sms > 0 ? num_sms : 148;
+  long long C = (total + slots - 1) / slots;
+  if (C < 2) C = 2;
+  if (C > 8 * kWarps) C = 8 * kWarps;
+  if (pages > C * kMaxChunks) C = (pages + kMaxChunks - 1) / kMaxChunks;
+  p.chunk_pages = (int)C;
+  p.n_items = pages > 0 ? (int)((pages + C - 1) / C) : 1;
+  p.tiles_per_item = (kBf16Tiles + p.n_items - 1) / p.n_items;
+  const size_t nq = (size_t)batch * chunk, bq = nq * Hkv;
+  size_t off = 0;
+  p.off_counters = off;
+  off = align256(off + bq * sizeof(int));
+  p.off_qfrag = off;
+  off = align256(off + bq * kQFragWords * sizeof(uint32_t));
+  p.off_qplain = off;
+  off = align256(off + bq * kQFragWords * sizeof(uint32_t));
+  p.off_qconst = off;
+  off = align256(off + bq * kQConstFloats * sizeof(float));
+  p.off_partials = off;
+  off = align256(off + bq * (size_t)p.n_items * 2 * kPartialFloats * sizeof(float));
+  p.total = off;
+  return p;
+}
+
+cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
+  const ExtendPlan& p = e.plan;
+  if (p.batch == 0 || p.chunk == 0) return cudaSuccess;
+  uint8_t* ws = e.workspace;
+  PrepArgs pa;
+  pa.q = e.q;
+  pa.R_K = e.rot.R_K;
+  pa.sm_scale = e.sm_scale;
+  pa.Hq = p.Hq;
+  pa.Hkv = p.Hkv;
+  pa.g = p.g;
+  pa.qfrag = reinterpret_cast<uint32_t*>(ws + p.off_qfrag);
+  pa.qplain = reinterpret_cast<uint32_t*>(ws + p.off_qplain);
+  pa.qconst = reinterpret_cast<float*>(ws + p.off_qconst);
+  pa.counters = reinterpret_cast<int*>(ws + p.off_counters);
+  void* pargs[] = {&pa};
+  cudaError_t err = launch_pdl(reinterpret_cast<const void*>(prep_kernel), dim3(p.Hkv, p.batch * p.chunk),
+                               dim3(kPrepThreads), 0, stream, pargs);
+  if (err != cudaSuccess) return err;
+  ExtendArgs a;
+  a.c = e.c;
+  a.ctx_len = e.ctx_len;
+  a.pos0 = e.pos0;
+  a.chunk = p.chunk;
+  a.ngpr = p.ngpr;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.g = p.g;
+  a.n_items = p.n_items;
+  a.chunk_pages = p.chunk_pages;
+  a.tiles_per_item = p.tiles_per_item;
+  a.qfrag = pa.qfrag;
+  a.qplain = pa.qplain;
+  a.qconst = pa.qconst;
+  a.partials = reinterpret_cast<float*>(ws + p.off_partials);
+  a.counters = pa.counters;
+  a.R_VT = e.rot.R_VT;
+  {
+    const float smax = std::isfinite(e.rot.tau_v) ? fminf(65504.f, e.rot.tau_v / 1.5f * 1.001f) : 65504.f;
+    int k = (int)floorf(log2f(60000.f / (16.f * smax)));
+    k = k < -20 ? -20 : (k > 20 ? 20 : k);
+    a.pscale = ldexpf(1.f, k);
+    a.inv_pscale = ldexpf(1.f, -k);
+  }
+  a.out = e.out;
+  a.err = e.err;
+  static bool attr = false;
+  if (!attr) {
+    err = cudaFuncSetAttribute(extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kExtSmem);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  void* args[] = {&a};
+  return launch_pdl(reinterpret_cast<const void*>(extend_kernel), dim3(p.n_items, p.Hkv, p.batch * p.ngpr),
+                    dim3(kThreads), kExtSmem, stream, args);
+}
 
 cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
   const DecodePlan& p = d.plan;

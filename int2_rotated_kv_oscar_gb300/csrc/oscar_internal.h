@@ -96,6 +96,29 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream);
 // fused: decode append (one token per request) + q rotation, then the decode kernel
 cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cudaStream_t stream);
 
+// extend (chunk) attention: a chunk of queries per request reading its cached pages
+struct ExtendPlan {
+  int32_t batch = 0, chunk = 0, Hq = 0, Hkv = 0, g = 0;
+  int32_t ngpr = 0;            // query groups (of 16) per request
+  int32_t chunk_pages = 0, n_items = 0, tiles_per_item = 0;
+  size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
+};
+ExtendPlan plan_extend(int batch, int chunk, int Hq, int Hkv, int max_ctx_len, int num_sms);
+
+struct ExtendLaunch {
+  CacheRefs c;
+  LayerRotation rot;
+  const uint16_t* q = nullptr;        // bf16 [batch][chunk][Hq][128]
+  float* out = nullptr;               // fp32 [batch][chunk][Hq][128]
+  const int32_t* ctx_len = nullptr;   // [batch] cache lengths
+  const int32_t* pos0 = nullptr;      // [batch] chunk start positions
+  float sm_scale = 0.f;
+  ExtendPlan plan;
+  uint8_t* workspace = nullptr;
+  unsigned* err = nullptr;
+};
+cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream);
+
 // offline calibration (oscar_calib.cu)
 int gram_parts(int64_t n_rows);  // fp64 partial tiles a Gram matrix of n_rows rows needs (x 128 x 128)
 // C = scale X^T X (or C += ...) for X [n_rows][128] fp32; partial: gram_parts(n_rows) x 128 x 128 doubles

@@ -99,3 +99,69 @@ def test_extend_with_the_whole_cache_equals_decode():
         assert np.array_equal(out.cpu().numpy().astype(np.float64), dec)
     finally:
         s.close()
+
+
+def _extend_chunk(s, q, B, n, L, P):
+    out = torch.full((B, n, s.Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ctx_len = torch.full((B,), L, dtype=torch.int32, device="cuda")
+    pos0 = torch.full((B,), P, dtype=torch.int32, device="cuda")
+    nbytes = abi.oscar_extend_workspace_bytes(s.ctx, B, n, L)
+    ws = torch.zeros(nbytes + 256, dtype=torch.uint8, device="cuda")
+    wptr = ws.data_ptr() + (-ws.data_ptr()) % 256
+    abi.oscar_extend_chunk(s.ctx, 0, s.cache.view(0), q, out, ctx_len, pos0, n, L, wptr, nbytes,
+                           stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("P,n,B,Hq,Hkv,cfg", [(10, 40, 1, 32, 8, 41),      # sink only
+                                              (100, 300, 1, 32, 8, 42),    # 19 query groups, wrapped ring
+                                              (1000, 8, 2, 16, 8, 43),     # GQA 2, half a group
+                                              (5000, 33, 2, 32, 8, 44)])   # a group with one query
+def test_extend_chunk_matches_the_oracle(P, n, B, Hq, Hkv, cfg):
+    """The shared-unpack chunk kernel: one block per (request, KV head, 16 queries)."""
+    L = P + n
+    s = harness.Setup(Hq, Hkv, L, B, cfg=cfg)
+    try:
+        for b in range(B):
+            tk = inputs.kv_tokens_device(cfg, 0, Hkv, inputs.STREAM_KV, L, "cuda", request=b)
+            restore = harness.request_view(s, b, b + 1)
+            try:
+                s.append(0, tk[0][:P], tk[1][:P], [0], [0, P], P, batch=1)
+                s.append(0, tk[0][P:], tk[1][P:], [P], [0, n], n, batch=1)
+            finally:
+                restore()
+        q = inputs.decode_queries_bf16(cfg, 0, B * n, Hq).reshape(B, n, Hq, 128)
+        out = _extend_chunk(s, q.cuda(), B, n, L, P)
+        assert s.device_error() == 0
+        got = out.cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        R_K, R_V, _, _ = s.rot[0]
+        worst = 0.0
+        for b in range(B):
+            Ks, Vs = [], []
+            for (sk, sv, rk, rv, blocks) in s.readback(0, b, L):
+                K, V = ocache.reconstruct_from_storage(sk, sv, rk, rv, blocks, L, R_K, R_V)
+                Ks.append(K)
+                Vs.append(V)
+            rows = range(n) if n <= 64 else sorted(set(list(range(0, n, 7)) + [n - 1]))
+            for i in rows:
+                lim = P + i + 1
+                ref = attention.decode_gqa(inputs.bf16_to_f64(q[b, i]), [K[:lim] for K in Ks],
+                                           [V[:lim] for V in Vs], harness.SM_SCALE)
+                worst = max(worst, float(np.abs(got[b, i] - ref).max()))
+        print("extend chunk P=%d n=%d B=%d: max-abs vs oracle %.2e" % (P, n, B, worst))
+        assert worst <= harness.DECODE_TOL
+    finally:
+        s.close()
+
+
+def test_extend_chunk_refuses_gqa_above_4():
+    s = harness.Setup(64, 8, 200, 1, cfg=45, calibrate=False)
+    try:
+        q = torch.zeros((1, 4, 64, 128), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(abi.OscarError) as e:
+            _extend_chunk(s, q, 1, 4, 200, 196)
+        assert e.value.status == 2  # OSCAR_ERR_UNSUPPORTED
+    finally:
+        s.close()
