@@ -138,176 +138,257 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 
 // Phase 2b: new tokens that go straight into the INT2 history.
 //
-// x R on the tensor cores: x is a bf16 row, R^T is held as three bf16 terms
-// (R = t0 + t1 + t2 to ~2^-24 relative), and each m16n8k16 product is exact
-// in the MMA.  The t0 products of each 16-channel step land in a fresh
-// accumulator and are summed in fp32 with round-to-nearest, so the tensor
-// core's truncation of its fp32 result does not pile up; the much smaller t1,
-// t2 products share one chained accumulator.  Persistent blocks of 512
-// threads, one per SM, keep the six R^T terms (192 KB) in shared memory and
-// run two tile slots: warps 0..7 and 8..15 each take one (request, KV head,
-// page) tile at a time, K rows on their first four warps and V rows on the
-// last four; each warp owns 16 rows of the tile.
-constexpr int kTcSlots = 2;
-constexpr int kTcThreads = 32 * 8 * kTcSlots;
+// x R on the 5th-generation tensor cores: one tile is 128 new tokens (two
+// pages) of one (request, KV head) and one matrix (K or V).  D[token][n] =
+// sum_k x[token][k] R^T[n][k] runs as M = 128, N = 64 (one quantisation
+// group), K = 16 tcgen05 MMAs from shared memory into tensor memory.  x is
+// bf16 (exact) and R^T is held as three bf16 terms (R = t0 + t1 + t2 to
+// ~2^-24 relative), so every product is exact; the tensor core truncates its
+// fp32 sums, so the t0 products of each run of 8 / kTcRegions 16-channel
+// steps land in a fresh TMEM region, the much smaller t1, t2 products share
+// one chained region, and the epilogue adds the regions in fp32 with
+// round-to-nearest.
+//
+// Persistent blocks, one per SM, each for one matrix (even blocks K, odd V):
+//   warps 0-3   group 0 epilogue (TMEM lane 32 (warp % 4) + lane = token row)
+//   warps 4-7   group 1 epilogue
+//   warps 8-11  loaders: x rows -> shared memory (128-byte swizzle), two buffers
+//   warp 12     TMEM allocation; one thread issues the MMAs
+// An epilogue thread owns one token row of its group: absmax, fp16 scale,
+// codes, and that row's packed words (K) or bytes (V) and scale.
+constexpr int kTcRegions = 2;
+constexpr int kTcThreads = 13 * 32;
+constexpr uint32_t kTcCols = 512;          // TMEM columns; group g's regions from column 256 g
+constexpr uint32_t kTcB = 0;               // R^T terms: 3 x [2 k-blocks][128 rows n][128 B]
+constexpr uint32_t kTcA = 3 * 32768;       // x tiles: 2 x [2 k-blocks][128 rows][128 B]
+constexpr uint32_t kTcBars = kTcA + 2 * 32768;
+constexpr size_t kTcSmem = kTcBars + 128 + 1024;  // barriers, TMEM address, flags, 1024-byte alignment slack
+static_assert(kTcRegions == 2, "the epilogue reads two t0 regions and the chain");
 
-struct TcSmem {
-  uint16_t rt[2][3][kD][kD];          // [K, V][term][n][k], 16-byte chunks swizzled by n % 8
-  uint8_t code[kTcSlots][2][64][kD];  // codes of the tile being packed
-  __half scale[kTcSlots][2][64][2];
+struct TcTile {
+  int b, h, lp0, lo, hi, tok0, p0;
 };
 
-__device__ __forceinline__ int rt_index(int n, int k) { return n * kD + ((((k >> 3) ^ (n & 7)) << 3) | (k & 7)); }
-
-// One (request, KV head, page) tile, rows [r_lo, r_hi) of page lp, for the
-// 128 threads of (slot, matrix m) -- m = 0: K, 1: V -- synchronised by named
-// barrier `bar`.
-__device__ __forceinline__ void tc_quantize_tile(const AppendLaunch& a, int b, int h, int tok0, int p0, int r_lo,
-                                                 int r_hi, int lp, uint8_t* blk, int slot, int m, int bar,
-                                                 TcSmem& sm) {
-  const int t = threadIdx.x & 127, lane = t & 31, wq = t >> 5, g = lane >> 2, tq = lane & 3;
-  const int Hkv = a.c.num_kv_heads;
-  const uint16_t* src = m ? a.v : a.k;
-  const float tau = m ? a.rot.tau_v : a.rot.tau_k;
-  // A fragments of this warp's rows 16 wq + {g, g + 8}, all 8 channel steps
-  uint32_t af[8][4];
-  {
-    const int r0 = 16 * wq + g, r1 = r0 + 8;
-    const bool v0 = r0 >= r_lo && r0 < r_hi, v1 = r1 >= r_lo && r1 < r_hi;
-    const uint16_t* x0 = src + ((size_t)(tok0 + lp * kPage + r0 - p0) * Hkv + h) * kD + 2 * tq;
-    const uint16_t* x1 = src + ((size_t)(tok0 + lp * kPage + r1 - p0) * Hkv + h) * kD + 2 * tq;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      af[i][0] = v0 ? *reinterpret_cast<const uint32_t*>(x0 + 16 * i) : 0u;
-      af[i][1] = v1 ? *reinterpret_cast<const uint32_t*>(x1 + 16 * i) : 0u;
-      af[i][2] = v0 ? *reinterpret_cast<const uint32_t*>(x0 + 16 * i + 8) : 0u;
-      af[i][3] = v1 ? *reinterpret_cast<const uint32_t*>(x1 + 16 * i + 8) : 0u;
-    }
-  }
-  const uint16_t* rtm = &sm.rt[m][0][0][0];
-  // ldmatrix row of this lane: matrix q = lane / 8 covers n-block (pair base + q / 2), k half q % 2
-  const int lq = lane >> 3, lr = lane & 7;
-#pragma unroll 1
-  for (int G = 0; G < 2; ++G) {  // quantisation group: output channels 64 G .. 64 G + 63
-    float run[8][4], chn[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) run[j][e] = chn[j][e] = 0.f;
-    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-#pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {
-        const int n = 64 * G + 16 * jp + 8 * (lq >> 1) + lr, k = 16 * i + 8 * (lq & 1);
-        const int off = rt_index(n, k);
-        uint32_t b[4];
-        ldmatrix_x4(b[0], b[1], b[2], b[3], rtm + off);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float f[4];
-          mma_bf16(f, af[i], b[2 * q], b[2 * q + 1], zero);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) run[2 * jp + q][e] += f[e];
-        }
-#pragma unroll
-        for (int term = 1; term < 3; ++term) {
-          ldmatrix_x4(b[0], b[1], b[2], b[3], rtm + term * kD * kD + off);
-#pragma unroll
-          for (int q = 0; q < 2; ++q) mma_bf16(chn[2 * jp + q], af[i], b[2 * q], b[2 * q + 1], chn[2 * jp + q]);
-        }
-      }
-    }
-    // x' of rows 16 wq + g (elements 0, 1) and + 8 (2, 3), channels 64 G + 8 j + 2 tq + {0, 1}
-    float mx0 = 0.f, mx1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) run[j][e] += chn[j][e];
-      mx0 = fmaxf(mx0, fmaxf(fabsf(run[j][0]), fabsf(run[j][1])));
-      mx1 = fmaxf(mx1, fmaxf(fabsf(run[j][2]), fabsf(run[j][3])));
-    }
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    const __half h0 = __float2half_rn(fminf(mx0, tau) / 1.5f), h1 = __float2half_rn(fminf(mx1, tau) / 1.5f);
-    const float s0 = __half2float(h0), s1 = __half2float(h1);
-    const int row0 = 16 * wq + g, row1 = row0 + 8;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int ch = 64 * G + 8 * j + 2 * tq;
-      const float* v = run[j];
-      sm.code[slot][m][row0][ch] = (uint8_t)((v[0] >= -s0) + (v[0] >= 0.f) + (v[0] >= s0));
-      sm.code[slot][m][row0][ch + 1] = (uint8_t)((v[1] >= -s0) + (v[1] >= 0.f) + (v[1] >= s0));
-      sm.code[slot][m][row1][ch] = (uint8_t)((v[2] >= -s1) + (v[2] >= 0.f) + (v[2] >= s1));
-      sm.code[slot][m][row1][ch + 1] = (uint8_t)((v[3] >= -s1) + (v[3] >= 0.f) + (v[3] >= s1));
-    }
-    if (tq == 0) {
-      sm.scale[slot][m][row0][G] = h0;
-      sm.scale[slot][m][row1][G] = h1;
-    }
-  }
-  half_sync(bar);
-  // pack the rows in [r_lo, r_hi) only: other rows of this page may hold
-  // history tokens written by earlier appends
-  for (int i = t; i < 64 * 8; i += 128) {
-    const int row = i >> 3, w = i & 7;
-    if (row < r_lo || row >= r_hi) continue;
-    const uint8_t* cr = sm.code[slot][m][row];
-    if (m == 0) {
-      *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(row, w & 3, w >> 2)) = k_word(cr, w & 3, w >> 2);
-    } else {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int jj = 2 * w + hh;
-        uint32_t hv = 0;
-#pragma unroll
-        for (int r = 0; r < 8; ++r) hv |= (uint32_t)cr[jj + 16 * r] << (2 * r);
-        *reinterpret_cast<uint16_t*>(blk + kVCodes + v_half_offset(row, jj)) = (uint16_t)hv;
-      }
-    }
-  }
-  {
-    const int row = t >> 1, gg = t & 1;
-    if (row >= r_lo && row < r_hi)
-      *reinterpret_cast<__half*>(blk + (m ? kVScales : kKScales) + 4 * row + 2 * gg) = sm.scale[slot][m][row][gg];
-  }
-  half_sync(bar);  // the staging is reused by this slot's next tile
+// The tile-th (request, KV head, page pair) of a matrix; false: nothing to write.
+__device__ __forceinline__ bool tc_tile(const AppendLaunch& a, unsigned tile, unsigned tiles2, TcTile& t) {
+  const unsigned Hkv = (unsigned)a.c.num_kv_heads, r = tile / tiles2;
+  t.h = (int)(r % Hkv);
+  t.b = (int)(r / Hkv);
+  int n;
+  if (!request_span(a, t.b, t.p0, n, t.tok0)) return false;
+  t.lo = max(t.p0, kSink);
+  t.hi = t.p0 + n - kRecent;
+  if (t.hi <= t.lo) return false;
+  t.lp0 = t.lo / kPage + 2 * (int)(tile % tiles2);
+  return t.lp0 * kPage < t.hi;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch a, int tiles_per_req) {
-  extern __shared__ __align__(16) uint8_t tile_smem_raw[];
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(tile_smem_raw);
-  // the six R^T terms into shared memory, 16-byte chunks swizzled
-  {
-    const uint4* srcv = reinterpret_cast<const uint4*>(a.rot.RT_split);
-    constexpr int kChunks = 2 * 3 * kD * kD / 8;
-    for (int c = threadIdx.x; c < kChunks; c += kTcThreads) {
-      const int row = c >> 4, chunk = c & 15, n = row & (kD - 1);
-      reinterpret_cast<uint4*>(&sm.rt[0][0][0][0])[(row << 4) | (chunk ^ (n & 7))] = __ldg(srcv + c);
+// Block of logical page lp (any thread may report a bad entry).
+__device__ __forceinline__ uint8_t* tc_block(const CacheRefs& c, int b, int h, int lp, unsigned* err) {
+  if (lp >= c.max_pages) {
+    set_error(err, kErrLength);
+    return nullptr;
+  }
+  const int phys = c.page_table[(size_t)b * c.max_pages + lp];
+  if (phys < 0 || phys >= c.num_pages) {
+    set_error(err, kErrPage);
+    return nullptr;
+  }
+  return c.pages + ((size_t)phys * c.num_kv_heads + h) * kBlockBytes;
+}
+
+// Byte offset of element (row, 16-byte chunk ch of K) in a [2][rows][128 B] swizzled operand.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
+  return (ch >> 3) * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + (((ch & 7) ^ (row & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch a, unsigned tiles2) {
+  extern __shared__ uint8_t tc_raw[];
+  const uint32_t raw_s = smem_u32(tc_raw);
+  uint8_t* sm = tc_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  const uint32_t sbase = smem_u32(sm);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTcBars);  // [2] x tile of buffer s stored
+  uint64_t* empty = full + 2;                                   // [2] buffer s read by its MMAs
+  uint64_t* tfull = full + 4;                                   // [2] group g's sums in TMEM
+  uint64_t* tempty = full + 6;                                  // [2] group g's TMEM columns read
+  uint64_t* done = full + 8;                                    // every MMA of the block finished
+  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(full + 9);
+  volatile int* work = reinterpret_cast<volatile int*>(full + 10);  // [2] buffer s holds a tile (0: no more)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x & 1;
+  const unsigned cta = blockIdx.x >> 1, n_cta = gridDim.x >> 1;
+  const int Hkv = a.c.num_kv_heads;
+  const unsigned n_tiles = tiles2 * (unsigned)Hkv * (unsigned)a.c.batch;
+  {  // this matrix's three R^T terms
+    const uint4* src = reinterpret_cast<const uint4*>(a.rot.RT_split) + (size_t)m * 3 * 128 * 16;
+    for (int c = threadIdx.x; c < 3 * 128 * 16; c += kTcThreads) {
+      const int term = c >> 11, n = (c >> 4) & 127;
+      *reinterpret_cast<uint4*>(sm + kTcB + term * 32768 + sw128_offset(n, c & 15)) = __ldg(src + c);
     }
   }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 128);
+      mbar_init(&empty[i], 1);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 12) tmem_alloc(tmem_at, kTcCols);
+  fence_proxy_async_smem();  // R^T, for the tensor core
+  tc_fence_before();
   __syncthreads();
-  const int slot = threadIdx.x / 256, m = (threadIdx.x >> 7) & 1, bar = 1 + 2 * slot + m;
-  const int Hkv = a.c.num_kv_heads;
-  const long long n_tiles = (long long)tiles_per_req * Hkv * a.c.batch;
-  for (long long tile = (long long)blockIdx.x * kTcSlots + slot; tile < n_tiles; tile += (long long)gridDim.x * kTcSlots) {
-    const int x = (int)(tile % tiles_per_req);
-    const int h = (int)((tile / tiles_per_req) % Hkv);
-    const int b = (int)(tile / ((long long)tiles_per_req * Hkv));
-    int p0, n, tok0;
-    if (!request_span(a, b, p0, n, tok0)) continue;
-    const int L = p0 + n;
-    const int lo = max(p0, kSink), hi = L - kRecent;
-    if (hi <= lo) continue;
-    const int lp = lo / kPage + x;
-    if (lp * kPage >= hi) continue;
-    const int r_lo = max(lo - lp * kPage, 0), r_hi = min(hi - lp * kPage, kPage);
-    uint8_t* blk = history_block(a.c, b, h, lp * kPage, a.err);
-    if (blk == nullptr) continue;
-    tc_quantize_tile(a, b, h, tok0, p0, r_lo, r_hi, lp, blk, slot, m, bar, sm);
+  tc_fence_after();
+  const uint32_t tbase = *tmem_at;
+
+  if (warp >= 8 && warp < 12) {
+    // loaders: thread lt stores 16-byte chunk (lt % 16) of rows lt / 16 + 8 i; after the
+    // last tile a buffer with work = 0 tells the MMA thread to stop
+    const int lt = threadIdx.x - 256, ch = lt & 15, r0 = lt >> 4;
+    const uint16_t* src = m ? a.v : a.k;
+    int it = 0;
+    for (unsigned tile = cta;; tile += n_cta) {
+      TcTile t;
+      const bool last = tile >= n_tiles;
+      if (!last && !tc_tile(a, tile, tiles2, t)) continue;
+      const int s = it & 1;
+      if (!mbar_wait_bounded(&empty[s], ((it >> 1) & 1) ^ 1, kWaitLimit)) {
+        set_error(a.err, kErrTimeout);
+        break;
+      }
+      if (last) {
+        if (lt == 0) work[s] = 0;
+        mbar_arrive(&full[s]);
+        break;
+      }
+      uint4 v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int p = t.lp0 * kPage + r0 + 8 * i;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (p >= t.lo && p < t.hi)
+          v[i] = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)(t.tok0 + p - t.p0) * Hkv + t.h) * kD) + ch);
+      }
+      uint8_t* A = sm + kTcA + s * 32768;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) *reinterpret_cast<uint4*>(A + sw128_offset(r0 + 8 * i, ch)) = v[i];
+      if (lt == 0) work[s] = 1;
+      fence_proxy_async_smem();
+      mbar_arrive(&full[s]);
+      ++it;
+    }
+  } else if (warp == 12) {
+    if (lane == 0) {
+      // descriptors differ only in the start-address field (low 14 bits), which the offsets never overflow
+      constexpr uint32_t idesc = umma_idesc_bf16_f32(128, 64);
+      const uint64_t dhi = umma_desc_sw128(0) & 0xFFFFFFFF00000000ull;
+      const uint32_t a_lo = (uint32_t)umma_desc_sw128(sbase + kTcA), b_lo = (uint32_t)umma_desc_sw128(sbase + kTcB);
+      for (int it = 0;; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait_bounded(&full[s], (it >> 1) & 1, kWaitLimit)) {
+          set_error(a.err, kErrTimeout);
+          break;
+        }
+        if (work[s] == 0) break;
+        bool ok = true;
+        for (int g = 0; g < 2; ++g) {
+          if (!mbar_wait_bounded(&tempty[g], (it & 1) ^ 1, kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t al = a_lo + (uint32_t)s * (32768 >> 4), bl = b_lo + (uint32_t)g * (8192 >> 4);
+          const uint32_t d = tbase + 256 * g;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t ko = (uint32_t)((i >> 2) * 16384 + (i & 3) * 32) >> 4;
+            const uint64_t ad = dhi | (al + ko);
+            const int reg = i * kTcRegions / 8;
+            const bool acc = i > 0 && (i - 1) * kTcRegions / 8 == reg;
+            umma_f16(d + 64 * reg, ad, dhi | (bl + ko), idesc, acc);
+            umma_f16(d + 64 * kTcRegions, ad, dhi | (bl + ko + (32768 >> 4)), idesc, i > 0);
+            umma_f16(d + 64 * kTcRegions, ad, dhi | (bl + ko + (65536 >> 4)), idesc, true);
+          }
+          umma_commit(&tfull[g]);
+        }
+        if (!ok) {
+          set_error(a.err, kErrTimeout);
+          break;
+        }
+        umma_commit(&empty[s]);
+      }
+      umma_commit(done);  // arrives once every MMA above has finished
+      if (!mbar_wait_bounded(done, 0, kWaitLimit)) set_error(a.err, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // epilogue of group g, token row 32 q + lane of each tile
+    const int g = warp >> 2, q = warp & 3, row = 32 * q + lane;
+    const float tau = m ? a.rot.tau_v : a.rot.tau_k;
+    const uint32_t taddr = tbase + ((uint32_t)(32 * q) << 16) + 256 * g;
+    int it = 0;
+    for (unsigned tile = cta; tile < n_tiles; tile += n_cta) {
+      TcTile t;
+      if (!tc_tile(a, tile, tiles2, t)) continue;
+      const int p = t.lp0 * kPage + row;
+      uint8_t* blk = (p >= t.lo && p < t.hi) ? tc_block(a.c, t.b, t.h, p >> 6, a.err) : nullptr;
+      if (!mbar_wait_bounded(&tfull[g], it & 1, kWaitLimit)) {
+        set_error(a.err, kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      float x[64];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[96];  // columns 32 hh .. of region 0, region 1 and the t1/t2 chain
+        tmem_ld32x3(taddr + 32 * hh, taddr + 64 + 32 * hh, taddr + 128 + 32 * hh, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[32 * hh + e] = (v[e] + v[32 + e]) + v[64 + e];
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[g]);
+      ++it;
+      if (blk == nullptr) continue;
+      const int rp = p & 63;
+      float mx = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) mx = fmaxf(mx, fabsf(x[j]));
+      const __half hs = __float2half_rn(fminf(mx, tau) / 1.5f);
+      const float sc = __half2float(hs);
+      if (m == 0) {
+        // K word tq of this row and group: channel 32 ks2 + 16 kh + 4 tq + b at bit 8 b + 2 (2 ks2 + kh)
+        uint32_t kw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const uint32_t bit = 1u << (8 * (j & 3) + 2 * (2 * (j >> 5) + ((j >> 4) & 1)));
+          kw[(j >> 2) & 3] += (x[j] >= -sc ? bit : 0u) + (x[j] >= 0.f ? bit : 0u) + (x[j] >= sc ? bit : 0u);
+        }
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq)
+          *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(rp, tq, g)) = kw[tq];
+      } else {
+        // V: byte g of the 16-bit half of channel residue c (mod 16) holds channels c + 16 r, r < 4, at bit 2 r
+        uint32_t vb[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) vb[c] = 0u;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const uint32_t bit = 1u << (2 * (j >> 4));
+          vb[j & 15] += (x[j] >= -sc ? bit : 0u) + (x[j] >= 0.f ? bit : 0u) + (x[j] >= sc ? bit : 0u);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) blk[kVCodes + v_half_offset(rp, c) + g] = (uint8_t)vb[c];
+      }
+      *reinterpret_cast<__half*>(blk + (m ? kVScales : kKScales) + 4 * rp + 2 * g) = hs;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTcCols);
   }
 }
 
@@ -321,21 +402,23 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   }
   if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
   append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
-  const int tiles = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
-  const size_t smem = sizeof(TcSmem);
+  const int pages = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
+  const int tiles2 = (pages + 1) / 2;                                    // page pairs
+  if ((long long)tiles2 * Hkv * B >= (1ll << 31)) return cudaErrorInvalidValue;
   static int sms = 0;
   if (sms == 0) {
     int dev = 0, n_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(append_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      e = cudaFuncSetAttribute(append_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     sms = n_sm;
   }
-  const long long work = (long long)tiles * Hkv * B;
-  const int blocks = (int)std::min<long long>((work + kTcSlots - 1) / kTcSlots, (long long)sms);
-  append_tile_kernel<<<blocks, kTcThreads, smem, stream>>>(a, tiles);
+  // an even grid: blocks 2 i take K, 2 i + 1 take V
+  const long long per_matrix = (long long)tiles2 * Hkv * B;
+  const int blocks = 2 * (int)std::min<long long>(per_matrix, std::max(1, sms / 2));
+  append_tile_kernel<<<blocks, kTcThreads, kTcSmem, stream>>>(a, (unsigned)tiles2);
   return cudaGetLastError();
 }
 
