@@ -143,27 +143,31 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 // sum_k x[token][k] R^T[n][k] runs as M = 128, N = 64 (one quantisation
 // group), K = 16 tcgen05 MMAs from shared memory into tensor memory.  x is
 // bf16 (exact) and R^T is held as three bf16 terms (R = t0 + t1 + t2 to
-// ~2^-24 relative), so every product is exact; the tensor core truncates its
-// fp32 sums, so the t0 products of each run of 8 / kTcRegions 16-channel
-// steps land in a fresh TMEM region, the much smaller t1, t2 products share
-// one chained region, and the epilogue adds the regions in fp32 with
-// round-to-nearest.
+// ~2^-24 relative), so every product is exact; the t0 products of a group
+// accumulate in one TMEM region, the much smaller t1, t2 products in a
+// second, and the epilogue adds the two in fp32 (the codes then match the
+// fp64 definition bit for bit outside the near-edge band).  Each group has
+// two TMEM buffers, so the MMAs of the next tile overlap the epilogue.
 //
 // Persistent blocks, one per SM, each for one matrix (even blocks K, odd V):
-//   warps 0-3   group 0 epilogue (TMEM lane 32 (warp % 4) + lane = token row)
-//   warps 4-7   group 1 epilogue
-//   warps 8-11  loaders: x rows -> shared memory (128-byte swizzle), two buffers
-//   warp 12     TMEM allocation; one thread issues the MMAs
-// An epilogue thread owns one token row of its group: absmax, fp16 scale,
-// codes, and that row's packed words (K) or bytes (V) and scale.
-constexpr int kTcRegions = 2;
-constexpr int kTcThreads = 13 * 32;
+//   warps 0-15  epilogue: warp (h, g, q) = (w / 8, w / 4 % 2, w % 4) takes
+//               token row 32 q + lane (its TMEM lane) of group g, channels
+//               16 k + 8 h + b (k < 4, b < 8); R^T's rows are permuted in
+//               shared memory so those channels come out in 32 adjacent
+//               TMEM columns; the two halves of a row swap their maxima
+//               through shared memory, then each writes whole K words or V
+//               bytes of its row
+//   warps 16-19 loaders: x rows -> shared memory (128-byte swizzle), two buffers
+//   warp 20     TMEM allocation; one thread issues the MMAs
+constexpr int kTcRegions = 1;
+constexpr int kTcThreads = 21 * 32;
 constexpr uint32_t kTcCols = 512;          // TMEM columns; group g's regions from column 256 g
 constexpr uint32_t kTcB = 0;               // R^T terms: 3 x [2 k-blocks][128 rows n][128 B]
 constexpr uint32_t kTcA = 3 * 32768;       // x tiles: 2 x [2 k-blocks][128 rows][128 B]
 constexpr uint32_t kTcBars = kTcA + 2 * 32768;
-constexpr size_t kTcSmem = kTcBars + 128 + 1024;  // barriers, TMEM address, flags, 1024-byte alignment slack
-static_assert(kTcRegions == 2, "the epilogue reads two t0 regions and the chain");
+constexpr uint32_t kTcPmax = kTcBars + 256;      // [tile parity][h][g][128 rows] float: half-row maxima
+constexpr size_t kTcSmem = kTcPmax + 4096 + 1024;  // + 1024-byte alignment slack
+static_assert(kTcRegions == 1, "the epilogue reads one t0 region and the chain");
 
 struct TcTile {
   int b, h, lp0, lo, hi, tok0, p0;
@@ -209,11 +213,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch
   const uint32_t sbase = smem_u32(sm);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTcBars);  // [2] x tile of buffer s stored
   uint64_t* empty = full + 2;                                   // [2] buffer s read by its MMAs
-  uint64_t* tfull = full + 4;                                   // [2] group g's sums in TMEM
-  uint64_t* tempty = full + 6;                                  // [2] group g's TMEM columns read
-  uint64_t* done = full + 8;                                    // every MMA of the block finished
-  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(full + 9);
-  volatile int* work = reinterpret_cast<volatile int*>(full + 10);  // [2] buffer s holds a tile (0: no more)
+  uint64_t* tfull = full + 4;                                   // [4] TMEM buffer holds its sums
+  uint64_t* tempty = full + 8;                                  // [4] TMEM buffer read
+  uint64_t* done = full + 12;                                   // every MMA of the block finished
+  uint64_t* xb = full + 13;                                     // [8] the two halves of (g, q) swapped maxima
+  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(full + 21);
+  volatile int* work = reinterpret_cast<volatile int*>(full + 22);  // [2] buffer s holds a tile (0: no more)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x & 1;
   const unsigned cta = blockIdx.x >> 1, n_cta = gridDim.x >> 1;
@@ -222,31 +227,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch
   {  // this matrix's three R^T terms
     const uint4* src = reinterpret_cast<const uint4*>(a.rot.RT_split) + (size_t)m * 3 * 128 * 16;
     for (int c = threadIdx.x; c < 3 * 128 * 16; c += kTcThreads) {
-      const int term = c >> 11, n = (c >> 4) & 127;
-      *reinterpret_cast<uint4*>(sm + kTcB + term * 32768 + sw128_offset(n, c & 15)) = __ldg(src + c);
+      const int term = c >> 11, n = (c >> 4) & 127, jj = n & 63;
+      const int col = (n & 64) | (jj & 8) << 2 | (jj >> 4) << 3 | (jj & 7);
+      *reinterpret_cast<uint4*>(sm + kTcB + term * 32768 + sw128_offset(col, c & 15)) = __ldg(src + c);
     }
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&full[i], 128);
       mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
+      mbar_init(&tempty[i], 256);
     }
     mbar_init(done, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&xb[i], 64);
     fence_mbar_init();
   }
-  if (warp == 12) tmem_alloc(tmem_at, kTcCols);
+  if (warp == 20) tmem_alloc(tmem_at, kTcCols);
   fence_proxy_async_smem();  // R^T, for the tensor core
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_at;
 
-  if (warp >= 8 && warp < 12) {
-    // loaders: thread lt stores 16-byte chunk (lt % 16) of rows lt / 16 + 8 i; after the
-    // last tile a buffer with work = 0 tells the MMA thread to stop
-    const int lt = threadIdx.x - 256, ch = lt & 15, r0 = lt >> 4;
+  if (warp >= 16 && warp < 20) {
+    const int lt = threadIdx.x - 512, ch = lt & 15, r0 = lt >> 4;
     const uint16_t* src = m ? a.v : a.k;
     int it = 0;
     for (unsigned tile = cta;; tile += n_cta) {
@@ -279,114 +286,122 @@ __global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch
       mbar_arrive(&full[s]);
       ++it;
     }
-  } else if (warp == 12) {
+  } else if (warp == 20) {
     if (lane == 0) {
-      // descriptors differ only in the start-address field (low 14 bits), which the offsets never overflow
-      constexpr uint32_t idesc = umma_idesc_bf16_f32(128, 64);
       const uint64_t dhi = umma_desc_sw128(0) & 0xFFFFFFFF00000000ull;
       const uint32_t a_lo = (uint32_t)umma_desc_sw128(sbase + kTcA), b_lo = (uint32_t)umma_desc_sw128(sbase + kTcB);
-      for (int it = 0;; ++it) {
-        const int s = it & 1;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int s = it & 1, bb = it & 1;
         if (!mbar_wait_bounded(&full[s], (it >> 1) & 1, kWaitLimit)) {
-          set_error(a.err, kErrTimeout);
+          ok = false;
           break;
         }
         if (work[s] == 0) break;
-        bool ok = true;
+        const uint32_t al = a_lo + (uint32_t)s * (32768 >> 4);
         for (int g = 0; g < 2; ++g) {
-          if (!mbar_wait_bounded(&tempty[g], (it & 1) ^ 1, kWaitLimit)) {
+          const int k = 2 * g + bb;
+          if (!mbar_wait_bounded(&tempty[k], ((it >> 1) & 1) ^ 1, kWaitLimit)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t al = a_lo + (uint32_t)s * (32768 >> 4), bl = b_lo + (uint32_t)g * (8192 >> 4);
-          const uint32_t d = tbase + 256 * g;
+          constexpr uint32_t idesc = umma_idesc_bf16_f32(128, 64);
+          const uint32_t d = tbase + 128 * k, bl = b_lo + (uint32_t)g * (8192 >> 4);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint32_t ko = (uint32_t)((i >> 2) * 16384 + (i & 3) * 32) >> 4;
             const uint64_t ad = dhi | (al + ko);
-            const int reg = i * kTcRegions / 8;
-            const bool acc = i > 0 && (i - 1) * kTcRegions / 8 == reg;
-            umma_f16(d + 64 * reg, ad, dhi | (bl + ko), idesc, acc);
-            umma_f16(d + 64 * kTcRegions, ad, dhi | (bl + ko + (32768 >> 4)), idesc, i > 0);
-            umma_f16(d + 64 * kTcRegions, ad, dhi | (bl + ko + (65536 >> 4)), idesc, true);
+            umma_f16(d, ad, dhi | (bl + ko), idesc, i > 0);
+            umma_f16(d + 64, ad, dhi | (bl + ko + (32768 >> 4)), idesc, i > 0);
+            umma_f16(d + 64, ad, dhi | (bl + ko + (65536 >> 4)), idesc, true);
           }
-          umma_commit(&tfull[g]);
+          umma_commit(&tfull[k]);
         }
-        if (!ok) {
-          set_error(a.err, kErrTimeout);
-          break;
-        }
+        if (!ok) break;
         umma_commit(&empty[s]);
       }
+      if (!ok) set_error(a.err, kErrTimeout);
       umma_commit(done);  // arrives once every MMA above has finished
       if (!mbar_wait_bounded(done, 0, kWaitLimit)) set_error(a.err, kErrTimeout);
     }
     __syncwarp();
   } else {
-    // epilogue of group g, token row 32 q + lane of each tile
-    const int g = warp >> 2, q = warp & 3, row = 32 * q + lane;
+    // epilogue: warp (h, g, q) = (warp / 8, warp / 4 % 2, warp % 4): token row 32 q + lane, group g,
+    // channels 16 k + 8 h + b (k < 4, b < 8), which the permuted R^T puts in TMEM columns 32 h + 8 k + b
+    const int g = (warp >> 2) & 1, h = warp >> 3, q = warp & 3, row = 32 * q + lane;
     const float tau = m ? a.rot.tau_v : a.rot.tau_k;
-    const uint32_t taddr = tbase + ((uint32_t)(32 * q) << 16) + 256 * g;
+    float* pmax = reinterpret_cast<float*>(sm + kTcPmax);
     int it = 0;
     for (unsigned tile = cta; tile < n_tiles; tile += n_cta) {
       TcTile t;
       if (!tc_tile(a, tile, tiles2, t)) continue;
       const int p = t.lp0 * kPage + row;
       uint8_t* blk = (p >= t.lo && p < t.hi) ? tc_block(a.c, t.b, t.h, p >> 6, a.err) : nullptr;
-      if (!mbar_wait_bounded(&tfull[g], it & 1, kWaitLimit)) {
+      const int bb = it & 1, k = 2 * g + bb;
+      if (!mbar_wait_bounded(&tfull[k], (it >> 1) & 1, kWaitLimit)) {
         set_error(a.err, kErrTimeout);
         break;
       }
       tc_fence_after();
-      float x[64];
+      float x[32];
+      {
+        float v[32], w[32];
+        const uint32_t ta = tbase + ((uint32_t)(32 * q) << 16) + 128 * k + 32 * h;
+        tmem_ld32(ta, v);
+        tmem_ld32(ta + 64, w);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float v[96];  // columns 32 hh .. of region 0, region 1 and the t1/t2 chain
-        tmem_ld32x3(taddr + 32 * hh, taddr + 64 + 32 * hh, taddr + 128 + 32 * hh, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[32 * hh + e] = (v[e] + v[32 + e]) + v[64 + e];
+        for (int e = 0; e < 32; ++e) x[e] = v[e] + w[e];
       }
       tc_fence_before();
-      mbar_arrive(&tempty[g]);
+      mbar_arrive(&tempty[k]);
+      float mx = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(x[e]));
+      // the group maximum over both halves of the row
+      float* pm = pmax + (((bb * 2 + h) * 2 + g) * 128);
+      pm[row] = mx;
+      mbar_arrive(&xb[4 * g + q]);
+      if (!mbar_wait_bounded(&xb[4 * g + q], (it & 1), kWaitLimit)) {
+        set_error(a.err, kErrTimeout);
+        break;
+      }
+      mx = fmaxf(mx, pmax[(((bb * 2 + (h ^ 1)) * 2 + g) * 128) + row]);
       ++it;
       if (blk == nullptr) continue;
       const int rp = p & 63;
-      float mx = 0.f;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) mx = fmaxf(mx, fabsf(x[j]));
       const __half hs = __float2half_rn(fminf(mx, tau) / 1.5f);
       const float sc = __half2float(hs);
       if (m == 0) {
-        // K word tq of this row and group: channel 32 ks2 + 16 kh + 4 tq + b at bit 8 b + 2 (2 ks2 + kh)
-        uint32_t kw[4] = {0u, 0u, 0u, 0u};
+        // K words tq = 2 h + b / 4: channel 16 k + 4 tq + b % 4 at bit 8 (b % 4) + 2 k
+        uint32_t kw[2] = {0u, 0u};
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const uint32_t bit = 1u << (8 * (j & 3) + 2 * (2 * (j >> 5) + ((j >> 4) & 1)));
-          kw[(j >> 2) & 3] += (x[j] >= -sc ? bit : 0u) + (x[j] >= 0.f ? bit : 0u) + (x[j] >= sc ? bit : 0u);
+        for (int e = 0; e < 32; ++e) {
+          const int kk = e >> 3, b = e & 7;
+          const uint32_t bit = 1u << (8 * (b & 3) + 2 * kk);
+          kw[b >> 2] += (x[e] >= -sc ? bit : 0u) + (x[e] >= 0.f ? bit : 0u) + (x[e] >= sc ? bit : 0u);
         }
-#pragma unroll
-        for (int tq = 0; tq < 4; ++tq)
-          *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(rp, tq, g)) = kw[tq];
+        *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(rp, 2 * h, g)) = kw[0];
+        *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(rp, 2 * h + 1, g)) = kw[1];
       } else {
-        // V: byte g of the 16-bit half of channel residue c (mod 16) holds channels c + 16 r, r < 4, at bit 2 r
-        uint32_t vb[16];
+        // V: byte g of the half of channel residue 8 h + b holds channels 16 k + 8 h + b at bit 2 k
+        uint32_t vb[8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) vb[c] = 0u;
+        for (int b = 0; b < 8; ++b) vb[b] = 0u;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const uint32_t bit = 1u << (2 * (j >> 4));
-          vb[j & 15] += (x[j] >= -sc ? bit : 0u) + (x[j] >= 0.f ? bit : 0u) + (x[j] >= sc ? bit : 0u);
+        for (int e = 0; e < 32; ++e) {
+          const uint32_t bit = 1u << (2 * (e >> 3));
+          vb[e & 7] += (x[e] >= -sc ? bit : 0u) + (x[e] >= 0.f ? bit : 0u) + (x[e] >= sc ? bit : 0u);
         }
 #pragma unroll
-        for (int c = 0; c < 16; ++c) blk[kVCodes + v_half_offset(rp, c) + g] = (uint8_t)vb[c];
+        for (int b = 0; b < 8; ++b) blk[kVCodes + v_half_offset(rp, 8 * h + b) + g] = (uint8_t)vb[b];
       }
-      *reinterpret_cast<__half*>(blk + (m ? kVScales : kKScales) + 4 * rp + 2 * g) = hs;
+      if (h == 0) *reinterpret_cast<__half*>(blk + (m ? kVScales : kKScales) + 4 * rp + 2 * g) = hs;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 12) {
+  if (warp == 20) {
     tc_fence_after();
     tmem_dealloc(tbase, kTcCols);
   }
