@@ -142,7 +142,7 @@ typedef struct {
                                        (else OSCAR_DEVERR_LENGTH, nothing written). */
 
 /*
- * New tokens.  k, v: device bf16 [n_tokens][num_kv_heads][128].
+ * New tokens.  k, v: device bf16 [n_tokens][num_kv_heads][128], 16-byte aligned.
  *   pos         device int32 [batch]: position of each request's first new token
  *               (its context length before this append).
  *   cu_seqlens  device int32 [batch + 1]: request b owns tokens

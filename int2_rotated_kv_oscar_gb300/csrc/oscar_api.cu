@@ -248,7 +248,7 @@ oscar_status oscar_kv_append(oscar_ctx* ctx, int32_t layer, const oscar_cache_vi
   } else if (args->max_tokens_per_req <= 0 || args->max_tokens_per_req > (1 << 28)) {
     return OSCAR_ERR_INVALID_ARG;
   }
-  if (!aligned16(view->int2_pages)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned16(view->int2_pages) || !aligned16(args->k) || !aligned16(args->v)) return OSCAR_ERR_INVALID_ARG;
   DeviceGuard guard(ctx->cfg.device);
   AppendLaunch a;
   a.c = refs_of(ctx, view);

@@ -14,6 +14,9 @@
 // 64 rotated channels: a = min(max|x'|, tau), s = fp16(a / 1.5),
 // code = [x' >= -s] + [x' >= 0] + [x' >= s].
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 
 #include "oscar_device.cuh"
@@ -157,15 +160,18 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 //               TMEM columns; the two halves of a row swap their maxima
 //               through shared memory, then each writes whole K words or V
 //               bytes of its row
-//   warps 16-19 loaders: x rows -> shared memory (128-byte swizzle), two buffers
-//   warp 20     TMEM allocation; one thread issues the MMAs
+//   warp 16     one thread loads x tiles by TMA (two 64-channel boxes of 128
+//               token rows each, 128-byte swizzle, rows outside the tensor
+//               read as zero) into a ring of kTcStages buffers
+//   warp 17     TMEM allocation; one thread issues the MMAs
 constexpr int kTcRegions = 1;
-constexpr int kTcThreads = 21 * 32;
+constexpr int kTcThreads = 18 * 32;
+constexpr int kTcStages = 3;
 constexpr uint32_t kTcCols = 512;          // TMEM columns; group g's regions from column 256 g
 constexpr uint32_t kTcB = 0;               // R^T terms: 3 x [2 k-blocks][128 rows n][128 B]
-constexpr uint32_t kTcA = 3 * 32768;       // x tiles: 2 x [2 k-blocks][128 rows][128 B]
-constexpr uint32_t kTcBars = kTcA + 2 * 32768;
-constexpr uint32_t kTcPmax = kTcBars + 256;      // [tile parity][h][g][128 rows] float: half-row maxima
+constexpr uint32_t kTcA = 3 * 32768;       // x tiles: kTcStages x [2 k-blocks][128 rows][128 B]
+constexpr uint32_t kTcBars = kTcA + kTcStages * 32768;
+constexpr uint32_t kTcPmax = kTcBars + 256;  // [tile parity][h][g][128 rows] float: half-row maxima
 constexpr size_t kTcSmem = kTcPmax + 4096 + 1024;  // + 1024-byte alignment slack
 static_assert(kTcRegions == 1, "the epilogue reads one t0 region and the chain");
 
@@ -206,19 +212,21 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
   return (ch >> 3) * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + (((ch & 7) ^ (row & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch a, unsigned tiles2) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    append_tile_kernel(const __grid_constant__ AppendLaunch a, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, unsigned tiles2) {
   extern __shared__ uint8_t tc_raw[];
   const uint32_t raw_s = smem_u32(tc_raw);
   uint8_t* sm = tc_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   const uint32_t sbase = smem_u32(sm);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTcBars);  // [2] x tile of buffer s stored
-  uint64_t* empty = full + 2;                                   // [2] buffer s read by its MMAs
-  uint64_t* tfull = full + 4;                                   // [4] TMEM buffer holds its sums
-  uint64_t* tempty = full + 8;                                  // [4] TMEM buffer read
-  uint64_t* done = full + 12;                                   // every MMA of the block finished
-  uint64_t* xb = full + 13;                                     // [8] the two halves of (g, q) swapped maxima
-  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(full + 21);
-  volatile int* work = reinterpret_cast<volatile int*>(full + 22);  // [2] buffer s holds a tile (0: no more)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTcBars);  // [kTcStages] x tile of buffer s landed
+  uint64_t* empty = full + kTcStages;                           // [kTcStages] buffer s read by its MMAs
+  uint64_t* tfull = empty + kTcStages;                          // [4] TMEM buffer holds its sums
+  uint64_t* tempty = tfull + 4;                                 // [4] TMEM buffer read
+  uint64_t* done = tempty + 4;                                  // every MMA of the block finished
+  uint64_t* xb = done + 1;                                      // [8] the two halves of (g, q) swapped maxima
+  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(xb + 8);
+  volatile int* work = reinterpret_cast<volatile int*>(tmem_at + 1);  // [kTcStages] buffer s holds a tile (0: no more)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x & 1;
   const unsigned cta = blockIdx.x >> 1, n_cta = gridDim.x >> 1;
@@ -233,8 +241,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch
     }
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&full[i], 128);
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -245,55 +253,57 @@ __global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch
     for (int i = 0; i < 8; ++i) mbar_init(&xb[i], 64);
     fence_mbar_init();
   }
-  if (warp == 20) tmem_alloc(tmem_at, kTcCols);
+  if (warp == 17) tmem_alloc(tmem_at, kTcCols);
   fence_proxy_async_smem();  // R^T, for the tensor core
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_at;
 
-  if (warp >= 16 && warp < 20) {
-    const int lt = threadIdx.x - 512, ch = lt & 15, r0 = lt >> 4;
-    const uint16_t* src = m ? a.v : a.k;
-    int it = 0;
-    for (unsigned tile = cta;; tile += n_cta) {
-      TcTile t;
-      const bool last = tile >= n_tiles;
-      if (!last && !tc_tile(a, tile, tiles2, t)) continue;
-      const int s = it & 1;
-      if (!mbar_wait_bounded(&empty[s], ((it >> 1) & 1) ^ 1, kWaitLimit)) {
-        set_error(a.err, kErrTimeout);
-        break;
+  if (warp == 16) {
+    if (lane == 0) {
+      // x tiles by TMA; after the last tile a buffer with work = 0 tells the MMA thread to stop
+      const CUtensorMap* tm = m ? &tmv : &tmk;
+      prefetch_tensormap(tm);
+      int it = 0;
+      bool timed_out = false;
+      for (unsigned tile = cta;; tile += n_cta) {
+        TcTile t;
+        const bool last = tile >= n_tiles;
+        if (!last && !tc_tile(a, tile, tiles2, t)) continue;
+        const int s = it % kTcStages;
+        if (!mbar_wait_bounded(&empty[s], ((it / kTcStages) & 1) ^ 1, kWaitLimit)) {
+          set_error(a.err, kErrTimeout);
+          timed_out = true;
+          break;
+        }
+        if (last) {
+          work[s] = 0;
+          mbar_arrive(&full[s]);
+          break;
+        }
+        work[s] = 1;
+        const int y0 = t.tok0 + t.lp0 * kPage - t.p0;  // token index of the tile's first row (may be < 0)
+        mbar_arrive_expect_tx(&full[s], 32768);
+        tma_load_3d(sm + kTcA + s * 32768, tm, 0, t.h, y0, &full[s]);
+        tma_load_3d(sm + kTcA + s * 32768 + 16384, tm, 64, t.h, y0, &full[s]);
+        ++it;
       }
-      if (last) {
-        if (lt == 0) work[s] = 0;
-        mbar_arrive(&full[s]);
-        break;
-      }
-      uint4 v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int p = t.lp0 * kPage + r0 + 8 * i;
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (p >= t.lo && p < t.hi)
-          v[i] = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)(t.tok0 + p - t.p0) * Hkv + t.h) * kD) + ch);
-      }
-      uint8_t* A = sm + kTcA + s * 32768;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) *reinterpret_cast<uint4*>(A + sw128_offset(r0 + 8 * i, ch)) = v[i];
-      if (lt == 0) work[s] = 1;
-      fence_proxy_async_smem();
-      mbar_arrive(&full[s]);
-      ++it;
+      // after a timeout, copies may still be in flight: wait for them, bounded (on the normal path
+      // the MMA thread has seen every one land)
+      if (timed_out)
+        for (int k = max(0, it - kTcStages); k < it; ++k)
+          mbar_wait_bounded(&full[k % kTcStages], (k / kTcStages) & 1, kWaitLimit);
     }
-  } else if (warp == 20) {
+    __syncwarp();
+  } else if (warp == 17) {
     if (lane == 0) {
       const uint64_t dhi = umma_desc_sw128(0) & 0xFFFFFFFF00000000ull;
       const uint32_t a_lo = (uint32_t)umma_desc_sw128(sbase + kTcA), b_lo = (uint32_t)umma_desc_sw128(sbase + kTcB);
       bool ok = true;
       for (int it = 0; ok; ++it) {
-        const int s = it & 1, bb = it & 1;
-        if (!mbar_wait_bounded(&full[s], (it >> 1) & 1, kWaitLimit)) {
+        const int s = it % kTcStages, bb = it & 1;
+        if (!mbar_wait_bounded(&full[s], (it / kTcStages) & 1, kWaitLimit)) {
           ok = false;
           break;
         }
@@ -401,7 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) append_tile_kernel(AppendLaunch
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 20) {
+  if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tbase, kTcCols);
   }
@@ -417,6 +427,7 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   }
   if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
   append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
+  if (a.n_tokens == 0) return cudaGetLastError();
   const int pages = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
   const int tiles2 = (pages + 1) / 2;                                    // page pairs
   if ((long long)tiles2 * Hkv * B >= (1ll << 31)) return cudaErrorInvalidValue;
@@ -430,10 +441,30 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     sms = n_sm;
   }
+  // tensor maps of k and v: [n_tokens][Hkv][128] bf16, boxes of 64 channels x 1 head x 128 tokens
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  CUtensorMap tm[2];
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)a.n_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2};
+  const cuuint32_t box[3] = {64, 1, 128}, estride[3] = {1, 1, 1};
+  for (int i = 0; i < 2; ++i) {
+    const CUresult r = encode(&tm[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(i ? a.v : a.k), dims,
+                              strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   // an even grid: blocks 2 i take K, 2 i + 1 take V
   const long long per_matrix = (long long)tiles2 * Hkv * B;
   const int blocks = 2 * (int)std::min<long long>(per_matrix, std::max(1, sms / 2));
-  append_tile_kernel<<<blocks, kTcThreads, kTcSmem, stream>>>(a, (unsigned)tiles2);
+  append_tile_kernel<<<blocks, kTcThreads, kTcSmem, stream>>>(a, tm[0], tm[1], (unsigned)tiles2);
   return cudaGetLastError();
 }
 

@@ -271,4 +271,18 @@ __device__ __forceinline__ void tmem_ld32x3(uint32_t t0, uint32_t t1, uint32_t t
   for (int i = 0; i < 96; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// TMA: a 3-D box of a tiled tensor map into shared memory, completion counted
+// on `bar` in bytes.  The map lives in kernel-parameter space (__grid_constant__).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 }  // namespace oscar
