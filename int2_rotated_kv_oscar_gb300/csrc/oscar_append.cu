@@ -38,7 +38,9 @@ __global__ void __launch_bounds__(2 * kQuantThreads, 1) append_one_kernel(Append
 }
 
 // ------------------------------------------------------------------ multi-token append
-__device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& p0, int& n, int& tok0) {
+// A request's new tokens; bad spans set an error bit (from the reporting thread).
+__device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& p0, int& n, int& tok0,
+                                             bool report = threadIdx.x == 0) {
   if (a.cu_seqlens == nullptr) {
     tok0 = b;
     n = 1;
@@ -46,18 +48,18 @@ __device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& 
     tok0 = a.cu_seqlens[b];
     n = a.cu_seqlens[b + 1] - tok0;
     if (n < 0 || tok0 < 0 || tok0 + n > a.n_tokens || n > a.max_tokens_per_req) {
-      if (threadIdx.x == 0) set_error(a.err, kErrTokens);
+      if (report) set_error(a.err, kErrTokens);
       return false;
     }
   }
   p0 = a.pos[b];
   if (p0 < 0) {
-    if (threadIdx.x == 0) set_error(a.err, kErrLength);
+    if (report) set_error(a.err, kErrLength);
     return false;
   }
   // a fresh ring holds only the new tokens: the recent window must lie inside them
   if ((a.flags & 1u) && p0 > kSink && n < kRecent) {
-    if (threadIdx.x == 0) set_error(a.err, kErrLength);
+    if (report) set_error(a.err, kErrLength);
     return false;
   }
   return n > 0;
@@ -171,8 +173,20 @@ constexpr uint32_t kTcCols = 512;          // TMEM columns; group g's regions fr
 constexpr uint32_t kTcB = 0;               // R^T terms: 3 x [2 k-blocks][128 rows n][128 B]
 constexpr uint32_t kTcA = 3 * 32768;       // x tiles: kTcStages x [2 k-blocks][128 rows][128 B]
 constexpr uint32_t kTcBars = kTcA + kTcStages * 32768;
-constexpr uint32_t kTcPmax = kTcBars + 256;  // [tile parity][h][g][128 rows] float: half-row maxima
-constexpr size_t kTcSmem = kTcPmax + 4096 + 1024;  // + 1024-byte alignment slack
+constexpr uint32_t kTcPmax = kTcBars + 512;  // [tile parity][h][g][128 rows] float: half-row maxima
+constexpr int kTcDescs = 8;                  // tile descriptors the TMA thread publishes ahead
+constexpr uint32_t kTcDesc = kTcPmax + 4096;
+constexpr size_t kTcSmem = kTcDesc + kTcDescs * 64 + 1024;  // + 1024-byte alignment slack
+// barriers (full, empty: kTcStages each; tfull, tempty: 4 each; done; 8 swaps; 2 kTcDescs), TMEM address, flags
+static_assert((2 * kTcStages + 8 + 1 + 8 + 2 * kTcDescs) * 8 + 4 + 4 * kTcStages <= 512, "barrier area");
+
+// What the epilogue needs of a tile: positions [lo, hi) of page pair (lp0, lp0 + 1) get written
+// to blk[0], blk[1] (null: nothing to write there); b < 0 marks the end of the block's tiles.
+struct TcDesc {
+  uint8_t* blk[2];
+  int b, lp0, lo, hi;
+};
+static_assert(sizeof(TcDesc) <= 64, "descriptor slot");
 static_assert(kTcRegions == 1, "the epilogue reads one t0 region and the chain");
 
 struct TcTile {
@@ -185,7 +199,7 @@ __device__ __forceinline__ bool tc_tile(const AppendLaunch& a, unsigned tile, un
   t.h = (int)(r % Hkv);
   t.b = (int)(r / Hkv);
   int n;
-  if (!request_span(a, t.b, t.p0, n, t.tok0)) return false;
+  if (!request_span(a, t.b, t.p0, n, t.tok0, true)) return false;
   t.lo = max(t.p0, kSink);
   t.hi = t.p0 + n - kRecent;
   if (t.hi <= t.lo) return false;
@@ -225,7 +239,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* tempty = tfull + 4;                                 // [4] TMEM buffer read
   uint64_t* done = tempty + 4;                                  // every MMA of the block finished
   uint64_t* xb = done + 1;                                      // [8] the two halves of (g, q) swapped maxima
-  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(xb + 8);
+  uint64_t* dfull = xb + 8;                                     // [kTcDescs] descriptor d written
+  uint64_t* dempty = dfull + kTcDescs;                          // [kTcDescs] descriptor d read by the epilogue
+  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(dempty + kTcDescs);
+  TcDesc* desc = reinterpret_cast<TcDesc*>(sm + kTcDesc);
   volatile int* work = reinterpret_cast<volatile int*>(tmem_at + 1);  // [kTcStages] buffer s holds a tile (0: no more)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x & 1;
@@ -251,6 +268,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(done, 1);
     for (int i = 0; i < 8; ++i) mbar_init(&xb[i], 64);
+    for (int i = 0; i < kTcDescs; ++i) {
+      mbar_init(&dfull[i], 1);
+      mbar_init(&dempty[i], 512);
+    }
     fence_mbar_init();
   }
   if (warp == 17) tmem_alloc(tmem_at, kTcCols);
@@ -272,16 +293,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool last = tile >= n_tiles;
         if (!last && !tc_tile(a, tile, tiles2, t)) continue;
         const int s = it % kTcStages;
-        if (!mbar_wait_bounded(&empty[s], ((it / kTcStages) & 1) ^ 1, kWaitLimit)) {
+        const int di = it % kTcDescs;
+        if (!mbar_wait_bounded(&empty[s], ((it / kTcStages) & 1) ^ 1, kWaitLimit) ||
+            !mbar_wait_bounded(&dempty[di], ((it / kTcDescs) & 1) ^ 1, kWaitLimit)) {
           set_error(a.err, kErrTimeout);
           timed_out = true;
           break;
         }
+        TcDesc& dsc = desc[di];
         if (last) {
+          dsc.b = -1;
+          mbar_arrive(&dfull[di]);
           work[s] = 0;
           mbar_arrive(&full[s]);
           break;
         }
+        dsc.b = t.b;
+        dsc.lp0 = t.lp0;
+        dsc.lo = t.lo;
+        dsc.hi = t.hi;
+        dsc.blk[0] = tc_block(a.c, t.b, t.h, t.lp0, a.err);
+        dsc.blk[1] = (t.lp0 + 1) * kPage < t.hi ? tc_block(a.c, t.b, t.h, t.lp0 + 1, a.err) : nullptr;
+        mbar_arrive(&dfull[di]);
         work[s] = 1;
         const int y0 = t.tok0 + t.lp0 * kPage - t.p0;  // token index of the tile's first row (may be < 0)
         mbar_arrive_expect_tx(&full[s], 32768);
@@ -342,12 +375,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int g = (warp >> 2) & 1, h = warp >> 3, q = warp & 3, row = 32 * q + lane;
     const float tau = m ? a.rot.tau_v : a.rot.tau_k;
     float* pmax = reinterpret_cast<float*>(sm + kTcPmax);
-    int it = 0;
-    for (unsigned tile = cta; tile < n_tiles; tile += n_cta) {
-      TcTile t;
-      if (!tc_tile(a, tile, tiles2, t)) continue;
-      const int p = t.lp0 * kPage + row;
-      uint8_t* blk = (p >= t.lo && p < t.hi) ? tc_block(a.c, t.b, t.h, p >> 6, a.err) : nullptr;
+    for (int it = 0;;) {
+      const int di = it % kTcDescs;
+      if (!mbar_wait_bounded(&dfull[di], (it / kTcDescs) & 1, kWaitLimit)) {
+        set_error(a.err, kErrTimeout);
+        break;
+      }
+      const TcDesc& dsc = desc[di];
+      const int b = dsc.b, p = dsc.lp0 * kPage + row;
+      uint8_t* blk = (b >= 0 && p >= dsc.lo && p < dsc.hi) ? dsc.blk[row >> 6] : nullptr;
+      mbar_arrive(&dempty[di]);
+      if (b < 0) break;
       const int bb = it & 1, k = 2 * g + bb;
       if (!mbar_wait_bounded(&tfull[k], (it >> 1) & 1, kWaitLimit)) {
         set_error(a.err, kErrTimeout);
