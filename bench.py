@@ -65,13 +65,12 @@ def replica_tokens_per_s(ms_per_step, world):
     return world * 1000.0 / ms_per_step
 
 
-def profiled_traffic():
-    """DRAM bytes per layer step (the fused decode-step kernel) from the
-    committed ncu summary of this workload, or None when the decode source has
-    changed since those counters were taken."""
+def profiled_figure(summary, source, key):
+    """A figure from a committed ncu summary under profiles/, or None when the
+    kernel source it names has changed since those counters were taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "decode_step_qwen3_8b_100k.md")
-    src = os.path.join(ROOT, "int2_rotated_kv_oscar_gb300", "csrc", "oscar_decode.cu")
+    path = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "int2_rotated_kv_oscar_gb300", "csrc", source)
     try:
         fields = {}
         with open(path) as f:
@@ -81,11 +80,16 @@ def profiled_traffic():
                     fields[k.strip()] = v.strip().strip("`")
         with open(src, "rb") as f:
             digest = hashlib.sha256(f.read()).hexdigest()
-        if fields.get("oscar_decode.cu sha256") != digest:
+        if fields.get(source + " sha256") != digest:
             return None
-        return int(fields["dram bytes per layer step"])
+        return int(fields[key])
     except Exception:
         return None
+
+
+def profiled_traffic():
+    """DRAM bytes per layer step of the fused decode-step kernel."""
+    return profiled_figure("decode_step_qwen3_8b_100k.md", "oscar_decode.cu", "dram bytes per layer step")
 
 
 def measured_peaks():
@@ -469,12 +473,21 @@ def run_cuda(args):
                 tc_peak, tc_kind = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16, burst)"
         except Exception:
             tc_peak, tc_kind = 1900.0, "fallback"
-        bulk = {"tokens": n_b, "kv_heads": HKV, "ms": a_ms, "gbs": a_bytes / (a_ms / 1e3) / 1e9,
-                "algorithmic_bytes": a_bytes, "hbm_frac": a_bytes / (a_ms / 1e3) / 1e9 / measured_peaks()[0],
-                "roofline": {"bound": "tensor", "achieved": a_flop / (a_ms / 1e3) / 1e12, "peak": tc_peak,
-                             "unit": "TFLOP/s", "frac": a_flop / (a_ms / 1e3) / 1e12 / tc_peak,
-                             "peak_kind": tc_kind, "flop_per_call": a_flop,
-                             "executed_tflops": 3 * a_flop / (a_ms / 1e3) / 1e12},
+        hbm_peak = measured_peaks()[0]
+        a_gbs = a_bytes / (a_ms / 1e3) / 1e9
+        bulk = {"tokens": n_b, "kv_heads": HKV, "ms": a_ms, "gbs": a_gbs, "algorithmic_bytes": a_bytes,
+                "roofline": {"bound": "hbm", "achieved": a_gbs, "peak": hbm_peak, "unit": "GB/s",
+                             "frac": a_gbs / hbm_peak,
+                             "traffic": profiled_figure("bulk_append_131k_8heads.md", "oscar_append.cu",
+                                                        "dram bytes per call"),
+                             "note": "algorithmic bytes: bf16 K and V in, INT2 codes + scales and BF16 sink/recent "
+                                     "rows out; the x R flops (68.7 GFLOP) take ~36 us at the bf16 peak, the bytes "
+                                     "~92 us at the copy bandwidth"},
+                "tensor": {"algorithmic_tflops": a_flop / (a_ms / 1e3) / 1e12,
+                           "executed_tflops": 3 * a_flop / (a_ms / 1e3) / 1e12, "peak": tc_peak,
+                           "executed_frac": 3 * a_flop / (a_ms / 1e3) / 1e12 / tc_peak, "peak_kind": tc_kind,
+                           "note": "tcgen05 M=128 N=64 K=16 MMAs; R^T as three bf16 terms, so the tensor cores "
+                                   "run x R three times to keep the codes exact"},
                 "note": "oscar_kv_append of one 131,072-token prompt (BF16 K and V in, INT2 history + BF16 "
                         "sink/recent out), mean of 10 eager calls"}
         del acache, ka, va
@@ -511,6 +524,39 @@ def run_cuda(args):
                        "decode over the shared pages with its causal limit, so the pages are read once per query "
                        "(from L2 when they stay there) and unpacked once per query; the prefix bytes are counted once"}
         del wse_t, etabs
+        # the chunk kernel: each page unpacked once per (KV head, 16 queries), for chunks of 16..256
+        ext["chunk_kernel"] = []
+        for n_c in (16, 64, 256):
+            q_c = inputs.decode_queries_bf16(CFG, 0, n_c, HQ, step=9).to(dev).reshape(1, n_c, HQ, D)
+            out_c = torch.empty((1, n_c, HQ, D), dtype=torch.float32, device=dev)
+            len_c = torch.full((1,), L_e, dtype=torch.int32, device=dev)
+            pos_c = torch.full((1,), L_e - n_c, dtype=torch.int32, device=dev)
+            wsc_t, wsc, wsc_bytes = kvcache.extend_workspace(ctx, 1, n_c, L_e, device=dev)
+            view0 = cache.view(0)
+
+            def call():
+                abi.oscar_extend_chunk(ctx, 0, view0, q_c, out_c, len_c, pos_c, n_c, L_e, wsc, wsc_bytes,
+                                       stream=cur)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+            torch.cuda.synchronize()
+            assert abi.oscar_check_device_error(ctx) == 0
+            c_ms = e0.elapsed_time(e1) / reps
+            c_flop = 4.0 * HQ * n_c * D * (L_e - n_c / 2.0)
+            ext["chunk_kernel"].append({
+                "chunk_tokens": n_c, "ms_per_call": c_ms, "tokens_per_s": n_c / (c_ms / 1e3),
+                "gbs_prefix_once": e_bytes / (c_ms / 1e3) / 1e9,
+                "hbm_frac_prefix_once": e_bytes / (c_ms / 1e3) / 1e9 / peak_e,
+                "attention_tflops": c_flop / (c_ms / 1e3) / 1e12})
+            del wsc_t
+        ext["chunk_kernel_note"] = ("oscar_extend_chunk: one block per (KV head, 16 queries, page range); a page "
+                                    "is unpacked once into fp16 tiles shared by the block's 16 x G query rows; "
+                                    "attention_tflops counts Q.K and P.V over each query's causal prefix")
 
     # ---- BF16-cache comparator of the same shape (decode attention, all 36 layers)
     bf16 = None

@@ -105,6 +105,15 @@ def decode_args(q, out, ctx_len, max_ctx_len, sm_scale=0.0):
                                  max_ctx_len=int(max_ctx_len), sm_scale=float(sm_scale))
 
 
+def extend_workspace(ctx, batch, chunk, max_ctx_len, device="cuda"):
+    """A caller-owned workspace for oscar_extend_chunk (uint8 tensor, 256-byte
+    aligned, zero-filled).  Returns (tensor, pointer, bytes)."""
+    n = abi.oscar_extend_workspace_bytes(ctx, batch, chunk, max_ctx_len)
+    t = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    off = (-t.data_ptr()) % 256
+    return t, t.data_ptr() + off, n
+
+
 def workspace(ctx, max_batch, max_ctx_len, device="cuda"):
     """A caller-owned decode workspace (uint8 tensor, 256-byte aligned, zero-filled
     as the fused decode step wants it before its first use)."""
