@@ -108,6 +108,8 @@ typedef struct {
  *   k_sink, v_sink  bf16 [num_sink_pages][num_kv_heads][64][128]: positions 0..63.
  *   k_ring, v_ring  bf16 [num_ring_slots][num_kv_heads][256][128]: position p >= 64
  *               of a request lives in row (p - 64) % 256 of its ring slot.
+ *               With a recent_page_table they are instead a pool of
+ *               num_ring_slots BF16 pages [num_kv_heads][64][128].
  *   page_table  int32 [batch][max_pages_per_req]: entry i (i >= 1) is the
  *               physical INT2 page of positions [64 i, 64 i + 64); entry 0 is
  *               unused.  Entries may alias (shared prefixes); the caller
@@ -132,6 +134,17 @@ typedef struct {
   const int32_t* sink_page;
   const int32_t* ring_slot;
   int32_t batch;
+  /*
+   * Optional paged recent window (NULL: the ring).  int32 [batch][max_pages_per_req]:
+   * entry i names the BF16 page (in k_ring / v_ring) holding the recent rows of
+   * positions [64 i, 64 i + 64), row p % 64 for position p.  The window is still
+   * the last 256 positions ([IT] "Architettura ...": the 256 most recent tokens
+   * stay BF16); the entries of the logical pages it touches (at most five, and
+   * the one an append writes) must be valid, the others are not read.  Pages of
+   * positions shared by several requests may alias; as with page_table, the
+   * caller never lets an append write a shared page.  ring_slot may be NULL.
+   */
+  const int32_t* recent_page_table;
 } oscar_cache_view;
 
 /* Append flags. */

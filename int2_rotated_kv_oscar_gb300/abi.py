@@ -55,7 +55,8 @@ class oscar_cache_view(ctypes.Structure):
                 ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p), ("num_sink_pages", ctypes.c_int64),
                 ("k_ring", ctypes.c_void_p), ("v_ring", ctypes.c_void_p), ("num_ring_slots", ctypes.c_int64),
                 ("page_table", ctypes.c_void_p), ("max_pages_per_req", ctypes.c_int32),
-                ("sink_page", ctypes.c_void_p), ("ring_slot", ctypes.c_void_p), ("batch", ctypes.c_int32)]
+                ("sink_page", ctypes.c_void_p), ("ring_slot", ctypes.c_void_p), ("batch", ctypes.c_int32),
+                ("recent_page_table", ctypes.c_void_p)]
 
 
 class oscar_append_args(ctypes.Structure):

@@ -41,7 +41,7 @@ bool valid_view(const oscar_ctx* ctx, const oscar_cache_view* v) {
   if (v == nullptr || v->batch < 0) return false;
   if (v->batch == 0) return true;
   return v->int2_pages && v->k_sink && v->v_sink && v->k_ring && v->v_ring && v->page_table && v->sink_page &&
-         v->ring_slot && v->num_pages > 0 && v->num_sink_pages > 0 && v->num_ring_slots > 0 &&
+         (v->ring_slot || v->recent_page_table) && v->num_pages > 0 && v->num_sink_pages > 0 && v->num_ring_slots > 0 &&
          v->max_pages_per_req > 0 && v->num_pages <= INT32_MAX && v->num_sink_pages <= INT32_MAX &&
          v->num_ring_slots <= INT32_MAX && ctx != nullptr;
 }
@@ -62,6 +62,7 @@ CacheRefs refs_of(const oscar_ctx* ctx, const oscar_cache_view* v) {
   c.ring_slot = v->ring_slot;
   c.batch = v->batch;
   c.num_kv_heads = ctx->cfg.num_kv_heads;
+  c.recent_table = v->recent_page_table;
   return c;
 }
 

@@ -80,15 +80,11 @@ __global__ void __launch_bounds__(2 * kQuantThreads, 1) append_evict_kernel(Appe
   const int e = e0 + x;
   if (e >= e1) return;
   const CacheRefs& c = a.c;
-  const int slot = c.ring_slot[b];
-  if (slot < 0 || slot >= c.num_ring) {
-    if (threadIdx.x == 0) set_error(a.err, kErrRing);
-    return;
-  }
+  size_t r;
+  if (!recent_row(c, b, h, e, r, a.err, threadIdx.x == 0)) return;
   uint8_t* blk = history_block(c, b, h, e, a.err);
   if (blk == nullptr) return;
-  const size_t r = (((size_t)slot * c.num_kv_heads + h) * kRecent + ((e - kSink) % kRecent)) * kD + t;
-  const float xv = bf16_bits_to_float((is_v ? c.v_ring : c.k_ring)[r]);
+  const float xv = bf16_bits_to_float((is_v ? c.v_ring : c.k_ring)[r + t]);
   quantize_token(xv, is_v ? a.rot.R_V : a.rot.R_K, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm[half], u,
                  1 + half);
 }
@@ -126,18 +122,14 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
   }
   p = max(max(p0, L - kRecent), kSink) + (x - kSink);
   if (p >= L) return;
-  const int slot = c.ring_slot[b];
-  if (slot < 0 || slot >= c.num_ring) {
-    if (t == 0) set_error(a.err, kErrRing);
-    return;
-  }
   kd = c.k_ring;
   vd = c.v_ring;
   for (int h = 0; h < Hkv; ++h) {
+    size_t d;
+    if (!recent_row(c, b, h, p, d, a.err, t == 0)) return;
     const size_t s = ((size_t)(tok0 + p - p0) * Hkv + h) * kD + t;
-    const size_t d = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
-    kd[d] = a.k[s];
-    vd[d] = a.v[s];
+    kd[d + t] = a.k[s];
+    vd[d + t] = a.v[s];
   }
 }
 

@@ -550,13 +550,19 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
 // SUB: row `sub` of the tile (-1: none) is read from knew / vnew instead.
 template <bool PACK4, bool SUB = false>
 __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
-                                          uint32_t rows, const uint32_t* qpf, float scaleEp, WarpState& st,
-                                          int lane, int sub = -1, const uint16_t* knew = nullptr,
+                                          const uint16_t* __restrict__ Kt2, const uint16_t* __restrict__ Vt2,
+                                          int split, uint32_t rows, const uint32_t* qpf, float scaleEp,
+                                          WarpState& st, int lane, int sub = -1, const uint16_t* knew = nullptr,
                                           const uint16_t* vnew = nullptr) {
   const int q = lane >> 2, tig = lane & 3;
   const bool va = (rows >> q) & 1u, vb = (rows >> (q + 8)) & 1u;
-  const uint16_t* krow_a = SUB && q == sub ? knew : Kt + q * kD;
-  const uint16_t* krow_b = SUB && q + 8 == sub ? knew : Kt + (q + 8) * kD;
+  // row r of the tile: (r < split ? Kt : Kt2) + r * 128 (two runs of positions in a paged recent window)
+  const uint16_t* Ka = q < split ? Kt : Kt2;
+  const uint16_t* Kb = q + 8 < split ? Kt : Kt2;
+  const uint16_t* Va = q < split ? Vt : Vt2;
+  const uint16_t* Vb = q + 8 < split ? Vt : Vt2;
+  const uint16_t* krow_a = SUB && q == sub ? knew : Ka + q * kD;
+  const uint16_t* krow_b = SUB && q + 8 == sub ? knew : Kb + (q + 8) * kD;
   uint32_t ka[16], kb[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -616,7 +622,7 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
       const int tr = blkid >> 1, cc = blkid & 1;  // token half, channel half
       const bool ok = tr ? vb : va;
       const int r = 8 * tr + q;
-      const uint16_t* vrow = SUB && r == sub ? vnew : Vt + r * kD;
+      const uint16_t* vrow = SUB && r == sub ? vnew : (tr ? Vb : Va) + r * kD;
       const uint32_t u = ok ? __ldg(reinterpret_cast<const uint32_t*>(vrow + 16 * mt + 8 * cc + 2 * tig)) : 0u;
       a[blkid] = movmatrix_trans(bf16x2_to_f16x2(u));
     }
@@ -667,6 +673,32 @@ __device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv
 
 // BF16 tile j (0..19) of a (request, KV head): tiles 0..3 are the sink page's
 // rows 16 j .. 16 j + 15, tiles 4..19 rows 16 (j - 4) .. of the 256-row ring.
+// Where the 16 ring rows rr0 .. rr0 + 15 of request b, KV head h live (element
+// offsets into k_ring / v_ring): row r at (r < split ? off1 : off2) + r * 128.
+// Ring row rr holds window position hist_end + ((rr - (hist_end - 64)) mod 256);
+// the rows of a tile form one or two runs of consecutive positions (split where
+// the oldest window position sits), each inside one 16-aligned block of
+// positions, so inside one page of a paged recent window.
+__device__ __forceinline__ bool recent_tile(const CacheRefs& c, int b, int h, int L, int rr0, size_t& off1,
+                                            size_t& off2, int& split, unsigned* err, bool report) {
+  const int hist_end = max(kSink, L - kRecent), rw = (hist_end - kSink) % kRecent;
+  if (c.recent_table == nullptr) {  // the ring: contiguous rows
+    split = 16;
+    if (!recent_row(c, b, h, kSink + rr0, off1, err, report)) return false;
+    off2 = off1;
+    return true;
+  }
+  split = (rw > rr0 && rw < rr0 + 16) ? rw - rr0 : 16;
+  const int p0 = hist_end + (((rr0 - rw) % kRecent) + kRecent) % kRecent;
+  if (!recent_row(c, b, h, p0, off1, err, report)) return false;
+  off2 = off1;
+  if (split < 16) {
+    if (!recent_row(c, b, h, hist_end, off2, err, report)) return false;
+    off2 -= (size_t)split * kD;
+  }
+  return true;
+}
+
 __device__ __forceinline__ int bf16_tile_rows(int j, int L, size_t& row_off, bool& ring) {
   if (j < 4) {
     ring = false;
@@ -1156,8 +1188,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
           }
           scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
         }
-        const int sp = c.sink_page[b], slot = c.ring_slot[b];
-        const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
+        const int sp = c.sink_page[b];
+        const bool sink_ok = sp >= 0 && sp < c.num_sink;
         for (int k = bk; k < a.tiles_per_item; k += kBf16Slots) {
           const int j = item * a.tiles_per_item + k;
           if (j >= kBf16Tiles) break;
@@ -1165,12 +1197,17 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
           bool ring;
           const int nv = bf16_tile_rows(j, L, row_off, ring);
           if (nv <= 0) continue;
-          if (ring ? !ring_ok : !sink_ok) {
-            if (lane == 0) set_error(a.err, ring ? kErrRing : kErrSink);
-            continue;
+          size_t off, off2;
+          int split = 16;
+          if (ring) {
+            if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) continue;
+          } else {
+            if (!sink_ok) {
+              if (lane == 0) set_error(a.err, kErrSink);
+              continue;
+            }
+            off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
           }
-          const size_t off = ring ? ((((size_t)slot * a.Hkv + h) * kRecent + row_off) * kD)
-                                  : ((((size_t)sp * a.Hkv + h) * kSink + row_off) * kD);
           // fused step: the new token's row comes from the input
           int sub = -1;
           if (FUSED && p_new >= 0) {
@@ -1193,9 +1230,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
             }
             if (rows == 0) continue;  // nothing to attend (and a state with no max yet must stay empty)
           }
-          bf16_tile<PACK4, FUSED>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, rows,
-                                  qpf, scaleEp, st, lane, sub, FUSED ? f->ap.k + nrow : nullptr,
-                                  FUSED ? f->ap.v + nrow : nullptr);
+          const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
+          const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
+          bf16_tile<PACK4, FUSED>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp,
+                                  st, lane, sub, FUSED ? f->ap.k + nrow : nullptr, FUSED ? f->ap.v + nrow : nullptr);
         }
       }
       store_state<PACK4>(st, bf16_slots + (size_t)bk * kPartialFloats, 1.0f / kPScaleBF16, lane);
@@ -1309,7 +1347,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
         const int nv = min(16, L - kPage * pg - 16 * tile);
         if (nv <= 0) continue;
         const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
-        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, (1u << nv) - 1u, qpf, scaleEp, st, lane);
+        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, a.kb_pages + off, a.vb_pages + off, 16, (1u << nv) - 1u,
+                         qpf, scaleEp, st, lane);
       }
     }
     store_state<PACK4>(st, reinterpret_cast<float*>(stage_ptr(1)), 1.0f / kPScaleBF16, lane);
@@ -1632,8 +1671,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
   // BF16 sink/recent tiles of this item, each warp for its query (original basis)
   state_init(st);
   if (active) {
-    const int sp = c.sink_page[b], slot = c.ring_slot[b];
-    const bool sink_ok = sp >= 0 && sp < c.num_sink, ring_ok = slot >= 0 && slot < c.num_ring;
+    const int sp = c.sink_page[b];
+    const bool sink_ok = sp >= 0 && sp < c.num_sink;
     for (int k = 0; k < a.tiles_per_item; ++k) {
       const int j = item * a.tiles_per_item + k;
       if (j >= kBf16Tiles) break;
@@ -1641,9 +1680,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
       bool ring;
       const int nv = bf16_tile_rows(j, L, row_off, ring);
       if (nv <= 0) continue;
-      if (ring ? !ring_ok : !sink_ok) {
-        if (lane == 0) set_error(a.err, ring ? kErrRing : kErrSink);
-        continue;
+      size_t off, off2;
+      int split = 16;
+      if (ring) {
+        if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) continue;
+      } else {
+        if (!sink_ok) {
+          if (lane == 0) set_error(a.err, kErrSink);
+          continue;
+        }
+        off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
       }
       uint32_t rows = (1u << nv) - 1u;
       if (!ring) {
@@ -1656,10 +1702,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
         }
       }
       if (rows == 0) continue;
-      const size_t off = ring ? ((((size_t)slot * a.Hkv + h) * kRecent + row_off) * kD)
-                              : ((((size_t)sp * a.Hkv + h) * kSink + row_off) * kD);
-      bf16_tile<true>((ring ? c.k_ring : c.k_sink) + off, (ring ? c.v_ring : c.v_sink) + off, rows, qpf, scaleEp,
-                      st, lane);
+      const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
+      const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
+      bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, st, lane);
     }
     store_state<true>(st, rec + kPartialFloats, 1.0f / kPScaleBF16, lane);
   }

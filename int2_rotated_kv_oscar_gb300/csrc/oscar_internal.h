@@ -36,6 +36,7 @@ struct CacheRefs {
   const int32_t* ring_slot = nullptr;
   int32_t batch = 0;
   int32_t num_kv_heads = 0;
+  const int32_t* recent_table = nullptr;  // [batch][max_pages] BF16 recent pages (null: the ring)
 };
 
 struct AppendLaunch {

@@ -135,6 +135,35 @@ __device__ __forceinline__ void quantize_token(float x, const float* __restrict_
 }
 
 // Locate (and check) the INT2 block of position e of request b, head h.
+// Element offset of the BF16 recent row of position p (>= 64) of request b,
+// KV head h (channel 0) in k_ring / v_ring: row (p - 64) % 256 of the request's
+// ring slot, or, with a recent page table, row p % 64 of the BF16 page holding
+// logical page p / 64.  False (and an error bit, if report) for a bad entry.
+__device__ __forceinline__ bool recent_row(const CacheRefs& c, int b, int h, int p, size_t& off, unsigned* err,
+                                           bool report) {
+  if (c.recent_table != nullptr) {
+    const int lp = p >> 6;
+    if (lp >= c.max_pages) {
+      if (report) set_error(err, kErrLength);
+      return false;
+    }
+    const int pg = c.recent_table[(size_t)b * c.max_pages + lp];
+    if (pg < 0 || pg >= c.num_ring) {
+      if (report) set_error(err, kErrRing);
+      return false;
+    }
+    off = (((size_t)pg * c.num_kv_heads + h) * kPage + (p & 63)) * kD;
+    return true;
+  }
+  const int slot = c.ring_slot[b];
+  if (slot < 0 || slot >= c.num_ring) {
+    if (report) set_error(err, kErrRing);
+    return false;
+  }
+  off = (((size_t)slot * c.num_kv_heads + h) * kRecent + ((p - kSink) % kRecent)) * kD;
+  return true;
+}
+
 __device__ __forceinline__ uint8_t* history_block(const CacheRefs& c, int b, int h, int e, unsigned* err) {
   const int lp = e >> 6;
   if (lp >= c.max_pages) {
@@ -164,7 +193,6 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
   const int Hkv = c.num_kv_heads;
   // independent loads first, so that their round trips overlap
   const int p = a.pos[b];
-  const int slot = c.ring_slot[b];
   const uint16_t xn = (is_v ? a.v : a.k)[((size_t)b * Hkv + h) * kD + t];
   if (p < 0 || ((a.flags & 1u) && p > kSink)) {
     if (threadIdx.x == 0) set_error(a.err, kErrLength);
@@ -179,16 +207,16 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
     if (mover) (is_v ? c.v_sink : c.k_sink)[(((size_t)sp * Hkv + h) * kSink + p) * kD + t] = xn;
     return;
   }
-  if (slot < 0 || slot >= c.num_ring) {
-    if (threadIdx.x == 0) set_error(a.err, kErrRing);
-    return;
-  }
   uint16_t* ring = is_v ? c.v_ring : c.k_ring;
-  const size_t rdst = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
+  size_t rdst;
+  if (!recent_row(c, b, h, p, rdst, a.err, threadIdx.x == 0)) return;
+  rdst += t;
   if (p >= kSink + kRecent) {
-    // the token at e = p - 256 leaves the window: same ring row, read before overwrite
+    // the token at e = p - 256 leaves the window (in the ring: the same row, read before overwrite)
     const int e = p - kRecent;
-    const uint16_t xo = ring[rdst];  // in flight while the page table is read
+    size_t rsrc;
+    if (!recent_row(c, b, h, e, rsrc, a.err, threadIdx.x == 0)) return;
+    const uint16_t xo = ring[rsrc + t];  // in flight while the page table is read
     uint8_t* blk = history_block(c, b, h, e, a.err);
     if (blk != nullptr)
       quantize_token(bf16_bits_to_float(xo), is_v ? Rv : Rk, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v,
@@ -209,7 +237,6 @@ __device__ __forceinline__ void append_pair_body(const AppendLaunch& a, int b, i
   const int Hkv = c.num_kv_heads, t = u & 127;
   const bool mover = u < kD;
   const int p = a.pos[b];
-  const int slot = c.ring_slot[b];
   const size_t nrow = ((size_t)b * Hkv + h) * kD + t;
   const uint16_t xk = a.k[nrow], xv = a.v[nrow];
   if (p < 0 || ((a.flags & 1u) && p > kSink)) {
@@ -229,14 +256,15 @@ __device__ __forceinline__ void append_pair_body(const AppendLaunch& a, int b, i
     }
     return;
   }
-  if (slot < 0 || slot >= c.num_ring) {
-    if (threadIdx.x == 0) set_error(a.err, kErrRing);
-    return;
-  }
-  const size_t rdst = (((size_t)slot * Hkv + h) * kRecent + ((p - kSink) % kRecent)) * kD + t;
+  size_t rdst;
+  if (!recent_row(c, b, h, p, rdst, a.err, threadIdx.x == 0)) return;
+  rdst += t;
   if (p >= kSink + kRecent) {
     const int e = p - kRecent;
-    const uint16_t ok = c.k_ring[rdst], ov = c.v_ring[rdst];  // in flight while the page table is read
+    size_t rsrc;
+    if (!recent_row(c, b, h, e, rsrc, a.err, threadIdx.x == 0)) return;
+    rsrc += t;
+    const uint16_t ok = c.k_ring[rsrc], ov = c.v_ring[rsrc];  // in flight while the page table is read
     uint8_t* blk = history_block(c, b, h, e, a.err);
     if (blk != nullptr) {
       quantize_token(bf16_bits_to_float(ok), rk, a.rot.tau_k, blk, e & 63, false, sm, u, bar, patch);

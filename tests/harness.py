@@ -37,7 +37,7 @@ class Setup:
     """One context + one mixed cache on cuda:0 for a batch of requests."""
 
     def __init__(self, Hq, Hkv, lengths_max, batch, num_layers=1, cfg=1, flags=abi.OSCAR_ROT_ALL, seed=0,
-                 extra_pages=3, shuffle=True, calibrate=True):
+                 extra_pages=3, shuffle=True, calibrate=True, paged_recent=False):
         self.Hq, self.Hkv, self.batch, self.cfg = Hq, Hkv, batch, cfg
         self.flags = flags
         conf = abi.oscar_config(num_layers=num_layers, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
@@ -57,10 +57,19 @@ class Setup:
             self.rot.append((R_K, R_V, float(tk), float(tv)))
         self.max_pages = (lengths_max + 63) // 64 + 1
         num_pages = batch * self.max_pages + extra_pages
-        self.cache = kvcache.MixedCache(num_layers, Hkv, num_pages, batch, batch, batch, self.max_pages)
+        # paged recent window: five BF16 pages per request, logical page lp in page lp % 5
+        # (the window touches at most five logical pages), shuffled over the pool
+        self.paged_recent = paged_recent
+        self.cache = kvcache.MixedCache(num_layers, Hkv, num_pages, batch, batch, batch, self.max_pages,
+                                        recent_pages=5 * batch + 2 if paged_recent else None)
         perm = inputs.shuffled_pages(cfg, num_pages, seed) if shuffle else np.arange(num_pages, dtype=np.int32)
         table = perm[:batch * self.max_pages].reshape(batch, self.max_pages)
         self.cache.page_table.copy_(torch.from_numpy(table))
+        if paged_recent:
+            rperm = inputs.shuffled_pages(cfg + 1000, 5 * batch + 2, seed)
+            lp = np.arange(self.max_pages)
+            rt = np.stack([rperm[5 * b + lp % 5] for b in range(batch)]).astype(np.int32)
+            self.cache.recent_table.copy_(torch.from_numpy(rt))
         self.ws_tensor, self.ws, self.ws_bytes = kvcache.workspace(self.ctx, batch, lengths_max + 1)
 
     def close(self):
@@ -102,8 +111,20 @@ class Setup:
         out = []
         sk = inputs.bf16_to_f64(c.k_sink[layer][sp])
         sv = inputs.bf16_to_f64(c.v_sink[layer][sp])
-        rk = inputs.bf16_to_f64(c.k_ring[layer][rs])
-        rv = inputs.bf16_to_f64(c.v_ring[layer][rs])
+        if c.paged_recent:
+            # gather the window's rows from the BF16 pages into ring order (row (p - 64) % 256)
+            (_, _), _, (r0, r1) = ocache.segments(L)
+            kp = inputs.bf16_to_f64(c.k_ring[layer])
+            vp = inputs.bf16_to_f64(c.v_ring[layer])
+            rt = c.recent_table[b].cpu().numpy()
+            rk = np.zeros((self.Hkv, 256, 128))
+            rv = np.zeros((self.Hkv, 256, 128))
+            for p in range(r0, r1):
+                rk[:, (p - 64) % 256] = kp[rt[p // 64], :, p % 64]
+                rv[:, (p - 64) % 256] = vp[rt[p // 64], :, p % 64]
+        else:
+            rk = inputs.bf16_to_f64(c.k_ring[layer][rs])
+            rv = inputs.bf16_to_f64(c.v_ring[layer][rs])
         for h in range(self.Hkv):
             blocks = pages[:, h, :] if n_pages else np.zeros((0, 4608), dtype=np.uint8)
             out.append((sk[h], sv[h], rk[h], rv[h], blocks))
@@ -190,11 +211,13 @@ def request_view(setup, b0, b1):
     """Swap the cache's per-request tables for rows [b0, b1) (for appending a
     subset of the batch); returns a function that restores them."""
     c = setup.cache
-    saved = (c.page_table, c.sink_page, c.ring_slot)
+    saved = (c.page_table, c.sink_page, c.ring_slot, c.recent_table)
     c.page_table = saved[0][b0:b1].contiguous()
     c.sink_page = saved[1][b0:b1].contiguous()
     c.ring_slot = saved[2][b0:b1].contiguous()
+    if saved[3] is not None:
+        c.recent_table = saved[3][b0:b1].contiguous()
 
     def restore():
-        c.page_table, c.sink_page, c.ring_slot = saved
+        c.page_table, c.sink_page, c.ring_slot, c.recent_table = saved
     return restore

@@ -77,6 +77,7 @@ def test_host_checks_need_no_gpu(lib):
 def test_struct_layouts_match_the_header():
     # field order and sizes of the ctypes mirrors (x86-64 / aarch64 LP64 ABI)
     assert ctypes.sizeof(abi.oscar_config) == 9 * 4
-    assert abi.oscar_cache_view.batch.offset == ctypes.sizeof(abi.oscar_cache_view) - 8
+    assert abi.oscar_cache_view.batch.offset == 96
+    assert abi.oscar_cache_view.recent_page_table.offset == 104 and ctypes.sizeof(abi.oscar_cache_view) == 112
     assert ctypes.sizeof(abi.oscar_append_args) == 8 * 4 + 3 * 4 + 4
     assert ctypes.sizeof(abi.oscar_decode_args) == 3 * 8 + 8
