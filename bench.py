@@ -558,6 +558,44 @@ def run_cuda(args):
                                     "is unpacked once into fp16 tiles shared by the block's 16 x G query rows; "
                                     "attention_tflops counts Q.K and P.V over each query's causal prefix")
 
+    # ---- paged BF16 recent window: the same one-layer decode step with the last 256
+    # positions in BF16 pages (five per request, logical page lp in page lp % 5)
+    # instead of the ring, each mode timed as 32 isolated launches behind a GPU-side sleep
+    paged = None
+    if rank == 0 and not args.no_paged:
+        pc = kvcache.MixedCache(1, HKV, maxp, 1, 1, 1, maxp, device=dev, recent_pages=5)
+        pc.page_table.copy_(cache.page_table)
+        pc.recent_table.copy_((torch.arange(maxp, dtype=torch.int32, device=dev) % 5).view(1, maxp))
+        kp, vp = inputs.kv_tokens_device(CFG, 0, HKV, inputs.STREAM_KV, CTX0, dev)
+        abi.oscar_kv_append(ctx, 0, pc.view(0), kvcache.append_args(kp, vp, pos0, cu, CTX0), cur)
+        del kp, vp
+        pws_t, pws, pws_bytes = kvcache.workspace(ctx, 1, max_ctx, device=dev)
+        pout = torch.zeros((1, HQ, D), dtype=torch.float32, device=dev)
+        pev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        times = {}
+        for mode, pv, w, wb in (("ring", views[0], ws, ws_bytes), ("paged", pc.view(0), pws, pws_bytes)):
+            ds = []
+            for j in range(40):
+                ap = kvcache.append_args(kn[0:1], vn[0:1], pos_buf[j:j + 1])
+                dp = kvcache.decode_args(q_all[0], pout, len_buf[j:j + 1], max_ctx)
+                if j >= 8:
+                    torch.cuda._sleep(20_000_000)
+                    pev[0].record(cur)
+                abi.oscar_decode_step(ctx, 0, pv, ap, dp, w, wb, cur)
+                if j >= 8:
+                    pev[1].record(cur)
+                    torch.cuda.synchronize()
+                    ds.append(pev[0].elapsed_time(pev[1]))
+            torch.cuda.synchronize()
+            times[mode] = float(np.median(ds))
+        assert abi.oscar_check_device_error(ctx) == 0
+        paged = {"ms_per_layer_step_paged": times["paged"], "ms_per_layer_step_ring": times["ring"],
+                 "paged_over_ring": times["paged"] / times["ring"],
+                 "note": "oscar_decode_step of one layer at positions 100,000 .. 100,039 (crossing a page "
+                         "boundary), isolated launches, median; the recent window in five recycled BF16 pages "
+                         "through the recent page table vs the ring slot"}
+        del pc, pws_t
+
     # ---- BF16-cache comparator of the same shape (decode attention, all 36 layers)
     bf16 = None
     if not args.no_bf16:
@@ -739,6 +777,7 @@ def run_cuda(args):
         "bf16_comparator": bf16,
         "bulk_append": bulk,
         "extend_attention": ext,
+        "paged_recent": paged,
         "ablation": ablation,
         "calibration_gpu": cal_gpu,
         "setup_s": {"calibration": t_cal, "prefill": t_prefill},
@@ -759,6 +798,7 @@ def main():
     ap.add_argument("--cal-keys", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-paged", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-append", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
