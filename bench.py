@@ -558,6 +558,69 @@ def run_cuda(args):
                                     "is unpacked once into fp16 tiles shared by the block's 16 x G query rows; "
                                     "attention_tflops counts Q.K and P.V over each query's causal prefix")
 
+    # ---- serving batch: 28 concurrent 100,000-token requests in one paged pool
+    # (shuffled pages), the same fused decode step; two layers resident, eager
+    # launches (each moves ~1.6 GB), per-layer time scaled to the 36-layer stack
+    serving = None
+    if rank == 0 and not args.no_batch:
+        Bs, Ls, layers_s, steps_s = 28, CTX0, 2, 12
+        maxp_s = (Ls + steps_s + 63) // 64 + 1
+        sc = kvcache.MixedCache(layers_s, HKV, Bs * maxp_s, Bs, Bs, Bs, maxp_s, device=dev)
+        sc.page_table.copy_(torch.from_numpy(inputs.shuffled_pages(CFG, Bs * maxp_s, layer=7).reshape(Bs, maxp_s)))
+        for layer in range(layers_s):
+            for b0 in range(0, Bs, 7):
+                kv = [inputs.kv_tokens_device(CFG, layer, HKV, inputs.STREAM_KV, Ls, dev, request=b) for b in range(b0, b0 + 7)]
+                ks = torch.cat([x[0] for x in kv])
+                vs = torch.cat([x[1] for x in kv])
+                del kv
+                cu_s = torch.arange(0, 8 * Ls, Ls, dtype=torch.int32, device=dev)
+                p0_s = torch.zeros(7, dtype=torch.int32, device=dev)
+                sv = sc.view(layer)
+                tabs = (sc.page_table[b0:b0 + 7].contiguous(), sc.sink_page[b0:b0 + 7].contiguous(),
+                        sc.ring_slot[b0:b0 + 7].contiguous())
+                sv.page_table, sv.sink_page, sv.ring_slot, sv.batch = (tabs[0].data_ptr(), tabs[1].data_ptr(),
+                                                                       tabs[2].data_ptr(), 7)
+                abi.oscar_kv_append(ctx, layer, sv, kvcache.append_args(ks, vs, p0_s, cu_s, Ls), cur)
+                torch.cuda.synchronize()
+                del ks, vs, tabs
+        assert abi.oscar_check_device_error(ctx) == 0
+        sviews = [sc.view(layer) for layer in range(layers_s)]
+        qs = torch.stack([inputs.decode_queries_bf16(CFG, layer, Bs, HQ) for layer in range(layers_s)]).to(dev)
+        outs = torch.zeros((layers_s, Bs, HQ, D), dtype=torch.float32, device=dev)
+        kns, vns = inputs.kv_tokens_device(CFG, 998, HKV, inputs.STREAM_APPEND, Bs, dev)
+        sws_t, sws, sws_bytes = kvcache.workspace(ctx, Bs, Ls + steps_s + 1, device=dev)
+        pos_s = [torch.full((Bs,), Ls + j, dtype=torch.int32, device=dev) for j in range(steps_s)]
+        len_s = [x + 1 for x in pos_s]
+        sargs = [[(kvcache.append_args(kns, vns, pos_s[j]), kvcache.decode_args(qs[layer], outs[layer], len_s[j],
+                                                                                 Ls + steps_s))
+                  for layer in range(layers_s)] for j in range(steps_s)]
+
+        def sstep(j):
+            for layer in range(layers_s):
+                ap_, dp_ = sargs[j][layer]
+                abi.oscar_decode_step(ctx, layer, sviews[layer], ap_, dp_, sws, sws_bytes, cur)
+        for j in range(3):
+            sstep(j)
+        torch.cuda.synchronize()
+        e0.record()
+        for j in range(3, steps_s):
+            sstep(j)
+        e1.record()
+        torch.cuda.synchronize()
+        assert abi.oscar_check_device_error(ctx) == 0
+        ms_layer = e0.elapsed_time(e1) / ((steps_s - 3) * layers_s)
+        b_layer = algorithmic_bytes_per_layer(Ls + (steps_s + 3) // 2, batch=Bs)
+        hbm_peak = measured_peaks()[0]
+        serving = {"requests": Bs, "context": Ls, "ms_per_layer_step": ms_layer,
+                   "tokens_per_s": Bs * 1000.0 / (N_LAYERS * ms_layer), "layers": N_LAYERS,
+                   "kv_read_gbs": b_layer / (ms_layer / 1e3) / 1e9,
+                   "hbm_frac": b_layer / (ms_layer / 1e3) / 1e9 / hbm_peak,
+                   "note": "Qwen3-4B-shaped serving batch (32 query / 8 KV heads): 28 requests at 100,000 tokens "
+                           "in one shuffled paged pool, oscar_decode_step per layer (append with eviction + "
+                           "decode), per-layer time of two resident layers scaled to 36; algorithmic bytes as "
+                           "for the batch-1 line"}
+        del sc, sws_t, sargs
+
     # ---- paged BF16 recent window: the same one-layer decode step with the last 256
     # positions in BF16 pages (five per request, logical page lp in page lp % 5)
     # instead of the ring, each mode timed as 32 isolated launches behind a GPU-side sleep
@@ -778,6 +841,7 @@ def run_cuda(args):
         "bulk_append": bulk,
         "extend_attention": ext,
         "paged_recent": paged,
+        "serving_batch": serving,
         "ablation": ablation,
         "calibration_gpu": cal_gpu,
         "setup_s": {"calibration": t_cal, "prefill": t_prefill},
@@ -799,6 +863,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-paged", action="store_true")
+    ap.add_argument("--no-batch", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-append", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
