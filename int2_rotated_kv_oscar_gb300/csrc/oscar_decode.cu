@@ -1383,15 +1383,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ extend (chunk) attention
 // The queries of a chunk read the same cached pages, so one block serves one
 // (request, KV head) and 16 of its chunk's queries, one per warp: a page is
-// bulk-copied once, all 512 threads unpack it once into fp16 level tiles in
-// shared memory (K: [64 tokens][128 columns in the decode's MMA order], V:
-// [128 channels][64 tokens], 16-byte chunks XOR-swizzled by row mod 8), and
-// every warp runs its query's Q.K and P.V MMAs from those tiles through
-// ldmatrix, with the decode's q fragments, softmax and state.  Records: per
+// bulk-copied once, the block's 256 threads unpack it once into fp16 level
+// tiles in shared memory (K: [64 tokens][128 columns in the decode's MMA
+// order], V: [128 channels][64 tokens], 16-byte chunks XOR-swizzled by row
+// mod 8), and each of the 8 warps runs the Q.K and P.V MMAs of two queries
+// from those tiles (every ldmatrix'd fragment feeds both), with the decode's
+// q fragments, softmax and state.  Records: per
 // (query, KV head, item) a rotated-basis (INT2) and an original-basis (BF16)
 // state; the last block of each (request, KV head, query group) merges them,
 // applies R_V^T and normalises.
-constexpr int kExtQ = kWarps;  // queries per block
+constexpr int kExtWarps = 8, kExtThreads = 32 * kExtWarps;
+constexpr int kExtQ = 2 * kExtWarps;  // queries per block: two per warp
 constexpr size_t kExtKp = 2 * kBlockBytes;                // after the two raw pages
 constexpr size_t kExtVp = kExtKp + 64 * 128 * 2;
 constexpr size_t kExtSc = kExtVp + 128 * 64 * 2;          // K scales [64][2], V scales [64][2] (float)
@@ -1419,7 +1421,7 @@ struct ExtendArgs {
 
 __device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
-// Unpack one staged INT2 block into the level tiles and scales (thread t of 512).
+// Unpack word t (< 512) of one staged INT2 block into the level tiles, and the scales (t < 64).
 __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint8_t* vp, float* ksc, float* vsc,
                                            int t) {
   const int T = t >> 7, ln = (t >> 2) & 31, wd = t & 3;
@@ -1477,66 +1479,92 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
   }
 }
 
-// One page for one warp's query from the unpacked tiles (g <= 4: the decode's
-// packed fragments and state); rows >= n_valid are not attended.
+// One page for a warp's two queries from the unpacked tiles (g <= 4: the
+// decode's packed fragments and state); rows >= n_valid[i] are not attended
+// by query i (FULL: both see all 64).  Each ldmatrix'd K or V fragment feeds
+// the MMAs of both queries.
 template <bool FULL>
 __device__ __forceinline__ void ext_page(const uint8_t* kp, const uint8_t* vp, const float* ksc, const float* vsc,
-                                         int n_valid, const uint32_t* qf, float scaleE, float kpl, WarpState& st,
-                                         int lane) {
+                                         const int (&n_valid)[2], const uint32_t (&qf)[2][16],
+                                         const float (&scaleE)[2], float kpl, WarpState (&st)[2], int lane) {
   const int q = lane >> 2, l7 = lane & 7, mi = lane >> 3;
-  float lg[4][2];
+  const int nmax = FULL ? kPage : max(n_valid[0], n_valid[1]);
+  float lg[2][4][2];
 #pragma unroll
   for (int T = 0; T < 4; ++T) {
-    if (!FULL && 16 * T >= n_valid) {
-      lg[T][0] = lg[T][1] = -INFINITY;
+    if (!FULL && 16 * T >= nmax) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) lg[i][T][0] = lg[i][T][1] = -INFINITY;
       continue;
     }
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    float d0[2][4] = {}, d1[2][4] = {};
     const int row = 16 * T + l7 + 8 * (mi & 1);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int chunk = 2 * i + (mi >> 1);
+    for (int ks = 0; ks < 8; ++ks) {
+      const int chunk = 2 * ks + (mi >> 1);
       uint32_t a0, a1, a2, a3;
       ldmatrix_x4(a0, a1, a2, a3, kp + row * 256 + ((chunk ^ (row & 7)) << 4));
-      if (i < 4)
-        mma_f16(d0, a0, a1, a2, a3, qf[2 * i], qf[2 * i + 1]);
-      else
-        mma_f16(d1, a0, a1, a2, a3, qf[2 * i], qf[2 * i + 1]);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (ks < 4)
+          mma_f16(d0[i], a0, a1, a2, a3, qf[i][2 * ks], qf[i][2 * ks + 1]);
+        else
+          mma_f16(d1[i], a0, a1, a2, a3, qf[i][2 * ks], qf[i][2 * ks + 1]);
+      }
     }
     const int ra = 16 * T + q, rb = ra + 8;
-    const float lq = fmaf(d0[0] + d0[1], ksc[2 * ra], (d1[0] + d1[1]) * ksc[2 * ra + 1]) * scaleE;
-    const float lq8 = fmaf(d0[2] + d0[3], ksc[2 * rb], (d1[2] + d1[3]) * ksc[2 * rb + 1]) * scaleE;
-    lg[T][0] = (FULL || ra < n_valid) ? lq : -INFINITY;
-    lg[T][1] = (FULL || rb < n_valid) ? lq8 : -INFINITY;
-  }
-  float mx = -INFINITY;
+    const float ka0 = ksc[2 * ra], ka1 = ksc[2 * ra + 1], kb0 = ksc[2 * rb], kb1 = ksc[2 * rb + 1];
 #pragma unroll
-  for (int T = 0; T < 4; ++T) mx = fmaxf(mx, fmaxf(lg[T][0], lg[T][1]));
-  online_max1(st, mx);
-  const float ms = st.m[0] - kpl;
+    for (int i = 0; i < 2; ++i) {
+      const float lq = fmaf(d0[i][0] + d0[i][1], ka0, (d1[i][0] + d1[i][1]) * ka1) * scaleE[i];
+      const float lq8 = fmaf(d0[i][2] + d0[i][3], kb0, (d1[i][2] + d1[i][3]) * kb1) * scaleE[i];
+      lg[i][T][0] = (FULL || ra < n_valid[i]) ? lq : -INFINITY;
+      lg[i][T][1] = (FULL || rb < n_valid[i]) ? lq8 : -INFINITY;
+    }
+  }
+  float ms[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int T = 0; T < 4; ++T) mx = fmaxf(mx, fmaxf(lg[i][T][0], lg[i][T][1]));
+    if (FULL || n_valid[i] > 0) {
+      online_max1(st[i], mx);
+      ms[i] = st[i].m[0] - kpl;
+    } else {
+      ms[i] = 0.f;  // no row of this page for query i: its weights are exactly 0, its state untouched
+    }
+  }
 #pragma unroll
   for (int T = 0; T < 4; ++T) {
-    if (!FULL && 16 * T >= n_valid) continue;
-    const float pq = ex2(lg[T][0] - ms), pq8 = ex2(lg[T][1] - ms);
-    st.l[0] += pq + pq8;
+    if (!FULL && 16 * T >= nmax) continue;
     const int ra = 16 * T + q, rb = ra + 8;
-    const bool va = FULL || ra < n_valid, vb = FULL || rb < n_valid;
-    const float sax = va ? vsc[2 * ra] : 0.f, say = va ? vsc[2 * ra + 1] : 0.f;
-    const float sbx = vb ? vsc[2 * rb] : 0.f, sby = vb ? vsc[2 * rb + 1] : 0.f;
-    const uint32_t b00 = movmatrix_trans(value_residual(pq * sax));
-    const uint32_t b01 = movmatrix_trans(value_residual(pq8 * sbx));
-    const uint32_t b10 = movmatrix_trans(value_residual(pq * say));
-    const uint32_t b11 = movmatrix_trans(value_residual(pq8 * sby));
+    uint32_t bf[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float pq = ex2(lg[i][T][0] - ms[i]), pq8 = ex2(lg[i][T][1] - ms[i]);
+      st[i].l[0] += pq + pq8;
+      const bool va = FULL || ra < n_valid[i], vb = FULL || rb < n_valid[i];
+      const float sax = va ? vsc[2 * ra] : 0.f, say = va ? vsc[2 * ra + 1] : 0.f;
+      const float sbx = vb ? vsc[2 * rb] : 0.f, sby = vb ? vsc[2 * rb + 1] : 0.f;
+      bf[i][0] = movmatrix_trans(value_residual(pq * sax));
+      bf[i][1] = movmatrix_trans(value_residual(pq8 * sbx));
+      bf[i][2] = movmatrix_trans(value_residual(pq * say));
+      bf[i][3] = movmatrix_trans(value_residual(pq8 * sby));
+    }
     const int chunk = 2 * T + (mi >> 1);
 #pragma unroll
     for (int M = 0; M < 8; ++M) {
       const int row = 16 * M + l7 + 8 * (mi & 1);
       uint32_t a0, a1, a2, a3;
       ldmatrix_x4(a0, a1, a2, a3, vp + row * 128 + ((chunk ^ (row & 7)) << 4));
-      if (M < 4)
-        mma_f16(st.acc[M], a0, a1, a2, a3, b00, b01);
-      else
-        mma_f16(st.acc[M], a0, a1, a2, a3, b10, b11);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (M < 4)
+          mma_f16(st[i].acc[M], a0, a1, a2, a3, bf[i][0], bf[i][1]);
+        else
+          mma_f16(st[i].acc[M], a0, a1, a2, a3, bf[i][2], bf[i][3]);
+      }
     }
   }
 }
@@ -1547,59 +1575,57 @@ __device__ __forceinline__ void ext_page(const uint8_t* kp, const uint8_t* vp, c
 __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* smem, int b, int h, int grp, int z) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   float* rvt = reinterpret_cast<float*>(smem);
-  for (int e = t; e < 128 * 128 / 4; e += kThreads)
+  for (int e = t; e < 128 * 128 / 4; e += kExtThreads)
     reinterpret_cast<float4*>(rvt)[e] = __ldg(reinterpret_cast<const float4*>(a.R_VT) + e);
   __syncthreads();
   if (t == 0) a.counters[z * a.Hkv + h] = 0;  // ready for the next launch on this workspace
-  const int qi = grp * kExtQ + warp;
-  if (qi >= a.chunk) return;
-  const int qg = b * a.chunk + qi;
-  for (int n = 0; n < a.g; ++n) {
-    float Mr = -INFINITY, Lr = 0.f, Mp = -INFINITY, Lp = 0.f;
-    float4 yr = make_float4(0.f, 0.f, 0.f, 0.f), yp = yr;
-    for (int x = 0; x < a.n_items; ++x) {
-      const float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + x) * 2 * kPartialFloats;
-      merge_record(Mr, Lr, yr, __ldcg(rec + n), __ldcg(rec + 8 + n),
-                   __ldcg(reinterpret_cast<const float4*>(rec + 16 + n * kStateStride) + lane));
-      const float* rp = rec + kPartialFloats;
-      merge_record(Mp, Lp, yp, __ldcg(rp + n), __ldcg(rp + 8 + n),
-                   __ldcg(reinterpret_cast<const float4*>(rp + 16 + n * kStateStride) + lane));
-    }
-    // y R_V^T: lane holds channels 4 lane .. + 3 of y and computes outputs 4 lane .. + 3
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < 32; ++s) {
-      const float y[4] = {__shfl_sync(0xffffffffu, yr.x, s), __shfl_sync(0xffffffffu, yr.y, s),
-                          __shfl_sync(0xffffffffu, yr.z, s), __shfl_sync(0xffffffffu, yr.w, s)};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 r = reinterpret_cast<const float4*>(rvt + (4 * s + c) * 128)[lane];
-        o.x = fmaf(y[c], r.x, o.x);
-        o.y = fmaf(y[c], r.y, o.y);
-        o.z = fmaf(y[c], r.z, o.z);
-        o.w = fmaf(y[c], r.w, o.w);
+  for (int jq = 0; jq < 2; ++jq) {  // this warp's two queries
+    const int qi = grp * kExtQ + 2 * warp + jq;
+    if (qi >= a.chunk) return;
+    const int qg = b * a.chunk + qi;
+    for (int n = 0; n < a.g; ++n) {
+      float Mr = -INFINITY, Lr = 0.f, Mp = -INFINITY, Lp = 0.f;
+      float4 yr = make_float4(0.f, 0.f, 0.f, 0.f), yp = yr;
+      for (int x = 0; x < a.n_items; ++x) {
+        const float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + x) * 2 * kPartialFloats;
+        merge_record(Mr, Lr, yr, __ldcg(rec + n), __ldcg(rec + 8 + n),
+                     __ldcg(reinterpret_cast<const float4*>(rec + 16 + n * kStateStride) + lane));
+        const float* rp = rec + kPartialFloats;
+        merge_record(Mp, Lp, yp, __ldcg(rp + n), __ldcg(rp + 8 + n),
+                     __ldcg(reinterpret_cast<const float4*>(rp + 16 + n * kStateStride) + lane));
       }
+      // y R_V^T: lane holds channels 4 lane .. + 3 of y and computes outputs 4 lane .. + 3
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < 32; ++s) {
+        const float y[4] = {__shfl_sync(0xffffffffu, yr.x, s), __shfl_sync(0xffffffffu, yr.y, s),
+                            __shfl_sync(0xffffffffu, yr.z, s), __shfl_sync(0xffffffffu, yr.w, s)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 r = reinterpret_cast<const float4*>(rvt + (4 * s + c) * 128)[lane];
+          o.x = fmaf(y[c], r.x, o.x);
+          o.y = fmaf(y[c], r.y, o.y);
+          o.z = fmaf(y[c], r.z, o.z);
+          o.w = fmaf(y[c], r.w, o.w);
+        }
+      }
+      const float M = fmaxf(Mr, Mp);
+      float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+        const float fr = ex2(Mr - M), fp = ex2(Mp - M);
+        const float inv_l = 1.0f / (fr * Lr + fp * Lp);
+        res = make_float4((fr * o.x + fp * yp.x) * inv_l, (fr * o.y + fp * yp.y) * inv_l,
+                          (fr * o.z + fp * yp.z) * inv_l, (fr * o.w + fp * yp.w) * inv_l);
+      }
+      *reinterpret_cast<float4*>(a.out + ((size_t)qg * a.Hq + h * a.g + n) * kD + 4 * lane) = res;
     }
-    const float M = fmaxf(Mr, Mp);
-    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-      const float fr = ex2(Mr - M), fp = ex2(Mp - M);
-      const float inv_l = 1.0f / (fr * Lr + fp * Lp);
-      res = make_float4((fr * o.x + fp * yp.x) * inv_l, (fr * o.y + fp * yp.y) * inv_l,
-                        (fr * o.z + fp * yp.z) * inv_l, (fr * o.w + fp * yp.w) * inv_l);
-    }
-    *reinterpret_cast<float4*>(a.out + ((size_t)qg * a.Hq + h * a.g + n) * kD + 4 * lane) = res;
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_constant__ ExtendArgs a) {
+__global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const __grid_constant__ ExtendArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int item = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const int b = z / a.ngpr, grp = z % a.ngpr;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int qi = grp * kExtQ + warp;
-  const bool active = qi < a.chunk;
-  const int qg = b * a.chunk + (active ? qi : 0);
-  const int bq = qg * a.Hkv + h;
   const CacheRefs& c = a.c;
   uint8_t* kp = smem + kExtKp;
   uint8_t* vp = smem + kExtVp;
@@ -1617,7 +1643,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
     if (t == 0 && item == 0) set_error(a.err, kErrLength);
     L = 0;
   }
-  const int lim = active ? max(0, min(a.pos0[b] + qi + 1, L)) : 0;
   const int hist_end = max(kSink, L - kRecent);
   const int n_hist = (hist_end + kPage - 1) / kPage - 1;
   if (n_hist + 1 > c.max_pages && t == 0 && item == 0) set_error(a.err, kErrLength);
@@ -1625,28 +1650,34 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
   const int lp0 = 1 + item * a.chunk_pages;
   const int lp1 = max(lp0, min(lp0 + a.chunk_pages, 1 + n_hist_ok));
   const int n_units = lp1 - lp0;
-  const int hlim = min(hist_end, lim);
-
-  uint32_t qf[16], qpf[16];
-  float scaleE = 0.f, scaleEp = 0.f;
-  if (active) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bq * kQFragWords + lane * 32);
-    const uint4* srcp = reinterpret_cast<const uint4*>(a.qplain + (size_t)bq * kQFragWords + lane * 32);
+  // this warp's two queries: chunk indices 2 warp, 2 warp + 1 of the group, causal limits
+  bool active[2];
+  int qg[2], lim[2], hlim[2];
+  uint32_t qf[2][16];
+  float scaleE[2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 u = __ldg(src + (k ^ (lane & 7)));
-      const uint4 v = __ldg(srcp + (k ^ (lane & 7)));
-      qf[4 * k] = u.x;
-      qf[4 * k + 1] = u.y;
-      qf[4 * k + 2] = u.z;
-      qf[4 * k + 3] = u.w;
-      qpf[4 * k] = v.x;
-      qpf[4 * k + 1] = v.y;
-      qpf[4 * k + 2] = v.z;
-      qpf[4 * k + 3] = v.w;
+  for (int jq = 0; jq < 2; ++jq) {
+    const int qi = grp * kExtQ + 2 * warp + jq;
+    active[jq] = qi < a.chunk;
+    qg[jq] = b * a.chunk + (active[jq] ? qi : 0);
+    lim[jq] = active[jq] ? max(0, min(a.pos0[b] + qi + 1, L)) : 0;
+    hlim[jq] = min(hist_end, lim[jq]);
+    scaleE[jq] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) qf[jq][k] = 0u;
+    if (active[jq]) {
+      const int bq = qg[jq] * a.Hkv + h;
+      const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bq * kQFragWords + lane * 32);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 u = __ldg(src + (k ^ (lane & 7)));
+        qf[jq][4 * k] = u.x;
+        qf[jq][4 * k + 1] = u.y;
+        qf[jq][4 * k + 2] = u.z;
+        qf[jq][4 * k + 3] = u.w;
+      }
+      scaleE[jq] = __ldg(a.qconst + (size_t)bq * kQConstFloats + 16);
     }
-    scaleE = __ldg(a.qconst + (size_t)bq * kQConstFloats + 16);
-    scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
   }
   // copies of this item's pages, two in flight
   auto issue = [&](int k) {  // thread 0
@@ -1666,11 +1697,25 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
     fence_proxy_async_smem();
     for (int k = 0; k < min(2, n_units); ++k) issue(k);
   }
-  WarpState st;
-  float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats;
-  // BF16 sink/recent tiles of this item, each warp for its query (original basis)
-  state_init(st);
-  if (active) {
+  // BF16 sink/recent tiles of this item, for each of the warp's queries (original basis)
+  for (int jq = 0; jq < 2; ++jq) {
+    if (!active[jq]) continue;
+    const int bq = qg[jq] * a.Hkv + h;
+    uint32_t qpf[16];
+    {
+      const uint4* srcp = reinterpret_cast<const uint4*>(a.qplain + (size_t)bq * kQFragWords + lane * 32);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = __ldg(srcp + (k ^ (lane & 7)));
+        qpf[4 * k] = v.x;
+        qpf[4 * k + 1] = v.y;
+        qpf[4 * k + 2] = v.z;
+        qpf[4 * k + 3] = v.w;
+      }
+    }
+    const float scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
+    WarpState sb;
+    state_init(sb);
     const int sp = c.sink_page[b];
     const bool sink_ok = sp >= 0 && sp < c.num_sink;
     for (int k = 0; k < a.tiles_per_item; ++k) {
@@ -1693,23 +1738,27 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
       }
       uint32_t rows = (1u << nv) - 1u;
       if (!ring) {
-        rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
+        rows &= (1u << max(0, min(16, lim[jq] - (int)row_off))) - 1u;
       } else {
         for (int r = 0; r < nv; ++r) {
           const int rr = (int)row_off + r;
           const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
-          if (p >= lim) rows &= ~(1u << r);
+          if (p >= lim[jq]) rows &= ~(1u << r);
         }
       }
       if (rows == 0) continue;
       const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
       const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
-      bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, st, lane);
+      bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, sb, lane);
     }
-    store_state<true>(st, rec + kPartialFloats, 1.0f / kPScaleBF16, lane);
+    store_state<true>(sb, a.partials + (((size_t)qg[jq] * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats +
+                              kPartialFloats,
+                      1.0f / kPScaleBF16, lane);
   }
   // INT2 history pages (rotated basis), unpacked once per block
-  state_init(st);
+  WarpState st[2];
+  state_init(st[0]);
+  state_init(st[1]);
   const float kpl = log2f(a.pscale);
   int k = 0;
   for (; k < n_units; ++k) {
@@ -1720,24 +1769,30 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const __grid_consta
       break;
     }
     ext_unpack(smem + (size_t)s * kBlockBytes, kp, vp, ksc, vsc, t);
+    ext_unpack(smem + (size_t)s * kBlockBytes, kp, vp, ksc, vsc, t + kExtThreads);
     __syncthreads();  // tiles ready; raw stage s free
     if (t == 0 && k + 2 < n_units) {
       fence_proxy_async_smem();
       issue(k + 2);
     }
     const int lp = lp0 + k;
-    const int n_valid = min(kPage, hlim - kPage * lp);
+    const int nv[2] = {active[0] ? min(kPage, hlim[0] - kPage * lp) : 0,
+                       active[1] ? min(kPage, hlim[1] - kPage * lp) : 0};
     const int ph = c.page_table[(size_t)b * c.max_pages + lp];
-    if (active && n_valid > 0 && ph >= 0 && ph < c.num_pages) {
-      if (n_valid == kPage)
-        ext_page<true>(kp, vp, ksc, vsc, n_valid, qf, scaleE, kpl, st, lane);
+    if ((nv[0] > 0 || nv[1] > 0) && ph >= 0 && ph < c.num_pages) {
+      if (nv[0] == kPage && nv[1] == kPage)
+        ext_page<true>(kp, vp, ksc, vsc, nv, qf, scaleE, kpl, st, lane);
       else
-        ext_page<false>(kp, vp, ksc, vsc, n_valid, qf, scaleE, kpl, st, lane);
+        ext_page<false>(kp, vp, ksc, vsc, nv, qf, scaleE, kpl, st, lane);
     }
   }
   // after a timeout, wait (bounded) for the copies still in flight
   for (int kk = k; kk < min(k + 2, n_units); ++kk) mbar_wait_bounded(&bars[kk & 1], (kk >> 1) & 1, kWaitLimit);
-  if (active) store_state<true>(st, rec, a.inv_pscale, lane);
+#pragma unroll
+  for (int jq = 0; jq < 2; ++jq)
+    if (active[jq])
+      store_state<true>(st[jq], a.partials + (((size_t)qg[jq] * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats,
+                        a.inv_pscale, lane);
   griddep_launch_dependents();
   __shared__ int s_last;
   __syncthreads();
@@ -1997,7 +2052,7 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   }
   void* args[] = {&a};
   return launch_pdl(reinterpret_cast<const void*>(extend_kernel), dim3(p.n_items, p.Hkv, p.batch * p.ngpr),
-                    dim3(kThreads), kExtSmem, stream, args);
+                    dim3(kExtThreads), kExtSmem, stream, args);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {

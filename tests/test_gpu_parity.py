@@ -270,6 +270,15 @@ def test_host_argument_errors_launch_nothing():
         assert e.value.status == 1
         with pytest.raises(abi.OscarError):
             abi.oscar_load_rotation(s.ctx, 0, np.eye(128), np.eye(128), 1e6, 1.0)
+        # k, v must be 16-byte aligned (the bulk append reads them by TMA)
+        kv = torch.zeros((2 * 100 * 2 * 128 + 8,), dtype=torch.bfloat16, device="cuda")
+        k_bad = kv[1:1 + 100 * 2 * 128].view(100, 2, 128)
+        pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+        cu = torch.tensor([0, 100], dtype=torch.int32, device="cuda")
+        with pytest.raises(abi.OscarError) as e:
+            abi.oscar_kv_append(s.ctx, 0, v, kvcache.append_args(k_bad, k_bad, pos, cu, 100), None)
+        assert e.value.status == 1
+        assert s.device_error() == 0
     finally:
         s.close()
 
