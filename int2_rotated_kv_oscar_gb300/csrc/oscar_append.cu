@@ -369,7 +369,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float* pmax = reinterpret_cast<float*>(sm + kTcPmax);
     for (int it = 0;;) {
       const int di = it % kTcDescs;
-      if (!mbar_wait_bounded(&dfull[di], (it / kTcDescs) & 1, kWaitLimit)) {
+      // waits are warp-uniform: the TMEM loads below are warp-wide (.sync.aligned)
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&dfull[di], (it / kTcDescs) & 1, kWaitLimit))) {
         set_error(a.err, kErrTimeout);
         break;
       }
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive(&dempty[di]);
       if (b < 0) break;
       const int bb = it & 1, k = 2 * g + bb;
-      if (!mbar_wait_bounded(&tfull[k], (it >> 1) & 1, kWaitLimit)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[k], (it >> 1) & 1, kWaitLimit))) {
         set_error(a.err, kErrTimeout);
         break;
       }
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float* pm = pmax + (((bb * 2 + h) * 2 + g) * 128);
       pm[row] = mx;
       mbar_arrive(&xb[4 * g + q]);
-      if (!mbar_wait_bounded(&xb[4 * g + q], (it & 1), kWaitLimit)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&xb[4 * g + q], (it & 1), kWaitLimit))) {
         set_error(a.err, kErrTimeout);
         break;
       }

@@ -1381,32 +1381,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ extend (chunk) attention
-// The queries of a chunk read the same cached pages, so one block serves one
-// (request, KV head) and 16 of its chunk's queries, one per warp: a page is
-// bulk-copied once, the block's 256 threads unpack it once into fp16 level
-// tiles in shared memory (K: [64 tokens][128 columns in the decode's MMA
-// order], V: [128 channels][64 tokens], 16-byte chunks XOR-swizzled by row
-// mod 8), and each of the 8 warps runs the Q.K and P.V MMAs of two queries
-// from those tiles (every ldmatrix'd fragment feeds both), with the decode's
-// q fragments, softmax and state.  Records: per
-// (query, KV head, item) a rotated-basis (INT2) and an original-basis (BF16)
-// state; the last block of each (request, KV head, query group) merges them,
-// applies R_V^T and normalises.
-constexpr int kExtWarps = 8, kExtThreads = 32 * kExtWarps;
-constexpr int kExtQ = 2 * kExtWarps;  // queries per block: two per warp
-constexpr size_t kExtKp = 2 * kBlockBytes;                // after the two raw pages
-constexpr size_t kExtVp = kExtKp + 64 * 128 * 2;
-constexpr size_t kExtSc = kExtVp + 128 * 64 * 2;          // K scales [64][2], V scales [64][2] (float)
-constexpr size_t kExtRv = 128 * 128 * 4;                  // the final merge stages R_V^T over the tiles
-constexpr size_t kExtBars = kExtRv;                        // the two stage barriers, past it
-constexpr size_t kExtSmem = kExtBars + 16;
-static_assert(kExtSc + 2 * 64 * 2 * 4 <= kExtRv, "extend staging");
-
+// The queries of a chunk read the same cached pages: one block serves one
+// (page range, KV head, group of queries) and unpacks each page once for the
+// whole group (the kernel below).  Records: per (query, KV head, item) a
+// rotated-basis (INT2) and an original-basis (BF16) state; the last block of
+// each (request, KV head, query group) merges them, applies R_V^T and
+// normalises.
 struct ExtendArgs {
   CacheRefs c;
   const int32_t* ctx_len;  // [B] cache lengths
   const int32_t* pos0;     // [B] chunk start positions
-  int chunk, ngpr, Hq, Hkv, g;
+  int chunk, ngpr, qpg, Hq, Hkv, g;  // qpg: queries per group (one block per group, item and KV head)
   int n_items, chunk_pages, tiles_per_item;
   const uint32_t* qfrag;
   const uint32_t* qplain;
@@ -1422,6 +1407,9 @@ struct ExtendArgs {
 __device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
 // Unpack word t (< 512) of one staged INT2 block into the level tiles, and the scales (t < 64).
+// TC: the tiles are tcgen05 operands in the 128-byte swizzle -- K as [2 blocks of 64 channels]
+// [64 tokens][64 channels] (channels in the decode's MMA order), V as [128 channels][64 tokens].
+template <bool TC = false>
 __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint8_t* vp, float* ksc, float* vsc,
                                            int t) {
   const int T = t >> 7, ln = (t >> 2) & 31, wd = t & 3;
@@ -1437,7 +1425,9 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
     constexpr int bb = (R) >> 2, p = (R)&3;                                                             \
     const int ks = 2 * kpar + (p >> 1), kh = p & 1;                                                     \
     const int col = 16 * (4 * (ks >> 1) + 2 * bb + (ks & 1)) + 8 * kh + 2 * tq;                         \
-    st_shared_u32(base + ((((col >> 3) ^ (row & 7))) << 4) + 2 * (col & 7), code_level<R>(cw));         \
+    st_shared_u32(TC ? kp + (col >> 6) * 8192 + sw128_elem(row, col & 63)                               \
+                     : base + ((((col >> 3) ^ (row & 7))) << 4) + 2 * (col & 7),                        \
+                  code_level<R>(cw));                                                                   \
   } while (0)
     OSCAR_EXT_K(0);
     OSCAR_EXT_K(1);
@@ -1457,7 +1447,8 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
 #define OSCAR_EXT_V(R)                                                                                  \
   do {                                                                                                  \
     const int j = 16 * (R) + jm;                                                                        \
-    st_shared_u32(vp + j * 128 + ((((col >> 3) ^ (j & 7))) << 4) + 2 * (col & 7), code_level<R>(cw));   \
+    st_shared_u32(TC ? vp + sw128_elem(j, col) : vp + j * 128 + ((((col >> 3) ^ (j & 7))) << 4) + 2 * (col & 7), \
+                  code_level<R>(cw));                                                                   \
   } while (0)
     OSCAR_EXT_V(0);
     OSCAR_EXT_V(1);
@@ -1479,108 +1470,18 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
   }
 }
 
-// One page for a warp's two queries from the unpacked tiles (g <= 4: the
-// decode's packed fragments and state); rows >= n_valid[i] are not attended
-// by query i (FULL: both see all 64).  Each ldmatrix'd K or V fragment feeds
-// the MMAs of both queries.
-template <bool FULL>
-__device__ __forceinline__ void ext_page(const uint8_t* kp, const uint8_t* vp, const float* ksc, const float* vsc,
-                                         const int (&n_valid)[2], const uint32_t (&qf)[2][16],
-                                         const float (&scaleE)[2], float kpl, WarpState (&st)[2], int lane) {
-  const int q = lane >> 2, l7 = lane & 7, mi = lane >> 3;
-  const int nmax = FULL ? kPage : max(n_valid[0], n_valid[1]);
-  float lg[2][4][2];
-#pragma unroll
-  for (int T = 0; T < 4; ++T) {
-    if (!FULL && 16 * T >= nmax) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) lg[i][T][0] = lg[i][T][1] = -INFINITY;
-      continue;
-    }
-    float d0[2][4] = {}, d1[2][4] = {};
-    const int row = 16 * T + l7 + 8 * (mi & 1);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int chunk = 2 * ks + (mi >> 1);
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4(a0, a1, a2, a3, kp + row * 256 + ((chunk ^ (row & 7)) << 4));
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (ks < 4)
-          mma_f16(d0[i], a0, a1, a2, a3, qf[i][2 * ks], qf[i][2 * ks + 1]);
-        else
-          mma_f16(d1[i], a0, a1, a2, a3, qf[i][2 * ks], qf[i][2 * ks + 1]);
-      }
-    }
-    const int ra = 16 * T + q, rb = ra + 8;
-    const float ka0 = ksc[2 * ra], ka1 = ksc[2 * ra + 1], kb0 = ksc[2 * rb], kb1 = ksc[2 * rb + 1];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float lq = fmaf(d0[i][0] + d0[i][1], ka0, (d1[i][0] + d1[i][1]) * ka1) * scaleE[i];
-      const float lq8 = fmaf(d0[i][2] + d0[i][3], kb0, (d1[i][2] + d1[i][3]) * kb1) * scaleE[i];
-      lg[i][T][0] = (FULL || ra < n_valid[i]) ? lq : -INFINITY;
-      lg[i][T][1] = (FULL || rb < n_valid[i]) ? lq8 : -INFINITY;
-    }
-  }
-  float ms[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int T = 0; T < 4; ++T) mx = fmaxf(mx, fmaxf(lg[i][T][0], lg[i][T][1]));
-    if (FULL || n_valid[i] > 0) {
-      online_max1(st[i], mx);
-      ms[i] = st[i].m[0] - kpl;
-    } else {
-      ms[i] = 0.f;  // no row of this page for query i: its weights are exactly 0, its state untouched
-    }
-  }
-#pragma unroll
-  for (int T = 0; T < 4; ++T) {
-    if (!FULL && 16 * T >= nmax) continue;
-    const int ra = 16 * T + q, rb = ra + 8;
-    uint32_t bf[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float pq = ex2(lg[i][T][0] - ms[i]), pq8 = ex2(lg[i][T][1] - ms[i]);
-      st[i].l[0] += pq + pq8;
-      const bool va = FULL || ra < n_valid[i], vb = FULL || rb < n_valid[i];
-      const float sax = va ? vsc[2 * ra] : 0.f, say = va ? vsc[2 * ra + 1] : 0.f;
-      const float sbx = vb ? vsc[2 * rb] : 0.f, sby = vb ? vsc[2 * rb + 1] : 0.f;
-      bf[i][0] = movmatrix_trans(value_residual(pq * sax));
-      bf[i][1] = movmatrix_trans(value_residual(pq8 * sbx));
-      bf[i][2] = movmatrix_trans(value_residual(pq * say));
-      bf[i][3] = movmatrix_trans(value_residual(pq8 * sby));
-    }
-    const int chunk = 2 * T + (mi >> 1);
-#pragma unroll
-    for (int M = 0; M < 8; ++M) {
-      const int row = 16 * M + l7 + 8 * (mi & 1);
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4(a0, a1, a2, a3, vp + row * 128 + ((chunk ^ (row & 7)) << 4));
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (M < 4)
-          mma_f16(st[i].acc[M], a0, a1, a2, a3, bf[i][0], bf[i][1]);
-        else
-          mma_f16(st[i].acc[M], a0, a1, a2, a3, bf[i][2], bf[i][3]);
-      }
-    }
-  }
-}
-
 // The last block of a (request, KV head, query group): warp w merges the
-// records of its query per head, applies R_V^T (staged in shared memory) to
+// records of queries w, w + warps, ... of the group per head, applies R_V^T (staged in shared memory) to
 // the rotated-basis part, joins the original-basis part and normalises.
 __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* smem, int b, int h, int grp, int z) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   float* rvt = reinterpret_cast<float*>(smem);
-  for (int e = t; e < 128 * 128 / 4; e += kExtThreads)
+  for (int e = t; e < 128 * 128 / 4; e += blockDim.x)
     reinterpret_cast<float4*>(rvt)[e] = __ldg(reinterpret_cast<const float4*>(a.R_VT) + e);
   __syncthreads();
   if (t == 0) a.counters[z * a.Hkv + h] = 0;  // ready for the next launch on this workspace
-  for (int jq = 0; jq < 2; ++jq) {  // this warp's two queries
-    const int qi = grp * kExtQ + 2 * warp + jq;
+  for (int ql = warp; ql < a.qpg; ql += blockDim.x >> 5) {
+    const int qi = grp * a.qpg + ql;
     if (qi >= a.chunk) return;
     const int qg = b * a.chunk + qi;
     for (int n = 0; n < a.g; ++n) {
@@ -1621,22 +1522,69 @@ __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* sm
   }
 }
 
-__global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const __grid_constant__ ExtendArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+// ---------------------------------------------------------------- extend attention on tcgen05
+// One block per (item = page range, KV head, group of 128 / g queries): the
+// group's (query, head) pairs are the 128 rows of every MMA (TMEM lane =
+// row).  Per INT2 page: S = Q'_value K^T + Q'_residual K^T for each 64-channel
+// group (f16 MMAs from the 128-byte-swizzled tiles into TMEM), one softmax
+// thread per row (its query's causal limit, lazy rescaling of its O row in
+// TMEM), P s_v as fp16 value + residual operands, O += P V (V transposed).
+// S of the next page overlaps the softmax of this one.  Warps:
+//   0-3  softmax; at the end the rows' rotated-basis records
+//   4-7  the q' operands (from the prep's fragments), the BF16 sink/recent
+//        tiles (per query, mma.sync, original-basis records), then the pages:
+//        bulk copies (thread 128) and the unpack into double-buffered tiles
+//   8    TMEM (256 columns: S, then O) and the MMA thread
+constexpr int kXtThreads = 9 * 32;
+constexpr unsigned kXtWaitLimit = 1u << 18;  // polls per wait: a broken hand-off ends in well under a second
+constexpr uint32_t kXtQ = 0;             // q' value / residual: 2 x [2 blocks of 64 channels][128 rows][128 B]
+constexpr uint32_t kXtP = 65536;         // P s_v: [group][value, residual][128 rows][64 tokens] (4 x 16 KB)
+constexpr uint32_t kXtK = 131072;        // K tiles: 2 x [2 blocks of 64 channels][64 tokens][128 B]
+constexpr uint32_t kXtV = 163840;        // V^T tiles: 2 x [128 channels][64 tokens]
+constexpr uint32_t kXtRaw = 196608;      // raw pages: 2 x 4608
+constexpr uint32_t kXtSc = kXtRaw + 2 * kBlockBytes;  // scales: 2 x [K 64 x 2, V 64 x 2] float
+constexpr uint32_t kXtBars = kXtSc + 2 * 1024;
+constexpr size_t kXtSmem = kXtBars + 256 + 1024;  // + 1024-byte alignment slack
+static_assert(kXtSc + 2 * 1024 <= kXtBars && kXtRaw == kXtV + 2 * 16384, "extend staging");
+
+__global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendArgs a) {
+  extern __shared__ uint8_t xt_raw[];
+  const uint32_t raw_s = smem_u32(xt_raw);
+  uint8_t* sm = xt_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  const uint32_t sbase = smem_u32(sm);
   const int item = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const int b = z / a.ngpr, grp = z % a.ngpr;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const CacheRefs& c = a.c;
-  uint8_t* kp = smem + kExtKp;
-  uint8_t* vp = smem + kExtVp;
-  float* ksc = reinterpret_cast<float*>(smem + kExtSc);
-  float* vsc = ksc + 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kExtBars);
+  const int g = a.g, qpg = a.qpg;
+  uint64_t* rawf = reinterpret_cast<uint64_t*>(sm + kXtBars);  // [2] raw page landed (tx)
+  uint64_t* rawe = rawf + 2;    // [2] raw stage read by the 128 unpack threads
+  uint64_t* tfull = rawf + 4;   // [2] tiles of buffer s unpacked (128)
+  uint64_t* tempty = rawf + 6;  // [2] tiles of buffer s read by their MMAs (commit)
+  uint64_t* sfull = rawf + 8;   // S in TMEM (commit)
+  uint64_t* sfree = rawf + 9;   // S read by the 128 softmax threads
+  uint64_t* pfull = rawf + 10;  // P written, O rescaled (128)
+  uint64_t* pvdone = rawf + 11; // P V finished (commit)
+  uint64_t* done = rawf + 12;   // every MMA finished (commit)
+  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(rawf + 13);
   if (t == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&rawf[i], 1);
+      mbar_init(&rawe[i], 128);
+      mbar_init(&tfull[i], 128);
+      mbar_init(&tempty[i], 1);
+    }
+    mbar_init(sfull, 1);
+    mbar_init(sfree, 128);
+    mbar_init(pfull, 128);
+    mbar_init(pvdone, 1);
+    mbar_init(done, 1);
     fence_mbar_init();
   }
+  for (int i = t; i < 65536 / 16; i += kXtThreads)  // q' operands: rows without a query stay zero
+    reinterpret_cast<uint4*>(sm + kXtQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();  // the tensor core reads them
+  if (warp == 8) tmem_alloc(tmem_at, 256);
   griddep_wait();
   int L = a.ctx_len[b];
   if (L < 0) {
@@ -1650,152 +1598,325 @@ __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const __grid_con
   const int lp0 = 1 + item * a.chunk_pages;
   const int lp1 = max(lp0, min(lp0 + a.chunk_pages, 1 + n_hist_ok));
   const int n_units = lp1 - lp0;
-  // this warp's two queries: chunk indices 2 warp, 2 warp + 1 of the group, causal limits
-  bool active[2];
-  int qg[2], lim[2], hlim[2];
-  uint32_t qf[2][16];
-  float scaleE[2];
-#pragma unroll
-  for (int jq = 0; jq < 2; ++jq) {
-    const int qi = grp * kExtQ + 2 * warp + jq;
-    active[jq] = qi < a.chunk;
-    qg[jq] = b * a.chunk + (active[jq] ? qi : 0);
-    lim[jq] = active[jq] ? max(0, min(a.pos0[b] + qi + 1, L)) : 0;
-    hlim[jq] = min(hist_end, lim[jq]);
-    scaleE[jq] = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) qf[jq][k] = 0u;
-    if (active[jq]) {
-      const int bq = qg[jq] * a.Hkv + h;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_at;
+
+  if (warp >= 4 && warp < 8) {
+    const int u = t - 128, w4 = warp - 4;
+    auto issue = [&](int k) {  // thread u = 0: page k into raw stage k % 2
+      const int st = k & 1;
+      const int ph = c.page_table[(size_t)b * c.max_pages + lp0 + k];
+      if (ph < 0 || ph >= c.num_pages) {
+        set_error(a.err, kErrPage);
+        mbar_arrive(&rawf[st]);
+        return;
+      }
+      mbar_arrive_expect_tx(&rawf[st], kBlockBytes);
+      bulk_copy_g2s(sm + kXtRaw + st * kBlockBytes, c.pages + ((size_t)ph * a.Hkv + h) * kBlockBytes, kBlockBytes,
+                    &rawf[st]);
+    };
+    if (u == 0) {
+      fence_proxy_async_smem();
+      for (int k = 0; k < min(2, n_units); ++k) issue(k);
+    }
+    // q' rows: query ql of the group, head n, part p (value / residual) -> operand p, row ql g + n,
+    // virtual channel 16 i + 8 bs + 2 tig (+1) for the word (i, bs) of lane 4 (2 n + p) + tig
+    for (int ql = w4; ql < qpg; ql += 4) {
+      const int qi = grp * qpg + ql;
+      if (qi >= a.chunk) continue;
+      const int bq = (b * a.chunk + qi) * a.Hkv + h;
+      const int col = lane >> 2, tig = lane & 3, n = col >> 1, part = col & 1;
+      if (n >= g) continue;
       const uint4* src = reinterpret_cast<const uint4*>(a.qfrag + (size_t)bq * kQFragWords + lane * 32);
+      const int row = ql * g + n;
+      uint8_t* dst = sm + kXtQ + part * 32768;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 u = __ldg(src + (k ^ (lane & 7)));
-        qf[jq][4 * k] = u.x;
-        qf[jq][4 * k + 1] = u.y;
-        qf[jq][4 * k + 2] = u.z;
-        qf[jq][4 * k + 3] = u.w;
-      }
-      scaleE[jq] = __ldg(a.qconst + (size_t)bq * kQConstFloats + 16);
-    }
-  }
-  // copies of this item's pages, two in flight
-  auto issue = [&](int k) {  // thread 0
-    const int s = k & 1;
-    const int ph = c.page_table[(size_t)b * c.max_pages + lp0 + k];
-    if (ph < 0 || ph >= c.num_pages) {
-      set_error(a.err, kErrPage);
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&bars[s])) : "memory");
-      return;
-    }
-    mbar_arrive_expect_tx(&bars[s], kBlockBytes);
-    bulk_copy_g2s(smem + (size_t)s * kBlockBytes, c.pages + ((size_t)ph * a.Hkv + h) * kBlockBytes, kBlockBytes,
-                  &bars[s]);
-  };
-  __syncthreads();  // barriers initialised
-  if (t == 0) {
-    fence_proxy_async_smem();
-    for (int k = 0; k < min(2, n_units); ++k) issue(k);
-  }
-  // BF16 sink/recent tiles of this item, for each of the warp's queries (original basis)
-  for (int jq = 0; jq < 2; ++jq) {
-    if (!active[jq]) continue;
-    const int bq = qg[jq] * a.Hkv + h;
-    uint32_t qpf[16];
-    {
-      const uint4* srcp = reinterpret_cast<const uint4*>(a.qplain + (size_t)bq * kQFragWords + lane * 32);
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint4 v = __ldg(src + (kk ^ (lane & 7)));
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = __ldg(srcp + (k ^ (lane & 7)));
-        qpf[4 * k] = v.x;
-        qpf[4 * k + 1] = v.y;
-        qpf[4 * k + 2] = v.z;
-        qpf[4 * k + 3] = v.w;
+        for (int x = 0; x < 4; ++x) {
+          const int wi = 4 * kk + x, i = wi >> 1, bs = wi & 1;
+          const int vc = 16 * i + 8 * bs + 2 * tig;
+          st_shared_u32(dst + (vc >> 6) * 16384 + sw128_elem(row, vc & 63), wv[x]);
+        }
       }
     }
-    const float scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
-    WarpState sb;
-    state_init(sb);
+    // BF16 sink/recent tiles of this item, per query (original basis, mma.sync)
     const int sp = c.sink_page[b];
     const bool sink_ok = sp >= 0 && sp < c.num_sink;
-    for (int k = 0; k < a.tiles_per_item; ++k) {
-      const int j = item * a.tiles_per_item + k;
-      if (j >= kBf16Tiles) break;
-      size_t row_off;
-      bool ring;
-      const int nv = bf16_tile_rows(j, L, row_off, ring);
-      if (nv <= 0) continue;
-      size_t off, off2;
-      int split = 16;
-      if (ring) {
-        if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) continue;
-      } else {
-        if (!sink_ok) {
-          if (lane == 0) set_error(a.err, kErrSink);
-          continue;
-        }
-        off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
-      }
-      uint32_t rows = (1u << nv) - 1u;
-      if (!ring) {
-        rows &= (1u << max(0, min(16, lim[jq] - (int)row_off))) - 1u;
-      } else {
-        for (int r = 0; r < nv; ++r) {
-          const int rr = (int)row_off + r;
-          const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
-          if (p >= lim[jq]) rows &= ~(1u << r);
-        }
-      }
-      if (rows == 0) continue;
-      const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
-      const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
-      bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, sb, lane);
-    }
-    store_state<true>(sb, a.partials + (((size_t)qg[jq] * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats +
-                              kPartialFloats,
-                      1.0f / kPScaleBF16, lane);
-  }
-  // INT2 history pages (rotated basis), unpacked once per block
-  WarpState st[2];
-  state_init(st[0]);
-  state_init(st[1]);
-  const float kpl = log2f(a.pscale);
-  int k = 0;
-  for (; k < n_units; ++k) {
-    const int s = k & 1;
-    const bool ok = mbar_wait_bounded(&bars[s], (k >> 1) & 1, kWaitLimit);
-    if (!__syncthreads_and(ok)) {  // also: the previous page's tiles are consumed
-      if (t == 0) set_error(a.err, kErrTimeout);
-      break;
-    }
-    ext_unpack(smem + (size_t)s * kBlockBytes, kp, vp, ksc, vsc, t);
-    ext_unpack(smem + (size_t)s * kBlockBytes, kp, vp, ksc, vsc, t + kExtThreads);
-    __syncthreads();  // tiles ready; raw stage s free
-    if (t == 0 && k + 2 < n_units) {
-      fence_proxy_async_smem();
-      issue(k + 2);
-    }
-    const int lp = lp0 + k;
-    const int nv[2] = {active[0] ? min(kPage, hlim[0] - kPage * lp) : 0,
-                       active[1] ? min(kPage, hlim[1] - kPage * lp) : 0};
-    const int ph = c.page_table[(size_t)b * c.max_pages + lp];
-    if ((nv[0] > 0 || nv[1] > 0) && ph >= 0 && ph < c.num_pages) {
-      if (nv[0] == kPage && nv[1] == kPage)
-        ext_page<true>(kp, vp, ksc, vsc, nv, qf, scaleE, kpl, st, lane);
-      else
-        ext_page<false>(kp, vp, ksc, vsc, nv, qf, scaleE, kpl, st, lane);
-    }
-  }
-  // after a timeout, wait (bounded) for the copies still in flight
-  for (int kk = k; kk < min(k + 2, n_units); ++kk) mbar_wait_bounded(&bars[kk & 1], (kk >> 1) & 1, kWaitLimit);
+    for (int ql = w4; ql < qpg; ql += 4) {
+      const int qi = grp * qpg + ql;
+      if (qi >= a.chunk) continue;
+      const int qg = b * a.chunk + qi, bq = qg * a.Hkv + h;
+      const int lim = max(0, min(a.pos0[b] + qi + 1, L));
+      uint32_t qpf[16];
+      {
+        const uint4* srcp = reinterpret_cast<const uint4*>(a.qplain + (size_t)bq * kQFragWords + lane * 32);
 #pragma unroll
-  for (int jq = 0; jq < 2; ++jq)
-    if (active[jq])
-      store_state<true>(st[jq], a.partials + (((size_t)qg[jq] * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats,
-                        a.inv_pscale, lane);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 v = __ldg(srcp + (kk ^ (lane & 7)));
+          qpf[4 * kk] = v.x;
+          qpf[4 * kk + 1] = v.y;
+          qpf[4 * kk + 2] = v.z;
+          qpf[4 * kk + 3] = v.w;
+        }
+      }
+      const float scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
+      WarpState sb;
+      state_init(sb);
+      for (int k = 0; k < a.tiles_per_item; ++k) {
+        const int j = item * a.tiles_per_item + k;
+        if (j >= kBf16Tiles) break;
+        size_t row_off;
+        bool ring;
+        const int nv = bf16_tile_rows(j, L, row_off, ring);
+        if (nv <= 0) continue;
+        size_t off, off2;
+        int split = 16;
+        if (ring) {
+          if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) continue;
+        } else {
+          if (!sink_ok) {
+            if (lane == 0) set_error(a.err, kErrSink);
+            continue;
+          }
+          off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
+        }
+        uint32_t rows = (1u << nv) - 1u;
+        if (!ring) {
+          rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
+        } else {
+          for (int r = 0; r < nv; ++r) {
+            const int rr = (int)row_off + r;
+            const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
+            if (p >= lim) rows &= ~(1u << r);
+          }
+        }
+        if (rows == 0) continue;
+        const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
+        const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
+        bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, sb, lane);
+      }
+      store_state<true>(sb, a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats +
+                                kPartialFloats,
+                        1.0f / kPScaleBF16, lane);
+    }
+    // INT2 pages: unpack into tiles of buffer k % 2
+    bool timed_out = false;
+    for (int k = 0; k < n_units; ++k) {
+      const int st = k & 1;
+      if (!mbar_wait_bounded(&rawf[st], (k >> 1) & 1, kXtWaitLimit) ||
+          !mbar_wait_bounded(&tempty[st], ((k >> 1) & 1) ^ 1, kXtWaitLimit)) {
+        set_error(a.err, kErrTimeout);
+        timed_out = true;
+        break;
+      }
+      const uint8_t* rp = sm + kXtRaw + st * kBlockBytes;
+      float* sc = reinterpret_cast<float*>(sm + kXtSc + st * 1024);
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+        ext_unpack<true>(rp, sm + kXtK + st * 16384, sm + kXtV + st * 16384, sc, sc + 128, u + 128 * x);
+      fence_proxy_async_smem();
+      mbar_arrive(&tfull[st]);
+      mbar_arrive(&rawe[st]);
+      if (u == 0 && k + 2 < n_units) {
+        if (!mbar_wait_bounded(&rawe[st], (k >> 1) & 1, kXtWaitLimit)) {
+          set_error(a.err, kErrTimeout);
+          timed_out = true;
+          break;
+        }
+        issue(k + 2);
+      }
+    }
+    if (u == 0 && timed_out)  // copies may still be in flight
+      for (int k = 0; k < min(2, n_units); ++k) mbar_wait_bounded(&rawf[k], 0, kXtWaitLimit);
+  } else if (warp == 8) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_f16_f32(128, 64);
+      const uint64_t dhi = umma_desc_sw128(0) & 0xFFFFFFFF00000000ull;
+      const uint32_t q_lo = (uint32_t)umma_desc_sw128(sbase + kXtQ), p_lo = (uint32_t)umma_desc_sw128(sbase + kXtP);
+      const uint32_t k_lo = (uint32_t)umma_desc_sw128(sbase + kXtK), v_lo = (uint32_t)umma_desc_sw128(sbase + kXtV);
+      const uint32_t tS = tbase, tO = tbase + 128;
+      bool ok = true;
+      // S = q' K^T of page k (tiles of buffer k % 2) for each 64-channel group
+      auto issue_s = [&](int k) {
+        const int st = k & 1;
+        tc_fence_after();
+#pragma unroll
+        for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+            for (int pt = 0; pt < 2; ++pt) {
+              const uint64_t ad = dhi | (q_lo + ((pt * 32768 + gr * 16384 + ks * 32) >> 4));
+              const uint64_t bd = dhi | (k_lo + ((st * 16384 + gr * 8192 + ks * 32) >> 4));
+              umma_f16(tS + 64 * gr, ad, bd, idesc, ks > 0 || pt > 0);
+            }
+        umma_commit(sfull);
+      };
+      if (n_units > 0) {
+        ok = mbar_wait_bounded(&tfull[0], 0, kXtWaitLimit);
+        if (ok) issue_s(0);
+      }
+      for (int k = 0; k < n_units && ok; ++k) {
+        const int st = k & 1;
+        if (k + 1 < n_units) {
+          ok = mbar_wait_bounded(&tfull[(k + 1) & 1], ((k + 1) >> 1) & 1, kXtWaitLimit) &&
+               mbar_wait_bounded(sfree, k & 1, kXtWaitLimit);
+          if (!ok) break;
+          issue_s(k + 1);
+        }
+        ok = mbar_wait_bounded(pfull, k & 1, kXtWaitLimit);
+        if (!ok) break;
+        tc_fence_after();
+        // O[:, 64 G ..] += P_G V^T[64 G ..]: value and residual parts, 4 steps of 16 tokens
+#pragma unroll
+        for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+            for (int pt = 0; pt < 2; ++pt) {
+              const uint64_t ad = dhi | (p_lo + (((2 * gr + pt) * 16384 + ks * 32) >> 4));
+              const uint64_t bd = dhi | (v_lo + ((st * 16384 + gr * 8192 + ks * 32) >> 4));
+              umma_f16(tO + 64 * gr, ad, bd, idesc, k > 0 || ks > 0 || pt > 0);
+            }
+        umma_commit(pvdone);
+        umma_commit(&tempty[st]);
+      }
+      if (!ok) set_error(a.err, kErrTimeout);
+      umma_commit(done);
+      if (!mbar_wait_bounded(done, 0, kXtWaitLimit)) set_error(a.err, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // softmax: row r = t (TMEM lane) = query ql = r / g of the group, head n = r % g
+    const int r = t, ql = r / g, n = r % g, qi = grp * qpg + ql;
+    const bool active = ql < qpg && qi < a.chunk;
+    const int qg = b * a.chunk + (active ? qi : 0);
+    const int lim = active ? max(0, min(a.pos0[b] + qi + 1, L)) : 0;
+    const int hlim = min(hist_end, lim);
+    const float scaleE = active ? __ldg(a.qconst + ((size_t)qg * a.Hkv + h) * kQConstFloats + 16) : 0.f;
+    const float kpl = log2f(a.pscale);
+    const uint32_t tS = tbase + ((uint32_t)(32 * warp) << 16), tO = tS + 128;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int k = 0; k < n_units; ++k) {
+      const int st = k & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(sfull, k & 1, kXtWaitLimit))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* sc = reinterpret_cast<const float*>(sm + kXtSc + st * 1024);  // K: [64][2], V: [64][2]
+      const int nv = min(kPage, hlim - kPage * (lp0 + k));
+      float lg[64];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float s0[32], s1[32];
+        tmem_ld32(tS + 32 * hh, s0);
+        tmem_ld32(tS + 64 + 32 * hh, s1);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int tk = 32 * hh + e;
+          const float x = fmaf(s0[e], sc[2 * tk], s1[e] * sc[2 * tk + 1]) * scaleE;
+          lg[tk] = tk < nv ? x : -INFINITY;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(sfree);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) mx = fmaxf(mx, lg[e]);
+      if (k > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(pvdone, (k - 1) & 1, kXtWaitLimit))) {
+        ok = false;  // (the wait: P buffer free, O settled)
+        break;
+      }
+      // lazy rescaling of this row's O; TMEM loads and stores are warp-wide (.sync.aligned), so
+      // every lane of the warp takes part whenever one needs it (factor 1 for the others)
+      const bool need = nv > 0 && mx > m + kLazy;
+      const float nm = need ? fmaxf(m, mx) : m;
+      const float al = (need && m != -INFINITY) ? ex2(m - nm) : 1.f;
+      if (__any_sync(0xffffffffu, need && m != -INFINITY)) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(tO + 32 * cc, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= al;
+          tmem_st32(tO + 32 * cc, o);
+        }
+        tmem_wait_st();
+      }
+      l *= al;
+      m = nm;
+      const float ms = nv > 0 ? m - kpl : 0.f;
+      const float* vs = sc + 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint32_t w[4][4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int tk = 8 * c8 + e;
+          const float p0 = ex2(lg[tk] - ms), p1 = ex2(lg[tk + 1] - ms);
+          l += p0 + p1;
+          const float a0 = p0 * vs[2 * tk], a1 = p1 * vs[2 * tk + 2];
+          const float b0 = p0 * vs[2 * tk + 1], b1 = p1 * vs[2 * tk + 3];
+          const float ha0 = __half2float(__float2half_rn(a0)), ha1 = __half2float(__float2half_rn(a1));
+          const float hb0 = __half2float(__float2half_rn(b0)), hb1 = __half2float(__float2half_rn(b1));
+          w[0][e >> 1] = pack_f16x2(ha0, ha1);
+          w[1][e >> 1] = pack_f16x2(a0 - ha0, a1 - ha1);
+          w[2][e >> 1] = pack_f16x2(hb0, hb1);
+          w[3][e >> 1] = pack_f16x2(b0 - hb0, b1 - hb1);
+        }
+#pragma unroll
+        for (int mtx = 0; mtx < 4; ++mtx)
+          *reinterpret_cast<uint4*>(sm + kXtP + mtx * 16384 + sw128_elem(r, 8 * c8)) =
+              make_uint4(w[mtx][0], w[mtx][1], w[mtx][2], w[mtx][3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(pfull);
+    }
+    // the row's rotated-basis record (the TMEM loads warp-wide, the stores per row)
+    if (ok && n_units > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(pvdone, (n_units - 1) & 1, kXtWaitLimit)))
+      ok = false;
+    if (!ok) set_error(a.err, kErrTimeout);
+    tc_fence_after();
+    float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats;
+    if (active) {
+      rec[n] = m;
+      rec[8 + n] = l * a.inv_pscale;
+    }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float o[32];
+      if (n_units > 0) {
+        tmem_ld32(tO + 32 * cc, o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+      if (active) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(rec + 16 + n * kStateStride + 32 * cc + e) =
+              make_float4(o[e] * a.inv_pscale, o[e + 1] * a.inv_pscale, o[e + 2] * a.inv_pscale,
+                          o[e + 3] * a.inv_pscale);
+      }
+    }
+  }
+  tc_fence_before();
   griddep_launch_dependents();
   __shared__ int s_last;
   __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 256);
+  }
   if (t == 0) {
     int ticket;
     asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(ticket) : "l"(&a.counters[z * a.Hkv + h]) : "memory");
@@ -1803,7 +1924,7 @@ __global__ void __launch_bounds__(kExtThreads, 1) extend_kernel(const __grid_con
   }
   __syncthreads();
   if (!s_last) return;
-  extend_final_merge(a, smem, b, h, grp, z);
+  extend_final_merge(a, sm, b, h, grp, z);
 }
 
 constexpr size_t decode_smem_bytes() { return kSlotsOffset + (size_t)kBf16Slots * kPartialFloats * sizeof(float); }
@@ -1969,7 +2090,8 @@ ExtendPlan plan_extend(int batch, int chunk, int Hq, int Hkv, int max_ctx_len, i
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
-  p.ngpr = (chunk + kExtQ - 1) / kExtQ;
+  p.qpg = 128 / p.g;  // the group's (query, head) pairs are the 128 rows of the MMAs
+  p.ngpr = (chunk + p.qpg - 1) / p.qpg;
   const int hist_end = max_ctx_len > kSink + kRecent ? max_ctx_len - kRecent : kSink;
   int pages = (hist_end + kPage - 1) / kPage - 1;
   if (pages < 0) pages = 0;
@@ -2023,6 +2145,7 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   a.pos0 = e.pos0;
   a.chunk = p.chunk;
   a.ngpr = p.ngpr;
+  a.qpg = p.qpg;
   a.Hq = p.Hq;
   a.Hkv = p.Hkv;
   a.g = p.g;
@@ -2046,13 +2169,13 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   a.err = e.err;
   static bool attr = false;
   if (!attr) {
-    err = cudaFuncSetAttribute(extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kExtSmem);
+    err = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kXtSmem);
     if (err != cudaSuccess) return err;
     attr = true;
   }
   void* args[] = {&a};
-  return launch_pdl(reinterpret_cast<const void*>(extend_kernel), dim3(p.n_items, p.Hkv, p.batch * p.ngpr),
-                    dim3(kExtThreads), kExtSmem, stream, args);
+  return launch_pdl(reinterpret_cast<const void*>(extend_tc_kernel), dim3(p.n_items, p.Hkv, p.batch * p.ngpr),
+                    dim3(kXtThreads), kXtSmem, stream, args);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {

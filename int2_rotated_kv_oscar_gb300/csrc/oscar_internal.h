@@ -100,7 +100,8 @@ cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cu
 // extend (chunk) attention: a chunk of queries per request reading its cached pages
 struct ExtendPlan {
   int32_t batch = 0, chunk = 0, Hq = 0, Hkv = 0, g = 0;
-  int32_t ngpr = 0;            // query groups (of 16) per request
+  int32_t ngpr = 0;            // query groups per request
+  int32_t qpg = 0;             // queries per group: 128 / g (the group's (query, head) rows fill one MMA)
   int32_t chunk_pages = 0, n_items = 0, tiles_per_item = 0;
   size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
 };
