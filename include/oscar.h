@@ -298,9 +298,11 @@ oscar_status oscar_extend_attention(oscar_ctx* ctx, int32_t layer, const oscar_c
  * among them (appended first); query i of request b attends positions
  * p < min(pos0[b] + i + 1, ctx_len[b]), as oscar_extend_attention would.
  * q: device bf16 [batch][chunk][H_q][128]; out: device fp32, same shape.
- * One block serves 16 queries of one (request, KV head): each INT2 page is
- * copied once and unpacked once into fp16 tiles in shared memory that the 16
- * queries' MMAs read.  Needs H_q / H_kv <= 4 (else OSCAR_ERR_UNSUPPORTED;
+ * One block serves 128 / g queries of one (request, KV head), g = H_q / H_kv:
+ * each INT2 page is copied once and unpacked once into fp16 tiles in shared
+ * memory, and the group's 128 (query, head) rows run its Q.K and P.V as
+ * tensor-core MMAs with the scores and outputs in tensor memory.  Needs
+ * g <= 4 (else OSCAR_ERR_UNSUPPORTED;
  * oscar_extend_attention serves any GQA ratio) and batch * chunk <= 65535.
  * workspace: device, 256-byte aligned, at least
  * oscar_extend_workspace_bytes(ctx, batch, chunk, max_ctx_len) bytes; zero
