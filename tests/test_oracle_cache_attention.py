@@ -219,3 +219,28 @@ def test_reconstruct_from_storage_matches_cache_model():
     K, V = cache.reconstruct_from_storage(c.sink_k, c.sink_v, c.ring_k, c.ring_v, blocks, L, R_K, R_V)
     Km, Vm = c.dequantized()
     assert np.abs(K - Km).max() < 1e-12 and np.abs(V - Vm).max() < 1e-12
+
+
+def test_calibrate_layer_composes_the_steps():
+    # Queries with an exactly diagonal covariance diag(sigma^2) in a shuffled
+    # channel order (+-1 columns of a 256-point Hadamard matrix, scaled):
+    # U_K must be the signed permutation sorting sigma^2 in descending order.
+    # Keys = unit rows: under R = U H P every |entry| is 1/sqrt(128), so that
+    # is tau_K; with every factor off (R = I) tau_K = 1.  With zero scores
+    # (sm_scale = 0) C_S = m^T m for the mean value row m, whose direction is
+    # U_V's first column.
+    import scipy.linalg
+    d = 128
+    r = np.random.default_rng(21)
+    sig2 = r.permutation(np.linspace(1.0, 4.0, d))
+    Q = scipy.linalg.hadamard(256)[:, :d] * np.sqrt(sig2)
+    K = np.eye(d)[:64]
+    V = r.standard_normal((64, d))
+    U_K, U_V, tau_k, tau_v = calibration.calibrate_layer(Q, [K], [V], 0.0)
+    perm = np.argsort(-sig2, kind="stable")
+    assert np.allclose(np.abs(U_K), np.eye(d)[:, perm])
+    assert abs(tau_k - 1.0 / np.sqrt(d)) < 1e-12
+    m = V.mean(0)
+    assert abs(abs(U_V[:, 0] @ m) - np.linalg.norm(m)) < 1e-9
+    _, _, tau_k0, _ = calibration.calibrate_layer(Q, [K], [V], 0.0, flags=(False, False, False))
+    assert abs(tau_k0 - 1.0) < 1e-12
