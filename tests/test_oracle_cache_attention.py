@@ -244,3 +244,21 @@ def test_calibrate_layer_composes_the_steps():
     assert abs(abs(U_V[:, 0] @ m) - np.linalg.norm(m)) < 1e-9
     _, _, tau_k0, _ = calibration.calibrate_layer(Q, [K], [V], 0.0, flags=(False, False, False))
     assert abs(tau_k0 - 1.0) < 1e-12
+
+
+def test_ring_rows_follow_the_documented_convention():
+    # Recent position p >= 64 lives in ring row (p - 64) mod 256 (the storage
+    # convention the C ABI documents for the 256 BF16 recent tokens of [IT]
+    # "Architettura ..."): special cases, and after 400 appends the model's
+    # window positions 144..399 occupy every row exactly once, each its own token.
+    assert [cache.ring_slot(p) for p in (64, 65, 319, 320, 575, 576)] == [0, 1, 255, 0, 255, 0]
+    r = np.random.default_rng(23)
+    R = rotation.composite_rotation(_rand_orth(24))
+    m = cache.RequestCache(R, R, 30.0, 30.0)
+    toks = r.standard_normal((400, 128))
+    for p in range(400):
+        m.append(toks[p:p + 1], toks[p:p + 1])
+    rows = sorted(cache.ring_slot(p) for p in range(144, 400))
+    assert rows == list(range(256))
+    for p in range(144, 400):
+        assert np.array_equal(m.ring_k[cache.ring_slot(p)], toks[p])

@@ -207,3 +207,22 @@ def test_vectorised_unpack_equals_unpack_block():
         a, b, c, d = layout.unpack_block(blocks[i])
         assert np.array_equal(kc[i], a) and np.array_equal(vc[i], c)
         assert np.array_equal(ks[i], b) and np.array_equal(vs[i], d)
+
+
+def test_near_edge_band_is_relative_to_the_scale():
+    # The exclusion band "within 1e-6 relative of a bin edge" is taken
+    # relative to the group's scale s: at s = 1024 a value 5e-4 above the edge
+    # s is inside it (band 1.024e-3); at s ~ 1e-3 a value 5e-7 above the edge 0
+    # is outside it (band ~1e-9), though both would flip under an absolute band.
+    big = np.zeros((1, 64))
+    big[0, 0] = 1536.0                      # a = 1536, s = fp16(1024) = 1024
+    big[0, 1] = 1024.0 + 5e-4
+    small = np.zeros((1, 64))
+    small[0, 0] = 1.5e-3                    # s = fp16(1e-3)
+    small[0, 1] = 5e-7
+    for X, col, want in ((big, 1, True), (small, 1, False)):
+        X = np.concatenate([X, np.full((1, 64), 7.0)], axis=1)   # second group far from every edge
+        _, scales = quant.quantize_rows(X, np.inf)
+        mask = quant.near_edge_mask(X, scales)
+        assert bool(mask[0, col]) == want
+        assert not mask[0, 64:].any()
