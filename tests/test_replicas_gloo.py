@@ -40,7 +40,7 @@ def _rank_main(rank, world, port, results):
 
 def test_two_replicas_report_the_slowest_rank():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a process that already runs torch threads
         results = m.dict()
         mp.spawn(_rank_main, args=(2, port, results), nprocs=2, join=True)
         got = dict(results)
