@@ -87,6 +87,11 @@ typedef enum {
 #define OSCAR_DEVERR_RING 4u       /* ring slot outside [0, num_ring_slots) */
 #define OSCAR_DEVERR_LENGTH 8u     /* a length or position beyond the table's capacity */
 #define OSCAR_DEVERR_TOKENS 16u    /* cu_seqlens inconsistent with n_tokens */
+#define OSCAR_DEVERR_TIMEOUT 32u   /* a kernel's bounded wait on an asynchronous copy or a
+                                      shared-memory barrier gave up (the copy never landed);
+                                      the kernel skipped the rest of that work item, waited
+                                      (bounded) for its copies in flight and returned, so the
+                                      context stays usable but that call's outputs are invalid */
 
 typedef struct oscar_ctx oscar_ctx;
 

@@ -617,6 +617,10 @@ extern "C" oscar_status oscar_decode_attention_noalloc(oscar_ctx* ctx, int32_t l
   const oscar_status st =
       check_decode_args(ctx, args, view->batch, scratch, OSCAR_NOALLOC_SCRATCH_BYTES, 0, &plan);
   if (st != OSCAR_OK) return st;  // OSCAR_ERR_WORKSPACE when the call needs more than the array holds
+  // the documented limit: what oscar_decode_workspace_bytes asks of a caller for this batch and length
+  // (never below the launch's own plan), so that callers can size their calls by that function
+  if (oscar_decode_workspace_bytes(ctx, view->batch, args->max_ctx_len) > OSCAR_NOALLOC_SCRATCH_BYTES)
+    return OSCAR_ERR_WORKSPACE;
   DecodeLaunch d;
   d.mode = 0;
   d.c = refs_of(ctx, view);

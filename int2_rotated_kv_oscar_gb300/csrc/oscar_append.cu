@@ -8,10 +8,11 @@
 // §2.2 A.3-4 (R = U H_Had P_br, per-layer clip thresholds) and §2.2 B (paged
 // cache, sink/recent in BF16, INT2 history after rotation and clipping).
 //
-// Rotation x' = x R is computed as (x U) in fp32, then the Walsh-Hadamard
-// factor as a butterfly (shuffles within a warp, shared memory across warps),
-// then the bit-reversal permutation as an index map.  Quantiser per group of
-// 64 rotated channels: a = min(max|x'|, tau), s = fp16(a / 1.5),
+// Rotation x' = x R uses the layer's composite R = U H P (formed on the host
+// in fp64, one dense 128 x 128 product on the device): the one-token paths
+// multiply in fp32 on the CUDA cores, the bulk path on the tensor cores with
+// R split into three bf16 terms.  Quantiser per group of 64 rotated
+// channels: a = min(max|x'|, tau), s = fp16(a / 1.5),
 // code = [x' >= -s] + [x' >= 0] + [x' >= s].
 
 #include <cuda.h>
@@ -462,26 +463,25 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   const int pages = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
   const int tiles2 = (pages + 1) / 2;                                    // page pairs
   if ((long long)tiles2 * Hkv * B >= (1ll << 31)) return cudaErrorInvalidValue;
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0, n_sm = 0;
+  int sms = 0;
+  {
+    int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(append_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static std::atomic<uint64_t> attr_done;
+    if (e == cudaSuccess) e = smem_attr_once(reinterpret_cast<const void*>(append_tile_kernel), kTcSmem, attr_done);
     if (e != cudaSuccess) return e;
-    sms = n_sm;
   }
   // tensor maps of k and v: [n_tokens][Hkv][128] bf16, boxes of 64 channels x 1 head x 128 tokens
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encode == nullptr) {
+  // (the driver entry point is looked up once; a function-local static is thread-safe to initialise)
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (encode == nullptr) return cudaErrorNotSupported;
   CUtensorMap tm[2];
   const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)a.n_tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2};

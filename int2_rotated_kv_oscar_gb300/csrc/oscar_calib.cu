@@ -236,12 +236,9 @@ cudaError_t launch_calib_attention(const float* Q, int64_t n_q, const float* K, 
                                    int n_heads, float sm_scale, float* O, cudaStream_t stream) {
   const dim3 grid((unsigned)((n_q + kAttnQ - 1) / kAttnQ), (unsigned)n_heads);
   const int smem = (kAttnQ * kD + kAttnK * (kD + 1) + kAttnK * kD) * 4;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(calib_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr_done;
+  const cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(calib_attention_kernel), smem, attr_done);
+  if (e != cudaSuccess) return e;
   calib_attention_kernel<<<grid, 256, smem, stream>>>(Q, n_q, K, V, n_k, sm_scale, O);
   return cudaGetLastError();
 }
@@ -255,13 +252,9 @@ int64_t sort_size(int64_t n) {
 cudaError_t launch_sorted_abs_rotated(const float* X, int64_t n_rows, const float* R, uint32_t* keys,
                                       cudaStream_t stream) {
   const int64_t n = sort_size(n_rows * kD);
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(rotate_abs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kD * kD * 4);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr_done;
+  const cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(rotate_abs_kernel), kD * kD * 4, attr_done);
+  if (e != cudaSuccess) return e;
   const int64_t blocks = (n_rows + 7) / 8;
   rotate_abs_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, kD * kD * 4, stream>>>(X, n_rows, R, keys, n);
   const unsigned nb = (unsigned)(n / kLocal);

@@ -375,156 +375,182 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = pack_f16x2(x0 - h.x, x1 - h.y);
 }
 
-// One 64-token INT2 page (NT = 4) or its 16-token tile T0 (NT = 1), K and V
-// codes + scales staged in shared memory at their block offsets.
-// FULL: all 64 rows valid (no masking).  The softmax weights come out scaled
-// by 2^kp (kp = log2 of the B-operand scale), which the caller undoes.
-template <bool PACK4, bool FULL, int NT>
-__device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n_valid, int T0, const uint32_t* qf,
-                                          float scaleE, float kp, WarpState& st, int lane) {
+// x as an fp16 pair (value, minus the residual): the value in the low half.
+// One rounding, one mixed-precision subtraction (h - x is exact in fp32)
+// and one pack; the consumer subtracts the residual column.
+__device__ __forceinline__ uint32_t value_negres(float x) {
+  unsigned short h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  float nr;
+  asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(nr) : "h"(h), "f"(x));
+  uint32_t p;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p) : "f"(nr), "f"(x));
+  return p;
+}
+
+// Q.K of one 16-token tile T of a staged INT2 page: the lane's raw logits
+// (packed: z[0], z[1] of head lane % 4 for tokens q, q + 8; unpacked:
+// z[0..3] = (q, head 2 tig), (q, 2 tig + 1), (q + 8, 2 tig), (q + 8, 2 tig + 1)),
+// sum over groups of s_K sum_j (c - 1.5) q'_j in the fragments' scale.  The
+// codes enter as exact fp16 levels c - 1.5 (code_level): the operand of the
+// tensor cores' products stays normal and zero-mean, which keeps the logits
+// at fp32 accuracy.  Two independent chains of four MMAs (one per group).
+template <bool PACK4>
+__device__ __forceinline__ void qk_tile(const uint8_t* __restrict__ blk, int T, const uint32_t* qf, float (&z)[4],
+                                        int lane) {
   const int q = lane >> 2;
-  float lg[NT][4];  // packed: [0] token q, [1] token q + 8 of head lane % 4
-#pragma unroll
-  for (int i = 0; i < NT; ++i) {
-    const int T = NT == 4 ? i : T0;
-    if (!FULL && 16 * T >= n_valid) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) lg[i][k] = -INFINITY;
-      continue;
-    }
-    const uint4 kw = *reinterpret_cast<const uint4*>(blk + kKCodes + 512 * T + 16 * lane);
-    const float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q)));
-    const float2 sb =
-        half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q + 8)));
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#define OSCAR_QK(D, X, Y, R, I)                                                              \
-  do {                                                                                      \
-    const uint32_t a0 = code_level<R>(X), a1 = code_level<R>(Y), a2 = code_level<R + 1>(X), \
-                   a3 = code_level<R + 1>(Y);                                             \
-    mma_f16(D, a0, a1, a2, a3, qf[2 * (I)], qf[2 * (I) + 1]);                              \
-    if (!PACK4) mma_f16(D, a0, a1, a2, a3, qf[16 + 2 * (I)], qf[16 + 2 * (I) + 1]);        \
+  const uint4 kw = *reinterpret_cast<const uint4*>(blk + kKCodes + 512 * T + 16 * lane);
+  const uint32_t ksa = *reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q));
+  const uint32_t ksb = *reinterpret_cast<const uint32_t*>(blk + kKScales + 4 * (16 * T + q + 8));
+  float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+  const CodeWord x0(kw.x), y0(kw.z), x1(kw.y), y1(kw.w);  // group 0 (token q, q + 8), group 1
+#define OSCAR_QK2(I, R)                                                                                        \
+  do {                                                                                                         \
+    const uint32_t a0 = code_level<R>(x0), a1 = code_level<R>(y0), a2 = code_level<R + 1>(x0),                 \
+                   a3 = code_level<R + 1>(y0);                                                                 \
+    const uint32_t e0 = code_level<R>(x1), e1 = code_level<R>(y1), e2 = code_level<R + 1>(x1),                 \
+                   e3 = code_level<R + 1>(y1);                                                                 \
+    mma_f16(d0, a0, a1, a2, a3, qf[2 * I], qf[2 * I + 1]);                                                     \
+    mma_f16(d1, e0, e1, e2, e3, qf[8 + 2 * I], qf[9 + 2 * I]);                                                 \
+    if (!PACK4) {                                                                                              \
+      mma_f16(d0, a0, a1, a2, a3, qf[16 + 2 * I], qf[17 + 2 * I]);                                             \
+      mma_f16(d1, e0, e1, e2, e3, qf[24 + 2 * I], qf[25 + 2 * I]);                                             \
+    }                                                                                                          \
   } while (0)
-    {
-      const CodeWord x(kw.x), y(kw.z);  // group 0: token q, token q+8
-      OSCAR_QK(d0, x, y, 0, 0);
-      OSCAR_QK(d0, x, y, 2, 1);
-      OSCAR_QK(d0, x, y, 4, 2);
-      OSCAR_QK(d0, x, y, 6, 3);
-    }
-    {
-      const CodeWord x(kw.y), y(kw.w);  // group 1
-      OSCAR_QK(d1, x, y, 0, 4);
-      OSCAR_QK(d1, x, y, 2, 5);
-      OSCAR_QK(d1, x, y, 4, 6);
-      OSCAR_QK(d1, x, y, 6, 7);
-    }
-#undef OSCAR_QK
-    if constexpr (PACK4) {  // columns 2 h, 2 h + 1: value and residual parts of head h = lane % 4
-      const float lq = fmaf(d0[0] + d0[1], sa.x, (d1[0] + d1[1]) * sa.y) * scaleE;
-      const float lq8 = fmaf(d0[2] + d0[3], sb.x, (d1[2] + d1[3]) * sb.y) * scaleE;
-      lg[i][0] = (FULL || 16 * T + q < n_valid) ? lq : -INFINITY;
-      lg[i][1] = (FULL || 16 * T + q + 8 < n_valid) ? lq8 : -INFINITY;
-      continue;
-    }
-    const float l0 = fmaf(d0[0], sa.x, d1[0] * sa.y) * scaleE;
-    const float l1 = fmaf(d0[1], sa.x, d1[1] * sa.y) * scaleE;
-    const float l2 = fmaf(d0[2], sb.x, d1[2] * sb.y) * scaleE;
-    const float l3 = fmaf(d0[3], sb.x, d1[3] * sb.y) * scaleE;
-    if (FULL) {
-      lg[i][0] = l0;
-      lg[i][1] = l1;
-      lg[i][2] = l2;
-      lg[i][3] = l3;
-    } else {
-      const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
-      lg[i][0] = va ? l0 : -INFINITY;
-      lg[i][1] = va ? l1 : -INFINITY;
-      lg[i][2] = vb ? l2 : -INFINITY;
-      lg[i][3] = vb ? l3 : -INFINITY;
-    }
+  OSCAR_QK2(0, 0);
+  OSCAR_QK2(1, 2);
+  OSCAR_QK2(2, 4);
+  OSCAR_QK2(3, 6);
+#undef OSCAR_QK2
+  const float2 sa = half2_bits_to_float2(ksa), sb = half2_bits_to_float2(ksb);
+  if (PACK4) {  // columns 2 h, 2 h + 1: value and residual parts of head h = lane % 4
+    z[0] = fmaf(d0[0] + d0[1], sa.x, (d1[0] + d1[1]) * sa.y);
+    z[1] = fmaf(d0[2] + d0[3], sb.x, (d1[2] + d1[3]) * sb.y);
+    z[2] = z[3] = 0.f;
+  } else {
+    z[0] = fmaf(d0[0], sa.x, d1[0] * sa.y);
+    z[1] = fmaf(d0[1], sa.x, d1[1] * sa.y);
+    z[2] = fmaf(d0[2], sb.x, d1[2] * sb.y);
+    z[3] = fmaf(d0[3], sb.x, d1[3] * sb.y);
   }
-  if constexpr (PACK4) {
-    float mx = -INFINITY;
+}
+
+// Online softmax over N tiles' raw logits z (scaled by E into the log2
+// domain): p = 2^(z E - m + kp).  The running maximum m is lazy: a warp
+// rescales its state only when a logit passes m by more than kLazy (then m
+// becomes the exact maximum so far), so p <= 2^(kLazy + kp).  MASKED: a
+// logit of -inf (a row past the end) gives p = 0.
+template <bool PACK4, bool MASKED, int N>
+__device__ __forceinline__ void softmax_weights(const float (&z)[N][4], float E, float kp, WarpState& st,
+                                                float (&p)[N][4]) {
+  constexpr int K = PACK4 ? 2 : 4;
+  const float thr = kp + kLazy;
+  auto arg = [&](float zz, float m) {
+    const float e = fmaf(zz, E, kp - m);
+    return MASKED ? (zz == -INFINITY ? -INFINITY : e) : e;
+  };
+  bool need = false;
 #pragma unroll
-    for (int i = 0; i < NT; ++i) mx = fmaxf(mx, fmaxf(lg[i][0], lg[i][1]));
-    online_max1(st, mx);
-    const float ms = st.m[0] - kp;  // weights p 2^kp
+  for (int i = 0; i < N; ++i)
 #pragma unroll
-    for (int i = 0; i < NT; ++i) {
-      const int T = NT == 4 ? i : T0;
-      if (!FULL && 16 * T >= n_valid) continue;
-      const float pq = ex2(lg[i][0] - ms), pq8 = ex2(lg[i][1] - ms);
-      st.l[0] += pq + pq8;
-      float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
-      float2 sb = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q + 8)));
-      if (!FULL) {  // rows past the history end may hold anything
-        const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
-        sa.x = va ? sa.x : 0.f;
-        sa.y = va ? sa.y : 0.f;
-        sb.x = vb ? sb.x : 0.f;
-        sb.y = vb ? sb.y : 0.f;
+    for (int k = 0; k < K; ++k) {
+      p[i][k] = arg(z[i][k], st.m[PACK4 ? 0 : (k & 1)]);
+      need |= p[i][k] > thr;
+    }
+  if (__any_sync(0xffffffffu, need)) {
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        if (PACK4 || (k & 1) == 0)
+          mx0 = fmaxf(mx0, z[i][k] * E);
+        else
+          mx1 = fmaxf(mx1, z[i][k] * E);
       }
-      const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVCodes + 512 * T + 16 * lane);
-      const CodeWord w0(vw.x), w1(vw.y), w2(vw.z), w3(vw.w);
-      const uint32_t b00 = movmatrix_trans(value_residual(pq * sa.x));
-      const uint32_t b01 = movmatrix_trans(value_residual(pq8 * sb.x));
-      const uint32_t b10 = movmatrix_trans(value_residual(pq * sa.y));
-      const uint32_t b11 = movmatrix_trans(value_residual(pq8 * sb.y));
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      if (!PACK4) mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float n0 = fmaxf(st.m[0], mx0), n1 = PACK4 ? n0 : fmaxf(st.m[1], mx1);
+    const float a0 = (n0 == -INFINITY) ? 1.f : ex2(st.m[0] - n0);
+    const float a1 = PACK4 ? a0 : ((n1 == -INFINITY) ? 1.f : ex2(st.m[1] - n1));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      st.acc[i][0] *= a0;
+      st.acc[i][2] *= a0;
+      st.acc[i][1] *= a1;
+      st.acc[i][3] *= a1;
+    }
+    st.l[0] *= a0;
+    st.l[1] *= a1;
+    st.m[0] = n0;
+    st.m[1] = n1;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+#pragma unroll
+      for (int k = 0; k < K; ++k) p[i][k] = arg(z[i][k], st.m[PACK4 ? 0 : (k & 1)]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+#pragma unroll
+    for (int k = 0; k < K; ++k) p[i][k] = ex2(p[i][k]);
+}
+
+// P.V of one tile T with the weights p of the lane's rows (as qk_tile's z):
+// B = p s_V 2^kp (value + residual) against the V codes as exact fp16
+// levels c - 1.5 (code_level).  MASKED: rows at or past nv have p = 0 and
+// their scales are ignored.
+template <bool PACK4, bool MASKED>
+__device__ __forceinline__ void pv_tile(const uint8_t* __restrict__ blk, int T, int nv, const float (&p)[4],
+                                        WarpState& st, int lane) {
+  const int q = lane >> 2;
+  const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVCodes + 512 * T + 16 * lane);
+  float2 wa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
+  float2 wb = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q + 8)));
+  if (MASKED) {  // rows past the history end may hold anything
+    const bool va = q < nv, vb = q + 8 < nv;
+    wa.x = va ? wa.x : 0.f;
+    wa.y = va ? wa.y : 0.f;
+    wb.x = vb ? wb.x : 0.f;
+    wb.y = vb ? wb.y : 0.f;
+  }
+  const CodeWord w0(vw.x), w1(vw.y), w2(vw.z), w3(vw.w);
+  if constexpr (PACK4) {
+    st.l[0] += p[0] + p[1];
+    const uint32_t b00 = movmatrix_trans(value_negres(p[0] * wa.x));
+    const uint32_t b01 = movmatrix_trans(value_negres(p[1] * wb.x));
+    const uint32_t b10 = movmatrix_trans(value_negres(p[0] * wa.y));
+    const uint32_t b11 = movmatrix_trans(value_negres(p[1] * wb.y));
 #define OSCAR_PV(M, B0, B1) \
   mma_f16(st.acc[M], code_level<M>(w0), code_level<M>(w1), code_level<M>(w2), code_level<M>(w3), B0, B1)
-      OSCAR_PV(0, b00, b01);
-      OSCAR_PV(1, b00, b01);
-      OSCAR_PV(2, b00, b01);
-      OSCAR_PV(3, b00, b01);
-      OSCAR_PV(4, b10, b11);
-      OSCAR_PV(5, b10, b11);
-      OSCAR_PV(6, b10, b11);
-      OSCAR_PV(7, b10, b11);
+    OSCAR_PV(0, b00, b01);
+    OSCAR_PV(1, b00, b01);
+    OSCAR_PV(2, b00, b01);
+    OSCAR_PV(3, b00, b01);
+    OSCAR_PV(4, b10, b11);
+    OSCAR_PV(5, b10, b11);
+    OSCAR_PV(6, b10, b11);
+    OSCAR_PV(7, b10, b11);
 #undef OSCAR_PV
-    }
     return;
   }
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < NT; ++i) {
-    mx0 = fmaxf(mx0, fmaxf(lg[i][0], lg[i][2]));
-    mx1 = fmaxf(mx1, fmaxf(lg[i][1], lg[i][3]));
-  }
-  online_max(st, mx0, mx1);
-  const float ms0 = st.m[0] - kp, ms1 = st.m[1] - kp;  // weights p 2^kp
-#pragma unroll
-  for (int i = 0; i < NT; ++i) {
-    const int T = NT == 4 ? i : T0;
-    if (!FULL && 16 * T >= n_valid) continue;
-    const float p0 = ex2(lg[i][0] - ms0), p1 = ex2(lg[i][1] - ms1);
-    const float p2 = ex2(lg[i][2] - ms0), p3 = ex2(lg[i][3] - ms1);
-    st.l[0] += p0 + p2;
-    st.l[1] += p1 + p3;
-    float2 sa = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q)));
-    float2 sb = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(blk + kVScales + 4 * (16 * T + q + 8)));
-    if (!FULL) {  // rows past the history end may hold anything
-      const bool va = 16 * T + q < n_valid, vb = 16 * T + q + 8 < n_valid;
-      sa.x = va ? sa.x : 0.f;
-      sa.y = va ? sa.y : 0.f;
-      sb.x = vb ? sb.x : 0.f;
-      sb.y = vb ? sb.y : 0.f;
-    }
-    const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVCodes + 512 * T + 16 * lane);
-    const CodeWord w0(vw.x), w1(vw.y), w2(vw.z), w3(vw.w);
-    {
-      uint32_t h00, l00, h01, l01, h10, l10, h11, l11;
-      split_pair(p0 * sa.x, p1 * sa.x, h00, l00);
-      split_pair(p2 * sb.x, p3 * sb.x, h01, l01);
-      split_pair(p0 * sa.y, p1 * sa.y, h10, l10);
-      split_pair(p2 * sb.y, p3 * sb.y, h11, l11);
-      h00 = movmatrix_trans(h00);
-      l00 = movmatrix_trans(l00);
-      h01 = movmatrix_trans(h01);
-      l01 = movmatrix_trans(l01);
-      h10 = movmatrix_trans(h10);
-      l10 = movmatrix_trans(l10);
-      h11 = movmatrix_trans(h11);
-      l11 = movmatrix_trans(l11);
+  st.l[0] += p[0] + p[2];
+  st.l[1] += p[1] + p[3];
+  uint32_t h00, l00, h01, l01, h10, l10, h11, l11;
+  split_pair(p[0] * wa.x, p[1] * wa.x, h00, l00);
+  split_pair(p[2] * wb.x, p[3] * wb.x, h01, l01);
+  split_pair(p[0] * wa.y, p[1] * wa.y, h10, l10);
+  split_pair(p[2] * wb.y, p[3] * wb.y, h11, l11);
+  h00 = movmatrix_trans(h00);
+  l00 = movmatrix_trans(l00);
+  h01 = movmatrix_trans(h01);
+  l01 = movmatrix_trans(l01);
+  h10 = movmatrix_trans(h10);
+  l10 = movmatrix_trans(l10);
+  h11 = movmatrix_trans(h11);
+  l11 = movmatrix_trans(l11);
 #define OSCAR_PV2(M, H0, H1, L0, L1)                                                       \
   do {                                                                                     \
     const uint32_t a0 = code_level<M>(w0), a1 = code_level<M>(w1), a2 = code_level<M>(w2), \
@@ -532,17 +558,50 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ blk, int n
     mma_f16(st.acc[M], a0, a1, a2, a3, H0, H1);                                            \
     mma_f16(st.acc[M], a0, a1, a2, a3, L0, L1);                                            \
   } while (0)
-      OSCAR_PV2(0, h00, h01, l00, l01);
-      OSCAR_PV2(1, h00, h01, l00, l01);
-      OSCAR_PV2(2, h00, h01, l00, l01);
-      OSCAR_PV2(3, h00, h01, l00, l01);
-      OSCAR_PV2(4, h10, h11, l10, l11);
-      OSCAR_PV2(5, h10, h11, l10, l11);
-      OSCAR_PV2(6, h10, h11, l10, l11);
-      OSCAR_PV2(7, h10, h11, l10, l11);
+  OSCAR_PV2(0, h00, h01, l00, l01);
+  OSCAR_PV2(1, h00, h01, l00, l01);
+  OSCAR_PV2(2, h00, h01, l00, l01);
+  OSCAR_PV2(3, h00, h01, l00, l01);
+  OSCAR_PV2(4, h10, h11, l10, l11);
+  OSCAR_PV2(5, h10, h11, l10, l11);
+  OSCAR_PV2(6, h10, h11, l10, l11);
+  OSCAR_PV2(7, h10, h11, l10, l11);
 #undef OSCAR_PV2
-    }
+}
+
+// One whole, full INT2 page (64 valid rows): Q.K of its four tiles (eight
+// independent MMA chains), one softmax update, P.V of the four tiles.  The
+// weights come out scaled by 2^kp (undone by the caller).
+template <bool PACK4>
+__device__ __forceinline__ void int2_page_full(const uint8_t* __restrict__ blk, const uint32_t* qf, float E,
+                                               float kp, WarpState& st, int lane) {
+  float z[4][4], p[4][4];
+#pragma unroll
+  for (int T = 0; T < 4; ++T) qk_tile<PACK4>(blk, T, qf, z[T], lane);
+  softmax_weights<PACK4, false, 4>(z, E, kp, st, p);
+#pragma unroll
+  for (int T = 0; T < 4; ++T) pv_tile<PACK4, false>(blk, T, 16, p[T], st, lane);
+}
+
+// One 16-token tile T with rows [0, nv) valid (a page's last tile, or a
+// tile of the left-over pages dealt one tile per warp).
+template <bool PACK4>
+__device__ __forceinline__ void int2_tile(const uint8_t* __restrict__ blk, int T, int nv, const uint32_t* qf,
+                                          float E, float kp, WarpState& st, int lane) {
+  const int q = lane >> 2;
+  float z[1][4], p[1][4];
+  qk_tile<PACK4>(blk, T, qf, z[0], lane);
+  if (PACK4) {
+    z[0][0] = q < nv ? z[0][0] : -INFINITY;
+    z[0][1] = q + 8 < nv ? z[0][1] : -INFINITY;
+  } else {
+    z[0][0] = q < nv ? z[0][0] : -INFINITY;
+    z[0][1] = q < nv ? z[0][1] : -INFINITY;
+    z[0][2] = q + 8 < nv ? z[0][2] : -INFINITY;
+    z[0][3] = q + 8 < nv ? z[0][3] : -INFINITY;
   }
+  softmax_weights<PACK4, true, 1>(z, E, kp, st, p);
+  pv_tile<PACK4, true>(blk, T, nv, p[0], st, lane);
 }
 
 // One 16-token BF16 tile (rows of K and V in global memory, original basis).
@@ -668,6 +727,29 @@ __device__ __forceinline__ void store_state(WarpState& st, float* dst, float inv
       const int ch = 16 * mt + q + 8 * (i >> 1), n = 2 * tig + (i & 1);
       dst[16 + n * kStateStride + ch] = st.acc[mt][i] * inv;
     }
+  }
+}
+
+// A warp's INT2 (rotated-basis) state, as store_state writes it, except that
+// in packed mode the residual column holds minus the residual (value_negres)
+// and is subtracted from the value column.
+template <bool PACK4>
+__device__ __forceinline__ void store_int2_state(WarpState& st, float* dst, float inv, int lane) {
+  if constexpr (PACK4) {
+    const int q = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
+    if (q == 0) {
+      dst[tig] = st.m[0];
+      dst[8 + tig] = st.l[0] * inv;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      dst[16 + tig * kStateStride + 16 * mt + q] = (st.acc[mt][0] - st.acc[mt][1]) * inv;
+      dst[16 + tig * kStateStride + 16 * mt + q + 8] = (st.acc[mt][2] - st.acc[mt][3]) * inv;
+    }
+  } else {
+    store_state<false>(st, dst, inv, lane);
   }
 }
 
@@ -1270,17 +1352,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
             __syncwarp();
           }
           const int n_valid = min(kPage, (LIMIT ? min(hist_end, lim) : hist_end) - kPage * lp);
-          if (LIMIT && n_valid <= 0) {
-          } else if (T < 0) {
-            if (n_valid == kPage)
-              int2_page<PACK4, true, 4>(blk, n_valid, 0, qf, scaleE, kp, st, lane);
-            else
-              int2_page<PACK4, false, 4>(blk, n_valid, 0, qf, scaleE, kp, st, lane);
-          } else if (16 * T < n_valid) {
-            if (n_valid >= 16 * T + 16)
-              int2_page<PACK4, true, 1>(blk, n_valid, T, qf, scaleE, kp, st, lane);
-            else
-              int2_page<PACK4, false, 1>(blk, n_valid, T, qf, scaleE, kp, st, lane);
+          if (T < 0 && n_valid == kPage) {
+            int2_page_full<PACK4>(blk, qf, scaleE, kp, st, lane);
+          } else {  // a partial page tile by tile, or tile T alone
+            const int T0 = T < 0 ? 0 : T, T1 = T < 0 ? 4 : T + 1;
+#pragma unroll 1
+            for (int TT = T0; TT < T1; ++TT) {
+              const int nv = min(16, n_valid - 16 * TT);
+              if (nv > 0) int2_tile<PACK4>(blk, TT, nv, qf, scaleE, kp, st, lane);
+            }
           }
         }
         __syncwarp();
@@ -1307,7 +1387,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
       }
       __syncwarp();
     }
-    store_state<PACK4>(st, wstate, a.inv_pscale, lane);
+    store_int2_state<PACK4>(st, wstate, a.inv_pscale, lane);
   } else {
     state_init(st);
     store_state<PACK4>(st, wstate, 1.f, lane);
@@ -1957,12 +2037,33 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
     pages = (max_ctx_len + kPage - 1) / kPage;
   }
   if (pages < 0) pages = 0;
-  // one balanced wave of blocks (one per SM) when the work is small, <= 8 pages per warp otherwise
-  const long long total = (long long)batch * Hkv * pages;
+  // Pages per work item C: the split whose waves of blocks (one block per
+  // SM) finish first.  A block costs a fixed amount -- the q rotation, the
+  // pipeline's first copies, the block merge with its R_V^T product -- about
+  // what 32 INT2 pages take its 16 warps (measured at 100K tokens: ~5 us
+  // against ~2.5 us per page per warp), plus its C pages; a BF16 page streams
+  // ~7x the bytes, so there the fixed part is ~5 pages.  At batch 1 this
+  // gives one wave of ~num_sms blocks; at large batches a few long items per
+  // (request, KV head) instead of many short ones.
+  const long long bh_count = (long long)batch * Hkv;
   const long long slots = num_sms > 0 ? num_sms : 148;
-  long long C = (total + slots - 1) / slots;
+  const long long fixed = mode == 0 ? 2 * kWarps : 5;
+  long long C = 2;
+  if (pages > 0 && bh_count > 0) {
+    long long best = -1;
+    for (long long n = 1; n <= kMaxChunks && n <= pages; ++n) {
+      const long long c = (pages + n - 1) / n;
+      if (c < 2 && n > 1) break;
+      const long long items = (pages + c - 1) / c;
+      const long long waves = (bh_count * items + slots - 1) / slots;
+      const long long cost = waves * (fixed + c);
+      if (best < 0 || cost < best) {
+        best = cost;
+        C = c;
+      }
+    }
+  }
   if (C < 2) C = 2;
-  if (C > 8 * kWarps) C = 8 * kWarps;
   if (pages > C * kMaxChunks) C = (pages + kMaxChunks - 1) / kMaxChunks;
   p.chunk_pages = (int)C;
   p.n_chunks = pages > 0 ? (int)((pages + C - 1) / C) : 0;
@@ -2070,13 +2171,10 @@ cudaError_t launch_decode_kernel(const DecodeLaunch& d, const PrepArgs& pa, cuda
       d.mode == 0 ? (lim ? (pack4 ? decode_kernel<0, true, true> : decode_kernel<0, false, true>)
                          : (pack4 ? decode_kernel<0, true> : decode_kernel<0, false>))
                   : (pack4 ? decode_kernel<1, true> : decode_kernel<1, false>);
-  static bool attr_done[6] = {false, false, false, false, false, false};
+  static std::atomic<uint64_t> attr_done[6];
   const int which = (lim ? 4 : 2 * d.mode) + (pack4 ? 1 : 0);
-  if (!attr_done[which]) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done[which] = true;
-  }
+  const cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), smem, attr_done[which]);
+  if (e != cudaSuccess) return e;
   void* args[] = {&a};
   return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), smem, stream, args);
 }
@@ -2167,12 +2265,9 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   }
   a.out = e.out;
   a.err = e.err;
-  static bool attr = false;
-  if (!attr) {
-    err = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kXtSmem);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr_done;
+  err = smem_attr_once(reinterpret_cast<const void*>(extend_tc_kernel), kXtSmem, attr_done);
+  if (err != cudaSuccess) return err;
   void* args[] = {&a};
   return launch_pdl(reinterpret_cast<const void*>(extend_tc_kernel), dim3(p.n_items, p.Hkv, p.batch * p.ngpr),
                     dim3(kXtThreads), kXtSmem, stream, args);
@@ -2200,12 +2295,9 @@ cudaError_t launch_decode_step(const AppendLaunch& ap, const DecodeLaunch& d, cu
   const size_t smem = kPatchOffset + sizeof(RowPatch);
   const bool pack4 = p.g <= 4;
   void (*kern)(DecodeArgs, StepArgs) = pack4 ? decode_step_kernel<true> : decode_step_kernel<false>;
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[pack4 ? 1 : 0]) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done[pack4 ? 1 : 0] = true;
-  }
+  static std::atomic<uint64_t> attr_done[2];
+  const cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), smem, attr_done[pack4 ? 1 : 0]);
+  if (e != cudaSuccess) return e;
   void* args[] = {&a, &sa};
   return launch_pdl(reinterpret_cast<const void*>(kern), dim3(p.n_items, p.Hkv, p.batch), dim3(kThreads), smem,
                     stream, args);

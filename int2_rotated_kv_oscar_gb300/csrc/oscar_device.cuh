@@ -3,7 +3,8 @@
 // Everything here is plain inline PTX or CUDA intrinsics: warp-level
 // tensor-core MMA (fp16 in, fp32 accumulate), 8x8 b16 transposes, mbarriers
 // and bulk asynchronous copies (the TMA engine's untiled mode) for staging
-// cache pages into shared memory, and the Walsh-Hadamard butterfly.
+// cache pages into shared memory, tcgen05 / TMA wrappers for the bulk append
+// and the chunk extend kernels.
 #pragma once
 
 #include <cstdint>

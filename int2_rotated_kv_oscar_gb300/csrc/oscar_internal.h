@@ -2,11 +2,27 @@
 // kernels (oscar_append.cu, oscar_decode.cu).  Not part of the public ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace oscar {
+
+// Raise a kernel's dynamic shared-memory limit once per device.  `done`
+// holds one bit per device ordinal (0..63) whose attribute is set; it is an
+// atomic, so concurrent first launches from several host threads are safe
+// (both may set the attribute, which is idempotent).
+inline cudaError_t smem_attr_once(const void* kernel, size_t bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Rotation constants of one layer on the device.
 // One layer's rotation as dense matrices: R = U H P (the factors a layer

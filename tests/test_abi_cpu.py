@@ -81,3 +81,25 @@ def test_struct_layouts_match_the_header():
     assert abi.oscar_cache_view.recent_page_table.offset == 104 and ctypes.sizeof(abi.oscar_cache_view) == 112
     assert ctypes.sizeof(abi.oscar_append_args) == 8 * 4 + 3 * 4 + 4
     assert ctypes.sizeof(abi.oscar_decode_args) == 3 * 8 + 8
+
+
+def test_binding_constants_match_the_header():
+    # every #define the header gives a C caller (device error bits, flags,
+    # block layout, sizes) has the same value in the binding, where it has one
+    text = open(HEADER).read()
+    defines = dict(re.findall(r"#define\s+(OSCAR_[A-Z0-9_]+)\s+\(?([0-9]+)u?\s*(?:<<\s*([0-9]+))?", text) and
+                   [(n, v) for n, v, _ in re.findall(r"#define\s+(OSCAR_[A-Z0-9_]+)\s+\(?([0-9]+)u?\s*(?:<<\s*([0-9]+))?", text)])
+    shifts = {n: int(s) for n, _, s in re.findall(r"#define\s+(OSCAR_[A-Z0-9_]+)\s+\(?([0-9]+)u?\s*(?:<<\s*([0-9]+))?", text) if s}
+    bits = sorted(n for n in defines if n.startswith("OSCAR_DEVERR_"))
+    assert bits == ["OSCAR_DEVERR_LENGTH", "OSCAR_DEVERR_PAGE", "OSCAR_DEVERR_RING", "OSCAR_DEVERR_SINK",
+                    "OSCAR_DEVERR_TIMEOUT", "OSCAR_DEVERR_TOKENS"]
+    values = []
+    for name, v in defines.items():
+        value = int(v) << shifts.get(name, 0)
+        if hasattr(abi, name):
+            assert getattr(abi, name) == value, name
+        if name.startswith("OSCAR_DEVERR_"):
+            values.append(value)
+            assert getattr(abi, name) == value, name  # the binding decodes every bit
+    # the error bits are distinct single bits
+    assert all(v & (v - 1) == 0 for v in values) and len(set(values)) == len(values)

@@ -119,7 +119,7 @@ def _extend_chunk(s, q, B, n, L, P):
                                               (1000, 8, 2, 16, 8, 43),     # GQA 2, half a group
                                               (5000, 33, 2, 32, 8, 44)])   # a group with one query
 def test_extend_chunk_matches_the_oracle(P, n, B, Hq, Hkv, cfg):
-    """The shared-unpack chunk kernel: one block per (request, KV head, 16 queries)."""
+    """The shared-unpack chunk kernel: one block per (request, KV head, 128 / g queries)."""
     L = P + n
     s = harness.Setup(Hq, Hkv, L, B, cfg=cfg)
     try:
