@@ -309,6 +309,264 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- serving batches
+def _graph_over(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn(torch.cuda.current_stream())
+    return g
+
+
+def _time_graphs(graphs, reps):
+    """ms per replay of a list of CUDA graphs replayed round-robin (after one warm pass)."""
+    import torch
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        graphs[i % len(graphs)].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_serving_batch(ctx, dev, cap, n_layers, hbm_peak):
+    """Qwen3-4B-shaped serving batch: 28 requests of 100,000 tokens in one paged
+    pool (shuffled pages), every layer resident; a step is the fused decode step
+    (append with eviction + decode) of every layer, captured in one CUDA graph per
+    position.  Then the BF16-cache decode of the same shape, with as many requests
+    as fit the memory left (the pages' comparison: BF16 runs out of memory first)."""
+    import torch
+    from int2_rotated_kv_oscar_gb300 import abi, inputs
+    from int2_rotated_kv_oscar_gb300 import cache as kvcache
+    Bs, Ls, n_pos = 28, CTX0, 4
+    maxp = (Ls + n_pos + 63) // 64 + 1
+    sc = kvcache.MixedCache(n_layers, HKV, Bs * maxp, Bs, Bs, Bs, maxp, device=dev)
+    sc.page_table.copy_(torch.from_numpy(inputs.shuffled_pages(CFG, Bs * maxp, layer=7).reshape(Bs, maxp)))
+    t0 = time.time()
+    cur = torch.cuda.current_stream()
+    # every layer gets the same seeded tokens (its own rotation makes its own codes)
+    for b0 in range(0, Bs, 7):
+        kv = [inputs.kv_tokens_device(CFG, 0, HKV, inputs.STREAM_KV, Ls, dev, request=b) for b in range(b0, b0 + 7)]
+        ks = torch.cat([x[0] for x in kv])
+        vs = torch.cat([x[1] for x in kv])
+        del kv
+        cu = torch.arange(0, 8 * Ls, Ls, dtype=torch.int32, device=dev)
+        p0 = torch.zeros(7, dtype=torch.int32, device=dev)
+        tabs = (sc.page_table[b0:b0 + 7].contiguous(), sc.sink_page[b0:b0 + 7].contiguous(),
+                sc.ring_slot[b0:b0 + 7].contiguous())
+        for layer in range(n_layers):
+            sv = sc.view(layer)
+            sv.page_table, sv.sink_page, sv.ring_slot, sv.batch = (tabs[0].data_ptr(), tabs[1].data_ptr(),
+                                                                   tabs[2].data_ptr(), 7)
+            abi.oscar_kv_append(ctx, layer, sv, kvcache.append_args(ks, vs, p0, cu, Ls), cur)
+        torch.cuda.synchronize()
+        del ks, vs, tabs
+    assert abi.oscar_check_device_error(ctx) == 0
+    t_fill = time.time() - t0
+    views = [sc.view(layer) for layer in range(n_layers)]
+    qs = torch.stack([inputs.decode_queries_bf16(CFG, layer, Bs, HQ) for layer in range(n_layers)]).to(dev)
+    outs = torch.zeros((n_layers, Bs, HQ, D), dtype=torch.float32, device=dev)
+    kn, vn = inputs.kv_tokens_device(CFG, 998, HKV, inputs.STREAM_APPEND, Bs, dev)
+    ws_t, ws, ws_bytes = kvcache.workspace(ctx, Bs, Ls + n_pos + 1, device=dev)
+    pos = [torch.full((Bs,), Ls + j, dtype=torch.int32, device=dev) for j in range(n_pos)]
+    lens = [x + 1 for x in pos]
+    args = [[(kvcache.append_args(kn, vn, pos[j]), kvcache.decode_args(qs[layer], outs[layer], lens[j], Ls + n_pos))
+             for layer in range(n_layers)] for j in range(n_pos)]
+
+    def step(j):
+        def run(stream):
+            for layer in range(n_layers):
+                a_, d_ = args[j][layer]
+                abi.oscar_decode_step(ctx, layer, views[layer], a_, d_, ws, ws_bytes, stream)
+        return run
+
+    step(0)(cur)  # eager first call (kernel attributes) before capture
+    torch.cuda.synchronize()
+    graphs = [_graph_over(step(j), cap) for j in range(n_pos)]
+    ms = _time_graphs(graphs, 8)
+    assert abi.oscar_check_device_error(ctx) == 0
+    b_step = n_layers * algorithmic_bytes_per_layer(Ls + (n_pos + 1) // 2, batch=Bs)
+    int2 = {"requests": Bs, "context": Ls, "layers": n_layers, "ms_per_step": ms,
+            "tokens_per_s": Bs * 1000.0 / ms, "tokens_per_s_per_request": 1000.0 / ms,
+            "kv_read_gbs": b_step / (ms / 1e3) / 1e9, "hbm_frac": b_step / (ms / 1e3) / 1e9 / hbm_peak,
+            "algorithmic_bytes_per_step": b_step, "setup_s": t_fill}
+    del graphs, args, views, sc, ws_t, outs, qs
+    torch.cuda.empty_cache()
+
+    # ---- the BF16 cache of the same shape, sized to fit what is left
+    L_b = Ls + 1
+    maxp_b = (L_b + 63) // 64
+    per_request = n_layers * maxp_b * HKV * 64 * D * 2 * 2
+    free = torch.cuda.mem_get_info(dev)[0]
+    B_b = max(1, min(Bs, int(0.85 * free // per_request)))
+    bcs = []
+    for layer in range(n_layers):
+        bc = kvcache.BF16PagedCache(HKV, B_b * maxp_b, B_b, maxp_b, device=dev)
+        bc.page_table.copy_(torch.from_numpy(
+            inputs.shuffled_pages(CFG, B_b * maxp_b, layer=100 + layer).reshape(B_b, maxp_b)))
+        g = torch.Generator(device=dev)
+        g.manual_seed(inputs.torch_seed(CFG, layer, inputs.STREAM_KV, 77))
+        bc.k_pages.normal_(generator=g)
+        bc.v_pages.normal_(generator=g)
+        bcs.append(bc)
+    lens_b = torch.full((B_b,), L_b, dtype=torch.int32, device=dev)
+    qb = torch.stack([inputs.decode_queries_bf16(CFG, layer, B_b, HQ) for layer in range(n_layers)]).to(dev)
+    ob = torch.zeros((n_layers, B_b, HQ, D), dtype=torch.float32, device=dev)
+    bws_t, bws, bws_bytes = kvcache.workspace(ctx, B_b, L_b, device=dev)
+    bviews = [c.view() for c in bcs]
+    bargs = [kvcache.decode_args(qb[layer], ob[layer], lens_b, L_b) for layer in range(n_layers)]
+
+    def bstep(stream):
+        for layer in range(n_layers):
+            abi.oscar_decode_attention_bf16(ctx, bviews[layer], bargs[layer], bws, bws_bytes, stream)
+
+    bstep(cur)
+    torch.cuda.synchronize()
+    gb = _graph_over(bstep, cap)
+    ms_b = _time_graphs([gb], 4)
+    assert abi.oscar_check_device_error(ctx) == 0
+    bb_step = n_layers * B_b * (HKV * L_b * 512 + HQ * D * 6)
+    bf16 = {"requests": B_b, "context": L_b, "layers": n_layers, "ms_per_step": ms_b,
+            "tokens_per_s": B_b * 1000.0 / ms_b, "tokens_per_s_per_request": 1000.0 / ms_b,
+            "kv_read_gbs": bb_step / (ms_b / 1e3) / 1e9, "hbm_frac": bb_step / (ms_b / 1e3) / 1e9 / hbm_peak,
+            "sizing": "floor(0.85 x free memory / %.2f GB per 100K-token request over %d layers)"
+                      % (per_request / 1e9, n_layers)}
+    del gb, bcs, bviews, bargs, qb, ob, bws_t
+    torch.cuda.empty_cache()
+    return {"int2": int2, "bf16_same_shape": bf16,
+            "int2_over_bf16_tokens_per_s": int2["tokens_per_s"] / bf16["tokens_per_s"],
+            "int2_over_bf16_per_request": int2["tokens_per_s_per_request"] / bf16["tokens_per_s_per_request"],
+            "note": "Qwen3-4B-shaped serving batch (32 query / 8 KV heads, 36 layers resident, one shuffled paged "
+                    "pool): one decode token per request per step, every layer's fused decode step in one CUDA "
+                    "graph; the BF16 comparator holds as many 100K-token requests as fit the memory left"}
+
+
+def run_ragged_batch(dev, cap, hbm_peak):
+    """Qwen3-32B-shaped ragged batch: 64 layers, 64 query / 8 KV heads, 64 requests
+    with lengths ~ U[8K, 128K] (seeded), the first 16 sharing a 32K-token prefix
+    through aliased page-table entries and sink page; one fused decode step per
+    request in every layer (one CUDA graph), roofline on logical and unique bytes."""
+    import torch
+    from int2_rotated_kv_oscar_gb300 import abi, calibrate, inputs
+    from int2_rotated_kv_oscar_gb300 import cache as kvcache
+    cfg5, n_layers, Hq5, B5, n_shared, prefix = 5, 64, 64, 64, 16, 32 * 1024
+    lens = [int(x) for x in inputs.ragged_lengths(cfg5, B5, 8 * 1024, 128 * 1024, n_shared=n_shared,
+                                                   shared_lo=prefix + 1024)]
+    ctx5 = abi.oscar_create(abi.oscar_config(num_layers=n_layers, num_q_heads=Hq5, num_kv_heads=HKV, head_dim=128,
+                                             page_size=64, sink=64, recent=256, group=64, device=dev.index or 0))
+    try:
+        t0 = time.time()
+        for layer in range(n_layers):
+            U_K, U_V, tk, tv = calibrate.synthetic_layer_rotation(ctx5, cfg5, layer, HKV, n_cal=2048, n_keys=1024,
+                                                                  device=dev)
+            abi.oscar_load_rotation(ctx5, layer, U_K, U_V, tk, tv)
+        t_cal = time.time() - t0
+        # page tables: every logical page a request can reach after one more token; the first n_pre
+        # entries of requests 1..15 alias request 0's (the shared prefix is sink + history)
+        n_pre = prefix // 64
+        maxp = (max(lens) + 1 + 63) // 64 + 1
+        need = [(L + 1 + 63) // 64 + 1 for L in lens]
+        own = [need[b] - (n_pre if 0 < b < n_shared else 0) for b in range(B5)]
+        n_pages = sum(own)
+        perm = inputs.shuffled_pages(cfg5, n_pages, layer=11)
+        table = np.zeros((B5, maxp), dtype=np.int32)
+        k = 0
+        for b in range(B5):
+            first = n_pre if 0 < b < n_shared else 0
+            table[b, first:need[b]] = perm[k:k + need[b] - first]
+            k += need[b] - first
+            if first:
+                table[b, :n_pre] = table[0, :n_pre]
+        n_sink = B5 - (n_shared - 1)
+        c = kvcache.MixedCache(n_layers, HKV, n_pages, n_sink, B5, B5, maxp, device=dev)
+        c.page_table.copy_(torch.from_numpy(table))
+        sink = [0 if b < n_shared else b - (n_shared - 1) for b in range(B5)]
+        c.sink_page.copy_(torch.tensor(sink, dtype=torch.int32))
+        cur = torch.cuda.current_stream()
+        t0 = time.time()
+
+        def fill(rows, start, fresh):
+            toks = [inputs.kv_tokens_device(cfg5, 0, HKV, inputs.STREAM_KV, lens[b], dev, request=b) for b in rows]
+            ks = torch.cat([t[0][p:] for t, p in zip(toks, start)])
+            vs = torch.cat([t[1][p:] for t, p in zip(toks, start)])
+            del toks
+            cu = [0]
+            for b, p in zip(rows, start):
+                cu.append(cu[-1] + lens[b] - p)
+            cu_t = torch.tensor(cu, dtype=torch.int32, device=dev)
+            p0 = torch.tensor(start, dtype=torch.int32, device=dev)
+            tabs = (c.page_table[rows[0]:rows[-1] + 1].contiguous(), c.sink_page[rows[0]:rows[-1] + 1].contiguous(),
+                    c.ring_slot[rows[0]:rows[-1] + 1].contiguous())
+            mx = max(lens[b] - p for b, p in zip(rows, start))
+            for layer in range(n_layers):
+                sv = c.view(layer)
+                sv.page_table, sv.sink_page, sv.ring_slot, sv.batch = (tabs[0].data_ptr(), tabs[1].data_ptr(),
+                                                                       tabs[2].data_ptr(), len(rows))
+                abi.oscar_kv_append(ctx5, layer, sv, kvcache.append_args(ks, vs, p0, cu_t, mx, fresh), cur)
+            torch.cuda.synchronize()
+
+        fill([0], [0], False)
+        fill(list(range(1, n_shared)), [prefix] * (n_shared - 1), True)
+        for b0 in range(n_shared, B5, 8):
+            fill(list(range(b0, b0 + 8)), [0] * 8, False)
+        assert abi.oscar_check_device_error(ctx5) == 0
+        t_fill = time.time() - t0
+        views = [c.view(layer) for layer in range(n_layers)]
+        qs = torch.stack([inputs.decode_queries_bf16(cfg5, layer, B5, Hq5) for layer in range(n_layers)]).to(dev)
+        outs = torch.zeros((n_layers, B5, Hq5, D), dtype=torch.float32, device=dev)
+        kn, vn = inputs.kv_tokens_device(cfg5, 998, HKV, inputs.STREAM_APPEND, B5, dev)
+        pos = torch.tensor(lens, dtype=torch.int32, device=dev)
+        lens_t = pos + 1
+        ws_t, ws, ws_bytes = kvcache.workspace(ctx5, B5, max(lens) + 1, device=dev)
+        args = [(kvcache.append_args(kn, vn, pos), kvcache.decode_args(qs[layer], outs[layer], lens_t, max(lens) + 1))
+                for layer in range(n_layers)]
+
+        def step(stream):
+            for layer in range(n_layers):
+                abi.oscar_decode_step(ctx5, layer, views[layer], args[layer][0], args[layer][1], ws, ws_bytes, stream)
+
+        step(cur)
+        torch.cuda.synchronize()
+        g = _graph_over(step, cap)
+        ms = _time_graphs([g], 6)
+        assert abi.oscar_check_device_error(ctx5) == 0
+        # bytes per layer: per request its history (72 B per token and KV head) and BF16 rows (512 B),
+        # q (bf16) and out (fp32); unique bytes count the 16 requests' shared prefix history once
+        logical = unique = 0
+        for b, L in enumerate(lens):
+            L1 = L + 1
+            hist = max(0, L1 - 320)
+            per = HKV * (hist * 72 + min(L1, 320) * 512) + Hq5 * D * 6
+            logical += per
+            shared = (prefix - 64) * HKV * 72 if 0 < b < n_shared else 0
+            unique += per - shared
+        logical *= n_layers
+        unique *= n_layers
+        out = {"requests": B5, "layers": n_layers, "q_heads": Hq5, "kv_heads": HKV, "ms_per_step": ms,
+               "tokens_per_s": B5 * 1000.0 / ms, "context_min": min(lens), "context_max": max(lens),
+               "context_mean": float(np.mean(lens)), "shared_prefix_requests": n_shared,
+               "shared_prefix_tokens": prefix,
+               "logical_bytes_per_step": logical, "unique_bytes_per_step": unique,
+               "kv_read_gbs_logical": logical / (ms / 1e3) / 1e9, "kv_read_gbs_unique": unique / (ms / 1e3) / 1e9,
+               "hbm_frac_logical": logical / (ms / 1e3) / 1e9 / hbm_peak,
+               "hbm_frac_unique": unique / (ms / 1e3) / 1e9 / hbm_peak,
+               "int2_pool_gb": n_pages * HKV * 4608 * n_layers / 1e9,
+               "setup_s": {"calibration": t_cal, "prefill": t_fill},
+               "note": "one fused decode step per request in each of 64 layers (one CUDA graph, replayed at the "
+                       "same positions); every layer holds the same seeded tokens under its own rotation; "
+                       "logical bytes count each request's whole history, unique bytes the shared prefix "
+                       "once"}
+        del g, args, views, c, ws_t, outs, qs
+        torch.cuda.empty_cache()
+        return out
+    finally:
+        abi.oscar_destroy(ctx5)
+
+
 # ----------------------------------------------------------------------------- CUDA arm
 def run_cuda(args):
     N_LAYERS = args.layers
@@ -621,68 +879,12 @@ def run_cuda(args):
                                     "is unpacked once into fp16 tiles shared by the block's 16 x G query rows; "
                                     "attention_tflops counts Q.K and P.V over each query's causal prefix")
 
-    # ---- serving batch: 28 concurrent 100,000-token requests in one paged pool
-    # (shuffled pages), the same fused decode step; two layers resident, eager
-    # launches (each moves ~1.6 GB), per-layer time scaled to the 36-layer stack
-    serving = None
+    # ---- serving batches: 28 x 100K over 36 resident layers with the same-shape BF16
+    # comparator sized to fit, then the ragged 64-request batch of a 64-layer stack
+    serving = ragged = None
     if rank == 0 and not args.no_batch:
-        Bs, Ls, layers_s, steps_s = 28, CTX0, 2, 12
-        maxp_s = (Ls + steps_s + 63) // 64 + 1
-        sc = kvcache.MixedCache(layers_s, HKV, Bs * maxp_s, Bs, Bs, Bs, maxp_s, device=dev)
-        sc.page_table.copy_(torch.from_numpy(inputs.shuffled_pages(CFG, Bs * maxp_s, layer=7).reshape(Bs, maxp_s)))
-        for layer in range(layers_s):
-            for b0 in range(0, Bs, 7):
-                kv = [inputs.kv_tokens_device(CFG, layer, HKV, inputs.STREAM_KV, Ls, dev, request=b) for b in range(b0, b0 + 7)]
-                ks = torch.cat([x[0] for x in kv])
-                vs = torch.cat([x[1] for x in kv])
-                del kv
-                cu_s = torch.arange(0, 8 * Ls, Ls, dtype=torch.int32, device=dev)
-                p0_s = torch.zeros(7, dtype=torch.int32, device=dev)
-                sv = sc.view(layer)
-                tabs = (sc.page_table[b0:b0 + 7].contiguous(), sc.sink_page[b0:b0 + 7].contiguous(),
-                        sc.ring_slot[b0:b0 + 7].contiguous())
-                sv.page_table, sv.sink_page, sv.ring_slot, sv.batch = (tabs[0].data_ptr(), tabs[1].data_ptr(),
-                                                                       tabs[2].data_ptr(), 7)
-                abi.oscar_kv_append(ctx, layer, sv, kvcache.append_args(ks, vs, p0_s, cu_s, Ls), cur)
-                torch.cuda.synchronize()
-                del ks, vs, tabs
-        assert abi.oscar_check_device_error(ctx) == 0
-        sviews = [sc.view(layer) for layer in range(layers_s)]
-        qs = torch.stack([inputs.decode_queries_bf16(CFG, layer, Bs, HQ) for layer in range(layers_s)]).to(dev)
-        outs = torch.zeros((layers_s, Bs, HQ, D), dtype=torch.float32, device=dev)
-        kns, vns = inputs.kv_tokens_device(CFG, 998, HKV, inputs.STREAM_APPEND, Bs, dev)
-        sws_t, sws, sws_bytes = kvcache.workspace(ctx, Bs, Ls + steps_s + 1, device=dev)
-        pos_s = [torch.full((Bs,), Ls + j, dtype=torch.int32, device=dev) for j in range(steps_s)]
-        len_s = [x + 1 for x in pos_s]
-        sargs = [[(kvcache.append_args(kns, vns, pos_s[j]), kvcache.decode_args(qs[layer], outs[layer], len_s[j],
-                                                                                 Ls + steps_s))
-                  for layer in range(layers_s)] for j in range(steps_s)]
-
-        def sstep(j):
-            for layer in range(layers_s):
-                ap_, dp_ = sargs[j][layer]
-                abi.oscar_decode_step(ctx, layer, sviews[layer], ap_, dp_, sws, sws_bytes, cur)
-        for j in range(3):
-            sstep(j)
-        torch.cuda.synchronize()
-        e0.record()
-        for j in range(3, steps_s):
-            sstep(j)
-        e1.record()
-        torch.cuda.synchronize()
-        assert abi.oscar_check_device_error(ctx) == 0
-        ms_layer = e0.elapsed_time(e1) / ((steps_s - 3) * layers_s)
-        b_layer = algorithmic_bytes_per_layer(Ls + (steps_s + 3) // 2, batch=Bs)
-        hbm_peak = measured_peaks()[0]
-        serving = {"requests": Bs, "context": Ls, "ms_per_layer_step": ms_layer,
-                   "tokens_per_s": Bs * 1000.0 / (N_LAYERS * ms_layer), "layers": N_LAYERS,
-                   "kv_read_gbs": b_layer / (ms_layer / 1e3) / 1e9,
-                   "hbm_frac": b_layer / (ms_layer / 1e3) / 1e9 / hbm_peak,
-                   "note": "Qwen3-4B-shaped serving batch (32 query / 8 KV heads): 28 requests at 100,000 tokens "
-                           "in one shuffled paged pool, oscar_decode_step per layer (append with eviction + "
-                           "decode), per-layer time of two resident layers scaled to 36; algorithmic bytes as "
-                           "for the batch-1 line"}
-        del sc, sws_t, sargs
+        serving = run_serving_batch(ctx, dev, cap, N_LAYERS, measured_peaks()[0])
+        ragged = run_ragged_batch(dev, cap, measured_peaks()[0])
 
     # ---- paged BF16 recent window: the same one-layer decode step with the last 256
     # positions in BF16 pages (five per request, logical page lp in page lp % 5)
@@ -910,6 +1112,7 @@ def run_cuda(args):
         "extend_attention": ext,
         "paged_recent": paged,
         "serving_batch": serving,
+        "ragged_batch": ragged,
         "ablation": ablation,
         "calibration_gpu": cal_gpu,
         "setup_s": {"calibration": t_cal, "prefill": t_prefill},

@@ -165,3 +165,51 @@ def test_extend_chunk_refuses_gqa_above_4():
         assert e.value.status == 2  # OSCAR_ERR_UNSUPPORTED
     finally:
         s.close()
+
+
+@pytest.mark.parametrize("path,n", [("per_query", 16), ("per_query", 256), ("chunk", 16), ("chunk", 256)])
+def test_extend_after_a_100k_prefix(path, n):
+    """Both extend paths at the size the benchmark times: a chunk of n tokens after a
+    100,000-token prefix (long page loops per block, many work items per (query, KV
+    head), the records' merge at full width), checked on sampled queries."""
+    cfg, Hq, Hkv, P = 46, 32, 8, 100_000
+    L = P + n
+    s = harness.Setup(Hq, Hkv, L, 1, cfg=cfg)
+    try:
+        tk = inputs.kv_tokens_device(cfg, 0, Hkv, inputs.STREAM_KV, L, "cuda")
+        s.append(0, tk[0][:P], tk[1][:P], [0], [0, P], P)
+        s.append(0, tk[0][P:], tk[1][P:], [P], [0, n], n)
+        del tk
+        q = inputs.decode_queries_bf16(cfg, 0, n, Hq)
+        if path == "per_query":
+            out = torch.full((n, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+            ctx_len = torch.full((n,), L, dtype=torch.int32, device="cuda")
+            limit = torch.arange(P + 1, L + 1, dtype=torch.int32, device="cuda")
+            ws_t, ws, ws_bytes = kvcache.workspace(s.ctx, n, L)
+            view, _tables = s.cache.chunk_view(0, 0, n)
+            abi.oscar_extend_attention(s.ctx, 0, view, kvcache.decode_args(q.cuda(), out, ctx_len, L), limit, ws,
+                                       ws_bytes, torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            got = out.cpu().numpy().astype(np.float64)
+        else:
+            got = _extend_chunk(s, q.reshape(1, n, Hq, 128).cuda(), 1, n, L, P)[0].cpu().numpy().astype(np.float64)
+        assert s.device_error() == 0
+        assert np.isfinite(got).all()
+        R_K, R_V, _, _ = s.rot[0]
+        Ks, Vs = [], []
+        for (sk, sv, rk, rv, blocks) in s.readback(0, 0, L):
+            K, V = ocache.reconstruct_from_storage(sk, sv, rk, rv, blocks, L, R_K, R_V)
+            Ks.append(K)
+            Vs.append(V)
+        rows = sorted({0, n // 3, (2 * n) // 3, n - 1})
+        errs = []
+        for i in rows:
+            lim = P + i + 1
+            ref = attention.decode_gqa(inputs.bf16_to_f64(q[i]), [K[:lim] for K in Ks], [V[:lim] for V in Vs],
+                                       harness.SM_SCALE)
+            errs.append(float(np.abs(got[i] - ref).max()))
+        print("extend %s after 100K, chunk %d: max-abs vs oracle %.2e over queries %s"
+              % (path, n, max(errs), rows))
+        assert max(errs) <= harness.DECODE_TOL
+    finally:
+        s.close()
