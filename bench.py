@@ -1026,6 +1026,34 @@ def run_cuda(args):
                                            wsa_bytes, cur)
                 torch.cuda.synchronize()
                 ablation[name] = float((o - ref).norm() / ref.norm())
+            # the rotation's cost in the one-token paths: the q rotation (inside the decode's two
+            # launches) and the one-token append with its eviction, per variant; without U the
+            # kernels apply H as the in-register butterfly and P as an index map, with U the
+            # dense product of the folded R (isolated launches behind a GPU-side sleep, median)
+            kn1, vn1 = inputs.kv_tokens_device(CFG, 997, HKV, inputs.STREAM_APPEND, 1, dev)
+            pos_a = torch.tensor([L_a], dtype=torch.int32, device=dev)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            timing = {}
+            for i, (name, _) in enumerate(variants):
+                o = torch.zeros_like(ref)
+                dargs = kvcache.decode_args(qa, o, lens_a, L_a)
+                aargs = kvcache.append_args(kn1, vn1, pos_a)
+                dts, ats = [], []
+                for rep in range(12):
+                    torch.cuda._sleep(5_000_000)
+                    ev[0].record(cur)
+                    abi.oscar_decode_attention(actx, i, acache2.view(i), dargs, wsa, wsa_bytes, cur)
+                    ev[1].record(cur)
+                    abi.oscar_kv_append(actx, i, acache2.view(i), aargs, cur)  # same row each time: idempotent
+                    ev[2].record(cur)
+                    torch.cuda.synchronize()
+                    if rep >= 2:
+                        dts.append(ev[0].elapsed_time(ev[1]))
+                        ats.append(ev[1].elapsed_time(ev[2]))
+                timing[name] = {"decode_ms": float(np.median(dts)), "append_one_token_ms": float(np.median(ats)),
+                                "rotation": "butterfly + index map" if "u_" not in name and name != "oscar"
+                                else "dense folded R"}
+            ablation["timing_16k"] = timing
             assert abi.oscar_check_device_error(actx) == 0
             del acache2, bref, ka, va
         finally:

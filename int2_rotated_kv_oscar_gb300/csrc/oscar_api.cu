@@ -21,6 +21,7 @@ struct oscar_ctx {
   // three-term splits of R_K^T and R_V^T (6 * 128 * 128 bf16)
   std::vector<float*> d_rot;
   std::vector<float> tau_k, tau_v;
+  std::vector<uint32_t> rot_flags;
   std::vector<bool> loaded;
 };
 
@@ -75,6 +76,7 @@ LayerRotation rotation_of(const oscar_ctx* ctx, int layer) {
   r.RT_split = reinterpret_cast<const uint16_t*>(base + 3 * 128 * 128);
   r.tau_k = ctx->tau_k[layer];
   r.tau_v = ctx->tau_v[layer];
+  r.flags = ctx->rot_flags[layer];
   return r;
 }
 
@@ -165,6 +167,7 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   }
   ctx->d_rot.assign(cfg->num_layers, nullptr);
   ctx->tau_k.assign(cfg->num_layers, 0.f);
+  ctx->rot_flags.assign(cfg->num_layers, OSCAR_ROT_ALL);
   ctx->tau_v.assign(cfg->num_layers, 0.f);
   ctx->loaded.assign(cfg->num_layers, false);
   *out = ctx;
@@ -231,6 +234,7 @@ oscar_status oscar_load_rotation(oscar_ctx* ctx, int32_t layer, const float* U_K
     return OSCAR_ERR_CUDA;
   ctx->tau_k[layer] = tau_k;
   ctx->tau_v[layer] = tau_v;
+  ctx->rot_flags[layer] = flags;
   ctx->loaded[layer] = true;
   return OSCAR_OK;
 }

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(2 * kQuantThreads, 1) append_evict_kernel(Appe
   if (blk == nullptr) return;
   const float xv = bf16_bits_to_float((is_v ? c.v_ring : c.k_ring)[r + t]);
   quantize_token(xv, is_v ? a.rot.R_V : a.rot.R_K, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v, sm[half], u,
-                 1 + half);
+                 1 + half, nullptr, a.rot.flags);
 }
 
 // Phase 2a: new tokens that stay BF16 (sink rows, ring rows).

@@ -120,6 +120,7 @@ struct PrepArgs {
   const float* R_K;
   float sm_scale;
   int Hq, Hkv, g;
+  uint32_t rot_flags;  // the layer's factors: without U, q R_K runs as the butterfly
   uint32_t* qfrag;
   uint32_t* qplain;
   float* qconst;
@@ -142,6 +143,7 @@ constexpr int kPrepThreads = 512;  // channel t = u % 128, row quarter u / 128 o
 struct PrepSmem {
   __align__(16) float xs[kMaxG][kD];
   float zq[4][kMaxG][kD];  // partial products over the four quarters of the rows of R_K
+  float qr[kMaxG][kD];     // q' times c, the partials summed (in quarter order)
   float red[kPrepThreads / 32];
 };
 
@@ -195,11 +197,14 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
   constexpr int kW = kPrepThreads / 32;
   if (lane == 0) sm.red[warp] = ss;
   group_sync(bar, kPrepThreads);
-  if (packed)
-    rotate_heads<4>(sm, rk, t, kq);
-  else
-    rotate_heads<kMaxG>(sm, rk, t, kq);
-  group_sync(bar, kPrepThreads);
+  const bool dense = (a.rot_flags & kRotU) != 0;
+  if (dense) {
+    if (packed)
+      rotate_heads<4>(sm, rk, t, kq);
+    else
+      rotate_heads<kMaxG>(sm, rk, t, kq);
+    group_sync(bar, kPrepThreads);
+  }
   // one power-of-two normalisation for q' and q: their magnitudes times 2^-E stay below 2^10
   float S = 0.f;
 #pragma unroll
@@ -211,10 +216,31 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
     er -= 10;
   }
   const float sr = ldexpf(1.f, -er);
-  // q' (scaled by c) of head n, channel j, from the four row-quarter partial products
-  auto qrot = [&](int n, int j) {
-    return (((sm.zq[0][n][j] + sm.zq[1][n][j]) + sm.zq[2][n][j]) + sm.zq[3][n][j]) * c;
-  };
+  // q' (scaled by c) of head n, channel j, from the four row-quarter partial
+  // products, summed once per (head, channel) before the fragments are built;
+  // without U, warp n applies H to head n as the butterfly and P as an index map
+  if (dense) {
+    for (int e = u; e < G * kD; e += kPrepThreads) {
+      const int n = e >> 7, j = e & (kD - 1);
+      sm.qr[n][j] = (((sm.zq[0][n][j] + sm.zq[1][n][j]) + sm.zq[2][n][j]) + sm.zq[3][n][j]) * c;
+    }
+  } else if (warp < G) {
+    float v[4];
+    const float4 xv = *reinterpret_cast<const float4*>(&sm.xs[warp][4 * lane]);
+    v[0] = xv.x;
+    v[1] = xv.y;
+    v[2] = xv.z;
+    v[3] = xv.w;
+    float f = c;
+    if (a.rot_flags & kRotH) {
+      hadamard128(v, lane);
+      f = kInvSqrt128 * c;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sm.qr[warp][(a.rot_flags & kRotP) ? brev7(4 * lane + e) : 4 * lane + e] = v[e] * f;
+  }
+  group_sync(bar, kPrepThreads);
+  auto qrot = [&](int n, int j) { return sm.qr[n][j]; };
   // QK B fragments over the INT2 history: MMA i reads the code pairs at
   // in-half position 2 R, R = 2 (i % 4) (b0) and R + 1 (b1), of word i / 4
   // (ks = 2 (i / 4) + (i % 4) % 2, byte parity pb = (i % 4) / 2), i.e.
@@ -279,6 +305,7 @@ struct DecodeArgs {
   float* out;
   unsigned* err;
   const int32_t* limit;  // extend attention: per-request causal limit (nullptr otherwise)
+  uint32_t rot_flags;    // the layer's factors: without U, acc R_V^T runs as an index map and the butterfly
 };
 
 // The fused decode step's other inputs: the append of this step's token and
@@ -943,7 +970,26 @@ __device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, con
         }
       }
     }
-    if (MODE == 0) {
+    const bool dense = (a.rot_flags & kRotU) != 0;
+    if (MODE == 0 && !dense) {
+      // R_V^T = (H P)^T = P H: (y P) H per head, by warp hn (the product lands in opart[0])
+      __syncthreads();  // ystage complete; the warp states are dead from here on
+      if (warp < a.g) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * lane + e;
+          v[e] = ystage[warp * kD + ((a.rot_flags & kRotP) ? brev7(i) : i)];
+        }
+        if (a.rot_flags & kRotH) {
+          hadamard128(v, lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] *= kInvSqrt128;
+        }
+        reinterpret_cast<float4*>(opart + warp * kD)[lane] = make_float4(v[0], v[1], v[2], v[3]);
+      }
+      __syncthreads();
+    } else if (MODE == 0) {
       __syncthreads();  // ystage complete; the warp states are dead from here on
       // partial products y R_V^T over warp w's rows, for every head
       float o[kG][4];
@@ -976,7 +1022,9 @@ __device__ __noinline__ void block_merge(const DecodeArgs& a, uint8_t* smem, con
       const int n = n0 + 4 * k;
       if (n >= a.g) continue;
       float yr = 0.f;
-      if (MODE == 0)
+      if (MODE == 0 && !dense)
+        yr = opart[n * kD + ch];
+      else if (MODE == 0)
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) yr += opart[(w * kG + n) * kD + ch];
       const float M = fmaxf(Mr[k], Mp[k]);
@@ -1042,6 +1090,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
     // page per warp competes with the previous layer's final merge.
     if (item == 0)  // every block of this layer reads R_V^T in its block merge
       for (int i = t; i < kD * kD / 32; i += kThreads) prefetch_l2(a.R_VT + 32 * i);
+    if constexpr (FUSED) {
+      // the rows the q rotation and the append read first: this request's g
+      // query rows and the new token's K and V rows (256 bytes each)
+      const int r = t >> 1, half = t & 1;
+      if (r < a.g)
+        prefetch_l2(f->pr.q + ((size_t)b * f->pr.Hq + h * a.g + r) * kD + 64 * half);
+      else if (r >= kMaxG && r < kMaxG + 2)
+        prefetch_l2((r == kMaxG ? f->ap.k : f->ap.v) + ((size_t)b * a.Hkv + h) * kD + 64 * half);
+    }
     if (lane == 0) {
       const int Lh = a.ctx_len[b];
       const int he = max(kSink, Lh - kRecent);
@@ -2065,6 +2122,15 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   }
   if (C < 2) C = 2;
   if (pages > C * kMaxChunks) C = (pages + kMaxChunks - 1) / kMaxChunks;
+  // The last item holds the newest history page, so in a decode step it is
+  // also the block that appends the token and moves the evicted row into
+  // INT2 (a few microseconds at the start).  Give it about one page per warp
+  // less than the others when that keeps the item count.
+  if (mode == 0 && pages > C) {
+    const long long n = (pages + C - 1) / C;
+    const long long C2 = (pages + kWarps + n - 1) / n;
+    if (C2 > C && (pages + C2 - 1) / C2 == n) C = C2;
+  }
   p.chunk_pages = (int)C;
   p.n_chunks = pages > 0 ? (int)((pages + C - 1) / C) : 0;
   p.n_items = p.n_chunks > 0 ? p.n_chunks : 1;
@@ -2111,6 +2177,7 @@ PrepArgs prep_args_of(const DecodeLaunch& d) {
   PrepArgs pa;
   pa.q = d.q;
   pa.R_K = d.rot.R_K;
+  pa.rot_flags = d.rot.flags;
   pa.sm_scale = d.sm_scale;
   pa.Hq = p.Hq;
   pa.Hkv = p.Hkv;
@@ -2156,6 +2223,7 @@ DecodeArgs decode_args_of(const DecodeLaunch& d, const PrepArgs& pa) {
   a.out = d.out;
   a.err = d.err;
   a.limit = d.limit;
+  a.rot_flags = d.rot.flags;
   return a;
 }
 
@@ -2225,6 +2293,7 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   PrepArgs pa;
   pa.q = e.q;
   pa.R_K = e.rot.R_K;
+  pa.rot_flags = e.rot.flags;
   pa.sm_scale = e.sm_scale;
   pa.Hq = p.Hq;
   pa.Hkv = p.Hkv;

@@ -40,6 +40,30 @@ __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) { atomic
 // reverse the 7 index bits of a channel (P_br for d = 128)
 __device__ __forceinline__ int brev7(int j) { return (int)(__brev((unsigned)j) >> 25); }
 
+// x H for the 128-point Walsh-Hadamard matrix in Sylvester (natural) order,
+// unnormalised (H_ij = (-1)^popcount(i & j)), of a row held four channels
+// per lane of a warp: channel 4 lane + e in v[e].  The fast transform's
+// seven add/subtract stages: strides 1 and 2 inside the lane, strides 4 .. 64
+// across lanes (lane bit m: the lane holding the upper index of each pair
+// keeps partner - own, the other partner + own).  ainsights.it "OSCAR: Come
+// Together AI ...", "I tre fattori della rotazione": the Hadamard factor.
+__device__ __forceinline__ void hadamard128(float (&v)[4], int lane) {
+  const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+  v[0] = a0 + a2;
+  v[1] = a1 + a3;
+  v[2] = a0 - a2;
+  v[3] = a1 - a3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float sgn = (lane & m) ? -1.f : 1.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = fmaf(sgn, v[e], __shfl_xor_sync(0xffffffffu, v[e], m));
+  }
+}
+
+// 1 / sqrt(128), the normalisation of the Hadamard factor
+constexpr float kInvSqrt128 = 0.08838834764831845f;
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -35,7 +35,14 @@ struct LayerRotation {
   // terms up to ~2^-24 relative (the bulk append's tensor-core operand)
   const uint16_t* RT_split = nullptr;
   float tau_k = 0.f, tau_v = 0.f;
+  // the factors R is made of (kRotU | kRotH | kRotP).  Without a calibrated U
+  // the one-token writes, the q rotation and the decode's inverse rotation
+  // apply H as an in-register Walsh-Hadamard butterfly and P as an index map
+  // instead of the dense product; the bulk append and the chunk kernel keep
+  // the dense R (its tensor-core product costs the same either way).
+  uint32_t flags = 7u;
 };
+constexpr uint32_t kRotU = 1u, kRotH = 2u, kRotP = 4u;
 
 struct CacheRefs {
   uint8_t* pages = nullptr;

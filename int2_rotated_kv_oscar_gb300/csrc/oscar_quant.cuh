@@ -70,26 +70,45 @@ struct RowPatch {
 // rows [32 (u / 128), 32 (u / 128) + 32) of R for channel u % 128; the four
 // partials are added in quarter order.
 // rr(ii) = R[32 (u / 128) + ii][u % 128] (from memory or from registers).
+// rflags: the layer's factors; without U the group's first warp applies H as
+// the in-register butterfly and P as an index map instead (R is not read).
 template <typename RowOf>
 __device__ __forceinline__ void quantize_token(float x, RowOf rr, float tau, uint8_t* block, int row, bool is_v,
-                                               QuantSmem& sm, int u, int bar, RowPatch* patch = nullptr) {
+                                               QuantSmem& sm, int u, int bar, RowPatch* patch, uint32_t rflags) {
   const int t = u & 127, kq = u >> 7, lane = u & 31, warp = (u >> 5) & 3;
+  const bool dense = (rflags & kRotU) != 0;
   if (kq == 0) sm.x[t] = x;
   group_sync(bar, kQuantThreads);
-  float z0 = 0.f, z1 = 0.f;
+  if (dense) {
+    float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-  for (int ii = 0; ii < 32; ii += 4) {
-    const float4 xv = *reinterpret_cast<const float4*>(&sm.x[32 * kq + ii]);
-    z0 = fmaf(xv.x, rr(ii), z0);
-    z1 = fmaf(xv.y, rr(ii + 1), z1);
-    z0 = fmaf(xv.z, rr(ii + 2), z0);
-    z1 = fmaf(xv.w, rr(ii + 3), z1);
+    for (int ii = 0; ii < 32; ii += 4) {
+      const float4 xv = *reinterpret_cast<const float4*>(&sm.x[32 * kq + ii]);
+      z0 = fmaf(xv.x, rr(ii), z0);
+      z1 = fmaf(xv.y, rr(ii + 1), z1);
+      z0 = fmaf(xv.z, rr(ii + 2), z0);
+      z1 = fmaf(xv.w, rr(ii + 3), z1);
+    }
+    sm.zq[kq][t] = z0 + z1;
+  } else if (u < 32) {  // x' = x H P: (x H)_i lands in channel rev(i)
+    float v[4];
+    const float4 xv = *reinterpret_cast<const float4*>(&sm.x[4 * u]);
+    v[0] = xv.x;
+    v[1] = xv.y;
+    v[2] = xv.z;
+    v[3] = xv.w;
+    if (rflags & kRotH) {
+      hadamard128(v, u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] *= kInvSqrt128;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sm.zq[0][(rflags & kRotP) ? brev7(4 * u + e) : 4 * u + e] = v[e];
   }
-  sm.zq[kq][t] = z0 + z1;
   group_sync(bar, kQuantThreads);
   float z = 0.f;
   if (kq == 0) {
-    z = ((sm.zq[0][t] + sm.zq[1][t]) + sm.zq[2][t]) + sm.zq[3][t];
+    z = dense ? ((sm.zq[0][t] + sm.zq[1][t]) + sm.zq[2][t]) + sm.zq[3][t] : sm.zq[0][t];
     const float amax = warp_max(fabsf(z));
     if (lane == 0) sm.red[warp] = amax;
   }
@@ -128,10 +147,10 @@ __device__ __forceinline__ void quantize_token(float x, RowOf rr, float tau, uin
 
 // R: the layer's composite rotation, row-major in global or shared memory.
 __device__ __forceinline__ void quantize_token(float x, const float* __restrict__ R, float tau, uint8_t* block,
-                                               int row, bool is_v, QuantSmem& sm, int u, int bar,
-                                               RowPatch* patch = nullptr) {
+                                               int row, bool is_v, QuantSmem& sm, int u, int bar, RowPatch* patch,
+                                               uint32_t rflags) {
   const float* col = R + (size_t)32 * (u >> 7) * kD + (u & 127);
-  quantize_token(x, [&](int ii) { return col[ii * kD]; }, tau, block, row, is_v, sm, u, bar, patch);
+  quantize_token(x, [&](int ii) { return col[ii * kD]; }, tau, block, row, is_v, sm, u, bar, patch, rflags);
 }
 
 // Locate (and check) the INT2 block of position e of request b, head h.
@@ -220,7 +239,7 @@ __device__ __forceinline__ void append_one_body(const AppendLaunch& a, int b, in
     uint8_t* blk = history_block(c, b, h, e, a.err);
     if (blk != nullptr)
       quantize_token(bf16_bits_to_float(xo), is_v ? Rv : Rk, is_v ? a.rot.tau_v : a.rot.tau_k, blk, e & 63, is_v,
-                     sm, u, bar, patch);
+                     sm, u, bar, patch, a.rot.flags);
   }
   if (mover) ring[rdst] = xn;
 }
@@ -267,8 +286,8 @@ __device__ __forceinline__ void append_pair_body(const AppendLaunch& a, int b, i
     const uint16_t ok = c.k_ring[rsrc], ov = c.v_ring[rsrc];  // in flight while the page table is read
     uint8_t* blk = history_block(c, b, h, e, a.err);
     if (blk != nullptr) {
-      quantize_token(bf16_bits_to_float(ok), rk, a.rot.tau_k, blk, e & 63, false, sm, u, bar, patch);
-      quantize_token(bf16_bits_to_float(ov), rv, a.rot.tau_v, blk, e & 63, true, sm, u, bar, patch);
+      quantize_token(bf16_bits_to_float(ok), rk, a.rot.tau_k, blk, e & 63, false, sm, u, bar, patch, a.rot.flags);
+      quantize_token(bf16_bits_to_float(ov), rv, a.rot.tau_v, blk, e & 63, true, sm, u, bar, patch, a.rot.flags);
     }
   }
   if (mover) {

@@ -35,15 +35,20 @@ def _cache_bytes(s):
     return [t[0].cpu().clone() for t in (c.int2_pages, c.k_sink, c.v_sink, c.k_ring, c.v_ring)]
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (16, 2)])
-def test_step_equals_append_then_decode(Hq, Hkv):
+@pytest.mark.parametrize("Hq,Hkv,flags", [(32, 8, abi.OSCAR_ROT_ALL), (16, 2, abi.OSCAR_ROT_ALL),
+                                           (32, 8, abi.OSCAR_ROT_H | abi.OSCAR_ROT_P),  # butterfly, bit reversal
+                                           (16, 2, abi.OSCAR_ROT_H), (32, 8, abi.OSCAR_ROT_P)])
+def test_step_equals_append_then_decode(Hq, Hkv, flags):
+    """Layers without U rotate the one-token writes, q and the output with the
+    in-register butterfly and the bit-reversal index map instead of the dense
+    product: the evicted rows' codes must still match the oracle bit for bit."""
     cfg = 11
     lens0 = [60, 318, 700]
     n_steps = 6
     B = len(lens0)
     toks = [inputs.kv_tokens_bf16(cfg, 0, Hkv, inputs.STREAM_KV, L + n_steps, b) for b, L in enumerate(lens0)]
-    fused = harness.Setup(Hq, Hkv, max(lens0) + n_steps, B, cfg=cfg, calibrate=False)
-    split = harness.Setup(Hq, Hkv, max(lens0) + n_steps, B, cfg=cfg, calibrate=False)
+    fused = harness.Setup(Hq, Hkv, max(lens0) + n_steps, B, cfg=cfg, calibrate=False, flags=flags)
+    split = harness.Setup(Hq, Hkv, max(lens0) + n_steps, B, cfg=cfg, calibrate=False, flags=flags)
     try:
         for s in (fused, split):
             _prefill(s, toks, lens0)
@@ -75,8 +80,20 @@ def test_step_equals_append_then_decode(Hq, Hkv):
         for b in range(B):
             ref = fused.oracle_decode(0, b, lens[b], q[b].cpu())
             errs.append(np.abs(got[b] - ref).max())
-        print("Hq %d Hkv %d: max-abs vs oracle after %d steps %s" % (Hq, Hkv, n_steps, ["%.2e" % e for e in errs]))
+        print("Hq %d Hkv %d flags %d: max-abs vs oracle after %d steps %s"
+              % (Hq, Hkv, flags, n_steps, ["%.2e" % e for e in errs]))
         assert max(errs) <= harness.DECODE_TOL
+        # the history rows (bulk prefill and the steps' evictions) against the oracle's definition
+        n_cmp = n_bad = 0
+        for b in range(B):
+            tk = inputs.bf16_to_f64(toks[b][0][:lens[b]])
+            tv = inputs.bf16_to_f64(toks[b][1][:lens[b]])
+            for h in range(Hkv):
+                c, bad, _, _ = harness.compare_history_codes(fused, 0, b, lens[b], tk[:, h], tv[:, h], h)
+                n_cmp += c
+                n_bad += bad
+        print("flags %d: %d history codes compared, %d mismatches" % (flags, n_cmp, n_bad))
+        assert n_bad == 0 and n_cmp > 0
     finally:
         fused.close()
         split.close()
