@@ -305,6 +305,8 @@ struct DecodeArgs {
   float* out;
   unsigned* err;
   const int32_t* limit;  // extend attention: per-request causal limit (nullptr otherwise)
+  const uint16_t* q;     // the queries as they came in (bf16; the BF16-cache comparator reads them)
+  float sm_scale;
   uint32_t rot_flags;    // the layer's factors: without U, acc R_V^T runs as an index map and the butterfly
 };
 
@@ -715,6 +717,70 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
     // a[0]: channels 16mt+q, tokens 2tig..; a[1]: channels +8; a[2]: tokens +8; a[3]: both
     mma_f16(st.acc[mt], a[0], a[1], a[2], a[3], b0h, b1h);
     if (!PACK4) mma_f16(st.acc[mt], a[0], a[1], a[2], a[3], b0l, b1l);
+  }
+}
+
+// One 16-token tile of the plain BF16 paged cache (the comparator), rows
+// [0, nv) valid, with the cached bf16 K and V rows and the query's own bf16
+// values as the tensor-core operands (no conversion): Q.K against B = q
+// (exact products; the softmax scale cE = sm_scale log2 e is applied to the
+// fp32 logits), P.V against B = p 2^11 as a bf16 value + residual pair.  The
+// lane's accumulator columns are heads 2 tig and 2 tig + 1 (store_state<false>).
+// qb: the lane's B words of Q.K, word 2 ks + i = q[head lane / 4][32 tig + 4 ks + 2 i .. + 1].
+__device__ __forceinline__ void bf16_tile_raw(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
+                                              int nv, const uint32_t (&qb)[16], float cE, WarpState& st, int lane) {
+  const int q = lane >> 2, tig = lane & 3;
+  const bool va = q < nv, vb = q + 8 < nv;
+  uint32_t ka[16], kb[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 u = va ? __ldg(reinterpret_cast<const uint4*>(Kt + q * kD + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+    ka[4 * k] = u.x;
+    ka[4 * k + 1] = u.y;
+    ka[4 * k + 2] = u.z;
+    ka[4 * k + 3] = u.w;
+    const uint4 w =
+        vb ? __ldg(reinterpret_cast<const uint4*>(Kt + (q + 8) * kD + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+    kb[4 * k] = w.x;
+    kb[4 * k + 1] = w.y;
+    kb[4 * k + 2] = w.z;
+    kb[4 * k + 3] = w.w;
+  }
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) mma_bf16_acc(d, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qb[2 * ks], qb[2 * ks + 1]);
+  const float l0 = va ? d[0] * cE : -INFINITY, l1 = va ? d[1] * cE : -INFINITY;
+  const float l2 = vb ? d[2] * cE : -INFINITY, l3 = vb ? d[3] * cE : -INFINITY;
+  online_max(st, fmaxf(l0, l2), fmaxf(l1, l3));
+  // weights scaled by 2^11 (kPScaleBF16) through the exponent
+  const float ms0 = st.m[0] - 11.f, ms1 = st.m[1] - 11.f;
+  const float p0 = ex2(l0 - ms0), p1 = ex2(l1 - ms1), p2 = ex2(l2 - ms0), p3 = ex2(l3 - ms1);
+  st.l[0] += p0 + p2;
+  st.l[1] += p1 + p3;
+  auto split = [](float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(x0, x1);
+    lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+  };
+  uint32_t b0h, b0l, b1h, b1l;
+  split(p0, p1, b0h, b0l);
+  split(p2, p3, b1h, b1l);
+  b0h = movmatrix_trans(b0h);
+  b0l = movmatrix_trans(b0l);
+  b1h = movmatrix_trans(b1h);
+  b1l = movmatrix_trans(b1l);
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    uint32_t a[4];
+#pragma unroll
+    for (int blkid = 0; blkid < 4; ++blkid) {
+      const int tr = blkid >> 1, cc = blkid & 1;  // token half, channel half
+      const int r = 8 * tr + q;
+      const uint32_t u = (tr ? vb : va) ? __ldg(reinterpret_cast<const uint32_t*>(Vt + r * kD + 16 * mt + 8 * cc + 2 * tig)) : 0u;
+      a[blkid] = movmatrix_trans(u);
+    }
+    // a[0]: channels 16mt+q, tokens 2tig..; a[1]: channels +8; a[2]: tokens +8; a[3]: both
+    mma_bf16_acc(st.acc[mt], a[0], a[1], a[2], a[3], b0h, b1h);
+    mma_bf16_acc(st.acc[mt], a[0], a[1], a[2], a[3], b0l, b1l);
   }
 }
 
@@ -1453,19 +1519,22 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
   // ---------------- BF16 paged cache (comparator): every warp, original basis
   if (MODE == 1) {
     state_init(st);
-    uint32_t qpf[kQW];
+    // the lane's Q.K B words: head lane / 4 (columns of absent heads stay zero),
+    // channels 32 tig .. 32 tig + 31 of the query as it came in (bf16)
+    uint32_t qb[16];
     {
-      const uint4* src = reinterpret_cast<const uint4*>(a.qplain + (size_t)bh * kQFragWords + lane * 32);
+      const int n = lane >> 2;
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)b * a.Hq + h * a.g + n) * kD + 32 * (lane & 3));
 #pragma unroll
-      for (int k = 0; k < kQW / 4; ++k) {
-        const uint4 u = __ldg(src + (k ^ (lane & 7)));
-        qpf[4 * k] = u.x;
-        qpf[4 * k + 1] = u.y;
-        qpf[4 * k + 2] = u.z;
-        qpf[4 * k + 3] = u.w;
+      for (int k = 0; k < 4; ++k) {
+        const uint4 u = n < a.g ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+        qb[4 * k] = u.x;
+        qb[4 * k + 1] = u.y;
+        qb[4 * k + 2] = u.z;
+        qb[4 * k + 3] = u.w;
       }
     }
-    const float scaleEp = __ldg(a.qconst + (size_t)bh * kQConstFloats + 17);
+    const float cE = a.sm_scale * kLog2e;
     {
       // plain BF16 paged cache: item covers pages [item*C, item*C + C), 4 tiles each
       const int n_pages = (L + kPage - 1) / kPage;
@@ -1484,11 +1553,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
         const int nv = min(16, L - kPage * pg - 16 * tile);
         if (nv <= 0) continue;
         const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
-        bf16_tile<PACK4>(a.kb_pages + off, a.vb_pages + off, a.kb_pages + off, a.vb_pages + off, 16, (1u << nv) - 1u,
-                         qpf, scaleEp, st, lane);
+        bf16_tile_raw(a.kb_pages + off, a.vb_pages + off, nv, qb, cE, st, lane);
       }
     }
-    store_state<PACK4>(st, reinterpret_cast<float*>(stage_ptr(1)), 1.0f / kPScaleBF16, lane);
+    store_state<false>(st, reinterpret_cast<float*>(stage_ptr(1)), 1.0f / kPScaleBF16, lane);
   }
   block_merge<MODE, PACK4>(a, smem, bf16_slots, bh, item);
 
@@ -2224,6 +2292,8 @@ DecodeArgs decode_args_of(const DecodeLaunch& d, const PrepArgs& pa) {
   a.err = d.err;
   a.limit = d.limit;
   a.rot_flags = d.rot.flags;
+  a.q = d.q;
+  a.sm_scale = d.sm_scale;
   return a;
 }
 
