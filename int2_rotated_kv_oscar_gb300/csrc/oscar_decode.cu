@@ -404,6 +404,20 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = pack_f16x2(x0 - h.x, x1 - h.y);
 }
 
+// The fp16 pair of the rounding residuals (x0 - h0, x1 - h1) of an fp16 pair
+// h = (h0, h1) = fp16(x0, x1): the halves' signs flipped, two mixed-precision
+// adds (exact in fp32), one pack.
+__device__ __forceinline__ uint32_t f16x2_residual(uint32_t h, float x0, float x1) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n .reg .b32 nh;\n .reg .f32 r0, r1;\n"
+      " xor.b32 nh, %1, 0x80008000;\n mov.b32 {lo, hi}, nh;\n"
+      " add.rn.f32.f16 r0, lo, %2;\n add.rn.f32.f16 r1, hi, %3;\n"
+      " cvt.rn.f16x2.f32 %0, r1, r0;\n}"
+      : "=r"(r)
+      : "r"(h), "f"(x0), "f"(x1));
+  return r;
+}
+
 // x as an fp16 pair (value, minus the residual): the value in the low half.
 // One rounding, one mixed-precision subtraction (h - x is exact in fp32)
 // and one pack; the consumer subtracts the residual column.
@@ -2017,6 +2031,9 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       tc_fence_after();
       const float* sc = reinterpret_cast<const float*>(sm + kXtSc + st * 1024);  // K: [64][2], V: [64][2]
       const int nv = min(kPage, hlim - kPage * (lp0 + k));
+      // raw logits (the q' scale 2^E applied in the exponent below); a warp whose
+      // rows all see the whole page skips the masking
+      const bool whole = __all_sync(0xffffffffu, nv >= kPage);
       float lg[64];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -2026,8 +2043,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int tk = 32 * hh + e;
-          const float x = fmaf(s0[e], sc[2 * tk], s1[e] * sc[2 * tk + 1]) * scaleE;
-          lg[tk] = tk < nv ? x : -INFINITY;
+          const float x = fmaf(s0[e], sc[2 * tk], s1[e] * sc[2 * tk + 1]);
+          lg[tk] = (whole || tk < nv) ? x : -INFINITY;
         }
       }
       tc_fence_before();
@@ -2035,6 +2052,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       float mx = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 64; ++e) mx = fmaxf(mx, lg[e]);
+      mx *= scaleE;
       if (k > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(pvdone, (k - 1) & 1, kXtWaitLimit))) {
         ok = false;  // (the wait: P buffer free, O settled)
         break;
@@ -2066,16 +2084,14 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
           const int tk = 8 * c8 + e;
-          const float p0 = ex2(lg[tk] - ms), p1 = ex2(lg[tk + 1] - ms);
+          const float p0 = ex2(fmaf(lg[tk], scaleE, -ms)), p1 = ex2(fmaf(lg[tk + 1], scaleE, -ms));
           l += p0 + p1;
           const float a0 = p0 * vs[2 * tk], a1 = p1 * vs[2 * tk + 2];
           const float b0 = p0 * vs[2 * tk + 1], b1 = p1 * vs[2 * tk + 3];
-          const float ha0 = __half2float(__float2half_rn(a0)), ha1 = __half2float(__float2half_rn(a1));
-          const float hb0 = __half2float(__float2half_rn(b0)), hb1 = __half2float(__float2half_rn(b1));
-          w[0][e >> 1] = pack_f16x2(ha0, ha1);
-          w[1][e >> 1] = pack_f16x2(a0 - ha0, a1 - ha1);
-          w[2][e >> 1] = pack_f16x2(hb0, hb1);
-          w[3][e >> 1] = pack_f16x2(b0 - hb0, b1 - hb1);
+          w[0][e >> 1] = pack_f16x2(a0, a1);
+          w[1][e >> 1] = f16x2_residual(w[0][e >> 1], a0, a1);
+          w[2][e >> 1] = pack_f16x2(b0, b1);
+          w[3][e >> 1] = f16x2_residual(w[2][e >> 1], b0, b1);
         }
 #pragma unroll
         for (int mtx = 0; mtx < 4; ++mtx)
