@@ -845,7 +845,7 @@ def run_cuda(args):
                        "decode over the shared pages with its causal limit, so the pages are read once per query "
                        "(from L2 when they stay there) and unpacked once per query; the prefix bytes are counted once"}
         del wse_t, etabs
-        # the chunk kernel: each page unpacked once per (KV head, 16 queries), for chunks of 16..256
+        # the chunk kernel: each page unpacked once per (KV head, 128 / g queries), for chunks of 16..256
         ext["chunk_kernel"] = []
         for n_c in (16, 64, 256):
             q_c = inputs.decode_queries_bf16(CFG, 0, n_c, HQ, step=9).to(dev).reshape(1, n_c, HQ, D)
@@ -861,11 +861,13 @@ def run_cuda(args):
             for _ in range(3):
                 call()
             torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("extend_chunk_%d" % n_c)
             e0.record()
             for _ in range(reps):
                 call()
             e1.record()
             torch.cuda.synchronize()
+            torch.cuda.nvtx.range_pop()
             assert abi.oscar_check_device_error(ctx) == 0
             c_ms = e0.elapsed_time(e1) / reps
             c_flop = 4.0 * HQ * n_c * D * (L_e - n_c / 2.0)
