@@ -138,14 +138,17 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 //
 // x R on the 5th-generation tensor cores: one tile is 128 new tokens (two
 // pages) of one (request, KV head) and one matrix (K or V).  D[token][n] =
-// sum_k x[token][k] R^T[n][k] runs as M = 128, N = 64 (one quantisation
-// group), K = 16 tcgen05 MMAs from shared memory into tensor memory.  x is
-// bf16 (exact) and R^T is held as three bf16 terms (R = t0 + t1 + t2 to
-// ~2^-24 relative), so every product is exact; the t0 products of a group
-// accumulate in one TMEM region, the much smaller t1, t2 products in a
-// second, and the epilogue adds the two in fp32 (the codes then match the
-// fp64 definition bit for bit outside the near-edge band).  Each group has
-// two TMEM buffers, so the MMAs of the next tile overlap the epilogue.
+// sum_k x[token][k] R^T[n][k] runs as tcgen05 MMAs (M = 128 tokens, K = 16)
+// from shared memory into tensor memory.  x is bf16 (exact) and R^T is held
+// as three bf16 terms (R = t0 + t1 + t2 to ~2^-24 relative), so every product
+// is exact; the t0 products accumulate in one TMEM region, the much smaller
+// t1, t2 products in a second, and the epilogue adds the two in fp32 (the
+// codes then match the fp64 definition bit for bit outside the near-edge
+// band).  Per K step one N = 256 MMA takes t0 and t1 at once (B = the t0 rows
+// followed by the t1 rows, D = both regions) and one N = 128 MMA adds t2
+// into the second region: 16 MMAs per tile, so that one thread issues them
+// faster than the tensor cores run them.  Two TMEM buffers of 256 columns:
+// the MMAs of the next tile overlap the epilogue of this one.
 //
 // Persistent blocks, one per SM, each for one matrix (even blocks K, odd V):
 //   warps 0-15  epilogue: warp (h, g, q) = (w / 8, w / 4 % 2, w % 4) takes
@@ -162,8 +165,8 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 constexpr int kTcRegions = 1;
 constexpr int kTcThreads = 18 * 32;
 constexpr int kTcStages = 3;
-constexpr uint32_t kTcCols = 512;          // TMEM columns; group g's regions from column 256 g
-constexpr uint32_t kTcB = 0;               // R^T terms: 3 x [2 k-blocks][128 rows n][128 B]
+constexpr uint32_t kTcCols = 512;          // TMEM columns: buffer bb = [t0: 128][t1 + t2: 128] from column 256 bb
+constexpr uint32_t kTcB = 0;               // R^T terms: [2 k-blocks][3 terms][128 rows n][128 B]
 constexpr uint32_t kTcA = 3 * 32768;       // x tiles: kTcStages x [2 k-blocks][128 rows][128 B]
 constexpr uint32_t kTcBars = kTcA + kTcStages * 32768;
 constexpr uint32_t kTcPmax = kTcBars + 512;  // [tile parity][h][g][128 rows] float: half-row maxima
@@ -228,8 +231,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTcBars);  // [kTcStages] x tile of buffer s landed
   uint64_t* empty = full + kTcStages;                           // [kTcStages] buffer s read by its MMAs
-  uint64_t* tfull = empty + kTcStages;                          // [4] TMEM buffer holds its sums
-  uint64_t* tempty = tfull + 4;                                 // [4] TMEM buffer read
+  uint64_t* tfull = empty + kTcStages;                          // [4, 2 used] TMEM buffer bb holds its sums
+  uint64_t* tempty = tfull + 4;                                 // [4, 2 used] TMEM buffer bb read
   uint64_t* done = tempty + 4;                                  // every MMA of the block finished
   uint64_t* xb = done + 1;                                      // [8] the two halves of (g, q) swapped maxima
   uint64_t* dfull = xb + 8;                                     // [kTcDescs] descriptor d written
@@ -247,7 +250,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int c = threadIdx.x; c < 3 * 128 * 16; c += kTcThreads) {
       const int term = c >> 11, n = (c >> 4) & 127, jj = n & 63;
       const int col = (n & 64) | (jj & 8) << 2 | (jj >> 4) << 3 | (jj & 7);
-      *reinterpret_cast<uint4*>(sm + kTcB + term * 32768 + sw128_offset(col, c & 15)) = __ldg(src + c);
+      const int ch = c & 15;  // 16-byte chunk along K: k-block ch / 8
+      *reinterpret_cast<uint4*>(sm + kTcB + (ch >> 3) * 49152 + term * 16384 + sw128_offset(col, ch & 7)) =
+          __ldg(src + c);
     }
   }
   if (threadIdx.x == 0) {
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 256);
+      mbar_init(&tempty[i], 512);  // every epilogue thread, once per tile of the buffer
     }
     mbar_init(done, 1);
     for (int i = 0; i < 8; ++i) mbar_init(&xb[i], 64);
@@ -335,26 +340,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (work[s] == 0) break;
         const uint32_t al = a_lo + (uint32_t)s * (32768 >> 4);
-        for (int g = 0; g < 2; ++g) {
-          const int k = 2 * g + bb;
-          if (!mbar_wait_bounded(&tempty[k], ((it >> 1) & 1) ^ 1, kWaitLimit)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          constexpr uint32_t idesc = umma_idesc_bf16_f32(128, 64);
-          const uint32_t d = tbase + 128 * k, bl = b_lo + (uint32_t)g * (8192 >> 4);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t ko = (uint32_t)((i >> 2) * 16384 + (i & 3) * 32) >> 4;
-            const uint64_t ad = dhi | (al + ko);
-            umma_f16(d, ad, dhi | (bl + ko), idesc, i > 0);
-            umma_f16(d + 64, ad, dhi | (bl + ko + (32768 >> 4)), idesc, i > 0);
-            umma_f16(d + 64, ad, dhi | (bl + ko + (65536 >> 4)), idesc, true);
-          }
-          umma_commit(&tfull[k]);
+        if (!mbar_wait_bounded(&tempty[bb], ((it >> 1) & 1) ^ 1, kWaitLimit)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        tc_fence_after();
+        constexpr uint32_t idesc256 = umma_idesc_bf16_f32(128, 256), idesc128 = umma_idesc_bf16_f32(128, 128);
+        const uint32_t d = tbase + 256 * bb;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t ka = (uint32_t)((i >> 2) * 16384 + (i & 3) * 32) >> 4;  // x: k-blocks 16 KB apart
+          const uint32_t kb = (uint32_t)((i >> 2) * 49152 + (i & 3) * 32) >> 4;  // R^T: 48 KB apart
+          const uint64_t ad = dhi | (al + ka);
+          umma_f16(d, ad, dhi | (b_lo + kb), idesc256, i > 0);                          // t0 | t1
+          umma_f16(d + 128, ad, dhi | (b_lo + kb + (32768 >> 4)), idesc128, true);      // + t2
+        }
+        umma_commit(&tfull[bb]);
         umma_commit(&empty[s]);
       }
       if (!ok) set_error(a.err, kErrTimeout);
@@ -364,7 +365,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // epilogue: warp (h, g, q) = (warp / 8, warp / 4 % 2, warp % 4): token row 32 q + lane, group g,
-    // channels 16 k + 8 h + b (k < 4, b < 8), which the permuted R^T puts in TMEM columns 32 h + 8 k + b
+    // channels 16 k + 8 h + b (k < 4, b < 8), which the permuted R^T puts in TMEM columns 64 g + 32 h + 8 k + b
+    // of the tile's buffer (t0 part; the t1 + t2 part 128 columns on)
     const int g = (warp >> 2) & 1, h = warp >> 3, q = warp & 3, row = 32 * q + lane;
     const float tau = m ? a.rot.tau_v : a.rot.tau_k;
     float* pmax = reinterpret_cast<float*>(sm + kTcPmax);
@@ -380,8 +382,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint8_t* blk = (b >= 0 && p >= dsc.lo && p < dsc.hi) ? dsc.blk[row >> 6] : nullptr;
       mbar_arrive(&dempty[di]);
       if (b < 0) break;
-      const int bb = it & 1, k = 2 * g + bb;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[k], (it >> 1) & 1, kWaitLimit))) {
+      const int bb = it & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[bb], (it >> 1) & 1, kWaitLimit))) {
         set_error(a.err, kErrTimeout);
         break;
       }
@@ -389,14 +391,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float x[32];
       {
         float v[32], w[32];
-        const uint32_t ta = tbase + ((uint32_t)(32 * q) << 16) + 128 * k + 32 * h;
-        tmem_ld32(ta, v);
-        tmem_ld32(ta + 64, w);
+        const uint32_t ta = tbase + ((uint32_t)(32 * q) << 16) + 256 * bb + 64 * g + 32 * h;
+        tmem_ld32x2(ta, ta + 128, v, w);
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = v[e] + w[e];
       }
       tc_fence_before();
-      mbar_arrive(&tempty[k]);
+      mbar_arrive(&tempty[bb]);
       float mx = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(x[e]));
@@ -414,14 +415,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int rp = p & 63;
       const __half hs = __float2half_rn(fminf(mx, tau) / 1.5f);
       const float sc = __half2float(hs);
+      // The code (x >= -s) + (x >= 0) + (x >= s) is floor(x / s + 2) while
+      // every |x| / s of the group stays below 2 (no clipped value, a normal
+      // scale).  Then one fma rounding down into the units of 1.5 2^23 gives
+      // it in the low bits of the result, and one multiply-add puts it at its
+      // bit: sum (bits - 1.5 2^23) 2^shift over a word = sum bits 2^shift
+      // minus a constant, mod 2^32.  x times the rounded reciprocal moves an
+      // edge by under 2^-23 relative.
+      const float inv = __frcp_rn(sc);
+      const bool fast = sc > 0.f && mx * inv < 1.99f;
+      constexpr float kMagic = 12582914.0f;         // 1.5 2^23 + 2
+      constexpr uint32_t kMagicBits = 0x4B400000u;  // bits of 1.5 2^23
       if (m == 0) {
         // K words tq = 2 h + b / 4: channel 16 k + 4 tq + b % 4 at bit 8 (b % 4) + 2 k
         uint32_t kw[2] = {0u, 0u};
+        if (fast) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int kk = e >> 3, b = e & 7;
-          const uint32_t bit = 1u << (8 * (b & 3) + 2 * kk);
-          kw[b >> 2] += (x[e] >= -sc ? bit : 0u) + (x[e] >= 0.f ? bit : 0u) + (x[e] >= sc ? bit : 0u);
+          for (int e = 0; e < 32; ++e) {
+            const int kk = e >> 3, b = e & 7;
+            kw[b >> 2] += __float_as_uint(__fmaf_rd(x[e], inv, kMagic)) * (1u << (8 * (b & 3) + 2 * kk));
+          }
+          kw[0] -= kMagicBits * 0x55555555u;
+          kw[1] -= kMagicBits * 0x55555555u;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int kk = e >> 3, b = e & 7;
+            const uint32_t bit = 1u << (8 * (b & 3) + 2 * kk);
+            kw[b >> 2] += (x[e] >= -sc ? bit : 0u) + (x[e] >= 0.f ? bit : 0u) + (x[e] >= sc ? bit : 0u);
+          }
         }
         *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(rp, 2 * h, g)) = kw[0];
         *reinterpret_cast<uint32_t*>(blk + kKCodes + k_word_offset(rp, 2 * h + 1, g)) = kw[1];
@@ -430,10 +452,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t vb[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b) vb[b] = 0u;
+        if (fast) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const uint32_t bit = 1u << (2 * (e >> 3));
-          vb[e & 7] += (x[e] >= -sc ? bit : 0u) + (x[e] >= 0.f ? bit : 0u) + (x[e] >= sc ? bit : 0u);
+          for (int e = 0; e < 32; ++e)
+            vb[e & 7] += __float_as_uint(__fmaf_rd(x[e], inv, kMagic)) * (1u << (2 * (e >> 3)));
+#pragma unroll
+          for (int b = 0; b < 8; ++b) vb[b] -= kMagicBits * 0x55u;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint32_t bit = 1u << (2 * (e >> 3));
+            vb[e & 7] += (x[e] >= -sc ? bit : 0u) + (x[e] >= 0.f ? bit : 0u) + (x[e] >= sc ? bit : 0u);
+          }
         }
 #pragma unroll
         for (int b = 0; b < 8; ++b) blk[kVCodes + v_half_offset(rp, 8 * h + b) + g] = (uint8_t)vb[b];
