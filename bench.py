@@ -807,7 +807,8 @@ def run_cuda(args):
                 "tensor": {"algorithmic_tflops": a_flop / (a_ms / 1e3) / 1e12,
                            "executed_tflops": 3 * a_flop / (a_ms / 1e3) / 1e12, "peak": tc_peak,
                            "executed_frac": 3 * a_flop / (a_ms / 1e3) / 1e12 / tc_peak, "peak_kind": tc_kind,
-                           "note": "tcgen05 M=128 N=64 K=16 MMAs; R^T as three bf16 terms, so the tensor cores "
+                           "note": "tcgen05 MMAs, M=128 tokens, K=16: per K step one N=256 (the t0 and t1 terms "
+                                   "of R^T) and one N=128 (t2); R^T as three bf16 terms, so the tensor cores "
                                    "run x R three times to keep the codes exact"},
                 "note": "oscar_kv_append of one 131,072-token prompt (BF16 K and V in, INT2 history + BF16 "
                         "sink/recent out), mean of 10 eager calls"}
