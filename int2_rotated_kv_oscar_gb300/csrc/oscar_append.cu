@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 constexpr int kTcRegions = 1;
 constexpr int kTcThreads = 18 * 32;
 constexpr int kTcStages = 3;
+constexpr unsigned kTcAhead = 3;           // x tiles pulled into L2 ahead of their loads
 constexpr uint32_t kTcCols = 512;          // TMEM columns: buffer bb = [t0: 128][t1 + t2: 128] from column 256 bb
 constexpr uint32_t kTcB = 0;               // R^T terms: [2 k-blocks][3 terms][128 rows n][128 B]
 constexpr uint32_t kTcA = 3 * 32768;       // x tiles: kTcStages x [2 k-blocks][128 rows][128 B]
@@ -280,51 +281,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tbase = *tmem_at;
 
   if (warp == 16) {
+    // x tiles by TMA; after the last tile a buffer with work = 0 tells the MMA thread to stop.  The
+    // warp looks up 32 candidate tiles at once (lane j: tile base + j n_cta, with its page blocks),
+    // so that lane 0 issues each load without waiting on a table read.
+    const CUtensorMap* tm = m ? &tmv : &tmk;
+    if (lane == 0) prefetch_tensormap(tm);
+    int it = 0;  // lane 0: tiles whose loads were issued
+    bool timed_out = false;
+    for (unsigned base = cta; base < n_tiles && !timed_out; base += 32u * n_cta) {
+      const unsigned tile = base + (unsigned)lane * n_cta;
+      TcTile t = {};
+      uint8_t* b0 = nullptr;
+      uint8_t* b1 = nullptr;
+      const bool valid = tile < n_tiles && tc_tile(a, tile, tiles2, t);
+      int y0 = 0;
+      if (valid) {
+        b0 = tc_block(a.c, t.b, t.h, t.lp0, a.err);
+        b1 = (t.lp0 + 1) * kPage < t.hi ? tc_block(a.c, t.b, t.h, t.lp0 + 1, a.err) : nullptr;
+        y0 = t.tok0 + t.lp0 * kPage - t.p0;  // token index of the tile's first row (may be < 0)
+      }
+      unsigned vmask = __ballot_sync(0xffffffffu, valid);
+      while (vmask != 0u) {
+        const int j = __ffs(vmask) - 1;
+        vmask &= vmask - 1u;
+        {
+          // the valid tile kTcAhead places on into L2 (a hint; the buffer ring bounds how far the loads run)
+          unsigned rest = vmask;
+          for (unsigned r = 1; r < kTcAhead && rest != 0u; ++r) rest &= rest - 1u;
+          if (rest != 0u && lane == __ffs(rest) - 1) {
+            tma_prefetch_3d(tm, 0, t.h, y0);
+            tma_prefetch_3d(tm, 64, t.h, y0);
+          }
+        }
+        const int th = __shfl_sync(0xffffffffu, t.h, j), ty0 = __shfl_sync(0xffffffffu, y0, j);
+        const int tb = __shfl_sync(0xffffffffu, t.b, j), tlp0 = __shfl_sync(0xffffffffu, t.lp0, j);
+        const int tlo = __shfl_sync(0xffffffffu, t.lo, j), thi = __shfl_sync(0xffffffffu, t.hi, j);
+        const uint64_t pb0 = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(b0), j);
+        const uint64_t pb1 = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(b1), j);
+        if (lane == 0) {
+          const int s = it % kTcStages, di = it % kTcDescs;
+          if (!mbar_wait_bounded(&empty[s], ((it / kTcStages) & 1) ^ 1, kWaitLimit)) {
+            timed_out = true;
+          } else {
+            work[s] = 1;
+            mbar_arrive_expect_tx(&full[s], 32768);
+            tma_load_3d(sm + kTcA + s * 32768, tm, 0, th, ty0, &full[s]);
+            tma_load_3d(sm + kTcA + s * 32768 + 16384, tm, 64, th, ty0, &full[s]);
+            ++it;
+            if (!mbar_wait_bounded(&dempty[di], (((it - 1) / kTcDescs) & 1) ^ 1, kWaitLimit)) {
+              timed_out = true;
+            } else {
+              TcDesc& dsc = desc[di];
+              dsc.b = tb;
+              dsc.lp0 = tlp0;
+              dsc.lo = tlo;
+              dsc.hi = thi;
+              dsc.blk[0] = reinterpret_cast<uint8_t*>(pb0);
+              dsc.blk[1] = reinterpret_cast<uint8_t*>(pb1);
+              mbar_arrive(&dfull[di]);
+            }
+          }
+        }
+        timed_out = __shfl_sync(0xffffffffu, timed_out, 0);
+        if (timed_out) break;
+      }
+    }
     if (lane == 0) {
-      // x tiles by TMA; after the last tile a buffer with work = 0 tells the MMA thread to stop
-      const CUtensorMap* tm = m ? &tmv : &tmk;
-      prefetch_tensormap(tm);
-      int it = 0;
-      bool timed_out = false;
-      for (unsigned tile = cta;; tile += n_cta) {
-        TcTile t;
-        const bool last = tile >= n_tiles;
-        if (!last && !tc_tile(a, tile, tiles2, t)) continue;
-        const int s = it % kTcStages;
-        const int di = it % kTcDescs;
+      if (timed_out) {
+        set_error(a.err, kErrTimeout);
+        // copies may still be in flight: wait for them, bounded (on the normal path the MMA thread
+        // has seen every one land)
+        for (int k = max(0, it - kTcStages); k < it; ++k)
+          mbar_wait_bounded(&full[k % kTcStages], (k / kTcStages) & 1, kWaitLimit);
+      } else {
+        const int s = it % kTcStages, di = it % kTcDescs;
         if (!mbar_wait_bounded(&empty[s], ((it / kTcStages) & 1) ^ 1, kWaitLimit) ||
             !mbar_wait_bounded(&dempty[di], ((it / kTcDescs) & 1) ^ 1, kWaitLimit)) {
           set_error(a.err, kErrTimeout);
-          timed_out = true;
-          break;
-        }
-        TcDesc& dsc = desc[di];
-        if (last) {
-          dsc.b = -1;
+        } else {
+          desc[di].b = -1;
           mbar_arrive(&dfull[di]);
           work[s] = 0;
           mbar_arrive(&full[s]);
-          break;
         }
-        dsc.b = t.b;
-        dsc.lp0 = t.lp0;
-        dsc.lo = t.lo;
-        dsc.hi = t.hi;
-        dsc.blk[0] = tc_block(a.c, t.b, t.h, t.lp0, a.err);
-        dsc.blk[1] = (t.lp0 + 1) * kPage < t.hi ? tc_block(a.c, t.b, t.h, t.lp0 + 1, a.err) : nullptr;
-        mbar_arrive(&dfull[di]);
-        work[s] = 1;
-        const int y0 = t.tok0 + t.lp0 * kPage - t.p0;  // token index of the tile's first row (may be < 0)
-        mbar_arrive_expect_tx(&full[s], 32768);
-        tma_load_3d(sm + kTcA + s * 32768, tm, 0, t.h, y0, &full[s]);
-        tma_load_3d(sm + kTcA + s * 32768 + 16384, tm, 64, t.h, y0, &full[s]);
-        ++it;
       }
-      // after a timeout, copies may still be in flight: wait for them, bounded (on the normal path
-      // the MMA thread has seen every one land)
-      if (timed_out)
-        for (int k = max(0, it - kTcStages); k < it; ++k)
-          mbar_wait_bounded(&full[k % kTcStages], (k / kTcStages) & 1, kWaitLimit);
     }
     __syncwarp();
   } else if (warp == 17) {
@@ -398,9 +438,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&tempty[bb]);
-      float mx = 0.f;
+      float mq[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
-      for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(x[e]));
+      for (int e = 0; e < 32; ++e) mq[e & 3] = fmaxf(mq[e & 3], fabsf(x[e]));
+      float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       // the group maximum over both halves of the row
       float* pm = pmax + (((bb * 2 + h) * 2 + g) * 128);
       pm[row] = mx;
@@ -420,9 +461,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // scale).  Then one fma rounding down into the units of 1.5 2^23 gives
       // it in the low bits of the result, and one multiply-add puts it at its
       // bit: sum (bits - 1.5 2^23) 2^shift over a word = sum bits 2^shift
-      // minus a constant, mod 2^32.  x times the rounded reciprocal moves an
-      // edge by under 2^-23 relative.
-      const float inv = __frcp_rn(sc);
+      // minus a constant, mod 2^32.  x times the approximate reciprocal moves
+      // an edge by about 2^-22 relative.
+      float inv;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sc));
       const bool fast = sc > 0.f && mx * inv < 1.99f;
       constexpr float kMagic = 12582914.0f;         // 1.5 2^23 + 2
       constexpr uint32_t kMagicBits = 0x4B400000u;  // bits of 1.5 2^23
@@ -430,13 +472,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // K words tq = 2 h + b / 4: channel 16 k + 4 tq + b % 4 at bit 8 (b % 4) + 2 k
         uint32_t kw[2] = {0u, 0u};
         if (fast) {
+          uint32_t part[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};  // short chains: by word and k
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int kk = e >> 3, b = e & 7;
-            kw[b >> 2] += __float_as_uint(__fmaf_rd(x[e], inv, kMagic)) * (1u << (8 * (b & 3) + 2 * kk));
+            part[b >> 2][kk] += __float_as_uint(__fmaf_rd(x[e], inv, kMagic)) * (1u << (8 * (b & 3) + 2 * kk));
           }
-          kw[0] -= kMagicBits * 0x55555555u;
-          kw[1] -= kMagicBits * 0x55555555u;
+          kw[0] = ((part[0][0] + part[0][1]) + (part[0][2] + part[0][3])) - kMagicBits * 0x55555555u;
+          kw[1] = ((part[1][0] + part[1][1]) + (part[1][2] + part[1][3])) - kMagicBits * 0x55555555u;
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
