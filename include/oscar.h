@@ -108,7 +108,8 @@ typedef struct {
 } oscar_config;
 
 /*
- * One layer's cache, all device memory owned by the caller.
+ * One layer's cache, all device memory owned by the caller; every pool
+ * 16-byte aligned.
  *   int2_pages  [num_pages][num_kv_heads][OSCAR_BLOCK_BYTES] bytes.
  *   k_sink, v_sink  bf16 [num_sink_pages][num_kv_heads][64][128]: positions 0..63.
  *   k_ring, v_ring  bf16 [num_ring_slots][num_kv_heads][256][128]: position p >= 64

@@ -41,6 +41,9 @@ struct DeviceGuard {
 bool valid_view(const oscar_ctx* ctx, const oscar_cache_view* v) {
   if (v == nullptr || v->batch < 0) return false;
   if (v->batch == 0) return true;
+  // the BF16 pools move in 16-byte pieces
+  for (const void* pool : {v->k_sink, v->v_sink, v->k_ring, v->v_ring})
+    if ((reinterpret_cast<uintptr_t>(pool) & 15u) != 0) return false;
   return v->int2_pages && v->k_sink && v->v_sink && v->k_ring && v->v_ring && v->page_table && v->sink_page &&
          (v->ring_slot || v->recent_page_table) && v->num_pages > 0 && v->num_sink_pages > 0 && v->num_ring_slots > 0 &&
          v->max_pages_per_req > 0 && v->num_pages <= INT32_MAX && v->num_sink_pages <= INT32_MAX &&

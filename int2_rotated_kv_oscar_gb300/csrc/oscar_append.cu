@@ -71,6 +71,7 @@ __device__ __forceinline__ bool request_span(const AppendLaunch& a, int b, int& 
 // by the first kQuantThreads threads, V by the others.
 __global__ void __launch_bounds__(2 * kQuantThreads, 1) append_evict_kernel(AppendLaunch a) {
   __shared__ QuantSmem sm[2];
+  griddep_launch_dependents();  // the BF16-row kernel may start; it waits for this one before its writes
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, half = threadIdx.x / kQuantThreads;
   const int u = threadIdx.x % kQuantThreads, t = u & 127;
   const bool is_v = half == 1;
@@ -93,44 +94,40 @@ __global__ void __launch_bounds__(2 * kQuantThreads, 1) append_evict_kernel(Appe
 // Phase 2a: new tokens that stay BF16 (sink rows, ring rows).
 // grid (320, B), 128 threads; all KV heads of one position per block.
 __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
-  const int x = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  // the tile kernel may start (it touches no BF16 row); the ring rows written
+  // here are the ones the eviction kernel before this one reads
+  griddep_launch_dependents();
+  griddep_wait();
+  // block x: one position of request blockIdx.y; thread t: 16 bytes (channels
+  // 8 (t % 16) ..) of KV head t / 16, t / 16 + 8, ...
+  const int x = blockIdx.x, b = blockIdx.y, t = threadIdx.x, c8 = 8 * (t & 15);
   int p0, n, tok0;
   if (!request_span(a, b, p0, n, tok0)) return;
   const int L = p0 + n;
   const CacheRefs& c = a.c;
   const int Hkv = c.num_kv_heads;
-  int p;
-  uint16_t *kd, *vd;
-  size_t row0;
+  auto copy = [&](int h, int p, uint16_t* kd, uint16_t* vd, size_t d) {
+    const size_t s = ((size_t)(tok0 + p - p0) * Hkv + h) * kD + c8;
+    *reinterpret_cast<uint4*>(kd + d + c8) = __ldg(reinterpret_cast<const uint4*>(a.k + s));
+    *reinterpret_cast<uint4*>(vd + d + c8) = __ldg(reinterpret_cast<const uint4*>(a.v + s));
+  };
   if (x < kSink) {
-    p = p0 + x;
+    const int p = p0 + x;
     if (p >= min(L, kSink)) return;
     const int sp = c.sink_page[b];
     if (sp < 0 || sp >= c.num_sink) {
       if (t == 0) set_error(a.err, kErrSink);
       return;
     }
-    kd = c.k_sink;
-    vd = c.v_sink;
-    row0 = (size_t)sp * Hkv * kSink;  // + h * 64 + p
-    for (int h = 0; h < Hkv; ++h) {
-      const size_t s = ((size_t)(tok0 + p - p0) * Hkv + h) * kD + t;
-      const size_t d = (row0 + (size_t)h * kSink + p) * kD + t;
-      kd[d] = a.k[s];
-      vd[d] = a.v[s];
-    }
+    for (int h = t >> 4; h < Hkv; h += 8) copy(h, p, c.k_sink, c.v_sink, (((size_t)sp * Hkv + h) * kSink + p) * kD);
     return;
   }
-  p = max(max(p0, L - kRecent), kSink) + (x - kSink);
+  const int p = max(max(p0, L - kRecent), kSink) + (x - kSink);
   if (p >= L) return;
-  kd = c.k_ring;
-  vd = c.v_ring;
-  for (int h = 0; h < Hkv; ++h) {
+  for (int h = t >> 4; h < Hkv; h += 8) {
     size_t d;
-    if (!recent_row(c, b, h, p, d, a.err, t == 0)) return;
-    const size_t s = ((size_t)(tok0 + p - p0) * Hkv + h) * kD + t;
-    kd[d + t] = a.k[s];
-    vd[d + t] = a.v[s];
+    if (!recent_row(c, b, h, p, d, a.err, (t & 15) == 0)) continue;
+    copy(h, p, c.k_ring, c.v_ring, d);
   }
 }
 
@@ -520,6 +517,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, kTcCols);
   }
+  // this kernel may have started beside the BF16-row and eviction kernels: its
+  // end also marks theirs for what comes next in the stream
+  griddep_wait();
 }
 
 }  // namespace
@@ -530,8 +530,22 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
     append_one_kernel<<<dim3(Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
     return cudaGetLastError();
   }
-  if (!(a.flags & 1u)) append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
-  append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
+  // The first kernel of the call starts after everything before it; the next
+  // ones may start early and overlap it (the tile kernel writes only INT2
+  // rows of the new tokens, which the eviction and BF16-row kernels do not
+  // touch).
+  AppendLaunch la = a;
+  void* args1[] = {&la};
+  cudaError_t e0;
+  if (!(a.flags & 1u)) {
+    append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
+    e0 = launch_pdl(reinterpret_cast<const void*>(append_bf16_kernel), dim3(kSink + kRecent, B), dim3(128), 0,
+                    stream, args1);
+  } else {
+    append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
+    e0 = cudaGetLastError();
+  }
+  if (e0 != cudaSuccess) return e0;
   if (a.n_tokens == 0) return cudaGetLastError();
   const int pages = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
   const int tiles2 = (pages + 1) / 2;                                    // page pairs
@@ -568,8 +582,10 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   // an even grid: blocks 2 i take K, 2 i + 1 take V
   const long long per_matrix = (long long)tiles2 * Hkv * B;
   const int blocks = 2 * (int)std::min<long long>(per_matrix, std::max(1, sms / 2));
-  append_tile_kernel<<<blocks, kTcThreads, kTcSmem, stream>>>(a, tm[0], tm[1], (unsigned)tiles2);
-  return cudaGetLastError();
+  unsigned t2 = (unsigned)tiles2;
+  void* args[] = {&la, &tm[0], &tm[1], &t2};
+  return launch_pdl(reinterpret_cast<const void*>(append_tile_kernel), dim3(blocks), dim3(kTcThreads), kTcSmem, stream,
+                    args);
 }
 
 }  // namespace oscar

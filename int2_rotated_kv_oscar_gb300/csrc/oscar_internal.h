@@ -77,6 +77,23 @@ struct AppendLaunch {
 
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
 
+// A launch that may start once the kernel before it in the stream has let its
+// dependents go (griddepcontrol.launch_dependents) or has finished; the kernel
+// waits (griddepcontrol.wait) before it touches what that kernel writes.
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // decode workspace layout (bytes, all offsets 256-aligned)
 struct DecodePlan {
   int32_t batch = 0, Hq = 0, Hkv = 0, g = 0;
