@@ -260,13 +260,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 512);  // every epilogue thread, once per tile of the buffer
+      mbar_init(&tempty[i], 16);  // every epilogue warp, once per tile of the buffer
     }
     mbar_init(done, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&xb[i], 64);
+    for (int i = 0; i < 8; ++i) mbar_init(&xb[i], 2);
     for (int i = 0; i < kTcDescs; ++i) {
       mbar_init(&dfull[i], 1);
-      mbar_init(&dempty[i], 512);
+      mbar_init(&dempty[i], 16);  // every epilogue warp
     }
     fence_mbar_init();
   }
@@ -417,7 +417,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const TcDesc& dsc = desc[di];
       const int b = dsc.b, p = dsc.lp0 * kPage + row;
       uint8_t* blk = (b >= 0 && p >= dsc.lo && p < dsc.hi) ? dsc.blk[row >> 6] : nullptr;
-      mbar_arrive(&dempty[di]);
+      // one arrival per warp (the lanes' reads are ordered before it by the warp barrier)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dempty[di]);
       if (b < 0) break;
       const int bb = it & 1;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[bb], (it >> 1) & 1, kWaitLimit))) {
@@ -434,7 +436,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int e = 0; e < 32; ++e) x[e] = v[e] + w[e];
       }
       tc_fence_before();
-      mbar_arrive(&tempty[bb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[bb]);
       float mq[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
       for (int e = 0; e < 32; ++e) mq[e & 3] = fmaxf(mq[e & 3], fabsf(x[e]));
@@ -442,7 +445,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // the group maximum over both halves of the row
       float* pm = pmax + (((bb * 2 + h) * 2 + g) * 128);
       pm[row] = mx;
-      mbar_arrive(&xb[4 * g + q]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xb[4 * g + q]);
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&xb[4 * g + q], (it & 1), kWaitLimit))) {
         set_error(a.err, kErrTimeout);
         break;
