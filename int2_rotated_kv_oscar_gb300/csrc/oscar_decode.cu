@@ -1745,26 +1745,32 @@ __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* sm
 // One block per (item = page range, KV head, group of 128 / g queries): the
 // group's (query, head) pairs are the 128 rows of every MMA (TMEM lane =
 // row).  Per INT2 page: S = Q'_value K^T + Q'_residual K^T for each 64-channel
-// group (f16 MMAs from the 128-byte-swizzled tiles into TMEM), one softmax
-// thread per row (its query's causal limit, lazy rescaling of its O row in
-// TMEM), P s_v as fp16 value + residual operands, O += P V (V transposed).
-// S of the next page overlaps the softmax of this one.  Warps:
-//   0-3  softmax; at the end the rows' rotated-basis records
-//   4-7  the q' operands (from the prep's fragments), the BF16 sink/recent
-//        tiles (per query, mma.sync, original-basis records), then the pages:
-//        bulk copies (thread 128) and the unpack into double-buffered tiles
-//   8    TMEM (256 columns: S, then O) and the MMA thread
-constexpr int kXtThreads = 9 * 32;
+// group (f16 MMAs into TMEM), one softmax thread per row (its query's causal
+// limit, lazy rescaling of its O row in TMEM), P s_v as fp16 value + residual
+// operands, O += P V (V transposed).  The A operands (q' and P) sit in TMEM,
+// so an MMA reads only its B tile (K or V^T, 128-byte-swizzled) from shared
+// memory.  S of the next page overlaps the softmax of this one.  Warps:
+//   0-3, 9-12  softmax, two warpgroups splitting every page (tokens 0-31, 32-63) and O's
+//        columns; warps 0-3 first put the q' rows into TMEM; at the end the rows'
+//        rotated-basis records
+//   4-7  the q' operands (from the prep's fragments, staged in shared memory),
+//        the BF16 sink/recent tiles (per query, mma.sync, original-basis
+//        records), then the pages: bulk copies (thread 128) and the unpack
+//        into double-buffered tiles
+//   8    TMEM (512 columns: S, O, q', P) and the MMA thread
+constexpr int kXtThreads = 13 * 32;
 constexpr unsigned kXtWaitLimit = 1u << 18;  // polls per wait: a broken hand-off ends in well under a second
 constexpr uint32_t kXtQ = 0;             // q' value / residual: 2 x [2 blocks of 64 channels][128 rows][128 B]
-constexpr uint32_t kXtP = 65536;         // P s_v: [group][value, residual][128 rows][64 tokens] (4 x 16 KB)
-constexpr uint32_t kXtK = 131072;        // K tiles: 2 x [2 blocks of 64 channels][64 tokens][128 B]
-constexpr uint32_t kXtV = 163840;        // V^T tiles: 2 x [128 channels][64 tokens]
+constexpr int kXtTiles = 4;              // unpacked-page buffers (the MMAs of a page hold theirs until P V)
+constexpr uint32_t kXtK = 65536;         // K tiles: kXtTiles x [2 blocks of 64 channels][64 tokens][128 B]
+constexpr uint32_t kXtV = 131072;        // V^T tiles: kXtTiles x [128 channels][64 tokens]
 constexpr uint32_t kXtRaw = 196608;      // raw pages: 2 x 4608
-constexpr uint32_t kXtSc = kXtRaw + 2 * kBlockBytes;  // scales: 2 x [K 64 x 2, V 64 x 2] float
-constexpr uint32_t kXtBars = kXtSc + 2 * 1024;
-constexpr size_t kXtSmem = kXtBars + 256 + 1024;  // + 1024-byte alignment slack
-static_assert(kXtSc + 2 * 1024 <= kXtBars && kXtRaw == kXtV + 2 * 16384, "extend staging");
+constexpr uint32_t kXtSc = kXtRaw + 2 * kBlockBytes;  // scales: kXtTiles x [K 64 x 2, V 64 x 2] float
+constexpr uint32_t kXtBars = kXtSc + kXtTiles * 1024;
+constexpr uint32_t kXtX = kXtBars + 256;  // softmax halves: page maxima [2][2][128], then l [2][128] (float)
+constexpr size_t kXtSmem = kXtX + 3072 + 1024;  // + 1024-byte alignment slack
+static_assert(kXtK == kXtQ + 65536 && kXtV == kXtK + kXtTiles * 16384 && kXtRaw == kXtV + kXtTiles * 16384,
+              "extend staging");
 
 __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_constant__ ExtendArgs a) {
   extern __shared__ uint8_t xt_raw[];
@@ -1777,33 +1783,46 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
   const CacheRefs& c = a.c;
   const int g = a.g, qpg = a.qpg;
   uint64_t* rawf = reinterpret_cast<uint64_t*>(sm + kXtBars);  // [2] raw page landed (tx)
-  uint64_t* rawe = rawf + 2;    // [2] raw stage read by the 128 unpack threads
-  uint64_t* tfull = rawf + 4;   // [2] tiles of buffer s unpacked (128)
-  uint64_t* tempty = rawf + 6;  // [2] tiles of buffer s read by their MMAs (commit)
-  uint64_t* sfull = rawf + 8;   // S in TMEM (commit)
-  uint64_t* sfree = rawf + 9;   // S read by the 128 softmax threads
-  uint64_t* pfull = rawf + 10;  // P written, O rescaled (128)
-  uint64_t* pvdone = rawf + 11; // P V finished (commit)
-  uint64_t* done = rawf + 12;   // every MMA finished (commit)
-  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(rawf + 13);
+  uint64_t* rawe = rawf + 2;     // [2] raw stage read by the unpack warps
+  uint64_t* tfull = rawf + 4;    // [kXtTiles] tiles of buffer s unpacked
+  uint64_t* tempty = rawf + 8;   // [kXtTiles] tiles of buffer s read by their MMAs (commit)
+  uint64_t* sfull = rawf + 12;   // S in TMEM (commit)
+  uint64_t* sfree = rawf + 13;   // S read by the softmax warps
+  uint64_t* pfull = rawf + 14;   // P written, O rescaled
+  uint64_t* pvdone = rawf + 15;  // P V finished (commit)
+  uint64_t* done = rawf + 16;    // every MMA finished (commit)
+  uint64_t* qsm = rawf + 17;     // q' operands staged in shared memory (4 warps)
+  uint64_t* qtm = rawf + 18;     // q' operands in TMEM (4 warps)
+  uint64_t* xm = rawf + 19;      // [2] page maxima of both softmax halves written (8 warps)
+  uint64_t* xl = rawf + 21;      // the rows' l of both halves written (8 warps)
+  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(rawf + 22);
+  // arrivals counted per warp: a lane's accesses are ordered before its
+  // warp's one arrival by the warp barrier
   if (t == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&rawf[i], 1);
-      mbar_init(&rawe[i], 128);
-      mbar_init(&tfull[i], 128);
+      mbar_init(&rawe[i], 4);
+    }
+    for (int i = 0; i < kXtTiles; ++i) {
+      mbar_init(&tfull[i], 4);
       mbar_init(&tempty[i], 1);
     }
     mbar_init(sfull, 1);
-    mbar_init(sfree, 128);
-    mbar_init(pfull, 128);
+    mbar_init(sfree, 8);
+    mbar_init(pfull, 8);
+    mbar_init(&xm[0], 8);
+    mbar_init(&xm[1], 8);
+    mbar_init(xl, 8);
     mbar_init(pvdone, 1);
     mbar_init(done, 1);
+    mbar_init(qsm, 4);
+    mbar_init(qtm, 4);
     fence_mbar_init();
   }
   for (int i = t; i < 65536 / 16; i += kXtThreads)  // q' operands: rows without a query stay zero
     reinterpret_cast<uint4*>(sm + kXtQ)[i] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();  // the tensor core reads them
-  if (warp == 8) tmem_alloc(tmem_at, 256);
+  if (warp == 8) tmem_alloc(tmem_at, 512);
   griddep_wait();
   int L = a.ctx_len[b];
   if (L < 0) {
@@ -1863,6 +1882,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(qsm);
     // BF16 sink/recent tiles of this item, per query (original basis, mma.sync)
     const int sp = c.sink_page[b];
     const bool sink_ok = sp >= 0 && sp < c.num_sink;
@@ -1923,26 +1944,29 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
                                 kPartialFloats,
                         1.0f / kPScaleBF16, lane);
     }
-    // INT2 pages: unpack into tiles of buffer k % 2
+    // INT2 pages: raw stage k % 2 unpacked into the tiles of buffer k % kXtTiles
     bool timed_out = false;
     for (int k = 0; k < n_units; ++k) {
-      const int st = k & 1;
-      if (!mbar_wait_bounded(&rawf[st], (k >> 1) & 1, kXtWaitLimit) ||
-          !mbar_wait_bounded(&tempty[st], ((k >> 1) & 1) ^ 1, kXtWaitLimit)) {
+      const int rs = k & 1, st = k % kXtTiles;
+      if (!mbar_wait_bounded(&rawf[rs], (k >> 1) & 1, kXtWaitLimit) ||
+          !mbar_wait_bounded(&tempty[st], ((k / kXtTiles) & 1) ^ 1, kXtWaitLimit)) {
         set_error(a.err, kErrTimeout);
         timed_out = true;
         break;
       }
-      const uint8_t* rp = sm + kXtRaw + st * kBlockBytes;
+      const uint8_t* rp = sm + kXtRaw + rs * kBlockBytes;
       float* sc = reinterpret_cast<float*>(sm + kXtSc + st * 1024);
 #pragma unroll
       for (int x = 0; x < 4; ++x)
         ext_unpack<true>(rp, sm + kXtK + st * 16384, sm + kXtV + st * 16384, sc, sc + 128, u + 128 * x);
       fence_proxy_async_smem();
-      mbar_arrive(&tfull[st]);
-      mbar_arrive(&rawe[st]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tfull[st]);
+        mbar_arrive(&rawe[rs]);
+      }
       if (u == 0 && k + 2 < n_units) {
-        if (!mbar_wait_bounded(&rawe[st], (k >> 1) & 1, kXtWaitLimit)) {
+        if (!mbar_wait_bounded(&rawe[rs], (k >> 1) & 1, kXtWaitLimit)) {
           set_error(a.err, kErrTimeout);
           timed_out = true;
           break;
@@ -1956,13 +1980,13 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_f16_f32(128, 64);
       const uint64_t dhi = umma_desc_sw128(0) & 0xFFFFFFFF00000000ull;
-      const uint32_t q_lo = (uint32_t)umma_desc_sw128(sbase + kXtQ), p_lo = (uint32_t)umma_desc_sw128(sbase + kXtP);
       const uint32_t k_lo = (uint32_t)umma_desc_sw128(sbase + kXtK), v_lo = (uint32_t)umma_desc_sw128(sbase + kXtV);
-      const uint32_t tS = tbase, tO = tbase + 128;
-      bool ok = true;
+      // TMEM columns: S [2 groups][64 tokens], O [128 channels], q' [part][2 blocks][32], P [group][part][32]
+      const uint32_t tS = tbase, tO = tbase + 128, tQ = tbase + 256, tP = tbase + 384;
+      bool ok = mbar_wait_bounded(qtm, 0, kXtWaitLimit);
       // S = q' K^T of page k (tiles of buffer k % 2) for each 64-channel group
       auto issue_s = [&](int k) {
-        const int st = k & 1;
+        const int st = k % kXtTiles;
         tc_fence_after();
 #pragma unroll
         for (int gr = 0; gr < 2; ++gr)
@@ -1970,20 +1994,19 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
           for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
             for (int pt = 0; pt < 2; ++pt) {
-              const uint64_t ad = dhi | (q_lo + ((pt * 32768 + gr * 16384 + ks * 32) >> 4));
               const uint64_t bd = dhi | (k_lo + ((st * 16384 + gr * 8192 + ks * 32) >> 4));
-              umma_f16(tS + 64 * gr, ad, bd, idesc, ks > 0 || pt > 0);
+              umma_f16_ts(tS + 64 * gr, tQ + 64 * pt + 32 * gr + 8 * ks, bd, idesc, ks > 0 || pt > 0);
             }
         umma_commit(sfull);
       };
-      if (n_units > 0) {
+      if (ok && n_units > 0) {
         ok = mbar_wait_bounded(&tfull[0], 0, kXtWaitLimit);
         if (ok) issue_s(0);
       }
       for (int k = 0; k < n_units && ok; ++k) {
-        const int st = k & 1;
+        const int st = k % kXtTiles;
         if (k + 1 < n_units) {
-          ok = mbar_wait_bounded(&tfull[(k + 1) & 1], ((k + 1) >> 1) & 1, kXtWaitLimit) &&
+          ok = mbar_wait_bounded(&tfull[(k + 1) % kXtTiles], ((k + 1) / kXtTiles) & 1, kXtWaitLimit) &&
                mbar_wait_bounded(sfree, k & 1, kXtWaitLimit);
           if (!ok) break;
           issue_s(k + 1);
@@ -1998,9 +2021,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
           for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
             for (int pt = 0; pt < 2; ++pt) {
-              const uint64_t ad = dhi | (p_lo + (((2 * gr + pt) * 16384 + ks * 32) >> 4));
               const uint64_t bd = dhi | (v_lo + ((st * 16384 + gr * 8192 + ks * 32) >> 4));
-              umma_f16(tO + 64 * gr, ad, bd, idesc, k > 0 || ks > 0 || pt > 0);
+              umma_f16_ts(tO + 64 * gr, tP + 32 * (2 * gr + pt) + 8 * ks, bd, idesc, k > 0 || ks > 0 || pt > 0);
             }
         umma_commit(pvdone);
         umma_commit(&tempty[st]);
@@ -2011,19 +2033,47 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     }
     __syncwarp();
   } else {
-    // softmax: row r = t (TMEM lane) = query ql = r / g of the group, head n = r % g
-    const int r = t, ql = r / g, n = r % g, qi = grp * qpg + ql;
+    // softmax, two warpgroups: wg 0 (warps 0-3) takes tokens 0-31 of every page and O columns
+    // 0-63, wg 1 (warps 9-12) tokens 32-63 and columns 64-127.  Row r (TMEM lane 32 (warp % 4) +
+    // lane) = query ql = r / g of the group, head n = r % g; the two threads of a row swap their
+    // page maxima, so both keep the same running maximum.
+    const int wg = warp >= 9 ? 1 : 0;
+    const int r = 32 * (warp & 3) + lane, ql = r / g, n = r % g, qi = grp * qpg + ql;
     const bool active = ql < qpg && qi < a.chunk;
     const int qg = b * a.chunk + (active ? qi : 0);
     const int lim = active ? max(0, min(a.pos0[b] + qi + 1, L)) : 0;
     const int hlim = min(hist_end, lim);
     const float scaleE = active ? __ldg(a.qconst + ((size_t)qg * a.Hkv + h) * kQConstFloats + 16) : 0.f;
     const float kpl = log2f(a.pscale);
-    const uint32_t tS = tbase + ((uint32_t)(32 * warp) << 16), tO = tS + 128;
+    const uint32_t tS = tbase + ((uint32_t)(32 * (warp & 3)) << 16), tO = tS + 128, tQ = tS + 256, tP = tS + 384;
+    float* pmx = reinterpret_cast<float*>(sm + kXtX);  // [page parity][wg][128 rows] page maxima, then [wg][128] l
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int k = 0; k < n_units; ++k) {
-      const int st = k & 1;
+    if (wg == 0) {
+      // this row's q' (both parts, K order of the staged tiles) into TMEM: the A operand of S
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(qsm, 0, kXtWaitLimit));
+      if (ok) {
+#pragma unroll
+        for (int pb = 0; pb < 4; ++pb) {  // part pb / 2, block of 64 channels pb % 2
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sm + kXtQ + pb * 16384 + sw128_elem(r, 8 * j));
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
+          }
+          tmem_st32u(tQ + 32 * pb, w);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qtm);
+    }
+    for (int k = 0; k < n_units && ok; ++k) {
+      const int st = k % kXtTiles;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(sfull, k & 1, kXtWaitLimit))) {
         ok = false;
         break;
@@ -2031,46 +2081,54 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       tc_fence_after();
       const float* sc = reinterpret_cast<const float*>(sm + kXtSc + st * 1024);  // K: [64][2], V: [64][2]
       const int nv = min(kPage, hlim - kPage * (lp0 + k));
-      // raw logits (the q' scale 2^E applied in the exponent below); a warp whose
-      // rows all see the whole page skips the masking
+      // raw logits of this half page (the q' scale 2^E applied in the exponent below); a warp
+      // whose rows all see the whole page skips the masking
       const bool whole = __all_sync(0xffffffffu, nv >= kPage);
-      float lg[64];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      float lg[32];
+      {
         float s0[32], s1[32];
-        tmem_ld32(tS + 32 * hh, s0);
-        tmem_ld32(tS + 64 + 32 * hh, s1);
+        tmem_ld32x2(tS + 32 * wg, tS + 64 + 32 * wg, s0, s1);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int tk = 32 * hh + e;
+          const int tk = 32 * wg + e;
           const float x = fmaf(s0[e], sc[2 * tk], s1[e] * sc[2 * tk + 1]);
-          lg[tk] = (whole || tk < nv) ? x : -INFINITY;
+          lg[e] = (whole || tk < nv) ? x : -INFINITY;
         }
       }
       tc_fence_before();
-      mbar_arrive(sfree);
-      float mx = -INFINITY;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree);
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < 64; ++e) mx = fmaxf(mx, lg[e]);
-      mx *= scaleE;
+      for (int e = 0; e < 32; ++e) mq[e & 3] = fmaxf(mq[e & 3], lg[e]);
+      float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scaleE;
+      // the row's page maximum over both halves
+      pmx[((k & 1) * 2 + wg) * 128 + r] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xm[k & 1]);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&xm[k & 1], (k >> 1) & 1, kXtWaitLimit))) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, pmx[((k & 1) * 2 + (wg ^ 1)) * 128 + r]);
       if (k > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(pvdone, (k - 1) & 1, kXtWaitLimit))) {
         ok = false;  // (the wait: P buffer free, O settled)
         break;
       }
-      // lazy rescaling of this row's O; TMEM loads and stores are warp-wide (.sync.aligned), so
-      // every lane of the warp takes part whenever one needs it (factor 1 for the others)
+      // lazy rescaling of this row's half of O; TMEM loads and stores are warp-wide
+      // (.sync.aligned), so every lane of the warp takes part whenever one needs it
       const bool need = nv > 0 && mx > m + kLazy;
       const float nm = need ? fmaxf(m, mx) : m;
       const float al = (need && m != -INFINITY) ? ex2(m - nm) : 1.f;
       if (__any_sync(0xffffffffu, need && m != -INFINITY)) {
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float o[32];
-          tmem_ld32(tO + 32 * cc, o);
+          tmem_ld32(tO + 64 * wg + 32 * cc, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= al;
-          tmem_st32(tO + 32 * cc, o);
+          tmem_st32(tO + 64 * wg + 32 * cc, o);
         }
         tmem_wait_st();
       }
@@ -2078,13 +2136,14 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       m = nm;
       const float ms = nv > 0 ? m - kpl : 0.f;
       const float* vs = sc + 128;
+      // P (A operand of P V) into TMEM: matrix 2 G + part, column = token pair
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint32_t w[4][4];
+      for (int c16 = 0; c16 < 2; ++c16) {
+        uint32_t w[4][8];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int tk = 8 * c8 + e;
-          const float p0 = ex2(fmaf(lg[tk], scaleE, -ms)), p1 = ex2(fmaf(lg[tk + 1], scaleE, -ms));
+        for (int e = 0; e < 16; e += 2) {
+          const int el = 16 * c16 + e, tk = 32 * wg + el;
+          const float p0 = ex2(fmaf(lg[el], scaleE, -ms)), p1 = ex2(fmaf(lg[el + 1], scaleE, -ms));
           l += p0 + p1;
           const float a0 = p0 * vs[2 * tk], a1 = p1 * vs[2 * tk + 2];
           const float b0 = p0 * vs[2 * tk + 1], b1 = p1 * vs[2 * tk + 3];
@@ -2094,29 +2153,35 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
           w[3][e >> 1] = f16x2_residual(w[2][e >> 1], b0, b1);
         }
 #pragma unroll
-        for (int mtx = 0; mtx < 4; ++mtx)
-          *reinterpret_cast<uint4*>(sm + kXtP + mtx * 16384 + sw128_elem(r, 8 * c8)) =
-              make_uint4(w[mtx][0], w[mtx][1], w[mtx][2], w[mtx][3]);
+        for (int mtx = 0; mtx < 4; ++mtx) tmem_st8u(tP + 32 * mtx + 16 * wg + 8 * c16, w[mtx]);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(pfull);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull);
     }
     // the row's rotated-basis record (the TMEM loads warp-wide, the stores per row)
     if (ok && n_units > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(pvdone, (n_units - 1) & 1, kXtWaitLimit)))
       ok = false;
+    // the row's l over both halves
+    float* pl = pmx + 512;
+    pl[wg * 128 + r] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xl);
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(xl, 0, kXtWaitLimit))) ok = false;
+    l += pl[(wg ^ 1) * 128 + r];
     if (!ok) set_error(a.err, kErrTimeout);
     tc_fence_after();
     float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats;
-    if (active) {
+    if (active && wg == 0) {
       rec[n] = m;
       rec[8 + n] = l * a.inv_pscale;
     }
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < 2; ++cc) {
       float o[32];
       if (n_units > 0) {
-        tmem_ld32(tO + 32 * cc, o);
+        tmem_ld32(tO + 64 * wg + 32 * cc, o);
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0.f;
@@ -2124,7 +2189,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       if (active) {
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(rec + 16 + n * kStateStride + 32 * cc + e) =
+          *reinterpret_cast<float4*>(rec + 16 + n * kStateStride + 64 * wg + 32 * cc + e) =
               make_float4(o[e] * a.inv_pscale, o[e + 1] * a.inv_pscale, o[e + 2] * a.inv_pscale,
                           o[e + 3] * a.inv_pscale);
       }
@@ -2136,7 +2201,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
   __syncthreads();
   if (warp == 8) {
     tc_fence_after();
-    tmem_dealloc(tbase, 256);
+    tmem_dealloc(tbase, 512);
   }
   if (t == 0) {
     int ticket;
