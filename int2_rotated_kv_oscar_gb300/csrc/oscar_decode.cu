@@ -618,12 +618,17 @@ __device__ __forceinline__ void pv_tile(const uint8_t* __restrict__ blk, int T, 
 template <bool PACK4>
 __device__ __forceinline__ void int2_page_full(const uint8_t* __restrict__ blk, const uint32_t* qf, float E,
                                                float kp, WarpState& st, int lane) {
-  float z[4][4], p[4][4];
+  // g > 4: two tiles at a time (twice the logits per tile, and twice the q' fragments)
+  constexpr int NT = PACK4 ? 4 : 2;
 #pragma unroll
-  for (int T = 0; T < 4; ++T) qk_tile<PACK4>(blk, T, qf, z[T], lane);
-  softmax_weights<PACK4, false, 4>(z, E, kp, st, p);
+  for (int T0 = 0; T0 < 4; T0 += NT) {
+    float z[NT][4], p[NT][4];
 #pragma unroll
-  for (int T = 0; T < 4; ++T) pv_tile<PACK4, false>(blk, T, 16, p[T], st, lane);
+    for (int T = 0; T < NT; ++T) qk_tile<PACK4>(blk, T0 + T, qf, z[T], lane);
+    softmax_weights<PACK4, false, NT>(z, E, kp, st, p);
+#pragma unroll
+    for (int T = 0; T < NT; ++T) pv_tile<PACK4, false>(blk, T0 + T, 16, p[T], st, lane);
+  }
 }
 
 // One 16-token tile T with rows [0, nv) valid (a page's last tile, or a
