@@ -1562,16 +1562,29 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
       }
       const int pg0 = item * a.chunk_pages;
       const int pg1 = min(min(pg0 + a.chunk_pages, n_pages), c.max_pages);
+      // tile i of the item: page pg0 + i / 4, rows 16 (i % 4) ..; the page-table
+      // entry of the warp's tile two on is read a tile ahead, and the rows of
+      // its next tile are pulled into L2 while this one is computed
+      auto entry = [&](int i) { return pg0 + i / 4 < pg1 ? c.page_table[(size_t)b * c.max_pages + pg0 + i / 4] : -1; };
+      int ph_next = entry(warp + kWarps);
+      int ph = entry(warp);
       for (int i = warp; pg0 + i / 4 < pg1; i += kWarps) {
         const int pg = pg0 + i / 4, tile = i & 3;
-        const int ph = c.page_table[(size_t)b * c.max_pages + pg];
-        if (ph < 0 || ph >= c.num_pages) {
+        const int ph_cur = ph;
+        if (lane == 0 && ph_next >= 0 && ph_next < c.num_pages) {
+          const size_t offn = (((size_t)ph_next * a.Hkv + h) * kPage + 16 * ((i + kWarps) & 3)) * kD;
+          bulk_prefetch_l2(a.kb_pages + offn, 16 * kD * 2);
+          bulk_prefetch_l2(a.vb_pages + offn, 16 * kD * 2);
+        }
+        ph = ph_next;
+        ph_next = entry(i + 2 * kWarps);
+        if (ph_cur < 0 || ph_cur >= c.num_pages) {
           if (lane == 0) set_error(a.err, kErrPage);
           continue;
         }
         const int nv = min(16, L - kPage * pg - 16 * tile);
         if (nv <= 0) continue;
-        const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * tile) * kD;
+        const size_t off = (((size_t)ph_cur * a.Hkv + h) * kPage + 16 * tile) * kD;
         bf16_tile_raw(a.kb_pages + off, a.vb_pages + off, nv, qb, cE, st, lane);
       }
     }
