@@ -37,7 +37,7 @@ class Setup:
     """One context + one mixed cache on cuda:0 for a batch of requests."""
 
     def __init__(self, Hq, Hkv, lengths_max, batch, num_layers=1, cfg=1, flags=abi.OSCAR_ROT_ALL, seed=0,
-                 extra_pages=3, shuffle=True, calibrate=True, paged_recent=False):
+                 extra_pages=3, shuffle=True, calibrate=True, paged_recent=False, tau_scale=1.0):
         self.Hq, self.Hkv, self.batch, self.cfg = Hq, Hkv, batch, cfg
         self.flags = flags
         conf = abi.oscar_config(num_layers=num_layers, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
@@ -52,6 +52,8 @@ class Setup:
                 U_K = np.linalg.qr(r.standard_normal((128, 128)))[0].astype(np.float32)
                 U_V = np.linalg.qr(r.standard_normal((128, 128)))[0].astype(np.float32)
                 tk, tv = np.float32(30.0), np.float32(30.0)
+            # tau_scale < 1: thresholds below the calibrated ones, so that most groups clip
+            tk, tv = np.float32(tk * tau_scale), np.float32(tv * tau_scale)
             abi.oscar_load_rotation(self.ctx, layer, U_K, U_V, tk, tv, flags)
             R_K, R_V = rotations_for_oracle(U_K, U_V, flags)
             self.rot.append((R_K, R_V, float(tk), float(tv)))

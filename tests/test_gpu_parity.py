@@ -74,6 +74,31 @@ def test_c1_single_layer_prefill_append_decode():
         s.close()
 
 
+@pytest.mark.parametrize("Hq,Hkv,tau_scale", [(6, 3, 1.0), (6, 3, 0.25), (32, 8, 0.25)])
+def test_bulk_append_clipping_and_odd_head_counts(Hq, Hkv, tau_scale):
+    """Bulk prefill append with thresholds far below the calibrated ones (most groups clip, so
+    the codes come from the three comparisons rather than the floor of x / s + 2) and with 3 KV
+    heads (the BF16 rows' 16-byte copies cover heads t / 16, t / 16 + 8, ...): codes bit-exact,
+    BF16 rows exact, decode within the bound."""
+    cfg, L = 3, 2500
+    s = harness.Setup(Hq, Hkv, L, 1, cfg=cfg, tau_scale=tau_scale)
+    try:
+        k, v = _tokens(cfg, 0, Hkv, L)
+        s.append(0, k, v, [0], [0, L], L)
+        assert s.device_error() == 0
+        _check_bf16_rows(s, 0, 0, L, k, v)
+        _check_codes(s, 0, 0, L, k, v, "bulk Hkv=%d tau x %.2f" % (Hkv, tau_scale))
+        q = inputs.decode_queries_bf16(cfg, 0, 1, Hq)
+        out = s.decode(0, q, [L])
+        assert s.device_error() == 0
+        ref = s.oracle_decode(0, 0, L, q[0])
+        err = np.abs(out[0] - ref).max()
+        print("bulk Hkv=%d tau x %.2f: decode max-abs %.3e" % (Hkv, tau_scale, err))
+        assert err <= harness.DECODE_TOL
+    finally:
+        s.close()
+
+
 @pytest.mark.parametrize("L", [1, 63, 64, 65, 320, 321, 384, 1000, 4096])
 def test_edge_lengths_incremental(L):
     """Contexts built token by token through the decode append (eviction at every step past 320)."""
