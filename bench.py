@@ -770,7 +770,9 @@ def run_cuda(args):
         acache.page_table.copy_(torch.from_numpy(inputs.shuffled_pages(CFG, maxp_a, layer=1).reshape(1, maxp_a)))
         ka, va = inputs.kv_tokens_device(4, 0, HKV, inputs.STREAM_KV, n_b, dev)
         cu_a = torch.tensor([0, n_b], dtype=torch.int32, device=dev)
-        aargs = kvcache.append_args(ka, va, pos0, cu_a, n_b)
+        # a fresh prompt (position 0): nothing precedes it, so nothing is evicted -- the flag that
+        # says so, as a serving engine passes it for a new request's prefill
+        aargs = kvcache.append_args(ka, va, pos0, cu_a, n_b, fresh_ring=True)
         aview = acache.view(0)
         for _ in range(3):
             abi.oscar_kv_append(ctx, 0, aview, aargs, cur)
@@ -810,8 +812,9 @@ def run_cuda(args):
                            "note": "tcgen05 MMAs, M=128 tokens, K=16: per K step one N=256 (the t0 and t1 terms "
                                    "of R^T) and one N=128 (t2); R^T as three bf16 terms, so the tensor cores "
                                    "run x R three times to keep the codes exact"},
-                "note": "oscar_kv_append of one 131,072-token prompt (BF16 K and V in, INT2 history + BF16 "
-                        "sink/recent out), mean of 10 eager calls"}
+                "note": "oscar_kv_append of one fresh 131,072-token prompt (OSCAR_APPEND_FRESH_RING: "
+                        "nothing to evict; BF16 K and V in, INT2 history + BF16 sink/recent out), mean of 10 "
+                        "eager calls"}
         del acache, ka, va
 
     # ---- extend attention: the queries of a 16-token chunk at the end of the context, one layer

@@ -93,11 +93,9 @@ __global__ void __launch_bounds__(2 * kQuantThreads, 1) append_evict_kernel(Appe
 
 // Phase 2a: new tokens that stay BF16 (sink rows, ring rows).
 // grid (320, B), 128 threads; all KV heads of one position per block.
-__global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
-  // the tile kernel may start (it touches no BF16 row); the ring rows written
-  // here are the ones the eviction kernel before this one reads
-  griddep_launch_dependents();
-  griddep_wait();
+// The BF16 rows of new tokens: sink positions into the sink page, the last
+// 256 positions into the ring (or the recent pages).
+__device__ __forceinline__ void bf16_rows(const AppendLaunch& a) {
   // block x: one position of request blockIdx.y; thread t: 16 bytes (channels
   // 8 (t % 16) ..) of KV head t / 16, t / 16 + 8, ...
   const int x = blockIdx.x, b = blockIdx.y, t = threadIdx.x, c8 = 8 * (t & 15);
@@ -129,6 +127,19 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
     if (!recent_row(c, b, h, p, d, a.err, (t & 15) == 0)) continue;
     copy(h, p, c.k_ring, c.v_ring, d);
   }
+}
+
+__global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
+  // Evicting: the tile kernel after this one may start (it touches no BF16
+  // row), and the ring rows written here are the ones the eviction kernel
+  // before this one reads, so wait for it first.  Fresh ring: this kernel
+  // runs beside the tile kernel before it and waits for it at the end, so
+  // that its end marks the call's.
+  const bool fresh = (a.flags & 1u) != 0;
+  griddep_launch_dependents();
+  if (!fresh) griddep_wait();
+  bf16_rows(a);
+  if (fresh) griddep_wait();
 }
 
 // Phase 2b: new tokens that go straight into the INT2 history.
@@ -223,6 +234,8 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
 __global__ void __launch_bounds__(kTcThreads, 1)
     append_tile_kernel(const __grid_constant__ AppendLaunch a, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, unsigned tiles2) {
+  // the kernel after this one may start beside it (it waits before it reads what this one writes)
+  griddep_launch_dependents();
   extern __shared__ uint8_t tc_raw[];
   const uint32_t raw_s = smem_u32(tc_raw);
   uint8_t* sm = tc_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -432,12 +445,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float v[32], w[32];
         const uint32_t ta = tbase + ((uint32_t)(32 * q) << 16) + 256 * bb + 64 * g + 32 * h;
         tmem_ld32x2(ta, ta + 128, v, w);
+        // the buffer is free once the loads have landed: the next tile's MMAs may start
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[bb]);
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[e] = v[e] + w[e];
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[bb]);
       float mq[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
       for (int e = 0; e < 32; ++e) mq[e & 3] = fmaxf(mq[e & 3], fabsf(x[e]));
@@ -535,22 +549,20 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
     return cudaGetLastError();
   }
   // The first kernel of the call starts after everything before it; the next
-  // ones may start early and overlap it (the tile kernel writes only INT2
-  // rows of the new tokens, which the eviction and BF16-row kernels do not
-  // touch).
+  // ones may start early and run beside it.  The tile kernel writes only the
+  // INT2 rows of new tokens, which the eviction and BF16-row kernels do not
+  // touch; the eviction reads ring rows that the BF16-row kernel overwrites.
+  //   evicting:     eviction -> BF16 rows (wait first) -> tiles (wait at the end)
+  //   fresh ring:   tiles -> BF16 rows (wait at the end)
+  // so the last kernel of the call always ends after the others.
   AppendLaunch la = a;
   void* args1[] = {&la};
-  cudaError_t e0;
-  if (!(a.flags & 1u)) {
-    append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
-    e0 = launch_pdl(reinterpret_cast<const void*>(append_bf16_kernel), dim3(kSink + kRecent, B), dim3(128), 0,
-                    stream, args1);
-  } else {
+  const bool fresh = (a.flags & 1u) != 0;
+  if (a.n_tokens == 0) {
+    if (!fresh) append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
     append_bf16_kernel<<<dim3(kSink + kRecent, B), 128, 0, stream>>>(a);
-    e0 = cudaGetLastError();
+    return cudaGetLastError();
   }
-  if (e0 != cudaSuccess) return e0;
-  if (a.n_tokens == 0) return cudaGetLastError();
   const int pages = (a.max_tokens_per_req + kPage - 1) / kPage + 1;  // INT2 pages a request can touch
   const int tiles2 = (pages + 1) / 2;                                    // page pairs
   if ((long long)tiles2 * Hkv * B >= (1ll << 31)) return cudaErrorInvalidValue;
@@ -588,8 +600,19 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   const int blocks = 2 * (int)std::min<long long>(per_matrix, std::max(1, sms / 2));
   unsigned t2 = (unsigned)tiles2;
   void* args[] = {&la, &tm[0], &tm[1], &t2};
-  return launch_pdl(reinterpret_cast<const void*>(append_tile_kernel), dim3(blocks), dim3(kTcThreads), kTcSmem, stream,
-                    args);
+  const void* tile_fn = reinterpret_cast<const void*>(append_tile_kernel);
+  const void* bf16_fn = reinterpret_cast<const void*>(append_bf16_kernel);
+  if (fresh) {
+    append_tile_kernel<<<blocks, kTcThreads, kTcSmem, stream>>>(a, tm[0], tm[1], t2);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pdl(bf16_fn, dim3(kSink + kRecent, B), dim3(128), 0, stream, args1);
+  }
+  append_evict_kernel<<<dim3(kRecent, Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_pdl(bf16_fn, dim3(kSink + kRecent, B), dim3(128), 0, stream, args1);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tile_fn, dim3(blocks), dim3(kTcThreads), kTcSmem, stream, args);
 }
 
 }  // namespace oscar
