@@ -430,6 +430,18 @@ oscar_status oscar_calib_clip_threshold(oscar_ctx* ctx, const float* x, int64_t 
  * (may be NULL).  Returns OSCAR_ERR_DEVICE_CHECK when any bit was set. */
 oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bits);
 
+/*
+ * Self-test of the failure path (no page passage: a library service).  One
+ * block waits, with the same bounded wait the kernels use on their copies and
+ * barriers, on a shared-memory barrier that nothing completes; after `polls`
+ * polls (1 .. 2^18, the kernels' own limit: about a second) it gives up,
+ * sets OSCAR_DEVERR_TIMEOUT in the context's device error word and returns,
+ * leaving nothing in flight.  The context stays usable.  Asynchronous on `stream`; read the result with
+ * oscar_check_device_error.  Errors: OSCAR_ERR_INVALID_ARG (null context,
+ * polls out of range), OSCAR_ERR_CUDA.
+ */
+oscar_status oscar_selftest_bounded_wait(oscar_ctx* ctx, uint32_t polls, void* stream);
+
 /* Number of SMs of the context's device (used to size launch grids). */
 int32_t oscar_device_sm_count(const oscar_ctx* ctx);
 

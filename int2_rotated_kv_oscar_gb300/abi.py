@@ -113,6 +113,7 @@ SIGNATURES = {
                                                   ctypes.c_uint32, ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "oscar_check_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "oscar_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]),
     "oscar_device_sm_count": (ctypes.c_int32, [ctypes.c_void_p]),
     "oscar_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -266,6 +267,11 @@ def oscar_calib_clip_threshold(ctx, x, n_rows, U, flags, percentile, workspace, 
                                              ctypes.byref(tau), _ptr(workspace), workspace_bytes, _stream(stream)),
            "oscar_calib_clip_threshold")
     return float(tau.value)
+
+
+def oscar_selftest_bounded_wait(ctx, polls, stream=None):
+    """One bounded wait on a barrier nothing completes (sets OSCAR_DEVERR_TIMEOUT)."""
+    _check(load().oscar_selftest_bounded_wait(ctx, int(polls), _stream(stream)), "oscar_selftest_bounded_wait")
 
 
 def oscar_check_device_error(ctx, stream=None):

@@ -577,6 +577,14 @@ oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bi
   return v ? OSCAR_ERR_DEVICE_CHECK : OSCAR_OK;
 }
 
+oscar_status oscar_selftest_bounded_wait(oscar_ctx* ctx, uint32_t polls, void* stream) {
+  if (ctx == nullptr || polls == 0 || polls > (1u << 18)) return OSCAR_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->cfg.device);
+  return oscar::launch_selftest_wait(ctx->d_err, polls, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? OSCAR_OK
+             : OSCAR_ERR_CUDA;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

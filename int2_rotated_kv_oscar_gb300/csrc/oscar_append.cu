@@ -542,6 +542,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace
 
+namespace {
+// The failure path of every asynchronous wait: a barrier that nothing
+// completes, a bounded wait that gives up, the timeout bit, a normal return.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(unsigned* err, unsigned polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bar, 0, polls)) && threadIdx.x == 0) set_error(err, kErrTimeout);
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(unsigned* err, unsigned polls, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err, polls);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   const int B = a.c.batch, Hkv = a.c.num_kv_heads;
   if (a.cu_seqlens == nullptr) {

@@ -1777,7 +1777,7 @@ __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* sm
 //        into double-buffered tiles
 //   8    TMEM (512 columns: S, O, q', P) and the MMA thread
 constexpr int kXtThreads = 13 * 32;
-constexpr unsigned kXtWaitLimit = 1u << 18;  // polls per wait: a broken hand-off ends in well under a second
+constexpr unsigned kXtWaitLimit = kWaitLimit;  // polls per wait: a broken hand-off ends in about a second
 constexpr uint32_t kXtQ = 0;             // q' value / residual: 2 x [2 blocks of 64 channels][128 rows][128 B]
 constexpr int kXtTiles = 4;              // unpacked-page buffers (the MMAs of a page hold theirs until P V)
 constexpr uint32_t kXtK = 65536;         // K tiles: kXtTiles x [2 blocks of 64 channels][64 tokens][128 B]

@@ -31,8 +31,11 @@ constexpr int kVScales = 4352;
 // device error word bits (mirror of the public OSCAR_DEVERR_* values)
 constexpr unsigned kErrPage = 1u, kErrSink = 2u, kErrRing = 4u, kErrLength = 8u, kErrTokens = 16u,
                    kErrTimeout = 32u;
-// polls of an mbarrier before a wait gives up and reports kErrTimeout
-constexpr unsigned kWaitLimit = 1u << 22;
+// polls of an mbarrier before a wait gives up and reports kErrTimeout: an
+// unsuccessful poll suspends the thread for a few microseconds (~3.8 us
+// measured on a barrier that never completes), so a broken hand-off ends in
+// about a second; the waits of a working kernel last microseconds
+constexpr unsigned kWaitLimit = 1u << 18;
 
 
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) { atomicOr(err, bits); }

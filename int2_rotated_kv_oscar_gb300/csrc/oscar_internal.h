@@ -77,6 +77,9 @@ struct AppendLaunch {
 
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
 
+// One block's bounded wait on a barrier nothing completes: sets the timeout bit in *err.
+cudaError_t launch_selftest_wait(unsigned* err, unsigned polls, cudaStream_t stream);
+
 // A launch that may start once the kernel before it in the stream has let its
 // dependents go (griddepcontrol.launch_dependents) or has finished; the kernel
 // waits (griddepcontrol.wait) before it touches what that kernel writes.

@@ -62,6 +62,7 @@ def test_host_checks_need_no_gpu(lib):
     assert lib.oscar_decode_attention(None, 0, None, None, None, 0, None) == 1
     assert lib.oscar_decode_workspace_bytes(None, 1, 10) == 0
     assert lib.oscar_check_device_error(None, None, None) == 1
+    assert lib.oscar_selftest_bounded_wait(None, 1024, None) == 1
     assert lib.oscar_device_sm_count(None) == 0
     # calibration: sizes out of range give 0 bytes, null arguments are rejected
     assert lib.oscar_calib_workspace_bytes(0, 1, 1, 1) == 0
