@@ -176,9 +176,9 @@ __device__ __forceinline__ void rotate_heads(PrepSmem& sm, RowOf rk, int t, int 
 // q[b][h g + n][u % 128] for n = u / 128 and u / 128 + 4 below g.  Outputs:
 // the history and BF16 fragment words (kQFragWords each) and the constants
 // (kQConstFloats).
-template <typename RowOf, typename QOf>
+template <typename RowOf, typename QOf, typename Mid>
 __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u, RowOf rk, QOf qbits, PrepSmem& sm,
-                                          int bar, uint32_t* qf, uint32_t* qpl, float* qc) {
+                                          int bar, uint32_t* qf, uint32_t* qpl, float* qc, Mid mid) {
   const int t = u & 127, kq = u >> 7, lane = u & 31, warp = u >> 5;
   const int g = a.g;
   const bool packed = g <= 4;
@@ -197,6 +197,7 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
   constexpr int kW = kPrepThreads / 32;
   if (lane == 0) sm.red[warp] = ss;
   group_sync(bar, kPrepThreads);
+  mid();  // the caller's work that may wait on loads issued before (every thread)
   const bool dense = (a.rot_flags & kRotU) != 0;
   if (dense) {
     if (packed)
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(PrepArgs a) {
   const uint16_t* qrow = a.q + ((size_t)b * a.Hq + h * a.g) * kD + (u & 127);
   prep_body(a, b, h, u, [&](int ii) { return RK[ii * kD]; }, [&](int n) { return qrow[(size_t)n * kD]; }, sm, 1,
             a.qfrag + (size_t)bh * kQFragWords, a.qplain + (size_t)bh * kQFragWords,
-            a.qconst + (size_t)bh * kQConstFloats);
+            a.qconst + (size_t)bh * kQConstFloats, [] {});
 }
 
 // ------------------------------------------------------------------ decode
@@ -1205,6 +1206,16 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
     for (int ii = 0; ii < 32; ++ii) rk[ii] = __ldg(RK + ii * kD);
   }
   griddep_wait();
+  // fused step: the first units' page-table entries, read before the length is known (they
+  // are whole pages lp0 + warp + kWarps k whenever the item has more than kStages rounds; the
+  // entries are used only then)
+  int spec_ph[kStages + 1];
+  if constexpr (FUSED) {
+    const int lps = 1 + item * a.chunk_pages + warp;
+#pragma unroll
+    for (int k = 0; k <= kStages; ++k)
+      spec_ph[k] = lps + kWarps * k < c.max_pages ? c.page_table[(size_t)b * c.max_pages + lps + kWarps * k] : -1;
+  }
   int L = a.ctx_len[b];
   if (L < 0) {
     if (t == 0 && item == 0) set_error(a.err, kErrLength);
@@ -1331,12 +1342,24 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
     // unit k waits on nothing.
     uint32_t valid = 0;
     int ph_ahead = -1, ph_late = -1;
+    int phs[kStages];
+    // the first units' page-table entries (fused step with enough rounds: those read right
+    // after the wait), then their copies -- in the fused step from inside the q rotation, so
+    // that neither the entries nor the copies hold up its start
     if (n_my > 0) {
-      // the entries first: the copies' asm keeps later loads from moving above them
-      int phs[kStages];
+      if (FUSED && R > kStages) {
+        auto checked = [&](int ph) { return (ph >= 0 && ph < c.num_pages) ? ph : -1; };
 #pragma unroll
-      for (int k = 0; k < kStages; ++k) phs[k] = k < n_my ? phys_unit(k) : -1;
-      if (kStages < n_my) ph_ahead = phys_unit(kStages);
+        for (int k = 0; k < kStages; ++k) phs[k] = checked(spec_ph[k]);
+        ph_ahead = checked(spec_ph[kStages]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kStages; ++k) phs[k] = k < n_my ? phys_unit(k) : -1;
+        if (kStages < n_my) ph_ahead = phys_unit(kStages);
+      }
+    }
+    auto first_copies = [&]() {
+      if (n_my <= 0) return;
 #pragma unroll
       for (int k = 0; k < kStages; ++k) {
         if (k >= n_my) break;
@@ -1347,7 +1370,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
           ph_late = phs[k];
         }
       }
-    }
+    };
+    if (!FUSED) first_copies();
     uint32_t qf[kQW], qpf[kQW];
     float scaleE = 0.f, scaleEp = 0.f;
     const bool bf16_warp = kWarps - 1 - warp < kBf16Slots;
@@ -1356,7 +1380,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
       RowPatch* patch = reinterpret_cast<RowPatch*>(smem + kPatchOffset);
       prep_body(
           f->pr, b, h, t, [&](int ii) { return rk[ii]; }, [&](int n) { return n == (t >> 7) ? qb0 : qb1; }, fs.prep,
-          1, fs.qf, fs.qpl, fs.qc);
+          1, fs.qf, fs.qpl, fs.qc, first_copies);
       // the append, by the block whose pages hold the evicted token's row (else item 0)
       if (item == owner) {
         if (t == 0) patch->row = -1;
