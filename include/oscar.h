@@ -432,11 +432,13 @@ oscar_status oscar_check_device_error(oscar_ctx* ctx, void* stream, uint32_t* bi
 
 /*
  * Self-test of the failure path (no page passage: a library service).  One
- * block waits, with the same bounded wait the kernels use on their copies and
- * barriers, on a shared-memory barrier that nothing completes; after `polls`
- * polls (1 .. 2^18, the kernels' own limit: about a second) it gives up,
- * sets OSCAR_DEVERR_TIMEOUT in the context's device error word and returns,
- * leaving nothing in flight.  The context stays usable.  Asynchronous on `stream`; read the result with
+ * block runs both bounded waits the kernels use on their copies and barriers,
+ * each on a shared-memory barrier that nothing completes: the polled wait
+ * gives up after `polls` polls (1 .. 2^18, the kernels' own limit: about a
+ * second), the timed wait (the chunk-extend kernel's) after polls x 4 us on
+ * the global timer.  When both have given up it sets OSCAR_DEVERR_TIMEOUT in
+ * the context's device error word and returns, leaving nothing in flight.
+ * The context stays usable.  Asynchronous on `stream`; read the result with
  * oscar_check_device_error.  Errors: OSCAR_ERR_INVALID_ARG (null context,
  * polls out of range), OSCAR_ERR_CUDA.
  */

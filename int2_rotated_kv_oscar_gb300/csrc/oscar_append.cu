@@ -545,19 +545,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 namespace {
 // The failure path of every asynchronous wait: a barrier that nothing
 // completes, a bounded wait that gives up, the timeout bit, a normal return.
-__global__ void __launch_bounds__(32) selftest_wait_kernel(unsigned* err, unsigned polls) {
-  __shared__ uint64_t bar;
+// Warp 0 runs the polled wait (`polls` polls), warp 1 the timed wait (polls x 4 us on the
+// global timer), each on its own barrier that nothing completes; the error bit is set only
+// when both give up.
+__global__ void __launch_bounds__(64) selftest_wait_kernel(unsigned* err, unsigned polls) {
+  __shared__ uint64_t bar[2];
+  __shared__ int gave_up[2];
+  const int w = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
     fence_mbar_init();
   }
-  __syncwarp();
-  if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bar, 0, polls)) && threadIdx.x == 0) set_error(err, kErrTimeout);
+  __syncthreads();
+  const bool ok = w == 0 ? mbar_wait_bounded(&bar[0], 0, polls)
+                         : mbar_wait_timed(&bar[1], 0, 4000ull * polls);
+  const bool all_ok = __all_sync(0xffffffffu, ok);
+  if ((threadIdx.x & 31) == 0) gave_up[w] = all_ok ? 0 : 1;
+  __syncthreads();
+  if (threadIdx.x == 0 && gave_up[0] && gave_up[1]) set_error(err, kErrTimeout);
 }
 }  // namespace
 
 cudaError_t launch_selftest_wait(unsigned* err, unsigned polls, cudaStream_t stream) {
-  selftest_wait_kernel<<<1, 32, 0, stream>>>(err, polls);
+  selftest_wait_kernel<<<1, 64, 0, stream>>>(err, polls);
   return cudaGetLastError();
 }
 

@@ -1801,7 +1801,6 @@ __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* sm
 //        into double-buffered tiles
 //   8    TMEM (512 columns: S, O, q', P) and the MMA thread
 constexpr int kXtThreads = 13 * 32;
-constexpr unsigned kXtWaitLimit = kWaitLimit;  // polls per wait: a broken hand-off ends in about a second
 constexpr uint32_t kXtQ = 0;             // q' value / residual: 2 x [2 blocks of 64 channels][128 rows][128 B]
 constexpr int kXtTiles = 4;              // unpacked-page buffers (the MMAs of a page hold theirs until P V)
 constexpr uint32_t kXtK = 65536;         // K tiles: kXtTiles x [2 blocks of 64 channels][64 tokens][128 B]
@@ -1990,8 +1989,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     bool timed_out = false;
     for (int k = 0; k < n_units; ++k) {
       const int rs = k & 1, st = k % kXtTiles;
-      if (!mbar_wait_bounded(&rawf[rs], (k >> 1) & 1, kXtWaitLimit) ||
-          !mbar_wait_bounded(&tempty[st], ((k / kXtTiles) & 1) ^ 1, kXtWaitLimit)) {
+      if (!mbar_wait_timed(&rawf[rs], (k >> 1) & 1, kWaitNs) ||
+          !mbar_wait_timed(&tempty[st], ((k / kXtTiles) & 1) ^ 1, kWaitNs)) {
         set_error(a.err, kErrTimeout);
         timed_out = true;
         break;
@@ -2008,7 +2007,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         mbar_arrive(&rawe[rs]);
       }
       if (u == 0 && k + 2 < n_units) {
-        if (!mbar_wait_bounded(&rawe[rs], (k >> 1) & 1, kXtWaitLimit)) {
+        if (!mbar_wait_timed(&rawe[rs], (k >> 1) & 1, kWaitNs)) {
           set_error(a.err, kErrTimeout);
           timed_out = true;
           break;
@@ -2017,7 +2016,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       }
     }
     if (u == 0 && timed_out)  // copies may still be in flight
-      for (int k = 0; k < min(2, n_units); ++k) mbar_wait_bounded(&rawf[k], 0, kXtWaitLimit);
+      for (int k = 0; k < min(2, n_units); ++k) mbar_wait_timed(&rawf[k], 0, kWaitNs);
   } else if (warp == 8) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_f16_f32(128, 64);
@@ -2025,7 +2024,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       const uint32_t k_lo = (uint32_t)umma_desc_sw128(sbase + kXtK), v_lo = (uint32_t)umma_desc_sw128(sbase + kXtV);
       // TMEM columns: S [2 groups][64 tokens], O [128 channels], q' [part][2 blocks][32], P [group][part][32]
       const uint32_t tS = tbase, tO = tbase + 128, tQ = tbase + 256, tP = tbase + 384;
-      bool ok = mbar_wait_bounded(qtm, 0, kXtWaitLimit);
+      bool ok = mbar_wait_timed(qtm, 0, kWaitNs);
       // S = q' K^T of page k (tiles of buffer k % 2) for each 64-channel group
       auto issue_s = [&](int k) {
         const int st = k % kXtTiles;
@@ -2042,18 +2041,18 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         umma_commit(sfull);
       };
       if (ok && n_units > 0) {
-        ok = mbar_wait_bounded(&tfull[0], 0, kXtWaitLimit);
+        ok = mbar_wait_timed(&tfull[0], 0, kWaitNs);
         if (ok) issue_s(0);
       }
       for (int k = 0; k < n_units && ok; ++k) {
         const int st = k % kXtTiles;
         if (k + 1 < n_units) {
-          ok = mbar_wait_bounded(&tfull[(k + 1) % kXtTiles], ((k + 1) / kXtTiles) & 1, kXtWaitLimit) &&
-               mbar_wait_bounded(sfree, k & 1, kXtWaitLimit);
+          ok = mbar_wait_timed(&tfull[(k + 1) % kXtTiles], ((k + 1) / kXtTiles) & 1, kWaitNs) &&
+               mbar_wait_timed(sfree, k & 1, kWaitNs);
           if (!ok) break;
           issue_s(k + 1);
         }
-        ok = mbar_wait_bounded(pfull, k & 1, kXtWaitLimit);
+        ok = mbar_wait_timed(pfull, k & 1, kWaitNs);
         if (!ok) break;
         tc_fence_after();
         // O[:, 64 G ..] += P_G V^T[64 G ..]: value and residual parts, 4 steps of 16 tokens
@@ -2071,7 +2070,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       }
       if (!ok) set_error(a.err, kErrTimeout);
       umma_commit(done);
-      if (!mbar_wait_bounded(done, 0, kXtWaitLimit)) set_error(a.err, kErrTimeout);
+      if (!mbar_wait_timed(done, 0, kWaitNs)) set_error(a.err, kErrTimeout);
     }
     __syncwarp();
   } else {
@@ -2093,7 +2092,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     bool ok = true;
     if (wg == 0) {
       // this row's q' (both parts, K order of the staged tiles) into TMEM: the A operand of S
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(qsm, 0, kXtWaitLimit));
+      ok = __all_sync(0xffffffffu, mbar_wait_timed(qsm, 0, kWaitNs));
       if (ok) {
 #pragma unroll
         for (int pb = 0; pb < 4; ++pb) {  // part pb / 2, block of 64 channels pb % 2
@@ -2116,7 +2115,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     }
     for (int k = 0; k < n_units && ok; ++k) {
       const int st = k % kXtTiles;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(sfull, k & 1, kXtWaitLimit))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_timed(sfull, k & 1, kWaitNs))) {
         ok = false;
         break;
       }
@@ -2148,12 +2147,12 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       pmx[((k & 1) * 2 + wg) * 128 + r] = mx;
       __syncwarp();
       if (lane == 0) mbar_arrive(&xm[k & 1]);
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&xm[k & 1], (k >> 1) & 1, kXtWaitLimit))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_timed(&xm[k & 1], (k >> 1) & 1, kWaitNs))) {
         ok = false;
         break;
       }
       mx = fmaxf(mx, pmx[((k & 1) * 2 + (wg ^ 1)) * 128 + r]);
-      if (k > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(pvdone, (k - 1) & 1, kXtWaitLimit))) {
+      if (k > 0 && !__all_sync(0xffffffffu, mbar_wait_timed(pvdone, (k - 1) & 1, kWaitNs))) {
         ok = false;  // (the wait: P buffer free, O settled)
         break;
       }
@@ -2203,14 +2202,14 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       if (lane == 0) mbar_arrive(pfull);
     }
     // the row's rotated-basis record (the TMEM loads warp-wide, the stores per row)
-    if (ok && n_units > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(pvdone, (n_units - 1) & 1, kXtWaitLimit)))
+    if (ok && n_units > 0 && !__all_sync(0xffffffffu, mbar_wait_timed(pvdone, (n_units - 1) & 1, kWaitNs)))
       ok = false;
     // the row's l over both halves
     float* pl = pmx + 512;
     pl[wg * 128 + r] = l;
     __syncwarp();
     if (lane == 0) mbar_arrive(xl);
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(xl, 0, kXtWaitLimit))) ok = false;
+    if (!__all_sync(0xffffffffu, mbar_wait_timed(xl, 0, kWaitNs))) ok = false;
     l += pl[(wg ^ 1) * 128 + r];
     if (!ok) set_error(a.err, kErrTimeout);
     tc_fence_after();

@@ -174,6 +174,41 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   return false;
 }
 
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// try_wait with a suspend-time hint: the thread may stay suspended for up to
+// kSuspendNs and resumes as soon as the phase completes.
+constexpr unsigned kSuspendNs = 10000000u;  // 10 ms
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Timed wait: gives up once limit_ns have passed on the global timer (or
+// after 2^24 polls, should the timer not advance).  A waiting warp stays
+// suspended rather than polling, which leaves its issue slots to the warps
+// that work; used by the kernels whose roles hand off every few hundred
+// nanoseconds.
+constexpr unsigned long long kWaitNs = 1000000000ull;  // a broken hand-off ends in about a second
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, unsigned parity, unsigned long long limit_ns) {
+  if (mbar_try_wait_suspend(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (unsigned i = 0; i < (1u << 24); ++i) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
 // Untiled bulk copy global -> shared (TMA), completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {

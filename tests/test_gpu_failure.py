@@ -1,11 +1,12 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
 Every asynchronous wait of the kernels (a bulk or tensor copy landing, a
-barrier between warp roles) polls a bounded number of times, then sets
-OSCAR_DEVERR_TIMEOUT in the context's device error word, skips the rest of its
-work and returns.  `oscar_selftest_bounded_wait` runs that path on a barrier
-that nothing completes; the host reads the bit, and the same context then
-appends and decodes as before, against the oracle.
+barrier between warp roles) is bounded, by a number of polls or by time on the
+global timer, then sets OSCAR_DEVERR_TIMEOUT in the context's device error
+word, skips the rest of its work and returns.  `oscar_selftest_bounded_wait`
+runs both kinds on barriers that nothing completes and sets the bit only when
+both gave up; the host reads it, and the same context then appends and decodes
+as before, against the oracle.
 """
 
 import time
@@ -34,7 +35,7 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
             abi.oscar_selftest_bounded_wait(s.ctx, polls, torch.cuda.current_stream())
             bits = s.device_error()
             dt = time.perf_counter() - t0
-            print("a bounded wait of %d polls gave up after %.2f ms (host-timed)" % (polls, 1e3 * dt))
+            print("bounded waits of %d polls / %d us gave up after %.2f ms (host-timed)" % (polls, 4 * polls, 1e3 * dt))
             assert bits == abi.OSCAR_DEVERR_TIMEOUT
         assert s.device_error() == 0  # read and cleared
         with pytest.raises(abi.OscarError):
