@@ -405,14 +405,13 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = pack_f16x2(x0 - h.x, x1 - h.y);
 }
 
-// The fp16 pair of the rounding residuals (x0 - h0, x1 - h1) of an fp16 pair
-// h = (h0, h1) = fp16(x0, x1): the halves' signs flipped, two mixed-precision
-// adds (exact in fp32), one pack.
-__device__ __forceinline__ uint32_t f16x2_residual(uint32_t h, float x0, float x1) {
+// The rounding residuals of an fp16 pair h = fp16(x0, x1), negated: (h0 - x0,
+// h1 - x1) as an fp16 pair, by two mixed-precision subtractions (exact in
+// fp32) and one pack; the MMA that reads them negates its A operand.
+__device__ __forceinline__ uint32_t f16x2_negres(uint32_t h, float x0, float x1) {
   uint32_t r;
-  asm("{\n .reg .b16 lo, hi;\n .reg .b32 nh;\n .reg .f32 r0, r1;\n"
-      " xor.b32 nh, %1, 0x80008000;\n mov.b32 {lo, hi}, nh;\n"
-      " add.rn.f32.f16 r0, lo, %2;\n add.rn.f32.f16 r1, hi, %3;\n"
+  asm("{\n .reg .b16 lo, hi;\n .reg .f32 r0, r1;\n mov.b32 {lo, hi}, %1;\n"
+      " sub.rn.f32.f16 r0, lo, %2;\n sub.rn.f32.f16 r1, hi, %3;\n"
       " cvt.rn.f16x2.f32 %0, r1, r0;\n}"
       : "=r"(r)
       : "r"(h), "f"(x0), "f"(x1));
@@ -2055,7 +2054,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         ok = mbar_wait_timed(pfull, k & 1, kWaitNs);
         if (!ok) break;
         tc_fence_after();
-        // O[:, 64 G ..] += P_G V^T[64 G ..]: value and residual parts, 4 steps of 16 tokens
+        // O[:, 64 G ..] += P_G V^T[64 G ..]: value and residual parts, 4 steps of 16 tokens (the
+        // residual matrices hold the residuals negated; bit 13 of the descriptor negates A)
 #pragma unroll
         for (int gr = 0; gr < 2; ++gr)
 #pragma unroll
@@ -2063,7 +2063,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
 #pragma unroll
             for (int pt = 0; pt < 2; ++pt) {
               const uint64_t bd = dhi | (v_lo + ((st * 16384 + gr * 8192 + ks * 32) >> 4));
-              umma_f16_ts(tO + 64 * gr, tP + 32 * (2 * gr + pt) + 8 * ks, bd, idesc, k > 0 || ks > 0 || pt > 0);
+              umma_f16_ts(tO + 64 * gr, tP + 32 * (2 * gr + pt) + 8 * ks, bd, pt ? (idesc | (1u << 13)) : idesc,
+                          k > 0 || ks > 0 || pt > 0);
             }
         umma_commit(pvdone);
         umma_commit(&tempty[st]);
@@ -2132,8 +2133,13 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int tk = 32 * wg + e;
-          const float x = fmaf(s0[e], sc[2 * tk], s1[e] * sc[2 * tk + 1]);
-          lg[e] = (whole || tk < nv) ? x : -INFINITY;
+          const float2 k2 = *reinterpret_cast<const float2*>(sc + 2 * tk);
+          lg[e] = fmaf(s0[e], k2.x, s1[e] * k2.y);
+        }
+        if (!whole) {  // rows past the query's limit or the history end
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * wg + e >= nv) lg[e] = -INFINITY;
         }
       }
       tc_fence_before();
@@ -2177,7 +2183,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       m = nm;
       const float ms = nv > 0 ? m - kpl : 0.f;
       const float* vs = sc + 128;
-      // P (A operand of P V) into TMEM: matrix 2 G + part, column = token pair
+      // P (A operand of P V) into TMEM: matrix 2 G + part (part 1: minus the residual), column =
+      // token pair
 #pragma unroll
       for (int c16 = 0; c16 < 2; ++c16) {
         uint32_t w[4][8];
@@ -2186,12 +2193,13 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
           const int el = 16 * c16 + e, tk = 32 * wg + el;
           const float p0 = ex2(fmaf(lg[el], scaleE, -ms)), p1 = ex2(fmaf(lg[el + 1], scaleE, -ms));
           l += p0 + p1;
-          const float a0 = p0 * vs[2 * tk], a1 = p1 * vs[2 * tk + 2];
-          const float b0 = p0 * vs[2 * tk + 1], b1 = p1 * vs[2 * tk + 3];
+          const float4 v4 = *reinterpret_cast<const float4*>(vs + 2 * tk);
+          const float a0 = p0 * v4.x, a1 = p1 * v4.z;
+          const float b0 = p0 * v4.y, b1 = p1 * v4.w;
           w[0][e >> 1] = pack_f16x2(a0, a1);
-          w[1][e >> 1] = f16x2_residual(w[0][e >> 1], a0, a1);
+          w[1][e >> 1] = f16x2_negres(w[0][e >> 1], a0, a1);
           w[2][e >> 1] = pack_f16x2(b0, b1);
-          w[3][e >> 1] = f16x2_residual(w[2][e >> 1], b0, b1);
+          w[3][e >> 1] = f16x2_negres(w[2][e >> 1], b0, b1);
         }
 #pragma unroll
         for (int mtx = 0; mtx < 4; ++mtx) tmem_st8u(tP + 32 * mtx + 16 * wg + 8 * c16, w[mtx]);
