@@ -1666,10 +1666,10 @@ struct ExtendArgs {
 
 __device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
-// Unpack word t (< 512) of one staged INT2 block into the level tiles, and the scales (t < 64).
-// TC: the tiles are tcgen05 operands in the 128-byte swizzle -- K as [2 blocks of 64 channels]
-// [64 tokens][64 channels] (channels in the decode's MMA order), V as [128 channels][64 tokens].
-template <bool TC = false>
+// Unpack word t (< 512) of one staged INT2 block into the level tiles, and the scales (t < 64,
+// as [group][token]).  The tiles are tcgen05 operands in the 128-byte swizzle -- K as [2 blocks
+// of 64 channels][64 tokens][64 channels] (channels in the decode's MMA order), V as [128
+// channels][64 tokens].
 __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint8_t* vp, float* ksc, float* vsc,
                                            int t) {
   const int T = t >> 7, ln = (t >> 2) & 31, wd = t & 3;
@@ -1679,15 +1679,12 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
     // 8 kh + 2 tq and + 1 of it
     const int row = 16 * T + 8 * (wd >> 1) + (ln >> 2), tq = ln & 3, kpar = wd & 1;
     const CodeWord cw(*reinterpret_cast<const uint32_t*>(raw + kKCodes + 4 * t));
-    uint8_t* base = kp + row * 256;
 #define OSCAR_EXT_K(R)                                                                                  \
   do {                                                                                                  \
     constexpr int bb = (R) >> 2, p = (R)&3;                                                             \
     const int ks = 2 * kpar + (p >> 1), kh = p & 1;                                                     \
     const int col = 16 * (4 * (ks >> 1) + 2 * bb + (ks & 1)) + 8 * kh + 2 * tq;                         \
-    st_shared_u32(TC ? kp + (col >> 6) * 8192 + sw128_elem(row, col & 63)                               \
-                     : base + ((((col >> 3) ^ (row & 7))) << 4) + 2 * (col & 7),                        \
-                  code_level<R>(cw));                                                                   \
+    st_shared_u32(kp + (col >> 6) * 8192 + sw128_elem(row, col & 63), code_level<R>(cw));             \
   } while (0)
     OSCAR_EXT_K(0);
     OSCAR_EXT_K(1);
@@ -1707,8 +1704,7 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
 #define OSCAR_EXT_V(R)                                                                                  \
   do {                                                                                                  \
     const int j = 16 * (R) + jm;                                                                        \
-    st_shared_u32(TC ? vp + sw128_elem(j, col) : vp + j * 128 + ((((col >> 3) ^ (j & 7))) << 4) + 2 * (col & 7), \
-                  code_level<R>(cw));                                                                   \
+    st_shared_u32(vp + sw128_elem(j, col), code_level<R>(cw));                                        \
   } while (0)
     OSCAR_EXT_V(0);
     OSCAR_EXT_V(1);
@@ -1723,10 +1719,10 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
   if (t < 64) {
     const float2 k2 = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(raw + kKScales + 4 * t));
     const float2 v2 = half2_bits_to_float2(*reinterpret_cast<const uint32_t*>(raw + kVScales + 4 * t));
-    ksc[2 * t] = k2.x;
-    ksc[2 * t + 1] = k2.y;
-    vsc[2 * t] = v2.x;
-    vsc[2 * t + 1] = v2.y;
+    ksc[t] = k2.x;
+    ksc[64 + t] = k2.y;
+    vsc[t] = v2.x;
+    vsc[64 + t] = v2.y;
   }
 }
 
@@ -1805,7 +1801,7 @@ constexpr int kXtTiles = 4;              // unpacked-page buffers (the MMAs of a
 constexpr uint32_t kXtK = 65536;         // K tiles: kXtTiles x [2 blocks of 64 channels][64 tokens][128 B]
 constexpr uint32_t kXtV = 131072;        // V^T tiles: kXtTiles x [128 channels][64 tokens]
 constexpr uint32_t kXtRaw = 196608;      // raw pages: 2 x 4608
-constexpr uint32_t kXtSc = kXtRaw + 2 * kBlockBytes;  // scales: kXtTiles x [K 64 x 2, V 64 x 2] float
+constexpr uint32_t kXtSc = kXtRaw + 2 * kBlockBytes;  // scales: kXtTiles x [K, V][group][64 tokens] float
 constexpr uint32_t kXtBars = kXtSc + kXtTiles * 1024;
 constexpr uint32_t kXtX = kXtBars + 256;  // softmax halves: page maxima [2][2][128], then l [2][128] (float)
 constexpr size_t kXtSmem = kXtX + 3072 + 1024;  // + 1024-byte alignment slack
@@ -1998,7 +1994,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       float* sc = reinterpret_cast<float*>(sm + kXtSc + st * 1024);
 #pragma unroll
       for (int x = 0; x < 4; ++x)
-        ext_unpack<true>(rp, sm + kXtK + st * 16384, sm + kXtV + st * 16384, sc, sc + 128, u + 128 * x);
+        ext_unpack(rp, sm + kXtK + st * 16384, sm + kXtV + st * 16384, sc, sc + 128, u + 128 * x);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -2089,7 +2085,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     const float kpl = log2f(a.pscale);
     const uint32_t tS = tbase + ((uint32_t)(32 * (warp & 3)) << 16), tO = tS + 128, tQ = tS + 256, tP = tS + 384;
     float* pmx = reinterpret_cast<float*>(sm + kXtX);  // [page parity][wg][128 rows] page maxima, then [wg][128] l
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;
+    float2 l2 = make_float2(0.f, 0.f);  // the row's sums over even and odd tokens
     bool ok = true;
     if (wg == 0) {
       // this row's q' (both parts, K order of the staged tiles) into TMEM: the A operand of S
@@ -2121,7 +2118,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         break;
       }
       tc_fence_after();
-      const float* sc = reinterpret_cast<const float*>(sm + kXtSc + st * 1024);  // K: [64][2], V: [64][2]
+      const float* sc = reinterpret_cast<const float*>(sm + kXtSc + st * 1024);  // K, V: [group][64 tokens]
       const int nv = min(kPage, hlim - kPage * (lp0 + k));
       // raw logits of this half page (the q' scale 2^E applied in the exponent below); a warp
       // whose rows all see the whole page skips the masking
@@ -2131,10 +2128,17 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         float s0[32], s1[32];
         tmem_ld32x2(tS + 32 * wg, tS + 64 + 32 * wg, s0, s1);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 32; e += 4) {  // token pairs on packed fp32 pairs
           const int tk = 32 * wg + e;
-          const float2 k2 = *reinterpret_cast<const float2*>(sc + 2 * tk);
-          lg[e] = fmaf(s0[e], k2.x, s1[e] * k2.y);
+          const float4 k0 = *reinterpret_cast<const float4*>(sc + tk), k1 = *reinterpret_cast<const float4*>(sc + 64 + tk);
+          const float2 x0 = ffma2(make_float2(s0[e], s0[e + 1]), make_float2(k0.x, k0.y),
+                                  fmul2(make_float2(s1[e], s1[e + 1]), make_float2(k1.x, k1.y)));
+          const float2 x1 = ffma2(make_float2(s0[e + 2], s0[e + 3]), make_float2(k0.z, k0.w),
+                                  fmul2(make_float2(s1[e + 2], s1[e + 3]), make_float2(k1.z, k1.w)));
+          lg[e] = x0.x;
+          lg[e + 1] = x0.y;
+          lg[e + 2] = x1.x;
+          lg[e + 3] = x1.y;
         }
         if (!whole) {  // rows past the query's limit or the history end
 #pragma unroll
@@ -2179,9 +2183,10 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         }
         tmem_wait_st();
       }
-      l *= al;
+      l2 = fmul2(l2, make_float2(al, al));
       m = nm;
       const float ms = nv > 0 ? m - kpl : 0.f;
+      const float2 sE = make_float2(scaleE, scaleE), nms = make_float2(-ms, -ms);
       const float* vs = sc + 128;
       // P (A operand of P V) into TMEM: matrix 2 G + part (part 1: minus the residual), column =
       // token pair
@@ -2189,17 +2194,22 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       for (int c16 = 0; c16 < 2; ++c16) {
         uint32_t w[4][8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
+        for (int e = 0; e < 16; e += 4) {
           const int el = 16 * c16 + e, tk = 32 * wg + el;
-          const float p0 = ex2(fmaf(lg[el], scaleE, -ms)), p1 = ex2(fmaf(lg[el + 1], scaleE, -ms));
-          l += p0 + p1;
-          const float4 v4 = *reinterpret_cast<const float4*>(vs + 2 * tk);
-          const float a0 = p0 * v4.x, a1 = p1 * v4.z;
-          const float b0 = p0 * v4.y, b1 = p1 * v4.w;
-          w[0][e >> 1] = pack_f16x2(a0, a1);
-          w[1][e >> 1] = f16x2_negres(w[0][e >> 1], a0, a1);
-          w[2][e >> 1] = pack_f16x2(b0, b1);
-          w[3][e >> 1] = f16x2_negres(w[2][e >> 1], b0, b1);
+          const float4 v0 = *reinterpret_cast<const float4*>(vs + tk), v1 = *reinterpret_cast<const float4*>(vs + 64 + tk);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float2 ar = ffma2(make_float2(lg[el + 2 * h2], lg[el + 2 * h2 + 1]), sE, nms);
+            const float2 p = make_float2(ex2(ar.x), ex2(ar.y));
+            l2 = fadd2(l2, p);
+            const float2 a = fmul2(p, h2 ? make_float2(v0.z, v0.w) : make_float2(v0.x, v0.y));
+            const float2 bq = fmul2(p, h2 ? make_float2(v1.z, v1.w) : make_float2(v1.x, v1.y));
+            const int c = (e >> 1) + h2;
+            w[0][c] = pack_f16x2(a.x, a.y);
+            w[1][c] = f16x2_negres(w[0][c], a.x, a.y);
+            w[2][c] = pack_f16x2(bq.x, bq.y);
+            w[3][c] = f16x2_negres(w[2][c], bq.x, bq.y);
+          }
         }
 #pragma unroll
         for (int mtx = 0; mtx < 4; ++mtx) tmem_st8u(tP + 32 * mtx + 16 * wg + 8 * c16, w[mtx]);
@@ -2213,6 +2223,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     if (ok && n_units > 0 && !__all_sync(0xffffffffu, mbar_wait_timed(pvdone, (n_units - 1) & 1, kWaitNs)))
       ok = false;
     // the row's l over both halves
+    float l = l2.x + l2.y;
     float* pl = pmx + 512;
     pl[wg * 128 + r] = l;
     __syncwarp();
