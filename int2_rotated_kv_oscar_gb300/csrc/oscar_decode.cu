@@ -1726,54 +1726,99 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
   }
 }
 
-// The last block of a (request, KV head, query group): warp w merges the
-// records of queries w, w + warps, ... of the group per head, applies R_V^T (staged in shared memory) to
-// the rotated-basis part, joins the original-basis part and normalises.
+// The last block of a (request, KV head, query group) merges the records of
+// every page range for the group's rows (row r = query ql of the group, head
+// n: r = ql g + n), then applies R_V^T to the rotated-basis part as one
+// 128 x 128 x 128 product, joins the original-basis part and normalises.
+// Shared memory: R_V^T [128][128], the merged rotated and original parts
+// [128 rows][128], per row (M_r, L_r, M_p, L_p).
 __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* smem, int b, int h, int grp, int z) {
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int t = threadIdx.x, nthr = blockDim.x, warp = t >> 5, lane = t & 31;
+  const int g = a.g, X = a.n_items;
   float* rvt = reinterpret_cast<float*>(smem);
-  for (int e = t; e < 128 * 128 / 4; e += blockDim.x)
+  float* ys = rvt + 128 * 128;
+  float* ps = ys + 128 * 128;
+  float4* rs = reinterpret_cast<float4*>(ps + 128 * 128);
+  for (int e = t; e < 128 * 128 / 4; e += nthr)
     reinterpret_cast<float4*>(rvt)[e] = __ldg(reinterpret_cast<const float4*>(a.R_VT) + e);
-  __syncthreads();
   if (t == 0) a.counters[z * a.Hkv + h] = 0;  // ready for the next launch on this workspace
-  for (int ql = warp; ql < a.qpg; ql += blockDim.x >> 5) {
-    const int qi = grp * a.qpg + ql;
-    if (qi >= a.chunk) return;
-    const int qg = b * a.chunk + qi;
-    for (int n = 0; n < a.g; ++n) {
-      float Mr = -INFINITY, Lr = 0.f, Mp = -INFINITY, Lp = 0.f;
-      float4 yr = make_float4(0.f, 0.f, 0.f, 0.f), yp = yr;
-      for (int x = 0; x < a.n_items; ++x) {
-        const float* rec = a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + x) * 2 * kPartialFloats;
-        merge_record(Mr, Lr, yr, __ldcg(rec + n), __ldcg(rec + 8 + n),
-                     __ldcg(reinterpret_cast<const float4*>(rec + 16 + n * kStateStride) + lane));
-        const float* rp = rec + kPartialFloats;
-        merge_record(Mp, Lp, yp, __ldcg(rp + n), __ldcg(rp + 8 + n),
-                     __ldcg(reinterpret_cast<const float4*>(rp + 16 + n * kStateStride) + lane));
-      }
-      // y R_V^T: lane holds channels 4 lane .. + 3 of y and computes outputs 4 lane .. + 3
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < 32; ++s) {
-        const float y[4] = {__shfl_sync(0xffffffffu, yr.x, s), __shfl_sync(0xffffffffu, yr.y, s),
-                            __shfl_sync(0xffffffffu, yr.z, s), __shfl_sync(0xffffffffu, yr.w, s)};
+  // the records, both kinds, by (row, 4-channel quad): a row's 32 quads in one warp; four page
+  // ranges' loads are issued before their merges
+  for (int task = t; task < 128 * 32; task += nthr) {
+    const int r = task >> 5, c4 = task & 31, ql = r / g, n = r % g, qi = grp * a.qpg + ql;
+    float Mr = -INFINITY, Lr = 0.f, Mp = -INFINITY, Lp = 0.f;
+    float4 yr = make_float4(0.f, 0.f, 0.f, 0.f), yp = yr;
+    if (ql < a.qpg && qi < a.chunk) {
+      const float* rec0 = a.partials + ((size_t)(b * a.chunk + qi) * a.Hkv + h) * X * 2 * kPartialFloats;
+      int x = 0;
+      for (; x + 4 <= X; x += 4) {
+        float mx[8], lx[8];
+        float4 vx[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float4 r = reinterpret_cast<const float4*>(rvt + (4 * s + c) * 128)[lane];
-          o.x = fmaf(y[c], r.x, o.x);
-          o.y = fmaf(y[c], r.y, o.y);
-          o.z = fmaf(y[c], r.z, o.z);
-          o.w = fmaf(y[c], r.w, o.w);
+        for (int i = 0; i < 8; ++i) {
+          const float* rc = rec0 + (size_t)(2 * x + i) * kPartialFloats;  // page range x + i / 2, kind i % 2
+          mx[i] = __ldcg(rc + n);
+          lx[i] = __ldcg(rc + 8 + n);
+          vx[i] = __ldcg(reinterpret_cast<const float4*>(rc + 16 + n * kStateStride) + c4);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          merge_record(Mr, Lr, yr, mx[i], lx[i], vx[i]);
+          merge_record(Mp, Lp, yp, mx[i + 1], lx[i + 1], vx[i + 1]);
         }
       }
-      const float M = fmaxf(Mr, Mp);
+      for (; x < X; ++x) {
+        const float* rc = rec0 + (size_t)2 * x * kPartialFloats;
+        merge_record(Mr, Lr, yr, __ldcg(rc + n), __ldcg(rc + 8 + n),
+                     __ldcg(reinterpret_cast<const float4*>(rc + 16 + n * kStateStride) + c4));
+        rc += kPartialFloats;
+        merge_record(Mp, Lp, yp, __ldcg(rc + n), __ldcg(rc + 8 + n),
+                     __ldcg(reinterpret_cast<const float4*>(rc + 16 + n * kStateStride) + c4));
+      }
+    }
+    reinterpret_cast<float4*>(ys + r * 128)[c4] = yr;
+    reinterpret_cast<float4*>(ps + r * 128)[c4] = yp;
+    if (c4 == 0) rs[r] = make_float4(Mr, Lr, Mp, Lp);
+  }
+  __syncthreads();
+  // y R_V^T: warp w takes rows 8 rb .. 8 rb + 7 (rb = w, w + warps, ...), lane the output
+  // channels 4 lane .. 4 lane + 3; the sums run over the input channels in order
+  for (int rb = warp; rb < 16; rb += nthr >> 5) {
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int k = 0; k < 128; k += 4) {
+      float4 y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = *reinterpret_cast<const float4*>(ys + (8 * rb + i) * 128 + k);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 rr = reinterpret_cast<const float4*>(rvt + (k + kk) * 128)[lane];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float yk = kk == 0 ? y[i].x : kk == 1 ? y[i].y : kk == 2 ? y[i].z : y[i].w;
+          o[i][0] = fmaf(yk, rr.x, o[i][0]);
+          o[i][1] = fmaf(yk, rr.y, o[i][1]);
+          o[i][2] = fmaf(yk, rr.z, o[i][2]);
+          o[i][3] = fmaf(yk, rr.w, o[i][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 8 * rb + i, ql = r / g, n = r % g, qi = grp * a.qpg + ql;
+      if (ql >= a.qpg || qi >= a.chunk) continue;
+      const float4 st = rs[r];
+      const float M = fmaxf(st.x, st.z);
       float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
       if (M != -INFINITY) {
-        const float fr = ex2(Mr - M), fp = ex2(Mp - M);
-        const float inv_l = 1.0f / (fr * Lr + fp * Lp);
-        res = make_float4((fr * o.x + fp * yp.x) * inv_l, (fr * o.y + fp * yp.y) * inv_l,
-                          (fr * o.z + fp * yp.z) * inv_l, (fr * o.w + fp * yp.w) * inv_l);
+        const float fr = ex2(st.x - M), fp = ex2(st.z - M);
+        const float inv_l = 1.0f / (fr * st.y + fp * st.w);
+        const float4 yp = reinterpret_cast<const float4*>(ps + r * 128)[lane];
+        res = make_float4((fr * o[i][0] + fp * yp.x) * inv_l, (fr * o[i][1] + fp * yp.y) * inv_l,
+                          (fr * o[i][2] + fp * yp.z) * inv_l, (fr * o[i][3] + fp * yp.w) * inv_l);
       }
-      *reinterpret_cast<float4*>(a.out + ((size_t)qg * a.Hq + h * a.g + n) * kD + 4 * lane) = res;
+      *reinterpret_cast<float4*>(a.out + ((size_t)(b * a.chunk + qi) * a.Hq + h * g + n) * kD + 4 * lane) = res;
     }
   }
 }
@@ -1805,6 +1850,7 @@ constexpr uint32_t kXtSc = kXtRaw + 2 * kBlockBytes;  // scales: kXtTiles x [K, 
 constexpr uint32_t kXtBars = kXtSc + kXtTiles * 1024;
 constexpr uint32_t kXtX = kXtBars + 256;  // softmax halves: page maxima [2][2][128], then l [2][128] (float)
 constexpr size_t kXtSmem = kXtX + 3072 + 1024;  // + 1024-byte alignment slack
+static_assert(3 * 128 * 128 * 4 + 128 * 16 <= kXtSmem - 1024, "the final merge's arrays in shared memory");
 static_assert(kXtK == kXtQ + 65536 && kXtV == kXtK + kXtTiles * 16384 && kXtRaw == kXtV + kXtTiles * 16384,
               "extend staging");
 
