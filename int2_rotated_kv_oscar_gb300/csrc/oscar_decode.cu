@@ -652,10 +652,18 @@ __device__ __forceinline__ void int2_tile(const uint8_t* __restrict__ blk, int T
   pv_tile<PACK4, true>(blk, T, nv, p[0], st, lane);
 }
 
+// A BF16 tile staged in shared memory (the chunk kernel): K as 16 rows of 16
+// 16-byte chunks, chunk c of row r at r * 16 + xt_kchunk(c, r); V as 16 rows of
+// 64 words, word w of row r at r * 64 + xt_vword(w, r).  The swizzles keep the
+// tile's MMA fragment loads free of bank conflicts.
+__device__ __forceinline__ int xt_kchunk(int c, int r) { return c ^ ((c >> 3) << 1) ^ (r & 1); }
+__device__ __forceinline__ int xt_vword(int w, int r) { return w ^ ((r & 7) << 2); }
+
 // One 16-token BF16 tile (rows of K and V in global memory, original basis).
 // rows: bit r set when row r of the tile is attended.
 // SUB: row `sub` of the tile (-1: none) is read from knew / vnew instead.
-template <bool PACK4, bool SUB = false>
+// SMEM: Kt and Vt are a tile staged in shared memory (Kt2, Vt2, split unused).
+template <bool PACK4, bool SUB = false, bool SMEM = false>
 __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
                                           const uint16_t* __restrict__ Kt2, const uint16_t* __restrict__ Vt2,
                                           int split, uint32_t rows, const uint32_t* qpf, float scaleEp,
@@ -673,12 +681,20 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
   uint32_t ka[16], kb[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint4 u = va ? __ldg(reinterpret_cast<const uint4*>(krow_a + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+    const uint4* ks = reinterpret_cast<const uint4*>(Kt);  // SMEM: chunks 4 tig + k of rows q and q + 8
+    uint4 u;
+    if constexpr (SMEM)
+      u = va ? ks[q * 16 + xt_kchunk(4 * tig + k, q)] : make_uint4(0, 0, 0, 0);
+    else
+      u = va ? __ldg(reinterpret_cast<const uint4*>(krow_a + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
     ka[4 * k + 0] = bf16x2_to_f16x2(u.x);
     ka[4 * k + 1] = bf16x2_to_f16x2(u.y);
     ka[4 * k + 2] = bf16x2_to_f16x2(u.z);
     ka[4 * k + 3] = bf16x2_to_f16x2(u.w);
-    u = vb ? __ldg(reinterpret_cast<const uint4*>(krow_b + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+    if constexpr (SMEM)
+      u = vb ? ks[(q + 8) * 16 + xt_kchunk(4 * tig + k, q + 8)] : make_uint4(0, 0, 0, 0);
+    else
+      u = vb ? __ldg(reinterpret_cast<const uint4*>(krow_b + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
     kb[4 * k + 0] = bf16x2_to_f16x2(u.x);
     kb[4 * k + 1] = bf16x2_to_f16x2(u.y);
     kb[4 * k + 2] = bf16x2_to_f16x2(u.z);
@@ -729,8 +745,13 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
       const int tr = blkid >> 1, cc = blkid & 1;  // token half, channel half
       const bool ok = tr ? vb : va;
       const int r = 8 * tr + q;
-      const uint16_t* vrow = SUB && r == sub ? vnew : (tr ? Vb : Va) + r * kD;
-      const uint32_t u = ok ? __ldg(reinterpret_cast<const uint32_t*>(vrow + 16 * mt + 8 * cc + 2 * tig)) : 0u;
+      uint32_t u;
+      if constexpr (SMEM) {
+        u = ok ? reinterpret_cast<const uint32_t*>(Vt)[r * 64 + xt_vword(8 * mt + 4 * cc + tig, r)] : 0u;
+      } else {
+        const uint16_t* vrow = SUB && r == sub ? vnew : (tr ? Vb : Va) + r * kD;
+        u = ok ? __ldg(reinterpret_cast<const uint32_t*>(vrow + 16 * mt + 8 * cc + 2 * tig)) : 0u;
+      }
       a[blkid] = movmatrix_trans(bf16x2_to_f16x2(u));
     }
     // a[0]: channels 16mt+q, tokens 2tig..; a[1]: channels +8; a[2]: tokens +8; a[3]: both
@@ -1966,9 +1987,86 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(qsm);
-    // BF16 sink/recent tiles of this item, per query (original basis, mma.sync)
+    // BF16 sink/recent tiles of this item, per query (original basis, mma.sync).  With at most
+    // two tiles an item, each copy warp stages them once in shared memory (its 16 KB of the q'
+    // staging area, free once q' is in TMEM) and its queries read them from there.
     const int sp = c.sink_page[b];
     const bool sink_ok = sp >= 0 && sp < c.num_sink;
+    // tile k of the item: its valid rows (0: none), positions and sources
+    auto tile_src = [&](int k, size_t& off, size_t& off2, int& split, size_t& row_off, bool& ring) -> int {
+      const int j = item * a.tiles_per_item + k;
+      if (j >= kBf16Tiles) return 0;
+      const int nv = bf16_tile_rows(j, L, row_off, ring);
+      if (nv <= 0) return 0;
+      split = 16;
+      if (ring) {
+        if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) return 0;
+      } else {
+        if (!sink_ok) {
+          if (lane == 0) set_error(a.err, kErrSink);
+          return 0;
+        }
+        off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
+      }
+      return nv;
+    };
+    // the rows of a tile that a query with causal limit lim attends
+    auto rows_of = [&](int nv, size_t row_off, bool ring, int lim) -> uint32_t {
+      uint32_t rows = (1u << nv) - 1u;
+      if (!ring) {
+        rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
+      } else {
+        for (int r = 0; r < nv; ++r) {
+          const int rr = (int)row_off + r;
+          const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
+          if (p >= lim) rows &= ~(1u << r);
+        }
+      }
+      return rows;
+    };
+    const bool staged = a.tiles_per_item <= 2;
+    uint8_t* stg = sm + kXtQ + w4 * 16384;  // [2 tiles][K 4 KB, V 4 KB]
+    int snv[2] = {0, 0};
+    size_t sro[2] = {0, 0};
+    bool sring[2] = {false, false};
+    if (staged) {
+      if (!__all_sync(0xffffffffu, mbar_wait_timed(qtm, 0, kWaitNs))) {  // q' has left for TMEM
+        if (lane == 0) set_error(a.err, kErrTimeout);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (k >= a.tiles_per_item) break;
+          size_t off = 0, off2 = 0;
+          int split = 16;
+          snv[k] = tile_src(k, off, off2, split, sro[k], sring[k]);
+          if (snv[k] == 0) continue;
+          const uint16_t* kg = sring[k] ? c.k_ring : c.k_sink;
+          const uint16_t* vg = sring[k] ? c.v_ring : c.v_sink;
+          uint4* kd = reinterpret_cast<uint4*>(stg + k * 8192);
+          uint4* vd = reinterpret_cast<uint4*>(stg + k * 8192 + 4096);
+          // element e = lane + 32 i: row e / 16, 16-byte chunk e % 16
+          uint4 kv[8], vv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i, r = e >> 4, ch = e & 15;
+            if (r < snv[k]) {
+              const size_t o = (r < split ? off : off2) + (size_t)r * kD;
+              kv[i] = __ldg(reinterpret_cast<const uint4*>(kg + o) + ch);
+              vv[i] = __ldg(reinterpret_cast<const uint4*>(vg + o) + ch);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i, r = e >> 4, ch = e & 15;
+            if (r < snv[k]) {
+              kd[r * 16 + xt_kchunk(ch, r)] = kv[i];
+              vd[(r * 64 + xt_vword(4 * ch, r)) >> 2] = vv[i];  // words 4 ch .. 4 ch + 3 stay together
+            }
+          }
+        }
+      }
+      __syncwarp();
+    }
     for (int ql = w4; ql < qpg; ql += 4) {
       const int qi = grp * qpg + ql;
       if (qi >= a.chunk) continue;
@@ -1989,38 +2087,28 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       const float scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
       WarpState sb;
       state_init(sb);
-      for (int k = 0; k < a.tiles_per_item; ++k) {
-        const int j = item * a.tiles_per_item + k;
-        if (j >= kBf16Tiles) break;
-        size_t row_off;
-        bool ring;
-        const int nv = bf16_tile_rows(j, L, row_off, ring);
-        if (nv <= 0) continue;
-        size_t off, off2;
-        int split = 16;
-        if (ring) {
-          if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) continue;
-        } else {
-          if (!sink_ok) {
-            if (lane == 0) set_error(a.err, kErrSink);
-            continue;
-          }
-          off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
+      if (staged) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (snv[k] == 0) continue;
+          const uint32_t rows = rows_of(snv[k], sro[k], sring[k], lim);
+          if (rows == 0) continue;
+          const uint16_t* kt = reinterpret_cast<const uint16_t*>(stg + k * 8192);
+          bf16_tile<true, false, true>(kt, kt + 2048, kt, kt + 2048, 16, rows, qpf, scaleEp, sb, lane);
         }
-        uint32_t rows = (1u << nv) - 1u;
-        if (!ring) {
-          rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
-        } else {
-          for (int r = 0; r < nv; ++r) {
-            const int rr = (int)row_off + r;
-            const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
-            if (p >= lim) rows &= ~(1u << r);
-          }
+      } else {
+        for (int k = 0; k < a.tiles_per_item; ++k) {
+          size_t off = 0, off2 = 0, row_off = 0;
+          int split = 16;
+          bool ring = false;
+          const int nv = tile_src(k, off, off2, split, row_off, ring);
+          if (nv == 0) continue;
+          const uint32_t rows = rows_of(nv, row_off, ring, lim);
+          if (rows == 0) continue;
+          const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
+          const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
+          bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, sb, lane);
         }
-        if (rows == 0) continue;
-        const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
-        const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
-        bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, sb, lane);
       }
       store_state<true>(sb, a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats +
                                 kPartialFloats,

@@ -120,9 +120,12 @@ def test_paged_bulk_and_chunked_append(P, n):
         paged.close()
 
 
-def test_paged_extend_equals_the_ring():
-    """Both extend paths read the window through the page table."""
-    cfg, Hq, Hkv, P, n = 53, 32, 8, 1000, 40
+@pytest.mark.parametrize("P,n", [(1000, 40), (1800, 32)])
+def test_paged_extend_equals_the_ring(P, n):
+    """Both extend paths read the window through the page table.  At P = 1800 the chunk kernel
+    has two BF16 tiles per page range, staged in shared memory, and the window's wrap point
+    (L mod 256 = 40) falls inside a tile, whose rows then come from two recent pages."""
+    cfg, Hq, Hkv = 53, 32, 8
     L = P + n
     tk = inputs.kv_tokens_bf16(cfg, 0, Hkv, inputs.STREAM_KV, L, 0)
     q = inputs.decode_queries_bf16(cfg, 0, n, Hq).reshape(1, n, Hq, 128).cuda()
