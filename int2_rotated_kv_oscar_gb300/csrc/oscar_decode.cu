@@ -1854,12 +1854,12 @@ __device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* sm
 // so an MMA reads only its B tile (K or V^T, 128-byte-swizzled) from shared
 // memory.  S of the next page overlaps the softmax of this one.  Warps:
 //   0-3, 9-12  softmax, two warpgroups splitting every page (tokens 0-31, 32-63) and O's
-//        columns; warps 0-3 first put the q' rows into TMEM; at the end the rows'
-//        rotated-basis records
+//        columns; warps 0-3 first put the q' rows into TMEM, then all eight run the
+//        BF16 sink/recent tiles (per query, mma.sync, original-basis records) while
+//        the first pages unpack; at the end the rows' rotated-basis records
 //   4-7  the q' operands (from the prep's fragments, staged in shared memory),
-//        the BF16 sink/recent tiles (per query, mma.sync, original-basis
-//        records), then the pages: bulk copies (thread 128) and the unpack
-//        into double-buffered tiles
+//        then the pages: bulk copies (thread 128) and the unpack into the tile
+//        buffers
 //   8    TMEM (512 columns: S, O, q', P) and the MMA thread
 constexpr int kXtThreads = 13 * 32;
 constexpr uint32_t kXtQ = 0;             // q' value / residual: 2 x [2 blocks of 64 channels][128 rows][128 B]
@@ -1899,6 +1899,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
   uint64_t* xm = rawf + 19;      // [2] page maxima of both softmax halves written (8 warps)
   uint64_t* xl = rawf + 21;      // the rows' l of both halves written (8 warps)
   uint32_t* tmem_at = reinterpret_cast<uint32_t*>(rawf + 22);
+  uint64_t* bstg = rawf + 23;    // the item's BF16 tiles staged in shared memory (4 warps)
   // arrivals counted per warp: a lane's accesses are ordered before its
   // warp's one arrival by the warp barrier
   if (t == 0) {
@@ -1920,6 +1921,7 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     mbar_init(done, 1);
     mbar_init(qsm, 4);
     mbar_init(qtm, 4);
+    mbar_init(bstg, 4);
     fence_mbar_init();
   }
   for (int i = t; i < 65536 / 16; i += kXtThreads)  // q' operands: rows without a query stay zero
@@ -1943,6 +1945,42 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_at;
+
+  // BF16 sink/recent tiles of this item (original basis, mma.sync per query).  Tile k: its
+  // valid rows (0: none), positions and sources.
+  const int sp = c.sink_page[b];
+  const bool sink_ok = sp >= 0 && sp < c.num_sink;
+  auto tile_src = [&](int k, size_t& off, size_t& off2, int& split, size_t& row_off, bool& ring) -> int {
+    const int j = item * a.tiles_per_item + k;
+    if (j >= kBf16Tiles) return 0;
+    const int nv = bf16_tile_rows(j, L, row_off, ring);
+    if (nv <= 0) return 0;
+    split = 16;
+    if (ring) {
+      if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) return 0;
+    } else {
+      if (!sink_ok) {
+        if (lane == 0) set_error(a.err, kErrSink);
+        return 0;
+      }
+      off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
+    }
+    return nv;
+  };
+  // the rows of a tile that a query with causal limit lim attends
+  auto rows_of = [&](int nv, size_t row_off, bool ring, int lim) -> uint32_t {
+    uint32_t rows = (1u << nv) - 1u;
+    if (!ring) {
+      rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
+    } else {
+      for (int r = 0; r < nv; ++r) {
+        const int rr = (int)row_off + r;
+        const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
+        if (p >= lim) rows &= ~(1u << r);
+      }
+    }
+    return rows;
+  };
 
   if (warp >= 4 && warp < 8) {
     const int u = t - 128, w4 = warp - 4;
@@ -1987,133 +2025,6 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(qsm);
-    // BF16 sink/recent tiles of this item, per query (original basis, mma.sync).  With at most
-    // two tiles an item, each copy warp stages them once in shared memory (its 16 KB of the q'
-    // staging area, free once q' is in TMEM) and its queries read them from there.
-    const int sp = c.sink_page[b];
-    const bool sink_ok = sp >= 0 && sp < c.num_sink;
-    // tile k of the item: its valid rows (0: none), positions and sources
-    auto tile_src = [&](int k, size_t& off, size_t& off2, int& split, size_t& row_off, bool& ring) -> int {
-      const int j = item * a.tiles_per_item + k;
-      if (j >= kBf16Tiles) return 0;
-      const int nv = bf16_tile_rows(j, L, row_off, ring);
-      if (nv <= 0) return 0;
-      split = 16;
-      if (ring) {
-        if (!recent_tile(c, b, h, L, (int)row_off, off, off2, split, a.err, lane == 0)) return 0;
-      } else {
-        if (!sink_ok) {
-          if (lane == 0) set_error(a.err, kErrSink);
-          return 0;
-        }
-        off = off2 = (((size_t)sp * a.Hkv + h) * kSink + row_off) * kD;
-      }
-      return nv;
-    };
-    // the rows of a tile that a query with causal limit lim attends
-    auto rows_of = [&](int nv, size_t row_off, bool ring, int lim) -> uint32_t {
-      uint32_t rows = (1u << nv) - 1u;
-      if (!ring) {
-        rows &= (1u << max(0, min(16, lim - (int)row_off))) - 1u;
-      } else {
-        for (int r = 0; r < nv; ++r) {
-          const int rr = (int)row_off + r;
-          const int p = hist_end + (((rr - (hist_end - kSink)) % kRecent) + kRecent) % kRecent;
-          if (p >= lim) rows &= ~(1u << r);
-        }
-      }
-      return rows;
-    };
-    const bool staged = a.tiles_per_item <= 2;
-    uint8_t* stg = sm + kXtQ + w4 * 16384;  // [2 tiles][K 4 KB, V 4 KB]
-    int snv[2] = {0, 0};
-    size_t sro[2] = {0, 0};
-    bool sring[2] = {false, false};
-    if (staged) {
-      if (!__all_sync(0xffffffffu, mbar_wait_timed(qtm, 0, kWaitNs))) {  // q' has left for TMEM
-        if (lane == 0) set_error(a.err, kErrTimeout);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (k >= a.tiles_per_item) break;
-          size_t off = 0, off2 = 0;
-          int split = 16;
-          snv[k] = tile_src(k, off, off2, split, sro[k], sring[k]);
-          if (snv[k] == 0) continue;
-          const uint16_t* kg = sring[k] ? c.k_ring : c.k_sink;
-          const uint16_t* vg = sring[k] ? c.v_ring : c.v_sink;
-          uint4* kd = reinterpret_cast<uint4*>(stg + k * 8192);
-          uint4* vd = reinterpret_cast<uint4*>(stg + k * 8192 + 4096);
-          // element e = lane + 32 i: row e / 16, 16-byte chunk e % 16
-          uint4 kv[8], vv[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i, r = e >> 4, ch = e & 15;
-            if (r < snv[k]) {
-              const size_t o = (r < split ? off : off2) + (size_t)r * kD;
-              kv[i] = __ldg(reinterpret_cast<const uint4*>(kg + o) + ch);
-              vv[i] = __ldg(reinterpret_cast<const uint4*>(vg + o) + ch);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i, r = e >> 4, ch = e & 15;
-            if (r < snv[k]) {
-              kd[r * 16 + xt_kchunk(ch, r)] = kv[i];
-              vd[(r * 64 + xt_vword(4 * ch, r)) >> 2] = vv[i];  // words 4 ch .. 4 ch + 3 stay together
-            }
-          }
-        }
-      }
-      __syncwarp();
-    }
-    for (int ql = w4; ql < qpg; ql += 4) {
-      const int qi = grp * qpg + ql;
-      if (qi >= a.chunk) continue;
-      const int qg = b * a.chunk + qi, bq = qg * a.Hkv + h;
-      const int lim = max(0, min(a.pos0[b] + qi + 1, L));
-      uint32_t qpf[16];
-      {
-        const uint4* srcp = reinterpret_cast<const uint4*>(a.qplain + (size_t)bq * kQFragWords + lane * 32);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint4 v = __ldg(srcp + (kk ^ (lane & 7)));
-          qpf[4 * kk] = v.x;
-          qpf[4 * kk + 1] = v.y;
-          qpf[4 * kk + 2] = v.z;
-          qpf[4 * kk + 3] = v.w;
-        }
-      }
-      const float scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
-      WarpState sb;
-      state_init(sb);
-      if (staged) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (snv[k] == 0) continue;
-          const uint32_t rows = rows_of(snv[k], sro[k], sring[k], lim);
-          if (rows == 0) continue;
-          const uint16_t* kt = reinterpret_cast<const uint16_t*>(stg + k * 8192);
-          bf16_tile<true, false, true>(kt, kt + 2048, kt, kt + 2048, 16, rows, qpf, scaleEp, sb, lane);
-        }
-      } else {
-        for (int k = 0; k < a.tiles_per_item; ++k) {
-          size_t off = 0, off2 = 0, row_off = 0;
-          int split = 16;
-          bool ring = false;
-          const int nv = tile_src(k, off, off2, split, row_off, ring);
-          if (nv == 0) continue;
-          const uint32_t rows = rows_of(nv, row_off, ring, lim);
-          if (rows == 0) continue;
-          const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
-          const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
-          bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, sb, lane);
-        }
-      }
-      store_state<true>(sb, a.partials + (((size_t)qg * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats +
-                                kPartialFloats,
-                        1.0f / kPScaleBF16, lane);
-    }
     // INT2 pages: raw stage k % 2 unpacked into the tiles of buffer k % kXtTiles
     bool timed_out = false;
     for (int k = 0; k < n_units; ++k) {
@@ -2244,6 +2155,101 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(qtm);
+    }
+    // The item's BF16 tiles, per query, while the copy warps unpack the first pages: with at most
+    // two tiles an item, warpgroup 1 stages them once in the q' staging area (free once q' is in
+    // TMEM; swizzled so the MMA fragment loads are free of bank conflicts); the eight softmax
+    // warps then take queries sw, sw + 8, ... of the group.
+    {
+      const bool staged = a.tiles_per_item <= 2;
+      const int sw = 4 * wg + (warp & 3);
+      uint8_t* stg = sm + kXtQ;  // [2 tiles][K 4 KB, V 4 KB]
+      int snv[2] = {0, 0}, ssplit[2] = {16, 16};
+      size_t sro[2] = {0, 0}, soff[2] = {0, 0}, soff2[2] = {0, 0};
+      bool sring[2] = {false, false};
+      if (staged) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (k < a.tiles_per_item) snv[k] = tile_src(k, soff[k], soff2[k], ssplit[k], sro[k], sring[k]);
+        if (wg == 1) {
+          if (!__all_sync(0xffffffffu, mbar_wait_timed(qtm, 0, kWaitNs))) {  // q' has left for TMEM
+            if (lane == 0) set_error(a.err, kErrTimeout);
+          } else {
+            // element e = 128 i + 32 (warp % 4) + lane of [2 tiles][16 rows][16 chunks of 16 bytes]
+            uint4 kv[4], vv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int e = 128 * i + 32 * (warp & 3) + lane, k = e >> 8, rw = (e >> 4) & 15, ch = e & 15;
+              if (rw < snv[k]) {
+                const size_t o = (rw < ssplit[k] ? soff[k] : soff2[k]) + (size_t)rw * kD;
+                kv[i] = __ldg(reinterpret_cast<const uint4*>((sring[k] ? c.k_ring : c.k_sink) + o) + ch);
+                vv[i] = __ldg(reinterpret_cast<const uint4*>((sring[k] ? c.v_ring : c.v_sink) + o) + ch);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int e = 128 * i + 32 * (warp & 3) + lane, k = e >> 8, rw = (e >> 4) & 15, ch = e & 15;
+              if (rw < snv[k]) {
+                reinterpret_cast<uint4*>(stg + k * 8192)[rw * 16 + xt_kchunk(ch, rw)] = kv[i];
+                reinterpret_cast<uint4*>(stg + k * 8192 + 4096)[(rw * 64 + xt_vword(4 * ch, rw)) >> 2] = vv[i];
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bstg);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait_timed(bstg, 0, kWaitNs))) {
+          if (lane == 0) set_error(a.err, kErrTimeout);
+          snv[0] = snv[1] = 0;
+        }
+      }
+      for (int qq = sw; qq < qpg && grp * qpg + qq < a.chunk; qq += 8) {
+        const int qiq = grp * qpg + qq;
+        const int qgq = b * a.chunk + qiq, bq = qgq * a.Hkv + h;
+        const int limq = max(0, min(a.pos0[b] + qiq + 1, L));
+        uint32_t qpf[16];
+        {
+          const uint4* srcp = reinterpret_cast<const uint4*>(a.qplain + (size_t)bq * kQFragWords + lane * 32);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint4 v = __ldg(srcp + (kk ^ (lane & 7)));
+            qpf[4 * kk] = v.x;
+            qpf[4 * kk + 1] = v.y;
+            qpf[4 * kk + 2] = v.z;
+            qpf[4 * kk + 3] = v.w;
+          }
+        }
+        const float scaleEp = __ldg(a.qconst + (size_t)bq * kQConstFloats + 17);
+        WarpState sb;
+        state_init(sb);
+        if (staged) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (snv[k] == 0) continue;
+            const uint32_t rows = rows_of(snv[k], sro[k], sring[k], limq);
+            if (rows == 0) continue;
+            const uint16_t* kt = reinterpret_cast<const uint16_t*>(stg + k * 8192);
+            bf16_tile<true, false, true>(kt, kt + 2048, kt, kt + 2048, 16, rows, qpf, scaleEp, sb, lane);
+          }
+        } else {
+          for (int k = 0; k < a.tiles_per_item; ++k) {
+            size_t off = 0, off2 = 0, row_off = 0;
+            int split = 16;
+            bool ring = false;
+            const int nv = tile_src(k, off, off2, split, row_off, ring);
+            if (nv == 0) continue;
+            const uint32_t rows = rows_of(nv, row_off, ring, limq);
+            if (rows == 0) continue;
+            const uint16_t* kbase = ring ? c.k_ring : c.k_sink;
+            const uint16_t* vbase = ring ? c.v_ring : c.v_sink;
+            bf16_tile<true>(kbase + off, vbase + off, kbase + off2, vbase + off2, split, rows, qpf, scaleEp, sb,
+                            lane);
+          }
+        }
+        store_state<true>(sb, a.partials + (((size_t)qgq * a.Hkv + h) * a.n_items + item) * 2 * kPartialFloats +
+                                  kPartialFloats,
+                          1.0f / kPScaleBF16, lane);
+      }
     }
     for (int k = 0; k < n_units && ok; ++k) {
       const int st = k % kXtTiles;
