@@ -1870,8 +1870,11 @@ constexpr uint32_t kXtRaw = 196608;      // raw pages: 2 x 4608
 constexpr uint32_t kXtSc = kXtRaw + 2 * kBlockBytes;  // scales: kXtTiles x [K, V][group][64 tokens] float
 constexpr uint32_t kXtBars = kXtSc + kXtTiles * 1024;
 constexpr uint32_t kXtX = kXtBars + 256;  // softmax halves: page maxima [2][2][128], then l [2][128] (float)
-constexpr size_t kXtSmem = kXtX + 3072 + 1024;  // + 1024-byte alignment slack
+constexpr uint32_t kXtTi = kXtX + 3072;   // staged BF16 tiles: [8] {valid rows, first row, ring}
+constexpr int kXtStaged = 8;              // BF16 tiles an item may stage (8 KB each, in the q' staging area)
+constexpr size_t kXtSmem = kXtTi + kXtStaged * 16 + 1024;  // + 1024-byte alignment slack
 static_assert(3 * 128 * 128 * 4 + 128 * 16 <= kXtSmem - 1024, "the final merge's arrays in shared memory");
+static_assert(kXtStaged * 8192 <= 65536, "staged BF16 tiles in the q' staging area");
 static_assert(kXtK == kXtQ + 65536 && kXtV == kXtK + kXtTiles * 16384 && kXtRaw == kXtV + kXtTiles * 16384,
               "extend staging");
 
@@ -2157,51 +2160,51 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
       if (lane == 0) mbar_arrive(qtm);
     }
     // The item's BF16 tiles, per query, while the copy warps unpack the first pages: with at most
-    // two tiles an item, warpgroup 1 stages them once in the q' staging area (free once q' is in
-    // TMEM; swizzled so the MMA fragment loads are free of bank conflicts); the eight softmax
-    // warps then take queries sw, sw + 8, ... of the group.
+    // kXtStaged tiles an item, the warps of warpgroup 1 stage them (warp w tiles w, w + 4) in the
+    // q' staging area (free once q' is in TMEM; swizzled so the MMA fragment loads are free of bank
+    // conflicts) with their rows and positions; the eight softmax warps then take queries sw,
+    // sw + 8, ... of the group.
     {
-      const bool staged = a.tiles_per_item <= 2;
+      const bool staged = a.tiles_per_item <= kXtStaged;
       const int sw = 4 * wg + (warp & 3);
-      uint8_t* stg = sm + kXtQ;  // [2 tiles][K 4 KB, V 4 KB]
-      int snv[2] = {0, 0}, ssplit[2] = {16, 16};
-      size_t sro[2] = {0, 0}, soff[2] = {0, 0}, soff2[2] = {0, 0};
-      bool sring[2] = {false, false};
+      uint8_t* stg = sm + kXtQ;  // [kXtStaged tiles][K 4 KB, V 4 KB]
+      int4* tinfo = reinterpret_cast<int4*>(sm + kXtTi);
       if (staged) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          if (k < a.tiles_per_item) snv[k] = tile_src(k, soff[k], soff2[k], ssplit[k], sro[k], sring[k]);
         if (wg == 1) {
-          if (!__all_sync(0xffffffffu, mbar_wait_timed(qtm, 0, kWaitNs))) {  // q' has left for TMEM
-            if (lane == 0) set_error(a.err, kErrTimeout);
-          } else {
-            // element e = 128 i + 32 (warp % 4) + lane of [2 tiles][16 rows][16 chunks of 16 bytes]
-            uint4 kv[4], vv[4];
+          const bool qok = __all_sync(0xffffffffu, mbar_wait_timed(qtm, 0, kWaitNs));  // q' has left for TMEM
+          if (!qok && lane == 0) set_error(a.err, kErrTimeout);
+          for (int k = warp & 3; k < a.tiles_per_item; k += 4) {
+            size_t off = 0, off2 = 0, row_off = 0;
+            int split = 16;
+            bool ring = false;
+            const int nv = qok ? tile_src(k, off, off2, split, row_off, ring) : 0;
+            const uint16_t* kg = ring ? c.k_ring : c.k_sink;
+            const uint16_t* vg = ring ? c.v_ring : c.v_sink;
+            // element e = lane + 32 i: row e / 16, 16-byte chunk e % 16
+            uint4 kv[8], vv[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int e = 128 * i + 32 * (warp & 3) + lane, k = e >> 8, rw = (e >> 4) & 15, ch = e & 15;
-              if (rw < snv[k]) {
-                const size_t o = (rw < ssplit[k] ? soff[k] : soff2[k]) + (size_t)rw * kD;
-                kv[i] = __ldg(reinterpret_cast<const uint4*>((sring[k] ? c.k_ring : c.k_sink) + o) + ch);
-                vv[i] = __ldg(reinterpret_cast<const uint4*>((sring[k] ? c.v_ring : c.v_sink) + o) + ch);
+            for (int i = 0; i < 8; ++i) {
+              const int e = lane + 32 * i, rw = e >> 4, ch = e & 15;
+              if (rw < nv) {
+                const size_t o = (rw < split ? off : off2) + (size_t)rw * kD;
+                kv[i] = __ldg(reinterpret_cast<const uint4*>(kg + o) + ch);
+                vv[i] = __ldg(reinterpret_cast<const uint4*>(vg + o) + ch);
               }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int e = 128 * i + 32 * (warp & 3) + lane, k = e >> 8, rw = (e >> 4) & 15, ch = e & 15;
-              if (rw < snv[k]) {
+            for (int i = 0; i < 8; ++i) {
+              const int e = lane + 32 * i, rw = e >> 4, ch = e & 15;
+              if (rw < nv) {
                 reinterpret_cast<uint4*>(stg + k * 8192)[rw * 16 + xt_kchunk(ch, rw)] = kv[i];
                 reinterpret_cast<uint4*>(stg + k * 8192 + 4096)[(rw * 64 + xt_vword(4 * ch, rw)) >> 2] = vv[i];
               }
             }
+            if (lane == 0) tinfo[k] = make_int4(nv, (int)row_off, ring ? 1 : 0, 0);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(bstg);
         }
-        if (!__all_sync(0xffffffffu, mbar_wait_timed(bstg, 0, kWaitNs))) {
-          if (lane == 0) set_error(a.err, kErrTimeout);
-          snv[0] = snv[1] = 0;
-        }
+        if (!__all_sync(0xffffffffu, mbar_wait_timed(bstg, 0, kWaitNs)) && lane == 0) set_error(a.err, kErrTimeout);
       }
       for (int qq = sw; qq < qpg && grp * qpg + qq < a.chunk; qq += 8) {
         const int qiq = grp * qpg + qq;
@@ -2223,10 +2226,10 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
         WarpState sb;
         state_init(sb);
         if (staged) {
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            if (snv[k] == 0) continue;
-            const uint32_t rows = rows_of(snv[k], sro[k], sring[k], limq);
+          for (int k = 0; k < a.tiles_per_item; ++k) {
+            const int4 ti = tinfo[k];
+            if (ti.x == 0) continue;
+            const uint32_t rows = rows_of(ti.x, (size_t)ti.y, ti.z != 0, limq);
             if (rows == 0) continue;
             const uint16_t* kt = reinterpret_cast<const uint16_t*>(stg + k * 8192);
             bf16_tile<true, false, true>(kt, kt + 2048, kt, kt + 2048, 16, rows, qpf, scaleEp, sb, lane);
@@ -2598,11 +2601,28 @@ ExtendPlan plan_extend(int batch, int chunk, int Hq, int Hkv, int max_ctx_len, i
   const int hist_end = max_ctx_len > kSink + kRecent ? max_ctx_len - kRecent : kSink;
   int pages = (hist_end + kPage - 1) / kPage - 1;
   if (pages < 0) pages = 0;
-  const long long total = (long long)batch * p.ngpr * Hkv * pages;
+  // Pages per page range C: the split whose waves of blocks (one block per SM)
+  // and final merge finish first.  In units of one page's period (~1.5 us at
+  // 100K tokens): a block's fixed work (q' staging, the BF16 tiles, its
+  // records) ~8, and every page range ~3 more in the last block's merge.
+  const long long pairs = (long long)batch * p.ngpr * Hkv;
   const long long slots = num_sms > 0 ? num_sms : 148;
-  long long C = (total + slots - 1) / slots;
+  long long C = 2;
+  if (pages > 0 && pairs > 0) {
+    long long best = -1;
+    for (long long n = 1; n <= kMaxChunks && n <= pages; ++n) {
+      const long long c = (pages + n - 1) / n;
+      if (c < 2 && n > 1) break;
+      const long long items = (pages + c - 1) / c;
+      const long long waves = (pairs * items + slots - 1) / slots;
+      const long long cost = waves * (8 + c) + 3 * items;
+      if (best < 0 || cost < best) {
+        best = cost;
+        C = c;
+      }
+    }
+  }
   if (C < 2) C = 2;
-  if (C > 8 * kWarps) C = 8 * kWarps;
   if (pages > C * kMaxChunks) C = (pages + kMaxChunks - 1) / kMaxChunks;
   p.chunk_pages = (int)C;
   p.n_items = pages > 0 ? (int)((pages + C - 1) / C) : 1;

@@ -120,11 +120,12 @@ def test_paged_bulk_and_chunked_append(P, n):
         paged.close()
 
 
-@pytest.mark.parametrize("P,n", [(1000, 40), (1800, 32)])
+@pytest.mark.parametrize("P,n", [(1000, 40), (2600, 32)])
 def test_paged_extend_equals_the_ring(P, n):
-    """Both extend paths read the window through the page table.  At P = 1800 the chunk kernel
-    has two BF16 tiles per page range, staged in shared memory, and the window's wrap point
-    (L mod 256 = 40) falls inside a tile, whose rows then come from two recent pages."""
+    """Both extend paths read the window through the page table.  At P = 2600 the chunk kernel
+    splits the history into three page ranges of seven BF16 tiles each, staged in shared memory,
+    and the window's wrap point (L mod 256 = 72) falls inside tile 8, whose rows then come from
+    two recent pages; at P = 1000 the tiles are read from global memory."""
     cfg, Hq, Hkv = 53, 32, 8
     L = P + n
     tk = inputs.kv_tokens_bf16(cfg, 0, Hkv, inputs.STREAM_KV, L, 0)
