@@ -1883,7 +1883,9 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
   const uint32_t raw_s = smem_u32(xt_raw);
   uint8_t* sm = xt_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   const uint32_t sbase = smem_u32(sm);
-  const int item = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  // blocks run KV head first and page range last, so that every (request, group, KV head)
+  // finishes its last range, and runs its final merge, in the last wave
+  const int h = blockIdx.x, z = blockIdx.y, item = blockIdx.z;
   const int b = z / a.ngpr, grp = z % a.ngpr;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const CacheRefs& c = a.c;
@@ -2695,7 +2697,7 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   err = smem_attr_once(reinterpret_cast<const void*>(extend_tc_kernel), kXtSmem, attr_done);
   if (err != cudaSuccess) return err;
   void* args[] = {&a};
-  return launch_pdl(reinterpret_cast<const void*>(extend_tc_kernel), dim3(p.n_items, p.Hkv, p.batch * p.ngpr),
+  return launch_pdl(reinterpret_cast<const void*>(extend_tc_kernel), dim3(p.Hkv, p.batch * p.ngpr, p.n_items),
                     dim3(kXtThreads), kXtSmem, stream, args);
 }
 
