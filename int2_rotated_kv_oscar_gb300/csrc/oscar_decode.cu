@@ -1678,7 +1678,6 @@ struct ExtendArgs {
   const uint32_t* qplain;
   const float* qconst;
   float* partials;  // [B chunk][Hkv][n_items][2][kPartialFloats]
-  int* counters;    // [(b ngpr + group) Hkv + h]
   const float* R_VT;
   float pscale, inv_pscale;
   float* out;  // [B chunk][Hq][128]
@@ -1747,103 +1746,6 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
   }
 }
 
-// The last block of a (request, KV head, query group) merges the records of
-// every page range for the group's rows (row r = query ql of the group, head
-// n: r = ql g + n), then applies R_V^T to the rotated-basis part as one
-// 128 x 128 x 128 product, joins the original-basis part and normalises.
-// Shared memory: R_V^T [128][128], the merged rotated and original parts
-// [128 rows][128], per row (M_r, L_r, M_p, L_p).
-__device__ __noinline__ void extend_final_merge(const ExtendArgs& a, uint8_t* smem, int b, int h, int grp, int z) {
-  const int t = threadIdx.x, nthr = blockDim.x, warp = t >> 5, lane = t & 31;
-  const int g = a.g, X = a.n_items;
-  float* rvt = reinterpret_cast<float*>(smem);
-  float* ys = rvt + 128 * 128;
-  float* ps = ys + 128 * 128;
-  float4* rs = reinterpret_cast<float4*>(ps + 128 * 128);
-  for (int e = t; e < 128 * 128 / 4; e += nthr)
-    reinterpret_cast<float4*>(rvt)[e] = __ldg(reinterpret_cast<const float4*>(a.R_VT) + e);
-  if (t == 0) a.counters[z * a.Hkv + h] = 0;  // ready for the next launch on this workspace
-  // the records, both kinds, by (row, 4-channel quad): a row's 32 quads in one warp; four page
-  // ranges' loads are issued before their merges
-  for (int task = t; task < 128 * 32; task += nthr) {
-    const int r = task >> 5, c4 = task & 31, ql = r / g, n = r % g, qi = grp * a.qpg + ql;
-    float Mr = -INFINITY, Lr = 0.f, Mp = -INFINITY, Lp = 0.f;
-    float4 yr = make_float4(0.f, 0.f, 0.f, 0.f), yp = yr;
-    if (ql < a.qpg && qi < a.chunk) {
-      const float* rec0 = a.partials + ((size_t)(b * a.chunk + qi) * a.Hkv + h) * X * 2 * kPartialFloats;
-      int x = 0;
-      for (; x + 4 <= X; x += 4) {
-        float mx[8], lx[8];
-        float4 vx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float* rc = rec0 + (size_t)(2 * x + i) * kPartialFloats;  // page range x + i / 2, kind i % 2
-          mx[i] = __ldcg(rc + n);
-          lx[i] = __ldcg(rc + 8 + n);
-          vx[i] = __ldcg(reinterpret_cast<const float4*>(rc + 16 + n * kStateStride) + c4);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          merge_record(Mr, Lr, yr, mx[i], lx[i], vx[i]);
-          merge_record(Mp, Lp, yp, mx[i + 1], lx[i + 1], vx[i + 1]);
-        }
-      }
-      for (; x < X; ++x) {
-        const float* rc = rec0 + (size_t)2 * x * kPartialFloats;
-        merge_record(Mr, Lr, yr, __ldcg(rc + n), __ldcg(rc + 8 + n),
-                     __ldcg(reinterpret_cast<const float4*>(rc + 16 + n * kStateStride) + c4));
-        rc += kPartialFloats;
-        merge_record(Mp, Lp, yp, __ldcg(rc + n), __ldcg(rc + 8 + n),
-                     __ldcg(reinterpret_cast<const float4*>(rc + 16 + n * kStateStride) + c4));
-      }
-    }
-    reinterpret_cast<float4*>(ys + r * 128)[c4] = yr;
-    reinterpret_cast<float4*>(ps + r * 128)[c4] = yp;
-    if (c4 == 0) rs[r] = make_float4(Mr, Lr, Mp, Lp);
-  }
-  __syncthreads();
-  // y R_V^T: warp w takes rows 8 rb .. 8 rb + 7 (rb = w, w + warps, ...), lane the output
-  // channels 4 lane .. 4 lane + 3; the sums run over the input channels in order
-  for (int rb = warp; rb < 16; rb += nthr >> 5) {
-    float o[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    for (int k = 0; k < 128; k += 4) {
-      float4 y[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = *reinterpret_cast<const float4*>(ys + (8 * rb + i) * 128 + k);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const float4 rr = reinterpret_cast<const float4*>(rvt + (k + kk) * 128)[lane];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float yk = kk == 0 ? y[i].x : kk == 1 ? y[i].y : kk == 2 ? y[i].z : y[i].w;
-          o[i][0] = fmaf(yk, rr.x, o[i][0]);
-          o[i][1] = fmaf(yk, rr.y, o[i][1]);
-          o[i][2] = fmaf(yk, rr.z, o[i][2]);
-          o[i][3] = fmaf(yk, rr.w, o[i][3]);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = 8 * rb + i, ql = r / g, n = r % g, qi = grp * a.qpg + ql;
-      if (ql >= a.qpg || qi >= a.chunk) continue;
-      const float4 st = rs[r];
-      const float M = fmaxf(st.x, st.z);
-      float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (M != -INFINITY) {
-        const float fr = ex2(st.x - M), fp = ex2(st.z - M);
-        const float inv_l = 1.0f / (fr * st.y + fp * st.w);
-        const float4 yp = reinterpret_cast<const float4*>(ps + r * 128)[lane];
-        res = make_float4((fr * o[i][0] + fp * yp.x) * inv_l, (fr * o[i][1] + fp * yp.y) * inv_l,
-                          (fr * o[i][2] + fp * yp.z) * inv_l, (fr * o[i][3] + fp * yp.w) * inv_l);
-      }
-      *reinterpret_cast<float4*>(a.out + ((size_t)(b * a.chunk + qi) * a.Hq + h * g + n) * kD + 4 * lane) = res;
-    }
-  }
-}
-
 // ---------------------------------------------------------------- extend attention on tcgen05
 // One block per (item = page range, KV head, group of 128 / g queries): the
 // group's (query, head) pairs are the 128 rows of every MMA (TMEM lane =
@@ -1873,7 +1775,6 @@ constexpr uint32_t kXtX = kXtBars + 256;  // softmax halves: page maxima [2][2][
 constexpr uint32_t kXtTi = kXtX + 3072;   // staged BF16 tiles: [8] {valid rows, first row, ring}
 constexpr int kXtStaged = 8;              // BF16 tiles an item may stage (8 KB each, in the q' staging area)
 constexpr size_t kXtSmem = kXtTi + kXtStaged * 16 + 1024;  // + 1024-byte alignment slack
-static_assert(3 * 128 * 128 * 4 + 128 * 16 <= kXtSmem - 1024, "the final merge's arrays in shared memory");
 static_assert(kXtStaged * 8192 <= 65536, "staged BF16 tiles in the q' staging area");
 static_assert(kXtK == kXtQ + 65536 && kXtV == kXtK + kXtTiles * 16384 && kXtRaw == kXtV + kXtTiles * 16384,
               "extend staging");
@@ -2401,22 +2302,117 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
     }
   }
   tc_fence_before();
-  griddep_launch_dependents();
-  __shared__ int s_last;
+  griddep_launch_dependents();  // the merge kernel may stage R_V^T
   __syncthreads();
   if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-  if (t == 0) {
-    int ticket;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;\n" : "=r"(ticket) : "l"(&a.counters[z * a.Hkv + h]) : "memory");
-    s_last = (ticket == a.n_items - 1);
+}
+
+// The merge of the chunk kernel's records: one block per (KV head, request and
+// query group, slice of 16 rows; row r = query ql of the group, head n:
+// r = ql g + n).  Every page range's records of both kinds are merged per
+// (row, 4-channel quad), then the rotated-basis part is multiplied by R_V^T
+// (staged before the dependency wait: a constant of the layer), joined with
+// the original-basis part and normalised.
+constexpr int kMgRows = 16;
+constexpr int kMgThreads = 256;
+constexpr size_t kMgSmem = (size_t)(128 * 128 + 2 * kMgRows * 128) * 4 + kMgRows * 16;
+
+__global__ void __launch_bounds__(kMgThreads) extend_merge_kernel(const __grid_constant__ ExtendArgs a) {
+  extern __shared__ float4 mg_raw[];
+  float* rvt = reinterpret_cast<float*>(mg_raw);  // R_V^T [128][128]
+  float* ys = rvt + 128 * 128;                   // merged rotated-basis parts [16 rows][128]
+  float* ps = ys + kMgRows * 128;                // merged original-basis parts [16 rows][128]
+  float4* rs = reinterpret_cast<float4*>(ps + kMgRows * 128);  // per row (M_r, L_r, M_p, L_p)
+  const int h = blockIdx.x, z = blockIdx.y, r0 = blockIdx.z * kMgRows;
+  const int b = z / a.ngpr, grp = z % a.ngpr;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, g = a.g, X = a.n_items;
+  for (int e = t; e < 128 * 128 / 4; e += kMgThreads)
+    reinterpret_cast<float4*>(rvt)[e] = __ldg(reinterpret_cast<const float4*>(a.R_VT) + e);
+  griddep_wait();
+  // the records, both kinds, by (row, 4-channel quad): a row's 32 quads in one warp; per eight
+  // page ranges, lane i loads m and l of record i and every lane its quads of all sixteen, which
+  // then merge in page-range order
+  for (int task = t; task < kMgRows * 32; task += kMgThreads) {
+    const int j = task >> 5, c4 = task & 31, r = r0 + j, ql = r / g, n = r % g, qi = grp * a.qpg + ql;
+    float Mr = -INFINITY, Lr = 0.f, Mp = -INFINITY, Lp = 0.f;
+    float4 yr = make_float4(0.f, 0.f, 0.f, 0.f), yp = yr;
+    if (ql < a.qpg && qi < a.chunk) {
+      const float* rec0 = a.partials + ((size_t)(b * a.chunk + qi) * a.Hkv + h) * X * 2 * kPartialFloats;
+      for (int x0 = 0; x0 < X; x0 += 8) {
+        const int nr = 2 * min(8, X - x0);  // records of this round: page range x0 + i / 2, kind i % 2
+        float mv = -INFINITY, lv = 0.f;
+        if (lane < nr) {
+          const float* rc = rec0 + (size_t)(2 * x0 + lane) * kPartialFloats;
+          mv = __ldcg(rc + n);
+          lv = __ldcg(rc + 8 + n);
+        }
+        float4 v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < nr)
+            v[i] = __ldcg(reinterpret_cast<const float4*>(rec0 + (size_t)(2 * x0 + i) * kPartialFloats + 16 +
+                                                          n * kStateStride) + c4);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float mi = __shfl_sync(0xffffffffu, mv, i), li = __shfl_sync(0xffffffffu, lv, i);
+          if (i < nr) {
+            if (i & 1)
+              merge_record(Mp, Lp, yp, mi, li, v[i]);
+            else
+              merge_record(Mr, Lr, yr, mi, li, v[i]);
+          }
+        }
+      }
+    }
+    reinterpret_cast<float4*>(ys + j * 128)[c4] = yr;
+    reinterpret_cast<float4*>(ps + j * 128)[c4] = yp;
+    if (c4 == 0) rs[j] = make_float4(Mr, Lr, Mp, Lp);
   }
   __syncthreads();
-  if (!s_last) return;
-  extend_final_merge(a, sm, b, h, grp, z);
+  // y R_V^T: warp w takes rows 2 w and 2 w + 1 of the slice, lane the output channels 4 lane ..
+  // 4 lane + 3; the sums run over the input channels in order
+  float o[2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int k = 0; k < 128; k += 4) {
+    const float4 y0 = *reinterpret_cast<const float4*>(ys + (2 * warp) * 128 + k);
+    const float4 y1 = *reinterpret_cast<const float4*>(ys + (2 * warp + 1) * 128 + k);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 rr = reinterpret_cast<const float4*>(rvt + (k + kk) * 128)[lane];
+      const float ya = kk == 0 ? y0.x : kk == 1 ? y0.y : kk == 2 ? y0.z : y0.w;
+      const float yb = kk == 0 ? y1.x : kk == 1 ? y1.y : kk == 2 ? y1.z : y1.w;
+      o[0][0] = fmaf(ya, rr.x, o[0][0]);
+      o[0][1] = fmaf(ya, rr.y, o[0][1]);
+      o[0][2] = fmaf(ya, rr.z, o[0][2]);
+      o[0][3] = fmaf(ya, rr.w, o[0][3]);
+      o[1][0] = fmaf(yb, rr.x, o[1][0]);
+      o[1][1] = fmaf(yb, rr.y, o[1][1]);
+      o[1][2] = fmaf(yb, rr.z, o[1][2]);
+      o[1][3] = fmaf(yb, rr.w, o[1][3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = 2 * warp + i, r = r0 + j, ql = r / g, n = r % g, qi = grp * a.qpg + ql;
+    if (ql >= a.qpg || qi >= a.chunk) continue;
+    const float4 st = rs[j];
+    const float M = fmaxf(st.x, st.z);
+    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      const float fr = ex2(st.x - M), fp = ex2(st.z - M);
+      const float inv_l = 1.0f / (fr * st.y + fp * st.w);
+      const float4 yp = reinterpret_cast<const float4*>(ps + j * 128)[lane];
+      res = make_float4((fr * o[i][0] + fp * yp.x) * inv_l, (fr * o[i][1] + fp * yp.y) * inv_l,
+                        (fr * o[i][2] + fp * yp.z) * inv_l, (fr * o[i][3] + fp * yp.w) * inv_l);
+    }
+    *reinterpret_cast<float4*>(a.out + ((size_t)(b * a.chunk + qi) * a.Hq + h * g + n) * kD + 4 * lane) = res;
+  }
 }
+static_assert(kMgRows == 2 * (kMgThreads / 32), "two rows a warp in the R_V^T product");
 
 constexpr size_t decode_smem_bytes() { return kSlotsOffset + (size_t)kBf16Slots * kPartialFloats * sizeof(float); }
 // a warp state fits in one stage (the rotated-basis one in the warp's first
@@ -2682,7 +2678,6 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   a.qplain = pa.qplain;
   a.qconst = pa.qconst;
   a.partials = reinterpret_cast<float*>(ws + p.off_partials);
-  a.counters = pa.counters;
   a.R_VT = e.rot.R_VT;
   {
     const float smax = std::isfinite(e.rot.tau_v) ? fminf(65504.f, e.rot.tau_v / 1.5f * 1.001f) : 65504.f;
@@ -2697,8 +2692,14 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   err = smem_attr_once(reinterpret_cast<const void*>(extend_tc_kernel), kXtSmem, attr_done);
   if (err != cudaSuccess) return err;
   void* args[] = {&a};
-  return launch_pdl(reinterpret_cast<const void*>(extend_tc_kernel), dim3(p.Hkv, p.batch * p.ngpr, p.n_items),
-                    dim3(kXtThreads), kXtSmem, stream, args);
+  err = launch_pdl(reinterpret_cast<const void*>(extend_tc_kernel), dim3(p.Hkv, p.batch * p.ngpr, p.n_items),
+                   dim3(kXtThreads), kXtSmem, stream, args);
+  if (err != cudaSuccess) return err;
+  static std::atomic<uint64_t> attr_done_mg;
+  err = smem_attr_once(reinterpret_cast<const void*>(extend_merge_kernel), kMgSmem, attr_done_mg);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(reinterpret_cast<const void*>(extend_merge_kernel), dim3(p.Hkv, p.batch * p.ngpr, 128 / kMgRows),
+                    dim3(kMgThreads), kMgSmem, stream, args);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
