@@ -881,10 +881,12 @@ def run_cuda(args):
                 "hbm_frac_prefix_once": e_bytes / (c_ms / 1e3) / 1e9 / peak_e,
                 "attention_tflops": c_flop / (c_ms / 1e3) / 1e12})
             del wsc_t
-        ext["chunk_kernel_note"] = ("oscar_extend_chunk: one block per (KV head, 128 / g queries, page range); a "
-                                    "page is unpacked once into fp16 tiles shared by the block's 128 (query, head) "
-                                    "rows, the MMAs on tcgen05 with S and O in tensor memory; attention_tflops "
-                                    "counts Q.K and P.V over each query's causal prefix")
+        ext["chunk_kernel_note"] = ("oscar_extend_chunk: one block per (KV head, 128 / g queries, page range), the "
+                                    "page ranges sized by a wave cost model; a page is unpacked once into fp16 "
+                                    "tiles shared by the block's 128 (query, head) rows, the MMAs on tcgen05 with S "
+                                    "and O in tensor memory; a second kernel merges the page ranges' records on "
+                                    "every SM; attention_tflops counts Q.K and P.V over each query's causal prefix "
+                                    "(the tensor cores execute twice that: value and residual parts of q' and of P)")
 
     # ---- serving batches: 28 x 100K over 36 resident layers with the same-shape BF16
     # comparator sized to fit, then the ragged 64-request batch of a 64-layer stack

@@ -1784,8 +1784,8 @@ __global__ void __launch_bounds__(kXtThreads, 1) extend_tc_kernel(const __grid_c
   const uint32_t raw_s = smem_u32(xt_raw);
   uint8_t* sm = xt_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   const uint32_t sbase = smem_u32(sm);
-  // blocks run KV head first and page range last, so that every (request, group, KV head)
-  // finishes its last range, and runs its final merge, in the last wave
+  // blocks run KV head first and page range last: every (request, group, KV head) has its last,
+  // possibly shorter, range in the last wave
   const int h = blockIdx.x, z = blockIdx.y, item = blockIdx.z;
   const int b = z / a.ngpr, grp = z % a.ngpr;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -2600,9 +2600,9 @@ ExtendPlan plan_extend(int batch, int chunk, int Hq, int Hkv, int max_ctx_len, i
   int pages = (hist_end + kPage - 1) / kPage - 1;
   if (pages < 0) pages = 0;
   // Pages per page range C: the split whose waves of blocks (one block per SM)
-  // and final merge finish first.  In units of one page's period (~1.5 us at
-  // 100K tokens): a block's fixed work (q' staging, the BF16 tiles, its
-  // records) ~8, and every page range ~3 more in the last block's merge.
+  // and records' merge finish first.  In units of one page's period (~1.5 us
+  // at 100K tokens): a block's fixed work (q' staging, the BF16 tiles, its
+  // records) ~8, and every page range ~3 more of records to merge.
   const long long pairs = (long long)batch * p.ngpr * Hkv;
   const long long slots = num_sms > 0 ? num_sms : 148;
   long long C = 2;
