@@ -450,7 +450,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[bb]);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = v[e] + w[e];
+        for (int e = 0; e < 32; e += 2) {
+          const float2 s2 = fadd2(make_float2(v[e], v[e + 1]), make_float2(w[e], w[e + 1]));
+          x[e] = s2.x;
+          x[e + 1] = s2.y;
+        }
       }
       float mq[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
@@ -489,9 +493,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (fast) {
           uint32_t part[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};  // short chains: by word and k
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
+          for (int e = 0; e < 32; e += 2) {
+            const float2 f = ffma2_rd(make_float2(x[e], x[e + 1]), make_float2(inv, inv), make_float2(kMagic, kMagic));
             const int kk = e >> 3, b = e & 7;
-            part[b >> 2][kk] += __float_as_uint(__fmaf_rd(x[e], inv, kMagic)) * (1u << (8 * (b & 3) + 2 * kk));
+            part[b >> 2][kk] += __float_as_uint(f.x) * (1u << (8 * (b & 3) + 2 * kk));
+            part[(b + 1) >> 2][kk] += __float_as_uint(f.y) * (1u << (8 * ((b + 1) & 3) + 2 * kk));
           }
           kw[0] = ((part[0][0] + part[0][1]) + (part[0][2] + part[0][3])) - kMagicBits * 0x55555555u;
           kw[1] = ((part[1][0] + part[1][1]) + (part[1][2] + part[1][3])) - kMagicBits * 0x55555555u;
@@ -512,8 +518,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int b = 0; b < 8; ++b) vb[b] = 0u;
         if (fast) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            vb[e & 7] += __float_as_uint(__fmaf_rd(x[e], inv, kMagic)) * (1u << (2 * (e >> 3)));
+          for (int e = 0; e < 32; e += 2) {
+            const float2 f = ffma2_rd(make_float2(x[e], x[e + 1]), make_float2(inv, inv), make_float2(kMagic, kMagic));
+            vb[e & 7] += __float_as_uint(f.x) * (1u << (2 * (e >> 3)));
+            vb[(e + 1) & 7] += __float_as_uint(f.y) * (1u << (2 * (e >> 3)));
+          }
 #pragma unroll
           for (int b = 0; b < 8; ++b) vb[b] -= kMagicBits * 0x55u;
         } else {
