@@ -167,14 +167,15 @@ def test_extend_chunk_refuses_gqa_above_4():
         s.close()
 
 
-@pytest.mark.parametrize("path,n", [("per_query", 16), ("per_query", 256), ("chunk", 16), ("chunk", 64),
-                                    ("chunk", 256)])
+@pytest.mark.parametrize("path,n", [("per_query", 16), ("per_query", 256), ("chunk", 16), ("chunk", 40),
+                                    ("chunk", 64), ("chunk", 256)])
 def test_extend_after_a_100k_prefix(path, n):
     """Both extend paths at the sizes the benchmark times: a chunk of n tokens after a
     100,000-token prefix (long page loops per block, many work items per (query, KV
     head), the records' merge at full width), checked on sampled queries.  The chunk
     kernel splits the history into 19, 9 and 7 page ranges for n = 16, 64 and 256 (two,
-    three and three BF16 tiles staged per range)."""
+    three and three BF16 tiles staged per range); at n = 40 its second query group holds
+    8 of 32 queries."""
     cfg, Hq, Hkv, P = 46, 32, 8, 100_000
     L = P + n
     s = harness.Setup(Hq, Hkv, L, 1, cfg=cfg)
