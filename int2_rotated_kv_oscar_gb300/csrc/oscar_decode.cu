@@ -1665,9 +1665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The queries of a chunk read the same cached pages: one block serves one
 // (page range, KV head, group of queries) and unpacks each page once for the
 // whole group (the kernel below).  Records: per (query, KV head, item) a
-// rotated-basis (INT2) and an original-basis (BF16) state; the last block of
-// each (request, KV head, query group) merges them, applies R_V^T and
-// normalises.
+// rotated-basis (INT2) and an original-basis (BF16) state; a second kernel
+// merges every item's records, applies R_V^T and normalises.
 struct ExtendArgs {
   CacheRefs c;
   const int32_t* ctx_len;  // [B] cache lengths
@@ -1747,14 +1746,17 @@ __device__ __forceinline__ void ext_unpack(const uint8_t* raw, uint8_t* kp, uint
 }
 
 // ---------------------------------------------------------------- extend attention on tcgen05
-// One block per (item = page range, KV head, group of 128 / g queries): the
-// group's (query, head) pairs are the 128 rows of every MMA (TMEM lane =
-// row).  Per INT2 page: S = Q'_value K^T + Q'_residual K^T for each 64-channel
-// group (f16 MMAs into TMEM), one softmax thread per row (its query's causal
-// limit, lazy rescaling of its O row in TMEM), P s_v as fp16 value + residual
-// operands, O += P V (V transposed).  The A operands (q' and P) sit in TMEM,
-// so an MMA reads only its B tile (K or V^T, 128-byte-swizzled) from shared
-// memory.  S of the next page overlaps the softmax of this one.  Warps:
+// One block per (KV head, group of 128 / g queries, item = page range; the
+// ranges sized by the plan's wave cost model): the group's (query, head)
+// pairs are the 128 rows of every MMA (TMEM lane = row).  Per INT2 page:
+// S = Q'_value K^T + Q'_residual K^T for each 64-channel group (f16 MMAs into
+// TMEM), one softmax thread per row and half page (its query's causal limit,
+// lazy rescaling of its half of the O row in TMEM), P s_v as fp16 value and
+// negated residual operands, O += P V (V transposed; the residual MMAs negate
+// A).  The A operands (q' and P) sit in TMEM, so an MMA reads only its B tile
+// (K or V^T, 128-byte-swizzled) from shared memory.  S of the next page
+// overlaps the softmax of this one.  Each block writes its rows' records;
+// extend_merge_kernel merges the ranges.  Warps:
 //   0-3, 9-12  softmax, two warpgroups splitting every page (tokens 0-31, 32-63) and O's
 //        columns; warps 0-3 first put the q' rows into TMEM, then all eight run the
 //        BF16 sink/recent tiles (per query, mma.sync, original-basis records) while
