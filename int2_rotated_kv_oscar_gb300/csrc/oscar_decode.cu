@@ -125,6 +125,7 @@ struct PrepArgs {
   uint32_t* qplain;
   float* qconst;
   int* counters;
+  int nb, per_block;  // rows (request or query) to rotate; rows per block of prep_kernel
 };
 
 // ------------------------------------------------------------------ prep
@@ -273,18 +274,37 @@ __device__ __forceinline__ void prep_body(const PrepArgs& a, int b, int h, int u
   }
 }
 
-// grid (Hkv, B), kPrepThreads threads
+// grid (Hkv, ceil(nb / per_block)), kPrepThreads threads: a block rotates rows
+// per_block y .. of KV head x with its rows of R_K in registers (a constant of
+// the layer, loaded before the dependency wait)
 __global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(PrepArgs a) {
   __shared__ PrepSmem sm;
+  const int h = blockIdx.x, u = threadIdx.x;
+  float rk[32];  // R_K[32 (u / 128) + ii][u % 128]
+  {
+    const float* RK = a.R_K + (size_t)32 * (u >> 7) * kD + (u & 127);
+#pragma unroll
+    for (int ii = 0; ii < 32; ++ii) rk[ii] = __ldg(RK + ii * kD);
+  }
   griddep_wait();
   griddep_launch_dependents();
-  const int b = blockIdx.y, h = blockIdx.x, u = threadIdx.x, bh = b * a.Hkv + h;
-  if (u == 0) a.counters[bh] = 0;
-  const float* RK = a.R_K + (size_t)32 * (u >> 7) * kD + (u & 127);
-  const uint16_t* qrow = a.q + ((size_t)b * a.Hq + h * a.g) * kD + (u & 127);
-  prep_body(a, b, h, u, [&](int ii) { return RK[ii * kD]; }, [&](int n) { return qrow[(size_t)n * kD]; }, sm, 1,
-            a.qfrag + (size_t)bh * kQFragWords, a.qplain + (size_t)bh * kQFragWords,
-            a.qconst + (size_t)bh * kQConstFloats, [] {});
+  const int b0 = blockIdx.y * a.per_block, b1 = min(b0 + a.per_block, a.nb);
+  for (int b = b0; b < b1; ++b) {
+    const int bh = b * a.Hkv + h;
+    if (u == 0) a.counters[bh] = 0;
+    const uint16_t* qrow = a.q + ((size_t)b * a.Hq + h * a.g) * kD + (u & 127);
+    prep_body(a, b, h, u, [&](int ii) { return rk[ii]; }, [&](int n) { return qrow[(size_t)n * kD]; }, sm, 1,
+              a.qfrag + (size_t)bh * kQFragWords, a.qplain + (size_t)bh * kQFragWords,
+              a.qconst + (size_t)bh * kQConstFloats, [] {});
+    group_sync(1, kPrepThreads);  // the next row reuses the scratch
+  }
+}
+
+// rows per prep block: about two blocks per SM
+int prep_rows_per_block(int nb, int Hkv, int num_sms) {
+  const long long slots = 2LL * (num_sms > 0 ? num_sms : 148);
+  const long long per = ((long long)nb * Hkv + slots - 1) / slots;
+  return (int)(per < 1 ? 1 : per);
 }
 
 // ------------------------------------------------------------------ decode
@@ -2503,6 +2523,7 @@ DecodePlan plan_decode(int mode, int batch, int Hq, int Hkv, int max_ctx_len, in
   p.off_partials = off;
   p.rec_floats = partial_record_floats(p.g);
   off = align256(off + bh * (size_t)p.n_items * p.rec_floats * sizeof(float));
+  p.prep_rows = prep_rows_per_block(batch, Hkv, num_sms);
   p.total = off;
   return p;
 }
@@ -2524,6 +2545,8 @@ PrepArgs prep_args_of(const DecodeLaunch& d) {
   pa.qplain = reinterpret_cast<uint32_t*>(ws + p.off_qplain);
   pa.qconst = reinterpret_cast<float*>(ws + p.off_qconst);
   pa.counters = reinterpret_cast<int*>(ws + p.off_counters);
+  pa.nb = p.batch;
+  pa.per_block = p.prep_rows;
   return pa;
 }
 
@@ -2639,6 +2662,7 @@ ExtendPlan plan_extend(int batch, int chunk, int Hq, int Hkv, int max_ctx_len, i
   off = align256(off + bq * kQConstFloats * sizeof(float));
   p.off_partials = off;
   off = align256(off + bq * (size_t)p.n_items * 2 * kPartialFloats * sizeof(float));
+  p.prep_rows = prep_rows_per_block(batch * chunk, Hkv, num_sms);
   p.total = off;
   return p;
 }
@@ -2659,9 +2683,12 @@ cudaError_t launch_extend(const ExtendLaunch& e, cudaStream_t stream) {
   pa.qplain = reinterpret_cast<uint32_t*>(ws + p.off_qplain);
   pa.qconst = reinterpret_cast<float*>(ws + p.off_qconst);
   pa.counters = reinterpret_cast<int*>(ws + p.off_counters);
+  pa.nb = p.batch * p.chunk;
+  pa.per_block = p.prep_rows;
   void* pargs[] = {&pa};
-  cudaError_t err = launch_pdl(reinterpret_cast<const void*>(prep_kernel), dim3(p.Hkv, p.batch * p.chunk),
-                               dim3(kPrepThreads), 0, stream, pargs);
+  cudaError_t err = launch_pdl(reinterpret_cast<const void*>(prep_kernel),
+                               dim3(p.Hkv, (pa.nb + p.prep_rows - 1) / p.prep_rows), dim3(kPrepThreads), 0, stream,
+                               pargs);
   if (err != cudaSuccess) return err;
   ExtendArgs a;
   a.c = e.c;
@@ -2709,7 +2736,8 @@ cudaError_t launch_decode(const DecodeLaunch& d, cudaStream_t stream) {
   if (p.batch == 0) return cudaSuccess;
   PrepArgs pa = prep_args_of(d);
   void* args[] = {&pa};
-  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(prep_kernel), dim3(p.Hkv, p.batch), dim3(kPrepThreads), 0, stream,
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(prep_kernel),
+                             dim3(p.Hkv, (p.batch + p.prep_rows - 1) / p.prep_rows), dim3(kPrepThreads), 0, stream,
                              args);
   if (e != cudaSuccess) return e;
   return launch_decode_kernel(d, pa, stream);

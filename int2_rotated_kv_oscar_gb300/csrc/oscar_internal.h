@@ -105,6 +105,7 @@ struct DecodePlan {
   int32_t n_items = 0;       // all work items per (request, KV head)
   int32_t tiles_per_item = 0;  // mixed cache: BF16 sink/recent tiles per item (items 0, 1, ... take them)
   int32_t rec_floats = 0;      // floats per partial record
+  int32_t prep_rows = 1;       // rows (requests) per block of the q rotation kernel
   size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
 };
 
@@ -146,6 +147,7 @@ struct ExtendPlan {
   int32_t ngpr = 0;            // query groups per request
   int32_t qpg = 0;             // queries per group: 128 / g (the group's (query, head) rows fill one MMA)
   int32_t chunk_pages = 0, n_items = 0, tiles_per_item = 0;
+  int32_t prep_rows = 1;       // rows (queries) per block of the q rotation kernel
   size_t off_counters = 0, off_qfrag = 0, off_qplain = 0, off_qconst = 0, off_partials = 0, total = 0;
 };
 ExtendPlan plan_extend(int batch, int chunk, int Hq, int Hkv, int max_ctx_len, int num_sms);
