@@ -786,21 +786,26 @@ __device__ __forceinline__ void bf16_tile(const uint16_t* __restrict__ Kt, const
 // (exact products; the softmax scale cE = sm_scale log2 e is applied to the
 // fp32 logits), P.V against B = p 2^11 as a bf16 value + residual pair.  The
 // lane's accumulator columns are heads 2 tig and 2 tig + 1 (store_state<false>).
+// The tile's 16 K rows and 16 V rows sit in shared memory, kRawRow bytes
+// apart (a row's 256 bytes plus 16, so that the fragment loads of the 16 rows
+// spread over the banks).  Two halves: Q.K and the softmax give the B words
+// of P.V (bw), then P.V.
 // qb: the lane's B words of Q.K, word 2 ks + i = q[head lane / 4][32 tig + 4 ks + 2 i .. + 1].
-__device__ __forceinline__ void bf16_tile_raw(const uint16_t* __restrict__ Kt, const uint16_t* __restrict__ Vt,
-                                              int nv, const uint32_t (&qb)[16], float cE, WarpState& st, int lane) {
+constexpr int kRawRow = 2 * kD + 16;
+__device__ __forceinline__ void bf16_raw_qk(const uint8_t* Ks, int nv, const uint32_t (&qb)[16], float cE,
+                                            WarpState& st, int lane, uint32_t (&bw)[4]) {
   const int q = lane >> 2, tig = lane & 3;
   const bool va = q < nv, vb = q + 8 < nv;
   uint32_t ka[16], kb[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint4 u = va ? __ldg(reinterpret_cast<const uint4*>(Kt + q * kD + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+    const uint4 u = va ? *reinterpret_cast<const uint4*>(Ks + q * kRawRow + 64 * tig + 16 * k) : make_uint4(0, 0, 0, 0);
     ka[4 * k] = u.x;
     ka[4 * k + 1] = u.y;
     ka[4 * k + 2] = u.z;
     ka[4 * k + 3] = u.w;
     const uint4 w =
-        vb ? __ldg(reinterpret_cast<const uint4*>(Kt + (q + 8) * kD + 32 * tig) + k) : make_uint4(0, 0, 0, 0);
+        vb ? *reinterpret_cast<const uint4*>(Ks + (q + 8) * kRawRow + 64 * tig + 16 * k) : make_uint4(0, 0, 0, 0);
     kb[4 * k] = w.x;
     kb[4 * k + 1] = w.y;
     kb[4 * k + 2] = w.z;
@@ -821,13 +826,16 @@ __device__ __forceinline__ void bf16_tile_raw(const uint16_t* __restrict__ Kt, c
     hi = pack_bf16x2(x0, x1);
     lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
   };
-  uint32_t b0h, b0l, b1h, b1l;
-  split(p0, p1, b0h, b0l);
-  split(p2, p3, b1h, b1l);
-  b0h = movmatrix_trans(b0h);
-  b0l = movmatrix_trans(b0l);
-  b1h = movmatrix_trans(b1h);
-  b1l = movmatrix_trans(b1l);
+  split(p0, p1, bw[0], bw[1]);
+  split(p2, p3, bw[2], bw[3]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) bw[i] = movmatrix_trans(bw[i]);
+}
+
+__device__ __forceinline__ void bf16_raw_pv(const uint8_t* Vs, int nv, const uint32_t (&bw)[4], WarpState& st,
+                                            int lane) {
+  const int q = lane >> 2, tig = lane & 3;
+  const bool va = q < nv, vb = q + 8 < nv;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     uint32_t a[4];
@@ -835,12 +843,12 @@ __device__ __forceinline__ void bf16_tile_raw(const uint16_t* __restrict__ Kt, c
     for (int blkid = 0; blkid < 4; ++blkid) {
       const int tr = blkid >> 1, cc = blkid & 1;  // token half, channel half
       const int r = 8 * tr + q;
-      const uint32_t u = (tr ? vb : va) ? __ldg(reinterpret_cast<const uint32_t*>(Vt + r * kD + 16 * mt + 8 * cc + 2 * tig)) : 0u;
+      const uint32_t u = (tr ? vb : va) ? *reinterpret_cast<const uint32_t*>(Vs + r * kRawRow + 32 * mt + 16 * cc + 4 * tig) : 0u;
       a[blkid] = movmatrix_trans(u);
     }
     // a[0]: channels 16mt+q, tokens 2tig..; a[1]: channels +8; a[2]: tokens +8; a[3]: both
-    mma_bf16_acc(st.acc[mt], a[0], a[1], a[2], a[3], b0h, b1h);
-    mma_bf16_acc(st.acc[mt], a[0], a[1], a[2], a[3], b0l, b1l);
+    mma_bf16_acc(st.acc[mt], a[0], a[1], a[2], a[3], bw[0], bw[2]);
+    mma_bf16_acc(st.acc[mt], a[0], a[1], a[2], a[3], bw[1], bw[3]);
   }
 }
 
@@ -1594,9 +1602,6 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
       __syncwarp();
     }
     store_int2_state<PACK4>(st, wstate, a.inv_pscale, lane);
-  } else {
-    state_init(st);
-    store_state<PACK4>(st, wstate, 1.f, lane);
   }
 
   // ---------------- BF16 paged cache (comparator): every warp, original basis
@@ -1619,40 +1624,83 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const StepArgs*
     }
     const float cE = a.sm_scale * kLog2e;
     {
-      // plain BF16 paged cache: item covers pages [item*C, item*C + C), 4 tiles each
+      // plain BF16 paged cache: item covers pages [item*C, item*C + C), 4 tiles each;
+      // the warp's tiles i = warp + kWarps j come through its kStages stages as units
+      // 2 j (the 16 K rows) and 2 j + 1 (the 16 V rows), copied row by row (kRawRow apart)
+      // kStages units ahead
       const int n_pages = (L + kPage - 1) / kPage;
       if (n_pages > c.max_pages) {
         if (t == 0 && item == 0) set_error(a.err, kErrLength);
       }
       const int pg0 = item * a.chunk_pages;
       const int pg1 = min(min(pg0 + a.chunk_pages, n_pages), c.max_pages);
-      // tile i of the item: page pg0 + i / 4, rows 16 (i % 4) ..; the page-table
-      // entry of the warp's tile two on is read a tile ahead, and the rows of
-      // its next tile are pulled into L2 while this one is computed
-      auto entry = [&](int i) { return pg0 + i / 4 < pg1 ? c.page_table[(size_t)b * c.max_pages + pg0 + i / 4] : -1; };
-      int ph_next = entry(warp + kWarps);
-      int ph = entry(warp);
-      for (int i = warp; pg0 + i / 4 < pg1; i += kWarps) {
-        const int pg = pg0 + i / 4, tile = i & 3;
-        const int ph_cur = ph;
-        if (lane == 0 && ph_next >= 0 && ph_next < c.num_pages) {
-          const size_t offn = (((size_t)ph_next * a.Hkv + h) * kPage + 16 * ((i + kWarps) & 3)) * kD;
-          bulk_prefetch_l2(a.kb_pages + offn, 16 * kD * 2);
-          bulk_prefetch_l2(a.vb_pages + offn, 16 * kD * 2);
-        }
-        ph = ph_next;
-        ph_next = entry(i + 2 * kWarps);
-        if (ph_cur < 0 || ph_cur >= c.num_pages) {
-          if (lane == 0) set_error(a.err, kErrPage);
-          continue;
-        }
-        const int nv = min(16, L - kPage * pg - 16 * tile);
-        if (nv <= 0) continue;
-        const size_t off = (((size_t)ph_cur * a.Hkv + h) * kPage + 16 * tile) * kD;
-        bf16_tile_raw(a.kb_pages + off, a.vb_pages + off, nv, qb, cE, st, lane);
+      const int n_item_tiles = 4 * max(0, pg1 - pg0);
+      const int n_my_t = n_item_tiles > warp ? (n_item_tiles - warp + kWarps - 1) / kWarps : 0;
+      const int n_units = 2 * n_my_t;
+      uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * kBlockBytes) + warp * kStages;
+      if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
       }
+      __syncwarp();
+      auto tile_ph = [&](int j) -> int {  // physical page of the warp's tile j (-1: none or invalid)
+        if (j >= n_my_t) return -1;
+        const int ph = c.page_table[(size_t)b * c.max_pages + pg0 + (warp + kWarps * j) / 4];
+        return (ph >= 0 && ph < c.num_pages) ? ph : -1;
+      };
+      // every lane: lane 0 arms the stage, lanes 0..15 copy one row each
+      auto issue_u = [&](int u, int ph) {
+        const int s = u % kStages, i = warp + kWarps * (u >> 1);
+        if (lane == 0) {
+          fence_proxy_async_smem();  // the stage's last reads came through the generic proxy
+          if (ph < 0) {
+            set_error(a.err, kErrPage);
+            mbar_arrive(&bars[s]);
+          } else {
+            mbar_arrive_expect_tx(&bars[s], 16 * 2 * kD);
+          }
+        }
+        __syncwarp();
+        if (ph >= 0 && lane < 16) {
+          const size_t off = (((size_t)ph * a.Hkv + h) * kPage + 16 * (i & 3) + lane) * kD;
+          bulk_copy_g2s(stage_ptr(s) + lane * kRawRow, ((u & 1) ? a.vb_pages : a.kb_pages) + off, 2 * kD, &bars[s]);
+        }
+      };
+      int ph_cur = tile_ph(0), ph_n1 = tile_ph(1);
+      for (int u = 0; u < min(kStages, n_units); ++u) issue_u(u, u < 2 ? ph_cur : ph_n1);
+      int j = 0;
+      bool ok = true;
+      for (; j < n_my_t && ok; ++j) {
+        const int i = warp + kWarps * j, pg = pg0 + i / 4, tile = i & 3;
+        const int ph_n2 = tile_ph(j + 2);
+        const int nv = min(16, L - kPage * pg - 16 * tile);
+        const bool use = ph_cur >= 0 && nv > 0;
+        uint32_t bw[4];
+        const int uk = 2 * j, uv = 2 * j + 1;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[uk % kStages], (uk / kStages) & 1, kWaitLimit));
+        if (!ok) break;
+        if (use) bf16_raw_qk(stage_ptr(uk % kStages), nv, qb, cE, st, lane, bw);
+        __syncwarp();
+        if (uk + kStages < n_units) issue_u(uk + kStages, ph_n1);  // V rows of tile j + 1
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[uv % kStages], (uv / kStages) & 1, kWaitLimit));
+        if (!ok) break;
+        if (use) bf16_raw_pv(stage_ptr(uv % kStages), nv, bw, st, lane);
+        __syncwarp();
+        if (uv + kStages < n_units) issue_u(uv + kStages, ph_n2);  // K rows of tile j + 2
+        ph_cur = ph_n1;
+        ph_n1 = ph_n2;
+      }
+      if (!ok) {
+        if (lane == 0) set_error(a.err, kErrTimeout);
+        // wait (bounded) for the copies still in flight
+        for (int u = 2 * j; u < min(2 * j + kStages + 1, n_units); ++u)
+          mbar_wait_bounded(&bars[u % kStages], (u / kStages) & 1, kWaitLimit);
+      }
+      __syncwarp();
     }
     store_state<false>(st, reinterpret_cast<float*>(stage_ptr(1)), 1.0f / kPScaleBF16, lane);
+    state_init(st);
+    store_state<PACK4>(st, wstate, 1.f, lane);  // the (empty) rotated-basis state
   }
   block_merge<MODE, PACK4>(a, smem, bf16_slots, bh, item);
 

@@ -308,11 +308,13 @@ def test_host_argument_errors_launch_nothing():
         s.close()
 
 
-def test_bf16_comparator_matches_plain_attention():
-    """The BF16 paged-cache decode (the comparator) against plain attention."""
+@pytest.mark.parametrize("lens", [[1, 130, 2000], [100_000]])
+def test_bf16_comparator_matches_plain_attention(lens):
+    """The BF16 paged-cache decode (the comparator) against plain attention: short and
+    partial pages, and a 100K context (long rings of staged tile halves per warp)."""
     from int2_rotated_kv_oscar_gb300 import cache as kvcache
     from oracle import attention
-    cfg, lens = 8, [1, 130, 2000]
+    cfg = 8
     B, Hq, Hkv = len(lens), 32, 8
     s = harness.Setup(Hq, Hkv, max(lens), B, cfg=cfg, calibrate=False)
     try:
