@@ -766,22 +766,26 @@ def run_cuda(args):
     if not args.no_append:
         n_b = 131_072
         maxp_a = (n_b + 63) // 64 + 1
-        acache = kvcache.MixedCache(1, HKV, maxp_a, 1, 1, 1, maxp_a, device=dev)
-        acache.page_table.copy_(torch.from_numpy(inputs.shuffled_pages(CFG, maxp_a, layer=1).reshape(1, maxp_a)))
+        # three destination caches in turn (~226 MB of page blocks, more than L2): each call's code
+        # writes go to other lines than the previous call's, so they reach DRAM as a new prompt's would
+        n_dst = 3
+        acaches = [kvcache.MixedCache(1, HKV, maxp_a, 1, 1, 1, maxp_a, device=dev) for _ in range(n_dst)]
+        for i, ac in enumerate(acaches):
+            ac.page_table.copy_(torch.from_numpy(inputs.shuffled_pages(CFG, maxp_a, layer=1 + i).reshape(1, maxp_a)))
         ka, va = inputs.kv_tokens_device(4, 0, HKV, inputs.STREAM_KV, n_b, dev)
         cu_a = torch.tensor([0, n_b], dtype=torch.int32, device=dev)
         # a fresh prompt (position 0): nothing precedes it, so nothing is evicted -- the flag that
         # says so, as a serving engine passes it for a new request's prefill
         aargs = kvcache.append_args(ka, va, pos0, cu_a, n_b, fresh_ring=True)
-        aview = acache.view(0)
-        for _ in range(3):
-            abi.oscar_kv_append(ctx, 0, aview, aargs, cur)
+        aviews = [ac.view(0) for ac in acaches]
+        for i in range(n_dst):
+            abi.oscar_kv_append(ctx, 0, aviews[i], aargs, cur)
         torch.cuda.synchronize()
         reps = 10
         torch.cuda.nvtx.range_push("bulk_append")
         e0.record()
-        for _ in range(reps):
-            abi.oscar_kv_append(ctx, 0, aview, aargs, cur)
+        for i in range(reps):
+            abi.oscar_kv_append(ctx, 0, aviews[i % n_dst], aargs, cur)
         e1.record()
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
@@ -814,8 +818,9 @@ def run_cuda(args):
                                    "run x R three times to keep the codes exact"},
                 "note": "oscar_kv_append of one fresh 131,072-token prompt (OSCAR_APPEND_FRESH_RING: "
                         "nothing to evict; BF16 K and V in, INT2 history + BF16 sink/recent out), mean of 10 "
-                        "eager calls"}
-        del acache, ka, va
+                        "eager calls into three destination caches in turn (226 MB of page blocks, more "
+                        "than L2, so each call's writes reach DRAM)"}
+        del acaches, aviews, ka, va
 
     # ---- extend attention: the queries of a 16-token chunk at the end of the context, one layer
     ext = None

@@ -173,7 +173,6 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 constexpr int kTcRegions = 1;
 constexpr int kTcThreads = 18 * 32;
 constexpr int kTcStages = 3;
-constexpr unsigned kTcAhead = 3;           // x tiles pulled into L2 ahead of their loads
 constexpr uint32_t kTcCols = 512;          // TMEM columns: buffer bb = [t0: 128][t1 + t2: 128] from column 256 bb
 constexpr uint32_t kTcB = 0;               // R^T terms: [2 k-blocks][3 terms][128 rows n][128 B]
 constexpr uint32_t kTcA = 3 * 32768;       // x tiles: kTcStages x [2 k-blocks][128 rows][128 B]
@@ -296,6 +295,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // so that lane 0 issues each load without waiting on a table read.
     const CUtensorMap* tm = m ? &tmv : &tmk;
     if (lane == 0) prefetch_tensormap(tm);
+    // x is read once: its lines go first when L2 needs room (the code writes stay)
+    const uint64_t once = l2_policy_evict_first();
     int it = 0;  // lane 0: tiles whose loads were issued
     bool timed_out = false;
     for (unsigned base = cta; base < n_tiles && !timed_out; base += 32u * n_cta) {
@@ -314,15 +315,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       while (vmask != 0u) {
         const int j = __ffs(vmask) - 1;
         vmask &= vmask - 1u;
-        {
-          // the valid tile kTcAhead places on into L2 (a hint; the buffer ring bounds how far the loads run)
-          unsigned rest = vmask;
-          for (unsigned r = 1; r < kTcAhead && rest != 0u; ++r) rest &= rest - 1u;
-          if (rest != 0u && lane == __ffs(rest) - 1) {
-            tma_prefetch_3d(tm, 0, t.h, y0);
-            tma_prefetch_3d(tm, 64, t.h, y0);
-          }
-        }
         const int th = __shfl_sync(0xffffffffu, t.h, j), ty0 = __shfl_sync(0xffffffffu, y0, j);
         const int tb = __shfl_sync(0xffffffffu, t.b, j), tlp0 = __shfl_sync(0xffffffffu, t.lp0, j);
         const int tlo = __shfl_sync(0xffffffffu, t.lo, j), thi = __shfl_sync(0xffffffffu, t.hi, j);
@@ -335,8 +327,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           } else {
             work[s] = 1;
             mbar_arrive_expect_tx(&full[s], 32768);
-            tma_load_3d(sm + kTcA + s * 32768, tm, 0, th, ty0, &full[s]);
-            tma_load_3d(sm + kTcA + s * 32768 + 16384, tm, 64, th, ty0, &full[s]);
+            tma_load_3d(sm + kTcA + s * 32768, tm, 0, th, ty0, &full[s], once);
+            tma_load_3d(sm + kTcA + s * 32768 + 16384, tm, 64, th, ty0, &full[s], once);
             ++it;
             if (!mbar_wait_bounded(&dempty[di], (((it - 1) / kTcDescs) & 1) ^ 1, kWaitLimit)) {
               timed_out = true;
