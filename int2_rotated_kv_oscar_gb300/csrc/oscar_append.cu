@@ -288,6 +288,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_at;
+  // For a fresh prompt this kernel comes first in the call and may start before the stream's
+  // previous work has finished: the set-up above reads only the rotation tables (written by a
+  // synchronous upload), so wait here, before the inputs, tables and page blocks are touched.
+  if (a.flags & 1u) griddep_wait();
 
   if (warp == 16) {
     // x tiles by TMA; after the last tile a buffer with work = 0 tells the MMA thread to stop.  The
@@ -579,12 +583,12 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
     append_one_kernel<<<dim3(Hkv, B), 2 * kQuantThreads, 0, stream>>>(a);
     return cudaGetLastError();
   }
-  // The first kernel of the call starts after everything before it; the next
-  // ones may start early and run beside it.  The tile kernel writes only the
-  // INT2 rows of new tokens, which the eviction and BF16-row kernels do not
-  // touch; the eviction reads ring rows that the BF16-row kernel overwrites.
+  // The kernels after the first may start early and run beside it.  The tile
+  // kernel writes only the INT2 rows of new tokens, which the eviction and
+  // BF16-row kernels do not touch; the eviction reads ring rows that the
+  // BF16-row kernel overwrites.
   //   evicting:     eviction -> BF16 rows (wait first) -> tiles (wait at the end)
-  //   fresh ring:   tiles -> BF16 rows (wait at the end)
+  //   fresh ring:   tiles (set-up, then wait) -> BF16 rows (wait at the end)
   // so the last kernel of the call always ends after the others.
   AppendLaunch la = a;
   void* args1[] = {&la};
@@ -634,8 +638,7 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
   const void* tile_fn = reinterpret_cast<const void*>(append_tile_kernel);
   const void* bf16_fn = reinterpret_cast<const void*>(append_bf16_kernel);
   if (fresh) {
-    append_tile_kernel<<<blocks, kTcThreads, kTcSmem, stream>>>(a, tm[0], tm[1], t2);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(tile_fn, dim3(blocks), dim3(kTcThreads), kTcSmem, stream, args);
     if (e != cudaSuccess) return e;
     return launch_pdl(bf16_fn, dim3(kSink + kRecent, B), dim3(128), 0, stream, args1);
   }
