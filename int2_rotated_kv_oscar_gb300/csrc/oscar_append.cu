@@ -8,11 +8,11 @@
 // §2.2 A.3-4 (R = U H_Had P_br, per-layer clip thresholds) and §2.2 B (paged
 // cache, sink/recent in BF16, INT2 history after rotation and clipping).
 //
-// Rotation x' = x R uses the layer's composite R = U H P (formed on the host
-// in fp64, one dense 128 x 128 product on the device): the one-token paths
-// multiply in fp32 on the CUDA cores, the bulk path on the tensor cores with
-// R split into three bf16 terms.  Quantiser per group of 64 rotated
-// channels: a = min(max|x'|, tau), s = fp16(a / 1.5),
+// Rotation x' = x R: the bulk path multiplies by the composite R = U H P
+// (formed on the host in fp64) on the tensor cores, R as three bf16 terms;
+// the one-token paths by R in fp32 on the CUDA cores, or, without U, apply H
+// as an in-register butterfly and P as an index map.  Quantiser per group
+// of 64 rotated channels: a = min(max|x'|, tau), s = fp16(a / 1.5),
 // code = [x' >= -s] + [x' >= 0] + [x' >= s].
 
 #include <cuda.h>
