@@ -7,23 +7,23 @@
 // Serving e Layout di Memoria": sink and recent tokens stay BF16.
 //
 // Design (GB300):
-//  * prep kernel, one block per (request, KV head): q' = q R_K (fp32 x U,
-//    Walsh-Hadamard butterfly, bit reversal), times sm_scale * log2(e) and a
-//    power-of-two normalisation, split into fp16 value + fp16 residual and
-//    laid out as tensor-core B fragments; the plain q for the BF16 segment
-//    likewise; zeroes the split counters.
-//  * decode kernel, one block per (work item, KV head, request), 4 warps.
-//    Work items are chunks of INT2 history pages (rotated basis) or 64-token
-//    BF16 blocks (sink, ring quarters; original basis).  Each warp streams
-//    its pages through a private ring of shared-memory stages filled by bulk
-//    asynchronous copies (one 4608-byte copy per page), turns each pair of
-//    2-bit codes into the exact fp16 levels (c - 1.5) with one LOP3 and one
-//    HFMA2, runs QK^T and PV on mma.sync m16n8k16 (tokens x channels and
-//    channels x tokens against the query heads) with an online softmax in
-//    the log2 domain.  Warps merge in shared memory; each block writes one
-//    partial (m, l, acc); the last block of a (request, KV head) merges all
-//    partials (log-sum-exp), rotates the INT2 part back (acc P H U_V^T) and
-//    writes the fp32 output.  No block ever waits on another.
+//  * decode_step_kernel: one launch per layer step, one 16-warp block per
+//    (work item, KV head, request).  Every block rotates its request's
+//    queries, q' = q R_K (R_K rows in registers, or without U the
+//    Walsh-Hadamard butterfly and the bit-reversal index map), times
+//    sm_scale * log2(e) and a power-of-two normalisation, as fp16 value +
+//    residual tensor-core fragments; the block whose pages hold the evicted
+//    ring row appends K and V.  prep_kernel, append_one_kernel and
+//    decode_kernel run the same steps as separate launches.  Work items are
+//    ranges of INT2 history pages (rotated basis) from a wave cost model; two
+//    warps of some items also take the BF16 sink/recent tiles (original
+//    basis).  Each warp streams its pages through a private 3-stage ring of
+//    bulk copies (one 4608-byte copy per page), turns each pair of 2-bit
+//    codes into the exact fp16 levels (c - 1.5) with one LOP3 and one HFMA2,
+//    and runs QK^T and PV on mma.sync m16n8k16 with an online softmax in the
+//    log2 domain.  The block merges its warps, applies R_V^T to the INT2 part
+//    and writes one record; an acq_rel ticket picks the last block of each
+//    (request, KV head), which merges the records.  No block waits on another.
 //
 // Precision: q and the softmax weights times the V scales enter the MMAs as
 // fp16 value + fp16 residual (~22 significant bits).  With at most 4 query

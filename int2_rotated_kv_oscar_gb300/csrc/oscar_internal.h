@@ -24,9 +24,9 @@ inline cudaError_t smem_attr_once(const void* kernel, size_t bytes, std::atomic<
   return e;
 }
 
-// Rotation constants of one layer on the device.
-// One layer's rotation as dense matrices: R = U H P (the factors a layer
-// enables), formed in double precision on the host and rounded to fp32.
+// One layer's rotation constants on the device: R = U H P (the factors the
+// layer enables) as dense matrices, formed in double precision on the host
+// and rounded to fp32.
 struct LayerRotation {
   const float* R_K = nullptr;   // [128][128] row-major: a K row x is rotated as x R_K
   const float* R_V = nullptr;   // [128][128] row-major
