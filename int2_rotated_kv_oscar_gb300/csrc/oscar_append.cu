@@ -181,8 +181,9 @@ constexpr uint32_t kTcPmax = kTcBars + 512;  // [tile parity][h][g][128 rows] fl
 constexpr int kTcDescs = 8;                  // tile descriptors the TMA thread publishes ahead
 constexpr uint32_t kTcDesc = kTcPmax + 4096;
 constexpr size_t kTcSmem = kTcDesc + kTcDescs * 64 + 1024;  // + 1024-byte alignment slack
-// barriers (full, empty: kTcStages each; tfull, tempty: 4 each; done; 8 swaps; 2 kTcDescs), TMEM address, flags
-static_assert((2 * kTcStages + 8 + 1 + 8 + 2 * kTcDescs) * 8 + 4 + 4 * kTcStages <= 512, "barrier area");
+// barriers (full, empty: kTcStages each; tfull, tempty: 4 each; done; 8 swaps; 2 kTcDescs; full1:
+// kTcStages), TMEM address, flags
+static_assert((3 * kTcStages + 8 + 1 + 8 + 2 * kTcDescs) * 8 + 4 + 4 * kTcStages <= 512, "barrier area");
 
 // What the epilogue needs of a tile: positions [lo, hi) of page pair (lp0, lp0 + 1) get written
 // to blk[0], blk[1] (null: nothing to write there); b < 0 marks the end of the block's tiles.
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t raw_s = smem_u32(tc_raw);
   uint8_t* sm = tc_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   const uint32_t sbase = smem_u32(sm);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTcBars);  // [kTcStages] x tile of buffer s landed
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kTcBars);  // [kTcStages] k-block 0 of buffer s landed
   uint64_t* empty = full + kTcStages;                           // [kTcStages] buffer s read by its MMAs
   uint64_t* tfull = empty + kTcStages;                          // [4, 2 used] TMEM buffer bb holds its sums
   uint64_t* tempty = tfull + 4;                                 // [4, 2 used] TMEM buffer bb read
@@ -247,7 +248,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* xb = done + 1;                                      // [8] the two halves of (g, q) swapped maxima
   uint64_t* dfull = xb + 8;                                     // [kTcDescs] descriptor d written
   uint64_t* dempty = dfull + kTcDescs;                          // [kTcDescs] descriptor d read by the epilogue
-  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(dempty + kTcDescs);
+  uint64_t* full1 = dempty + kTcDescs;                          // [kTcStages] k-block 1 of buffer s landed
+  uint32_t* tmem_at = reinterpret_cast<uint32_t*>(full1 + kTcStages);
   TcDesc* desc = reinterpret_cast<TcDesc*>(sm + kTcDesc);
   volatile int* work = reinterpret_cast<volatile int*>(tmem_at + 1);  // [kTcStages] buffer s holds a tile (0: no more)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&full[i], 1);
+      mbar_init(&full1[i], 1);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -330,9 +333,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             timed_out = true;
           } else {
             work[s] = 1;
-            mbar_arrive_expect_tx(&full[s], 32768);
+            // the two k-blocks land on their own barriers: the first half's MMAs start without the second
+            mbar_arrive_expect_tx(&full[s], 16384);
             tma_load_3d(sm + kTcA + s * 32768, tm, 0, th, ty0, &full[s], once);
-            tma_load_3d(sm + kTcA + s * 32768 + 16384, tm, 64, th, ty0, &full[s], once);
+            mbar_arrive_expect_tx(&full1[s], 16384);
+            tma_load_3d(sm + kTcA + s * 32768 + 16384, tm, 64, th, ty0, &full1[s], once);
             ++it;
             if (!mbar_wait_bounded(&dempty[di], (((it - 1) / kTcDescs) & 1) ^ 1, kWaitLimit)) {
               timed_out = true;
@@ -357,8 +362,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         set_error(a.err, kErrTimeout);
         // copies may still be in flight: wait for them, bounded (on the normal path the MMA thread
         // has seen every one land)
-        for (int k = max(0, it - kTcStages); k < it; ++k)
+        for (int k = max(0, it - kTcStages); k < it; ++k) {
           mbar_wait_bounded(&full[k % kTcStages], (k / kTcStages) & 1, kWaitLimit);
+          mbar_wait_bounded(&full1[k % kTcStages], (k / kTcStages) & 1, kWaitLimit);
+        }
       } else {
         const int s = it % kTcStages, di = it % kTcDescs;
         if (!mbar_wait_bounded(&empty[s], ((it / kTcStages) & 1) ^ 1, kWaitLimit) ||
@@ -395,12 +402,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t d = tbase + 256 * bb;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+          if (i == 4 && !mbar_wait_bounded(&full1[s], (it / kTcStages) & 1, kWaitLimit)) {
+            ok = false;  // the MMAs issued so far are covered by the final commit below
+            break;
+          }
           const uint32_t ka = (uint32_t)((i >> 2) * 16384 + (i & 3) * 32) >> 4;  // x: k-blocks 16 KB apart
           const uint32_t kb = (uint32_t)((i >> 2) * 49152 + (i & 3) * 32) >> 4;  // R^T: 48 KB apart
           const uint64_t ad = dhi | (al + ka);
           umma_f16(d, ad, dhi | (b_lo + kb), idesc256, i > 0);                          // t0 | t1
           umma_f16(d + 128, ad, dhi | (b_lo + kb + (32768 >> 4)), idesc128, true);      // + t2
         }
+        if (!ok) break;
         umma_commit(&tfull[bb]);
         umma_commit(&empty[s]);
       }
