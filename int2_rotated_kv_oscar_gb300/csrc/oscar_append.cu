@@ -19,6 +19,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "oscar_device.cuh"
 #include "oscar_internal.h"
@@ -158,7 +159,8 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendLaunch a) {
 // faster than the tensor cores run them.  Two TMEM buffers of 256 columns:
 // the MMAs of the next tile overlap the epilogue of this one.
 //
-// Persistent blocks, one per SM, each for one matrix (even blocks K, odd V):
+// Persistent blocks, one per SM, each for one matrix (a little more than half,
+// spread evenly over the grid, for V; the others for K):
 //   warps 0-15  epilogue: warp (h, g, q) = (w / 8, w / 4 % 2, w % 4) takes
 //               token row 32 q + lane (its TMEM lane) of group g, channels
 //               16 k + 8 h + b (k < 4, b < 8); R^T's rows are permuted in
@@ -178,6 +180,7 @@ constexpr uint32_t kTcB = 0;               // R^T terms: [2 k-blocks][3 terms][1
 constexpr uint32_t kTcA = 3 * 32768;       // x tiles: kTcStages x [2 k-blocks][128 rows][128 B]
 constexpr uint32_t kTcBars = kTcA + kTcStages * 32768;
 constexpr uint32_t kTcPmax = kTcBars + 512;  // [tile parity][h][g][128 rows] float: half-row maxima
+constexpr double kTcVShare = 0.52;          // share of the blocks that take V tiles
 constexpr int kTcDescs = 8;                  // tile descriptors the TMA thread publishes ahead
 constexpr uint32_t kTcDesc = kTcPmax + 4096;
 constexpr size_t kTcSmem = kTcDesc + kTcDescs * 64 + 1024;  // + 1024-byte alignment slack
@@ -233,7 +236,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     append_tile_kernel(const __grid_constant__ AppendLaunch a, const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv, unsigned tiles2) {
+                       const __grid_constant__ CUtensorMap tmv, unsigned tiles2, unsigned nv) {
   // the kernel after this one may start beside it (it waits before it reads what this one writes)
   griddep_launch_dependents();
   extern __shared__ uint8_t tc_raw[];
@@ -253,8 +256,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   TcDesc* desc = reinterpret_cast<TcDesc*>(sm + kTcDesc);
   volatile int* work = reinterpret_cast<volatile int*>(tmem_at + 1);  // [kTcStages] buffer s holds a tile (0: no more)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = blockIdx.x & 1;
-  const unsigned cta = blockIdx.x >> 1, n_cta = gridDim.x >> 1;
+  // nv of the blocks take V, spread evenly over the grid: block i is the v_before(i)-th V block
+  // when v_before(i + 1) > v_before(i), v_before(i) = floor(i nv / blocks), else a K block
+  const unsigned vb0 = blockIdx.x * nv / gridDim.x, vb1 = (blockIdx.x + 1) * nv / gridDim.x;
+  const int m = vb1 > vb0 ? 1 : 0;
+  const unsigned cta = m ? vb0 : blockIdx.x - vb0, n_cta = m ? nv : gridDim.x - nv;
   const int Hkv = a.c.num_kv_heads;
   const unsigned n_tiles = tiles2 * (unsigned)Hkv * (unsigned)a.c.batch;
   {  // this matrix's three R^T terms
@@ -642,11 +648,16 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream) {
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  // an even grid: blocks 2 i take K, 2 i + 1 take V
+  // one block per SM, nv of them for V and the rest for K: a V tile takes a little longer (its
+  // epilogue stores bytes, K's whole words), so V gets a little more than half; neither matrix
+  // gets more blocks than it has tiles
   const long long per_matrix = (long long)tiles2 * Hkv * B;
-  const int blocks = 2 * (int)std::min<long long>(per_matrix, std::max(1, sms / 2));
-  unsigned t2 = (unsigned)tiles2;
-  void* args[] = {&la, &tm[0], &tm[1], &t2};
+  const int blocks = (int)std::min<long long>(2 * per_matrix, std::max(2, sms));
+  long long nv_ll = std::llround(blocks * kTcVShare);
+  nv_ll = std::min<long long>(std::max<long long>(nv_ll, blocks - per_matrix), per_matrix);
+  nv_ll = std::min<long long>(std::max<long long>(nv_ll, 1), blocks - 1);
+  unsigned t2 = (unsigned)tiles2, nv = (unsigned)nv_ll;
+  void* args[] = {&la, &tm[0], &tm[1], &t2, &nv};
   const void* tile_fn = reinterpret_cast<const void*>(append_tile_kernel);
   const void* bf16_fn = reinterpret_cast<const void*>(append_bf16_kernel);
   if (fresh) {
